@@ -1,0 +1,9 @@
+"""Seeded synthetic netlists and stimuli for the gate-level re-simulator.
+
+Inputs only: nothing here simulates.  Both the CPU oracle and the CUDA path take
+their inputs from these generators.
+"""
+from .cells import CELL_MIX, SCAN_MIX, truth_table  # noqa: F401
+from .netlist import INF, Netlist, NetlistSpec, build_netlist, generate_netlist, possible_rows  # noqa: F401
+from .stimulus import EOW, Stimulus, StimulusSpec, from_waveforms, generate_stimulus, select_windows  # noqa: F401
+from .workloads import WORKLOADS, make, sweep  # noqa: F401

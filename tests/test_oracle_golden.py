@@ -1,0 +1,147 @@
+"""Pins of the CPU oracle to the worked examples the GATSPI page prints.
+
+Fixtures in tests/golden/ hold the page's values with their citations:
+* fig3_waveforms.json -- GATSPI page, Section 3, Fig. 3 (array format);
+* fig4_lookup.json    -- GATSPI page, Section 3, Fig. 4 (truth table, SDF delay LUT).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from helpers import EOW, INF, changes, single_gate, uniform_delays, value_at
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _run(oracle_lib, net, waves, window_len):
+    stim = synth.from_waveforms([[w] for w in waves], window_len)
+    return oracle_lib.simulate(net, stim)
+
+
+def test_fig3_format_through_buffer_and_inverter(oracle_lib):
+    fx = _load("fig3_waveforms.json")
+    for key in ("A", "B"):
+        wave = fx[key]["printed"] + [fx["EOW"]]
+        assert value_at(wave, 0) == fx[key]["initial_value"]
+        for t, v in fx[key]["values_at"]:
+            assert value_at(wave, t) == v
+        # a zero-delay buffer reproduces the array; an inverter flips the head
+        buf = single_gate(synth.truth_table("BUF"), 1, uniform_delays(1, 0, 0))
+        r = _run(oracle_lib, buf, [wave], 200)
+        assert r.gate_wave(0, 0).tolist() == wave
+        inv = single_gate(synth.truth_table("INV"), 1, uniform_delays(1, 0, 0))
+        r = _run(oracle_lib, inv, [wave], 200)
+        out = r.gate_wave(0, 0).tolist()
+        assert changes(out) == changes(wave)
+        assert value_at(out, 0) == 1 - fx[key]["initial_value"]
+        for t, v in fx[key]["values_at"]:
+            assert value_at(out, t) == 1 - v
+
+
+def test_fig3_time_at_one():
+    """T1 of example A over [0, 200): value 1 on [0, 34) and [59, 123)."""
+    import oracle
+    fx = _load("fig3_waveforms.json")
+    wave = fx["A"]["printed"] + [fx["EOW"]]
+    buf = single_gate(synth.truth_table("BUF"), 1, uniform_delays(1, 0, 0))
+    r = oracle.simulate(buf, synth.from_waveforms([[wave]], 200))
+    assert int(r.t1[0]) == 34 + (123 - 59)
+    assert int(r.t0[0]) == 200 - 98
+    assert int(r.tc[0]) == 3
+
+
+def test_fig4_nand2_index_and_value(oracle_lib):
+    fx = _load("fig4_lookup.json")["nand2"]
+    tt = np.array(fx["truth_table"], np.uint8)
+    assert synth.truth_table("NAND2").tolist() == fx["truth_table"]
+    ex = fx["example"]
+    idx = ex["A"] * fx["pin_weights"]["A"] + ex["B"] * fx["pin_weights"]["B"]
+    assert idx == ex["index"] and tt[idx] == ex["Y"]
+    net = single_gate(tt, 2, uniform_delays(2, 3, 5, tt))
+    assert net.pin_weight.tolist() == [fx["pin_weights"]["A"], fx["pin_weights"]["B"]]
+    # A rises at 10, B at 20: the output (1 at start) falls when both are 1, 5 units later
+    r = _run(oracle_lib, net, [[0, 10, EOW], [0, 20, EOW]], 100)
+    assert r.gate_wave(0, 0).tolist() == [-1, 0, 25, EOW]
+
+
+def _aoi21_table(fx):
+    """AOI21 (A1, A2, B) delay table: B rows from the page, A1/A2 rows test-chosen."""
+    tt = synth.truth_table("AOI21")
+    n = 3
+    D = np.full((4 * n, 4), 0, np.int64)
+    for pin in (0, 1):                       # A1, A2: rise -> Y fall 30, fall -> Y rise 40
+        for e_in in (0, 1):
+            for e_out in (0, 1):
+                D[4 * pin + 2 * e_in + e_out] = 30 if e_out == 1 else 40
+    rows = fx["rows_printed"]
+    D[4 * 2 + 2 * 1 + 0] = rows["B fall -> Y rise"]
+    D[4 * 2 + 2 * 0 + 1] = rows["B rise -> Y fall"]
+    ok = synth.possible_rows(tt, n)
+    D[~ok] = INF
+    # the page marks exactly the B rise->Y rise and B fall->Y fall rows impossible
+    assert not ok[8] and ok[9] and ok[10] and not ok[11]
+    return tt, D.astype(np.int32)
+
+
+@pytest.mark.parametrize("a1,a2,expect", [
+    (0, 1, [-1, 0, 105, 307]),   # COND A2==1 && A1==0 holds: column 1 -> 5 / 7
+    (0, 0, [-1, 0, 106, 308]),   # plain IOPATH: 6 / 8
+    (1, 0, [-1, 0, 106, 308]),
+    (1, 1, [0]),                 # A1 & A2 hold Y at 0: B never changes it
+])
+def test_fig4_aoi21_conditional_delay(oracle_lib, a1, a2, expect):
+    fx = _load("fig4_lookup.json")["aoi21_B_to_Y"]
+    tt, D = _aoi21_table(fx)
+    col = a1 * fx["side_pin_arc_weights"]["A1"] + a2 * fx["side_pin_arc_weights"]["A2"]
+    assert (col == fx["column_of_condition"]) == (a1 == 0 and a2 == 1)
+    net = single_gate(tt, 3, D, type_name="AOI21")
+    static = lambda v: [-1, 0, EOW] if v else [0, EOW]  # noqa: E731
+    r = _run(oracle_lib, net, [static(a1), static(a2), [0, 100, 300, EOW]], 1000)
+    assert r.gate_wave(0, 0).tolist() == expect + [EOW]
+
+
+def test_msi_takes_smallest_switching_arc(oracle_lib):
+    """Both NAND2 inputs fall together: the output rises after the smaller arc delay
+    (reading: IEEE 1364 shortest-path rule for simultaneous input changes)."""
+    tt = synth.truth_table("NAND2")
+    D = uniform_delays(2, 0, 0, tt).astype(np.int64)
+    D[4 * 0 + 2 * 1 + 0] = 3     # A fall -> Y rise
+    D[4 * 1 + 2 * 1 + 0] = 9     # B fall -> Y rise
+    net = single_gate(tt, 2, D.astype(np.int32))
+    r = _run(oracle_lib, net, [[-1, 0, 50, EOW], [-1, 0, 50, EOW]], 100)
+    assert r.gate_wave(0, 0).tolist() == [0, 53, EOW]
+
+
+def test_msi_skips_impossible_arc(oracle_lib):
+    """f(A, B) = A: B has no arcs at all; A and B switching together uses A's arc."""
+    tt = np.array([0, 0, 1, 1], np.uint8)
+    D = uniform_delays(2, 7, 4, tt)
+    assert (D[4:] == INF).all()
+    net = single_gate(tt, 2, D)
+    r = _run(oracle_lib, net, [[0, 50, 90, EOW], [-1, 0, 50, EOW]], 200)
+    assert r.gate_wave(0, 0).tolist() == [0, 57, 94, EOW]
+
+
+def test_missing_arc_is_an_error(oracle_lib):
+    tt = np.array([0, 0, 1, 1], np.uint8)
+    D = np.full((8, 2), INF, np.int32)
+    net = single_gate(tt, 2, D)
+    with pytest.raises(oracle_lib.OracleError) as e:
+        _run(oracle_lib, net, [[0, 50, EOW], [0, EOW]], 100)
+    assert e.value.code == 7
+
+
+def test_malformed_input_is_an_error(oracle_lib):
+    net = single_gate(synth.truth_table("BUF"), 1, uniform_delays(1, 1, 1))
+    for bad in ([0, 5, 5, EOW], [0, 9, 3, EOW], [1, EOW], [0, 5], [-1, 3, EOW]):
+        with pytest.raises(oracle_lib.OracleError) as e:
+            _run(oracle_lib, net, [bad], 100)
+        assert e.value.code == 4

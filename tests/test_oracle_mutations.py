@@ -1,0 +1,111 @@
+"""The oracle's pins are sharp: each plausible slip planted in a copy of the oracle
+source (compiled on the CPU, in a temporary directory) fails at least one pin.
+
+The committed oracle is never modified; every mutant is a text substitution applied
+to a temporary copy.
+"""
+import functools
+import os
+import shutil
+import types
+
+import pytest
+
+import oracle
+import test_oracle_golden as golden
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__))
+
+MUTANTS = {
+    "wire filter tested once, not repeated": (
+        "                    p[i] += 2;\n                else\n                    break;",
+        "                    p[i] += 2;\n                break;"),
+    "wire filter not strict": (
+        "(int64_t)Win[i][p[i] + 1] < 0)", "(int64_t)Win[i][p[i] + 1] <= 0)"),
+    "wire rise/fall swapped": (
+        "d = (p[i] % 2) ? wire_fall[i] : wire_rise[i];", "d = (p[i] % 2) ? wire_rise[i] : wire_fall[i];"),
+    "gate filter not strict": (
+        "if (t_o - (int64_t)O->w[po] < d) {", "if (t_o - (int64_t)O->w[po] <= d) {"),
+    "gate filter never cancels": (
+        "if (t_o - (int64_t)O->w[po] < d) {", "if (0) {"),
+    "MSI takes the last finite arc, not the smallest": (
+        "if (dd != NO_ARC && dd < d) d = dd;", "if (dd != NO_ARC) d = dd;"),
+    "row: input and output edge transposed": (
+        "const int64_t row = 4 * i + 2 * e_in + e_out;", "const int64_t row = 4 * i + 2 * e_out + e_in;"),
+    "input edge sense flipped": (
+        "const int e_in = (p[i] % 2) ? RISE : FALL;", "const int e_in = (p[i] % 2) ? FALL : RISE;"),
+    "column with the first pin least significant": (
+        "if (j != i) col = col * 2 + (p[j] % 2);",
+        "if (j != i) col += (int64_t)(p[j] % 2) << (j < i ? j : j - 1);"),
+    "column from values before the switch": (
+        "if (j != i) col = col * 2 + (p[j] % 2);", "if (j != i) col = col * 2 + ((p[j] - sw[j]) % 2);"),
+    "only one simultaneous pin switches": (
+        "            sw[i] = (a[i] == t);\n            if (sw[i]) p[i] += 1;",
+        "            sw[i] = (a[i] == t);\n            for (int j = 0; j < i; ++j) if (sw[j]) sw[i] = 0;\n"
+        "            if (sw[i]) p[i] += 1;"),
+    "initial value ignored": (
+        "p[i] = (Win[i][0] == -1) ? 1 : 0;", "p[i] = 0;"),
+    "toggle count includes the head": (
+        "*tc = po - (y0 ? 1 : 0);", "*tc = po;"),
+    "time at 1 clipped one unit short": (
+        "if (e > Lw) e = Lw;", "if (e > Lw - 1) e = Lw - 1;"),
+    "time at 1 counts the value-0 intervals": (
+        "for (int64_t k = 1; k <= po; k += 2) {", "for (int64_t k = 0; k <= po; k += 2) {"),
+}
+
+
+def _battery(lib_path):
+    """Run a compact set of pins through the oracle at lib_path; True if all hold."""
+    shim = types.SimpleNamespace(simulate=functools.partial(oracle.simulate, lib_path=lib_path),
+                                 bruteforce=functools.partial(oracle.bruteforce, lib_path=lib_path),
+                                 OracleError=oracle.OracleError)
+    checks = [
+        lambda: golden.test_fig3_format_through_buffer_and_inverter(shim),
+        lambda: golden.test_fig4_nand2_index_and_value(shim),
+        lambda: golden.test_msi_takes_smallest_switching_arc(shim),
+        lambda: golden.test_msi_skips_impossible_arc(shim),
+    ]
+    for a1, a2, e in [(0, 1, [-1, 0, 105, 307]), (0, 0, [-1, 0, 106, 308]), (1, 1, [0])]:
+        checks.append(functools.partial(golden.test_fig4_aoi21_conditional_delay, shim, a1, a2, e))
+    for seed in range(3):
+        checks.append(functools.partial(pins.test_buffer_inverter_chain_is_inertial_delay_line, shim, seed))
+    checks.append(lambda: pins.test_output_invariants(shim, "tiny"))
+
+    def brute():
+        import numpy as np
+        for seed in range(150):
+            net, stim = pins._random_case(seed)
+            r = shim.simulate(net, stim)
+            b = shim.bruteforce(net, stim)
+            assert np.array_equal(r.pool, b.pool) and np.array_equal(r.tc, b.tc) and np.array_equal(r.t1, b.t1)
+    checks.append(brute)
+    for c in checks:
+        try:
+            c()
+        except (AssertionError, oracle.OracleError):
+            return False
+    return True
+
+
+def _build_variant(tmp_path, old, new):
+    d = tmp_path / "src"
+    d.mkdir()
+    for f in ("gatspi_oracle.c", "bruteforce.c", "oracle_abi.h"):
+        shutil.copy(os.path.join(SRC, f), d / f)
+    text = (d / "gatspi_oracle.c").read_text()
+    if old is not None:
+        assert text.count(old) == 1, "mutation anchor not found exactly once: %r" % old
+        text = text.replace(old, new)
+    (d / "gatspi_oracle.c").write_text(text)
+    return oracle.build(force=True, src_dir=str(d), out=str(tmp_path / "libvariant.so"))
+
+
+def test_unmutated_copy_passes(tmp_path):
+    assert _battery(_build_variant(tmp_path, None, None))
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    old, new = MUTANTS[name]
+    assert not _battery(_build_variant(tmp_path, old, new)), "pins missed: " + name
