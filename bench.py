@@ -1,0 +1,380 @@
+"""Throughput of the GB300 gate-level re-simulator on the 1M-gate workload.
+
+A step is one re-simulation of the whole netlist (all 40 logic levels, every gate in
+every one of the 256 cycle windows: Algorithm 1, the output-offset scan, the stores
+and the TC/T1 reduction) with the input waveforms already resident in HBM.
+
+Prints one JSON line (rank 0):
+  value      output toggle events per second over device time (sum of TC / time)
+  e2e        the same metric through the C ABI with host buffers: H2D of the input
+             waveforms, simulate, D2H of the toggle statistics, every step
+  roofline   the level kernel against the measured HBM copy bandwidth, on
+             algorithmic bytes (each consumed waveform read once, each output
+             written once, window index read and written once, descriptors once)
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+
+``--impl reference`` times the CPU oracle instead (the reference arm of this
+build: a plain serial event-driven simulator), on a bounded sample per step.
+Under torchrun every rank runs its own replica of the workload (replicas only:
+the method needs no exchange between GPUs); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "output toggle events/sec and gate-cycles/sec at 1 GB300; % of HBM roofline"
+UNIT = "output toggle events/s"
+WORKLOAD = "1M"
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = ("gate_level_logic_gb300/csrc/level_kernel.cu", "gate_level_logic_gb300/csrc/gatspi_internal.cuh")
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _init_pg(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo")
+    return dist
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _sum_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def workload_config(net, stim, stage_words):
+    return {
+        "workload": "1M-gate synthetic netlist, 40 levels, 9-cell mix with SDF-conditional arcs; "
+                    "4096 inputs, 10k cycles x period 1000, 5% activity, 10% glitch pairs; 256 cycle windows",
+        "gates": int(net.num_gates), "levels": int(net.num_levels), "inputs": int(net.num_inputs),
+        "edges": int(net.num_edges), "windows": int(stim.num_windows), "cycles": int(stim.window_cycles.sum()),
+        "stage_words": stage_words,
+        "l2": "inputs larger than L2 (waveform pool of several GB per step, no flush needed)",
+    }
+
+
+def algorithmic_bytes(net, off, W):
+    """Per-level algorithmic bytes from the run's own output lengths."""
+    P, G, L = net.num_inputs, net.num_gates, net.num_levels
+    lens = np.diff(off).reshape(P + G, W)
+    net_words = lens.sum(axis=1)
+    nchunks = (W + 31) // 32
+    idx_bytes_per_net = 4 * W + 8 * nchunks          # wend + chunk base
+    per_level = []
+    lo = net.level_offsets
+    for lvl in range(L):
+        g0, g1 = int(lo[lvl]), int(lo[lvl + 1])
+        srcs = np.unique(net.fanin_net[net.fanin_off[g0]:net.fanin_off[g1]])
+        read = 4 * int(net_words[srcs].sum()) + idx_bytes_per_net * srcs.size
+        write = 4 * int(net_words[P + g0:P + g1].sum()) + idx_bytes_per_net * (g1 - g0)
+        desc = 16 * (g1 - g0) + 16 * int(net.fanin_off[g1] - net.fanin_off[g0])
+        stats = 16 * (g1 - g0) * nchunks
+        per_level.append(read + write + desc + stats)
+    return np.array(per_level, dtype=np.int64)
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(launches):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this
+    exact kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "level_kernel_1M_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_sha") != _kernel_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = list(csv.reader(io.StringIO(getattr(self, "out", "") or "")))
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() in ("active", "1"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(net, stim, seconds_target=15.0):
+    """The CPU oracle as it stands, windows spread over all host cores, on a bounded
+    sample of the workload's windows (all gates)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    W = stim.num_windows
+    n = max(1, min(W, cores))
+    sel = np.linspace(0, W - 1, n).astype(np.int64)
+    t = time.perf_counter()
+    r = oracle.simulate(net, synth_select(stim, sel), threads=cores)
+    dt = time.perf_counter() - t
+    # grow the sample once to land near the target duration
+    if dt < seconds_target / 4 and n < W:
+        n2 = int(min(W, max(n + 1, n * min(8.0, seconds_target / max(dt, 1e-3)))))
+        sel = np.linspace(0, W - 1, n2).astype(np.int64)
+        t = time.perf_counter()
+        r = oracle.simulate(net, synth_select(stim, sel), threads=cores)
+        dt = time.perf_counter() - t
+    events = int(r.tc.sum())
+    cycles = int(stim.window_cycles[sel].sum())
+    return {
+        "value": events / dt, "unit": UNIT, "cores": min(cores, len(sel)), "kind": "oracle",
+        "sample": "%d of %d windows (all %d gates, %d cycles), %.1f s" % (len(sel), W, net.num_gates, cycles, dt),
+        "gate_cycles_per_s": net.num_gates * cycles / dt,
+    }
+
+
+def synth_select(stim, sel):
+    import synth
+    return synth.select_windows(stim, sel)
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return 0
+    import synth
+    import oracle
+    oracle.build()
+    net, stim = synth.make(WORKLOAD)
+    cores = os.cpu_count() or 1
+    W = stim.num_windows
+    n = min(W, 2 * cores)
+    sel = np.linspace(0, W - 1, n).astype(np.int64)
+    sub = synth.select_windows(stim, sel)
+    for _ in range(args.warmup):
+        oracle.simulate(net, sub, threads=cores)
+    times, events = [], 0
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        r = oracle.simulate(net, sub, threads=cores)
+        times.append(time.perf_counter() - t)
+        events += int(r.tc.sum())
+    total = sum(times)
+    value = events / total
+    cycles = int(stim.window_cycles[sel].sum())
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": workload_config(net, stim, None),
+        "gate_cycles_per_s": net.num_gates * cycles * args.steps / total,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, n), "kind": "oracle",
+                         "sample": "%d of %d windows per step (all gates)" % (n, W)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_gpu(args):
+    import torch
+
+    import synth
+    from gate_level_logic_gb300 import Simulator, build, gatspi
+
+    rank, world, local = _dist()
+    dist = _init_pg(world)
+    torch.cuda.set_device(local)
+    build.build()
+    net, stim = synth.make(WORKLOAD)
+    W = stim.num_windows
+    flags = gatspi.GATSPI_FLAG_LEVEL_TIMING
+    pool_words = int(args.pool_gb * (1 << 30) / 4)
+    sim = Simulator(net, stim.window_len, pool_words=pool_words, stage_words=args.stage_words, flags=flags)
+    stream = torch.cuda.current_stream()
+    sim.load(stim.pi_off, stim.pi_words, stream=stream)
+
+    for _ in range(max(args.warmup, 1)):
+        sim.simulate(stream=stream)
+    tc, t0, t1 = sim.toggle_stats()
+    events_per_step = int(tc.sum())
+    off = sim.export_offsets()
+    lvl_bytes = algorithmic_bytes(net, off, W)
+    pool_used = int(off[-1])
+    del off
+
+    # ---- timed region: device time, inputs resident ----------------------------
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    level_ms = np.zeros(net.num_levels, np.float64)
+    _barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for k in range(args.steps):
+            starts[k].record(stream)
+            sim.simulate(stream=stream)
+            ends[k].record(stream)
+            sim.sync()
+            level_ms += sim.level_times()
+        torch.cuda.synchronize()
+    _barrier(dist)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_s = _max_over_ranks(dist, sum(step_ms) / 1e3)
+    all_events = _sum_over_ranks(dist, events_per_step * args.steps)
+    value = all_events / total_s
+    gate_cycles = net.num_gates * int(stim.window_cycles.sum())
+    gate_cycles_per_s = _sum_over_ranks(dist, gate_cycles * args.steps) / total_s
+
+    # roofline of the level kernel: algorithmic bytes / its own event time
+    kern_s = level_ms.sum() / 1e3
+    achieved = float(lvl_bytes.sum() * args.steps / kern_s / 1e9)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        with open(peaks_path) as f:
+            peak = float(json.load(f)["hbm_gbs"])
+        peak_src = "measured"
+    else:
+        peak, peak_src = 6800.0, "fallback"
+    traffic = _traffic(net.num_levels)
+
+    # ---- end to end through the C ABI: host buffers, copies inside the region ---
+    pin_off = torch.from_numpy(np.ascontiguousarray(stim.pi_off, np.int64)).pin_memory()
+    pin_words = torch.from_numpy(np.ascontiguousarray(stim.pi_words, np.int32)).pin_memory()
+    e2e_steps = max(1, args.steps)
+    _barrier(dist)
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(e2e_steps):
+        sim.load(pin_off, pin_words, stream=stream)
+        sim.simulate(stream=stream)
+        tc_e, _, t1_e = sim.toggle_stats()
+    torch.cuda.synchronize()
+    e2e_s = _max_over_ranks(dist, time.perf_counter() - t)
+    assert int(tc_e.sum()) == events_per_step
+    e2e_value = _sum_over_ranks(dist, events_per_step * e2e_steps) / e2e_s
+    h2d = pin_off.numel() * 8 + pin_words.numel() * 4
+    d2h = 2 * 8 * net.num_gates + 16       # TC and T1 per gate, status word
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": workload_config(net, stim, args.stage_words),
+        "gate_cycles_per_s": gate_cycles_per_s,
+        "events_per_step": events_per_step,
+        "pool_words_used": pool_used,
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "peak_source": peak_src,
+            "kernel": "level_kernel (one launch per logic level)",
+            "algorithmic_bytes_per_launch": float(lvl_bytes.mean()),
+            "avg_launch_ms": float(level_ms.sum() / (args.steps * net.num_levels)),
+        },
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(args.steps * net.num_levels),
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        sim.close()
+        line["cpu_baseline"] = cpu_baseline(net, stim)
+    if rank == 0:
+        print(json.dumps(line))
+    sim.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--stage-words", type=int, default=-1)
+    ap.add_argument("--pool-gb", type=float, default=24.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,595 @@
+// Host side of the GB300 gate-level re-simulator: the C ABI of include/gatspi.h.
+//
+// It validates and uploads the levelised netlist, owns the window index, the
+// toggle statistics and the scan state on the device, borrows the caller's
+// waveform pool, and enqueues one level kernel per logic level (GATSPI, Section 3,
+// Fig. 5) -- captured once into a CUDA graph and replayed.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "gatspi_internal.cuh"
+
+using namespace gatspi;
+
+namespace {
+
+thread_local std::string g_err;
+
+gatspi_status fail(gatspi_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+gatspi_status fail(gatspi_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return s;
+}
+
+gatspi_status cuda_fail(cudaError_t e, const char *what) {
+    if (e == cudaErrorMemoryAllocation) return fail(GATSPI_ENOMEM, "%s: %s", what, cudaGetErrorString(e));
+    return fail(GATSPI_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CUDA_TRY(call, what)                     \
+    do {                                         \
+        cudaError_t e_ = (call);                 \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+template <class T>
+cudaError_t dev_alloc(T **p, size_t n) {
+    return cudaMalloc((void **)p, std::max<size_t>(n, 1) * sizeof(T));
+}
+
+}  // namespace
+
+struct gatspi_ctx {
+    int device = 0;
+    int32_t P = 0, G = 0, L = 0, W = 0;
+    int32_t nchunks = 1, lpg_log2 = 0, slots_per_gate = 1;
+    long long num_nets = 0;
+    int32_t *pool = nullptr;
+    long long pool_words = 0;
+    int stage = kDefaultStage;
+    uint32_t flags = 0;
+
+    // device arrays owned by the context
+    int4 *gate_desc = nullptr;
+    int4 *edge_desc = nullptr;
+    int32_t *dly = nullptr;
+    long long *chunk_base = nullptr;
+    uint32_t *wend = nullptr;
+    int32_t *window_len = nullptr;
+    unsigned long long *tc = nullptr, *t1 = nullptr;
+    unsigned long long *tile_status = nullptr;
+    int32_t *tickets = nullptr;
+    long long *level_base = nullptr;
+    int32_t *status = nullptr;
+    long long *load_off = nullptr;
+    int32_t *max_time = nullptr;
+
+    // host copies
+    std::vector<int32_t> level_offsets;
+    std::vector<LevelLaunch> launches;
+    long long total_tiles = 0;
+    long long sum_window_len = 0;
+    long long path_delay_bound = 0;   // levels * (max wire delay + max gate delay)
+    bool loaded = false;
+    bool simulated = false;
+    cudaStream_t last_stream = nullptr;
+
+    // replayed level sequence
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t graph_exec = nullptr;
+    cudaStream_t capture_stream = nullptr;
+    std::vector<cudaEvent_t> events;
+
+    DevParams params() const {
+        DevParams p{};
+        p.gate_desc = gate_desc;
+        p.edge_desc = edge_desc;
+        p.dly_data = dly;
+        p.pool = pool;
+        p.pool_words = pool_words;
+        p.chunk_base = chunk_base;
+        p.wend = wend;
+        p.window_len = window_len;
+        p.tc = tc;
+        p.t1 = t1;
+        p.tile_status = tile_status;
+        p.tickets = tickets;
+        p.level_base = level_base;
+        p.status = status;
+        p.num_inputs = P;
+        p.W = W;
+        p.nchunks = nchunks;
+        p.lpg_log2 = lpg_log2;
+        p.slots_per_gate = slots_per_gate;
+        p.stage = stage;
+        return p;
+    }
+};
+
+namespace {
+
+gatspi_status validate(const gatspi_netlist *nl, const gatspi_config *cfg, long long *path_bound) {
+    if (!nl || !cfg) return fail(GATSPI_EINVAL, "netlist and config are required");
+    const long long P = nl->num_inputs, G = nl->num_gates, L = nl->num_levels, T = nl->num_types;
+    if (P < 0 || G < 0 || L < 0 || T < 0 || P + G > INT32_MAX)
+        return fail(GATSPI_EINVAL, "negative or too large netlist sizes");
+    if (G > 0 && (L < 1 || T < 1)) return fail(GATSPI_EINVAL, "gates need at least one level and one type");
+    if (cfg->num_windows < 1) return fail(GATSPI_EINVAL, "num_windows must be >= 1");
+    if (!cfg->window_len) return fail(GATSPI_EINVAL, "window_len is required");
+    for (int w = 0; w < cfg->num_windows; ++w)
+        if (cfg->window_len[w] < 1 || cfg->window_len[w] > (1ll << 30))
+            return fail(GATSPI_EINVAL, "window %d: length must be in 1 .. 2^30", w);
+    if (cfg->stage_words < -1 || cfg->stage_words > kMaxStage)
+        return fail(GATSPI_EINVAL, "stage_words must be -1 or 0 .. %d", kMaxStage);
+    if (G == 0) {
+        *path_bound = 0;
+        return GATSPI_OK;
+    }
+    if (!nl->level_offsets || !nl->gate_type || !nl->type_num_pins || !nl->type_tt_off || !nl->tt_data ||
+        !nl->fanin_off || !nl->fanin_net || !nl->pin_weight || !nl->wire_rise || !nl->wire_fall ||
+        !nl->gate_dly_off || !nl->dly_data)
+        return fail(GATSPI_EINVAL, "a netlist array is missing");
+    if (nl->level_offsets[0] != 0 || nl->level_offsets[L] != G)
+        return fail(GATSPI_EINVAL, "level_offsets must run from 0 to num_gates");
+    for (long long l = 0; l < L; ++l)
+        if (nl->level_offsets[l + 1] < nl->level_offsets[l]) return fail(GATSPI_EINVAL, "level %lld: negative size", l);
+    for (long long t = 0; t < T; ++t) {
+        const int n = nl->type_num_pins[t];
+        if (n < 1 || n > GATSPI_MAX_PINS) return fail(GATSPI_EINVAL, "type %lld: %d pins (1 .. %d)", t, n, GATSPI_MAX_PINS);
+        if (nl->type_tt_off[t] < 0 || nl->type_tt_off[t] + (1ll << n) > nl->tt_len)
+            return fail(GATSPI_EINVAL, "type %lld: truth table out of range", t);
+        for (int k = 0; k < (1 << n); ++k)
+            if (nl->tt_data[nl->type_tt_off[t] + k] > 1) return fail(GATSPI_EINVAL, "type %lld: truth-table entry not 0/1", t);
+    }
+    if (nl->fanin_off[0] != 0) return fail(GATSPI_EINVAL, "fanin_off[0] must be 0");
+    int max_wire = 0, max_gate = 0;
+    long long lvl = 0;
+    for (long long g = 0; g < G; ++g) {
+        while (g >= nl->level_offsets[lvl + 1]) ++lvl;
+        const long long level_first_net = P + nl->level_offsets[lvl];
+        const int t = nl->gate_type[g];
+        if (t < 0 || t >= T) return fail(GATSPI_EINVAL, "gate %lld: type %d out of range", g, t);
+        const int n = nl->type_num_pins[t];
+        const long long e0 = nl->fanin_off[g];
+        if (nl->fanin_off[g + 1] - e0 != n) return fail(GATSPI_EINVAL, "gate %lld: %d pins expected", g, n);
+        unsigned seen = 0;
+        for (int i = 0; i < n; ++i) {
+            const long long s = nl->fanin_net[e0 + i];
+            if (s < 0 || s >= level_first_net)
+                return fail(GATSPI_EINVAL, "gate %lld pin %d: net %lld is not an input or a gate of a lower level", g, i, s);
+            const int wt = nl->pin_weight[e0 + i];
+            if (wt <= 0 || wt >= (1 << n) || (wt & (wt - 1)) || (seen & (unsigned)wt))
+                return fail(GATSPI_EINVAL, "gate %lld: pin weights must be the distinct powers 2^0 .. 2^(n-1)", g);
+            seen |= (unsigned)wt;
+            const int wr = nl->wire_rise[e0 + i], wf = nl->wire_fall[e0 + i];
+            if (wr < 0 || wr > 0xffff || wf < 0 || wf > 0xffff)
+                return fail(GATSPI_EINVAL, "gate %lld pin %d: interconnect delay out of 0 .. 65535", g, i);
+            max_wire = std::max(max_wire, std::max(wr, wf));
+        }
+        const long long d0 = nl->gate_dly_off[g];
+        const long long dn = 4ll * n * (1ll << (n - 1));
+        if (d0 < 0 || d0 + dn > nl->dly_len) return fail(GATSPI_EINVAL, "gate %lld: delay table out of range", g);
+        for (long long k = 0; k < dn; ++k) {
+            const int d = nl->dly_data[d0 + k];
+            if (d == GATSPI_NO_ARC) continue;
+            if (d < 0 || d >= (1 << 24)) return fail(GATSPI_EINVAL, "gate %lld: delay %d out of 0 .. 2^24-1", g, d);
+            max_gate = std::max(max_gate, d);
+        }
+    }
+    *path_bound = L * ((long long)max_wire + max_gate);
+    return GATSPI_OK;
+}
+
+void free_all(gatspi_ctx *c) {
+    if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
+    if (c->graph) cudaGraphDestroy(c->graph);
+    if (c->capture_stream) cudaStreamDestroy(c->capture_stream);
+    for (cudaEvent_t e : c->events) cudaEventDestroy(e);
+    void *ptrs[] = {c->gate_desc, c->edge_desc, c->dly, c->chunk_base, c->wend, c->window_len, c->tc, c->t1,
+                    c->tile_status, c->tickets, c->level_base, c->status, c->load_off, c->max_time};
+    for (void *p : ptrs)
+        if (p) cudaFree(p);
+}
+
+gatspi_status read_status(gatspi_ctx *c) {
+    int32_t st[kStatusWords];
+    CUDA_TRY(cudaMemcpy(st, c->status, sizeof st, cudaMemcpyDeviceToHost), "reading the device status");
+    switch (st[0]) {
+        case GATSPI_OK: return GATSPI_OK;
+        case GATSPI_EPOOL_OVERFLOW:
+            return fail(GATSPI_EPOOL_OVERFLOW, "waveform pool too small (%lld words) at level %d", c->pool_words, st[1]);
+        case GATSPI_EBADWAVE:
+            return fail(GATSPI_EBADWAVE, "malformed waveform while simulating %d, window %d", st[1], st[2]);
+        case GATSPI_EBADLUT:
+            return fail(GATSPI_EBADLUT, "gate %d window %d: every switching arc of an output change has no delay", st[1], st[2]);
+        case GATSPI_ETIMEOUT:
+            return fail(GATSPI_ETIMEOUT, "scan look-back stalled at level %d tile %d (waiting on tile %d)", st[1], st[2], st[3]);
+        default: return fail((gatspi_status)st[0], "device error %d", st[0]);
+    }
+}
+
+gatspi_status sync_ctx(gatspi_ctx *c) {
+    CUDA_TRY(cudaSetDevice(c->device), "cudaSetDevice");
+    CUDA_TRY(cudaStreamSynchronize(c->last_stream), "synchronising the stream");
+    CUDA_TRY(cudaGetLastError(), "pending CUDA error");
+    return read_status(c);
+}
+
+// Enqueue the whole level sequence on stream s.
+gatspi_status enqueue_levels(gatspi_ctx *c, cudaStream_t s) {
+    CUDA_TRY(cudaMemsetAsync(c->tc, 0, sizeof(unsigned long long) * std::max(c->G, 1), s), "clearing TC");
+    CUDA_TRY(cudaMemsetAsync(c->t1, 0, sizeof(unsigned long long) * std::max(c->G, 1), s), "clearing T1");
+    CUDA_TRY(cudaMemsetAsync(c->tile_status, 0, sizeof(unsigned long long) * std::max<long long>(c->total_tiles, 1), s),
+             "clearing the scan state");
+    CUDA_TRY(cudaMemsetAsync(c->tickets, 0, sizeof(int32_t) * std::max(c->L, 1), s), "clearing the tile tickets");
+    CUDA_TRY(cudaMemsetAsync(c->status, 0, sizeof(int32_t) * kStatusWords, s), "clearing the status");
+    const DevParams p = c->params();
+    const bool timing = (c->flags & GATSPI_FLAG_LEVEL_TIMING) != 0;
+    for (int l = 0; l < c->L; ++l) {
+        if (timing) CUDA_TRY(cudaEventRecord(c->events[l], s), "recording a level event");
+        CUDA_TRY(launch_level(p, c->launches[l], s), "launching a level kernel");
+    }
+    if (timing && c->L > 0) CUDA_TRY(cudaEventRecord(c->events[c->L], s), "recording a level event");
+    return GATSPI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gatspi_last_error(void) { return g_err.c_str(); }
+
+const char *gatspi_status_name(gatspi_status s) {
+    switch (s) {
+        case GATSPI_OK: return "GATSPI_OK";
+        case GATSPI_EINVAL: return "GATSPI_EINVAL";
+        case GATSPI_ENOMEM: return "GATSPI_ENOMEM";
+        case GATSPI_EPOOL_OVERFLOW: return "GATSPI_EPOOL_OVERFLOW";
+        case GATSPI_EBADWAVE: return "GATSPI_EBADWAVE";
+        case GATSPI_ECUDA: return "GATSPI_ECUDA";
+        case GATSPI_ESTATE: return "GATSPI_ESTATE";
+        case GATSPI_EBADLUT: return "GATSPI_EBADLUT";
+        case GATSPI_ETIMEOUT: return "GATSPI_ETIMEOUT";
+    }
+    return "GATSPI_UNKNOWN";
+}
+
+gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, int32_t *d_pool, size_t pool_words,
+                            gatspi_ctx **out) {
+    g_err.clear();
+    if (!out) return fail(GATSPI_EINVAL, "out is NULL");
+    *out = nullptr;
+    long long path_bound = 0;
+    gatspi_status st = validate(nl, cfg, &path_bound);
+    if (st != GATSPI_OK) return st;
+    if (!d_pool || pool_words == 0 || (pool_words & 3) || ((uintptr_t)d_pool & 15))
+        return fail(GATSPI_EINVAL, "the pool must be a non-empty, 16-byte aligned device buffer of 4k words");
+
+    gatspi_ctx *c = new (std::nothrow) gatspi_ctx();
+    if (!c) return fail(GATSPI_ENOMEM, "host allocation failed");
+    st = [&]() -> gatspi_status {
+        CUDA_TRY(cudaGetDevice(&c->device), "cudaGetDevice");
+        c->P = nl->num_inputs;
+        c->G = nl->num_gates;
+        c->L = nl->num_gates > 0 ? nl->num_levels : 0;
+        c->W = cfg->num_windows;
+        c->pool = d_pool;
+        c->pool_words = (long long)pool_words;
+        c->flags = cfg->flags;
+        c->stage = cfg->stage_words < 0 ? kDefaultStage : cfg->stage_words;
+        c->num_nets = (long long)c->P + c->G;
+        c->nchunks = (c->W + 31) / 32;
+        int lpg = 32;
+        if (c->W < 32) {
+            lpg = 1;
+            while (lpg < c->W) lpg <<= 1;
+        }
+        while ((1 << c->lpg_log2) < lpg) ++c->lpg_log2;
+        c->slots_per_gate = c->nchunks << c->lpg_log2;
+        c->path_delay_bound = path_bound;
+        for (int w = 0; w < c->W; ++w) c->sum_window_len += cfg->window_len[w];
+
+        // gate and edge descriptors
+        const long long E = c->G > 0 ? nl->fanin_off[c->G] : 0;
+        std::vector<int4> gd(std::max(c->G, 1));
+        std::vector<int4> ed(std::max<long long>(E, 1));
+        for (long long g = 0; g < c->G; ++g) {
+            const int t = nl->gate_type[g];
+            const int n = nl->type_num_pins[t];
+            uint32_t mask = 0;
+            for (int k = 0; k < (1 << n); ++k) mask |= (uint32_t)nl->tt_data[nl->type_tt_off[t] + k] << k;
+            const long long d0 = nl->gate_dly_off[g];
+            gd[g] = make_int4(nl->fanin_off[g], (int)(n | (mask << 8)), (int)(uint32_t)(d0 & 0xffffffffll),
+                              (int)(d0 >> 32));
+        }
+        for (long long e = 0; e < E; ++e)
+            ed[e] = make_int4(nl->fanin_net[e], nl->pin_weight[e],
+                              (int)((uint32_t)nl->wire_rise[e] | ((uint32_t)nl->wire_fall[e] << 16)), 0);
+
+        // levels and tiles
+        c->level_offsets.assign(nl->level_offsets, nl->level_offsets + c->L + 1);
+        for (int l = 0; l < c->L; ++l) {
+            LevelLaunch ll{};
+            ll.level = l;
+            ll.gate_begin = c->level_offsets[l];
+            ll.num_gates = c->level_offsets[l + 1] - c->level_offsets[l];
+            const long long slots = (long long)ll.num_gates * c->slots_per_gate;
+            const long long tiles = std::max<long long>(1, (slots + kBlock - 1) / kBlock);
+            if (tiles > INT32_MAX) return fail(GATSPI_EINVAL, "level %d has too many (gate, window) slots", l);
+            ll.num_tiles = (int32_t)tiles;
+            ll.tile_base = c->total_tiles;
+            c->total_tiles += tiles;
+            c->launches.push_back(ll);
+        }
+
+        const long long dly_len = c->G > 0 ? nl->dly_len : 0;
+        CUDA_TRY(dev_alloc(&c->gate_desc, gd.size()), "allocating gate descriptors");
+        CUDA_TRY(dev_alloc(&c->edge_desc, ed.size()), "allocating edge descriptors");
+        CUDA_TRY(dev_alloc(&c->dly, (size_t)dly_len), "allocating delay tables");
+        CUDA_TRY(dev_alloc(&c->chunk_base, (size_t)(c->num_nets * c->nchunks)), "allocating the window index");
+        CUDA_TRY(dev_alloc(&c->wend, (size_t)(c->num_nets * c->W)), "allocating the window index");
+        CUDA_TRY(dev_alloc(&c->window_len, (size_t)c->W), "allocating window lengths");
+        CUDA_TRY(dev_alloc(&c->tc, (size_t)c->G), "allocating TC");
+        CUDA_TRY(dev_alloc(&c->t1, (size_t)c->G), "allocating T1");
+        CUDA_TRY(dev_alloc(&c->tile_status, (size_t)c->total_tiles), "allocating the scan state");
+        CUDA_TRY(dev_alloc(&c->tickets, (size_t)c->L), "allocating tile tickets");
+        CUDA_TRY(dev_alloc(&c->level_base, (size_t)c->L + 1), "allocating level bases");
+        CUDA_TRY(dev_alloc(&c->status, (size_t)kStatusWords), "allocating the status word");
+        CUDA_TRY(dev_alloc(&c->load_off, (size_t)((long long)c->P * c->W + 1)), "allocating load offsets");
+        CUDA_TRY(dev_alloc(&c->max_time, 1), "allocating the load scratch");
+
+        std::vector<int32_t> wl(c->W);
+        for (int w = 0; w < c->W; ++w) wl[w] = (int32_t)cfg->window_len[w];
+        CUDA_TRY(cudaMemcpy(c->gate_desc, gd.data(), gd.size() * sizeof(int4), cudaMemcpyHostToDevice), "uploading gates");
+        CUDA_TRY(cudaMemcpy(c->edge_desc, ed.data(), ed.size() * sizeof(int4), cudaMemcpyHostToDevice), "uploading edges");
+        if (dly_len > 0)
+            CUDA_TRY(cudaMemcpy(c->dly, nl->dly_data, (size_t)dly_len * sizeof(int32_t), cudaMemcpyHostToDevice),
+                     "uploading delay tables");
+        CUDA_TRY(cudaMemcpy(c->window_len, wl.data(), wl.size() * sizeof(int32_t), cudaMemcpyHostToDevice),
+                 "uploading window lengths");
+        CUDA_TRY(cudaMemset(c->status, 0, sizeof(int32_t) * kStatusWords), "clearing the status");
+        CUDA_TRY(cudaMemset(c->tc, 0, sizeof(unsigned long long) * std::max(c->G, 1)), "clearing TC");
+        CUDA_TRY(cudaMemset(c->t1, 0, sizeof(unsigned long long) * std::max(c->G, 1)), "clearing T1");
+        CUDA_TRY(set_level_smem_limit(c->stage), "configuring shared memory");
+        if (c->flags & GATSPI_FLAG_LEVEL_TIMING) {
+            c->events.resize(c->L + 1, nullptr);
+            for (auto &e : c->events) CUDA_TRY(cudaEventCreate(&e), "creating level events");
+        }
+        return GATSPI_OK;
+    }();
+    if (st != GATSPI_OK) {
+        free_all(c);
+        delete c;
+        return st;
+    }
+    *out = c;
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_load_waveforms(gatspi_ctx *c, const int64_t *off, const int32_t *words, size_t nwords, int where,
+                                    void *stream) {
+    g_err.clear();
+    if (!c || !off || (!words && nwords)) return fail(GATSPI_EINVAL, "ctx, off and words are required");
+    if (where != GATSPI_HOST && where != GATSPI_DEVICE) return fail(GATSPI_EINVAL, "where must be HOST or DEVICE");
+    if ((long long)nwords > c->pool_words)
+        return fail(GATSPI_EPOOL_OVERFLOW, "%zu input words exceed the pool (%lld words)", nwords, c->pool_words);
+    CUDA_TRY(cudaSetDevice(c->device), "cudaSetDevice");
+    cudaStream_t s = (cudaStream_t)stream;
+    const long long n = (long long)c->P * c->W + 1;
+    const cudaMemcpyKind kind = where == GATSPI_HOST ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    if (where == GATSPI_HOST && off[n - 1] != (long long)nwords)
+        return fail(GATSPI_EINVAL, "off[num_inputs * W] (%lld) must equal nwords (%zu)", (long long)off[n - 1], nwords);
+    c->loaded = false;
+    c->last_stream = s;
+    CUDA_TRY(cudaMemcpyAsync(c->load_off, off, (size_t)n * sizeof(long long), kind, s), "copying input offsets");
+    if (nwords) CUDA_TRY(cudaMemcpyAsync(c->pool, words, nwords * sizeof(int32_t), kind, s), "copying input words");
+    CUDA_TRY(cudaMemsetAsync(c->status, 0, sizeof(int32_t) * kStatusWords, s), "clearing the status");
+    CUDA_TRY(cudaMemsetAsync(c->max_time, 0, sizeof(int32_t), s), "clearing the load scratch");
+    CUDA_TRY(launch_load_index(c->params(), c->load_off, (long long)nwords, c->max_time, s), "indexing the inputs");
+    CUDA_TRY(cudaStreamSynchronize(s), "loading waveforms");
+    int32_t st[kStatusWords];
+    int32_t tmax = 0;
+    CUDA_TRY(cudaMemcpy(st, c->status, sizeof st, cudaMemcpyDeviceToHost), "reading the load status");
+    CUDA_TRY(cudaMemcpy(&tmax, c->max_time, sizeof tmax, cudaMemcpyDeviceToHost), "reading the load status");
+    if (st[0] == GATSPI_EBADWAVE)
+        return fail(GATSPI_EBADWAVE, "input %d window %d: malformed waveform or offsets", st[1], st[2]);
+    if (st[0] != 0) return read_status(c);
+    if ((long long)tmax + c->path_delay_bound >= (long long)GATSPI_EOW)
+        return fail(GATSPI_EINVAL, "latest input time %d plus the longest path delay bound %lld reaches EOW", tmax,
+                    c->path_delay_bound);
+    c->loaded = true;
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_simulate(gatspi_ctx *c, void *stream) {
+    g_err.clear();
+    if (!c) return fail(GATSPI_EINVAL, "ctx is NULL");
+    if (!c->loaded) return fail(GATSPI_ESTATE, "load the input waveforms first");
+    CUDA_TRY(cudaSetDevice(c->device), "cudaSetDevice");
+    cudaStream_t s = (cudaStream_t)stream;
+    c->last_stream = s;
+    c->simulated = true;
+    if (c->flags & GATSPI_FLAG_NO_GRAPH) return enqueue_levels(c, s);
+    if (!c->graph_exec) {
+        CUDA_TRY(cudaStreamCreateWithFlags(&c->capture_stream, cudaStreamNonBlocking), "creating the capture stream");
+        CUDA_TRY(cudaStreamBeginCapture(c->capture_stream, cudaStreamCaptureModeThreadLocal), "beginning capture");
+        gatspi_status st = enqueue_levels(c, c->capture_stream);
+        cudaGraph_t g = nullptr;
+        cudaError_t e = cudaStreamEndCapture(c->capture_stream, &g);
+        if (st != GATSPI_OK) {
+            if (g) cudaGraphDestroy(g);
+            return st;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "ending capture");
+        c->graph = g;
+        CUDA_TRY(cudaGraphInstantiate(&c->graph_exec, c->graph, 0), "instantiating the level graph");
+    }
+    CUDA_TRY(cudaGraphLaunch(c->graph_exec, s), "launching the level graph");
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_sync(gatspi_ctx *c) {
+    g_err.clear();
+    if (!c) return fail(GATSPI_EINVAL, "ctx is NULL");
+    return sync_ctx(c);
+}
+
+gatspi_status gatspi_toggle_stats(gatspi_ctx *c, int64_t *tc, int64_t *t0, int64_t *t1) {
+    g_err.clear();
+    if (!c) return fail(GATSPI_EINVAL, "ctx is NULL");
+    if (!c->simulated) return fail(GATSPI_ESTATE, "simulate first");
+    gatspi_status st = sync_ctx(c);
+    if (st != GATSPI_OK) return st;
+    if (c->G == 0) return GATSPI_OK;
+    if (tc) CUDA_TRY(cudaMemcpy(tc, c->tc, sizeof(int64_t) * c->G, cudaMemcpyDeviceToHost), "reading TC");
+    if (t0 || t1) {
+        std::vector<int64_t> one(c->G);
+        CUDA_TRY(cudaMemcpy(one.data(), c->t1, sizeof(int64_t) * c->G, cudaMemcpyDeviceToHost), "reading T1");
+        for (int g = 0; g < c->G; ++g) {
+            if (t1) t1[g] = one[g];
+            if (t0) t0[g] = c->sum_window_len - one[g];
+        }
+    }
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_get_waveform(gatspi_ctx *c, int32_t net, int32_t window, int32_t *buf, size_t cap, size_t *len) {
+    g_err.clear();
+    if (!c || !len) return fail(GATSPI_EINVAL, "ctx and len are required");
+    if (net < 0 || net >= c->num_nets || window < 0 || window >= c->W)
+        return fail(GATSPI_EINVAL, "net %d / window %d out of range", net, window);
+    if (!c->loaded || (net >= c->P && !c->simulated)) return fail(GATSPI_ESTATE, "waveform not computed yet");
+    gatspi_status st = sync_ctx(c);
+    if (st != GATSPI_OK) return st;
+    long long base = 0;
+    uint32_t end = 0, start = 0;
+    const long long k = (long long)net * c->W + window;
+    CUDA_TRY(cudaMemcpy(&base, c->chunk_base + (long long)net * c->nchunks + window / 32, sizeof base,
+                        cudaMemcpyDeviceToHost), "reading the window index");
+    CUDA_TRY(cudaMemcpy(&end, c->wend + k, sizeof end, cudaMemcpyDeviceToHost), "reading the window index");
+    if (window % 32) CUDA_TRY(cudaMemcpy(&start, c->wend + k - 1, sizeof start, cudaMemcpyDeviceToHost), "reading the window index");
+    *len = (size_t)(end - start);
+    if (*len > cap || !buf) return fail(GATSPI_EINVAL, "buffer of %zu words too small for %zu", cap, *len);
+    CUDA_TRY(cudaMemcpy(buf, c->pool + base + start, *len * sizeof(int32_t), cudaMemcpyDeviceToHost), "reading a waveform");
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_export_offsets(gatspi_ctx *c, int64_t *off, size_t n) {
+    g_err.clear();
+    if (!c || !off) return fail(GATSPI_EINVAL, "ctx and off are required");
+    if ((long long)n != c->num_nets * c->W + 1) return fail(GATSPI_EINVAL, "off needs num_nets * W + 1 entries");
+    if (!c->loaded || !c->simulated) return fail(GATSPI_ESTATE, "simulate first");
+    gatspi_status st = sync_ctx(c);
+    if (st != GATSPI_OK) return st;
+    std::vector<long long> base((size_t)(c->num_nets * c->nchunks));
+    std::vector<uint32_t> wend((size_t)(c->num_nets * c->W));
+    long long used = 0;
+    CUDA_TRY(cudaMemcpy(base.data(), c->chunk_base, base.size() * sizeof(long long), cudaMemcpyDeviceToHost), "reading the window index");
+    CUDA_TRY(cudaMemcpy(wend.data(), c->wend, wend.size() * sizeof(uint32_t), cudaMemcpyDeviceToHost), "reading the window index");
+    CUDA_TRY(cudaMemcpy(&used, c->level_base + c->L, sizeof used, cudaMemcpyDeviceToHost), "reading the pool size");
+    for (long long net = 0; net < c->num_nets; ++net)
+        for (int w = 0; w < c->W; ++w) {
+            const long long k = net * c->W + w;
+            off[k] = base[net * c->nchunks + w / 32] + ((w % 32) ? wend[k - 1] : 0);
+        }
+    off[c->num_nets * c->W] = used;
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_export_windows(gatspi_ctx *c, const int32_t *windows, int32_t nsel, int64_t *off, int32_t *words,
+                                    size_t cap) {
+    g_err.clear();
+    if (!c || !windows || !off || nsel < 1) return fail(GATSPI_EINVAL, "ctx, windows (nsel >= 1) and off are required");
+    for (int s = 0; s < nsel; ++s)
+        if (windows[s] < 0 || windows[s] >= c->W) return fail(GATSPI_EINVAL, "window %d out of range", windows[s]);
+    if (!c->loaded || !c->simulated) return fail(GATSPI_ESTATE, "simulate first");
+    gatspi_status st = sync_ctx(c);
+    if (st != GATSPI_OK) return st;
+    const long long n = c->num_nets * nsel;
+    int32_t *d_sel = nullptr;
+    long long *d_len = nullptr;
+    int32_t *d_words = nullptr;
+    st = [&]() -> gatspi_status {
+        CUDA_TRY(dev_alloc(&d_sel, (size_t)nsel), "allocating export scratch");
+        CUDA_TRY(dev_alloc(&d_len, (size_t)n + 1), "allocating export scratch");
+        CUDA_TRY(cudaMemcpy(d_sel, windows, sizeof(int32_t) * nsel, cudaMemcpyHostToDevice), "copying windows");
+        const DevParams p = c->params();
+        CUDA_TRY(launch_window_lengths(p, c->num_nets, d_sel, nsel, d_len, nullptr), "measuring waveforms");
+        std::vector<long long> len((size_t)n);
+        CUDA_TRY(cudaMemcpy(len.data(), d_len, sizeof(long long) * n, cudaMemcpyDeviceToHost), "reading lengths");
+        long long acc = 0;
+        for (long long k = 0; k < n; ++k) {
+            off[k] = acc;
+            acc += len[k];
+        }
+        off[n] = acc;
+        if (!words) return GATSPI_OK;
+        if ((long long)cap < acc) return fail(GATSPI_EINVAL, "words buffer of %zu too small for %lld", cap, acc);
+        CUDA_TRY(cudaMemcpy(d_len, off, sizeof(long long) * (n + 1), cudaMemcpyHostToDevice), "copying offsets");
+        CUDA_TRY(dev_alloc(&d_words, (size_t)acc), "allocating export scratch");
+        CUDA_TRY(launch_window_gather(p, c->num_nets, d_sel, nsel, d_len, d_words, nullptr), "gathering waveforms");
+        CUDA_TRY(cudaMemcpy(words, d_words, sizeof(int32_t) * acc, cudaMemcpyDeviceToHost), "reading waveforms");
+        return GATSPI_OK;
+    }();
+    if (d_sel) cudaFree(d_sel);
+    if (d_len) cudaFree(d_len);
+    if (d_words) cudaFree(d_words);
+    return st;
+}
+
+gatspi_status gatspi_device_views(gatspi_ctx *c, gatspi_views *v) {
+    g_err.clear();
+    if (!c || !v) return fail(GATSPI_EINVAL, "ctx and out are required");
+    v->pool = c->pool;
+    v->pool_words = c->pool_words;
+    v->pool_used = 0;
+    if (c->loaded) {
+        gatspi_status st = sync_ctx(c);
+        if (st != GATSPI_OK) return st;
+        long long used = 0;
+        CUDA_TRY(cudaMemcpy(&used, c->level_base + (c->simulated ? c->L : 0), sizeof used, cudaMemcpyDeviceToHost),
+                 "reading the pool size");
+        v->pool_used = used;
+    }
+    v->chunk_base = (const int64_t *)c->chunk_base;
+    v->wend = c->wend;
+    v->tc = c->tc;
+    v->t1 = c->t1;
+    v->num_nets = (int32_t)c->num_nets;
+    v->num_windows = c->W;
+    v->num_chunks = c->nchunks;
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_level_times(gatspi_ctx *c, float *ms, int32_t n) {
+    g_err.clear();
+    if (!c || !ms) return fail(GATSPI_EINVAL, "ctx and ms are required");
+    if (!(c->flags & GATSPI_FLAG_LEVEL_TIMING)) return fail(GATSPI_ESTATE, "created without GATSPI_FLAG_LEVEL_TIMING");
+    if (n != c->L) return fail(GATSPI_EINVAL, "ms needs num_levels entries");
+    if (!c->simulated) return fail(GATSPI_ESTATE, "simulate first");
+    gatspi_status st = sync_ctx(c);
+    if (st != GATSPI_OK) return st;
+    for (int l = 0; l < c->L; ++l)
+        CUDA_TRY(cudaEventElapsedTime(&ms[l], c->events[l], c->events[l + 1]), "reading level events");
+    return GATSPI_OK;
+}
+
+void gatspi_destroy(gatspi_ctx *c) {
+    if (!c) return;
+    cudaSetDevice(c->device);
+    if (c->loaded || c->simulated) cudaStreamSynchronize(c->last_stream);
+    free_all(c);
+    delete c;
+}
+
+}  // extern "C"

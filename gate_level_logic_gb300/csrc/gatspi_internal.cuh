@@ -1,0 +1,75 @@
+// Internal declarations shared by the host code (gatspi.cu) and the level kernel
+// (level_kernel.cu) of the GB300 gate-level re-simulator.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gatspi.h"
+
+namespace gatspi {
+
+constexpr int kBlock = 256;               // threads per level-kernel block = (gate, window) slots per tile
+constexpr int kWarps = kBlock / 32;
+constexpr int kMaxStage = 64;             // upper bound of stage_words
+constexpr int kDefaultStage = 24;
+constexpr int32_t kEOW = GATSPI_EOW;
+constexpr int32_t kNoArc = GATSPI_NO_ARC;
+
+// Look-back status words: flag in the top two bits, inclusive/aggregate value below.
+constexpr unsigned long long kFlagAgg = 1ull << 62;
+constexpr unsigned long long kFlagIncl = 2ull << 62;
+constexpr unsigned long long kValueMask = (1ull << 62) - 1;
+constexpr unsigned long long kSpinLimitNs = 2000000000ull;   // 2 s without progress -> ETIMEOUT
+
+// Device status word: [0] first error code, [1..3] details (gate / net, window, extra).
+constexpr int kStatusWords = 4;
+
+// Everything a level kernel reads or writes, by value in the kernel parameters.
+struct DevParams {
+    // netlist
+    const int4 *gate_desc;     // [G] x = first edge, y = n | truth-table mask << 8, z/w = delay-table offset lo/hi
+    const int4 *edge_desc;     // [E] x = source net, y = truth-table weight, z = wire rise | wire fall << 16
+    const int32_t *dly_data;   // per-instance conditional delay tables
+    // waveform store
+    int32_t *pool;
+    long long pool_words;
+    long long *chunk_base;     // [num_nets * nchunks]
+    uint32_t *wend;            // [num_nets * W]
+    const int32_t *window_len; // [W]
+    // toggle statistics
+    unsigned long long *tc;    // [G]
+    unsigned long long *t1;    // [G]
+    // scan state
+    unsigned long long *tile_status;  // [total tiles], zeroed per simulate
+    int32_t *tickets;                 // [L], zeroed per simulate
+    long long *level_base;            // [L+1]; [0] = words of the input waveforms
+    int32_t *status;                  // [kStatusWords]
+    // shape
+    int32_t num_inputs;
+    int32_t W;
+    int32_t nchunks;          // ceil(W / 32)
+    int32_t lpg_log2;         // log2(lanes per (gate, chunk) segment)
+    int32_t slots_per_gate;   // nchunks << lpg_log2
+    int32_t stage;            // output words staged on chip per lane
+};
+
+struct LevelLaunch {
+    int32_t level;
+    int32_t gate_begin;
+    int32_t num_gates;
+    int32_t num_tiles;
+    long long tile_base;
+};
+
+size_t level_smem_bytes(int stage);
+cudaError_t set_level_smem_limit(int stage);
+cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s);
+cudaError_t launch_window_lengths(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,
+                                  long long *len, cudaStream_t s);
+cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,
+                                 const long long *off, int32_t *words, cudaStream_t s);
+cudaError_t launch_load_index(const DevParams &p, const long long *off, long long nwords, int32_t *max_time,
+                              cudaStream_t s);
+
+}  // namespace gatspi

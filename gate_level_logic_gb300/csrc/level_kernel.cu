@@ -1,0 +1,481 @@
+// Level kernel of the GB300 gate-level re-simulator.
+//
+// One launch per logic level (GATSPI, Section 3, Fig. 5).  A block owns a tile of
+// 256 consecutive (gate, window) slots of the level; a warp holds one gate and 32
+// consecutive windows (or, for W < 32, several gates with W windows each), the
+// thread mapping the page chooses so that a warp's lanes run the same cell.
+//
+// Each lane runs Algorithm 1 of the page for its (gate, window): merge the fanin
+// waveforms with interconnect inertial filtering, resolve simultaneous switching,
+// look up the truth table by summed pin weights, pick the conditional delay (row =
+// switching pin and edges, column = the other pins' values) and apply the gate's
+// inertial filter (PATHPULSEPERCENT = 100).  The page runs this twice: a pass that
+// only counts output toggles (to size every output), a prefix sum over the counts,
+// and a pass that stores.  Here both passes share one kernel:
+//   1. every lane simulates once, keeping the first `stage` output words in shared
+//      memory ([word][lane] layout, bank-conflict free) and the toggle count, the
+//      time at 1 and the output length in registers;
+//   2. output lengths are scanned: warp shuffles, then the block's warps, then a
+//      decoupled look-back over earlier tiles of the level (tile order from an
+//      atomic ticket, so a block only ever waits for blocks that are running);
+//   3. lanes whose output fit store it from shared memory to the pool; lanes whose
+//      output was longer simulate a second time storing straight to the pool (the
+//      page's second pass, kept for them only);
+//   4. TC and T1 are reduced per gate with shuffles and one 64-bit atomic per
+//      (gate, chunk of 32 windows), and the window index of the level's nets is
+//      written.
+// No kernel traps: a malformed waveform, a missing delay arc, pool overflow or a
+// stalled look-back sets the device status word and the kernel carries on without
+// writing out of bounds.
+#include "gatspi_internal.cuh"
+
+namespace gatspi {
+
+namespace {
+
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_status(const int32_t *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ void raise_error(int32_t *status, int code, int a, int b, int c) {
+    if (atomicCAS(status, 0, code) == 0) {
+        status[1] = a;
+        status[2] = b;
+        status[3] = c;
+    }
+}
+
+// One fanin pin of a lane.
+struct Pin {
+    const int32_t *w;  // the source net's waveform for this window
+    int32_t len;       // its length in words, EOW included
+    int32_t p;         // index of the entry in effect (value = p & 1)
+    int32_t a;         // arrival time of the next transition at the pin, or EOW
+    uint32_t drf;      // interconnect delays: rise | fall << 16
+    uint32_t wbit;     // truth-table weight
+};
+
+// Next arrival of a pin: skip every pulse narrower than the interconnect delay of
+// its first edge (the fall delay when the pin is at 1, the rise delay when at 0);
+// the arrival is the next timestamp plus that delay.  False on a malformed wave.
+__device__ __forceinline__ bool next_arrival(Pin &s) {
+    for (;;) {
+        const int32_t d = (s.p & 1) ? (int32_t)(s.drf >> 16) : (int32_t)(s.drf & 0xffffu);
+        if (s.p + 1 >= s.len) return false;
+        const int32_t t1 = __ldg(s.w + s.p + 1);
+        if (t1 == kEOW) {
+            s.a = kEOW;
+            return true;
+        }
+        if (s.p + 2 >= s.len) return false;
+        const int32_t t2 = __ldg(s.w + s.p + 2);
+        if (t2 - t1 < d) {  // the pulse [t1, t2) never reaches the pin
+            s.p += 2;
+            continue;
+        }
+        s.a = t1 + d;
+        return true;
+    }
+}
+
+struct LaneResult {
+    int32_t len;   // output words, EOW included
+    int32_t tc;    // output toggles
+    int32_t t1;    // time at 1 within [0, Lw)
+    int32_t err;   // 0 or a gatspi_status
+};
+
+// Algorithm 1 for one (gate, window).  kGlobal = false: the first `stage` output
+// words go to shared memory (stride 32); kGlobal = true: every word goes to gout.
+template <int N, bool kGlobal>
+__device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const int32_t *__restrict__ D, int32_t Lw,
+                                               int32_t *stage, int stage_words, int32_t *__restrict__ gout) {
+    constexpr int kCols = 1 << (N - 1);
+    LaneResult r{0, 0, 0, 0};
+    auto put = [&](int32_t k, int32_t v) {
+        if (kGlobal) {
+            gout[k] = v;
+        } else if (k < stage_words) {
+            stage[k * 32] = v;
+        }
+    };
+
+    // initial values: pin index 1 when the waveform starts with -1
+    uint32_t vbits = 0, idx = 0;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        pin[i].p = (__ldg(pin[i].w) == -1) ? 1 : 0;
+        if (pin[i].p) {
+            vbits |= 1u << (N - 1 - i);
+            idx |= pin[i].wbit;
+        }
+    }
+    const int32_t y0 = (tt >> idx) & 1;
+    int32_t po = y0;        // index of the last output entry
+    int32_t top = 0;        // O[po]
+    int32_t second = 0;     // O[po - 1] (read only after a store)
+    int32_t t1acc = 0;      // signed sum of clipped entries: time at 1 before the final adjustment
+    put(0, y0 ? -1 : 0);
+    if (y0) put(1, 0);
+
+    bool ok = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i) ok &= next_arrival(pin[i]);
+
+    while (ok) {
+        int32_t t = pin[0].a;
+#pragma unroll
+        for (int i = 1; i < N; ++i) t = min(t, pin[i].a);
+        if (t == kEOW) break;
+
+        // every pin arriving at t switches together
+        uint32_t sw = 0;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            if (pin[i].a == t) {
+                pin[i].p += 1;
+                vbits ^= 1u << (N - 1 - i);
+                idx ^= pin[i].wbit;
+                sw |= 1u << i;
+            }
+        }
+        const int32_t y = (tt >> idx) & 1;
+        if (y != (po & 1)) {
+            // smallest finite conditional delay among the switching pins
+            const int e_out = y ? 0 : 1;
+            int32_t d = kNoArc;
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                if (sw & (1u << i)) {
+                    const int e_in = (pin[i].p & 1) ? 0 : 1;
+                    const uint32_t lo = vbits & ((1u << (N - 1 - i)) - 1u);
+                    const uint32_t col = ((vbits >> (N - i)) << (N - 1 - i)) | lo;
+                    d = min(d, __ldg(D + (4 * i + 2 * e_in + e_out) * kCols + col));
+                }
+            }
+            if (d == kNoArc) {
+                r.err = GATSPI_EBADLUT;
+                break;
+            }
+            if (top > t) {
+                // inertial filter: the last entry has not matured, cancel it
+                t1acc -= (po & 1) ? -min(top, Lw) : min(top, Lw);
+                --po;
+                top = second;
+            } else {
+                const int32_t to = t + d;
+                ++po;
+                put(po, to);
+                t1acc += (po & 1) ? -min(to, Lw) : min(to, Lw);
+                second = top;
+                top = to;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (sw & (1u << i)) ok &= next_arrival(pin[i]);
+    }
+    if (!ok) r.err = GATSPI_EBADWAVE;
+    put(po + 1, kEOW);
+    r.len = po + 2;
+    r.tc = po - y0;
+    r.t1 = t1acc + ((po & 1) ? Lw : 0);
+    return r;
+}
+
+// Pins of gate `g` in window `w` (chunk c): source waveforms from the window index.
+template <int N>
+__device__ __forceinline__ void load_pins(const DevParams &P, int first_edge, int c, int w, Pin (&pin)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const int4 e = __ldg(P.edge_desc + first_edge + i);
+        const long long src = e.x;
+        const long long base = __ldg(P.chunk_base + src * P.nchunks + c);
+        const uint32_t end = __ldg(P.wend + src * P.W + w);
+        const uint32_t start = (w & 31) ? __ldg(P.wend + src * P.W + w - 1) : 0u;
+        pin[i].w = P.pool + base + start;
+        pin[i].len = (int32_t)(end - start);
+        pin[i].wbit = (uint32_t)e.y;
+        pin[i].drf = (uint32_t)e.z;
+    }
+}
+
+template <int N, bool kGlobal>
+__device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd, int c, int w, int32_t Lw,
+                                                 int32_t *stage, int32_t *gout) {
+    Pin pin[N];
+    load_pins<N>(P, gd.x, c, w, pin);
+    const uint32_t tt = (uint32_t)gd.y >> 8;
+    const long long dly = (long long)(uint32_t)gd.z | ((long long)gd.w << 32);
+    return run_lane<N, kGlobal>(pin, tt, P.dly_data + dly, Lw, stage, P.stage, gout);
+}
+
+template <bool kGlobal>
+__device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, int c, int w, int32_t Lw, int32_t *stage,
+                                               int32_t *gout) {
+    switch (gd.y & 7) {
+        case 1: return simulate_gate<1, kGlobal>(P, gd, c, w, Lw, stage, gout);
+        case 2: return simulate_gate<2, kGlobal>(P, gd, c, w, Lw, stage, gout);
+        case 3: return simulate_gate<3, kGlobal>(P, gd, c, w, Lw, stage, gout);
+        default: return simulate_gate<4, kGlobal>(P, gd, c, w, Lw, stage, gout);
+    }
+}
+
+// Exclusive prefix of this tile within the level (decoupled look-back).  Called by
+// one thread.  Publishes the tile's aggregate, then its inclusive prefix.
+__device__ long long look_back(const DevParams &P, const LevelLaunch &L, int tile, long long total) {
+    unsigned long long *st = P.tile_status + L.tile_base;
+    if (tile == 0) {
+        st_relaxed(st, kFlagIncl | (unsigned long long)total);
+        return 0;
+    }
+    st_relaxed(st + tile, kFlagAgg | (unsigned long long)total);
+    long long excl = 0;
+    int k = tile - 1;
+    const unsigned long long t0 = global_ns();
+    unsigned sleep = 32;
+    for (;;) {
+        const unsigned long long v = ld_relaxed(st + k);
+        if ((v >> 62) == 0) {
+            if (ld_status(P.status) != 0) break;                 // another block failed: stop waiting
+            if (global_ns() - t0 > kSpinLimitNs) {
+                raise_error(P.status, GATSPI_ETIMEOUT, L.level, tile, k);
+                break;
+            }
+            __nanosleep(sleep);
+            if (sleep < 1024) sleep <<= 1;
+            continue;
+        }
+        excl += (long long)(v & kValueMask);
+        if ((v >> 62) == 2) break;
+        --k;
+    }
+    st_relaxed(st + tile, kFlagIncl | (unsigned long long)(excl + total));
+    return excl;
+}
+
+__global__ void __launch_bounds__(kBlock, 4) level_kernel(const DevParams P, const LevelLaunch L) {
+    extern __shared__ int32_t smem[];
+    __shared__ int s_tile;
+    __shared__ int s_skip;
+    __shared__ uint32_t s_warp[kWarps];
+    __shared__ long long s_out0;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    if (tid == 0) {
+        s_tile = atomicAdd(P.tickets + L.level, 1);
+        s_skip = ld_status(P.status) != 0;   // an earlier level failed: publish empty tiles only
+    }
+    __syncthreads();
+    const int tile = s_tile;
+    const bool skip = s_skip != 0;
+
+    // slot -> (gate, chunk, window)
+    const long long slot = (long long)tile * kBlock + tid;
+    const long long gl = slot / P.slots_per_gate;
+    const int r = (int)(slot - gl * P.slots_per_gate);
+    const int c = r >> P.lpg_log2;
+    const int j = r & ((1 << P.lpg_log2) - 1);
+    const int w = c * 32 + j;
+    const bool gate_ok = !skip && gl < L.num_gates;
+    const bool valid = gate_ok && w < P.W;
+    const int g = L.gate_begin + (int)gl;
+
+    int32_t *stage = smem + warp * (P.stage * 32) + lane;
+    LaneResult res{0, 0, 0, 0};
+    int4 gd = make_int4(0, 0, 0, 0);
+    int32_t Lw = 0;
+    if (valid) {
+        gd = __ldg(P.gate_desc + g);
+        Lw = __ldg(P.window_len + w);
+        res = dispatch<false>(P, gd, c, w, Lw, stage, nullptr);
+        if (res.err) {
+            raise_error(P.status, res.err, g, w, 0);
+            res.len = 0;
+        }
+    }
+    const bool overflow = valid && res.len > P.stage;
+
+    // warp scan of the output lengths
+    uint32_t incl = (uint32_t)res.len;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const uint32_t excl = incl - (uint32_t)res.len;
+    if (lane == 31) s_warp[warp] = incl;
+
+    // TC and T1 per (gate, chunk): reduce over the segment's lanes, one atomic each
+    long long tcs = res.tc, t1s = res.t1;
+    for (int o = (1 << P.lpg_log2) >> 1; o >= 1; o >>= 1) {
+        tcs += __shfl_xor_sync(0xffffffffu, tcs, o);
+        t1s += __shfl_xor_sync(0xffffffffu, t1s, o);
+    }
+    if (gate_ok && j == 0) {
+        atomicAdd(P.tc + g, (unsigned long long)tcs);
+        atomicAdd(P.t1 + g, (unsigned long long)t1s);
+    }
+    __syncthreads();
+
+    if (tid == 0) {
+        long long total = 0;
+        for (int k = 0; k < kWarps; ++k) {
+            const uint32_t v = s_warp[k];
+            s_warp[k] = (uint32_t)total;
+            total += v;
+        }
+        const long long prefix = look_back(P, L, tile, total);
+        long long out0 = P.level_base[L.level] + prefix;
+        if (tile == L.num_tiles - 1) P.level_base[L.level + 1] = out0 + total;
+        if (out0 + total > P.pool_words) {
+            raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, tile, 0);
+            out0 = -1;
+        }
+        s_out0 = out0;
+    }
+    __syncthreads();
+    const long long out0 = s_out0;
+    const long long my_off = out0 + s_warp[warp] + excl;
+    const uint32_t lead_excl = __shfl_sync(0xffffffffu, excl, lane & ~((1 << P.lpg_log2) - 1));
+
+    if (valid && out0 >= 0) {
+        const long long net = (long long)P.num_inputs + g;
+        if (!overflow) {
+            int32_t *dst = P.pool + my_off;
+            for (int k = 0; k < res.len; ++k) dst[k] = stage[k * 32];
+        } else {
+            const LaneResult again = dispatch<true>(P, gd, c, w, Lw, nullptr, P.pool + my_off);
+            if (again.len != res.len) raise_error(P.status, GATSPI_EBADWAVE, g, w, 1);
+        }
+        P.wend[net * P.W + w] = excl + (uint32_t)res.len - lead_excl;
+        if (j == 0) P.chunk_base[net * P.nchunks + c] = out0 + s_warp[warp] + lead_excl;
+    }
+}
+
+// Window index of the loaded input waveforms and a format check of every one of
+// them (Fig. 3): head [0] or [-1, 0], timestamps strictly increasing in 1 .. 2^30,
+// EOW last.  One thread per (input, window).
+__global__ void load_index_kernel(const DevParams P, const long long *__restrict__ off, long long nwords,
+                                  int32_t *max_time) {
+    const long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long n = (long long)P.num_inputs * P.W;
+    if (k == 0) P.level_base[0] = nwords;
+    if (k >= n) return;
+    const int w = (int)(k % P.W);
+    const long long pi = k / P.W;
+    const long long s = off[k], e = off[k + 1];
+    const long long c0 = off[k - (w & 31)];            // first window of the chunk
+    bool ok = s >= 0 && e <= nwords && e - s >= 2 && e - c0 < (1ll << 32) && c0 <= s && (k > 0 || s == 0);
+    int32_t tmax = 0;
+    if (ok) {
+        const int32_t *x = P.pool + s;
+        long long q = 0;
+        if (x[0] == -1) {
+            ok = x[1] == 0;
+            q = 1;
+        } else {
+            ok = x[0] == 0;
+        }
+        int32_t prev = 0;
+        for (long long i = q + 1; ok && i < e - s - 1; ++i) {
+            ok = x[i] > prev && x[i] <= (1 << 30);
+            prev = x[i];
+        }
+        ok = ok && x[e - s - 1] == kEOW;
+        tmax = prev;
+    }
+    if (!ok) {
+        raise_error(P.status, GATSPI_EBADWAVE, (int)pi, w, 0);
+        return;
+    }
+    atomicMax(max_time, tmax);
+    if ((w & 31) == 0) P.chunk_base[pi * P.nchunks + (w >> 5)] = c0;
+    P.wend[k] = (uint32_t)(e - c0);
+}
+
+// Length of waveform (net, sel[s]) for an export of selected windows.
+__global__ void window_lengths_kernel(const DevParams P, long long num_nets, const int32_t *__restrict__ sel, int nsel,
+                                      long long *__restrict__ len) {
+    const long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= num_nets * nsel) return;
+    const long long net = k / nsel;
+    const int w = sel[k % nsel];
+    const uint32_t end = P.wend[net * P.W + w];
+    const uint32_t start = (w & 31) ? P.wend[net * P.W + w - 1] : 0u;
+    len[k] = (long long)(end - start);
+}
+
+// Copy of waveform (net, sel[s]) to words[off[k] ..], one warp per waveform.
+__global__ void window_gather_kernel(const DevParams P, long long num_nets, const int32_t *__restrict__ sel, int nsel,
+                                     const long long *__restrict__ off, int32_t *__restrict__ words) {
+    const long long k = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (k >= num_nets * nsel) return;
+    const long long net = k / nsel;
+    const int w = sel[k % nsel];
+    const uint32_t start = (w & 31) ? P.wend[net * P.W + w - 1] : 0u;
+    const int32_t *src = P.pool + P.chunk_base[net * P.nchunks + (w >> 5)] + start;
+    const long long n = off[k + 1] - off[k];
+    for (long long i = lane; i < n; i += 32) words[off[k] + i] = src[i];
+}
+
+}  // namespace
+
+cudaError_t launch_window_lengths(const DevParams &p, long long num_nets, const int32_t *sel, int nsel, long long *len,
+                                  cudaStream_t s) {
+    const long long n = num_nets * nsel;
+    window_lengths_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p, num_nets, sel, nsel, len);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,
+                                 const long long *off, int32_t *words, cudaStream_t s) {
+    const long long n = num_nets * nsel;
+    window_gather_kernel<<<(unsigned)((n * 32 + 255) / 256), 256, 0, s>>>(p, num_nets, sel, nsel, off, words);
+    return cudaGetLastError();
+}
+
+size_t level_smem_bytes(int stage) { return (size_t)kWarps * 32 * (size_t)stage * sizeof(int32_t); }
+
+cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
+    const size_t smem = level_smem_bytes(p.stage);
+    level_kernel<<<l.num_tiles, kBlock, smem, s>>>(p, l);
+    return cudaGetLastError();
+}
+
+cudaError_t set_level_smem_limit(int stage) {
+    return cudaFuncSetAttribute(level_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)level_smem_bytes(stage));
+}
+
+cudaError_t launch_load_index(const DevParams &p, const long long *off, long long nwords, int32_t *max_time,
+                              cudaStream_t s) {
+    const long long n = (long long)p.num_inputs * p.W;
+    const int threads = 256;
+    const long long blocks = n > 0 ? (n + threads - 1) / threads : 1;
+    load_index_kernel<<<(unsigned)blocks, threads, 0, s>>>(p, off, nwords, max_time);
+    return cudaGetLastError();
+}
+
+}  // namespace gatspi

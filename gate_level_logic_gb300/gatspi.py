@@ -1,0 +1,161 @@
+"""ctypes binding of the C ABI in include/gatspi.h (argument marshalling only).
+
+Every function keeps the C name.  Nothing here simulates: every step of the
+re-simulation runs in the CUDA library ``libgatspi.so``; if that library is missing
+the import fails loudly (there is no fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgatspi.so")
+
+GATSPI_EOW = 2147483647
+GATSPI_NO_ARC = 2147483647
+GATSPI_MAX_PINS = 4
+GATSPI_HOST, GATSPI_DEVICE = 0, 1
+GATSPI_FLAG_LEVEL_TIMING = 0x1
+GATSPI_FLAG_NO_GRAPH = 0x2
+
+STATUS = {
+    0: "GATSPI_OK", 1: "GATSPI_EINVAL", 2: "GATSPI_ENOMEM", 3: "GATSPI_EPOOL_OVERFLOW", 4: "GATSPI_EBADWAVE",
+    5: "GATSPI_ECUDA", 6: "GATSPI_ESTATE", 7: "GATSPI_EBADLUT", 8: "GATSPI_ETIMEOUT",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+_p = ctypes.c_void_p
+
+
+class gatspi_netlist(ctypes.Structure):
+    _fields_ = [
+        ("num_inputs", ctypes.c_int32), ("num_gates", ctypes.c_int32), ("num_levels", ctypes.c_int32),
+        ("num_types", ctypes.c_int32), ("level_offsets", _p), ("gate_type", _p), ("type_num_pins", _p),
+        ("type_tt_off", _p), ("tt_len", ctypes.c_int64), ("tt_data", _p), ("fanin_off", _p), ("fanin_net", _p),
+        ("pin_weight", _p), ("wire_rise", _p), ("wire_fall", _p), ("gate_dly_off", _p), ("dly_len", ctypes.c_int64),
+        ("dly_data", _p),
+    ]
+
+
+class gatspi_config(ctypes.Structure):
+    _fields_ = [("num_windows", ctypes.c_int32), ("window_len", _p), ("flags", ctypes.c_uint32),
+                ("stage_words", ctypes.c_int32)]
+
+
+class gatspi_views(ctypes.Structure):
+    _fields_ = [
+        ("pool", _p), ("pool_words", ctypes.c_int64), ("pool_used", ctypes.c_int64), ("chunk_base", _p),
+        ("wend", _p), ("tc", _p), ("t1", _p), ("num_nets", ctypes.c_int32), ("num_windows", ctypes.c_int32),
+        ("num_chunks", ctypes.c_int32),
+    ]
+
+
+# exported symbol -> (restype, argtypes)
+SIGNATURES = {
+    "gatspi_create": (ctypes.c_int, [ctypes.POINTER(gatspi_netlist), ctypes.POINTER(gatspi_config), _p, ctypes.c_size_t,
+                                     ctypes.POINTER(_p)]),
+    "gatspi_load_waveforms": (ctypes.c_int, [_p, _p, _p, ctypes.c_size_t, ctypes.c_int, _p]),
+    "gatspi_simulate": (ctypes.c_int, [_p, _p]),
+    "gatspi_sync": (ctypes.c_int, [_p]),
+    "gatspi_toggle_stats": (ctypes.c_int, [_p, _p, _p, _p]),
+    "gatspi_get_waveform": (ctypes.c_int, [_p, ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_size_t,
+                                           ctypes.POINTER(ctypes.c_size_t)]),
+    "gatspi_export_offsets": (ctypes.c_int, [_p, _p, ctypes.c_size_t]),
+    "gatspi_export_windows": (ctypes.c_int, [_p, _p, ctypes.c_int32, _p, _p, ctypes.c_size_t]),
+    "gatspi_device_views": (ctypes.c_int, [_p, ctypes.POINTER(gatspi_views)]),
+    "gatspi_level_times": (ctypes.c_int, [_p, _p, ctypes.c_int32]),
+    "gatspi_destroy": (None, [_p]),
+    "gatspi_last_error": (ctypes.c_char_p, []),
+    "gatspi_status_name": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+_lib = None
+
+
+def library():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libgatspi.so is missing: build it with gate_level_logic_gb300.build.build() "
+                               "(needs nvcc); there is no CPU fallback")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+class GatspiError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (STATUS.get(status, status), message))
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise GatspiError(rc, library().gatspi_last_error().decode(errors="replace"))
+
+
+def gatspi_create(nl: gatspi_netlist, cfg: gatspi_config, d_pool: int, pool_words: int) -> int:
+    ctx = _p()
+    _check(library().gatspi_create(ctypes.byref(nl), ctypes.byref(cfg), _p(d_pool), pool_words, ctypes.byref(ctx)))
+    return ctx.value
+
+
+def gatspi_load_waveforms(ctx: int, off: int, words: int, nwords: int, where: int, stream: int = 0):
+    _check(library().gatspi_load_waveforms(_p(ctx), _p(off), _p(words), nwords, where, _p(stream)))
+
+
+def gatspi_simulate(ctx: int, stream: int = 0):
+    _check(library().gatspi_simulate(_p(ctx), _p(stream)))
+
+
+def gatspi_sync(ctx: int):
+    _check(library().gatspi_sync(_p(ctx)))
+
+
+def gatspi_toggle_stats(ctx: int, tc: int, t0: int, t1: int):
+    _check(library().gatspi_toggle_stats(_p(ctx), _p(tc), _p(t0), _p(t1)))
+
+
+def gatspi_get_waveform(ctx: int, net: int, window: int, buf: int, cap: int) -> int:
+    n = ctypes.c_size_t()
+    rc = library().gatspi_get_waveform(_p(ctx), net, window, _p(buf), cap, ctypes.byref(n))
+    if rc != 0 and not (rc == 1 and n.value > cap):
+        _check(rc)
+    return n.value
+
+
+def gatspi_export_offsets(ctx: int, off: int, n: int):
+    _check(library().gatspi_export_offsets(_p(ctx), _p(off), n))
+
+
+def gatspi_export_windows(ctx: int, windows: int, nsel: int, off: int, words: int, cap: int):
+    _check(library().gatspi_export_windows(_p(ctx), _p(windows), nsel, _p(off), _p(words), cap))
+
+
+def gatspi_device_views(ctx: int) -> gatspi_views:
+    v = gatspi_views()
+    _check(library().gatspi_device_views(_p(ctx), ctypes.byref(v)))
+    return v
+
+
+def gatspi_level_times(ctx: int, ms: int, n: int):
+    _check(library().gatspi_level_times(_p(ctx), _p(ms), n))
+
+
+def gatspi_destroy(ctx: int):
+    library().gatspi_destroy(_p(ctx))
+
+
+def gatspi_last_error() -> str:
+    return library().gatspi_last_error().decode(errors="replace")
+
+
+def gatspi_status_name(status: int) -> str:
+    return library().gatspi_status_name(status).decode()

@@ -1,0 +1,158 @@
+"""A small Python front end over the C ABI: marshals numpy netlist arrays into the
+C structs, allocates the waveform pool as a torch int32 CUDA tensor, and passes
+torch streams through.  All simulation work happens in libgatspi.so.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import gatspi as _c
+
+
+def _arr(a, dtype):
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class Simulator:
+    """One netlist, one window configuration, one borrowed waveform pool.
+
+    ``net`` is any object with the netlist arrays of include/gatspi.h as attributes
+    (num_inputs, num_gates, num_levels, level_offsets, gate_type, type_num_pins,
+    type_tt_off, tt_data, fanin_off, fanin_net, pin_weight, wire_rise, wire_fall,
+    gate_dly_off, dly_data).
+    """
+
+    def __init__(self, net, window_len, pool_words: int = None, pool=None, stage_words: int = -1, flags: int = 0,
+                 device: int = None):
+        import torch
+        self._torch = torch
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+        wl = _arr(window_len, np.int64).reshape(-1)
+        self.num_windows = int(wl.size)
+        self.num_inputs = int(net.num_inputs)
+        self.num_gates = int(net.num_gates)
+        self.num_levels = int(net.num_levels)
+        self.num_nets = self.num_inputs + self.num_gates
+        if pool is None:
+            if pool_words is None:
+                raise ValueError("give pool_words or pool")
+            pool_words = (int(pool_words) + 3) // 4 * 4
+            pool = torch.empty(pool_words, dtype=torch.int32, device=self.device)
+        self.pool = pool
+        keep = dict(
+            level_offsets=_arr(net.level_offsets, np.int32), gate_type=_arr(net.gate_type, np.int32),
+            type_num_pins=_arr(net.type_num_pins, np.int32), type_tt_off=_arr(net.type_tt_off, np.int32),
+            tt_data=_arr(net.tt_data, np.uint8), fanin_off=_arr(net.fanin_off, np.int32),
+            fanin_net=_arr(net.fanin_net, np.int32), pin_weight=_arr(net.pin_weight, np.int32),
+            wire_rise=_arr(net.wire_rise, np.int32), wire_fall=_arr(net.wire_fall, np.int32),
+            gate_dly_off=_arr(net.gate_dly_off, np.int64), dly_data=_arr(net.dly_data, np.int32),
+            window_len=wl,
+        )
+        nl = _c.gatspi_netlist(
+            self.num_inputs, self.num_gates, self.num_levels, len(keep["type_num_pins"]),
+            keep["level_offsets"].ctypes.data, keep["gate_type"].ctypes.data, keep["type_num_pins"].ctypes.data,
+            keep["type_tt_off"].ctypes.data, keep["tt_data"].size, keep["tt_data"].ctypes.data,
+            keep["fanin_off"].ctypes.data, keep["fanin_net"].ctypes.data, keep["pin_weight"].ctypes.data,
+            keep["wire_rise"].ctypes.data, keep["wire_fall"].ctypes.data, keep["gate_dly_off"].ctypes.data,
+            keep["dly_data"].size, keep["dly_data"].ctypes.data)
+        cfg = _c.gatspi_config(self.num_windows, keep["window_len"].ctypes.data, int(flags), int(stage_words))
+        with torch.cuda.device(self.device):
+            self.ctx = _c.gatspi_create(nl, cfg, self.pool.data_ptr(), self.pool.numel())
+        self.window_len = wl
+
+    # -- lifecycle ---------------------------------------------------------------
+    def close(self):
+        if getattr(self, "ctx", None):
+            _c.gatspi_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # -- calls -------------------------------------------------------------------
+    def load(self, pi_off, pi_words, stream=None):
+        """Load input waveforms from numpy (host) arrays or torch CUDA tensors."""
+        torch = self._torch
+        if isinstance(pi_words, torch.Tensor) and pi_words.is_cuda:
+            off = pi_off.to(torch.int64).contiguous()
+            words = pi_words.to(torch.int32).contiguous()
+            _c.gatspi_load_waveforms(self.ctx, off.data_ptr(), words.data_ptr(), words.numel(), _c.GATSPI_DEVICE,
+                                     _stream_handle(stream))
+            return
+        if isinstance(pi_words, torch.Tensor):
+            off_a, words_a = pi_off.contiguous(), pi_words.contiguous()
+            off_p, words_p, n = off_a.data_ptr(), words_a.data_ptr(), words_a.numel()
+        else:
+            off_a, words_a = _arr(pi_off, np.int64), _arr(pi_words, np.int32)
+            off_p, words_p, n = off_a.ctypes.data, words_a.ctypes.data, words_a.size
+        _c.gatspi_load_waveforms(self.ctx, off_p, words_p, n, _c.GATSPI_HOST, _stream_handle(stream))
+
+    def simulate(self, stream=None):
+        _c.gatspi_simulate(self.ctx, _stream_handle(stream))
+
+    def sync(self):
+        _c.gatspi_sync(self.ctx)
+
+    def toggle_stats(self):
+        """(tc, t0, t1) int64 arrays [num_gates], summed over windows."""
+        tc = np.zeros(max(self.num_gates, 1), np.int64)
+        t0 = np.zeros_like(tc)
+        t1 = np.zeros_like(tc)
+        _c.gatspi_toggle_stats(self.ctx, tc.ctypes.data, t0.ctypes.data, t1.ctypes.data)
+        n = self.num_gates
+        return tc[:n], t0[:n], t1[:n]
+
+    def waveform(self, net: int, window: int) -> np.ndarray:
+        n = _c.gatspi_get_waveform(self.ctx, net, window, 0, 0)
+        buf = np.zeros(max(n, 1), np.int32)
+        _c.gatspi_get_waveform(self.ctx, net, window, buf.ctypes.data, buf.size)
+        return buf[:n]
+
+    def export_offsets(self) -> np.ndarray:
+        off = np.zeros(self.num_nets * self.num_windows + 1, np.int64)
+        _c.gatspi_export_offsets(self.ctx, off.ctypes.data, off.size)
+        return off
+
+    def export_windows(self, windows):
+        """(off, words) CSR of the waveforms of the given windows for every net,
+        net-major: waveform (net, windows[s]) is entry net * len(windows) + s."""
+        sel = _arr(windows, np.int32).reshape(-1)
+        off = np.zeros(self.num_nets * sel.size + 1, np.int64)
+        _c.gatspi_export_windows(self.ctx, sel.ctypes.data, sel.size, off.ctypes.data, 0, 0)
+        words = np.zeros(max(int(off[-1]), 1), np.int32)
+        _c.gatspi_export_windows(self.ctx, sel.ctypes.data, sel.size, off.ctypes.data, words.ctypes.data, words.size)
+        return off, words[:int(off[-1])]
+
+    def views(self) -> _c.gatspi_views:
+        return _c.gatspi_device_views(self.ctx)
+
+    def pool_used(self) -> int:
+        return int(self.views().pool_used)
+
+    def pool_host(self) -> np.ndarray:
+        """Copy of the used part of the pool."""
+        used = self.pool_used()
+        return self.pool[:used].cpu().numpy()
+
+    def level_times(self) -> np.ndarray:
+        ms = np.zeros(max(self.num_levels, 1), np.float32)
+        _c.gatspi_level_times(self.ctx, ms.ctypes.data, self.num_levels)
+        return ms[:self.num_levels]

@@ -1,0 +1,266 @@
+/*
+ * gatspi.h -- C ABI of the GB300 gate-level re-simulator.
+ *
+ * The library re-simulates a levelised gate-level netlist, cycle window by cycle
+ * window, from known primary / pseudo-primary input waveforms, as described in
+ * "GATSPI: GPU-Accelerated Gate-Level Simulation for Power Improvement" (DAC '22):
+ *   - Section 3, Fig. 3: the waveform array format;
+ *   - Section 3, Fig. 4: truth-table lookup by summed pin weights and the
+ *     conditional (SDF COND) delay table indexed by switching arc and the weights
+ *     of the non-switching pins;
+ *   - Section 3, Fig. 5: one device-resident waveform pool, levels simulated in
+ *     order, each gate/cycle-window re-simulated by one GPU thread;
+ *   - Section 3, Algorithm 1: per (gate, window) the merge of the fanin waveforms,
+ *     interconnect inertial filtering, multiple-simultaneous-input-switching
+ *     resolution, delay selection and gate inertial filtering with
+ *     PATHPULSEPERCENT = 100, and the output toggle count (TC) that sizes the
+ *     output before it is stored (the two-pass scheme).
+ *
+ * Conventions for every call:
+ *   - every call returns a gatspi_status; nothing throws across this ABI, nothing
+ *     exits, no kernel traps;
+ *   - gatspi_last_error() returns a message about the calling thread's last failure;
+ *   - host arrays passed in are copied during the call; the caller keeps ownership;
+ *   - the waveform pool is borrowed: a device buffer the caller allocates (for
+ *     example a torch int32 tensor) and keeps alive until gatspi_destroy;
+ *   - asynchronous failures (pool overflow, malformed waveform, missing delay arc,
+ *     a stalled scan) are latched in a device status word and reported by the next
+ *     synchronising call (gatspi_sync, gatspi_toggle_stats, gatspi_get_waveform,
+ *     gatspi_export_offsets);
+ *   - a context is used by one host thread at a time.
+ *
+ * Waveform format (Fig. 3): int32 timestamps of signal toggles; the index parity
+ * is the logic value (even = 0, odd = 1); a waveform that starts at 1 begins with
+ * -1, 0 and one that starts at 0 begins with 0; the array ends with
+ * GATSPI_EOW = INT32_MAX.  Timestamps are relative to the start of their window.
+ *
+ * Windows (cycle parallelism, Section 1 and Section 4): the testbench is cut into
+ * W independent windows; every window starts from the zero-delay steady state of
+ * its input values and is simulated to completion (events scheduled past the
+ * window's end are kept in the waveform and counted in TC; T1/T0 count only
+ * [0, window_len)).
+ */
+#ifndef GATSPI_H
+#define GATSPI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GATSPI_EOW 2147483647
+#define GATSPI_NO_ARC 2147483647   /* delay-table entry of an arc that cannot occur */
+#define GATSPI_MAX_PINS 4
+
+typedef enum {
+    GATSPI_OK = 0,
+    GATSPI_EINVAL = 1,          /* invalid argument or netlist                       */
+    GATSPI_ENOMEM = 2,          /* a device allocation failed                        */
+    GATSPI_EPOOL_OVERFLOW = 3,  /* the waveform pool is too small for the outputs    */
+    GATSPI_EBADWAVE = 4,        /* an input waveform breaks the Fig. 3 format        */
+    GATSPI_ECUDA = 5,           /* a CUDA runtime call failed                        */
+    GATSPI_ESTATE = 6,          /* call out of order (e.g. simulate before load)     */
+    GATSPI_EBADLUT = 7,         /* every switching arc of an output change is NO_ARC */
+    GATSPI_ETIMEOUT = 8         /* a device-side wait gave up (scan look-back)       */
+} gatspi_status;
+
+/* Where a buffer passed to gatspi_load_waveforms lives. */
+enum { GATSPI_HOST = 0, GATSPI_DEVICE = 1 };
+
+/* gatspi_config.flags */
+#define GATSPI_FLAG_LEVEL_TIMING 0x1u  /* record CUDA events around every level kernel */
+#define GATSPI_FLAG_NO_GRAPH 0x2u      /* launch level kernels directly, no CUDA graph  */
+
+/*
+ * Levelised netlist (all host arrays, copied by gatspi_create).
+ *
+ * Nets 0 .. num_inputs-1 are primary / pseudo-primary inputs; gate g drives net
+ * num_inputs + g.  Gates are numbered in level order: level l holds gates
+ * [level_offsets[l], level_offsets[l+1]); every fanin of a gate in level l is an
+ * input or a gate of a lower level.
+ *
+ *   gate_type[G]          cell type of every gate, 0 .. num_types-1
+ *   type_num_pins[T]      pins of every type, 1 .. GATSPI_MAX_PINS
+ *   type_tt_off[T], tt_data[tt_len]
+ *                         truth table of type t: tt_data[type_tt_off[t] + k], k < 2^n,
+ *                         entries 0/1; k is the sum of pin_weight over the pins at 1
+ *                         (Fig. 4: NAND2 with A = 2^1, B = 2^0 has Y = [1, 1, 1, 0])
+ *   fanin_off[G+1], fanin_net[E], pin_weight[E], wire_rise[E], wire_fall[E]
+ *                         pins of gate g are edges fanin_off[g] .. fanin_off[g+1]-1 in pin
+ *                         order: driving net, truth-table weight (the weights of one gate
+ *                         are the distinct powers 2^0 .. 2^(n-1)), interconnect rise / fall
+ *                         delay (0 .. 65535)
+ *   gate_dly_off[G], dly_data[dly_len]
+ *                         per-instance conditional delay table of gate g at
+ *                         dly_data[gate_dly_off[g]], laid out [4n][2^(n-1)] int32:
+ *                         row = 4*pin + 2*e_in + e_out (RISE = 0, FALL = 1; e_in is the
+ *                         switching pin's new edge, e_out the output's), column = the
+ *                         values of the other pins, in pin order with the first one most
+ *                         significant (Fig. 4: for AOI21 B->Y, A1 = 2^1 and A2 = 2^0);
+ *                         entries are 0 .. 2^24-1 or GATSPI_NO_ARC.  Instances may share
+ *                         a table.
+ */
+typedef struct {
+    int32_t num_inputs;
+    int32_t num_gates;
+    int32_t num_levels;
+    int32_t num_types;
+    const int32_t *level_offsets;
+    const int32_t *gate_type;
+    const int32_t *type_num_pins;
+    const int32_t *type_tt_off;
+    int64_t tt_len;
+    const uint8_t *tt_data;
+    const int32_t *fanin_off;
+    const int32_t *fanin_net;
+    const int32_t *pin_weight;
+    const int32_t *wire_rise;
+    const int32_t *wire_fall;
+    const int64_t *gate_dly_off;
+    int64_t dly_len;
+    const int32_t *dly_data;
+} gatspi_netlist;
+
+/*
+ * Run configuration.
+ *   num_windows   W >= 1 independent cycle windows
+ *   window_len    host array [W] of window lengths in time units (1 .. 2^30)
+ *   flags         GATSPI_FLAG_*
+ *   stage_words   output words a thread keeps on chip while it simulates (0 .. 64);
+ *                 -1 selects the library default.  A (gate, window) whose output
+ *                 waveform is longer is simulated a second time once its output
+ *                 offset is known, storing straight to the pool; 0 makes every
+ *                 (gate, window) take that second pass (the count-then-write scheme).
+ */
+typedef struct {
+    int32_t num_windows;
+    const int64_t *window_len;
+    uint32_t flags;
+    int32_t stage_words;
+} gatspi_config;
+
+typedef struct gatspi_ctx gatspi_ctx;
+
+/*
+ * Device views of the simulation state (valid until gatspi_destroy).
+ *
+ * The pool holds every (net, window) waveform, net-major and window-minor, without
+ * gaps: first the input waveforms as loaded, then the gates' outputs level by level.
+ * Windows are grouped in chunks of 32 (one chunk when W <= 32): waveform (net, w)
+ * starts at pool[chunk_base[net * num_chunks + w / 32] + start] and ends (EOW
+ * included) at pool[chunk_base[...] + wend[net * W + w]], where start = 0 for the
+ * first window of a chunk and wend[net * W + w - 1] otherwise.
+ */
+typedef struct {
+    const int32_t *pool;
+    int64_t pool_words;            /* capacity                                       */
+    int64_t pool_used;             /* words written by the last load + simulate      */
+    const int64_t *chunk_base;     /* [num_nets * num_chunks]                        */
+    const uint32_t *wend;          /* [num_nets * num_windows]                       */
+    const unsigned long long *tc;  /* [num_gates] output toggles summed over windows */
+    const unsigned long long *t1;  /* [num_gates] time at 1 summed over windows      */
+    int32_t num_nets;
+    int32_t num_windows;
+    int32_t num_chunks;
+} gatspi_views;
+
+/*
+ * Create a simulator for one netlist and window configuration.
+ *   d_pool      device int32 buffer of pool_words words, 16-byte aligned, borrowed
+ *   pool_words  capacity, a multiple of 4 words
+ * Validates the netlist (EINVAL with a message naming the first offending gate),
+ * copies it to the device and allocates the context's own device arrays (ENOMEM).
+ * Fig. 5 / Algorithm 1 inputs.
+ */
+gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, int32_t *d_pool,
+                            size_t pool_words, gatspi_ctx **out);
+
+/*
+ * Load the input waveforms of every (input, window).
+ *   off    int64 [num_inputs * W + 1] offsets into words, input-major and window-minor,
+ *          non-decreasing (CSR)
+ *   words  int32 [nwords] waveform words (Fig. 3 format)
+ *   where  GATSPI_HOST (pageable or pinned host memory) or GATSPI_DEVICE
+ * Copies the words to the front of the pool on `stream`, checks the format of every
+ * waveform on the device (timestamps after the head strictly increasing, 1 .. 2^30)
+ * and builds the window index.  Synchronises `stream` before returning: EBADWAVE
+ * names the first malformed (input, window); EPOOL_OVERFLOW if nwords exceeds the
+ * pool; EINVAL if the longest path could carry a timestamp to EOW.
+ */
+gatspi_status gatspi_load_waveforms(gatspi_ctx *ctx, const int64_t *off, const int32_t *words, size_t nwords,
+                                    int where, void *stream);
+
+/*
+ * Re-simulate every level, in order, on `stream` (a cudaStream_t; NULL = legacy
+ * default stream).  Asynchronous: returns after enqueueing.  Clears TC/T1 and the
+ * device status first.  Per level one kernel runs Algorithm 1 for every
+ * (gate, window) of the level, scans the output lengths into pool offsets and
+ * stores the output waveforms and window index; TC and T1 are reduced per gate in
+ * the same kernel.  The level sequence is captured once into a CUDA graph (unless
+ * GATSPI_FLAG_NO_GRAPH) and replayed by later calls.
+ */
+gatspi_status gatspi_simulate(gatspi_ctx *ctx, void *stream);
+
+/* Wait for the last simulate / load and report a latched device error. */
+gatspi_status gatspi_sync(gatspi_ctx *ctx);
+
+/*
+ * SAIF-style toggle statistics per gate, summed over windows (host arrays [G]; any
+ * may be NULL): tc = output toggles, t1 = time at 1, t0 = time at 0, with
+ * t0 + t1 = sum of window_len.  Synchronises first.
+ */
+gatspi_status gatspi_toggle_stats(gatspi_ctx *ctx, int64_t *tc, int64_t *t0, int64_t *t1);
+
+/*
+ * Copy one (net, window) waveform to host memory.  *len receives its length in
+ * words (EOW included) even when it exceeds cap, in which case nothing is copied
+ * and EINVAL is returned.  Synchronises first.
+ */
+gatspi_status gatspi_get_waveform(gatspi_ctx *ctx, int32_t net, int32_t window, int32_t *buf, size_t cap,
+                                  size_t *len);
+
+/*
+ * Write CSR offsets of every (net, window) waveform, net-major and window-minor, to
+ * host memory: off[k] .. off[k+1] delimit waveform k = net * W + w in the pool
+ * (n = num_nets * W + 1 entries).  Synchronises first.
+ */
+gatspi_status gatspi_export_offsets(gatspi_ctx *ctx, int64_t *off, size_t n);
+
+/*
+ * Export the waveforms of selected windows for every net, as CSR in host memory:
+ *   windows  host int32 [nsel], each 0 .. W-1 (any order, repeats allowed)
+ *   off      host int64 [num_nets * nsel + 1]: waveform (net, windows[s]) occupies
+ *            words[off[net * nsel + s] .. off[net * nsel + s + 1])
+ *   words    host int32 [cap], or NULL to query the size (off is still filled)
+ * Windows are independent re-simulations, so this is the natural unit to check or
+ * dump a slice of a large run.  Allocates and frees device scratch; synchronises.
+ * EINVAL if cap < off[num_nets * nsel] (off is filled either way).
+ */
+gatspi_status gatspi_export_windows(gatspi_ctx *ctx, const int32_t *windows, int32_t nsel, int64_t *off,
+                                    int32_t *words, size_t cap);
+
+/* Device views of the pool, window index and statistics (see gatspi_views). */
+gatspi_status gatspi_device_views(gatspi_ctx *ctx, gatspi_views *out);
+
+/*
+ * Per-level kernel times in milliseconds of the last simulate (needs
+ * GATSPI_FLAG_LEVEL_TIMING); ms has num_levels entries.  Synchronises first.
+ */
+gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *ms, int32_t n);
+
+/* Release the context's device arrays (not the borrowed pool).  NULL is allowed. */
+void gatspi_destroy(gatspi_ctx *ctx);
+
+/* Message about the calling thread's last failed call ("" if none). */
+const char *gatspi_last_error(void);
+
+/* Name of a status code. */
+const char *gatspi_status_name(gatspi_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GATSPI_H */

@@ -1,0 +1,104 @@
+"""The C ABI library on the CPU: it loads, exports every entry point that
+include/gatspi.h declares, and its host-side validation rejects bad netlists
+before touching a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gatspi.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gatspi_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gate_level_logic_gb300 import build
+    build.build()
+    from gate_level_logic_gb300 import gatspi
+    return gatspi
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert set(names) == set(lib.SIGNATURES), "binding and header disagree"
+
+
+def _struct(lib, net, W=1, stage=-1):
+    keep = dict(lo=np.ascontiguousarray(net.level_offsets, np.int32), gt=np.ascontiguousarray(net.gate_type, np.int32),
+                tp=np.ascontiguousarray(net.type_num_pins, np.int32), to=np.ascontiguousarray(net.type_tt_off, np.int32),
+                tt=np.ascontiguousarray(net.tt_data, np.uint8), fo=np.ascontiguousarray(net.fanin_off, np.int32),
+                fn=np.ascontiguousarray(net.fanin_net, np.int32), pw=np.ascontiguousarray(net.pin_weight, np.int32),
+                wr=np.ascontiguousarray(net.wire_rise, np.int32), wf=np.ascontiguousarray(net.wire_fall, np.int32),
+                do=np.ascontiguousarray(net.gate_dly_off, np.int64), dd=np.ascontiguousarray(net.dly_data, np.int32),
+                wl=np.full(W, 100, np.int64))
+    nl = lib.gatspi_netlist(net.num_inputs, net.num_gates, net.num_levels, len(keep["tp"]), keep["lo"].ctypes.data,
+                            keep["gt"].ctypes.data, keep["tp"].ctypes.data, keep["to"].ctypes.data, keep["tt"].size,
+                            keep["tt"].ctypes.data, keep["fo"].ctypes.data, keep["fn"].ctypes.data,
+                            keep["pw"].ctypes.data, keep["wr"].ctypes.data, keep["wf"].ctypes.data,
+                            keep["do"].ctypes.data, keep["dd"].size, keep["dd"].ctypes.data)
+    cfg = lib.gatspi_config(W, keep["wl"].ctypes.data, 0, stage)
+    return nl, cfg, keep
+
+
+def _create_status(lib, nl, cfg, pool=0x10000, words=1024):
+    ctx = ctypes.c_void_p()
+    rc = lib.library().gatspi_create(ctypes.byref(nl), ctypes.byref(cfg), ctypes.c_void_p(pool), words,
+                                     ctypes.byref(ctx))
+    if rc == 0:
+        lib.gatspi_destroy(ctx.value)
+    return rc, lib.gatspi_last_error()
+
+
+def _mutated(**changes):
+    net, _ = synth.make("tiny")
+    for k, v in changes.items():
+        arr = getattr(net, k).copy()
+        idx, val = v
+        arr[idx] = val
+        setattr(net, k, arr)
+    return net
+
+
+@pytest.mark.parametrize("change,needle", [
+    (dict(fanin_net=(60 * 2, 150)), "not an input or a gate of a lower level"),   # gate 60 reads a later net
+    (dict(pin_weight=(0, 3)), "pin weights"),
+    (dict(wire_rise=(5, -1)), "interconnect delay"),
+    (dict(wire_fall=(5, 70000)), "interconnect delay"),
+    (dict(gate_type=(7, 99)), "type"),
+    (dict(dly_data=(3, -5)), "delay"),
+    (dict(level_offsets=(2, 250)), "level"),
+])
+def test_invalid_netlists_are_rejected_on_the_host(lib, change, needle):
+    net = _mutated(**change)
+    nl, cfg, keep = _struct(lib, net)
+    rc, msg = _create_status(lib, nl, cfg)
+    assert rc == 1 and needle in msg, (rc, msg)
+
+
+def test_invalid_config_and_pool_are_rejected(lib):
+    net, _ = synth.make("tiny")
+    nl, cfg, keep = _struct(lib, net, W=1, stage=65)
+    assert _create_status(lib, nl, cfg)[0] == 1
+    nl, cfg, keep = _struct(lib, net, W=1)
+    assert _create_status(lib, nl, cfg, pool=0x10004)[0] == 1       # not 16-byte aligned
+    assert _create_status(lib, nl, cfg, words=1023)[0] == 1         # not a multiple of 4 words
+    cfg.num_windows = 0
+    assert _create_status(lib, nl, cfg)[0] == 1
+
+
+def test_status_names(lib):
+    for code, name in lib.STATUS.items():
+        assert lib.gatspi_status_name(code) == name

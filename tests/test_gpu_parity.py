@@ -1,0 +1,231 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Waveforms, window offsets and toggle statistics are integers: the bar is bit-exact
+equality.  Small and medium cases compare the whole pool; the 1M-gate workload (the
+configuration bench.py times) compares the whole pool too; the 5M-gate, scan-style
+and sweep workloads compare every net's waveform in sampled windows (windows are
+independent re-simulations, so the oracle can recompute any subset of them) plus
+invariants that hold at any size.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from helpers import EOW, INF, single_gate, uniform_delays
+
+pytestmark = pytest.mark.gpu
+
+THREADS = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module")
+def gpu():
+    import torch
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    torch.cuda.set_device(0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from gate_level_logic_gb300 import Simulator
+    return Simulator
+
+
+def run_gpu(Simulator, net, stim, pool_words, stage_words=-1, flags=0, repeat=1):
+    with Simulator(net, stim.window_len, pool_words=pool_words, stage_words=stage_words, flags=flags) as sim:
+        sim.load(stim.pi_off, stim.pi_words)
+        for _ in range(repeat):
+            sim.simulate()
+        tc, t0, t1 = sim.toggle_stats()
+        return dict(off=sim.export_offsets(), pool=sim.pool_host(), tc=tc, t0=t0, t1=t1)
+
+
+def assert_same(got, ref, what=""):
+    assert np.array_equal(got["off"], ref.off), "window offsets differ " + what
+    if not np.array_equal(got["pool"], ref.pool):
+        bad = np.nonzero(got["pool"] != ref.pool)[0][:5] if got["pool"].size == ref.pool.size else "size"
+        raise AssertionError("waveforms differ %s at %s" % (what, bad))
+    assert np.array_equal(got["tc"], ref.tc), "TC differs " + what
+    assert np.array_equal(got["t1"], ref.t1), "T1 differs " + what
+    assert np.array_equal(got["t0"], ref.t0), "T0 differs " + what
+
+
+def pool_for(ref, slack=1.05):
+    return int(ref.pool.size * slack) + 4096
+
+
+def test_tiny_full(gpu, oracle_lib):
+    net, stim = synth.make("tiny")
+    ref = oracle_lib.simulate(net, stim)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref)), ref)
+
+
+def test_50k_full(gpu, oracle_lib):
+    net, stim = synth.make("50k")
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref)), ref)
+
+
+@pytest.mark.parametrize("stage_words,flags", [(0, 0), (1, 0), (3, 0), (8, 0), (64, 0), (24, 2)])
+def test_50k_staging_and_launch_variants(gpu, oracle_lib, stage_words, flags):
+    """stage 0 is the count-then-write scheme for every lane; other sizes mix both."""
+    net, stim = synth.make("50k")
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref), stage_words=stage_words, flags=flags), ref,
+                "stage=%d flags=%d" % (stage_words, flags))
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 7, 16, 31, 32, 33, 63, 64, 65, 100, 257])
+def test_window_counts(gpu, oracle_lib, W):
+    """Ragged window chunks, several gates per warp (W < 32), ragged tiles."""
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=3001, num_inputs=37, num_levels=9, seed=W,
+                                                   cond_fraction=0.3))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=37, cycles=max(W, 300), period=500,
+                                                      activity=0.2, windows=W, seed=W, glitch_frac=0.2))
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref), stage_words=8), ref, "W=%d" % W)
+
+
+def test_random_small_netlists(gpu, oracle_lib):
+    """The seeded corner-heavy cases the oracle was pinned on (zero delays, zero-width
+    pulses, 1-4 pin random cells, conditional arcs, multiple windows)."""
+    import test_oracle_pins as pins
+    for seed in range(120):
+        net, stim = pins._random_case(seed)
+        ref = oracle_lib.simulate(net, stim)
+        assert_same(run_gpu(gpu, net, stim, pool_for(ref), stage_words=(0, 2, 24)[seed % 3]), ref,
+                    "seed %d" % seed)
+
+
+def test_quiet_inputs_and_empty_level(gpu, oracle_lib):
+    tts = [synth.truth_table("NAND2"), synth.truth_table("INV")]
+    D2 = uniform_delays(2, 3, 4, tts[0])
+    D1 = uniform_delays(1, 2, 2, tts[1])
+    net = synth.build_netlist(num_inputs=2, level_gates=[2, 0, 1], type_names=["NAND2", "INV"],
+                              type_num_pins=[2, 1], type_tts=tts, gate_type=[0, 1, 0],
+                              fanins=[[0, 1], [0], [2, 3]], wire_rise=np.zeros(5), wire_fall=np.ones(5),
+                              delay_tables=[D2, D1, D2])
+    for waves in ([[0, EOW], [-1, 0, EOW]], [[0, 5, 9, 40, EOW], [-1, 0, 20, EOW]]):
+        stim = synth.from_waveforms([[w] for w in waves], 100)
+        ref = oracle_lib.simulate(net, stim)
+        assert_same(run_gpu(gpu, net, stim, pool_for(ref)), ref)
+
+
+def test_maximum_activity(gpu, oracle_lib):
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=4000, num_inputs=64, num_levels=16, seed=5,
+                                                   cond_fraction=0.5))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=64, cycles=256, period=200, activity=1.0,
+                                                      windows=64, seed=5, glitch_frac=0.5, glitch_span=(1, 4)))
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref), stage_words=16), ref)
+
+
+def test_replay_is_deterministic(gpu, oracle_lib):
+    net, stim = synth.make("50k")
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref), repeat=3), ref, "after 3 replays")
+
+
+def test_errors_leave_context_usable(gpu, oracle_lib):
+    from gate_level_logic_gb300 import GatspiError
+    net, stim = synth.make("tiny")
+    ref = oracle_lib.simulate(net, stim)
+    # pool too small for the outputs: reported at the next synchronising call; a quiet
+    # stimulus needs at most 3 words per gate output and fits
+    small = int(stim.pi_words.size) + 3 * net.num_gates + 64
+    assert small < ref.pool.size
+    with gpu(net, stim.window_len, pool_words=small) as sim:
+        with pytest.raises(GatspiError) as e:
+            sim.simulate()
+        assert e.value.name == "GATSPI_ESTATE"
+        sim.load(stim.pi_off, stim.pi_words)
+        sim.simulate()
+        with pytest.raises(GatspiError) as e:
+            sim.toggle_stats()
+        assert e.value.name == "GATSPI_EPOOL_OVERFLOW"
+        # a quiet stimulus fits: the same context simulates correctly afterwards
+        quiet = synth.from_waveforms([[[0, EOW]] for _ in range(net.num_inputs)], stim.window_len)
+        sim.load(quiet.pi_off, quiet.pi_words)
+        sim.simulate()
+        tc, _, _ = sim.toggle_stats()
+        assert (tc == 0).all()
+    # malformed input waveforms are rejected at load
+    with gpu(net, stim.window_len, pool_words=pool_for(ref)) as sim:
+        bad = stim.pi_words.copy()
+        bad[stim.pi_off[3] + 2] = bad[stim.pi_off[3] + 1]       # repeated timestamp
+        with pytest.raises(GatspiError) as e:
+            sim.load(stim.pi_off, bad)
+        assert e.value.name == "GATSPI_EBADWAVE"
+        sim.load(stim.pi_off, stim.pi_words)
+        sim.simulate()
+        tc, _, _ = sim.toggle_stats()
+        assert np.array_equal(tc, ref.tc)
+    # an output change whose switching arcs are all missing
+    tt = np.array([0, 0, 1, 1], np.uint8)
+    lut = single_gate(tt, 2, np.full((8, 2), INF, np.int32))
+    st = synth.from_waveforms([[[0, 50, EOW]], [[0, EOW]]], 100)
+    with gpu(lut, st.window_len, pool_words=1024) as sim:
+        sim.load(st.pi_off, st.pi_words)
+        sim.simulate()
+        with pytest.raises(GatspiError) as e:
+            sim.sync()
+        assert e.value.name == "GATSPI_EBADLUT"
+
+
+def test_single_waveform_and_window_export(gpu, oracle_lib):
+    net, stim = synth.make("50k")
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    with gpu(net, stim.window_len, pool_words=pool_for(ref)) as sim:
+        sim.load(stim.pi_off, stim.pi_words)
+        sim.simulate()
+        for net_id, w in [(0, 0), (255, 15), (256, 3), (net.num_inputs + net.num_gates - 1, 15), (30000, 7)]:
+            assert np.array_equal(sim.waveform(net_id, w), ref.wave(net_id, w))
+        sel = [15, 0, 7, 7]
+        off, words = sim.export_windows(sel)
+        sub = oracle_lib.simulate(net, synth.select_windows(stim, sel))
+        assert np.array_equal(off, sub.off) and np.array_equal(words, sub.pool)
+
+
+@pytest.mark.slow
+def test_1M_full(gpu, oracle_lib):
+    """The configuration bench.py times: 1M gates, 40 levels, 256 windows; whole pool."""
+    net, stim = synth.make("1M")
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref)), ref, "1M")
+
+
+def _sampled(gpu, oracle_lib, net, stim, windows, pool_words):
+    with gpu(net, stim.window_len, pool_words=pool_words) as sim:
+        sim.load(stim.pi_off, stim.pi_words)
+        sim.simulate()
+        tc, t0, t1 = sim.toggle_stats()
+        off, words = sim.export_windows(windows)
+        used = sim.pool_used()
+    sub = oracle_lib.simulate(net, synth.select_windows(stim, windows), threads=min(THREADS, len(windows)))
+    assert np.array_equal(off, sub.off), "offsets of the sampled windows differ"
+    assert np.array_equal(words, sub.pool), "waveforms of the sampled windows differ"
+    # properties at any size: T0 + T1 covers every window; TC at least the sampled windows' toggles
+    assert np.array_equal(t0 + t1, np.full(net.num_gates, int(stim.window_len.sum())))
+    assert (tc >= sub.tc).all() and (t1 >= sub.t1).all()
+    assert used <= pool_words
+    return tc
+
+
+@pytest.mark.slow
+def test_5M_sampled(gpu, oracle_lib):
+    net, stim = synth.make("5M")
+    _sampled(gpu, oracle_lib, net, stim, [0, 77, 127], pool_words=60 << 28)
+
+
+@pytest.mark.slow
+def test_scan500k_sampled(gpu, oracle_lib):
+    net, stim = synth.make("scan500k")
+    _sampled(gpu, oracle_lib, net, stim, [0, 131, 255], pool_words=48 << 28)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("activity,W", [(0.01, 1), (0.20, 16), (0.50, 256), (0.05, 4096)])
+def test_1M_sweep_points_sampled(gpu, oracle_lib, activity, W):
+    net, stim = synth.sweep(activity, W)
+    windows = [0] if W == 1 else [0, W // 2 + 1, W - 1]
+    _sampled(gpu, oracle_lib, net, stim, windows, pool_words=120 << 28)
