@@ -252,6 +252,28 @@ def run_reference(args):
     return 0
 
 
+def _e2e(args, sim, stim, net, stream, dist, events_per_step):
+    import torch
+    pin_off = torch.from_numpy(np.ascontiguousarray(stim.pi_off, np.int64)).pin_memory()
+    pin_words = torch.from_numpy(np.ascontiguousarray(stim.pi_words, np.int32)).pin_memory()
+    e2e_steps = max(1, args.steps)
+    _barrier(dist)
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(e2e_steps):
+        sim.load(pin_off, pin_words, stream=stream)
+        sim.simulate(stream=stream)
+        tc_e, _, t1_e = sim.toggle_stats()
+    torch.cuda.synchronize()
+    e2e_s = _max_over_ranks(dist, time.perf_counter() - t)
+    assert int(tc_e.sum()) == events_per_step
+    e2e_value = _sum_over_ranks(dist, events_per_step * e2e_steps) / e2e_s
+    h2d = pin_off.numel() * 8 + pin_words.numel() * 4
+    d2h = 2 * 8 * net.num_gates + 16       # TC and T1 per gate, status word
+
+    return e2e_value, h2d, d2h
+
+
 def run_gpu(args):
     import torch
 
@@ -262,7 +284,12 @@ def run_gpu(args):
     dist = _init_pg(world)
     torch.cuda.set_device(local)
     build.build()
-    net, stim = synth.make(WORKLOAD)
+    over = {}
+    if args.windows:
+        over["windows"] = args.windows
+    if args.cycles:
+        over["cycles"] = args.cycles
+    net, stim = synth.make(WORKLOAD, **over)
     W = stim.num_windows
     flags = gatspi.GATSPI_FLAG_LEVEL_TIMING
     pool_words = int(args.pool_gb * (1 << 30) / 4)
@@ -314,22 +341,10 @@ def run_gpu(args):
     traffic = _traffic(net.num_levels)
 
     # ---- end to end through the C ABI: host buffers, copies inside the region ---
-    pin_off = torch.from_numpy(np.ascontiguousarray(stim.pi_off, np.int64)).pin_memory()
-    pin_words = torch.from_numpy(np.ascontiguousarray(stim.pi_words, np.int32)).pin_memory()
-    e2e_steps = max(1, args.steps)
-    _barrier(dist)
-    torch.cuda.synchronize()
-    t = time.perf_counter()
-    for _ in range(e2e_steps):
-        sim.load(pin_off, pin_words, stream=stream)
-        sim.simulate(stream=stream)
-        tc_e, _, t1_e = sim.toggle_stats()
-    torch.cuda.synchronize()
-    e2e_s = _max_over_ranks(dist, time.perf_counter() - t)
-    assert int(tc_e.sum()) == events_per_step
-    e2e_value = _sum_over_ranks(dist, events_per_step * e2e_steps) / e2e_s
-    h2d = pin_off.numel() * 8 + pin_words.numel() * 4
-    d2h = 2 * 8 * net.num_gates + 16       # TC and T1 per gate, status word
+    if args.no_e2e:
+        e2e_value, h2d, d2h = None, 0, 0
+    else:
+        e2e_value, h2d, d2h = _e2e(args, sim, stim, net, stream, dist, events_per_step)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -346,7 +361,8 @@ def run_gpu(args):
             "algorithmic_bytes_per_launch": float(lvl_bytes.mean()),
             "avg_launch_ms": float(level_ms.sum() / (args.steps * net.num_levels)),
         },
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "e2e": None if e2e_value is None else {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                                               "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(args.steps * net.num_levels),
         "clocks": clocks.summary(),
     }
@@ -370,6 +386,9 @@ def main():
     ap.add_argument("--stage-words", type=int, default=-1)
     ap.add_argument("--pool-gb", type=float, default=24.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--windows", type=int, default=0, help="profiling only: number of cycle windows")
+    ap.add_argument("--cycles", type=int, default=0, help="profiling only: number of stimulus cycles")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

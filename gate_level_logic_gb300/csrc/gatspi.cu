@@ -419,7 +419,9 @@ gatspi_status gatspi_simulate(gatspi_ctx *c, void *stream) {
     cudaStream_t s = (cudaStream_t)stream;
     c->last_stream = s;
     c->simulated = true;
-    if (c->flags & GATSPI_FLAG_NO_GRAPH) return enqueue_levels(c, s);
+    // per-level events are recorded on the caller's stream: they cannot be read back
+    // from a replayed graph, so timing runs launch the levels directly
+    if (c->flags & (GATSPI_FLAG_NO_GRAPH | GATSPI_FLAG_LEVEL_TIMING)) return enqueue_levels(c, s);
     if (!c->graph_exec) {
         CUDA_TRY(cudaStreamCreateWithFlags(&c->capture_stream, cudaStreamNonBlocking), "creating the capture stream");
         CUDA_TRY(cudaStreamBeginCapture(c->capture_stream, cudaStreamCaptureModeThreadLocal), "beginning capture");

@@ -70,7 +70,7 @@ typedef enum {
 enum { GATSPI_HOST = 0, GATSPI_DEVICE = 1 };
 
 /* gatspi_config.flags */
-#define GATSPI_FLAG_LEVEL_TIMING 0x1u  /* record CUDA events around every level kernel */
+#define GATSPI_FLAG_LEVEL_TIMING 0x1u  /* record CUDA events around every level kernel (no graph) */
 #define GATSPI_FLAG_NO_GRAPH 0x2u      /* launch level kernels directly, no CUDA graph  */
 
 /*
@@ -198,8 +198,9 @@ gatspi_status gatspi_load_waveforms(gatspi_ctx *ctx, const int64_t *off, const i
  * device status first.  Per level one kernel runs Algorithm 1 for every
  * (gate, window) of the level, scans the output lengths into pool offsets and
  * stores the output waveforms and window index; TC and T1 are reduced per gate in
- * the same kernel.  The level sequence is captured once into a CUDA graph (unless
- * GATSPI_FLAG_NO_GRAPH) and replayed by later calls.
+ * the same kernel.  The level sequence is captured once into a CUDA graph and
+ * replayed by later calls, unless GATSPI_FLAG_NO_GRAPH or GATSPI_FLAG_LEVEL_TIMING
+ * is set (then the level kernels are launched directly on `stream`).
  */
 gatspi_status gatspi_simulate(gatspi_ctx *ctx, void *stream);
 
