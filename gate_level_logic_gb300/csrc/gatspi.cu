@@ -49,6 +49,8 @@ cudaError_t dev_alloc(T **p, size_t n) {
 
 }  // namespace
 
+void gatspi_set_last_error(const char *msg) { g_err = msg ? msg : ""; }
+
 struct gatspi_ctx {
     int device = 0;
     int32_t P = 0, G = 0, L = 0, W = 0;

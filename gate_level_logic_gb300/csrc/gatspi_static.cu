@@ -1,0 +1,138 @@
+// Allocation-free entry point: one logic level re-simulated with caller-owned
+// buffers only.
+//
+// Some callers cannot allocate device memory: code that runs inside a framework
+// which owns the whole device memory through its own allocator, or code that is
+// not allowed to allocate once it has started.  gatspi_create allocates the
+// context's arrays; this entry point instead takes every input and output buffer
+// from the caller and keeps the only scratch the level kernel needs -- the
+// look-back flags of its tiles, the tile ticket and the status word -- in a
+// file-scope device array of fixed size.  Every GPU that loads the library holds
+// that array until the process exits.
+#include <cstdio>
+#include <mutex>
+
+#include "gatspi_internal.cuh"
+
+using namespace gatspi;
+
+namespace {
+
+constexpr int kStaticTiles = 1 << 16;                     // tiles of one level at most
+constexpr int kTicketWord = kStaticTiles;                 // index of the ticket word
+constexpr int kStatusWord = kStaticTiles + 1;             // index of the status words (2 x 8 bytes)
+constexpr int kScratchWords = kStaticTiles + 4;
+
+// Look-back flags, then the tile ticket, then the 4-int status word.  Shared by
+// every call on a device; a call clears what it uses before its kernel runs.
+static __device__ __align__(256) unsigned long long g_level_scratch[kScratchWords];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void *g_scratch_addr[kMaxDevices] = {};
+
+thread_local char g_msg[256];
+
+}  // namespace
+
+// Defined in gatspi.cu: routes a message to gatspi_last_error().
+void gatspi_set_last_error(const char *msg);
+
+extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a, void *stream) {
+    auto err = [](gatspi_status s, const char *m) {
+        gatspi_set_last_error(m);
+        return s;
+    };
+    if (!a) return err(GATSPI_EINVAL, "args are required");
+    if (!a->gate_desc || !a->edge_desc || !a->dly_data || !a->window_len || !a->pool || !a->chunk_base ||
+        !a->wend || !a->tc || !a->t1 || !a->level_base)
+        return err(GATSPI_EINVAL, "every buffer of gatspi_level_args is required");
+    if (((uintptr_t)a->gate_desc & 15) || ((uintptr_t)a->edge_desc & 15))
+        return err(GATSPI_EINVAL, "gate_desc and edge_desc must be 16-byte aligned");
+    if (a->num_inputs < 0 || a->num_windows < 1 || a->gate_begin < 0 || a->num_gates < 0 || a->pool_words < 0)
+        return err(GATSPI_EINVAL, "negative sizes");
+    if (a->stage_words < -1 || a->stage_words > kMaxStage) return err(GATSPI_EINVAL, "stage_words out of range");
+
+    DevParams p{};
+    p.W = a->num_windows;
+    p.nchunks = (p.W + 31) / 32;
+    int lpg = 32;
+    if (p.W < 32) {
+        lpg = 1;
+        while (lpg < p.W) lpg <<= 1;
+    }
+    p.lpg_log2 = 0;
+    while ((1 << p.lpg_log2) < lpg) ++p.lpg_log2;
+    p.slots_per_gate = p.nchunks << p.lpg_log2;
+    const long long slots = (long long)a->num_gates * p.slots_per_gate;
+    const long long tiles = slots > 0 ? (slots + kBlock - 1) / kBlock : 1;
+    if (tiles > kStaticTiles)
+        return err(GATSPI_EINVAL, "level too large for the static scratch (at most 65536 tiles of 256 slots)");
+
+    // once per device, with that device current: the device address of the scratch
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return err(GATSPI_ECUDA, "no current CUDA device");
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        if (!g_scratch_addr[dev]) {
+            void *ptr = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&ptr, g_level_scratch);
+            if (e != cudaSuccess || !ptr) {
+                snprintf(g_msg, sizeof g_msg, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+                return err(GATSPI_ECUDA, g_msg);
+            }
+            g_scratch_addr[dev] = ptr;
+        }
+        scratch = g_scratch_addr[dev];
+    }
+    unsigned long long *words = (unsigned long long *)scratch;
+
+    p.gate_desc = (const int4 *)a->gate_desc;
+    p.edge_desc = (const int4 *)a->edge_desc;
+    p.dly_data = a->dly_data;
+    p.pool = a->pool;
+    p.pool_words = a->pool_words;
+    p.chunk_base = (long long *)a->chunk_base;
+    p.wend = a->wend;
+    p.window_len = a->window_len;
+    p.tc = a->tc;
+    p.t1 = a->t1;
+    p.tile_status = words;
+    p.tickets = (int32_t *)(words + kTicketWord);
+    p.level_base = (long long *)a->level_base;
+    p.status = (int32_t *)(words + kStatusWord);
+    p.num_inputs = a->num_inputs;
+    p.stage = a->stage_words < 0 ? kDefaultStage : a->stage_words;
+
+    LevelLaunch l{};
+    l.level = 0;
+    l.gate_begin = a->gate_begin;
+    l.num_gates = a->num_gates;
+    l.num_tiles = (int32_t)tiles;
+    l.tile_base = 0;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = set_level_smem_limit(p.stage);
+    // clear the flags of the tiles this call uses, the ticket and the status
+    if (e == cudaSuccess) e = cudaMemsetAsync(words, 0, sizeof(unsigned long long) * (size_t)tiles, s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(words + kTicketWord, 0, sizeof(unsigned long long) * (kScratchWords - kTicketWord), s);
+    if (e == cudaSuccess) e = launch_level(p, l, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        snprintf(g_msg, sizeof g_msg, "level kernel: %s", cudaGetErrorString(e));
+        return err(GATSPI_ECUDA, g_msg);
+    }
+    int32_t st[kStatusWords] = {0, 0, 0, 0};
+    e = cudaMemcpy(st, words + kStatusWord, sizeof st, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return err(GATSPI_ECUDA, "reading the status word");
+    if (st[0] != GATSPI_OK) {
+        snprintf(g_msg, sizeof g_msg, "device error %d (detail %d, %d, %d)", st[0], st[1], st[2], st[3]);
+        return err((gatspi_status)st[0], g_msg);
+    }
+    gatspi_set_last_error("");
+    return GATSPI_OK;
+}

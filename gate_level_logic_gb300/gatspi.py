@@ -51,6 +51,15 @@ class gatspi_views(ctypes.Structure):
     ]
 
 
+class gatspi_level_args(ctypes.Structure):
+    _fields_ = [
+        ("gate_desc", _p), ("edge_desc", _p), ("dly_data", _p), ("window_len", _p), ("pool", _p),
+        ("pool_words", ctypes.c_int64), ("chunk_base", _p), ("wend", _p), ("tc", _p), ("t1", _p),
+        ("level_base", _p), ("num_inputs", ctypes.c_int32), ("num_windows", ctypes.c_int32),
+        ("gate_begin", ctypes.c_int32), ("num_gates", ctypes.c_int32), ("stage_words", ctypes.c_int32),
+    ]
+
+
 # exported symbol -> (restype, argtypes)
 SIGNATURES = {
     "gatspi_create": (ctypes.c_int, [ctypes.POINTER(gatspi_netlist), ctypes.POINTER(gatspi_config), _p, ctypes.c_size_t,
@@ -65,6 +74,7 @@ SIGNATURES = {
     "gatspi_export_windows": (ctypes.c_int, [_p, _p, ctypes.c_int32, _p, _p, ctypes.c_size_t]),
     "gatspi_device_views": (ctypes.c_int, [_p, ctypes.POINTER(gatspi_views)]),
     "gatspi_level_times": (ctypes.c_int, [_p, _p, ctypes.c_int32]),
+    "gatspi_simulate_level_static": (ctypes.c_int, [ctypes.POINTER(gatspi_level_args), _p]),
     "gatspi_destroy": (None, [_p]),
     "gatspi_last_error": (ctypes.c_char_p, []),
     "gatspi_status_name": (ctypes.c_char_p, [ctypes.c_int]),
@@ -147,6 +157,10 @@ def gatspi_device_views(ctx: int) -> gatspi_views:
 
 def gatspi_level_times(ctx: int, ms: int, n: int):
     _check(library().gatspi_level_times(_p(ctx), _p(ms), n))
+
+
+def gatspi_simulate_level_static(args: gatspi_level_args, stream: int = 0):
+    _check(library().gatspi_simulate_level_static(ctypes.byref(args), _p(stream)))
 
 
 def gatspi_destroy(ctx: int):

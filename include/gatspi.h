@@ -251,6 +251,66 @@ gatspi_status gatspi_device_views(gatspi_ctx *ctx, gatspi_views *out);
  */
 gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *ms, int32_t n);
 
+/*
+ * Buffers of one logic level for gatspi_simulate_level_static (all device memory,
+ * owned by the caller).  The layouts are the library's own:
+ *   gate_desc   int32 [4 * num_gates of the netlist], 16-byte aligned; for gate g:
+ *               {first edge of g, n | truth-table bits << 8 (bit k = entry k),
+ *                low and high 32 bits of the delay-table offset}
+ *   edge_desc   int32 [4 * edges], 16-byte aligned; for edge e:
+ *               {driving net, truth-table weight, wire rise | wire fall << 16, 0}
+ *   dly_data    the delay tables of gatspi_netlist
+ *   window_len  int32 [num_windows]
+ *   pool, chunk_base, wend
+ *               the waveform store of gatspi_views (pool_words = capacity); the
+ *               sources of this level must already be in it
+ *   tc, t1      per-gate toggle count and time at 1, accumulated (not cleared)
+ *   level_base  int64 [2]: [0] = first pool word of this level's outputs (read),
+ *               [1] = one past its last word (written)
+ */
+typedef struct {
+    const int32_t *gate_desc;
+    const int32_t *edge_desc;
+    const int32_t *dly_data;
+    const int32_t *window_len;
+    int32_t *pool;
+    int64_t pool_words;
+    int64_t *chunk_base;
+    uint32_t *wend;
+    unsigned long long *tc;
+    unsigned long long *t1;
+    int64_t *level_base;
+    int32_t num_inputs;
+    int32_t num_windows;
+    int32_t gate_begin;   /* first gate of the level */
+    int32_t num_gates;    /* gates in the level */
+    int32_t stage_words;  /* as in gatspi_config */
+} gatspi_level_args;
+
+/*
+ * Re-simulate one logic level without allocating any memory.  The paper has no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory -- code running under a framework that owns all of the device memory
+ * through its own allocator, or code that must not allocate once it has started.
+ * The caller passes every input and output buffer (gatspi_level_args); the only
+ * scratch, the look-back flags, tile ticket and status word of the level kernel,
+ * lives in a file-scope device array of 65536 tile flags plus 32 bytes (about
+ * 512 KiB) that every GPU which loads the library holds until the process exits.
+ *
+ *   - No cudaMalloc, cudaFree or allocating library call is made.
+ *   - A level may have at most 65536 tiles of 256 (gate, window) slots; a larger
+ *     level returns GATSPI_EINVAL before anything runs.
+ *   - The first call on a device looks up the device address of the scratch array
+ *     (with that device current); make that first call before any stream capture.
+ *   - Every call shares the one array and clears the part it uses before its
+ *     kernel runs; calls that overlap on the GPU (other streams, other threads)
+ *     race on it and must be serialised by the caller.
+ *   - Synchronous: enqueues on `stream`, waits for it, and returns the kernel's
+ *     status (GATSPI_EPOOL_OVERFLOW, GATSPI_EBADWAVE, GATSPI_EBADLUT, ...).
+ * Results are identical to the level kernels gatspi_simulate runs.
+ */
+gatspi_status gatspi_simulate_level_static(const gatspi_level_args *args, void *stream);
+
 /* Release the context's device arrays (not the borrowed pool).  NULL is allowed. */
 void gatspi_destroy(gatspi_ctx *ctx);
 

@@ -1,0 +1,158 @@
+"""The allocation-free entry point gatspi_simulate_level_static.
+
+It serves callers that cannot allocate device memory (for example code running
+under a framework that owns all of the device memory, or code that must not
+allocate after start-up): they hand over every buffer, and the level kernel's only
+scratch sits in a fixed device array inside the library.  This test plays such a
+caller: it allocates every buffer itself (torch tensors), lays out the input
+waveforms and their window index itself, runs every logic level through the new
+entry point, and checks the result against the regular path (gatspi_simulate)
+bit for bit -- twice in a row, since every call reuses the one scratch array.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _pack(net):
+    """The library's per-gate and per-edge descriptors (layout of gatspi_level_args)."""
+    G, E = net.num_gates, net.num_edges
+    n = net.type_num_pins[net.gate_type].astype(np.int64)
+    mask = np.zeros(G, np.int64)
+    for t in range(len(net.type_num_pins)):
+        nt = int(net.type_num_pins[t])
+        bits = sum(int(net.tt_data[net.type_tt_off[t] + k]) << k for k in range(1 << nt))
+        mask[net.gate_type == t] = bits
+    gd = np.zeros((G, 4), np.int64)
+    gd[:, 0] = net.fanin_off[:-1]
+    gd[:, 1] = n | (mask << 8)
+    gd[:, 2] = net.gate_dly_off & 0xFFFFFFFF
+    gd[:, 3] = net.gate_dly_off >> 32
+    ed = np.zeros((E, 4), np.int64)
+    ed[:, 0] = net.fanin_net
+    ed[:, 1] = net.pin_weight
+    ed[:, 2] = net.wire_rise.astype(np.int64) | (net.wire_fall.astype(np.int64) << 16)
+    return gd.astype(np.uint32).view(np.int32).ravel(), ed.astype(np.int32).ravel()
+
+
+class Caller:
+    """Owns every buffer; runs levels through the allocation-free entry point."""
+
+    def __init__(self, net, stim, pool_words, stage_words=-1):
+        import torch
+        from gate_level_logic_gb300 import gatspi
+        self.gatspi, self.torch = gatspi, torch
+        self.net, self.stim = net, stim
+        P, G, W = net.num_inputs, net.num_gates, stim.num_windows
+        self.N, self.W, self.nch = P + G, W, (W + 31) // 32
+        dev = torch.device("cuda", 0)
+        gd, ed = _pack(net)
+        self.gate_desc = torch.from_numpy(gd).to(dev)
+        self.edge_desc = torch.from_numpy(ed).to(dev)
+        self.dly = torch.from_numpy(np.ascontiguousarray(net.dly_data, np.int32)).to(dev)
+        self.window_len = torch.from_numpy(np.ascontiguousarray(stim.window_len, np.int32)).to(dev)
+        self.pool = torch.zeros(pool_words, dtype=torch.int32, device=dev)
+        self.chunk_base = torch.zeros(self.N * self.nch, dtype=torch.int64, device=dev)
+        self.wend = torch.zeros(self.N * W, dtype=torch.int32, device=dev)
+        self.tc = torch.zeros(G, dtype=torch.int64, device=dev)
+        self.t1 = torch.zeros(G, dtype=torch.int64, device=dev)
+        self.level_base = torch.zeros(2, dtype=torch.int64, device=dev)
+        self.stage_words = stage_words
+        # input waveforms at the front of the pool, with their window index
+        off = stim.pi_off
+        nw = int(off[-1])
+        self.pool[:nw] = torch.from_numpy(np.ascontiguousarray(stim.pi_words, np.int32)).to(dev)
+        k = np.arange(P * W)
+        first = k - (k % W) % 32                      # first window of each (input, chunk)
+        cb = off[first].reshape(P, W)[:, ::32]
+        self.chunk_base[:P * self.nch] = torch.from_numpy(np.ascontiguousarray(cb.ravel(), np.int64)).to(dev)
+        self.wend[:P * W] = torch.from_numpy((off[k + 1] - off[first]).astype(np.int32)).to(dev)
+        self.inputs_words = nw
+
+    def args(self, gate_begin, num_gates, pool_words=None):
+        g = self.gatspi
+        return g.gatspi_level_args(
+            self.gate_desc.data_ptr(), self.edge_desc.data_ptr(), self.dly.data_ptr(), self.window_len.data_ptr(),
+            self.pool.data_ptr(), self.pool.numel() if pool_words is None else pool_words,
+            self.chunk_base.data_ptr(), self.wend.data_ptr(), self.tc.data_ptr(), self.t1.data_ptr(),
+            self.level_base.data_ptr(), self.net.num_inputs, self.W, gate_begin, num_gates, self.stage_words)
+
+    def run(self):
+        """Every level, in order; returns (offsets, pool, tc, t1) as host arrays."""
+        torch, g = self.torch, self.gatspi
+        self.tc.zero_()
+        self.t1.zero_()
+        base = self.inputs_words
+        lo = self.net.level_offsets
+        stream = torch.cuda.current_stream().cuda_stream
+        for lvl in range(self.net.num_levels):
+            self.level_base[0] = base
+            g.gatspi_simulate_level_static(self.args(int(lo[lvl]), int(lo[lvl + 1] - lo[lvl])), stream)
+            base = int(self.level_base[1].item())
+        cb = self.chunk_base.cpu().numpy()
+        we = self.wend.cpu().numpy().astype(np.int64)
+        k = np.arange(self.N * self.W)
+        net_id, w = k // self.W, k % self.W
+        off = np.empty(self.N * self.W + 1, np.int64)
+        off[:-1] = cb[net_id * self.nch + w // 32] + np.where(w % 32 == 0, 0, we[np.maximum(k - 1, 0)])
+        off[-1] = base
+        return off, self.pool[:base].cpu().numpy(), self.tc.cpu().numpy(), self.t1.cpu().numpy()
+
+
+def _regular(net, stim, pool_words):
+    from gate_level_logic_gb300 import Simulator
+    with Simulator(net, stim.window_len, pool_words=pool_words) as sim:
+        sim.load(stim.pi_off, stim.pi_words)
+        sim.simulate()
+        tc, _, t1 = sim.toggle_stats()
+        return sim.export_offsets(), sim.pool_host(), tc, t1
+
+
+@pytest.fixture(scope="module")
+def built():
+    import torch
+    assert torch.cuda.is_available(), "needs a CUDA device"
+    torch.cuda.set_device(0)
+    from gate_level_logic_gb300 import build
+    build.build()
+
+
+@pytest.mark.parametrize("name", ["tiny", "50k"])
+def test_static_levels_match_regular_path(built, name):
+    net, stim = synth.make(name)
+    pool_words = 1 << 24
+    ref = _regular(net, stim, pool_words)
+    caller = Caller(net, stim, pool_words)
+    for attempt in range(2):                        # two runs in a row share the scratch
+        off, pool, tc, t1 = caller.run()
+        assert np.array_equal(off, ref[0]), "window offsets differ (run %d)" % attempt
+        assert np.array_equal(pool, ref[1]), "waveforms differ (run %d)" % attempt
+        assert np.array_equal(tc, ref[2]) and np.array_equal(t1, ref[3]), "statistics differ (run %d)" % attempt
+
+
+def test_static_errors_and_limits(built):
+    from gate_level_logic_gb300 import GatspiError, gatspi
+    net, stim = synth.make("tiny")
+    caller = Caller(net, stim, 1 << 20)
+    lo = net.level_offsets
+    # a pool too small for the first level: reported, and the next call starts clean
+    caller.level_base[0] = caller.inputs_words
+    with pytest.raises(GatspiError) as e:
+        gatspi.gatspi_simulate_level_static(caller.args(0, int(lo[1]), pool_words=caller.inputs_words + 8))
+    assert e.value.name == "GATSPI_EPOOL_OVERFLOW"
+    ref = _regular(net, stim, 1 << 20)
+    off, pool, tc, t1 = caller.run()
+    assert np.array_equal(pool, ref[1]) and np.array_equal(tc, ref[2])
+    # a level beyond the fixed scratch is refused before anything runs: with one
+    # window a tile holds 256 gates, so 2^25 gates need 131072 tiles (> 65536)
+    assert stim.num_windows == 1
+    big = caller.args(0, 1 << 25)
+    with pytest.raises(GatspiError) as e:
+        gatspi.gatspi_simulate_level_static(big)
+    assert e.value.name == "GATSPI_EINVAL"
+    assert ctypes.sizeof(gatspi.gatspi_level_args) > 0
