@@ -93,10 +93,10 @@ def workload_config(net, stim, stage_words):
     }
 
 
-def algorithmic_bytes(net, off, W):
-    """Per-level algorithmic bytes from the run's own output lengths."""
+def algorithmic_bytes(net, lengths, W):
+    """Per-level algorithmic bytes from the run's own waveform lengths."""
     P, G, L = net.num_inputs, net.num_gates, net.num_levels
-    lens = np.diff(off).reshape(P + G, W)
+    lens = np.asarray(lengths, np.int64).reshape(P + G, W)
     net_words = lens.sum(axis=1)
     nchunks = (W + 31) // 32
     idx_bytes_per_net = 4 * W + 8 * nchunks          # wend + chunk base
@@ -301,10 +301,11 @@ def run_gpu(args):
         sim.simulate(stream=stream)
     tc, t0, t1 = sim.toggle_stats()
     events_per_step = int(tc.sum())
-    off = sim.export_offsets()
-    lvl_bytes = algorithmic_bytes(net, off, W)
-    pool_used = int(off[-1])
-    del off
+    _, lengths = sim.export_offsets()
+    lvl_bytes = algorithmic_bytes(net, lengths, W)
+    waveform_words = int(lengths.sum())
+    pool_used = sim.pool_used()
+    del lengths
 
     # ---- timed region: device time, inputs resident ----------------------------
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -354,6 +355,7 @@ def run_gpu(args):
         "gate_cycles_per_s": gate_cycles_per_s,
         "events_per_step": events_per_step,
         "pool_words_used": pool_used,
+        "waveform_words": waveform_words,
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": traffic, "peak_source": peak_src,
@@ -384,7 +386,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--stage-words", type=int, default=-1)
-    ap.add_argument("--pool-gb", type=float, default=24.0)
+    ap.add_argument("--pool-gb", type=float, default=48.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--windows", type=int, default=0, help="profiling only: number of cycle windows")

@@ -326,11 +326,16 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
             ll.gate_begin = c->level_offsets[l];
             ll.num_gates = c->level_offsets[l + 1] - c->level_offsets[l];
             const long long slots = (long long)ll.num_gates * c->slots_per_gate;
-            const long long tiles = std::max<long long>(1, (slots + kBlock - 1) / kBlock);
-            if (tiles > INT32_MAX) return fail(GATSPI_EINVAL, "level %d has too many (gate, window) slots", l);
+            const long long tiles = std::max<long long>(1, (slots + kTileSlots - 1) / kTileSlots);
+            const long long items = (long long)ll.num_gates * c->nchunks;
+            const long long scan = std::max<long long>(1, (items + kTileSlots - 1) / kTileSlots);
+            if (tiles > INT32_MAX / kTileSlots || items > INT32_MAX)
+                return fail(GATSPI_EINVAL, "level %d has too many (gate, window) slots", l);
             ll.num_tiles = (int32_t)tiles;
+            ll.num_items = (int32_t)items;
+            ll.scan_tiles = (int32_t)scan;
             ll.tile_base = c->total_tiles;
-            c->total_tiles += tiles;
+            c->total_tiles += scan;
             c->launches.push_back(ll);
         }
 
@@ -488,25 +493,24 @@ gatspi_status gatspi_get_waveform(gatspi_ctx *c, int32_t net, int32_t window, in
     return GATSPI_OK;
 }
 
-gatspi_status gatspi_export_offsets(gatspi_ctx *c, int64_t *off, size_t n) {
+gatspi_status gatspi_export_offsets(gatspi_ctx *c, int64_t *start, int32_t *len, size_t n) {
     g_err.clear();
-    if (!c || !off) return fail(GATSPI_EINVAL, "ctx and off are required");
-    if ((long long)n != c->num_nets * c->W + 1) return fail(GATSPI_EINVAL, "off needs num_nets * W + 1 entries");
+    if (!c || (!start && !len)) return fail(GATSPI_EINVAL, "ctx and start or len are required");
+    if ((long long)n != c->num_nets * c->W) return fail(GATSPI_EINVAL, "the arrays need num_nets * W entries");
     if (!c->loaded || !c->simulated) return fail(GATSPI_ESTATE, "simulate first");
     gatspi_status st = sync_ctx(c);
     if (st != GATSPI_OK) return st;
     std::vector<long long> base((size_t)(c->num_nets * c->nchunks));
     std::vector<uint32_t> wend((size_t)(c->num_nets * c->W));
-    long long used = 0;
     CUDA_TRY(cudaMemcpy(base.data(), c->chunk_base, base.size() * sizeof(long long), cudaMemcpyDeviceToHost), "reading the window index");
     CUDA_TRY(cudaMemcpy(wend.data(), c->wend, wend.size() * sizeof(uint32_t), cudaMemcpyDeviceToHost), "reading the window index");
-    CUDA_TRY(cudaMemcpy(&used, c->level_base + c->L, sizeof used, cudaMemcpyDeviceToHost), "reading the pool size");
     for (long long net = 0; net < c->num_nets; ++net)
         for (int w = 0; w < c->W; ++w) {
             const long long k = net * c->W + w;
-            off[k] = base[net * c->nchunks + w / 32] + ((w % 32) ? wend[k - 1] : 0);
+            const uint32_t s0 = (w % 32) ? wend[k - 1] : 0u;
+            if (start) start[k] = base[net * c->nchunks + w / 32] + s0;
+            if (len) len[k] = (int32_t)(wend[k] - s0);
         }
-    off[c->num_nets * c->W] = used;
     return GATSPI_OK;
 }
 

@@ -9,8 +9,9 @@
 
 namespace gatspi {
 
-constexpr int kBlock = 256;               // threads per level-kernel block = (gate, window) slots per tile
+constexpr int kBlock = 256;               // threads per level-kernel block (8 independent warps)
 constexpr int kWarps = kBlock / 32;
+constexpr int kTileSlots = 32;            // (gate, window) slots per look-back tile = one warp
 constexpr int kMaxStage = 64;             // upper bound of stage_words
 constexpr int kDefaultStage = 24;
 constexpr int32_t kEOW = GATSPI_EOW;
@@ -41,7 +42,7 @@ struct DevParams {
     unsigned long long *tc;    // [G]
     unsigned long long *t1;    // [G]
     // scan state
-    unsigned long long *tile_status;  // [total tiles], zeroed per simulate
+    unsigned long long *tile_status;  // [total warp tiles], zeroed per simulate
     int32_t *tickets;                 // [L], zeroed per simulate
     long long *level_base;            // [L+1]; [0] = words of the input waveforms
     int32_t *status;                  // [kStatusWords]
@@ -58,13 +59,15 @@ struct LevelLaunch {
     int32_t level;
     int32_t gate_begin;
     int32_t num_gates;
-    int32_t num_tiles;
-    long long tile_base;
+    int32_t num_tiles;      // warps of the level kernel: ceil(gates * slots_per_gate / 32)
+    int32_t num_items;      // (gate, chunk) output regions of the level
+    int32_t scan_tiles;     // warps of the bounds scan: max(1, ceil(num_items / 32))
+    long long tile_base;    // first look-back word of this level's bounds scan
 };
 
 size_t level_smem_bytes(int stage);
 cudaError_t set_level_smem_limit(int stage);
-cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s);
+cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // bounds scan + level kernel
 cudaError_t launch_window_lengths(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,
                                   long long *len, cudaStream_t s);
 cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,

@@ -5,9 +5,9 @@
 // which owns the whole device memory through its own allocator, or code that is
 // not allowed to allocate once it has started.  gatspi_create allocates the
 // context's arrays; this entry point instead takes every input and output buffer
-// from the caller and keeps the only scratch the level kernel needs -- the
-// look-back flags of its tiles, the tile ticket and the status word -- in a
-// file-scope device array of fixed size.  Every GPU that loads the library holds
+// from the caller and keeps the only scratch the level's kernels need -- the
+// look-back flags of the output-region scan, its tile ticket and the status word
+// -- in a file-scope device array of fixed size.  Every GPU that loads the library holds
 // that array until the process exits.
 #include <cstdio>
 #include <mutex>
@@ -18,7 +18,7 @@ using namespace gatspi;
 
 namespace {
 
-constexpr int kStaticTiles = 1 << 16;                     // tiles of one level at most
+constexpr int kStaticTiles = 1 << 18;                     // scan tiles of one level at most
 constexpr int kTicketWord = kStaticTiles;                 // index of the ticket word
 constexpr int kStatusWord = kStaticTiles + 1;             // index of the status words (2 x 8 bytes)
 constexpr int kScratchWords = kStaticTiles + 4;
@@ -65,9 +65,11 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     while ((1 << p.lpg_log2) < lpg) ++p.lpg_log2;
     p.slots_per_gate = p.nchunks << p.lpg_log2;
     const long long slots = (long long)a->num_gates * p.slots_per_gate;
-    const long long tiles = slots > 0 ? (slots + kBlock - 1) / kBlock : 1;
-    if (tiles > kStaticTiles)
-        return err(GATSPI_EINVAL, "level too large for the static scratch (at most 65536 tiles of 256 slots)");
+    const long long tiles = slots > 0 ? (slots + kTileSlots - 1) / kTileSlots : 1;
+    const long long items = (long long)a->num_gates * p.nchunks;
+    const long long scan = items > 0 ? (items + kTileSlots - 1) / kTileSlots : 1;
+    if (scan > kStaticTiles)
+        return err(GATSPI_EINVAL, "level too large for the static scratch (at most 262144 x 32 (gate, chunk) regions)");
 
     // once per device, with that device current: the device address of the scratch
     int dev = 0;
@@ -111,13 +113,15 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     l.gate_begin = a->gate_begin;
     l.num_gates = a->num_gates;
     l.num_tiles = (int32_t)tiles;
+    l.num_items = (int32_t)items;
+    l.scan_tiles = (int32_t)scan;
     l.tile_base = 0;
 
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
     if (e == cudaSuccess) e = set_level_smem_limit(p.stage);
     // clear the flags of the tiles this call uses, the ticket and the status
-    if (e == cudaSuccess) e = cudaMemsetAsync(words, 0, sizeof(unsigned long long) * (size_t)tiles, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(words, 0, sizeof(unsigned long long) * (size_t)scan, s);
     if (e == cudaSuccess)
         e = cudaMemsetAsync(words + kTicketWord, 0, sizeof(unsigned long long) * (kScratchWords - kTicketWord), s);
     if (e == cudaSuccess) e = launch_level(p, l, s);

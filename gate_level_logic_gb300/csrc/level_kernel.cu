@@ -1,31 +1,36 @@
-// Level kernel of the GB300 gate-level re-simulator.
+// Level kernels of the GB300 gate-level re-simulator.
 //
-// One launch per logic level (GATSPI, Section 3, Fig. 5).  A block owns a tile of
-// 256 consecutive (gate, window) slots of the level; a warp holds one gate and 32
-// consecutive windows (or, for W < 32, several gates with W windows each), the
-// thread mapping the page chooses so that a warp's lanes run the same cell.
+// Two launches per logic level (GATSPI, Section 3, Fig. 5).
 //
+// level_bounds_kernel sizes the output region of every (gate, chunk of 32 windows)
+// of the level before anything is simulated.  An output window can hold at most
+// 3 + sum over pins of (input length - 2) words: every stored toggle needs an
+// iteration of the event loop and every iteration consumes at least one input
+// transition.  Summed over the chunk's windows this is the sum of the pins' source
+// spans (one window-index load per pin) plus (3 - 2n) per window.  The bounds are
+// scanned in (gate, chunk) order -- warp shuffles plus a decoupled look-back over
+// warp tiles; the work per item is a handful of loads, so the waits are short --
+// and give every region its pool offset.  The page sizes its outputs with a full
+// counting pass instead; the bound replaces that pass and leaves a gap after each
+// region (its size is the only cost).
+//
+// level_kernel simulates.  A warp owns 32 consecutive (gate, window) slots: one gate
+// and 32 consecutive windows (or, for W < 32, several gates with W windows each),
+// the thread mapping the page chooses so that a warp's lanes run the same cell.
 // Each lane runs Algorithm 1 of the page for its (gate, window): merge the fanin
 // waveforms with interconnect inertial filtering, resolve simultaneous switching,
 // look up the truth table by summed pin weights, pick the conditional delay (row =
 // switching pin and edges, column = the other pins' values) and apply the gate's
-// inertial filter (PATHPULSEPERCENT = 100).  The page runs this twice: a pass that
-// only counts output toggles (to size every output), a prefix sum over the counts,
-// and a pass that stores.  Here both passes share one kernel:
-//   1. every lane simulates once, keeping the first `stage` output words in shared
-//      memory ([word][lane] layout, bank-conflict free) and the toggle count, the
-//      time at 1 and the output length in registers;
-//   2. output lengths are scanned: warp shuffles, then the block's warps, then a
-//      decoupled look-back over earlier tiles of the level (tile order from an
-//      atomic ticket, so a block only ever waits for blocks that are running);
-//   3. lanes whose output fit store it from shared memory to the pool; lanes whose
-//      output was longer simulate a second time storing straight to the pool (the
-//      page's second pass, kept for them only);
-//   4. TC and T1 are reduced per gate with shuffles and one 64-bit atomic per
-//      (gate, chunk of 32 windows), and the window index of the level's nets is
-//      written.
+// inertial filter (PATHPULSEPERCENT = 100).  The lane keeps the first `stage`
+// output words in shared memory ([word][lane] layout, bank-conflict free); a warp
+// shuffle scan of the lengths places every window in its region, the staged words
+// are stored, and a lane whose output was longer simulates a second time storing
+// straight to the pool (the page's second pass, kept for those lanes only).  TC and
+// T1 are reduced per (gate, chunk) with shuffles and one 64-bit atomic each.  No
+// warp waits for another.
+//
 // No kernel traps: a malformed waveform, a missing delay arc, pool overflow or a
-// stalled look-back sets the device status word and the kernel carries on without
+// stalled look-back sets the device status word and the kernels carry on without
 // writing out of bounds.
 #include "gatspi_internal.cuh"
 
@@ -239,67 +244,121 @@ __device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, int 
     }
 }
 
-// Exclusive prefix of this tile within the level (decoupled look-back).  Called by
-// one thread.  Publishes the tile's aggregate, then its inclusive prefix.
-__device__ long long look_back(const DevParams &P, const LevelLaunch &L, int tile, long long total) {
+// Exclusive prefix of this warp's tile within the level (decoupled look-back over
+// warp tiles).  All 32 lanes take part: each probe reads the look-back words of 32
+// predecessors at once, closest first, and stops at the first inclusive prefix.
+// Publishes the tile's aggregate before looking back and its inclusive prefix
+// after.  Waits are bounded: a stalled predecessor raises GATSPI_ETIMEOUT.
+__device__ long long look_back(const DevParams &P, const LevelLaunch &L, int tile, long long total, int lane) {
     unsigned long long *st = P.tile_status + L.tile_base;
     if (tile == 0) {
-        st_relaxed(st, kFlagIncl | (unsigned long long)total);
+        if (lane == 0) st_relaxed(st, kFlagIncl | (unsigned long long)total);
         return 0;
     }
-    st_relaxed(st + tile, kFlagAgg | (unsigned long long)total);
+    if (lane == 0) st_relaxed(st + tile, kFlagAgg | (unsigned long long)total);
     long long excl = 0;
     int k = tile - 1;
     const unsigned long long t0 = global_ns();
     unsigned sleep = 32;
     for (;;) {
-        const unsigned long long v = ld_relaxed(st + k);
-        if ((v >> 62) == 0) {
-            if (ld_status(P.status) != 0) break;                 // another block failed: stop waiting
-            if (global_ns() - t0 > kSpinLimitNs) {
-                raise_error(P.status, GATSPI_ETIMEOUT, L.level, tile, k);
-                break;
+        const int idx = k - lane;
+        unsigned long long v = idx >= 0 ? ld_relaxed(st + idx) : kFlagIncl;
+        const unsigned incl = __ballot_sync(0xffffffffu, (v >> 62) == 2);
+        const unsigned busy = __ballot_sync(0xffffffffu, (v >> 62) == 0);
+        const unsigned need = incl ? ((incl & (0u - incl)) << 1) - 1u : 0xffffffffu;  // lanes up to the first inclusive
+        if (busy & need) {
+            bool stop = false;
+            if (lane == 0) {
+                if (ld_status(P.status) != 0) {
+                    stop = true;                                       // another warp failed: stop waiting
+                } else if (global_ns() - t0 > kSpinLimitNs) {
+                    raise_error(P.status, GATSPI_ETIMEOUT, L.level, tile, k);
+                    stop = true;
+                }
             }
+            if (__shfl_sync(0xffffffffu, (int)stop, 0)) break;
             __nanosleep(sleep);
             if (sleep < 1024) sleep <<= 1;
             continue;
         }
-        excl += (long long)(v & kValueMask);
-        if ((v >> 62) == 2) break;
-        --k;
+        long long part = (need >> lane) & 1u ? (long long)(v & kValueMask) : 0;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        excl += part;
+        if (incl) break;
+        k -= 32;
     }
-    st_relaxed(st + tile, kFlagIncl | (unsigned long long)(excl + total));
+    if (lane == 0) st_relaxed(st + tile, kFlagIncl | (unsigned long long)(excl + total));
     return excl;
 }
 
+// Output region of every (gate, chunk) of the level: bound, scan, chunk_base.
+__global__ void __launch_bounds__(kBlock) level_bounds_kernel(const DevParams P, const LevelLaunch L) {
+    const int lane = threadIdx.x & 31;
+    int tile = 0;
+    if (lane == 0) tile = atomicAdd(P.tickets + L.level, 1);
+    tile = __shfl_sync(0xffffffffu, tile, 0);
+    if (tile >= L.scan_tiles) return;                      // spare warps of the last block
+    const bool skip = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
+    const int item = tile * 32 + lane;
+    const bool valid = !skip && item < L.num_items;
+    int g = 0, c = 0;
+    long long bound = 0;
+    if (valid) {
+        const int gl = item / P.nchunks;
+        c = item - gl * P.nchunks;
+        g = L.gate_begin + gl;
+        const int4 gd = __ldg(P.gate_desc + g);
+        const int n = gd.y & 7;
+        const int w_last = min(c * 32 + 31, P.W - 1);
+        bound = (long long)(w_last - c * 32 + 1) * (3 - 2 * n);
+        for (int i = 0; i < n; ++i) {
+            const long long src = __ldg(P.edge_desc + gd.x + i).x;
+            bound += __ldg(P.wend + src * P.W + w_last);      // span of the source's chunk
+        }
+    }
+    long long incl = bound;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const long long total = __shfl_sync(0xffffffffu, incl, 31);
+    const long long base = P.level_base[L.level] + look_back(P, L, tile, total, lane);
+    if (lane == 0 && tile == L.scan_tiles - 1) {
+        P.level_base[L.level + 1] = base + total;
+        if (base + total > P.pool_words) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, 0, 0);
+    }
+    if (valid) P.chunk_base[((long long)P.num_inputs + g) * P.nchunks + c] = base + incl - bound;
+}
+
+// One warp = 32 consecutive (gate, window) slots of the level.  Warps share nothing
+// but the shared-memory allocation of their block and never wait for each other.
 __global__ void __launch_bounds__(kBlock, 4) level_kernel(const DevParams P, const LevelLaunch L) {
     extern __shared__ int32_t smem[];
-    __shared__ int s_tile;
-    __shared__ int s_skip;
-    __shared__ uint32_t s_warp[kWarps];
-    __shared__ long long s_out0;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int tile = blockIdx.x * kWarps + warp;
+    if (tile >= L.num_tiles) return;                       // spare warps of the last block
+    const bool skip = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
 
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    if (tid == 0) {
-        s_tile = atomicAdd(P.tickets + L.level, 1);
-        s_skip = ld_status(P.status) != 0;   // an earlier level failed: publish empty tiles only
+    // slot -> (gate, chunk, window): W >= 32 gives one (gate, chunk) per warp,
+    // W < 32 gives 32 >> lpg_log2 gates of lpg lanes each
+    int gl, c, j;
+    if (P.lpg_log2 == 5) {
+        gl = tile / P.nchunks;
+        c = tile - gl * P.nchunks;
+        j = lane;
+    } else {
+        const int slot = tile * 32 + lane;
+        gl = slot >> P.lpg_log2;
+        c = 0;
+        j = slot & ((1 << P.lpg_log2) - 1);
     }
-    __syncthreads();
-    const int tile = s_tile;
-    const bool skip = s_skip != 0;
-
-    // slot -> (gate, chunk, window)
-    const long long slot = (long long)tile * kBlock + tid;
-    const long long gl = slot / P.slots_per_gate;
-    const int r = (int)(slot - gl * P.slots_per_gate);
-    const int c = r >> P.lpg_log2;
-    const int j = r & ((1 << P.lpg_log2) - 1);
     const int w = c * 32 + j;
     const bool gate_ok = !skip && gl < L.num_gates;
     const bool valid = gate_ok && w < P.W;
-    const int g = L.gate_begin + (int)gl;
+    const int g = L.gate_begin + gl;
 
     int32_t *stage = smem + warp * (P.stage * 32) + lane;
     LaneResult res{0, 0, 0, 0};
@@ -316,7 +375,7 @@ __global__ void __launch_bounds__(kBlock, 4) level_kernel(const DevParams P, con
     }
     const bool overflow = valid && res.len > P.stage;
 
-    // warp scan of the output lengths
+    // warp scan of the output lengths; a segment (gate, chunk) starts at its leader
     uint32_t incl = (uint32_t)res.len;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -324,7 +383,7 @@ __global__ void __launch_bounds__(kBlock, 4) level_kernel(const DevParams P, con
         if (lane >= o) incl += v;
     }
     const uint32_t excl = incl - (uint32_t)res.len;
-    if (lane == 31) s_warp[warp] = incl;
+    const uint32_t lead_excl = __shfl_sync(0xffffffffu, excl, lane & ~((1 << P.lpg_log2) - 1));
 
     // TC and T1 per (gate, chunk): reduce over the segment's lanes, one atomic each
     long long tcs = res.tc, t1s = res.t1;
@@ -336,31 +395,11 @@ __global__ void __launch_bounds__(kBlock, 4) level_kernel(const DevParams P, con
         atomicAdd(P.tc + g, (unsigned long long)tcs);
         atomicAdd(P.t1 + g, (unsigned long long)t1s);
     }
-    __syncthreads();
 
-    if (tid == 0) {
-        long long total = 0;
-        for (int k = 0; k < kWarps; ++k) {
-            const uint32_t v = s_warp[k];
-            s_warp[k] = (uint32_t)total;
-            total += v;
-        }
-        const long long prefix = look_back(P, L, tile, total);
-        long long out0 = P.level_base[L.level] + prefix;
-        if (tile == L.num_tiles - 1) P.level_base[L.level + 1] = out0 + total;
-        if (out0 + total > P.pool_words) {
-            raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, tile, 0);
-            out0 = -1;
-        }
-        s_out0 = out0;
-    }
-    __syncthreads();
-    const long long out0 = s_out0;
-    const long long my_off = out0 + s_warp[warp] + excl;
-    const uint32_t lead_excl = __shfl_sync(0xffffffffu, excl, lane & ~((1 << P.lpg_log2) - 1));
-
-    if (valid && out0 >= 0) {
+    if (valid) {
         const long long net = (long long)P.num_inputs + g;
+        const uint32_t rel = excl - lead_excl;              // offset of this window in its region
+        const long long my_off = __ldg(P.chunk_base + net * P.nchunks + c) + rel;
         if (!overflow) {
             int32_t *dst = P.pool + my_off;
             for (int k = 0; k < res.len; ++k) dst[k] = stage[k * 32];
@@ -368,8 +407,7 @@ __global__ void __launch_bounds__(kBlock, 4) level_kernel(const DevParams P, con
             const LaneResult again = dispatch<true>(P, gd, c, w, Lw, nullptr, P.pool + my_off);
             if (again.len != res.len) raise_error(P.status, GATSPI_EBADWAVE, g, w, 1);
         }
-        P.wend[net * P.W + w] = excl + (uint32_t)res.len - lead_excl;
-        if (j == 0) P.chunk_base[net * P.nchunks + c] = out0 + s_warp[warp] + lead_excl;
+        P.wend[net * P.W + w] = rel + (uint32_t)res.len;
     }
 }
 
@@ -459,8 +497,13 @@ cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const i
 size_t level_smem_bytes(int stage) { return (size_t)kWarps * 32 * (size_t)stage * sizeof(int32_t); }
 
 cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
+    const unsigned scan_blocks = (unsigned)((l.scan_tiles + kWarps - 1) / kWarps);
+    level_bounds_kernel<<<scan_blocks, kBlock, 0, s>>>(p, l);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     const size_t smem = level_smem_bytes(p.stage);
-    level_kernel<<<l.num_tiles, kBlock, smem, s>>>(p, l);
+    const unsigned blocks = (unsigned)((l.num_tiles + kWarps - 1) / kWarps);
+    level_kernel<<<blocks, kBlock, smem, s>>>(p, l);
     return cudaGetLastError();
 }
 

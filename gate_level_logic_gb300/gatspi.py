@@ -70,7 +70,7 @@ SIGNATURES = {
     "gatspi_toggle_stats": (ctypes.c_int, [_p, _p, _p, _p]),
     "gatspi_get_waveform": (ctypes.c_int, [_p, ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_size_t,
                                            ctypes.POINTER(ctypes.c_size_t)]),
-    "gatspi_export_offsets": (ctypes.c_int, [_p, _p, ctypes.c_size_t]),
+    "gatspi_export_offsets": (ctypes.c_int, [_p, _p, _p, ctypes.c_size_t]),
     "gatspi_export_windows": (ctypes.c_int, [_p, _p, ctypes.c_int32, _p, _p, ctypes.c_size_t]),
     "gatspi_device_views": (ctypes.c_int, [_p, ctypes.POINTER(gatspi_views)]),
     "gatspi_level_times": (ctypes.c_int, [_p, _p, ctypes.c_int32]),
@@ -141,8 +141,8 @@ def gatspi_get_waveform(ctx: int, net: int, window: int, buf: int, cap: int) -> 
     return n.value
 
 
-def gatspi_export_offsets(ctx: int, off: int, n: int):
-    _check(library().gatspi_export_offsets(_p(ctx), _p(off), n))
+def gatspi_export_offsets(ctx: int, start: int, length: int, n: int):
+    _check(library().gatspi_export_offsets(_p(ctx), _p(start), _p(length), n))
 
 
 def gatspi_export_windows(ctx: int, windows: int, nsel: int, off: int, words: int, cap: int):

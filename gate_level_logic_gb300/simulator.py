@@ -126,10 +126,18 @@ class Simulator:
         _c.gatspi_get_waveform(self.ctx, net, window, buf.ctypes.data, buf.size)
         return buf[:n]
 
-    def export_offsets(self) -> np.ndarray:
-        off = np.zeros(self.num_nets * self.num_windows + 1, np.int64)
-        _c.gatspi_export_offsets(self.ctx, off.ctypes.data, off.size)
-        return off
+    def export_offsets(self):
+        """(start, length) of every (net, window) waveform in the pool, net-major."""
+        n = self.num_nets * self.num_windows
+        start = np.zeros(max(n, 1), np.int64)
+        length = np.zeros(max(n, 1), np.int32)
+        _c.gatspi_export_offsets(self.ctx, start.ctypes.data, length.ctypes.data, n)
+        return start[:n], length[:n]
+
+    def export_all(self):
+        """(off, words): every (net, window) waveform gathered gap-free, net-major and
+        window-minor, as CSR."""
+        return self.export_windows(np.arange(self.num_windows))
 
     def export_windows(self, windows):
         """(off, words) CSR of the waveforms of the given windows for every net,

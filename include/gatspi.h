@@ -146,12 +146,15 @@ typedef struct gatspi_ctx gatspi_ctx;
 /*
  * Device views of the simulation state (valid until gatspi_destroy).
  *
- * The pool holds every (net, window) waveform, net-major and window-minor, without
- * gaps: first the input waveforms as loaded, then the gates' outputs level by level.
- * Windows are grouped in chunks of 32 (one chunk when W <= 32): waveform (net, w)
- * starts at pool[chunk_base[net * num_chunks + w / 32] + start] and ends (EOW
- * included) at pool[chunk_base[...] + wend[net * W + w]], where start = 0 for the
- * first window of a chunk and wend[net * W + w - 1] otherwise.
+ * Windows are grouped in chunks of 32 (one chunk when W <= 32).  The pool holds
+ * first the input waveforms as loaded, then the gates' outputs level by level; a
+ * level holds one region per (gate, chunk), in (gate, chunk) order, sized by an upper
+ * bound of its output (see gatspi_simulate) and filled from its start with the
+ * chunk's windows in order, so a gap may follow a region.  Waveform (net, w) starts
+ * at pool[chunk_base[net * num_chunks + w / 32] + start] and ends (EOW included) at
+ * pool[chunk_base[...] + wend[net * W + w]], where start = 0 for the first window of
+ * a chunk and wend[net * W + w - 1] otherwise.  The layout depends only on the
+ * inputs: every run gives the same pool.
  */
 typedef struct {
     const int32_t *pool;
@@ -195,10 +198,13 @@ gatspi_status gatspi_load_waveforms(gatspi_ctx *ctx, const int64_t *off, const i
 /*
  * Re-simulate every level, in order, on `stream` (a cudaStream_t; NULL = legacy
  * default stream).  Asynchronous: returns after enqueueing.  Clears TC/T1 and the
- * device status first.  Per level one kernel runs Algorithm 1 for every
- * (gate, window) of the level, scans the output lengths into pool offsets and
- * stores the output waveforms and window index; TC and T1 are reduced per gate in
- * the same kernel.  The level sequence is captured once into a CUDA graph and
+ * device status first.  Per level two kernels run: the first sizes the output
+ * region of every (gate, chunk) by an upper bound (an output window holds at most
+ * 3 + the sum over its pins of (input length - 2) words, since each stored toggle
+ * takes an event-loop iteration and each iteration consumes an input transition)
+ * and scans the bounds into pool offsets, in place of the page's counting pass;
+ * the second runs Algorithm 1 for every (gate, window) of the level and stores the
+ * output waveforms, the window index and TC/T1 per gate.  The level sequence is captured once into a CUDA graph and
  * replayed by later calls, unless GATSPI_FLAG_NO_GRAPH or GATSPI_FLAG_LEVEL_TIMING
  * is set (then the level kernels are launched directly on `stream`).
  */
@@ -223,11 +229,12 @@ gatspi_status gatspi_get_waveform(gatspi_ctx *ctx, int32_t net, int32_t window, 
                                   size_t *len);
 
 /*
- * Write CSR offsets of every (net, window) waveform, net-major and window-minor, to
- * host memory: off[k] .. off[k+1] delimit waveform k = net * W + w in the pool
- * (n = num_nets * W + 1 entries).  Synchronises first.
+ * Write the pool position and length (EOW included) of every (net, window)
+ * waveform, net-major and window-minor, to host memory: waveform k = net * W + w
+ * occupies pool[start[k] .. start[k] + len[k]) (n = num_nets * W entries; either
+ * array may be NULL).  Synchronises first.
  */
-gatspi_status gatspi_export_offsets(gatspi_ctx *ctx, int64_t *off, size_t n);
+gatspi_status gatspi_export_offsets(gatspi_ctx *ctx, int64_t *start, int32_t *len, size_t n);
 
 /*
  * Export the waveforms of selected windows for every net, as CSR in host memory:
@@ -293,13 +300,15 @@ typedef struct {
  * memory -- code running under a framework that owns all of the device memory
  * through its own allocator, or code that must not allocate once it has started.
  * The caller passes every input and output buffer (gatspi_level_args); the only
- * scratch, the look-back flags, tile ticket and status word of the level kernel,
- * lives in a file-scope device array of 65536 tile flags plus 32 bytes (about
- * 512 KiB) that every GPU which loads the library holds until the process exits.
+ * scratch, the look-back flags of the output-region scan, its tile ticket and the
+ * status word, lives in a file-scope device array of 262144 tile flags plus 32
+ * bytes (about 2 MiB) that every GPU which loads the library holds until the
+ * process exits.
  *
  *   - No cudaMalloc, cudaFree or allocating library call is made.
- *   - A level may have at most 65536 tiles of 256 (gate, window) slots; a larger
- *     level returns GATSPI_EINVAL before anything runs.
+ *   - A level may have at most 262144 x 32 = 8388608 (gate, chunk) regions (a
+ *     gate has ceil(W / 32) of them); a larger level returns GATSPI_EINVAL before
+ *     anything runs.  The caller also makes sure the gates exist.
  *   - The first call on a device looks up the device address of the scratch array
  *     (with that device current); make that first call before any stream capture.
  *   - Every call shares the one array and clears the part it uses before its

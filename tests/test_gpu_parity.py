@@ -32,12 +32,14 @@ def gpu():
 
 
 def run_gpu(Simulator, net, stim, pool_words, stage_words=-1, flags=0, repeat=1):
+    """Simulate; return every waveform gathered gap-free (CSR, net-major) + statistics."""
     with Simulator(net, stim.window_len, pool_words=pool_words, stage_words=stage_words, flags=flags) as sim:
         sim.load(stim.pi_off, stim.pi_words)
         for _ in range(repeat):
             sim.simulate()
         tc, t0, t1 = sim.toggle_stats()
-        return dict(off=sim.export_offsets(), pool=sim.pool_host(), tc=tc, t0=t0, t1=t1)
+        off, words = sim.export_all()
+        return dict(off=off, pool=words, tc=tc, t0=t0, t1=t1)
 
 
 def assert_same(got, ref, what=""):
@@ -50,20 +52,27 @@ def assert_same(got, ref, what=""):
     assert np.array_equal(got["t0"], ref.t0), "T0 differs " + what
 
 
-def pool_for(ref, slack=1.05):
-    return int(ref.pool.size * slack) + 4096
+def pool_for(ref, net=None):
+    """Pool words the output regions need: inputs plus, per gate and chunk, the sum of
+    its pins' source spans plus 3 words per window (the kernel's upper bound)."""
+    P, G, W = ref.num_inputs, len(ref.tc), ref.num_windows
+    net_words = np.diff(ref.off).reshape(P + G, W).sum(axis=1)
+    if net is None:
+        return int(4 * ref.pool.size) + 4096
+    inputs = int(net_words[:P].sum())
+    return inputs + int(net_words[net.fanin_net].sum()) + 3 * G * W + 4096
 
 
 def test_tiny_full(gpu, oracle_lib):
     net, stim = synth.make("tiny")
     ref = oracle_lib.simulate(net, stim)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref)), ref)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref)
 
 
 def test_50k_full(gpu, oracle_lib):
     net, stim = synth.make("50k")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref)), ref)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref)
 
 
 @pytest.mark.parametrize("stage_words,flags", [(0, 0), (1, 0), (3, 0), (8, 0), (64, 0), (24, 2)])
@@ -71,7 +80,7 @@ def test_50k_staging_and_launch_variants(gpu, oracle_lib, stage_words, flags):
     """stage 0 is the count-then-write scheme for every lane; other sizes mix both."""
     net, stim = synth.make("50k")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref), stage_words=stage_words, flags=flags), ref,
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=stage_words, flags=flags), ref,
                 "stage=%d flags=%d" % (stage_words, flags))
 
 
@@ -83,7 +92,7 @@ def test_window_counts(gpu, oracle_lib, W):
     stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=37, cycles=max(W, 300), period=500,
                                                       activity=0.2, windows=W, seed=W, glitch_frac=0.2))
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref), stage_words=8), ref, "W=%d" % W)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=8), ref, "W=%d" % W)
 
 
 def test_random_small_netlists(gpu, oracle_lib):
@@ -93,7 +102,7 @@ def test_random_small_netlists(gpu, oracle_lib):
     for seed in range(120):
         net, stim = pins._random_case(seed)
         ref = oracle_lib.simulate(net, stim)
-        assert_same(run_gpu(gpu, net, stim, pool_for(ref), stage_words=(0, 2, 24)[seed % 3]), ref,
+        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=(0, 2, 24)[seed % 3]), ref,
                     "seed %d" % seed)
 
 
@@ -108,7 +117,7 @@ def test_quiet_inputs_and_empty_level(gpu, oracle_lib):
     for waves in ([[0, EOW], [-1, 0, EOW]], [[0, 5, 9, 40, EOW], [-1, 0, 20, EOW]]):
         stim = synth.from_waveforms([[w] for w in waves], 100)
         ref = oracle_lib.simulate(net, stim)
-        assert_same(run_gpu(gpu, net, stim, pool_for(ref)), ref)
+        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref)
 
 
 def test_maximum_activity(gpu, oracle_lib):
@@ -117,13 +126,13 @@ def test_maximum_activity(gpu, oracle_lib):
     stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=64, cycles=256, period=200, activity=1.0,
                                                       windows=64, seed=5, glitch_frac=0.5, glitch_span=(1, 4)))
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref), stage_words=16), ref)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=16), ref)
 
 
 def test_replay_is_deterministic(gpu, oracle_lib):
     net, stim = synth.make("50k")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref), repeat=3), ref, "after 3 replays")
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), repeat=3), ref, "after 3 replays")
 
 
 def test_errors_leave_context_usable(gpu, oracle_lib):
@@ -131,7 +140,7 @@ def test_errors_leave_context_usable(gpu, oracle_lib):
     net, stim = synth.make("tiny")
     ref = oracle_lib.simulate(net, stim)
     # pool too small for the outputs: reported at the next synchronising call; a quiet
-    # stimulus needs at most 3 words per gate output and fits
+    # stimulus needs regions of 3 words per gate and window and fits
     small = int(stim.pi_words.size) + 3 * net.num_gates + 64
     assert small < ref.pool.size
     with gpu(net, stim.window_len, pool_words=small) as sim:
@@ -150,7 +159,7 @@ def test_errors_leave_context_usable(gpu, oracle_lib):
         tc, _, _ = sim.toggle_stats()
         assert (tc == 0).all()
     # malformed input waveforms are rejected at load
-    with gpu(net, stim.window_len, pool_words=pool_for(ref)) as sim:
+    with gpu(net, stim.window_len, pool_words=pool_for(ref, net)) as sim:
         bad = stim.pi_words.copy()
         bad[stim.pi_off[3] + 2] = bad[stim.pi_off[3] + 1]       # repeated timestamp
         with pytest.raises(GatspiError) as e:
@@ -175,7 +184,7 @@ def test_errors_leave_context_usable(gpu, oracle_lib):
 def test_single_waveform_and_window_export(gpu, oracle_lib):
     net, stim = synth.make("50k")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    with gpu(net, stim.window_len, pool_words=pool_for(ref)) as sim:
+    with gpu(net, stim.window_len, pool_words=pool_for(ref, net)) as sim:
         sim.load(stim.pi_off, stim.pi_words)
         sim.simulate()
         for net_id, w in [(0, 0), (255, 15), (256, 3), (net.num_inputs + net.num_gates - 1, 15), (30000, 7)]:
@@ -191,7 +200,7 @@ def test_1M_full(gpu, oracle_lib):
     """The configuration bench.py times: 1M gates, 40 levels, 256 windows; whole pool."""
     net, stim = synth.make("1M")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref)), ref, "1M")
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref, "1M")
 
 
 def _sampled(gpu, oracle_lib, net, stim, windows, pool_words):
@@ -214,13 +223,13 @@ def _sampled(gpu, oracle_lib, net, stim, windows, pool_words):
 @pytest.mark.slow
 def test_5M_sampled(gpu, oracle_lib):
     net, stim = synth.make("5M")
-    _sampled(gpu, oracle_lib, net, stim, [0, 77, 127], pool_words=60 << 28)
+    _sampled(gpu, oracle_lib, net, stim, [0, 77, 127], pool_words=36 << 30)
 
 
 @pytest.mark.slow
 def test_scan500k_sampled(gpu, oracle_lib):
     net, stim = synth.make("scan500k")
-    _sampled(gpu, oracle_lib, net, stim, [0, 131, 255], pool_words=48 << 28)
+    _sampled(gpu, oracle_lib, net, stim, [0, 131, 255], pool_words=24 << 30)
 
 
 @pytest.mark.slow
@@ -228,4 +237,4 @@ def test_scan500k_sampled(gpu, oracle_lib):
 def test_1M_sweep_points_sampled(gpu, oracle_lib, activity, W):
     net, stim = synth.sweep(activity, W)
     windows = [0] if W == 1 else [0, W // 2 + 1, W - 1]
-    _sampled(gpu, oracle_lib, net, stim, windows, pool_words=120 << 28)
+    _sampled(gpu, oracle_lib, net, stim, windows, pool_words=40 << 30)

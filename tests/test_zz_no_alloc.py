@@ -98,10 +98,10 @@ class Caller:
         we = self.wend.cpu().numpy().astype(np.int64)
         k = np.arange(self.N * self.W)
         net_id, w = k // self.W, k % self.W
-        off = np.empty(self.N * self.W + 1, np.int64)
-        off[:-1] = cb[net_id * self.nch + w // 32] + np.where(w % 32 == 0, 0, we[np.maximum(k - 1, 0)])
-        off[-1] = base
-        return off, self.pool[:base].cpu().numpy(), self.tc.cpu().numpy(), self.t1.cpu().numpy()
+        first = np.where(w % 32 == 0, 0, we[np.maximum(k - 1, 0)])
+        start = cb[net_id * self.nch + w // 32] + first
+        length = we - first
+        return (start, length, base), self.pool[:base].cpu().numpy(), self.tc.cpu().numpy(), self.t1.cpu().numpy()
 
 
 def _regular(net, stim, pool_words):
@@ -110,7 +110,22 @@ def _regular(net, stim, pool_words):
         sim.load(stim.pi_off, stim.pi_words)
         sim.simulate()
         tc, _, t1 = sim.toggle_stats()
-        return sim.export_offsets(), sim.pool_host(), tc, t1
+        start, length = sim.export_offsets()
+        used = sim.pool_used()
+        return (start, length, used), sim.pool_host(), tc, t1
+
+
+def _same_index(a, b):
+    return np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and a[2] == b[2]
+
+
+def _gather(pool, index):
+    """Every waveform's words, in (net, window) order (the gaps between output regions
+    hold whatever the buffer held before and are not compared)."""
+    start, length = np.asarray(index[0], np.int64), np.asarray(index[1], np.int64)
+    first = np.concatenate(([0], np.cumsum(length)[:-1]))
+    pos = np.repeat(start - first, length) + np.arange(int(length.sum()))
+    return pool[pos]
 
 
 @pytest.fixture(scope="module")
@@ -129,9 +144,9 @@ def test_static_levels_match_regular_path(built, name):
     ref = _regular(net, stim, pool_words)
     caller = Caller(net, stim, pool_words)
     for attempt in range(2):                        # two runs in a row share the scratch
-        off, pool, tc, t1 = caller.run()
-        assert np.array_equal(off, ref[0]), "window offsets differ (run %d)" % attempt
-        assert np.array_equal(pool, ref[1]), "waveforms differ (run %d)" % attempt
+        index, pool, tc, t1 = caller.run()
+        assert _same_index(index, ref[0]), "waveform positions differ (run %d)" % attempt
+        assert np.array_equal(_gather(pool, index), _gather(ref[1], ref[0])), "waveforms differ (run %d)" % attempt
         assert np.array_equal(tc, ref[2]) and np.array_equal(t1, ref[3]), "statistics differ (run %d)" % attempt
 
 
@@ -146,10 +161,11 @@ def test_static_errors_and_limits(built):
         gatspi.gatspi_simulate_level_static(caller.args(0, int(lo[1]), pool_words=caller.inputs_words + 8))
     assert e.value.name == "GATSPI_EPOOL_OVERFLOW"
     ref = _regular(net, stim, 1 << 20)
-    off, pool, tc, t1 = caller.run()
-    assert np.array_equal(pool, ref[1]) and np.array_equal(tc, ref[2])
+    index, pool, tc, t1 = caller.run()
+    assert _same_index(index, ref[0]) and np.array_equal(tc, ref[2])
+    assert np.array_equal(_gather(pool, index), _gather(ref[1], ref[0]))
     # a level beyond the fixed scratch is refused before anything runs: with one
-    # window a tile holds 256 gates, so 2^25 gates need 131072 tiles (> 65536)
+    # window every gate is one output region, and 2^25 regions > 262144 x 32
     assert stim.num_windows == 1
     big = caller.args(0, 1 << 25)
     with pytest.raises(GatspiError) as e:
