@@ -308,8 +308,16 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         for (long long g = 0; g < c->G; ++g) {
             const int t = nl->gate_type[g];
             const int n = nl->type_num_pins[t];
+            // truth table re-indexed by the pin values (first pin most significant):
+            // entry v is the page's entry at the sum of the weights of the pins at 1
             uint32_t mask = 0;
-            for (int k = 0; k < (1 << n); ++k) mask |= (uint32_t)nl->tt_data[nl->type_tt_off[t] + k] << k;
+            const long long e0 = nl->fanin_off[g];
+            for (int v = 0; v < (1 << n); ++v) {
+                int k = 0;
+                for (int i = 0; i < n; ++i)
+                    if ((v >> (n - 1 - i)) & 1) k += nl->pin_weight[e0 + i];
+                mask |= (uint32_t)nl->tt_data[nl->type_tt_off[t] + k] << v;
+            }
             const long long d0 = nl->gate_dly_off[g];
             gd[g] = make_int4(nl->fanin_off[g], (int)(n | (mask << 8)), (int)(uint32_t)(d0 & 0xffffffffll),
                               (int)(d0 >> 32));

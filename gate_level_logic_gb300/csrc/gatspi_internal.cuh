@@ -9,8 +9,10 @@
 
 namespace gatspi {
 
-constexpr int kBlock = 256;               // threads per level-kernel block (8 independent warps)
+constexpr int kBlock = 256;               // threads per block of the light kernels
 constexpr int kWarps = kBlock / 32;
+constexpr int kLevelWarps = 2;            // warps per level-kernel block (independent warps)
+constexpr int kLevelBlock = 32 * kLevelWarps;
 constexpr int kTileSlots = 32;            // (gate, window) slots per look-back tile = one warp
 constexpr int kMaxStage = 64;             // upper bound of stage_words
 constexpr int kDefaultStage = 24;
@@ -29,8 +31,9 @@ constexpr int kStatusWords = 4;
 // Everything a level kernel reads or writes, by value in the kernel parameters.
 struct DevParams {
     // netlist
-    const int4 *gate_desc;     // [G] x = first edge, y = n | truth-table mask << 8, z/w = delay-table offset lo/hi
-    const int4 *edge_desc;     // [E] x = source net, y = truth-table weight, z = wire rise | wire fall << 16
+    const int4 *gate_desc;     // [G] x = first edge, y = n | truth table << 8, z/w = delay-table offset lo/hi;
+                               //     truth-table bit k = output for pin values k (first pin most significant)
+    const int4 *edge_desc;     // [E] x = source net, y = truth-table weight (unused here), z = wire rise | fall << 16
     const int32_t *dly_data;   // per-instance conditional delay tables
     // waveform store
     int32_t *pool;

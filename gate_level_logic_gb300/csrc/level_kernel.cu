@@ -75,7 +75,6 @@ struct Pin {
     int32_t p;         // index of the entry in effect (value = p & 1)
     int32_t a;         // arrival time of the next transition at the pin, or EOW
     uint32_t drf;      // interconnect delays: rise | fall << 16
-    uint32_t wbit;     // truth-table weight
 };
 
 // Next arrival of a pin: skip every pulse narrower than the interconnect delay of
@@ -108,12 +107,46 @@ struct LaneResult {
     int32_t err;   // 0 or a gatspi_status
 };
 
+// Delay of the arc of switching pin i (its new value is in vbits) to output edge
+// e_out: row = 4*i + 2*e_in + e_out, column = the other pins' values, first pin most
+// significant (vbits holds pin i at bit N-1-i).
+template <int N>
+__device__ __forceinline__ int32_t arc_delay(const int32_t *__restrict__ D, uint32_t vbits, int i, int e_out) {
+    constexpr int kCols = 1 << (N - 1);
+    const int b = N - 1 - i;
+    const int e_in = ((vbits >> b) & 1u) ? 0 : 1;
+    const uint32_t col = ((vbits >> (b + 1)) << b) | (vbits & ((1u << b) - 1u));
+    return __ldg(D + (4 * i + 2 * e_in + e_out) * kCols + col);
+}
+
+// Advance pin k, chosen per lane: its state is gathered and written back with
+// predicated moves so that the lanes of a warp advance different pins together.
+template <int N>
+__device__ __forceinline__ bool advance_pin(Pin (&pin)[N], int k) {
+    if (N == 1) return next_arrival(pin[0]);
+    Pin s = pin[0];
+#pragma unroll
+    for (int q = 1; q < N; ++q)
+        if (k == q) s = pin[q];
+    const bool ok = next_arrival(s);
+#pragma unroll
+    for (int q = 0; q < N; ++q)
+        if (k == q) {
+            pin[q].p = s.p;
+            pin[q].a = s.a;
+        }
+    return ok;
+}
+
 // Algorithm 1 for one (gate, window).  kGlobal = false: the first `stage` output
 // words go to shared memory (stride 32); kGlobal = true: every word goes to gout.
+// The loop body is written so that a warp's lanes stay together: the switching
+// pins form a bit mask, the delay lookup and the pin advance serve the first
+// switching pin through a lane-selected pin state, and only simultaneous
+// switching of several pins takes an extra (rare) loop.
 template <int N, bool kGlobal>
 __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const int32_t *__restrict__ D, int32_t Lw,
                                                int32_t *stage, int stage_words, int32_t *__restrict__ gout) {
-    constexpr int kCols = 1 << (N - 1);
     LaneResult r{0, 0, 0, 0};
     auto put = [&](int32_t k, int32_t v) {
         if (kGlobal) {
@@ -123,17 +156,16 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
         }
     };
 
-    // initial values: pin index 1 when the waveform starts with -1
-    uint32_t vbits = 0, idx = 0;
+    // initial values: pin index 1 when the waveform starts with -1.  The truth table
+    // was re-indexed at create by the pin weights, so its index is the pin values
+    // read as a binary number, first pin most significant.
+    uint32_t vbits = 0;
 #pragma unroll
     for (int i = 0; i < N; ++i) {
         pin[i].p = (__ldg(pin[i].w) == -1) ? 1 : 0;
-        if (pin[i].p) {
-            vbits |= 1u << (N - 1 - i);
-            idx |= pin[i].wbit;
-        }
+        vbits |= (uint32_t)pin[i].p << (N - 1 - i);
     }
-    const int32_t y0 = (tt >> idx) & 1;
+    const int32_t y0 = (tt >> vbits) & 1;
     int32_t po = y0;        // index of the last output entry
     int32_t top = 0;        // O[po]
     int32_t second = 0;     // O[po - 1] (read only after a store)
@@ -151,31 +183,24 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
         for (int i = 1; i < N; ++i) t = min(t, pin[i].a);
         if (t == kEOW) break;
 
-        // every pin arriving at t switches together
-        uint32_t sw = 0;
+        // every pin arriving at t switches together (bit N-1-i = pin i)
+        uint32_t swb = 0;
 #pragma unroll
         for (int i = 0; i < N; ++i) {
-            if (pin[i].a == t) {
-                pin[i].p += 1;
-                vbits ^= 1u << (N - 1 - i);
-                idx ^= pin[i].wbit;
-                sw |= 1u << i;
-            }
+            const uint32_t hit = pin[i].a == t ? 1u : 0u;
+            swb |= hit << (N - 1 - i);
+            pin[i].p += (int32_t)hit;
         }
-        const int32_t y = (tt >> idx) & 1;
+        vbits ^= swb;
+        const int hb = 31 - __clz(swb);
+        const int k = N - 1 - hb;                       // first switching pin
+        const uint32_t more = swb & ~(1u << hb);        // any others (simultaneous switching)
+        const int32_t y = (tt >> vbits) & 1;
         if (y != (po & 1)) {
             // smallest finite conditional delay among the switching pins
             const int e_out = y ? 0 : 1;
-            int32_t d = kNoArc;
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-                if (sw & (1u << i)) {
-                    const int e_in = (pin[i].p & 1) ? 0 : 1;
-                    const uint32_t lo = vbits & ((1u << (N - 1 - i)) - 1u);
-                    const uint32_t col = ((vbits >> (N - i)) << (N - 1 - i)) | lo;
-                    d = min(d, __ldg(D + (4 * i + 2 * e_in + e_out) * kCols + col));
-                }
-            }
+            int32_t d = arc_delay<N>(D, vbits, k, e_out);
+            for (uint32_t m = more; m; m &= m - 1u) d = min(d, arc_delay<N>(D, vbits, N - __ffs(m), e_out));
             if (d == kNoArc) {
                 r.err = GATSPI_EBADLUT;
                 break;
@@ -194,9 +219,8 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
                 top = to;
             }
         }
-#pragma unroll
-        for (int i = 0; i < N; ++i)
-            if (sw & (1u << i)) ok &= next_arrival(pin[i]);
+        ok &= advance_pin<N>(pin, k);
+        for (uint32_t m = more; m; m &= m - 1u) ok &= advance_pin<N>(pin, N - __ffs(m));   // lowest bit first
     }
     if (!ok) r.err = GATSPI_EBADWAVE;
     put(po + 1, kEOW);
@@ -218,7 +242,6 @@ __device__ __forceinline__ void load_pins(const DevParams &P, int first_edge, in
         const uint32_t start = (w & 31) ? __ldg(P.wend + src * P.W + w - 1) : 0u;
         pin[i].w = P.pool + base + start;
         pin[i].len = (int32_t)(end - start);
-        pin[i].wbit = (uint32_t)e.y;
         pin[i].drf = (uint32_t)e.z;
     }
 }
@@ -334,11 +357,11 @@ __global__ void __launch_bounds__(kBlock) level_bounds_kernel(const DevParams P,
 
 // One warp = 32 consecutive (gate, window) slots of the level.  Warps share nothing
 // but the shared-memory allocation of their block and never wait for each other.
-__global__ void __launch_bounds__(kBlock, 4) level_kernel(const DevParams P, const LevelLaunch L) {
+__global__ void __launch_bounds__(kLevelBlock, 32 / kLevelWarps) level_kernel(const DevParams P, const LevelLaunch L) {
     extern __shared__ int32_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int tile = blockIdx.x * kWarps + warp;
+    const int tile = blockIdx.x * kLevelWarps + warp;
     if (tile >= L.num_tiles) return;                       // spare warps of the last block
     const bool skip = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
 
@@ -494,7 +517,7 @@ cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const i
     return cudaGetLastError();
 }
 
-size_t level_smem_bytes(int stage) { return (size_t)kWarps * 32 * (size_t)stage * sizeof(int32_t); }
+size_t level_smem_bytes(int stage) { return (size_t)kLevelWarps * 32 * (size_t)stage * sizeof(int32_t); }
 
 cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
     const unsigned scan_blocks = (unsigned)((l.scan_tiles + kWarps - 1) / kWarps);
@@ -502,8 +525,8 @@ cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t smem = level_smem_bytes(p.stage);
-    const unsigned blocks = (unsigned)((l.num_tiles + kWarps - 1) / kWarps);
-    level_kernel<<<blocks, kBlock, smem, s>>>(p, l);
+    const unsigned blocks = (unsigned)((l.num_tiles + kLevelWarps - 1) / kLevelWarps);
+    level_kernel<<<blocks, kLevelBlock, smem, s>>>(p, l);
     return cudaGetLastError();
 }
 

@@ -262,10 +262,13 @@ gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *ms, int32_t n);
  * Buffers of one logic level for gatspi_simulate_level_static (all device memory,
  * owned by the caller).  The layouts are the library's own:
  *   gate_desc   int32 [4 * num_gates of the netlist], 16-byte aligned; for gate g:
- *               {first edge of g, n | truth-table bits << 8 (bit k = entry k),
- *                low and high 32 bits of the delay-table offset}
+ *               {first edge of g, n | truth-table bits << 8, low and high 32 bits
+ *               of the delay-table offset}; truth-table bit v is the output when the
+ *               pin values, read as a binary number with the first pin most
+ *               significant, equal v (the page's table re-indexed by pin weight)
  *   edge_desc   int32 [4 * edges], 16-byte aligned; for edge e:
- *               {driving net, truth-table weight, wire rise | wire fall << 16, 0}
+ *               {driving net, truth-table weight (not read), wire rise | wire fall
+ *               << 16, 0}
  *   dly_data    the delay tables of gatspi_netlist
  *   window_len  int32 [num_windows]
  *   pool, chunk_base, wend

@@ -46,3 +46,33 @@ def uniform_delays(n, rise, fall, tt=None):
         ok = synth.possible_rows(tt, n)
         D[~ok, :] = INF
     return D.astype(np.int32)
+
+
+def permute_pin_weights(net, seed):
+    """The same circuit with every gate's truth-table pin weights permuted at random
+    and its truth table re-indexed to match (one cell type per gate)."""
+    rng = np.random.default_rng(seed)
+    G = net.num_gates
+    tts, names, pins, weights = [], [], [], []
+    for g in range(G):
+        t = int(net.gate_type[g])
+        n = int(net.type_num_pins[t])
+        tt = net.tt_data[net.type_tt_off[t]:net.type_tt_off[t] + (1 << n)]
+        wt = [1 << b for b in rng.permutation(n)]
+        new = np.zeros(1 << n, np.uint8)
+        for v in range(1 << n):                 # v: pin values, first pin most significant
+            old_k = sum(((v >> (n - 1 - i)) & 1) << (n - 1 - i) for i in range(n))
+            new_k = sum(((v >> (n - 1 - i)) & 1) * wt[i] for i in range(n))
+            new[new_k] = tt[old_k]
+        tts.append(new)
+        names.append("%s_%d" % (net.type_names[t], g))
+        pins.append(n)
+        weights.extend(wt)
+    out = synth.Netlist(
+        num_inputs=net.num_inputs, num_gates=G, num_levels=net.num_levels, level_offsets=net.level_offsets,
+        type_names=names, type_num_pins=np.array(pins, np.int32),
+        type_tt_off=np.concatenate(([0], np.cumsum([len(t) for t in tts])[:-1])).astype(np.int32),
+        tt_data=np.concatenate(tts).astype(np.uint8), gate_type=np.arange(G, dtype=np.int32),
+        fanin_off=net.fanin_off, fanin_net=net.fanin_net, pin_weight=np.array(weights, np.int32),
+        wire_rise=net.wire_rise, wire_fall=net.wire_fall, gate_dly_off=net.gate_dly_off, dly_data=net.dly_data)
+    return out

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import synth
-from helpers import EOW, INF, single_gate, uniform_delays
+from helpers import EOW, INF, permute_pin_weights, single_gate, uniform_delays
 
 pytestmark = pytest.mark.gpu
 
@@ -104,6 +104,35 @@ def test_random_small_netlists(gpu, oracle_lib):
         ref = oracle_lib.simulate(net, stim)
         assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=(0, 2, 24)[seed % 3]), ref,
                     "seed %d" % seed)
+
+
+def test_permuted_pin_weights(gpu, oracle_lib):
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=2000, num_inputs=40, num_levels=8, seed=21,
+                                                   cond_fraction=0.4))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=40, cycles=200, period=300, activity=0.3,
+                                                      windows=40, seed=21, glitch_frac=0.2))
+    perm = permute_pin_weights(net, seed=21)
+    ref = oracle_lib.simulate(perm, stim, threads=THREADS)
+    assert_same(run_gpu(gpu, perm, stim, pool_for(ref, perm)), ref, "permuted weights")
+    assert np.array_equal(ref.pool, oracle_lib.simulate(net, stim, threads=THREADS).pool)
+
+
+def test_simultaneous_switching_of_all_pins(gpu, oracle_lib):
+    """Every pin of a gate driven by one source with equal wire delays: 2, 3 and 4
+    pins switch at the same instant (the smallest-arc rule and the pin advance of
+    every switching pin)."""
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=3000, num_inputs=32, num_levels=10, seed=31,
+                                                   cond_fraction=0.5))
+    fo = net.fanin_off
+    first = np.repeat(net.fanin_net[fo[:-1]], np.diff(fo))
+    rise = np.repeat(net.wire_rise[fo[:-1]], np.diff(fo))
+    fall = np.repeat(net.wire_fall[fo[:-1]], np.diff(fo))
+    net.fanin_net, net.wire_rise, net.wire_fall = first.astype(np.int32), rise, fall
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=32, cycles=300, period=200, activity=0.4,
+                                                      windows=50, seed=31, glitch_frac=0.3, glitch_span=(1, 5)))
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    for stage in (0, 24):
+        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=stage), ref, "stage %d" % stage)
 
 
 def test_quiet_inputs_and_empty_level(gpu, oracle_lib):

@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 
 import synth
-from helpers import EOW, changes, single_gate, uniform_delays, value_at
+from helpers import EOW, changes, permute_pin_weights, single_gate, uniform_delays, value_at
 from synth.netlist import NetlistSpec, generate_netlist
 from synth.stimulus import StimulusSpec, generate_stimulus
 
@@ -252,3 +252,14 @@ def test_threads_do_not_change_results(oracle_lib):
     b = oracle_lib.simulate(net, stim, threads=5)
     assert np.array_equal(a.off, b.off) and np.array_equal(a.pool, b.pool)
     assert np.array_equal(a.tc, b.tc) and np.array_equal(a.t1, b.t1)
+
+
+def test_pin_weights_are_data(oracle_lib):
+    """Permuting every gate's truth-table pin weights, with the table re-indexed to the
+    same function, changes nothing (Fig. 4: weights come from the translator)."""
+    net, stim = synth.make("tiny")
+    perm = permute_pin_weights(net, seed=3)
+    assert not np.array_equal(perm.pin_weight, net.pin_weight)
+    a = oracle_lib.simulate(net, stim)
+    b = oracle_lib.simulate(perm, stim)
+    assert np.array_equal(a.pool, b.pool) and np.array_equal(a.tc, b.tc) and np.array_equal(a.t1, b.t1)

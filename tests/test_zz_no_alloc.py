@@ -140,7 +140,7 @@ def built():
 @pytest.mark.parametrize("name", ["tiny", "50k"])
 def test_static_levels_match_regular_path(built, name):
     net, stim = synth.make(name)
-    pool_words = 1 << 24
+    pool_words = 1 << 26            # room for the bound-sized output regions of every level
     ref = _regular(net, stim, pool_words)
     caller = Caller(net, stim, pool_words)
     for attempt in range(2):                        # two runs in a row share the scratch
