@@ -11,8 +11,15 @@ namespace gatspi {
 
 constexpr int kBlock = 256;               // threads per block of the light kernels
 constexpr int kWarps = kBlock / 32;
-constexpr int kLevelWarps = 2;            // warps per level-kernel block (independent warps)
+#ifndef GATSPI_LEVEL_WARPS
+#define GATSPI_LEVEL_WARPS 4
+#endif
+#ifndef GATSPI_LEVEL_MIN_BLOCKS
+#define GATSPI_LEVEL_MIN_BLOCKS (32 / GATSPI_LEVEL_WARPS)
+#endif
+constexpr int kLevelWarps = GATSPI_LEVEL_WARPS;   // warps per level-kernel block (independent warps)
 constexpr int kLevelBlock = 32 * kLevelWarps;
+constexpr int kLevelMinBlocks = GATSPI_LEVEL_MIN_BLOCKS;  // resident blocks per SM the registers must allow
 constexpr int kTileSlots = 32;            // (gate, window) slots per look-back tile = one warp
 constexpr int kMaxStage = 64;             // upper bound of stage_words
 constexpr int kDefaultStage = 24;

@@ -21,13 +21,15 @@
 // waveforms with interconnect inertial filtering, resolve simultaneous switching,
 // look up the truth table by summed pin weights, pick the conditional delay (row =
 // switching pin and edges, column = the other pins' values) and apply the gate's
-// inertial filter (PATHPULSEPERCENT = 100).  The lane keeps the first `stage`
-// output words in shared memory ([word][lane] layout, bank-conflict free); a warp
-// shuffle scan of the lengths places every window in its region, the staged words
-// are stored, and a lane whose output was longer simulates a second time storing
-// straight to the pool (the page's second pass, kept for those lanes only).  TC and
-// T1 are reduced per (gate, chunk) with shuffles and one 64-bit atomic each.  No
-// warp waits for another.
+// inertial filter (PATHPULSEPERCENT = 100).  Before simulating, each lane turns its
+// inputs' lengths into its window's own bound and a warp scan gives the window a
+// provisional slot in the region.  The lane keeps the first `stage` output words in
+// shared memory ([word][lane] layout, bank-conflict free) and writes any further
+// word straight to its provisional slot.  A warp scan of the actual lengths then
+// places every window; spilled words are moved down to their final place and the
+// staged words are stored.  Every (gate, window) is simulated once.  TC and T1 are
+// reduced per (gate, chunk) with shuffles and one 64-bit atomic each.  No warp waits
+// for another.
 //
 // No kernel traps: a malformed waveform, a missing delay arc, pool overflow or a
 // stalled look-back sets the device status word and the kernels carry on without
@@ -138,22 +140,22 @@ __device__ __forceinline__ bool advance_pin(Pin (&pin)[N], int k) {
     return ok;
 }
 
-// Algorithm 1 for one (gate, window).  kGlobal = false: the first `stage` output
-// words go to shared memory (stride 32); kGlobal = true: every word goes to gout.
+// Algorithm 1 for one (gate, window).  The first `stage_words` output words go to
+// shared memory (stride 32), the rest to gout, the window's provisional slot in the
+// pool.
 // The loop body is written so that a warp's lanes stay together: the switching
 // pins form a bit mask, the delay lookup and the pin advance serve the first
 // switching pin through a lane-selected pin state, and only simultaneous
 // switching of several pins takes an extra (rare) loop.
-template <int N, bool kGlobal>
+template <int N>
 __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const int32_t *__restrict__ D, int32_t Lw,
                                                int32_t *stage, int stage_words, int32_t *__restrict__ gout) {
     LaneResult r{0, 0, 0, 0};
     auto put = [&](int32_t k, int32_t v) {
-        if (kGlobal) {
-            gout[k] = v;
-        } else if (k < stage_words) {
+        if (k < stage_words)
             stage[k * 32] = v;
-        }
+        else
+            gout[k] = v;
     };
 
     // initial values: pin index 1 when the waveform starts with -1.  The truth table
@@ -246,25 +248,34 @@ __device__ __forceinline__ void load_pins(const DevParams &P, int first_edge, in
     }
 }
 
-template <int N, bool kGlobal>
+template <int N>
 __device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd, int c, int w, int32_t Lw,
                                                  int32_t *stage, int32_t *gout) {
     Pin pin[N];
     load_pins<N>(P, gd.x, c, w, pin);
     const uint32_t tt = (uint32_t)gd.y >> 8;
     const long long dly = (long long)(uint32_t)gd.z | ((long long)gd.w << 32);
-    return run_lane<N, kGlobal>(pin, tt, P.dly_data + dly, Lw, stage, P.stage, gout);
+    return run_lane<N>(pin, tt, P.dly_data + dly, Lw, stage, P.stage, gout);
 }
 
-template <bool kGlobal>
 __device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, int c, int w, int32_t Lw, int32_t *stage,
                                                int32_t *gout) {
     switch (gd.y & 7) {
-        case 1: return simulate_gate<1, kGlobal>(P, gd, c, w, Lw, stage, gout);
-        case 2: return simulate_gate<2, kGlobal>(P, gd, c, w, Lw, stage, gout);
-        case 3: return simulate_gate<3, kGlobal>(P, gd, c, w, Lw, stage, gout);
-        default: return simulate_gate<4, kGlobal>(P, gd, c, w, Lw, stage, gout);
+        case 1: return simulate_gate<1>(P, gd, c, w, Lw, stage, gout);
+        case 2: return simulate_gate<2>(P, gd, c, w, Lw, stage, gout);
+        case 3: return simulate_gate<3>(P, gd, c, w, Lw, stage, gout);
+        default: return simulate_gate<4>(P, gd, c, w, Lw, stage, gout);
     }
+}
+
+// Inclusive warp scan.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += v;
+    }
+    return x;
 }
 
 // Exclusive prefix of this warp's tile within the level (decoupled look-back over
@@ -357,7 +368,7 @@ __global__ void __launch_bounds__(kBlock) level_bounds_kernel(const DevParams P,
 
 // One warp = 32 consecutive (gate, window) slots of the level.  Warps share nothing
 // but the shared-memory allocation of their block and never wait for each other.
-__global__ void __launch_bounds__(kLevelBlock, 32 / kLevelWarps) level_kernel(const DevParams P, const LevelLaunch L) {
+__global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(const DevParams P, const LevelLaunch L) {
     extern __shared__ int32_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -384,29 +395,47 @@ __global__ void __launch_bounds__(kLevelBlock, 32 / kLevelWarps) level_kernel(co
     const int g = L.gate_begin + gl;
 
     int32_t *stage = smem + warp * (P.stage * 32) + lane;
-    LaneResult res{0, 0, 0, 0};
+    const int seg_lead = lane & ~((1 << P.lpg_log2) - 1);  // first lane of this (gate, chunk) segment
+    const long long net = (long long)P.num_inputs + g;
+
+    // Provisional slot of this window inside its (gate, chunk) region: the window's
+    // own bound, 3 + sum over pins of (input length - 2), scanned over the segment.
+    // These bounds add up to the region the bounds kernel reserved.
     int4 gd = make_int4(0, 0, 0, 0);
     int32_t Lw = 0;
+    uint32_t bound = 0;
+    long long base = 0;
     if (valid) {
         gd = __ldg(P.gate_desc + g);
         Lw = __ldg(P.window_len + w);
-        res = dispatch<false>(P, gd, c, w, Lw, stage, nullptr);
+        const int n = gd.y & 7;
+        bound = 3u - 2u * (uint32_t)n;
+        for (int i = 0; i < n; ++i) {
+            const long long src = __ldg(P.edge_desc + gd.x + i).x;
+            const uint32_t end = __ldg(P.wend + src * P.W + w);
+            const uint32_t start = (w & 31) ? __ldg(P.wend + src * P.W + w - 1) : 0u;
+            bound += end - start;
+        }
+        base = __ldg(P.chunk_base + net * P.nchunks + c);
+    }
+    const uint32_t bincl = warp_incl_scan(bound, lane);
+    const uint32_t bexcl = bincl - bound;
+    const long long prov = base + (bexcl - __shfl_sync(0xffffffffu, bexcl, seg_lead));
+
+    LaneResult res{0, 0, 0, 0};
+    if (valid) {
+        res = dispatch(P, gd, c, w, Lw, stage, P.pool + prov);
         if (res.err) {
             raise_error(P.status, res.err, g, w, 0);
             res.len = 0;
         }
     }
-    const bool overflow = valid && res.len > P.stage;
 
-    // warp scan of the output lengths; a segment (gate, chunk) starts at its leader
-    uint32_t incl = (uint32_t)res.len;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
+    // final place: scan of the actual lengths over the segment
+    const uint32_t incl = warp_incl_scan((uint32_t)res.len, lane);
     const uint32_t excl = incl - (uint32_t)res.len;
-    const uint32_t lead_excl = __shfl_sync(0xffffffffu, excl, lane & ~((1 << P.lpg_log2) - 1));
+    const uint32_t rel = excl - __shfl_sync(0xffffffffu, excl, seg_lead);
+    const long long fin = base + rel;
 
     // TC and T1 per (gate, chunk): reduce over the segment's lanes, one atomic each
     long long tcs = res.tc, t1s = res.t1;
@@ -419,17 +448,39 @@ __global__ void __launch_bounds__(kLevelBlock, 32 / kLevelWarps) level_kernel(co
         atomicAdd(P.t1 + g, (unsigned long long)t1s);
     }
 
-    if (valid) {
-        const long long net = (long long)P.num_inputs + g;
-        const uint32_t rel = excl - lead_excl;              // offset of this window in its region
-        const long long my_off = __ldg(P.chunk_base + net * P.nchunks + c) + rel;
-        if (!overflow) {
-            int32_t *dst = P.pool + my_off;
-            for (int k = 0; k < res.len; ++k) dst[k] = stage[k * 32];
-        } else {
-            const LaneResult again = dispatch<true>(P, gd, c, w, Lw, nullptr, P.pool + my_off);
-            if (again.len != res.len) raise_error(P.status, GATSPI_EBADWAVE, g, w, 1);
+    // Words that did not fit on chip sit at their provisional place; move them to the
+    // final one, one window at a time in lane order, the whole warp copying upward in
+    // steps of 32 words.  A final position never exceeds its provisional one, and the
+    // final range of a window ends before the provisional words of any later window
+    // begin, so in sequential order no copy overwrites a word still to be read.  The
+    // lanes of a warp are not ordered in memory without a barrier, though: a later
+    // step's store could land before another lane's earlier-step load of the same
+    // word, hence the __syncwarp between every step's loads and its stores.
+    unsigned spilled = __ballot_sync(0xffffffffu, valid && res.len > P.stage);
+    if (spilled) {
+        __syncwarp();
+        while (spilled) {
+            const int src_lane = __ffs(spilled) - 1;
+            spilled &= spilled - 1u;
+            const long long from = __shfl_sync(0xffffffffu, prov, src_lane) + P.stage;
+            const long long to = __shfl_sync(0xffffffffu, fin, src_lane) + P.stage;
+            const int count = __shfl_sync(0xffffffffu, res.len, src_lane) - P.stage;
+            if (from == to) continue;                       // warp-uniform
+            for (int q0 = 0; q0 < count; q0 += 32) {        // warp-uniform trip count
+                const int q = q0 + lane;
+                int32_t v = 0;
+                if (q < count) v = P.pool[from + q];
+                __syncwarp();
+                if (q < count) P.pool[to + q] = v;
+            }
+            __syncwarp();
         }
+    }
+
+    if (valid) {
+        int32_t *dst = P.pool + fin;
+        const int kept = min(res.len, P.stage);
+        for (int k = 0; k < kept; ++k) dst[k] = stage[k * 32];
         P.wend[net * P.W + w] = rel + (uint32_t)res.len;
     }
 }

@@ -13,8 +13,8 @@
  *   - Section 3, Algorithm 1: per (gate, window) the merge of the fanin waveforms,
  *     interconnect inertial filtering, multiple-simultaneous-input-switching
  *     resolution, delay selection and gate inertial filtering with
- *     PATHPULSEPERCENT = 100, and the output toggle count (TC) that sizes the
- *     output before it is stored (the two-pass scheme).
+ *     PATHPULSEPERCENT = 100.  The page sizes every output with a first counting
+ *     pass; here an upper bound computed from the input lengths takes its place.
  *
  * Conventions for every call:
  *   - every call returns a gatspi_status; nothing throws across this ABI, nothing
@@ -128,11 +128,12 @@ typedef struct {
  *   num_windows   W >= 1 independent cycle windows
  *   window_len    host array [W] of window lengths in time units (1 .. 2^30)
  *   flags         GATSPI_FLAG_*
- *   stage_words   output words a thread keeps on chip while it simulates (0 .. 64);
- *                 -1 selects the library default.  A (gate, window) whose output
- *                 waveform is longer is simulated a second time once its output
- *                 offset is known, storing straight to the pool; 0 makes every
- *                 (gate, window) take that second pass (the count-then-write scheme).
+ *   stage_words   output words a thread keeps in shared memory while it simulates
+ *                 (0 .. 64); -1 selects the library default.  Words beyond them are
+ *                 written to the window's provisional slot in its output region (a
+ *                 slot as long as the window's own bound) and moved to their final
+ *                 place once the lengths of the chunk's windows are known; every
+ *                 (gate, window) is simulated exactly once whatever the value.
  */
 typedef struct {
     int32_t num_windows;
