@@ -84,16 +84,20 @@ struct Pin {
 // the arrival is the next timestamp plus that delay.  False on a malformed wave.
 __device__ __forceinline__ bool next_arrival(Pin &s) {
     for (;;) {
-        const int32_t d = (s.p & 1) ? (int32_t)(s.drf >> 16) : (int32_t)(s.drf & 0xffffu);
-        if (s.p + 1 >= s.len) return false;
-        const int32_t t1 = __ldg(s.w + s.p + 1);
-        if (t1 == kEOW) {
+        // p + 1 == len - 1 is the EOW slot: no further transition
+        if (s.p + 2 >= s.len) {
             s.a = kEOW;
-            return true;
+            return s.p + 2 == s.len;
         }
-        if (s.p + 2 >= s.len) return false;
+        // both words are inside the waveform: load them together
+        const int32_t t1 = __ldg(s.w + s.p + 1);
         const int32_t t2 = __ldg(s.w + s.p + 2);
-        if (t2 - t1 < d) {  // the pulse [t1, t2) never reaches the pin
+        if (t1 == kEOW) {                // EOW before the last slot: malformed
+            s.a = kEOW;
+            return false;
+        }
+        const int32_t d = (s.p & 1) ? (int32_t)(s.drf >> 16) : (int32_t)(s.drf & 0xffffu);
+        if (t2 - t1 < d) {               // the pulse [t1, t2) never reaches the pin
             s.p += 2;
             continue;
         }
