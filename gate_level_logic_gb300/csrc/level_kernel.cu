@@ -236,39 +236,24 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
     return r;
 }
 
-// Pins of gate `g` in window `w` (chunk c): source waveforms from the window index.
 template <int N>
-__device__ __forceinline__ void load_pins(const DevParams &P, int first_edge, int c, int w, Pin (&pin)[N]) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const int4 e = __ldg(P.edge_desc + first_edge + i);
-        const long long src = e.x;
-        const long long base = __ldg(P.chunk_base + src * P.nchunks + c);
-        const uint32_t end = __ldg(P.wend + src * P.W + w);
-        const uint32_t start = (w & 31) ? __ldg(P.wend + src * P.W + w - 1) : 0u;
-        pin[i].w = P.pool + base + start;
-        pin[i].len = (int32_t)(end - start);
-        pin[i].drf = (uint32_t)e.z;
-    }
-}
-
-template <int N>
-__device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd, int c, int w, int32_t Lw,
-                                                 int32_t *stage, int32_t *gout) {
+__device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS],
+                                                 int32_t Lw, int32_t *stage, int32_t *gout) {
     Pin pin[N];
-    load_pins<N>(P, gd.x, c, w, pin);
+#pragma unroll
+    for (int i = 0; i < N; ++i) pin[i] = pins[i];
     const uint32_t tt = (uint32_t)gd.y >> 8;
     const long long dly = (long long)(uint32_t)gd.z | ((long long)gd.w << 32);
     return run_lane<N>(pin, tt, P.dly_data + dly, Lw, stage, P.stage, gout);
 }
 
-__device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, int c, int w, int32_t Lw, int32_t *stage,
-                                               int32_t *gout) {
+__device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS], int32_t Lw,
+                                               int32_t *stage, int32_t *gout) {
     switch (gd.y & 7) {
-        case 1: return simulate_gate<1>(P, gd, c, w, Lw, stage, gout);
-        case 2: return simulate_gate<2>(P, gd, c, w, Lw, stage, gout);
-        case 3: return simulate_gate<3>(P, gd, c, w, Lw, stage, gout);
-        default: return simulate_gate<4>(P, gd, c, w, Lw, stage, gout);
+        case 1: return simulate_gate<1>(P, gd, pins, Lw, stage, gout);
+        case 2: return simulate_gate<2>(P, gd, pins, Lw, stage, gout);
+        case 3: return simulate_gate<3>(P, gd, pins, Lw, stage, gout);
+        default: return simulate_gate<4>(P, gd, pins, Lw, stage, gout);
     }
 }
 
@@ -405,20 +390,29 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     // Provisional slot of this window inside its (gate, chunk) region: the window's
     // own bound, 3 + sum over pins of (input length - 2), scanned over the segment.
     // These bounds add up to the region the bounds kernel reserved.
+    // Pins of the gate in window w: source waveforms from the window index.
     int4 gd = make_int4(0, 0, 0, 0);
     int32_t Lw = 0;
     uint32_t bound = 0;
     long long base = 0;
+    Pin pins[GATSPI_MAX_PINS];
     if (valid) {
         gd = __ldg(P.gate_desc + g);
         Lw = __ldg(P.window_len + w);
         const int n = gd.y & 7;
         bound = 3u - 2u * (uint32_t)n;
-        for (int i = 0; i < n; ++i) {
-            const long long src = __ldg(P.edge_desc + gd.x + i).x;
-            const uint32_t end = __ldg(P.wend + src * P.W + w);
-            const uint32_t start = (w & 31) ? __ldg(P.wend + src * P.W + w - 1) : 0u;
-            bound += end - start;
+#pragma unroll
+        for (int i = 0; i < GATSPI_MAX_PINS; ++i) {
+            if (i < n) {
+                const int4 e = __ldg(P.edge_desc + gd.x + i);
+                const long long src = e.x;
+                const uint32_t end = __ldg(P.wend + src * P.W + w);
+                const uint32_t start = (w & 31) ? __ldg(P.wend + src * P.W + w - 1) : 0u;
+                pins[i].w = P.pool + __ldg(P.chunk_base + src * P.nchunks + c) + start;
+                pins[i].len = (int32_t)(end - start);
+                pins[i].drf = (uint32_t)e.z;
+                bound += end - start;
+            }
         }
         base = __ldg(P.chunk_base + net * P.nchunks + c);
     }
@@ -428,7 +422,7 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
 
     LaneResult res{0, 0, 0, 0};
     if (valid) {
-        res = dispatch(P, gd, c, w, Lw, stage, P.pool + prov);
+        res = dispatch(P, gd, pins, Lw, stage, P.pool + prov);
         if (res.err) {
             raise_error(P.status, res.err, g, w, 0);
             res.len = 0;
