@@ -310,7 +310,8 @@ def run_gpu(args):
     # ---- timed region: device time, inputs resident ----------------------------
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    level_ms = np.zeros(net.num_levels, np.float64)
+    level_ms = np.zeros(net.num_levels, np.float64)      # simulation kernel of every level
+    bounds_ms = np.zeros(net.num_levels, np.float64)     # output-region kernel of every level
     _barrier(dist)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
@@ -319,7 +320,9 @@ def run_gpu(args):
             sim.simulate(stream=stream)
             ends[k].record(stream)
             sim.sync()
-            level_ms += sim.level_times()
+            lt, bt = sim.level_times()
+            level_ms += lt
+            bounds_ms += bt
         torch.cuda.synchronize()
     _barrier(dist)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -362,10 +365,12 @@ def run_gpu(args):
             "kernel": "level_kernel (one launch per logic level)",
             "algorithmic_bytes_per_launch": float(lvl_bytes.mean()),
             "avg_launch_ms": float(level_ms.sum() / (args.steps * net.num_levels)),
+            "share_of_step": float(level_ms.sum() / (total_s * 1e3)),
+            "bounds_kernel_avg_ms": float(bounds_ms.sum() / (args.steps * net.num_levels)),
         },
         "e2e": None if e2e_value is None else {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                                                "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": int(args.steps * net.num_levels),
+        "gpu_launches": int(args.steps * net.num_levels * 2),   # bounds + simulation kernel per level
         "clocks": clocks.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -237,11 +237,15 @@ gatspi_status enqueue_levels(gatspi_ctx *c, cudaStream_t s) {
     CUDA_TRY(cudaMemsetAsync(c->status, 0, sizeof(int32_t) * kStatusWords, s), "clearing the status");
     const DevParams p = c->params();
     const bool timing = (c->flags & GATSPI_FLAG_LEVEL_TIMING) != 0;
+    // events: [2l] before the bounds kernel of level l, [2l+1] between it and the
+    // simulation kernel, [2l+2] after the simulation kernel
     for (int l = 0; l < c->L; ++l) {
-        if (timing) CUDA_TRY(cudaEventRecord(c->events[l], s), "recording a level event");
-        CUDA_TRY(launch_level(p, c->launches[l], s), "launching a level kernel");
+        if (timing) CUDA_TRY(cudaEventRecord(c->events[2 * l], s), "recording a level event");
+        CUDA_TRY(launch_level_bounds(p, c->launches[l], s), "launching a bounds kernel");
+        if (timing) CUDA_TRY(cudaEventRecord(c->events[2 * l + 1], s), "recording a level event");
+        CUDA_TRY(launch_level_sim(p, c->launches[l], s), "launching a level kernel");
     }
-    if (timing && c->L > 0) CUDA_TRY(cudaEventRecord(c->events[c->L], s), "recording a level event");
+    if (timing && c->L > 0) CUDA_TRY(cudaEventRecord(c->events[2 * c->L], s), "recording a level event");
     return GATSPI_OK;
 }
 
@@ -377,7 +381,7 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(cudaMemset(c->t1, 0, sizeof(unsigned long long) * std::max(c->G, 1)), "clearing T1");
         CUDA_TRY(set_level_smem_limit(c->stage), "configuring shared memory");
         if (c->flags & GATSPI_FLAG_LEVEL_TIMING) {
-            c->events.resize(c->L + 1, nullptr);
+            c->events.resize(2 * c->L + 1, nullptr);
             for (auto &e : c->events) CUDA_TRY(cudaEventCreate(&e), "creating level events");
         }
         return GATSPI_OK;
@@ -587,16 +591,20 @@ gatspi_status gatspi_device_views(gatspi_ctx *c, gatspi_views *v) {
     return GATSPI_OK;
 }
 
-gatspi_status gatspi_level_times(gatspi_ctx *c, float *ms, int32_t n) {
+gatspi_status gatspi_level_times(gatspi_ctx *c, float *sim_ms, float *bounds_ms, int32_t n) {
     g_err.clear();
-    if (!c || !ms) return fail(GATSPI_EINVAL, "ctx and ms are required");
+    if (!c || (!sim_ms && !bounds_ms)) return fail(GATSPI_EINVAL, "ctx and an output array are required");
     if (!(c->flags & GATSPI_FLAG_LEVEL_TIMING)) return fail(GATSPI_ESTATE, "created without GATSPI_FLAG_LEVEL_TIMING");
     if (n != c->L) return fail(GATSPI_EINVAL, "ms needs num_levels entries");
     if (!c->simulated) return fail(GATSPI_ESTATE, "simulate first");
     gatspi_status st = sync_ctx(c);
     if (st != GATSPI_OK) return st;
-    for (int l = 0; l < c->L; ++l)
-        CUDA_TRY(cudaEventElapsedTime(&ms[l], c->events[l], c->events[l + 1]), "reading level events");
+    for (int l = 0; l < c->L; ++l) {
+        if (bounds_ms)
+            CUDA_TRY(cudaEventElapsedTime(&bounds_ms[l], c->events[2 * l], c->events[2 * l + 1]), "reading level events");
+        if (sim_ms)
+            CUDA_TRY(cudaEventElapsedTime(&sim_ms[l], c->events[2 * l + 1], c->events[2 * l + 2]), "reading level events");
+    }
     return GATSPI_OK;
 }
 

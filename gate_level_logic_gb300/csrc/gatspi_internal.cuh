@@ -77,7 +77,9 @@ struct LevelLaunch {
 
 size_t level_smem_bytes(int stage);
 cudaError_t set_level_smem_limit(int stage);
-cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // bounds scan + level kernel
+cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // output regions
+cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s);      // the simulation
+cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s);          // both, in order
 cudaError_t launch_window_lengths(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,
                                   long long *len, cudaStream_t s);
 cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,

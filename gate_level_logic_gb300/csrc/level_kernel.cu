@@ -568,15 +568,22 @@ cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const i
 
 size_t level_smem_bytes(int stage) { return (size_t)kLevelWarps * 32 * (size_t)stage * sizeof(int32_t); }
 
-cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
+cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
     const unsigned scan_blocks = (unsigned)((l.scan_tiles + kWarps - 1) / kWarps);
     level_bounds_kernel<<<scan_blocks, kBlock, 0, s>>>(p, l);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
     const size_t smem = level_smem_bytes(p.stage);
     const unsigned blocks = (unsigned)((l.num_tiles + kLevelWarps - 1) / kLevelWarps);
     level_kernel<<<blocks, kLevelBlock, smem, s>>>(p, l);
     return cudaGetLastError();
+}
+
+cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
+    const cudaError_t e = launch_level_bounds(p, l, s);
+    return e != cudaSuccess ? e : launch_level_sim(p, l, s);
 }
 
 cudaError_t set_level_smem_limit(int stage) {

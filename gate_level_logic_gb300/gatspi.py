@@ -73,7 +73,7 @@ SIGNATURES = {
     "gatspi_export_offsets": (ctypes.c_int, [_p, _p, _p, ctypes.c_size_t]),
     "gatspi_export_windows": (ctypes.c_int, [_p, _p, ctypes.c_int32, _p, _p, ctypes.c_size_t]),
     "gatspi_device_views": (ctypes.c_int, [_p, ctypes.POINTER(gatspi_views)]),
-    "gatspi_level_times": (ctypes.c_int, [_p, _p, ctypes.c_int32]),
+    "gatspi_level_times": (ctypes.c_int, [_p, _p, _p, ctypes.c_int32]),
     "gatspi_simulate_level_static": (ctypes.c_int, [ctypes.POINTER(gatspi_level_args), _p]),
     "gatspi_destroy": (None, [_p]),
     "gatspi_last_error": (ctypes.c_char_p, []),
@@ -155,8 +155,8 @@ def gatspi_device_views(ctx: int) -> gatspi_views:
     return v
 
 
-def gatspi_level_times(ctx: int, ms: int, n: int):
-    _check(library().gatspi_level_times(_p(ctx), _p(ms), n))
+def gatspi_level_times(ctx: int, sim_ms: int, bounds_ms: int, n: int):
+    _check(library().gatspi_level_times(_p(ctx), _p(sim_ms), _p(bounds_ms), n))
 
 
 def gatspi_simulate_level_static(args: gatspi_level_args, stream: int = 0):

@@ -160,7 +160,9 @@ class Simulator:
         used = self.pool_used()
         return self.pool[:used].cpu().numpy()
 
-    def level_times(self) -> np.ndarray:
-        ms = np.zeros(max(self.num_levels, 1), np.float32)
-        _c.gatspi_level_times(self.ctx, ms.ctypes.data, self.num_levels)
-        return ms[:self.num_levels]
+    def level_times(self):
+        """(simulation-kernel ms, bounds-kernel ms) per level of the last simulate."""
+        sim = np.zeros(max(self.num_levels, 1), np.float32)
+        bnd = np.zeros_like(sim)
+        _c.gatspi_level_times(self.ctx, sim.ctypes.data, bnd.ctypes.data, self.num_levels)
+        return sim[:self.num_levels], bnd[:self.num_levels]

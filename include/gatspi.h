@@ -255,9 +255,11 @@ gatspi_status gatspi_device_views(gatspi_ctx *ctx, gatspi_views *out);
 
 /*
  * Per-level kernel times in milliseconds of the last simulate (needs
- * GATSPI_FLAG_LEVEL_TIMING); ms has num_levels entries.  Synchronises first.
+ * GATSPI_FLAG_LEVEL_TIMING): sim_ms[l] for the simulation kernel of level l,
+ * bounds_ms[l] for the kernel that sizes its output regions (either may be NULL;
+ * n = num_levels).  Synchronises first.
  */
-gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *ms, int32_t n);
+gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *sim_ms, float *bounds_ms, int32_t n);
 
 /*
  * Buffers of one logic level for gatspi_simulate_level_static (all device memory,
