@@ -67,7 +67,8 @@ def _load(path=None):
         if path == _LIB_PATH:
             build()
         lib = ctypes.CDLL(path)
-        sig = [ctypes.POINTER(_Net), ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        sig = [ctypes.POINTER(_Net), ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+               ctypes.c_int32]
         lib.oracle_simulate.argtypes = sig + [ctypes.c_int, ctypes.c_void_p,
                                               ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int64),
                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_char_p, ctypes.c_int]
@@ -142,8 +143,10 @@ def _finish(lib, rc, err, pool_ptr, pool_words, off, tc, t1, net, stim):
                   num_windows=stim.num_windows)
 
 
-def simulate(net, stim, threads: int = 1, lib_path: str = None) -> Result:
-    """Event-driven oracle (Algorithm 1) over all gates and windows."""
+def simulate(net, stim, threads: int = 1, lib_path: str = None, pulse_percent: int = 100) -> Result:
+    """Event-driven oracle (Algorithm 1) over all gates and windows.  ``pulse_percent``
+    is PATHPULSEPERCENT: the inertial reject limit of both filters as a percentage of
+    the delay (100 = the page's setting, 0 = transport delay)."""
     lib = _load(lib_path)
     s, keep = _marshal(net, stim)
     W = int(stim.num_windows)
@@ -153,13 +156,13 @@ def simulate(net, stim, threads: int = 1, lib_path: str = None) -> Result:
     pool_ptr, pool_words = ctypes.c_void_p(), ctypes.c_int64()
     err = ctypes.create_string_buffer(512)
     rc = lib.oracle_simulate(ctypes.byref(s), W, keep["window_len"].ctypes.data, keep["pi_off"].ctypes.data,
-                             keep["pi_words"].ctypes.data, int(threads), off.ctypes.data,
+                             keep["pi_words"].ctypes.data, int(pulse_percent), int(threads), off.ctypes.data,
                              ctypes.byref(pool_ptr), ctypes.byref(pool_words), tc.ctypes.data, t1.ctypes.data,
                              err, 512)
     return _finish(lib, rc, err, pool_ptr, pool_words, off, tc[:net.num_gates], t1[:net.num_gates], net, stim)
 
 
-def bruteforce(net, stim, lib_path: str = None) -> Result:
+def bruteforce(net, stim, lib_path: str = None, pulse_percent: int = 100) -> Result:
     """Unit-time-step inertial-element simulator (tiny cases only)."""
     lib = _load(lib_path)
     s, keep = _marshal(net, stim)
@@ -170,6 +173,6 @@ def bruteforce(net, stim, lib_path: str = None) -> Result:
     pool_ptr, pool_words = ctypes.c_void_p(), ctypes.c_int64()
     err = ctypes.create_string_buffer(512)
     rc = lib.brute_simulate(ctypes.byref(s), W, keep["window_len"].ctypes.data, keep["pi_off"].ctypes.data,
-                            keep["pi_words"].ctypes.data, off.ctypes.data, ctypes.byref(pool_ptr),
+                            keep["pi_words"].ctypes.data, int(pulse_percent), off.ctypes.data, ctypes.byref(pool_ptr),
                             ctypes.byref(pool_words), tc.ctypes.data, t1.ctypes.data, err, 512)
     return _finish(lib, rc, err, pool_ptr, pool_words, off, tc[:net.num_gates], t1[:net.num_gates], net, stim)

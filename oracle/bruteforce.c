@@ -3,25 +3,35 @@
  * event-driven oracle on tiny netlists.  It shares no code with the oracle's
  * event loop nor with the CUDA library.
  *
- * Model (inertial delays as in Verilog-style gate and interconnect delays, the
- * semantics the GATSPI page's Algorithm 1 implements with PATHPULSEPERCENT = 100):
+ * Model (inertial delays as in Verilog-style gate and interconnect delays with a
+ * pulse reject limit of q percent of the delay, q = PATHPULSEPERCENT; the GATSPI
+ * page's Algorithm 1 implements q = 100):
  *   - every fanin edge (interconnect) and every gate is an inertial element with
- *     an output value and at most one pending event (value, time);
+ *     an output value and a queue of pending events (value, due time, the time it
+ *     was scheduled, its delay), oldest first;
  *   - time advances one unit per step; within a step, elements are visited in
  *     topological order (wires of a gate, then the gate, gates in level order);
- *   - at each step an element first lets a pending event due now take effect,
+ *   - at each step an element first lets the pending events due now take effect,
  *     then applies the input changes of this step one after another; a net can
  *     change more than once in one step (zero-width pulses) and its k-th change is
  *     applied at the k-th sub-step;
- *   - an input change to value v first cancels a pending event that is not yet
- *     due; then, if v differs from the element's output, an event (v, now + d)
- *     is scheduled (d = rise delay for v = 1, fall delay for v = 0 on a wire; on
- *     a gate, the smallest finite conditional delay among the pins that changed
- *     in this sub-step, looked up at row 4*pin + 2*e_in + e_out, RISE = 0,
- *     FALL = 1, and at the column formed by the other pins' values, first pin
- *     most significant); a zero delay takes effect at once;
- *   - a gate compares its new value with its last scheduled value (the pending
- *     value if an event is pending, else its output) and does nothing when equal;
+ *   - delays: rise delay for a new value 1, fall delay for 0 on a wire; on a gate,
+ *     the smallest finite conditional delay among the pins that changed in this
+ *     sub-step, looked up at row 4*pin + 2*e_in + e_out, RISE = 0, FALL = 1, and at
+ *     the column formed by the other pins' values, first pin most significant;
+ *     r(d) = floor(d * q / 100) is the reject limit of delay d;
+ *   - a wire input change at time now withdraws the newest pending event when that
+ *     event was scheduled less than r(its delay) ago (the pulse it starts is too
+ *     narrow); otherwise it schedules (v, now + d);
+ *   - a gate compares its new value with its last scheduled value (the newest
+ *     pending value, else its output) and does nothing when equal; otherwise it
+ *     withdraws the newest pending event when the output pulse between that event
+ *     and now + d would be narrower than r(d), else schedules (v, now + d);
+ *   - with q = 100 both withdrawal tests mean "not yet due", so at most one event
+ *     is ever pending; a zero delay with nothing pending takes effect at once;
+ *   - an element whose events would fall due out of order (a wire whose rise and
+ *     fall delays differ by more than a pulse it lets through) is outside this
+ *     model: the run fails with ORACLE_EINVAL;
  *   - each window starts from the zero-delay steady state of the inputs' values.
  * Output waveforms are written in the Fig. 3 array format: [0] or [-1, 0], then
  * one timestamp per change, then EOW.
@@ -37,11 +47,45 @@
 #define BF_MAXP 8
 
 typedef struct {
+    int val;
+    long long due, at, d;   /* due time, time scheduled, delay */
+} event;
+
+typedef struct {
     int out;
-    int pending;
-    int pend_val;
-    long long pend_time;
+    int n, cap;     /* pending events q[0 .. n), oldest first */
+    event *q;
 } element;
+
+static long long bf_reject(long long d, int32_t q) { return d * q / 100; }
+
+static int el_push(element *x, int v, long long now, long long d) {
+    if (x->n > 0 && now + d < x->q[x->n - 1].due) return -2; /* out of order */
+    if (x->n == x->cap) {
+        int c = x->cap ? 2 * x->cap : 4;
+        event *nq = (event *)realloc(x->q, (size_t)c * sizeof(event));
+        if (!nq) return -1;
+        x->q = nq;
+        x->cap = c;
+    }
+    x->q[x->n].val = v;
+    x->q[x->n].due = now + d;
+    x->q[x->n].at = now;
+    x->q[x->n].d = d;
+    x->n += 1;
+    return 0;
+}
+
+/* Let the events due now take effect; returns how many did. */
+static int el_mature(element *x, long long now) {
+    int k = 0;
+    while (k < x->n && x->q[k].due == now) x->out = x->q[k++].val;
+    if (k) {
+        memmove(x->q, x->q + k, (size_t)(x->n - k) * sizeof(event));
+        x->n -= k;
+    }
+    return k;
+}
 
 typedef struct {
     int32_t *t;
@@ -69,7 +113,8 @@ static int bf_lookup(const uint8_t *tt, const int32_t *wt, const int *v, int n) 
 
 /* Simulate one window; fills per-gate change lists and initial values. */
 static int bf_window(const oracle_netlist *nl, int32_t W, int32_t w, long long Lw, const int64_t *pi_off,
-                     const int32_t *pi_words, tlist *changes, int *init, long long *ones, char *err, int errlen) {
+                     const int32_t *pi_words, int32_t q, tlist *changes, int *init, long long *ones, char *err,
+                     int errlen) {
     const int32_t P = nl->num_inputs, G = nl->num_gates, N = P + G;
     const int32_t E = nl->fanin_off[G];
     int *val = (int *)calloc((size_t)N + 1, sizeof(int));      /* value at the end of the step */
@@ -113,8 +158,8 @@ static int bf_window(const oracle_netlist *nl, int32_t W, int32_t w, long long L
     for (long long now = 0;; ++now) {
         if (now > 0) {
             int busy = now <= last_input;
-            for (int32_t e = 0; e < E && !busy; ++e) busy = wire[e].pending;
-            for (int32_t g = 0; g < G && !busy; ++g) busy = gate[g].pending;
+            for (int32_t e = 0; e < E && !busy; ++e) busy = wire[e].n > 0;
+            for (int32_t g = 0; g < G && !busy; ++g) busy = gate[g].n > 0;
             if (!busy && now >= Lw) break;
             /* input changes at this step */
             for (int32_t s = 0; s < P; ++s) {
@@ -147,23 +192,25 @@ static int bf_window(const oracle_netlist *nl, int32_t W, int32_t w, long long L
                     element *x = &wire[e];
                     wprev[e] = x->out;
                     wcnt[e] = 0;
-                    if (x->pending && x->pend_time == now) {
-                        x->out = x->pend_val;
-                        x->pending = 0;
-                        wcnt[e] += 1;
-                    }
+                    wcnt[e] += el_mature(x, now);
                     for (int k = 1; k <= cnt[s]; ++k) {
                         const int sv = prev[s] ^ (k & 1);
-                        if (x->pending) x->pending = 0; /* not yet due: cancelled */
-                        if (sv != x->out) {
+                        const int last = x->n ? x->q[x->n - 1].val : x->out;
+                        if (x->n && now - x->q[x->n - 1].at < bf_reject(x->q[x->n - 1].d, q)) {
+                            x->n -= 1; /* the pulse the newest event starts is too narrow */
+                        } else if (sv != last) {
                             const long long d = sv ? nl->wire_rise[e] : nl->wire_fall[e];
-                            if (d == 0) {
+                            if (d == 0 && x->n == 0) {
                                 x->out = sv;
                                 wcnt[e] += 1;
                             } else {
-                                x->pending = 1;
-                                x->pend_val = sv;
-                                x->pend_time = now + d;
+                                const int pr = el_push(x, sv, now, d);
+                                if (pr) {
+                                    snprintf(err, errlen, "wire %d window %d: %s", e, w,
+                                             pr == -2 ? "events fall due out of order" : "out of memory");
+                                    rc = pr == -2 ? ORACLE_EINVAL : ORACLE_ENOMEM;
+                                    goto done;
+                                }
                             }
                         }
                     }
@@ -173,9 +220,7 @@ static int bf_window(const oracle_netlist *nl, int32_t W, int32_t w, long long L
                 element *y = &gate[g];
                 prev[P + g] = y->out;
                 cnt[P + g] = 0;
-                if (y->pending && y->pend_time == now) {
-                    y->out = y->pend_val;
-                    y->pending = 0;
+                for (int k = el_mature(y, now); k > 0; --k) {
                     cnt[P + g] += 1;
                     if (tl_push(&changes[g], (int32_t)now)) {
                         rc = ORACLE_ENOMEM;
@@ -191,7 +236,7 @@ static int bf_window(const oracle_netlist *nl, int32_t W, int32_t w, long long L
                         if (changed[i]) pv[i] ^= 1;
                     }
                     const int nv = bf_lookup(tt, nl->pin_weight + e0, pv, n);
-                    const int last = y->pending ? y->pend_val : y->out;
+                    const int last = y->n ? y->q[y->n - 1].val : y->out;
                     if (nv == last) continue;
                     long long d = BF_NONE;
                     for (int i = 0; i < n; ++i) {
@@ -210,9 +255,9 @@ static int bf_window(const oracle_netlist *nl, int32_t W, int32_t w, long long L
                         rc = ORACLE_EBADLUT;
                         goto done;
                     }
-                    if (y->pending) {
-                        y->pending = 0; /* not yet due: cancelled */
-                    } else if (d == 0) {
+                    if (y->n && now + d - y->q[y->n - 1].due < bf_reject(d, q)) {
+                        y->n -= 1; /* the output pulse would be too narrow */
+                    } else if (d == 0 && y->n == 0) {
                         y->out = nv;
                         cnt[P + g] += 1;
                         if (tl_push(&changes[g], (int32_t)now)) {
@@ -220,9 +265,13 @@ static int bf_window(const oracle_netlist *nl, int32_t W, int32_t w, long long L
                             goto done;
                         }
                     } else {
-                        y->pending = 1;
-                        y->pend_val = nv;
-                        y->pend_time = now + d;
+                        const int pr = el_push(y, nv, now, d);
+                        if (pr) {
+                            snprintf(err, errlen, "gate %d window %d: %s", g, w,
+                                     pr == -2 ? "events fall due out of order" : "out of memory");
+                            rc = pr == -2 ? ORACLE_EINVAL : ORACLE_ENOMEM;
+                            goto done;
+                        }
                     }
                 }
                 val[P + g] = y->out;
@@ -232,6 +281,10 @@ static int bf_window(const oracle_netlist *nl, int32_t W, int32_t w, long long L
             for (int32_t g = 0; g < G; ++g) ones[g] += gate[g].out;
     }
 done:
+    if (wire)
+        for (int32_t e = 0; e < E; ++e) free(wire[e].q);
+    if (gate)
+        for (int32_t g = 0; g < G; ++g) free(gate[g].q);
     free(val);
     free(prev);
     free(cnt);
@@ -245,7 +298,7 @@ done:
 
 /* Same output layout as oracle_simulate: CSR offsets over (net, window), net-major. */
 int brute_simulate(const oracle_netlist *nl, int32_t W, const int64_t *window_len, const int64_t *pi_off,
-                   const int32_t *pi_words, int64_t *out_off, int32_t **out_pool, int64_t *out_pool_words,
+                   const int32_t *pi_words, int32_t pulse_percent, int64_t *out_off, int32_t **out_pool, int64_t *out_pool_words,
                    int64_t *tc, int64_t *t1, char *err, int errlen) {
     const int32_t P = nl->num_inputs, G = nl->num_gates;
     tlist *ch = (tlist *)calloc((size_t)G * W + 1, sizeof(tlist));
@@ -262,7 +315,7 @@ int brute_simulate(const oracle_netlist *nl, int32_t W, const int64_t *window_le
         long long *on = (long long *)calloc((size_t)G + 1, sizeof(long long));
         for (int32_t w = 0; w < W && rc == ORACLE_OK; ++w) {
             for (int32_t g = 0; g < G; ++g) tmp[g].n = 0;
-            rc = bf_window(nl, W, w, window_len[w], pi_off, pi_words, tmp, ini, on, err, errlen);
+            rc = bf_window(nl, W, w, window_len[w], pi_off, pi_words, pulse_percent, tmp, ini, on, err, errlen);
             for (int32_t g = 0; g < G && rc == ORACLE_OK; ++g) {
                 tlist *dst = &ch[(int64_t)g * W + w];
                 for (long long k = 0; k < tmp[g].n; ++k) tl_push(dst, tmp[g].t[k]);

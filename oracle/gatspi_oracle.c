@@ -39,6 +39,17 @@
  *     switching pin's new edge, e_out the output's); column = the values (after
  *     the switch) of the other pins in pin order, first pin most significant;
  *   - each window starts from the zero-delay steady state of its input values.
+ *
+ * Other pulse limits.  The page fixes PATHPULSEPERCENT at 100 and notes that other
+ * values come from editing the inertial comparison.  With a percentage q (0..100)
+ * the delay in both comparisons -- the interconnect pulse test and the gate's
+ * filter -- is replaced by its reject limit r = floor(d * q / 100): a pulse on a
+ * fanin whose width is below r of its first edge's wire delay is skipped, and the
+ * last output entry is cancelled when t_o - O[last] < r.  q = 100 gives the rules
+ * above.  Below 100 several output entries can be pending at once; a cancel then
+ * exposes the entry before it, which a later event may cancel in turn.  q = 0 is
+ * transport delay: no pulse is filtered, and only an output event scheduled before
+ * the last scheduled one replaces it.
  */
 #include <pthread.h>
 #include <stdio.h>
@@ -52,6 +63,9 @@
 #define MAXP 8
 #define RISE 0
 #define FALL 1
+
+/* reject limit of a delay d at PATHPULSEPERCENT q */
+static int64_t reject_limit(int64_t d, int32_t q) { return d * q / 100; }
 
 typedef struct {
     int32_t *w;
@@ -74,7 +88,7 @@ static int wbuf_reserve(wbuf *b, int64_t need) {
  * window's toggle count and time at 1. */
 static int simulate_task(int n, const int32_t *const *Win, const int32_t *wire_rise,
                          const int32_t *wire_fall, const int32_t *weight, const uint8_t *T,
-                         const int32_t *D, int64_t Lw, wbuf *O, int64_t *tc, int64_t *t1) {
+                         const int32_t *D, int64_t Lw, int32_t q, wbuf *O, int64_t *tc, int64_t *t1) {
     int64_t p[MAXP];
     int64_t a[MAXP];
     int sw[MAXP];
@@ -108,8 +122,9 @@ static int simulate_task(int n, const int32_t *const *Win, const int32_t *wire_r
             for (;;) {
                 d = (p[i] % 2) ? wire_fall[i] : wire_rise[i]; /* edge leaving the current value */
                 if (Win[i][p[i] + 1] == EOW) break;
-                /* interconnect inertial filter: a pulse narrower than d never reaches the pin */
-                if ((int64_t)Win[i][p[i] + 2] - d - (int64_t)Win[i][p[i] + 1] < 0)
+                /* interconnect inertial filter: a pulse narrower than the reject limit
+                 * of d never reaches the pin (the limit is d itself at q = 100) */
+                if ((int64_t)Win[i][p[i] + 2] - reject_limit(d, q) - (int64_t)Win[i][p[i] + 1] < 0)
                     p[i] += 2;
                 else
                     break;
@@ -144,7 +159,7 @@ static int simulate_task(int n, const int32_t *const *Win, const int32_t *wire_r
             if (d == NO_ARC) return ORACLE_EBADLUT;
             const int64_t t_o = t + d;
             if (t_o >= EOW) return ORACLE_EINVAL;
-            if (t_o - (int64_t)O->w[po] < d) { /* gate inertial filter */
+            if (t_o - (int64_t)O->w[po] < reject_limit(d, q)) { /* gate inertial filter */
                 po -= 1;                        /* cancel the unmatured entry */
             } else {
                 po += 1;
@@ -192,6 +207,7 @@ typedef struct {
     const int64_t *window_len;
     const int64_t *pi_off;
     const int32_t *pi_words;
+    int32_t pulse_percent;
     int32_t w0, w1;         /* window range of this worker */
     wbuf pool;              /* gate outputs of this worker, task order (gate, window) */
     int64_t *start;         /* [G * nw] start of each (gate, local window) in pool */
@@ -230,7 +246,7 @@ static void *worker_run(void *arg) {
                     Win[i] = wk->pool.w + wk->start[(int64_t)(s - P) * nw + lw];
             }
             int64_t tc = 0, t1 = 0;
-            int st = simulate_task(n, Win, wr, wf, wt, T, D, wk->window_len[w], &O, &tc, &t1);
+            int st = simulate_task(n, Win, wr, wf, wt, T, D, wk->window_len[w], wk->pulse_percent, &O, &tc, &t1);
             if (st != ORACLE_OK) {
                 wk->status = st;
                 snprintf(wk->msg, sizeof wk->msg, "gate %d window %d: %s", g, w,
@@ -299,8 +315,13 @@ static int validate(const oracle_netlist *nl, int32_t W, const int64_t *pi_off, 
  * holds the input waveforms followed by the gate outputs in (gate, window)
  * order.  *out_pool is malloc'd and must be released with oracle_free. */
 int oracle_simulate(const oracle_netlist *nl, int32_t W, const int64_t *window_len, const int64_t *pi_off,
-                    const int32_t *pi_words, int nthreads, int64_t *out_off, int32_t **out_pool,
-                    int64_t *out_pool_words, int64_t *tc, int64_t *t1, char *err, int errlen) {
+                    const int32_t *pi_words, int32_t pulse_percent, int nthreads, int64_t *out_off,
+                    int32_t **out_pool, int64_t *out_pool_words, int64_t *tc, int64_t *t1, char *err,
+                    int errlen) {
+    if (pulse_percent < 0 || pulse_percent > 100) {
+        snprintf(err, errlen, "PATHPULSEPERCENT must be 0 .. 100");
+        return ORACLE_EINVAL;
+    }
     int st = validate(nl, W, pi_off, pi_words, err, errlen);
     if (st) return st;
     const int32_t P = nl->num_inputs, G = nl->num_gates;
@@ -321,6 +342,7 @@ int oracle_simulate(const oracle_netlist *nl, int32_t W, const int64_t *window_l
         x->window_len = window_len;
         x->pi_off = pi_off;
         x->pi_words = pi_words;
+        x->pulse_percent = pulse_percent;
         x->w0 = (int32_t)((int64_t)W * k / nthreads);
         x->w1 = (int32_t)((int64_t)W * (k + 1) / nthreads);
         const int64_t nw = x->w1 - x->w0;

@@ -3,6 +3,8 @@
 Fixtures in tests/golden/ hold the page's values with their citations:
 * fig3_waveforms.json -- GATSPI page, Section 3, Fig. 3 (array format);
 * fig4_lookup.json    -- GATSPI page, Section 3, Fig. 4 (truth table, SDF delay LUT).
+The PATHPULSEPERCENT examples at the end are worked by hand from the rule the page
+states (derivations beside them).
 """
 import json
 import os
@@ -145,3 +147,48 @@ def test_malformed_input_is_an_error(oracle_lib):
         with pytest.raises(oracle_lib.OracleError) as e:
             _run(oracle_lib, net, [bad], 100)
         assert e.value.code == 4
+
+
+# PATHPULSEPERCENT.  The GATSPI page (Section 3, the prose after Algorithm 1) fixes
+# the pulse limit at 100 % of the delay and says other limits come from editing
+# the gate filter's comparison.  Worked by hand from that rule, reading the limit as
+# floor(delay * q / 100) in both the interconnect and the gate comparison:
+#
+# BUF, interconnect rise = fall = 4, gate delay 10 on both arcs; input pulses of
+# widths 3, 7, 6, 14, 8, 12, 12 starting at 10.
+#   q = 100: the interconnect drops [10, 13) (3 < 4); arrivals 24 30 44 52 64 76; the
+#            gate (limit 10) cancels 34 at 30 (40 - 34 < 10) and 54 at 52, keeps 74, 86.
+#   q = 50:  limits 2 and 5; every pulse reaches the pin: arrivals 14 17 24 30 44 52
+#            64 76; 24 is cancelled at 17 (27 - 24 < 5); the rest stay.
+#   q = 0:   nothing is filtered: every arrival + 10.
+PULSE_WAVE = [0, 10, 13, 20, 26, 40, 48, 60, 72, EOW]
+PULSE_EXPECT = {
+    100: [0, 74, 86, EOW],
+    50: [0, 34, 40, 54, 62, 74, 86, EOW],
+    0: [0, 24, 27, 34, 40, 54, 62, 74, 86, EOW],
+}
+
+# BUF with a slow rise (10) and a fast fall (2), no interconnect delay; arrivals
+# 5 7 20 21 22 31.  Each fall lands before the pending rise and cancels it, at any
+# limit.  The last pair: the rise at 22 gives 32, the fall at 31 gives 33:
+# 33 - 32 = 1 is below the q = 100 limit 2 (cancelled) but not below the q = 50
+# limit 1 nor the q = 0 limit 0 (kept).
+SKEW_WAVE = [0, 5, 7, 20, 21, 22, 31, EOW]
+SKEW_EXPECT = {100: [0, EOW], 50: [0, 32, 33, EOW], 0: [0, 32, 33, EOW]}
+
+
+@pytest.mark.parametrize("q", sorted(PULSE_EXPECT))
+def test_pulse_percent_worked_example(oracle_lib, q):
+    buf = single_gate(synth.truth_table("BUF"), 1, uniform_delays(1, 10, 10, synth.truth_table("BUF")),
+                      wire_rise=[4], wire_fall=[4])
+    r = oracle_lib.simulate(buf, synth.from_waveforms([[PULSE_WAVE]], 200), pulse_percent=q)
+    assert r.gate_wave(0, 0).tolist() == PULSE_EXPECT[q]
+    assert int(r.tc[0]) == len(PULSE_EXPECT[q]) - 2
+
+
+@pytest.mark.parametrize("q", sorted(SKEW_EXPECT))
+def test_pulse_percent_skewed_delays(oracle_lib, q):
+    tt = synth.truth_table("BUF")
+    buf = single_gate(tt, 1, uniform_delays(1, 10, 2, tt))
+    r = oracle_lib.simulate(buf, synth.from_waveforms([[SKEW_WAVE]], 100), pulse_percent=q)
+    assert r.gate_wave(0, 0).tolist() == SKEW_EXPECT[q]

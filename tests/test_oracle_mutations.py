@@ -26,9 +26,19 @@ MUTANTS = {
     "wire rise/fall swapped": (
         "d = (p[i] % 2) ? wire_fall[i] : wire_rise[i];", "d = (p[i] % 2) ? wire_rise[i] : wire_fall[i];"),
     "gate filter not strict": (
-        "if (t_o - (int64_t)O->w[po] < d) {", "if (t_o - (int64_t)O->w[po] <= d) {"),
+        "if (t_o - (int64_t)O->w[po] < reject_limit(d, q)) {",
+        "if (t_o - (int64_t)O->w[po] <= reject_limit(d, q)) {"),
     "gate filter never cancels": (
-        "if (t_o - (int64_t)O->w[po] < d) {", "if (0) {"),
+        "if (t_o - (int64_t)O->w[po] < reject_limit(d, q)) {", "if (0) {"),
+    "wire filter ignores PATHPULSEPERCENT": (
+        "reject_limit(d, q) - (int64_t)Win[i][p[i] + 1] < 0)", "d - (int64_t)Win[i][p[i] + 1] < 0)"),
+    "gate filter ignores PATHPULSEPERCENT": (
+        "if (t_o - (int64_t)O->w[po] < reject_limit(d, q)) {", "if (t_o - (int64_t)O->w[po] < d) {"),
+    "reject limit rounded up": (
+        "return d * q / 100;", "return (d * q + 99) / 100;"),
+    "a cancel never exposes a pending entry": (
+        "if (t_o - (int64_t)O->w[po] < reject_limit(d, q)) {",
+        "if (t_o - (int64_t)O->w[po] < reject_limit(d, q) && (po < 1 || O->w[po - 1] <= t)) {"),
     "MSI takes the last finite arc, not the smallest": (
         "if (dd != NO_ARC && dd < d) d = dd;", "if (dd != NO_ARC) d = dd;"),
     "row: input and output edge transposed": (
@@ -72,12 +82,24 @@ def _battery(lib_path):
         checks.append(functools.partial(pins.test_buffer_inverter_chain_is_inertial_delay_line, shim, seed))
     checks.append(lambda: pins.test_output_invariants(shim, "tiny"))
 
+    for q in (50, 0):
+        checks.append(functools.partial(golden.test_pulse_percent_worked_example, shim, q))
+        checks.append(functools.partial(golden.test_pulse_percent_skewed_delays, shim, q))
+        checks.append(functools.partial(pins.test_chain_with_pulse_limit_is_filtered_delay_line, shim, q, 0))
+
     def brute():
         import numpy as np
         for seed in range(150):
             net, stim = pins._random_case(seed)
             r = shim.simulate(net, stim)
             b = shim.bruteforce(net, stim)
+            assert np.array_equal(r.pool, b.pool) and np.array_equal(r.tc, b.tc) and np.array_equal(r.t1, b.t1)
+        for seed in range(100):
+            net, stim = pins._random_case(seed)
+            net = pins._skew_free(net)
+            q = (0, 30, 50, 90)[seed % 4]
+            r = shim.simulate(net, stim, pulse_percent=q)
+            b = shim.bruteforce(net, stim, pulse_percent=q)
             assert np.array_equal(r.pool, b.pool) and np.array_equal(r.tc, b.tc) and np.array_equal(r.t1, b.t1)
     checks.append(brute)
     for c in checks:

@@ -5,7 +5,10 @@
   inertial wire and gate elements, over many seeded tiny netlists;
 * all-zero delays: every net equals the combinational function of the inputs;
 * BUF / INV chains with equal rise and fall delay d: a delay line that drops every
-  pulse shorter than d (inertial delay);
+  pulse shorter than d (inertial delay), or shorter than floor(d * q / 100) at
+  PATHPULSEPERCENT q (q = 0: transport delay, nothing dropped);
+* other PATHPULSEPERCENT values against the unit-step simulator, whose elements
+  then hold queues of pending events;
 * cycle windows: when every event settles inside its cycle, simulating W windows
   equals the single-window run cut at the window boundaries;
 * format invariants of every output waveform and of the toggle statistics.
@@ -146,14 +149,16 @@ def test_zero_delay_equals_combinational(oracle_lib):
         assert changes(out) == expect[g], g
 
 
-def _inertial_closed_form(times, init, d):
-    """Inertial delay d: an input change to v at t reaches the output at t + d when
-    the input then holds v for at least d and v differs from the output."""
+def _inertial_closed_form(times, init, d, r=None):
+    """Inertial delay d with pulse reject limit r (r = d unless given): an input change
+    to v at t reaches the output at t + d when the input then holds v for at least r
+    and v differs from the output."""
+    r = d if r is None else r
     out, cur = [], init
     for k, t in enumerate(times):
         v = init ^ ((k + 1) & 1)
         nxt = times[k + 1] if k + 1 < len(times) else None
-        if (nxt is None or nxt - t >= d) and v != cur:
+        if (nxt is None or nxt - t >= r) and v != cur:
             out.append(t + d)
             cur = v
     return out
@@ -183,6 +188,84 @@ def test_buffer_inverter_chain_is_inertial_delay_line(oracle_lib, seed):
         out = r.gate_wave(g, 0)
         assert changes(out) == [t + g * d for t in stage1]
         assert value_at(out, 0) == init ^ inv
+
+
+@pytest.mark.parametrize("q", [100, 60, 25, 0])
+@pytest.mark.parametrize("seed", range(6))
+def test_chain_with_pulse_limit_is_filtered_delay_line(oracle_lib, q, seed):
+    """PATHPULSEPERCENT q: every interconnect (rise = fall = dw) and every gate (delay d)
+    of a BUF/INV chain is a delay line that drops the pulses narrower than its reject
+    limit floor(delay * q / 100); q = 0 drops none (transport delay)."""
+    rng = np.random.default_rng(500 + seed)
+    k = int(rng.integers(1, 6))
+    d = int(rng.integers(1, 14))
+    dw = int(rng.integers(0, 7))
+    kinds = [("BUF", "INV")[int(b)] for b in rng.integers(0, 2, size=k)]
+    types = ["BUF", "INV"]
+    tts = [synth.truth_table(c) for c in types]
+    net = synth.build_netlist(num_inputs=1, level_gates=[1] * k, type_names=types, type_num_pins=[1, 1],
+                              type_tts=tts, gate_type=[types.index(c) for c in kinds],
+                              fanins=[[g] for g in range(k)], wire_rise=np.full(k, dw), wire_fall=np.full(k, dw),
+                              delay_tables=[uniform_delays(1, d, d, tts[types.index(c)]) for c in kinds])
+    times = np.cumsum(rng.integers(1, 2 * (d + dw) + 2, size=80)).tolist()
+    wave = [0] + times + [EOW]
+    r = oracle_lib.simulate(net, synth.from_waveforms([[wave]], times[-1] + 10 * k * (d + dw)), pulse_percent=q)
+    cur = times
+    for g in range(k):
+        cur = _inertial_closed_form(cur, 0, dw, dw * q // 100)      # the gate's interconnect
+        cur = _inertial_closed_form(cur, 0, d, d * q // 100)        # the gate
+        assert changes(r.gate_wave(g, 0)) == cur, (q, seed, g)
+    if q == 0:
+        assert len(changes(r.gate_wave(k - 1, 0))) == len(times)
+
+
+def _skew_free(net):
+    """The same netlist with every interconnect's fall delay set to its rise delay."""
+    net.wire_fall = net.wire_rise.copy()
+    return net
+
+
+@pytest.mark.parametrize("q", [0, 20, 50, 75, 99])
+def test_oracle_equals_bruteforce_pulse_percent(oracle_lib, q):
+    """Other PATHPULSEPERCENT values against the unit-step model with pending-event
+    queues (interconnect rise = fall, so that no element's events fall due out of
+    order); the sample must differ from the q = 100 result often."""
+    differ = 0
+    for seed in range(200):
+        net, stim = _random_case(seed)
+        net = _skew_free(net)
+        r = oracle_lib.simulate(net, stim, pulse_percent=q)
+        b = oracle_lib.bruteforce(net, stim, pulse_percent=q)
+        assert np.array_equal(r.off, b.off), (q, seed)
+        assert np.array_equal(r.pool, b.pool), (q, seed)
+        assert np.array_equal(r.tc, b.tc) and np.array_equal(r.t1, b.t1), (q, seed)
+        differ += not np.array_equal(r.pool, oracle_lib.simulate(net, stim).pool)
+    assert differ >= 40
+
+
+def test_oracle_equals_bruteforce_pulse_percent_skewed_wires(oracle_lib):
+    """Interconnects with different rise and fall delays: every case the unit-step
+    model can order (its events fall due in order) agrees with the oracle."""
+    agree = 0
+    for seed in range(300):
+        net, stim = _random_case(seed)
+        q = (0, 40, 80)[seed % 3]
+        r = oracle_lib.simulate(net, stim, pulse_percent=q)
+        try:
+            b = oracle_lib.bruteforce(net, stim, pulse_percent=q)
+        except oracle_lib.OracleError as e:
+            assert "out of order" in str(e)
+            continue
+        assert np.array_equal(r.pool, b.pool) and np.array_equal(r.tc, b.tc) and np.array_equal(r.t1, b.t1), seed
+        agree += 1
+    assert agree >= 150
+
+
+def test_pulse_percent_out_of_range_is_rejected(oracle_lib):
+    net, stim = synth.make("tiny")
+    for q in (-1, 101):
+        with pytest.raises(oracle_lib.OracleError):
+            oracle_lib.simulate(net, stim, pulse_percent=q)
 
 
 def test_windows_equal_cut_single_run(oracle_lib):
