@@ -82,13 +82,14 @@ def _sum_over_ranks(dist, x: float) -> float:
     return float(t.item())
 
 
-def workload_config(net, stim, stage_words):
+def workload_config(net, stim, stage_words, pulse_percent=100):
     return {
         "workload": "1M-gate synthetic netlist, 40 levels, 9-cell mix with SDF-conditional arcs; "
                     "4096 inputs, 10k cycles x period 1000, 5% activity, 10% glitch pairs; 256 cycle windows",
         "gates": int(net.num_gates), "levels": int(net.num_levels), "inputs": int(net.num_inputs),
         "edges": int(net.num_edges), "windows": int(stim.num_windows), "cycles": int(stim.window_cycles.sum()),
         "stage_words": stage_words,
+        "pulse_percent": pulse_percent,
         "l2": "inputs larger than L2 (waveform pool of several GB per step, no flush needed)",
     }
 
@@ -182,7 +183,7 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(net, stim, seconds_target=15.0):
+def cpu_baseline(net, stim, seconds_target=15.0, pulse_percent=100):
     """The CPU oracle as it stands, windows spread over all host cores, on a bounded
     sample of the workload's windows (all gates)."""
     import oracle
@@ -191,14 +192,14 @@ def cpu_baseline(net, stim, seconds_target=15.0):
     n = max(1, min(W, cores))
     sel = np.linspace(0, W - 1, n).astype(np.int64)
     t = time.perf_counter()
-    r = oracle.simulate(net, synth_select(stim, sel), threads=cores)
+    r = oracle.simulate(net, synth_select(stim, sel), threads=cores, pulse_percent=pulse_percent)
     dt = time.perf_counter() - t
     # grow the sample once to land near the target duration
     if dt < seconds_target / 4 and n < W:
         n2 = int(min(W, max(n + 1, n * min(8.0, seconds_target / max(dt, 1e-3)))))
         sel = np.linspace(0, W - 1, n2).astype(np.int64)
         t = time.perf_counter()
-        r = oracle.simulate(net, synth_select(stim, sel), threads=cores)
+        r = oracle.simulate(net, synth_select(stim, sel), threads=cores, pulse_percent=pulse_percent)
         dt = time.perf_counter() - t
     events = int(r.tc.sum())
     cycles = int(stim.window_cycles[sel].sum())
@@ -228,11 +229,11 @@ def run_reference(args):
     sel = np.linspace(0, W - 1, n).astype(np.int64)
     sub = synth.select_windows(stim, sel)
     for _ in range(args.warmup):
-        oracle.simulate(net, sub, threads=cores)
+        oracle.simulate(net, sub, threads=cores, pulse_percent=args.pulse_percent)
     times, events = [], 0
     for _ in range(args.steps):
         t = time.perf_counter()
-        r = oracle.simulate(net, sub, threads=cores)
+        r = oracle.simulate(net, sub, threads=cores, pulse_percent=args.pulse_percent)
         times.append(time.perf_counter() - t)
         events += int(r.tc.sum())
     total = sum(times)
@@ -242,7 +243,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": workload_config(net, stim, None),
+        "config": workload_config(net, stim, None, args.pulse_percent),
         "gate_cycles_per_s": net.num_gates * cycles * args.steps / total,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, n), "kind": "oracle",
                          "sample": "%d of %d windows per step (all gates)" % (n, W)},
@@ -293,7 +294,8 @@ def run_gpu(args):
     W = stim.num_windows
     flags = gatspi.GATSPI_FLAG_LEVEL_TIMING
     pool_words = int(args.pool_gb * (1 << 30) / 4)
-    sim = Simulator(net, stim.window_len, pool_words=pool_words, stage_words=args.stage_words, flags=flags)
+    sim = Simulator(net, stim.window_len, pool_words=pool_words, stage_words=args.stage_words, flags=flags,
+                    pulse_percent=args.pulse_percent)
     stream = torch.cuda.current_stream()
     sim.load(stim.pi_off, stim.pi_words, stream=stream)
 
@@ -354,7 +356,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": workload_config(net, stim, args.stage_words),
+        "config": workload_config(net, stim, args.stage_words, args.pulse_percent),
         "gate_cycles_per_s": gate_cycles_per_s,
         "events_per_step": events_per_step,
         "pool_words_used": pool_used,
@@ -375,7 +377,7 @@ def run_gpu(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         sim.close()
-        line["cpu_baseline"] = cpu_baseline(net, stim)
+        line["cpu_baseline"] = cpu_baseline(net, stim, pulse_percent=args.pulse_percent)
     if rank == 0:
         print(json.dumps(line))
     sim.close()
@@ -391,6 +393,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--stage-words", type=int, default=-1)
+    ap.add_argument("--pulse-percent", type=int, default=100,
+                    help="PATHPULSEPERCENT of both inertial filters (100 = the page's setting, 0 = transport)")
     ap.add_argument("--pool-gb", type=float, default=48.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

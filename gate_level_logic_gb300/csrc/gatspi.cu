@@ -60,6 +60,7 @@ struct gatspi_ctx {
     long long pool_words = 0;
     int stage = kDefaultStage;
     uint32_t flags = 0;
+    int32_t pulse_percent = 100;
 
     // device arrays owned by the context
     int4 *gate_desc = nullptr;
@@ -114,6 +115,7 @@ struct gatspi_ctx {
         p.lpg_log2 = lpg_log2;
         p.slots_per_gate = slots_per_gate;
         p.stage = stage;
+        p.pulse_percent = pulse_percent;
         return p;
     }
 };
@@ -133,6 +135,8 @@ gatspi_status validate(const gatspi_netlist *nl, const gatspi_config *cfg, long 
             return fail(GATSPI_EINVAL, "window %d: length must be in 1 .. 2^30", w);
     if (cfg->stage_words < -1 || cfg->stage_words > kMaxStage)
         return fail(GATSPI_EINVAL, "stage_words must be -1 or 0 .. %d", kMaxStage);
+    if ((cfg->flags & GATSPI_FLAG_PULSE_PERCENT) && (cfg->pulse_percent < 0 || cfg->pulse_percent > 100))
+        return fail(GATSPI_EINVAL, "pulse_percent must be 0 .. 100");
     if (G == 0) {
         *path_bound = 0;
         return GATSPI_OK;
@@ -293,6 +297,7 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         c->pool_words = (long long)pool_words;
         c->flags = cfg->flags;
         c->stage = cfg->stage_words < 0 ? kDefaultStage : cfg->stage_words;
+        c->pulse_percent = (cfg->flags & GATSPI_FLAG_PULSE_PERCENT) ? cfg->pulse_percent : 100;
         c->num_nets = (long long)c->P + c->G;
         c->nchunks = (c->W + 31) / 32;
         int lpg = 32;

@@ -63,6 +63,7 @@ struct DevParams {
     int32_t lpg_log2;         // log2(lanes per (gate, chunk) segment)
     int32_t slots_per_gate;   // nchunks << lpg_log2
     int32_t stage;            // output words staged on chip per lane
+    int32_t pulse_percent;    // PATHPULSEPERCENT, 0 .. 100
 };
 
 struct LevelLaunch {
@@ -76,7 +77,7 @@ struct LevelLaunch {
 };
 
 size_t level_smem_bytes(int stage);
-cudaError_t set_level_smem_limit(int stage);
+cudaError_t set_level_smem_limit(int stage);   // both variants of the simulation kernel
 cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // output regions
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s);      // the simulation
 cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s);          // both, in order

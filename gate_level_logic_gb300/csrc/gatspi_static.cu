@@ -52,6 +52,9 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     if (a->num_inputs < 0 || a->num_windows < 1 || a->gate_begin < 0 || a->num_gates < 0 || a->pool_words < 0)
         return err(GATSPI_EINVAL, "negative sizes");
     if (a->stage_words < -1 || a->stage_words > kMaxStage) return err(GATSPI_EINVAL, "stage_words out of range");
+    const bool own_percent = (a->flags & GATSPI_FLAG_PULSE_PERCENT) != 0;
+    if (own_percent && (a->pulse_percent < 0 || a->pulse_percent > 100))
+        return err(GATSPI_EINVAL, "pulse_percent must be 0 .. 100");
 
     DevParams p{};
     p.W = a->num_windows;
@@ -107,6 +110,7 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     p.status = (int32_t *)(words + kStatusWord);
     p.num_inputs = a->num_inputs;
     p.stage = a->stage_words < 0 ? kDefaultStage : a->stage_words;
+    p.pulse_percent = own_percent ? a->pulse_percent : 100;
 
     LevelLaunch l{};
     l.level = 0;

@@ -21,7 +21,12 @@
 // waveforms with interconnect inertial filtering, resolve simultaneous switching,
 // look up the truth table by summed pin weights, pick the conditional delay (row =
 // switching pin and edges, column = the other pins' values) and apply the gate's
-// inertial filter (PATHPULSEPERCENT = 100).  Before simulating, each lane turns its
+// inertial filter.  The kernel comes in two variants: PATHPULSEPERCENT = 100, the
+// page's setting, where the filter cancels exactly the output entries that have
+// not matured and at most one is ever pending; and any other percentage q, where
+// both filters compare against the reject limit floor(d * q / 100), several
+// output entries can be pending and a cancel re-reads the entry before the one it
+// exposes from the lane's own output.  Before simulating, each lane turns its
 // inputs' lengths into its window's own bound and a warp scan gives the window a
 // provisional slot in the region.  The lane keeps the first `stage` output words in
 // shared memory ([word][lane] layout, bank-conflict free) and writes any further
@@ -79,10 +84,18 @@ struct Pin {
     uint32_t drf;      // interconnect delays: rise | fall << 16
 };
 
+// Reject limit of delay d at PATHPULSEPERCENT q (d * q < 2^31 for every delay the
+// library accepts).
+__device__ __forceinline__ int32_t reject_limit(int32_t d, int32_t q) {
+    return (int32_t)((uint32_t)d * (uint32_t)q / 100u);
+}
+
 // Next arrival of a pin: skip every pulse narrower than the interconnect delay of
-// its first edge (the fall delay when the pin is at 1, the rise delay when at 0);
-// the arrival is the next timestamp plus that delay.  False on a malformed wave.
-__device__ __forceinline__ bool next_arrival(Pin &s) {
+// its first edge (the fall delay when the pin is at 1, the rise delay when at 0),
+// or than that delay's reject limit when kFull is false; the arrival is the next
+// timestamp plus the delay.  False on a malformed wave.
+template <bool kFull>
+__device__ __forceinline__ bool next_arrival(Pin &s, int32_t q) {
     for (;;) {
         // p + 1 == len - 1 is the EOW slot: no further transition
         if (s.p + 2 >= s.len) {
@@ -97,7 +110,7 @@ __device__ __forceinline__ bool next_arrival(Pin &s) {
             return false;
         }
         const int32_t d = (s.p & 1) ? (int32_t)(s.drf >> 16) : (int32_t)(s.drf & 0xffffu);
-        if (t2 - t1 < d) {               // the pulse [t1, t2) never reaches the pin
+        if (t2 - t1 < (kFull ? d : reject_limit(d, q))) {   // the pulse [t1, t2) never reaches the pin
             s.p += 2;
             continue;
         }
@@ -127,19 +140,19 @@ __device__ __forceinline__ int32_t arc_delay(const int32_t *__restrict__ D, uint
 
 // Advance pin k, chosen per lane: its state is gathered and written back with
 // predicated moves so that the lanes of a warp advance different pins together.
-template <int N>
-__device__ __forceinline__ bool advance_pin(Pin (&pin)[N], int k) {
-    if (N == 1) return next_arrival(pin[0]);
+template <int N, bool kFull>
+__device__ __forceinline__ bool advance_pin(Pin (&pin)[N], int k, int32_t q) {
+    if (N == 1) return next_arrival<kFull>(pin[0], q);
     Pin s = pin[0];
 #pragma unroll
-    for (int q = 1; q < N; ++q)
-        if (k == q) s = pin[q];
-    const bool ok = next_arrival(s);
+    for (int i = 1; i < N; ++i)
+        if (k == i) s = pin[i];
+    const bool ok = next_arrival<kFull>(s, q);
 #pragma unroll
-    for (int q = 0; q < N; ++q)
-        if (k == q) {
-            pin[q].p = s.p;
-            pin[q].a = s.a;
+    for (int i = 0; i < N; ++i)
+        if (k == i) {
+            pin[i].p = s.p;
+            pin[i].a = s.a;
         }
     return ok;
 }
@@ -151,9 +164,9 @@ __device__ __forceinline__ bool advance_pin(Pin (&pin)[N], int k) {
 // pins form a bit mask, the delay lookup and the pin advance serve the first
 // switching pin through a lane-selected pin state, and only simultaneous
 // switching of several pins takes an extra (rare) loop.
-template <int N>
+template <int N, bool kFull>
 __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const int32_t *__restrict__ D, int32_t Lw,
-                                               int32_t *stage, int stage_words, int32_t *__restrict__ gout) {
+                                               int32_t *stage, int stage_words, int32_t *__restrict__ gout, int32_t q) {
     LaneResult r{0, 0, 0, 0};
     auto put = [&](int32_t k, int32_t v) {
         if (k < stage_words)
@@ -161,6 +174,7 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
         else
             gout[k] = v;
     };
+    auto get = [&](int32_t k) { return k < stage_words ? stage[k * 32] : gout[k]; };   // this lane's own words
 
     // initial values: pin index 1 when the waveform starts with -1.  The truth table
     // was re-indexed at create by the pin weights, so its index is the pin values
@@ -174,14 +188,14 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
     const int32_t y0 = (tt >> vbits) & 1;
     int32_t po = y0;        // index of the last output entry
     int32_t top = 0;        // O[po]
-    int32_t second = 0;     // O[po - 1] (read only after a store)
+    int32_t second = 0;     // O[po - 1] (read only after a store, or after a cancel when kFull is false)
     int32_t t1acc = 0;      // signed sum of clipped entries: time at 1 before the final adjustment
     put(0, y0 ? -1 : 0);
     if (y0) put(1, 0);
 
     bool ok = true;
 #pragma unroll
-    for (int i = 0; i < N; ++i) ok &= next_arrival(pin[i]);
+    for (int i = 0; i < N; ++i) ok &= next_arrival<kFull>(pin[i], q);
 
     while (ok) {
         int32_t t = pin[0].a;
@@ -211,13 +225,15 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
                 r.err = GATSPI_EBADLUT;
                 break;
             }
-            if (top > t) {
-                // inertial filter: the last entry has not matured, cancel it
+            const int32_t to = t + d;
+            // inertial filter: at q = 100, to - top < d exactly when the last entry
+            // has not matured (top > t); otherwise the reject limit decides
+            if (kFull ? top > t : to - top < reject_limit(d, q)) {
                 t1acc -= (po & 1) ? -min(top, Lw) : min(top, Lw);
                 --po;
                 top = second;
+                if (!kFull) second = po > 0 ? get(po - 1) : 0;   // the exposed entry may be pending too
             } else {
-                const int32_t to = t + d;
                 ++po;
                 put(po, to);
                 t1acc += (po & 1) ? -min(to, Lw) : min(to, Lw);
@@ -225,8 +241,8 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
                 top = to;
             }
         }
-        ok &= advance_pin<N>(pin, k);
-        for (uint32_t m = more; m; m &= m - 1u) ok &= advance_pin<N>(pin, N - __ffs(m));   // lowest bit first
+        ok &= advance_pin<N, kFull>(pin, k, q);
+        for (uint32_t m = more; m; m &= m - 1u) ok &= advance_pin<N, kFull>(pin, N - __ffs(m), q);   // lowest bit first
     }
     if (!ok) r.err = GATSPI_EBADWAVE;
     put(po + 1, kEOW);
@@ -236,7 +252,7 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
     return r;
 }
 
-template <int N>
+template <int N, bool kFull>
 __device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS],
                                                  int32_t Lw, int32_t *stage, int32_t *gout) {
     Pin pin[N];
@@ -244,16 +260,17 @@ __device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd,
     for (int i = 0; i < N; ++i) pin[i] = pins[i];
     const uint32_t tt = (uint32_t)gd.y >> 8;
     const long long dly = (long long)(uint32_t)gd.z | ((long long)gd.w << 32);
-    return run_lane<N>(pin, tt, P.dly_data + dly, Lw, stage, P.stage, gout);
+    return run_lane<N, kFull>(pin, tt, P.dly_data + dly, Lw, stage, P.stage, gout, P.pulse_percent);
 }
 
+template <bool kFull>
 __device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS], int32_t Lw,
                                                int32_t *stage, int32_t *gout) {
     switch (gd.y & 7) {
-        case 1: return simulate_gate<1>(P, gd, pins, Lw, stage, gout);
-        case 2: return simulate_gate<2>(P, gd, pins, Lw, stage, gout);
-        case 3: return simulate_gate<3>(P, gd, pins, Lw, stage, gout);
-        default: return simulate_gate<4>(P, gd, pins, Lw, stage, gout);
+        case 1: return simulate_gate<1, kFull>(P, gd, pins, Lw, stage, gout);
+        case 2: return simulate_gate<2, kFull>(P, gd, pins, Lw, stage, gout);
+        case 3: return simulate_gate<3, kFull>(P, gd, pins, Lw, stage, gout);
+        default: return simulate_gate<4, kFull>(P, gd, pins, Lw, stage, gout);
     }
 }
 
@@ -357,6 +374,8 @@ __global__ void __launch_bounds__(kBlock) level_bounds_kernel(const DevParams P,
 
 // One warp = 32 consecutive (gate, window) slots of the level.  Warps share nothing
 // but the shared-memory allocation of their block and never wait for each other.
+// kFull: PATHPULSEPERCENT = 100.
+template <bool kFull>
 __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(const DevParams P, const LevelLaunch L) {
     extern __shared__ int32_t smem[];
     const int lane = threadIdx.x & 31;
@@ -422,7 +441,7 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
 
     LaneResult res{0, 0, 0, 0};
     if (valid) {
-        res = dispatch(P, gd, pins, Lw, stage, P.pool + prov);
+        res = dispatch<kFull>(P, gd, pins, Lw, stage, P.pool + prov);
         if (res.err) {
             raise_error(P.status, res.err, g, w, 0);
             res.len = 0;
@@ -577,7 +596,10 @@ cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaSt
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
     const size_t smem = level_smem_bytes(p.stage);
     const unsigned blocks = (unsigned)((l.num_tiles + kLevelWarps - 1) / kLevelWarps);
-    level_kernel<<<blocks, kLevelBlock, smem, s>>>(p, l);
+    if (p.pulse_percent == 100)
+        level_kernel<true><<<blocks, kLevelBlock, smem, s>>>(p, l);
+    else
+        level_kernel<false><<<blocks, kLevelBlock, smem, s>>>(p, l);
     return cudaGetLastError();
 }
 
@@ -587,7 +609,10 @@ cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t 
 }
 
 cudaError_t set_level_smem_limit(int stage) {
-    return cudaFuncSetAttribute(level_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(level_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)level_smem_bytes(stage));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(level_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)level_smem_bytes(stage));
 }
 

@@ -18,6 +18,7 @@ GATSPI_MAX_PINS = 4
 GATSPI_HOST, GATSPI_DEVICE = 0, 1
 GATSPI_FLAG_LEVEL_TIMING = 0x1
 GATSPI_FLAG_NO_GRAPH = 0x2
+GATSPI_FLAG_PULSE_PERCENT = 0x4
 
 STATUS = {
     0: "GATSPI_OK", 1: "GATSPI_EINVAL", 2: "GATSPI_ENOMEM", 3: "GATSPI_EPOOL_OVERFLOW", 4: "GATSPI_EBADWAVE",
@@ -40,7 +41,7 @@ class gatspi_netlist(ctypes.Structure):
 
 class gatspi_config(ctypes.Structure):
     _fields_ = [("num_windows", ctypes.c_int32), ("window_len", _p), ("flags", ctypes.c_uint32),
-                ("stage_words", ctypes.c_int32)]
+                ("stage_words", ctypes.c_int32), ("pulse_percent", ctypes.c_int32)]
 
 
 class gatspi_views(ctypes.Structure):
@@ -57,6 +58,7 @@ class gatspi_level_args(ctypes.Structure):
         ("pool_words", ctypes.c_int64), ("chunk_base", _p), ("wend", _p), ("tc", _p), ("t1", _p),
         ("level_base", _p), ("num_inputs", ctypes.c_int32), ("num_windows", ctypes.c_int32),
         ("gate_begin", ctypes.c_int32), ("num_gates", ctypes.c_int32), ("stage_words", ctypes.c_int32),
+        ("flags", ctypes.c_uint32), ("pulse_percent", ctypes.c_int32),
     ]
 
 

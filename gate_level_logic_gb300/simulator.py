@@ -28,11 +28,13 @@ class Simulator:
     ``net`` is any object with the netlist arrays of include/gatspi.h as attributes
     (num_inputs, num_gates, num_levels, level_offsets, gate_type, type_num_pins,
     type_tt_off, tt_data, fanin_off, fanin_net, pin_weight, wire_rise, wire_fall,
-    gate_dly_off, dly_data).
+    gate_dly_off, dly_data).  ``pulse_percent`` is PATHPULSEPERCENT, the inertial
+    reject limit of the interconnect and gate filters as a percentage of the delay
+    (100 = the GATSPI page's setting; 0 = transport delay).
     """
 
     def __init__(self, net, window_len, pool_words: int = None, pool=None, stage_words: int = -1, flags: int = 0,
-                 device: int = None):
+                 device: int = None, pulse_percent: int = 100):
         import torch
         self._torch = torch
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None else device)
@@ -64,7 +66,11 @@ class Simulator:
             keep["fanin_off"].ctypes.data, keep["fanin_net"].ctypes.data, keep["pin_weight"].ctypes.data,
             keep["wire_rise"].ctypes.data, keep["wire_fall"].ctypes.data, keep["gate_dly_off"].ctypes.data,
             keep["dly_data"].size, keep["dly_data"].ctypes.data)
-        cfg = _c.gatspi_config(self.num_windows, keep["window_len"].ctypes.data, int(flags), int(stage_words))
+        if int(pulse_percent) != 100:
+            flags = int(flags) | _c.GATSPI_FLAG_PULSE_PERCENT
+        cfg = _c.gatspi_config(self.num_windows, keep["window_len"].ctypes.data, int(flags), int(stage_words),
+                               int(pulse_percent))
+        self.pulse_percent = int(pulse_percent)
         with torch.cuda.device(self.device):
             self.ctx = _c.gatspi_create(nl, cfg, self.pool.data_ptr(), self.pool.numel())
         self.window_len = wl

@@ -15,6 +15,16 @@
  *     resolution, delay selection and gate inertial filtering with
  *     PATHPULSEPERCENT = 100.  The page sizes every output with a first counting
  *     pass; here an upper bound computed from the input lengths takes its place.
+ *   - Section 3, the prose after Algorithm 1: other PATHPULSEPERCENT values come
+ *     from editing the filter comparison.  With GATSPI_FLAG_PULSE_PERCENT and a
+ *     percentage q, the delay d in both inertial comparisons (the interconnect
+ *     pulse test and the gate filter) becomes the reject limit floor(d * q / 100):
+ *     a fanin pulse narrower than the limit of its first edge's wire delay never
+ *     reaches the pin, and the last output entry is cancelled when the new output
+ *     time minus that entry is below the limit of the new event's delay.  Below
+ *     100 several output events can be pending; a cancel exposes the entry before
+ *     it.  q = 0 is transport delay: nothing is filtered, and only an output
+ *     event scheduled before the last scheduled one replaces it.
  *
  * Conventions for every call:
  *   - every call returns a gatspi_status; nothing throws across this ABI, nothing
@@ -72,6 +82,7 @@ enum { GATSPI_HOST = 0, GATSPI_DEVICE = 1 };
 /* gatspi_config.flags */
 #define GATSPI_FLAG_LEVEL_TIMING 0x1u  /* record CUDA events around every level kernel (no graph) */
 #define GATSPI_FLAG_NO_GRAPH 0x2u      /* launch level kernels directly, no CUDA graph  */
+#define GATSPI_FLAG_PULSE_PERCENT 0x4u /* apply pulse_percent (else PATHPULSEPERCENT = 100) */
 
 /*
  * Levelised netlist (all host arrays, copied by gatspi_create).
@@ -134,12 +145,15 @@ typedef struct {
  *                 slot as long as the window's own bound) and moved to their final
  *                 place once the lengths of the chunk's windows are known; every
  *                 (gate, window) is simulated exactly once whatever the value.
+ *   pulse_percent PATHPULSEPERCENT q, 0 .. 100, read only with
+ *                 GATSPI_FLAG_PULSE_PERCENT (a zeroed config means 100).
  */
 typedef struct {
     int32_t num_windows;
     const int64_t *window_len;
     uint32_t flags;
     int32_t stage_words;
+    int32_t pulse_percent;
 } gatspi_config;
 
 typedef struct gatspi_ctx gatspi_ctx;
@@ -280,6 +294,9 @@ gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *sim_ms, float *bounds_m
  *   tc, t1      per-gate toggle count and time at 1, accumulated (not cleared)
  *   level_base  int64 [2]: [0] = first pool word of this level's outputs (read),
  *               [1] = one past its last word (written)
+ *   flags, pulse_percent
+ *               GATSPI_FLAG_PULSE_PERCENT selects pulse_percent as in gatspi_config
+ *               (other flags are ignored); zeroed fields mean PATHPULSEPERCENT = 100
  */
 typedef struct {
     const int32_t *gate_desc;
@@ -298,6 +315,8 @@ typedef struct {
     int32_t gate_begin;   /* first gate of the level */
     int32_t num_gates;    /* gates in the level */
     int32_t stage_words;  /* as in gatspi_config */
+    uint32_t flags;
+    int32_t pulse_percent;
 } gatspi_level_args;
 
 /*

@@ -97,6 +97,13 @@ def test_invalid_config_and_pool_are_rejected(lib):
     assert _create_status(lib, nl, cfg, words=1023)[0] == 1         # not a multiple of 4 words
     cfg.num_windows = 0
     assert _create_status(lib, nl, cfg)[0] == 1
+    # PATHPULSEPERCENT outside 0 .. 100, when the flag selects it
+    for q in (-1, 101):
+        nl, cfg, keep = _struct(lib, net, W=1)
+        cfg.flags = lib.GATSPI_FLAG_PULSE_PERCENT
+        cfg.pulse_percent = q
+        rc, msg = _create_status(lib, nl, cfg)
+        assert rc == 1 and "pulse_percent" in msg, (rc, msg)
 
 
 def test_status_names(lib):

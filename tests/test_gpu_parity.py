@@ -31,9 +31,10 @@ def gpu():
     return Simulator
 
 
-def run_gpu(Simulator, net, stim, pool_words, stage_words=-1, flags=0, repeat=1):
+def run_gpu(Simulator, net, stim, pool_words, stage_words=-1, flags=0, repeat=1, pulse_percent=100):
     """Simulate; return every waveform gathered gap-free (CSR, net-major) + statistics."""
-    with Simulator(net, stim.window_len, pool_words=pool_words, stage_words=stage_words, flags=flags) as sim:
+    with Simulator(net, stim.window_len, pool_words=pool_words, stage_words=stage_words, flags=flags,
+                   pulse_percent=pulse_percent) as sim:
         sim.load(stim.pi_off, stim.pi_words)
         for _ in range(repeat):
             sim.simulate()
@@ -77,7 +78,7 @@ def test_50k_full(gpu, oracle_lib):
 
 @pytest.mark.parametrize("stage_words,flags", [(0, 0), (1, 0), (3, 0), (8, 0), (64, 0), (24, 2)])
 def test_50k_staging_and_launch_variants(gpu, oracle_lib, stage_words, flags):
-    """stage 0 is the count-then-write scheme for every lane; other sizes mix both."""
+    """stage 0 sends every output word to the provisional slot; other sizes mix both."""
     net, stim = synth.make("50k")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
     assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=stage_words, flags=flags), ref,
@@ -267,3 +268,39 @@ def test_1M_sweep_points_sampled(gpu, oracle_lib, activity, W):
     net, stim = synth.sweep(activity, W)
     windows = [0] if W == 1 else [0, W // 2 + 1, W - 1]
     _sampled(gpu, oracle_lib, net, stim, windows, pool_words=40 << 30)
+
+
+# ---- PATHPULSEPERCENT below 100 (several pending output events; transport at 0) ----
+
+@pytest.mark.parametrize("q", [0, 35, 70, 99])
+def test_pulse_percent_random_small(gpu, oracle_lib, q):
+    """The seeded corner-heavy cases at other pulse limits; staging 0 and 2 make the
+    re-read of an exposed entry come from the pool, 24 from shared memory."""
+    import test_oracle_pins as pins
+    for seed in range(40):
+        net, stim = pins._random_case(seed)
+        ref = oracle_lib.simulate(net, stim, pulse_percent=q)
+        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=(0, 2, 24)[seed % 3], pulse_percent=q),
+                    ref, "q=%d seed %d" % (q, seed))
+
+
+@pytest.mark.parametrize("q,stage_words", [(0, -1), (50, -1), (50, 0), (80, 3)])
+def test_pulse_percent_50k(gpu, oracle_lib, q, stage_words):
+    net, stim = synth.make("50k")
+    ref = oracle_lib.simulate(net, stim, threads=THREADS, pulse_percent=q)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=stage_words, pulse_percent=q), ref,
+                "q=%d stage=%d" % (q, stage_words))
+    if q == 0:     # transport delay lets every pulse through: more toggles than the inertial default
+        assert ref.tc.sum() > oracle_lib.simulate(net, stim, threads=THREADS).tc.sum()
+
+
+@pytest.mark.parametrize("W", [5, 32, 70])
+def test_pulse_percent_window_counts(gpu, oracle_lib, W):
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=2500, num_inputs=29, num_levels=8, seed=100 + W,
+                                                   cond_fraction=0.4))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=29, cycles=max(W, 200), period=400,
+                                                      activity=0.3, windows=W, seed=W, glitch_frac=0.4))
+    for q in (10, 60):
+        ref = oracle_lib.simulate(net, stim, threads=THREADS, pulse_percent=q)
+        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=4, pulse_percent=q), ref,
+                    "q=%d W=%d" % (q, W))

@@ -43,7 +43,7 @@ def _pack(net):
 class Caller:
     """Owns every buffer; runs levels through the allocation-free entry point."""
 
-    def __init__(self, net, stim, pool_words, stage_words=-1):
+    def __init__(self, net, stim, pool_words, stage_words=-1, pulse_percent=100):
         import torch
         from gate_level_logic_gb300 import gatspi
         self.gatspi, self.torch = gatspi, torch
@@ -63,6 +63,7 @@ class Caller:
         self.t1 = torch.zeros(G, dtype=torch.int64, device=dev)
         self.level_base = torch.zeros(2, dtype=torch.int64, device=dev)
         self.stage_words = stage_words
+        self.pulse_percent = pulse_percent
         # input waveforms at the front of the pool, with their window index
         off = stim.pi_off
         nw = int(off[-1])
@@ -80,7 +81,8 @@ class Caller:
             self.gate_desc.data_ptr(), self.edge_desc.data_ptr(), self.dly.data_ptr(), self.window_len.data_ptr(),
             self.pool.data_ptr(), self.pool.numel() if pool_words is None else pool_words,
             self.chunk_base.data_ptr(), self.wend.data_ptr(), self.tc.data_ptr(), self.t1.data_ptr(),
-            self.level_base.data_ptr(), self.net.num_inputs, self.W, gate_begin, num_gates, self.stage_words)
+            self.level_base.data_ptr(), self.net.num_inputs, self.W, gate_begin, num_gates, self.stage_words,
+            g.GATSPI_FLAG_PULSE_PERCENT, self.pulse_percent)
 
     def run(self):
         """Every level, in order; returns (offsets, pool, tc, t1) as host arrays."""
@@ -104,9 +106,9 @@ class Caller:
         return (start, length, base), self.pool[:base].cpu().numpy(), self.tc.cpu().numpy(), self.t1.cpu().numpy()
 
 
-def _regular(net, stim, pool_words):
+def _regular(net, stim, pool_words, pulse_percent=100):
     from gate_level_logic_gb300 import Simulator
-    with Simulator(net, stim.window_len, pool_words=pool_words) as sim:
+    with Simulator(net, stim.window_len, pool_words=pool_words, pulse_percent=pulse_percent) as sim:
         sim.load(stim.pi_off, stim.pi_words)
         sim.simulate()
         tc, _, t1 = sim.toggle_stats()
@@ -137,12 +139,12 @@ def built():
     build.build()
 
 
-@pytest.mark.parametrize("name", ["tiny", "50k"])
-def test_static_levels_match_regular_path(built, name):
+@pytest.mark.parametrize("name,q", [("tiny", 100), ("50k", 100), ("tiny", 30)])
+def test_static_levels_match_regular_path(built, name, q):
     net, stim = synth.make(name)
     pool_words = 1 << 26            # room for the bound-sized output regions of every level
-    ref = _regular(net, stim, pool_words)
-    caller = Caller(net, stim, pool_words)
+    ref = _regular(net, stim, pool_words, pulse_percent=q)
+    caller = Caller(net, stim, pool_words, pulse_percent=q)
     for attempt in range(2):                        # two runs in a row share the scratch
         index, pool, tc, t1 = caller.run()
         assert _same_index(index, ref[0]), "waveform positions differ (run %d)" % attempt
