@@ -12,6 +12,9 @@ Two independent CPU simulators, both plain C compiled with gcc:
 * ``bruteforce`` -- a unit-time-step simulator of inertial wire and gate
   elements, used to pin ``simulate`` on tiny netlists.
 
+And the testbench restructuring: ``restructure`` cuts whole-testbench input
+waveforms into the cycle windows (GATSPI page, Sections 1, 4 and 5).
+
 Both return the same layout: CSR offsets over every (net, window) waveform,
 net-major and window-minor, into a pool that holds the input waveforms followed by
 the gate outputs; plus per-gate toggle counts TC and time-at-1 T1 summed over
@@ -28,7 +31,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
-_SOURCES = ("gatspi_oracle.c", "bruteforce.c")
+_SOURCES = ("gatspi_oracle.c", "bruteforce.c", "testbench.c")
 _libs = {}
 
 
@@ -77,6 +80,10 @@ def _load(path=None):
                                              ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_char_p, ctypes.c_int]
         lib.brute_simulate.restype = ctypes.c_int
+        lib.oracle_restructure.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
+                                           ctypes.POINTER(ctypes.c_int64), ctypes.c_char_p, ctypes.c_int]
+        lib.oracle_restructure.restype = ctypes.c_int
         lib.oracle_free.argtypes = [ctypes.c_void_p]
         lib.oracle_free.restype = None
         _libs[path] = lib
@@ -176,3 +183,27 @@ def bruteforce(net, stim, lib_path: str = None, pulse_percent: int = 100) -> Res
                             keep["pi_words"].ctypes.data, int(pulse_percent), off.ctypes.data, ctypes.byref(pool_ptr),
                             ctypes.byref(pool_words), tc.ctypes.data, t1.ctypes.data, err, 512)
     return _finish(lib, rc, err, pool_ptr, pool_words, off, tc[:net.num_gates], t1[:net.num_gates], net, stim)
+
+
+def restructure(tb_off, tb_words, window_len, lib_path: str = None):
+    """Cut whole-testbench input waveforms (CSR ``tb_off[P+1]`` over ``tb_words``) into
+    windows of ``window_len`` time units.  Returns ``(off, words)``: CSR offsets over the
+    (input, window) waveforms, input-major and window-minor, and their words."""
+    lib = _load(lib_path)
+    tb_off = _c(tb_off, np.int64)
+    tb_words = _c(tb_words, np.int32)
+    wl = _c(window_len, np.int64).reshape(-1)
+    P, W = tb_off.size - 1, wl.size
+    off = np.zeros(P * W + 1, dtype=np.int64)
+    ptr, n = ctypes.c_void_p(), ctypes.c_int64()
+    err = ctypes.create_string_buffer(512)
+    rc = lib.oracle_restructure(P, tb_off.ctypes.data, tb_words.ctypes.data, W, wl.ctypes.data, off.ctypes.data,
+                                ctypes.byref(ptr), ctypes.byref(n), err, 512)
+    if rc != 0:
+        raise OracleError(rc, err.value.decode(errors="replace"))
+    try:
+        buf = (ctypes.c_int32 * max(int(n.value), 1)).from_address(ptr.value)
+        words = np.frombuffer(buf, dtype=np.int32, count=int(n.value)).copy()
+    finally:
+        lib.oracle_free(ptr)
+    return off, words

@@ -5,5 +5,6 @@ their inputs from these generators.
 """
 from .cells import CELL_MIX, SCAN_MIX, truth_table  # noqa: F401
 from .netlist import INF, Netlist, NetlistSpec, build_netlist, generate_netlist, possible_rows  # noqa: F401
-from .stimulus import EOW, Stimulus, StimulusSpec, from_waveforms, generate_stimulus, select_windows  # noqa: F401
-from .workloads import WORKLOADS, make, sweep  # noqa: F401
+from .stimulus import (EOW, Stimulus, StimulusSpec, Testbench, from_waveforms, generate_stimulus,  # noqa: F401
+                       generate_testbench, select_windows)
+from .workloads import WORKLOADS, make, sweep, testbench  # noqa: F401

@@ -62,7 +62,9 @@ def window_cycles(cycles: int, windows: int) -> np.ndarray:
     return wc
 
 
-def generate_stimulus(spec: StimulusSpec) -> Stimulus:
+def _draw_edges(spec: StimulusSpec):
+    """The seeded input edges: initial values and (input, cycle, offset) of every edge,
+    sorted by input, then time."""
     rng = np.random.default_rng(spec.seed)
     P, C, T, W = spec.num_inputs, spec.cycles, spec.period, spec.windows
     if W < 1 or W > C:
@@ -100,7 +102,12 @@ def generate_stimulus(spec: StimulusSpec) -> Stimulus:
     e_cyc = np.concatenate([cyc, cyc[glitch]])
     e_off = np.concatenate([off1, off2[glitch]])
     order = np.lexsort((e_off, e_cyc, e_pi))
-    e_pi, e_cyc, e_off = e_pi[order], e_cyc[order], e_off[order]
+    return init, e_pi[order], e_cyc[order], e_off[order], n_tog, int(glitch.sum())
+
+
+def generate_stimulus(spec: StimulusSpec) -> Stimulus:
+    P, C, T, W = spec.num_inputs, spec.cycles, spec.period, spec.windows
+    init, e_pi, e_cyc, e_off, n_tog, n_glitch = _draw_edges(spec)
 
     wc = window_cycles(C, W)
     wstart = np.concatenate(([0], np.cumsum(wc)))          # first cycle of each window
@@ -133,7 +140,7 @@ def generate_stimulus(spec: StimulusSpec) -> Stimulus:
 
     stats = {
         "toggles": int(n_tog),
-        "glitch_pairs": int(glitch.sum()),
+        "glitch_pairs": n_glitch,
         "edges": int(e_pi.size),
         "words": int(words.size),
     }
@@ -167,3 +174,45 @@ def from_waveforms(waves, window_len) -> Stimulus:
         wl = np.repeat(wl, W)
     return Stimulus(num_inputs=P, num_windows=W, window_len=wl, window_cycles=np.zeros(W, dtype=np.int64),
                     pi_off=off, pi_words=np.concatenate(flat) if flat else np.zeros(0, np.int32), stats={})
+
+
+@dataclass
+class Testbench:
+    """Whole-testbench input waveforms, before the cut into cycle windows: one Fig. 3
+    array per input with times from the start of the testbench, and the lengths of
+    the windows it is to be cut into (window w starts at the sum of the lengths of
+    the windows before it)."""
+    num_inputs: int
+    num_windows: int
+    window_len: np.ndarray     # int64 [W]
+    window_cycles: np.ndarray  # int64 [W]
+    off: np.ndarray            # int64 [P + 1]
+    words: np.ndarray          # int32
+
+    def wave(self, pi: int) -> np.ndarray:
+        return self.words[self.off[pi]:self.off[pi + 1]]
+
+
+def generate_testbench(spec: StimulusSpec) -> Testbench:
+    """The edges generate_stimulus draws for the same spec, as one waveform per input
+    over the whole testbench (absolute times cycle * period + offset)."""
+    P, C, T, W = spec.num_inputs, spec.cycles, spec.period, spec.windows
+    init, e_pi, e_cyc, e_off, _, _ = _draw_edges(spec)
+    if C * T >= 2**31 - 1:
+        raise ValueError("testbench longer than the int32 time range")
+    cnt = np.bincount(e_pi, minlength=P)
+    length = 1 + init + cnt + 1
+    off = np.zeros(P + 1, dtype=np.int64)
+    off[1:] = np.cumsum(length)
+    words = np.empty(int(off[-1]), dtype=np.int32)
+    s1 = off[:-1][init == 1]
+    words[s1] = -1
+    words[s1 + 1] = 0
+    words[off[:-1][init == 0]] = 0
+    first = np.zeros(P + 1, dtype=np.int64)
+    first[1:] = np.cumsum(cnt)
+    rank = np.arange(e_pi.size) - first[e_pi]
+    words[(off[:-1] + 1 + init)[e_pi] + rank] = (e_cyc * T + e_off).astype(np.int32)
+    words[off[1:] - 1] = EOW
+    wc = window_cycles(C, W)
+    return Testbench(num_inputs=P, num_windows=W, window_len=wc * T, window_cycles=wc, off=off, words=words)

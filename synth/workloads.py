@@ -8,7 +8,7 @@ from __future__ import annotations
 
 from .cells import CELL_MIX, SCAN_MIX
 from .netlist import NetlistSpec, generate_netlist
-from .stimulus import StimulusSpec, generate_stimulus
+from .stimulus import StimulusSpec, generate_stimulus, generate_testbench
 
 # name -> (netlist spec kwargs, stimulus spec kwargs)
 WORKLOADS = {
@@ -66,6 +66,14 @@ def make(name: str, **overrides):
     net = generate_netlist(NetlistSpec(**net_kw))
     stim = generate_stimulus(StimulusSpec(**stim_kw))
     return net, stim
+
+
+def testbench(name: str, **overrides):
+    """The named workload's stimulus before the cut into windows (the same seeded edges
+    as ``make``), for the testbench-restructuring path."""
+    _, stim_kw = (dict(d) for d in WORKLOADS[name])
+    stim_kw.update({k: v for k, v in overrides.items() if not k.startswith("net_")})
+    return generate_testbench(StimulusSpec(**stim_kw))
 
 
 def sweep(activity: float, windows: int):

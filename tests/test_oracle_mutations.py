@@ -110,16 +110,16 @@ def _battery(lib_path):
     return True
 
 
-def _build_variant(tmp_path, old, new):
+def _build_variant(tmp_path, old, new, target="gatspi_oracle.c"):
     d = tmp_path / "src"
     d.mkdir()
-    for f in ("gatspi_oracle.c", "bruteforce.c", "oracle_abi.h"):
+    for f in ("gatspi_oracle.c", "bruteforce.c", "testbench.c", "oracle_abi.h"):
         shutil.copy(os.path.join(SRC, f), d / f)
-    text = (d / "gatspi_oracle.c").read_text()
+    text = (d / target).read_text()
     if old is not None:
         assert text.count(old) == 1, "mutation anchor not found exactly once: %r" % old
         text = text.replace(old, new)
-    (d / "gatspi_oracle.c").write_text(text)
+    (d / target).write_text(text)
     return oracle.build(force=True, src_dir=str(d), out=str(tmp_path / "libvariant.so"))
 
 
@@ -131,3 +131,49 @@ def test_unmutated_copy_passes(tmp_path):
 def test_mutant_is_caught(tmp_path, name):
     old, new = MUTANTS[name]
     assert not _battery(_build_variant(tmp_path, old, new)), "pins missed: " + name
+
+
+# ---- the testbench restructuring (oracle/testbench.c) ----
+
+TB_MUTANTS = {
+    "boundary transition kept in the earlier window": (
+        "while (!bad && x[i] != TB_EOW && x[i] < end) {", "while (!bad && x[i] != TB_EOW && x[i] <= end) {"),
+    "boundary transition not folded into the initial value": (
+        "while (x[i] != TB_EOW && x[i] <= start) {", "while (x[i] != TB_EOW && x[i] < start) {"),
+    "times not made window-relative": (
+        "bad = tb_push(&out, (int32_t)(x[i] - start));", "bad = tb_push(&out, (int32_t)x[i]);"),
+    "window head written for the opposite value": (
+        "int bad = value ? (tb_push(&out, -1) || tb_push(&out, 0)) : tb_push(&out, 0);",
+        "int bad = !value ? (tb_push(&out, -1) || tb_push(&out, 0)) : tb_push(&out, 0);"),
+    "every window starts from the testbench's initial value": (
+        "        int64_t start = 0;\n        for (int32_t w = 0; w < W; ++w) {\n",
+        "        int64_t start = 0;\n        for (int32_t w = 0; w < W; ++w) {\n            value = (x[0] == -1);\n"),
+}
+
+
+def _tb_battery(lib_path):
+    import test_oracle_testbench as tbt
+    shim = types.SimpleNamespace(restructure=functools.partial(oracle.restructure, lib_path=lib_path),
+                                 OracleError=oracle.OracleError)
+    checks = [lambda: tbt.test_restructure_equals_generator_windows(shim),
+              lambda: tbt.test_boundary_transitions_fold_into_the_later_window(shim),
+              lambda: tbt.test_initial_one_and_quiet_windows(shim),
+              lambda: tbt.test_uneven_windows(shim),
+              lambda: tbt.test_single_window_is_identity(shim)]
+    checks += [functools.partial(tbt.test_windows_put_back_give_the_testbench, shim, seed) for seed in range(3)]
+    for c in checks:
+        try:
+            c()
+        except (AssertionError, oracle.OracleError):
+            return False
+    return True
+
+
+def test_unmutated_testbench_copy_passes(tmp_path):
+    assert _tb_battery(_build_variant(tmp_path, None, None, "testbench.c"))
+
+
+@pytest.mark.parametrize("name", sorted(TB_MUTANTS))
+def test_testbench_mutant_is_caught(tmp_path, name):
+    old, new = TB_MUTANTS[name]
+    assert not _tb_battery(_build_variant(tmp_path, old, new, "testbench.c")), "pins missed: " + name
