@@ -1,6 +1,6 @@
 """Build the CUDA library ``libgatspi.so`` in-tree for sm_103a (GB300).
 
-Two translation units compiled in parallel with nvcc, then linked into one shared
+The translation units are compiled in parallel with nvcc, then linked into one shared
 library (CUDA runtime linked statically).  Objects go to ``_build/``.
 """
 from __future__ import annotations
@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgatspi.so")
-SOURCES = ("gatspi.cu", "level_kernel.cu", "gatspi_static.cu")
+SOURCES = ("gatspi.cu", "level_kernel.cu", "gatspi_static.cu", "testbench.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "gatspi_internal.cuh"
+#include "testbench.cuh"
 
 using namespace gatspi;
 
@@ -76,6 +77,7 @@ struct gatspi_ctx {
     int32_t *status = nullptr;
     long long *load_off = nullptr;
     int32_t *max_time = nullptr;
+    long long *win_start = nullptr;   // [W+1] start of every window on the testbench's time axis
 
     // host copies
     std::vector<int32_t> level_offsets;
@@ -83,6 +85,7 @@ struct gatspi_ctx {
     long long total_tiles = 0;
     long long sum_window_len = 0;
     long long path_delay_bound = 0;   // levels * (max wire delay + max gate delay)
+    long long max_window_len = 0;
     bool loaded = false;
     bool simulated = false;
     cudaStream_t last_stream = nullptr;
@@ -202,7 +205,8 @@ void free_all(gatspi_ctx *c) {
     if (c->capture_stream) cudaStreamDestroy(c->capture_stream);
     for (cudaEvent_t e : c->events) cudaEventDestroy(e);
     void *ptrs[] = {c->gate_desc, c->edge_desc, c->dly, c->chunk_base, c->wend, c->window_len, c->tc, c->t1,
-                    c->tile_status, c->tickets, c->level_base, c->status, c->load_off, c->max_time};
+                    c->tile_status, c->tickets, c->level_base, c->status, c->load_off, c->max_time,
+                    c->win_start};
     for (void *p : ptrs)
         if (p) cudaFree(p);
 }
@@ -371,9 +375,17 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(dev_alloc(&c->status, (size_t)kStatusWords), "allocating the status word");
         CUDA_TRY(dev_alloc(&c->load_off, (size_t)((long long)c->P * c->W + 1)), "allocating load offsets");
         CUDA_TRY(dev_alloc(&c->max_time, 1), "allocating the load scratch");
+        CUDA_TRY(dev_alloc(&c->win_start, (size_t)c->W + 1), "allocating window starts");
 
         std::vector<int32_t> wl(c->W);
-        for (int w = 0; w < c->W; ++w) wl[w] = (int32_t)cfg->window_len[w];
+        std::vector<long long> ws(c->W + 1, 0);
+        for (int w = 0; w < c->W; ++w) {
+            wl[w] = (int32_t)cfg->window_len[w];
+            ws[w + 1] = ws[w] + cfg->window_len[w];
+            c->max_window_len = std::max(c->max_window_len, (long long)cfg->window_len[w]);
+        }
+        CUDA_TRY(cudaMemcpy(c->win_start, ws.data(), ws.size() * sizeof(long long), cudaMemcpyHostToDevice),
+                 "uploading window starts");
         CUDA_TRY(cudaMemcpy(c->gate_desc, gd.data(), gd.size() * sizeof(int4), cudaMemcpyHostToDevice), "uploading gates");
         CUDA_TRY(cudaMemcpy(c->edge_desc, ed.data(), ed.size() * sizeof(int4), cudaMemcpyHostToDevice), "uploading edges");
         if (dly_len > 0)
@@ -431,6 +443,54 @@ gatspi_status gatspi_load_waveforms(gatspi_ctx *c, const int64_t *off, const int
     if ((long long)tmax + c->path_delay_bound >= (long long)GATSPI_EOW)
         return fail(GATSPI_EINVAL, "latest input time %d plus the longest path delay bound %lld reaches EOW", tmax,
                     c->path_delay_bound);
+    c->loaded = true;
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_load_testbench(gatspi_ctx *c, const int64_t *off, const int32_t *words, size_t nwords, int where,
+                                    void *stream) {
+    g_err.clear();
+    if (!c || !off || (!words && nwords)) return fail(GATSPI_EINVAL, "ctx, off and words are required");
+    if (where != GATSPI_HOST && where != GATSPI_DEVICE) return fail(GATSPI_EINVAL, "where must be HOST or DEVICE");
+    const long long P = c->P, W = c->W;
+    // the windows of input p take at most (its transitions) + 3 W words
+    const long long region = (long long)nwords + 3 * W * P;
+    const long long stage_at = where == GATSPI_HOST ? ((c->pool_words - (long long)nwords) & ~3ll) : c->pool_words;
+    if (stage_at < 0 || region > stage_at)
+        return fail(GATSPI_EPOOL_OVERFLOW,
+                    "%zu testbench words need %lld pool words for the windows%s (pool: %lld words)", nwords, region,
+                    where == GATSPI_HOST ? " plus the staged testbench" : "", c->pool_words);
+    if (where == GATSPI_HOST) {
+        if (off[0] != 0 || off[P] != (long long)nwords)
+            return fail(GATSPI_EINVAL, "off[0] must be 0 and off[num_inputs] (%lld) must equal nwords (%zu)",
+                        (long long)off[P], nwords);
+        for (long long p = 0; p < P; ++p)
+            if (off[p + 1] < off[p]) return fail(GATSPI_EINVAL, "off must be non-decreasing (input %lld)", p);
+    }
+    if (c->max_window_len - 1 + c->path_delay_bound >= (long long)GATSPI_EOW)
+        return fail(GATSPI_EINVAL, "the longest window plus the longest path delay bound %lld reaches EOW",
+                    c->path_delay_bound);
+    CUDA_TRY(cudaSetDevice(c->device), "cudaSetDevice");
+    cudaStream_t s = (cudaStream_t)stream;
+    const cudaMemcpyKind kind = where == GATSPI_HOST ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    c->loaded = false;
+    c->last_stream = s;
+    // a host testbench is staged at the far end of the pool, behind the windows' regions
+    const int32_t *tb = where == GATSPI_HOST ? c->pool + stage_at : words;
+    if (where == GATSPI_HOST && nwords)
+        CUDA_TRY(cudaMemcpyAsync(c->pool + stage_at, words, nwords * sizeof(int32_t), kind, s), "copying the testbench");
+    CUDA_TRY(cudaMemcpyAsync(c->load_off, off, (size_t)(P + 1) * sizeof(long long), kind, s),
+             "copying testbench offsets");
+    CUDA_TRY(cudaMemsetAsync(c->status, 0, sizeof(int32_t) * kStatusWords, s), "clearing the status");
+    if (P == 0) CUDA_TRY(cudaMemsetAsync(c->level_base, 0, sizeof(long long), s), "setting the first level base");
+    CUDA_TRY(launch_testbench_cut(c->params(), c->load_off, tb, (long long)nwords, c->win_start, s),
+             "cutting the testbench into windows");
+    CUDA_TRY(cudaStreamSynchronize(s), "loading the testbench");
+    int32_t st[kStatusWords];
+    CUDA_TRY(cudaMemcpy(st, c->status, sizeof st, cudaMemcpyDeviceToHost), "reading the load status");
+    if (st[0] == GATSPI_EBADWAVE)
+        return fail(GATSPI_EBADWAVE, "input %d: malformed testbench waveform or offsets", st[1]);
+    if (st[0] != 0) return read_status(c);
     c->loaded = true;
     return GATSPI_OK;
 }

@@ -67,6 +67,7 @@ SIGNATURES = {
     "gatspi_create": (ctypes.c_int, [ctypes.POINTER(gatspi_netlist), ctypes.POINTER(gatspi_config), _p, ctypes.c_size_t,
                                      ctypes.POINTER(_p)]),
     "gatspi_load_waveforms": (ctypes.c_int, [_p, _p, _p, ctypes.c_size_t, ctypes.c_int, _p]),
+    "gatspi_load_testbench": (ctypes.c_int, [_p, _p, _p, ctypes.c_size_t, ctypes.c_int, _p]),
     "gatspi_simulate": (ctypes.c_int, [_p, _p]),
     "gatspi_sync": (ctypes.c_int, [_p]),
     "gatspi_toggle_stats": (ctypes.c_int, [_p, _p, _p, _p]),
@@ -121,6 +122,10 @@ def gatspi_create(nl: gatspi_netlist, cfg: gatspi_config, d_pool: int, pool_word
 
 def gatspi_load_waveforms(ctx: int, off: int, words: int, nwords: int, where: int, stream: int = 0):
     _check(library().gatspi_load_waveforms(_p(ctx), _p(off), _p(words), nwords, where, _p(stream)))
+
+
+def gatspi_load_testbench(ctx: int, off: int, words: int, nwords: int, where: int, stream: int = 0):
+    _check(library().gatspi_load_testbench(_p(ctx), _p(off), _p(words), nwords, where, _p(stream)))
 
 
 def gatspi_simulate(ctx: int, stream: int = 0):

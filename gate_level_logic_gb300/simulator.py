@@ -111,6 +111,25 @@ class Simulator:
             off_p, words_p, n = off_a.ctypes.data, words_a.ctypes.data, words_a.size
         _c.gatspi_load_waveforms(self.ctx, off_p, words_p, n, _c.GATSPI_HOST, _stream_handle(stream))
 
+    def load_testbench(self, tb_off, tb_words, stream=None):
+        """Load whole-testbench input waveforms (one per input, times from the start of
+        the testbench) and cut them into this simulator's windows on the GPU.  Numpy
+        (host) arrays or torch tensors (host or CUDA)."""
+        torch = self._torch
+        if isinstance(tb_words, torch.Tensor) and tb_words.is_cuda:
+            off = tb_off.to(device=tb_words.device, dtype=torch.int64).contiguous()
+            words = tb_words.to(torch.int32).contiguous()
+            _c.gatspi_load_testbench(self.ctx, off.data_ptr(), words.data_ptr(), words.numel(), _c.GATSPI_DEVICE,
+                                     _stream_handle(stream))
+            return
+        if isinstance(tb_words, torch.Tensor):
+            off_a, words_a = tb_off.contiguous(), tb_words.contiguous()
+            off_p, words_p, n = off_a.data_ptr(), words_a.data_ptr(), words_a.numel()
+        else:
+            off_a, words_a = _arr(tb_off, np.int64), _arr(tb_words, np.int32)
+            off_p, words_p, n = off_a.ctypes.data, words_a.ctypes.data, words_a.size
+        _c.gatspi_load_testbench(self.ctx, off_p, words_p, n, _c.GATSPI_HOST, _stream_handle(stream))
+
     def simulate(self, stream=None):
         _c.gatspi_simulate(self.ctx, _stream_handle(stream))
 

@@ -211,6 +211,34 @@ gatspi_status gatspi_load_waveforms(gatspi_ctx *ctx, const int64_t *off, const i
                                     int where, void *stream);
 
 /*
+ * Load the inputs from whole-testbench waveforms and cut them into the windows on
+ * the device.  GATSPI re-simulates cycle windows from known input waveforms
+ * (Sections 1 and 4) and restructures its inputs into that per-window format on the
+ * host, most of its set-up time (Section 5, Table 5); this call does it on the GPU.
+ *   off    int64 [num_inputs + 1] offsets into words (off[0] = 0, off[num_inputs] =
+ *          nwords, non-decreasing)
+ *   words  int32 [nwords]: one Fig. 3 waveform per input with times from the start
+ *          of the testbench (head [0] or [-1, 0], times strictly increasing from 1,
+ *          GATSPI_EOW last)
+ *   where  GATSPI_HOST (pageable or pinned) or GATSPI_DEVICE (off and words both in
+ *          device memory, outside the first nwords + 3 * W * num_inputs words of the
+ *          pool)
+ * Window w covers [S_w, S_w + window_len[w]) of the testbench, S_w being the sum of
+ * the lengths of the windows before it.  Its waveform starts at the input's value at
+ * S_w (a transition exactly at S_w folds into it) and holds the transitions inside
+ * the window minus S_w; transitions at or after the end of the last window belong
+ * to no window.  The windows of input p go to a region of the pool bounded by its
+ * transitions + 3 * W words (gaps between regions, as for gate outputs); a host
+ * testbench is first staged at the far end of the pool.  Synchronises `stream`
+ * before returning: EBADWAVE names the first malformed input; EPOOL_OVERFLOW when
+ * nwords + 3 * W * num_inputs words (plus nwords staged, from the host) exceed the
+ * pool; EINVAL for bad offsets or when the longest window plus the longest path
+ * could carry a timestamp to EOW.  Replaces gatspi_load_waveforms for the run.
+ */
+gatspi_status gatspi_load_testbench(gatspi_ctx *ctx, const int64_t *off, const int32_t *words, size_t nwords,
+                                    int where, void *stream);
+
+/*
  * Re-simulate every level, in order, on `stream` (a cudaStream_t; NULL = legacy
  * default stream).  Asynchronous: returns after enqueueing.  Clears TC/T1 and the
  * device status first.  Per level two kernels run: the first sizes the output

@@ -34,6 +34,8 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         assert hasattr(raw, n), n
     assert set(names) == set(lib.SIGNATURES), "binding and header disagree"
+    for n in names:
+        assert callable(getattr(lib, n, None)), "no Python wrapper for " + n
 
 
 def _struct(lib, net, W=1, stage=-1):
