@@ -6,15 +6,17 @@ and the TC/T1 reduction) with the input waveforms already resident in HBM.
 
 Prints one JSON line (rank 0):
   value      output toggle events per second over device time (sum of TC / time)
-  e2e        the same metric through the C ABI with host buffers: H2D of the input
-             waveforms, simulate, D2H of the toggle statistics, every step
+  e2e        the same metric through the C ABI with host buffers, every step: H2D of
+             the whole-testbench input waveforms, their cut into cycle windows on the
+             GPU, simulate, D2H of the toggle statistics (and, for comparison, the same
+             with windows cut on the host beforehand)
   roofline   the level kernel against the measured HBM copy bandwidth, on
              algorithmic bytes (each consumed waveform read once, each output
              written once, window index read and written once, descriptors once)
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
 
-``--impl reference`` times the CPU oracle instead (the reference arm of this
-build: a plain serial event-driven simulator), on a bounded sample per step.
+``--impl reference`` times the CPU oracle instead (a plain event-driven simulator,
+windows spread over the host cores), on a bounded sample per step.
 Under torchrun every rank runs its own replica of the workload (replicas only:
 the method needs no exchange between GPUs); rank 0 prints the aggregate.
 """
@@ -253,16 +255,20 @@ def run_reference(args):
     return 0
 
 
-def _e2e(args, sim, stim, net, stream, dist, events_per_step):
+def _e2e(args, sim, inputs, net, stream, dist, events_per_step, testbench):
+    """Same metric through the public API with host buffers: every step copies the
+    inputs in (and, with ``testbench``, cuts the whole-testbench waveforms into windows
+    on the GPU), simulates and reads the statistics back."""
     import torch
-    pin_off = torch.from_numpy(np.ascontiguousarray(stim.pi_off, np.int64)).pin_memory()
-    pin_words = torch.from_numpy(np.ascontiguousarray(stim.pi_words, np.int32)).pin_memory()
+    pin_off = torch.from_numpy(np.ascontiguousarray(inputs[0], np.int64)).pin_memory()
+    pin_words = torch.from_numpy(np.ascontiguousarray(inputs[1], np.int32)).pin_memory()
+    load = sim.load_testbench if testbench else sim.load
     e2e_steps = max(1, args.steps)
     _barrier(dist)
     torch.cuda.synchronize()
     t = time.perf_counter()
     for _ in range(e2e_steps):
-        sim.load(pin_off, pin_words, stream=stream)
+        load(pin_off, pin_words, stream=stream)
         sim.simulate(stream=stream)
         tc_e, _, t1_e = sim.toggle_stats()
     torch.cuda.synchronize()
@@ -273,6 +279,35 @@ def _e2e(args, sim, stim, net, stream, dist, events_per_step):
     d2h = 2 * 8 * net.num_gates + 16       # TC and T1 per gate, status word
 
     return e2e_value, h2d, d2h
+
+
+def _testbench_cut(args, sim, tb, stream, with_oracle):
+    """Time the device-side cut of the whole-testbench waveforms into windows
+    (gatspi_load_testbench from device memory: format check + cut + window index),
+    and, for scale, the oracle's host cut of the same testbench on one core."""
+    import torch
+    d_off = torch.from_numpy(np.ascontiguousarray(tb.off, np.int64)).cuda()
+    d_words = torch.from_numpy(np.ascontiguousarray(tb.words, np.int32)).cuda()
+    for _ in range(3):
+        sim.load_testbench(d_off, d_words, stream=stream)
+    reps = 20
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(reps):
+        sim.load_testbench(d_off, d_words, stream=stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / reps
+    out = {"gpu_ms": ms, "testbench_words": int(tb.words.size), "note": "per call, host synchronisation included"}
+    if with_oracle:
+        import oracle
+        oracle.build()
+        t = time.perf_counter()
+        _, words = oracle.restructure(tb.off, tb.words, tb.window_len)
+        out["oracle_cpu_ms"] = 1e3 * (time.perf_counter() - t)
+        out["window_words"] = int(words.size)
+    return out
 
 
 def run_gpu(args):
@@ -348,9 +383,12 @@ def run_gpu(args):
 
     # ---- end to end through the C ABI: host buffers, copies inside the region ---
     if args.no_e2e:
-        e2e_value, h2d, d2h = None, 0, 0
+        e2e_value, h2d, d2h, e2e_win, cut = None, 0, 0, None, None
     else:
-        e2e_value, h2d, d2h = _e2e(args, sim, stim, net, stream, dist, events_per_step)
+        tb = synth.testbench(WORKLOAD, **over)
+        e2e_value, h2d, d2h = _e2e(args, sim, (tb.off, tb.words), net, stream, dist, events_per_step, True)
+        e2e_win = _e2e(args, sim, (stim.pi_off, stim.pi_words), net, stream, dist, events_per_step, False)
+        cut = _testbench_cut(args, sim, tb, stream, rank == 0 and not args.no_cpu_baseline)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -370,8 +408,13 @@ def run_gpu(args):
             "share_of_step": float(level_ms.sum() / (total_s * 1e3)),
             "bounds_kernel_avg_ms": float(bounds_ms.sum() / (args.steps * net.num_levels)),
         },
-        "e2e": None if e2e_value is None else {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                                               "d2h_bytes_per_step": int(d2h)},
+        "e2e": None if e2e_value is None else {
+            "value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "path": "gatspi_load_testbench (whole-testbench waveforms from pinned host memory, cut into windows "
+                    "on the GPU) + gatspi_simulate + gatspi_toggle_stats",
+            "windowed_inputs": {"value": e2e_win[0], "h2d_bytes_per_step": int(e2e_win[1]),
+                                "path": "gatspi_load_waveforms (host-cut windows) + simulate + toggle_stats"}},
+        "testbench_cut": cut,
         "gpu_launches": int(args.steps * net.num_levels * 2),   # bounds + simulation kernel per level
         "clocks": clocks.summary(),
     }
