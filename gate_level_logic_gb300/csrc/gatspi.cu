@@ -78,6 +78,8 @@ struct gatspi_ctx {
     long long *load_off = nullptr;
     int32_t *max_time = nullptr;
     long long *win_start = nullptr;   // [W+1] start of every window on the testbench's time axis
+    unsigned long long *tc_in = nullptr, *t1_in = nullptr;   // [P] input statistics of the last load
+    std::vector<unsigned long long> tc_in_host, t1_in_host;
 
     // host copies
     std::vector<int32_t> level_offsets;
@@ -89,6 +91,12 @@ struct gatspi_ctx {
     bool loaded = false;
     bool simulated = false;
     cudaStream_t last_stream = nullptr;
+
+    // TC/T1 copied to pinned host memory level by level while later levels run
+    unsigned long long *tc_host = nullptr, *t1_host = nullptr;
+    cudaStream_t dump_stream = nullptr;
+    std::vector<cudaEvent_t> dump_events;   // [L] after each level's simulation kernel
+    cudaEvent_t dump_done = nullptr;
 
     // replayed level sequence
     cudaGraph_t graph = nullptr;
@@ -204,9 +212,14 @@ void free_all(gatspi_ctx *c) {
     if (c->graph) cudaGraphDestroy(c->graph);
     if (c->capture_stream) cudaStreamDestroy(c->capture_stream);
     for (cudaEvent_t e : c->events) cudaEventDestroy(e);
+    for (cudaEvent_t e : c->dump_events) cudaEventDestroy(e);
+    if (c->dump_done) cudaEventDestroy(c->dump_done);
+    if (c->dump_stream) cudaStreamDestroy(c->dump_stream);
+    if (c->tc_host) cudaFreeHost(c->tc_host);
+    if (c->t1_host) cudaFreeHost(c->t1_host);
     void *ptrs[] = {c->gate_desc, c->edge_desc, c->dly, c->chunk_base, c->wend, c->window_len, c->tc, c->t1,
                     c->tile_status, c->tickets, c->level_base, c->status, c->load_off, c->max_time,
-                    c->win_start};
+                    c->win_start, c->tc_in, c->t1_in};
     for (void *p : ptrs)
         if (p) cudaFree(p);
 }
@@ -235,6 +248,21 @@ gatspi_status sync_ctx(gatspi_ctx *c) {
     return read_status(c);
 }
 
+// Statistics of the loaded inputs (their window index has been checked): computed on
+// the device, kept on the host.
+gatspi_status input_stats(gatspi_ctx *c, cudaStream_t s) {
+    c->tc_in_host.assign(c->P, 0);
+    c->t1_in_host.assign(c->P, 0);
+    if (c->P == 0) return GATSPI_OK;
+    CUDA_TRY(launch_input_stats(c->params(), c->tc_in, c->t1_in, s), "input statistics");
+    CUDA_TRY(cudaStreamSynchronize(s), "input statistics");
+    CUDA_TRY(cudaMemcpy(c->tc_in_host.data(), c->tc_in, sizeof(unsigned long long) * c->P, cudaMemcpyDeviceToHost),
+             "reading input statistics");
+    CUDA_TRY(cudaMemcpy(c->t1_in_host.data(), c->t1_in, sizeof(unsigned long long) * c->P, cudaMemcpyDeviceToHost),
+             "reading input statistics");
+    return GATSPI_OK;
+}
+
 // Enqueue the whole level sequence on stream s.
 gatspi_status enqueue_levels(gatspi_ctx *c, cudaStream_t s) {
     CUDA_TRY(cudaMemsetAsync(c->tc, 0, sizeof(unsigned long long) * std::max(c->G, 1), s), "clearing TC");
@@ -252,8 +280,23 @@ gatspi_status enqueue_levels(gatspi_ctx *c, cudaStream_t s) {
         CUDA_TRY(launch_level_bounds(p, c->launches[l], s), "launching a bounds kernel");
         if (timing) CUDA_TRY(cudaEventRecord(c->events[2 * l + 1], s), "recording a level event");
         CUDA_TRY(launch_level_sim(p, c->launches[l], s), "launching a level kernel");
+        // the level's TC/T1 are final: copy them out on the side stream while the
+        // next levels run
+        const long long gb = c->level_offsets[l], ng = c->level_offsets[l + 1] - gb;
+        if (ng > 0) {
+            CUDA_TRY(cudaEventRecord(c->dump_events[l], s), "recording a dump event");
+            CUDA_TRY(cudaStreamWaitEvent(c->dump_stream, c->dump_events[l], 0), "ordering the dump");
+            CUDA_TRY(cudaMemcpyAsync(c->tc_host + gb, c->tc + gb, sizeof(unsigned long long) * ng,
+                                     cudaMemcpyDeviceToHost, c->dump_stream), "dumping TC");
+            CUDA_TRY(cudaMemcpyAsync(c->t1_host + gb, c->t1 + gb, sizeof(unsigned long long) * ng,
+                                     cudaMemcpyDeviceToHost, c->dump_stream), "dumping T1");
+        }
     }
     if (timing && c->L > 0) CUDA_TRY(cudaEventRecord(c->events[2 * c->L], s), "recording a level event");
+    if (c->G > 0) {   // the stream's later work waits for the dump
+        CUDA_TRY(cudaEventRecord(c->dump_done, c->dump_stream), "recording the dump's end");
+        CUDA_TRY(cudaStreamWaitEvent(s, c->dump_done, 0), "joining the dump");
+    }
     return GATSPI_OK;
 }
 
@@ -376,6 +419,8 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(dev_alloc(&c->load_off, (size_t)((long long)c->P * c->W + 1)), "allocating load offsets");
         CUDA_TRY(dev_alloc(&c->max_time, 1), "allocating the load scratch");
         CUDA_TRY(dev_alloc(&c->win_start, (size_t)c->W + 1), "allocating window starts");
+        CUDA_TRY(dev_alloc(&c->tc_in, (size_t)std::max(c->P, 1)), "allocating input statistics");
+        CUDA_TRY(dev_alloc(&c->t1_in, (size_t)std::max(c->P, 1)), "allocating input statistics");
 
         std::vector<int32_t> wl(c->W);
         std::vector<long long> ws(c->W + 1, 0);
@@ -400,6 +445,17 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         if (c->flags & GATSPI_FLAG_LEVEL_TIMING) {
             c->events.resize(2 * c->L + 1, nullptr);
             for (auto &e : c->events) CUDA_TRY(cudaEventCreate(&e), "creating level events");
+        }
+        if (c->G > 0) {
+            CUDA_TRY(cudaHostAlloc((void **)&c->tc_host, sizeof(unsigned long long) * c->G, cudaHostAllocDefault),
+                     "allocating pinned TC");
+            CUDA_TRY(cudaHostAlloc((void **)&c->t1_host, sizeof(unsigned long long) * c->G, cudaHostAllocDefault),
+                     "allocating pinned T1");
+            CUDA_TRY(cudaStreamCreateWithFlags(&c->dump_stream, cudaStreamNonBlocking), "creating the dump stream");
+            c->dump_events.resize(c->L, nullptr);
+            for (auto &e : c->dump_events)
+                CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "creating dump events");
+            CUDA_TRY(cudaEventCreateWithFlags(&c->dump_done, cudaEventDisableTiming), "creating dump events");
         }
         return GATSPI_OK;
     }();
@@ -443,6 +499,8 @@ gatspi_status gatspi_load_waveforms(gatspi_ctx *c, const int64_t *off, const int
     if ((long long)tmax + c->path_delay_bound >= (long long)GATSPI_EOW)
         return fail(GATSPI_EINVAL, "latest input time %d plus the longest path delay bound %lld reaches EOW", tmax,
                     c->path_delay_bound);
+    gatspi_status ist = input_stats(c, s);
+    if (ist != GATSPI_OK) return ist;
     c->loaded = true;
     return GATSPI_OK;
 }
@@ -491,6 +549,8 @@ gatspi_status gatspi_load_testbench(gatspi_ctx *c, const int64_t *off, const int
     if (st[0] == GATSPI_EBADWAVE)
         return fail(GATSPI_EBADWAVE, "input %d: malformed testbench waveform or offsets", st[1]);
     if (st[0] != 0) return read_status(c);
+    gatspi_status ist = input_stats(c, s);
+    if (ist != GATSPI_OK) return ist;
     c->loaded = true;
     return GATSPI_OK;
 }
@@ -537,15 +597,65 @@ gatspi_status gatspi_toggle_stats(gatspi_ctx *c, int64_t *tc, int64_t *t0, int64
     gatspi_status st = sync_ctx(c);
     if (st != GATSPI_OK) return st;
     if (c->G == 0) return GATSPI_OK;
-    if (tc) CUDA_TRY(cudaMemcpy(tc, c->tc, sizeof(int64_t) * c->G, cudaMemcpyDeviceToHost), "reading TC");
-    if (t0 || t1) {
-        std::vector<int64_t> one(c->G);
-        CUDA_TRY(cudaMemcpy(one.data(), c->t1, sizeof(int64_t) * c->G, cudaMemcpyDeviceToHost), "reading T1");
-        for (int g = 0; g < c->G; ++g) {
-            if (t1) t1[g] = one[g];
-            if (t0) t0[g] = c->sum_window_len - one[g];
-        }
+    // simulate copied the statistics to pinned host memory level by level; the
+    // stream it ran on has finished, and with it the copies
+    if (tc) std::memcpy(tc, c->tc_host, sizeof(int64_t) * c->G);
+    for (int g = 0; g < c->G; ++g) {
+        if (t1) t1[g] = (int64_t)c->t1_host[g];
+        if (t0) t0[g] = c->sum_window_len - (int64_t)c->t1_host[g];
     }
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_input_stats(gatspi_ctx *c, int64_t *tc, int64_t *t0, int64_t *t1) {
+    g_err.clear();
+    if (!c) return fail(GATSPI_EINVAL, "ctx is NULL");
+    if (!c->loaded) return fail(GATSPI_ESTATE, "load the inputs first");
+    for (int p = 0; p < c->P; ++p) {
+        if (tc) tc[p] = (int64_t)c->tc_in_host[p];
+        if (t1) t1[p] = (int64_t)c->t1_in_host[p];
+        if (t0) t0[p] = c->sum_window_len - (int64_t)c->t1_in_host[p];
+    }
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_write_saif(gatspi_ctx *c, const char *path, const char *design, const char *timescale,
+                                const char *const *net_names) {
+    g_err.clear();
+    if (!c || !path) return fail(GATSPI_EINVAL, "ctx and path are required");
+    if (!c->loaded || !c->simulated) return fail(GATSPI_ESTATE, "simulate first");
+    gatspi_status st = sync_ctx(c);
+    if (st != GATSPI_OK) return st;
+    FILE *f = std::fopen(path, "w");
+    if (!f) return fail(GATSPI_EINVAL, "cannot open %s for writing", path);
+    const char *top = design && *design ? design : "top";
+    std::fprintf(f, "(SAIFILE\n(SAIFVERSION \"2.0\")\n(DIRECTION \"backward\")\n(DESIGN \"%s\")\n", top);
+    std::fprintf(f, "(PROGRAM_NAME \"gate_level_logic_gb300\")\n(DIVIDER / )\n(TIMESCALE %s)\n(DURATION %lld)\n",
+                 timescale && *timescale ? timescale : "1 ps", c->sum_window_len);
+    std::fprintf(f, "(INSTANCE %s\n  (NET\n", top);
+    std::string name;
+    for (long long n = 0; n < c->num_nets; ++n) {
+        name.clear();
+        if (net_names && net_names[n]) {
+            for (const char *q = net_names[n]; *q; ++q) {   // escape what is not an identifier character
+                const char ch = *q;
+                const bool plain = (ch >= 'a' && ch <= 'z') || (ch >= 'A' && ch <= 'Z') || (ch >= '0' && ch <= '9') ||
+                                   ch == '_';
+                if (!plain) name.push_back('\\');
+                name.push_back(ch);
+            }
+        } else {
+            name = "n" + std::to_string(n);
+        }
+        const bool in = n < c->P;
+        const long long tc = in ? (long long)c->tc_in_host[n] : (long long)c->tc_host[n - c->P];
+        const long long t1 = in ? (long long)c->t1_in_host[n] : (long long)c->t1_host[n - c->P];
+        std::fprintf(f, "    (%s\n      (T0 %lld) (T1 %lld) (TX 0)\n      (TC %lld) (IG 0)\n    )\n", name.c_str(),
+                     c->sum_window_len - t1, t1, tc);
+    }
+    std::fprintf(f, "  )\n)\n)\n");
+    const bool bad = std::ferror(f) != 0;
+    if (std::fclose(f) != 0 || bad) return fail(GATSPI_EINVAL, "writing %s failed", path);
     return GATSPI_OK;
 }
 

@@ -147,7 +147,54 @@ __global__ void tb_cut_kernel(const DevParams P, const long long *__restrict__ t
     if (warp == 0 && lane == 0) P.level_base[0] = (tb_off[P.num_inputs] - tb_off[0]) + 3ll * P.W * P.num_inputs;
 }
 
+// Toggle count and time at 1 of every input, summed over its windows (the inputs'
+// part of the SAIF statistics): one warp per input, a lane per window.
+__global__ void input_stats_kernel(const DevParams P, unsigned long long *__restrict__ tc,
+                                   unsigned long long *__restrict__ t1) {
+    const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= P.num_inputs) return;
+    const long long p = warp;
+    long long toggles = 0, ones = 0;
+    for (int w = lane; w < P.W; w += 32) {
+        const long long cb = P.chunk_base[p * P.nchunks + (w >> 5)];
+        const uint32_t end = P.wend[p * P.W + w];
+        const uint32_t start = (w & 31) ? P.wend[p * P.W + w - 1] : 0u;
+        const int32_t *x = P.pool + cb + start;
+        const int len = (int)(end - start);
+        const long long Lw = P.window_len[w];
+        const int h = x[0] == -1 ? 2 : 1;
+        int v = h - 1;               // value from time 0
+        long long from = 0;          // start of the current interval, clipped to Lw
+        for (int k = h; k < len - 1; ++k) {
+            const long long t = min((long long)x[k], Lw);
+            if (v) ones += t - from;
+            from = t;
+            v ^= 1;
+        }
+        if (v) ones += Lw - from;
+        toggles += len - h - 1;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        toggles += __shfl_xor_sync(0xffffffffu, toggles, o);
+        ones += __shfl_xor_sync(0xffffffffu, ones, o);
+    }
+    if (lane == 0) {
+        tc[p] = (unsigned long long)toggles;
+        t1[p] = (unsigned long long)ones;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_input_stats(const DevParams &p, unsigned long long *tc, unsigned long long *t1, cudaStream_t s) {
+    if (p.num_inputs == 0) return cudaSuccess;
+    const int threads = 256;
+    const long long warps = p.num_inputs;
+    input_stats_kernel<<<(unsigned)((warps * 32 + threads - 1) / threads), threads, 0, s>>>(p, tc, t1);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_testbench_cut(const DevParams &p, const long long *tb_off, const int32_t *tb, long long nwords,
                                  const long long *wstart, cudaStream_t s) {

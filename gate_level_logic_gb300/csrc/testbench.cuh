@@ -13,4 +13,8 @@ namespace gatspi {
 cudaError_t launch_testbench_cut(const DevParams &p, const long long *tb_off, const int32_t *tb, long long nwords,
                                  const long long *wstart, cudaStream_t s);
 
+// Toggle count and time at 1 (within each window) of every input, summed over its
+// windows, from the loaded inputs' window index: tc[num_inputs], t1[num_inputs].
+cudaError_t launch_input_stats(const DevParams &p, unsigned long long *tc, unsigned long long *t1, cudaStream_t s);
+
 }  // namespace gatspi

@@ -71,6 +71,8 @@ SIGNATURES = {
     "gatspi_simulate": (ctypes.c_int, [_p, _p]),
     "gatspi_sync": (ctypes.c_int, [_p]),
     "gatspi_toggle_stats": (ctypes.c_int, [_p, _p, _p, _p]),
+    "gatspi_input_stats": (ctypes.c_int, [_p, _p, _p, _p]),
+    "gatspi_write_saif": (ctypes.c_int, [_p, ctypes.c_char_p, ctypes.c_char_p, ctypes.c_char_p, _p]),
     "gatspi_get_waveform": (ctypes.c_int, [_p, ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_size_t,
                                            ctypes.POINTER(ctypes.c_size_t)]),
     "gatspi_export_offsets": (ctypes.c_int, [_p, _p, _p, ctypes.c_size_t]),
@@ -138,6 +140,15 @@ def gatspi_sync(ctx: int):
 
 def gatspi_toggle_stats(ctx: int, tc: int, t0: int, t1: int):
     _check(library().gatspi_toggle_stats(_p(ctx), _p(tc), _p(t0), _p(t1)))
+
+
+def gatspi_input_stats(ctx: int, tc: int, t0: int, t1: int):
+    _check(library().gatspi_input_stats(_p(ctx), _p(tc), _p(t0), _p(t1)))
+
+
+def gatspi_write_saif(ctx: int, path: str, design: str = None, timescale: str = None, net_names: int = 0):
+    enc = (lambda x: None if x is None else x.encode())
+    _check(library().gatspi_write_saif(_p(ctx), enc(path), enc(design), enc(timescale), _p(net_names)))
 
 
 def gatspi_get_waveform(ctx: int, net: int, window: int, buf: int, cap: int) -> int:

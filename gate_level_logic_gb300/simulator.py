@@ -4,6 +4,8 @@ torch streams through.  All simulation work happens in libgatspi.so.
 """
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 
 from . import gatspi as _c
@@ -150,6 +152,26 @@ class Simulator:
         buf = np.zeros(max(n, 1), np.int32)
         _c.gatspi_get_waveform(self.ctx, net, window, buf.ctypes.data, buf.size)
         return buf[:n]
+
+    def input_stats(self):
+        """(tc, t0, t1) int64 arrays [num_inputs], summed over windows."""
+        tc = np.zeros(max(self.num_inputs, 1), np.int64)
+        t0 = np.zeros_like(tc)
+        t1 = np.zeros_like(tc)
+        _c.gatspi_input_stats(self.ctx, tc.ctypes.data, t0.ctypes.data, t1.ctypes.data)
+        n = self.num_inputs
+        return tc[:n], t0[:n], t1[:n]
+
+    def write_saif(self, path, design: str = "top", timescale: str = "1 ps", net_names=None):
+        """Write every net's statistics as a SAIF 2.0 file (names: n<index> unless given)."""
+        if net_names is None:
+            _c.gatspi_write_saif(self.ctx, str(path), design, timescale, 0)
+            return
+        names = [n.encode() for n in net_names]
+        if len(names) != self.num_nets:
+            raise ValueError("need one name per net (%d)" % self.num_nets)
+        arr = (ctypes.c_char_p * len(names))(*names)
+        _c.gatspi_write_saif(self.ctx, str(path), design, timescale, ctypes.addressof(arr))
 
     def export_offsets(self):
         """(start, length) of every (net, window) waveform in the pool, net-major."""

@@ -253,6 +253,14 @@ gatspi_status gatspi_load_testbench(gatspi_ctx *ctx, const int64_t *off, const i
  */
 gatspi_status gatspi_simulate(gatspi_ctx *ctx, void *stream);
 
+/*
+ * (continuation of gatspi_simulate) After each level's simulation kernel, that
+ * level's TC and T1 are copied to pinned host memory on a side stream while the
+ * later levels run (the page dumps its statistics asynchronously as well, Section 3);
+ * `stream` waits for the copies at the end, so the statistics are on the host once
+ * the stream has finished and gatspi_toggle_stats reads no device memory.
+ */
+
 /* Wait for the last simulate / load and report a latched device error. */
 gatspi_status gatspi_sync(gatspi_ctx *ctx);
 
@@ -262,6 +270,27 @@ gatspi_status gatspi_sync(gatspi_ctx *ctx);
  * t0 + t1 = sum of window_len.  Synchronises first.
  */
 gatspi_status gatspi_toggle_stats(gatspi_ctx *ctx, int64_t *tc, int64_t *t0, int64_t *t1);
+
+/*
+ * The same statistics for the inputs, from the loaded windows (host arrays
+ * [num_inputs]; any may be NULL): computed on the device by every load.
+ */
+gatspi_status gatspi_input_stats(gatspi_ctx *ctx, int64_t *tc, int64_t *t0, int64_t *t1);
+
+/*
+ * Write the toggle statistics of every net (inputs, then gate outputs) as a SAIF 2.0
+ * file, the output format the GATSPI page produces for power analysis (Section 3,
+ * Fig. 2): (DURATION) = the sum of the window lengths; per net (T0) (T1) (TX 0)
+ * (TC) (IG 0), summed over the windows.
+ *   path       file to write (overwritten)
+ *   design     design / top instance name (NULL: "top")
+ *   timescale  the time unit of the waveforms, e.g. "1 ps" (NULL: "1 ps")
+ *   net_names  NULL (nets named n<index>) or num_inputs + num_gates C strings;
+ *              characters other than letters, digits and '_' are escaped with '\'
+ * Synchronises first.  EINVAL if the file cannot be written.
+ */
+gatspi_status gatspi_write_saif(gatspi_ctx *ctx, const char *path, const char *design, const char *timescale,
+                                const char *const *net_names);
 
 /*
  * Copy one (net, window) waveform to host memory.  *len receives its length in
