@@ -8,3 +8,4 @@ from .netlist import INF, Netlist, NetlistSpec, build_netlist, generate_netlist,
 from .stimulus import (EOW, Stimulus, StimulusSpec, Testbench, from_waveforms, generate_stimulus,  # noqa: F401
                        generate_testbench, select_windows)
 from .workloads import WORKLOADS, make, sweep, testbench  # noqa: F401
+from .sdf import SdfText, write_sdf  # noqa: F401

@@ -177,3 +177,65 @@ def test_unmutated_testbench_copy_passes(tmp_path):
 def test_testbench_mutant_is_caught(tmp_path, name):
     old, new = TB_MUTANTS[name]
     assert not _tb_battery(_build_variant(tmp_path, old, new, "testbench.c")), "pins missed: " + name
+
+
+# ---- the SDF translation (oracle/sdf.py) ----
+
+SDF_MUTANTS = {
+    "rise and fall swapped": (
+        "            table[4 * i + 2 * e_in + 0, c] = r\n            table[4 * i + 2 * e_in + 1, c] = f",
+        "            table[4 * i + 2 * e_in + 0, c] = f\n            table[4 * i + 2 * e_in + 1, c] = r"),
+    "posedge read as the falling input edge": (
+        'edges = [0] if port[0] == "posedge" else [1]', 'edges = [1] if port[0] == "posedge" else [0]'),
+    "column with the first other pin least significant": (
+        "env = {others[k]: (c >> (n - 2 - k)) & 1 for k in range(n - 1)}",
+        "env = {others[k]: (c >> k) & 1 for k in range(n - 1)}"),
+    "COND applied where it is written": (
+        "                conds.append(st)",
+        "                _iopath(tables[g], type_pins[gate_type[g]], out_pin, st[-1], _Cond(_flatten(st[1:-1])),"
+        " file_fs, unit_fs)"),
+    "first COND wins": ("        for st in conds:", "        for st in reversed(conds):"),
+    "triple gives min": ("        text = parts[1]", "        text = parts[0]"),
+    "rounding down": ("    n = int(x + Fraction(1, 2))", "    n = int(x)"),
+    "one value leaves no fall delay": (
+        "    f = _value(vals[1], file_fs, unit_fs) if len(vals) > 1 else r",
+        "    f = _value(vals[1], file_fs, unit_fs) if len(vals) > 1 else INF"),
+}
+
+
+def _sdf_variant(tmp_path, old, new):
+    import importlib.util
+    text = open(os.path.join(SRC, "sdf.py")).read()
+    if old is not None:
+        assert text.count(old) == 1, "mutation anchor not found exactly once: %r" % old
+        text = text.replace(old, new)
+    path = tmp_path / "sdf_variant.py"
+    path.write_text(text)
+    spec = importlib.util.spec_from_file_location("sdf_variant_%d" % abs(hash(str(tmp_path))), path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _sdf_battery(mod):
+    import test_oracle_sdf as ts
+    checks = [lambda: ts.test_fig4_aoi21(mod), lambda: ts.test_interconnect(mod),
+              lambda: ts.test_round_trip_tiny(mod, "1ns")]
+    checks += [functools.partial(ts.test_hand_statements, mod, name) for name in sorted(ts.HAND)]
+    checks += [functools.partial(ts.test_round_trip_conditional_cells, mod, seed) for seed in (0, 1)]
+    for c in checks:
+        try:
+            c()
+        except (AssertionError, mod.SdfError):
+            return False
+    return True
+
+
+def test_unmutated_sdf_copy_passes(tmp_path):
+    assert _sdf_battery(_sdf_variant(tmp_path, None, None))
+
+
+@pytest.mark.parametrize("name", sorted(SDF_MUTANTS))
+def test_sdf_mutant_is_caught(tmp_path, name):
+    old, new = SDF_MUTANTS[name]
+    assert not _sdf_battery(_sdf_variant(tmp_path, old, new)), "pins missed: " + name
