@@ -310,6 +310,31 @@ def _testbench_cut(args, sim, tb, stream, with_oracle):
     return out
 
 
+def _sdf_translate(with_oracle):
+    """SDF text -> delay tables: the library's translator (host code) against the
+    oracle's translation of the same text, in MB of SDF per second."""
+    import synth
+    from gate_level_logic_gb300 import sdf_annotate
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=4000, num_inputs=128, num_levels=12, seed=1,
+                                                   cond_cells=("AOI21", "MUX2", "OAI22", "NAND4"),
+                                                   cond_fraction=0.5))
+    s = synth.write_sdf(net, seed=1, file_unit="1ns")
+    args = (s.text, net.type_names, s.pin_names, net.gate_type, s.instance_names, net.fanin_off, net.gate_dly_off,
+            net.dly_data.size, 1000)
+    mb = len(s.text) / 1e6
+    t = time.perf_counter()
+    dly, _, _ = sdf_annotate(*args)
+    lib_s = time.perf_counter() - t
+    assert np.array_equal(dly, net.dly_data)
+    out = {"sdf_mb": mb, "gates": net.num_gates, "library_mb_per_s": mb / lib_s}
+    if with_oracle:
+        from oracle import sdf as osdf
+        t = time.perf_counter()
+        osdf.annotate(*args)
+        out["oracle_mb_per_s"] = mb / (time.perf_counter() - t)
+    return out
+
+
 def run_gpu(args):
     import torch
 
@@ -421,6 +446,8 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline:
         sim.close()
         line["cpu_baseline"] = cpu_baseline(net, stim, pulse_percent=args.pulse_percent)
+    if rank == 0 and not args.no_e2e:
+        line["sdf_translate"] = _sdf_translate(not args.no_cpu_baseline)
     if rank == 0:
         print(json.dumps(line))
     sim.close()

@@ -62,6 +62,14 @@ class gatspi_level_args(ctypes.Structure):
     ]
 
 
+class gatspi_sdf_design(ctypes.Structure):
+    _fields_ = [
+        ("num_types", ctypes.c_int32), ("type_names", _p), ("type_num_pins", _p), ("pin_names", _p),
+        ("out_pin", ctypes.c_char_p), ("num_gates", ctypes.c_int32), ("gate_type", _p), ("instance_names", _p),
+        ("fanin_off", _p), ("gate_dly_off", _p), ("dly_len", ctypes.c_int64), ("unit_fs", ctypes.c_int64),
+    ]
+
+
 # exported symbol -> (restype, argtypes)
 SIGNATURES = {
     "gatspi_create": (ctypes.c_int, [ctypes.POINTER(gatspi_netlist), ctypes.POINTER(gatspi_config), _p, ctypes.c_size_t,
@@ -80,6 +88,8 @@ SIGNATURES = {
     "gatspi_device_views": (ctypes.c_int, [_p, ctypes.POINTER(gatspi_views)]),
     "gatspi_level_times": (ctypes.c_int, [_p, _p, _p, ctypes.c_int32]),
     "gatspi_simulate_level_static": (ctypes.c_int, [ctypes.POINTER(gatspi_level_args), _p]),
+    "gatspi_sdf_annotate": (ctypes.c_int, [ctypes.POINTER(gatspi_sdf_design), ctypes.c_char_p, ctypes.c_size_t, _p,
+                                           _p, _p]),
     "gatspi_destroy": (None, [_p]),
     "gatspi_last_error": (ctypes.c_char_p, []),
     "gatspi_status_name": (ctypes.c_char_p, [ctypes.c_int]),
@@ -179,6 +189,12 @@ def gatspi_level_times(ctx: int, sim_ms: int, bounds_ms: int, n: int):
 
 def gatspi_simulate_level_static(args: gatspi_level_args, stream: int = 0):
     _check(library().gatspi_simulate_level_static(ctypes.byref(args), _p(stream)))
+
+
+def gatspi_sdf_annotate(design: gatspi_sdf_design, text: bytes, dly_data: int, wire_rise: int = 0,
+                        wire_fall: int = 0):
+    _check(library().gatspi_sdf_annotate(ctypes.byref(design), text, len(text), _p(dly_data), _p(wire_rise),
+                                         _p(wire_fall)))
 
 
 def gatspi_destroy(ctx: int):

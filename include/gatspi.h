@@ -402,6 +402,56 @@ typedef struct {
  */
 gatspi_status gatspi_simulate_level_static(const gatspi_level_args *args, void *stream);
 
+/*
+ * SDF -> delay tables.  GATSPI translates SDF IOPATH and COND statements into the
+ * Fig. 4 arrays with no calibration run (Section 3, Fig. 4); this is that translator,
+ * on the host.  The design names what the SDF text refers to:
+ *   type_names[T]       CELLTYPE of every cell type
+ *   type_num_pins[T]    its input pins (1 .. GATSPI_MAX_PINS)
+ *   pin_names[]         the input pin names of every type in pin order, types one
+ *                       after another
+ *   out_pin             the output pin name of every cell (e.g. "Y")
+ *   gate_type[G], instance_names[G]
+ *                       every gate's type and SDF instance name (unique)
+ *   fanin_off[G+1]      gate g's fanin edges fanin_off[g] .. fanin_off[g+1]-1, in pin
+ *                       order (for INTERCONNECT destinations inst/pin)
+ *   gate_dly_off[G], dly_len
+ *                       where gate g's [4n][2^(n-1)] table goes in dly_data
+ *   unit_fs             the simulator's time unit in femtoseconds (1000 = 1 ps)
+ * Writes dly_data[dly_len] (every gate's table: rows 4*pin + 2*e_in + e_out, RISE = 0,
+ * FALL = 1; columns the other pins' values, first pin most significant; entries no
+ * statement sets are GATSPI_NO_ARC; words outside every table 0) and, if not NULL,
+ * wire_rise/wire_fall[fanin_off[G]] (0 where no INTERCONNECT names the pin).
+ * Rules: (posedge P) / (negedge P) / bare P select the input edge(s); the first
+ * value is the output-rise delay and the second the output-fall delay (one value
+ * serves both); () is no arc; min:typ:max gives typ; an unconditional IOPATH sets
+ * every column and a COND IOPATH the columns where its condition holds for the other
+ * pins, over the unconditional one (the last COND written wins where several hold);
+ * values are converted from the TIMESCALE (1 ns when absent) exactly and rounded to
+ * the nearest unit, halves up.  Conditions: Verilog == === != !== ! ~ & | ^ && ||,
+ * parentheses, 0, 1, 1'b0, 1'b1, 'b0, 'b1.  Only ABSOLUTE delays are read.
+ * EINVAL (message with the offending item) on malformed text, an unknown instance or
+ * pin, a CELLTYPE that does not match, a condition on the switching pin or a negative
+ * delay; the outputs are then unspecified.  Host memory only; no GPU is used.
+ */
+typedef struct {
+    int32_t num_types;
+    const char *const *type_names;
+    const int32_t *type_num_pins;
+    const char *const *pin_names;
+    const char *out_pin;
+    int32_t num_gates;
+    const int32_t *gate_type;
+    const char *const *instance_names;
+    const int32_t *fanin_off;
+    const int64_t *gate_dly_off;
+    int64_t dly_len;
+    int64_t unit_fs;
+} gatspi_sdf_design;
+
+gatspi_status gatspi_sdf_annotate(const gatspi_sdf_design *design, const char *text, size_t len, int32_t *dly_data,
+                                  int32_t *wire_rise, int32_t *wire_fall);
+
 /* Release the context's device arrays (not the borrowed pool).  NULL is allowed. */
 void gatspi_destroy(gatspi_ctx *ctx);
 

@@ -1,0 +1,106 @@
+"""Parity of the library's SDF translator (gatspi_sdf_annotate, host code behind the C
+ABI) with the oracle's translation: identical tables and wire delays on the hand-
+worked statements, on synthetic SDF of many netlists, spellings and time scales,
+and the same refusals.  The translator uses no GPU; the last test simulates on the
+GPU from translated tables.
+"""
+import numpy as np
+import pytest
+
+import synth
+import test_oracle_sdf as ts
+from oracle import sdf as osdf
+
+
+class _Lib:
+    """The library's translator with the oracle's calling convention."""
+
+    class SdfError(Exception):
+        pass
+
+    @staticmethod
+    def annotate(text, type_names, type_pins, gate_type, instance_names, fanin_off, gate_dly_off, dly_len, unit_fs):
+        from gate_level_logic_gb300 import GatspiError, sdf_annotate
+        try:
+            return sdf_annotate(text, type_names, type_pins, gate_type, instance_names, fanin_off, gate_dly_off,
+                                dly_len, unit_fs)
+        except GatspiError as e:
+            assert e.name == "GATSPI_EINVAL", e
+            raise _Lib.SdfError(str(e))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gate_level_logic_gb300 import build
+    build.build()
+    return _Lib
+
+
+@pytest.mark.parametrize("name", sorted(ts.HAND))
+def test_hand_statements(lib, name):
+    text, cells, _ = ts.HAND[name]
+    got = ts.translate(lib, text, cells)
+    want = ts.translate(osdf, text, cells)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
+
+
+def test_fig4_and_interconnect(lib):
+    ts.test_fig4_aoi21(lib)
+    ts.test_interconnect(lib)
+
+
+@pytest.mark.parametrize("name", sorted(ts.ERRORS))
+def test_same_refusals(lib, name):
+    with pytest.raises(lib.SdfError):
+        ts.translate(lib, ts.ERRORS[name], ts.NAND2)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_synthetic_netlists(lib, seed):
+    rng = np.random.default_rng(seed)
+    net = synth.generate_netlist(synth.NetlistSpec(
+        num_gates=int(rng.integers(50, 2000)), num_inputs=int(rng.integers(2, 40)), num_levels=int(rng.integers(1, 8)),
+        seed=seed, cell_mix=[synth.CELL_MIX, ("random", 2), ("random", 4), ("random", 1)][seed % 4],
+        cond_cells=("AOI21", "MUX2", "OAI22", "NAND4"), cond_fraction=float(rng.choice([0.0, 0.5, 1.0])),
+        delay_mode=("arc", "pin_out")[seed % 2], wire_delay=(0, int(rng.integers(0, 50)))))
+    unit = ["1ps", "1ns", "10ps", "100ps"][seed % 4]
+    s = synth.write_sdf(net, seed=seed, file_unit=unit)
+    args = (s.text, net.type_names, s.pin_names, net.gate_type, s.instance_names, net.fanin_off, net.gate_dly_off,
+            net.dly_data.size, 1000)
+    got = lib.annotate(*args)
+    want = osdf.annotate(*args)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
+    assert np.array_equal(got[0], net.dly_data)
+
+
+def test_coarser_simulation_unit_rounds_like_the_oracle(lib):
+    """The tables in 1 ps, translated into a 10 ps simulator unit: every value rounds."""
+    net, _ = synth.make("tiny")
+    s = synth.write_sdf(net, seed=7, file_unit="1ps")
+    args = (s.text, net.type_names, s.pin_names, net.gate_type, s.instance_names, net.fanin_off, net.gate_dly_off,
+            net.dly_data.size, 10000)
+    got, want = lib.annotate(*args), osdf.annotate(*args)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
+    finite = net.dly_data != synth.INF
+    assert np.array_equal(got[0][finite], (net.dly_data[finite] + 5) // 10)
+
+
+@pytest.mark.gpu
+def test_simulation_from_translated_tables(lib, oracle_lib):
+    """The 50k workload's delays written as SDF, translated by the library and
+    simulated on the GPU, equal the oracle simulating the oracle's translation."""
+    import copy
+    from test_gpu_parity import assert_same, pool_for, run_gpu
+    from gate_level_logic_gb300 import Simulator
+    net, stim = synth.make("50k")
+    s = synth.write_sdf(net, seed=11, file_unit="1ns")
+    args = (s.text, net.type_names, s.pin_names, net.gate_type, s.instance_names, net.fanin_off, net.gate_dly_off,
+            net.dly_data.size, 1000)
+    mine, theirs = copy.copy(net), copy.copy(net)
+    mine.dly_data, mine.wire_rise, mine.wire_fall = lib.annotate(*args)
+    theirs.dly_data, theirs.wire_rise, theirs.wire_fall = osdf.annotate(*args)
+    ref = oracle_lib.simulate(theirs, stim, threads=8)
+    assert_same(run_gpu(Simulator, mine, stim, pool_for(ref, mine)), ref, "from SDF")
