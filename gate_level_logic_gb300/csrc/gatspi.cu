@@ -10,6 +10,7 @@
 #include <cstring>
 #include <new>
 #include <string>
+#include <unordered_set>
 #include <vector>
 
 #include "gatspi_internal.cuh"
@@ -205,6 +206,32 @@ gatspi_status validate(const gatspi_netlist *nl, const gatspi_config *cfg, long 
     }
     *path_bound = L * ((long long)max_wire + max_gate);
     return GATSPI_OK;
+}
+
+// The level kernel's delay-table layout: the entry of Fig. 4's row 4*i + 2*e_in +
+// e_out and column c (the other pins' values, first pin most significant) moves to
+// ((2*i + e_out) << n) | v, v being all n pin values after the switch (pin j at bit
+// n-1-j), so that the kernel indexes with the pin values it already holds.  Same size
+// (4n * 2^(n-1) = 2n * 2^n); tables shared by several gates are moved once.
+void layout_delay_tables(const gatspi_netlist *nl, std::vector<int32_t> &out) {
+    out.assign(nl->dly_data, nl->dly_data + nl->dly_len);
+    std::unordered_set<long long> done;
+    for (long long g = 0; g < nl->num_gates; ++g) {
+        const long long off = nl->gate_dly_off[g];
+        if (!done.insert(off).second) continue;
+        const int n = nl->type_num_pins[nl->gate_type[g]];
+        const int cols = 1 << (n - 1);
+        const int32_t *src = nl->dly_data + off;
+        int32_t *dst = out.data() + off;
+        for (int i = 0; i < n; ++i)
+            for (int e_out = 0; e_out < 2; ++e_out)
+                for (uint32_t v = 0; v < (1u << n); ++v) {
+                    const int b = n - 1 - i;
+                    const int e_in = ((v >> b) & 1u) ? 0 : 1;   // the pin's new value 1: a rising input
+                    const uint32_t col = ((v >> (b + 1)) << b) | (v & ((1u << b) - 1u));
+                    dst[(((uint32_t)i << 1 | (uint32_t)e_out) << n) | v] = src[(4 * i + 2 * e_in + e_out) * cols + col];
+                }
+    }
 }
 
 void free_all(gatspi_ctx *c) {
@@ -433,9 +460,12 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
                  "uploading window starts");
         CUDA_TRY(cudaMemcpy(c->gate_desc, gd.data(), gd.size() * sizeof(int4), cudaMemcpyHostToDevice), "uploading gates");
         CUDA_TRY(cudaMemcpy(c->edge_desc, ed.data(), ed.size() * sizeof(int4), cudaMemcpyHostToDevice), "uploading edges");
-        if (dly_len > 0)
-            CUDA_TRY(cudaMemcpy(c->dly, nl->dly_data, (size_t)dly_len * sizeof(int32_t), cudaMemcpyHostToDevice),
+        if (dly_len > 0) {
+            std::vector<int32_t> packed;
+            layout_delay_tables(nl, packed);
+            CUDA_TRY(cudaMemcpy(c->dly, packed.data(), (size_t)dly_len * sizeof(int32_t), cudaMemcpyHostToDevice),
                      "uploading delay tables");
+        }
         CUDA_TRY(cudaMemcpy(c->window_len, wl.data(), wl.size() * sizeof(int32_t), cudaMemcpyHostToDevice),
                  "uploading window lengths");
         CUDA_TRY(cudaMemset(c->status, 0, sizeof(int32_t) * kStatusWords), "clearing the status");

@@ -81,6 +81,7 @@ struct Pin {
     int32_t len;       // its length in words, EOW included
     int32_t p;         // index of the entry in effect (value = p & 1)
     int32_t a;         // arrival time of the next transition at the pin, or EOW
+    int32_t nx;        // w[p + 1]: the next transition's time, kept from the previous step
     uint32_t drf;      // interconnect delays: rise | fall << 16
 };
 
@@ -93,7 +94,9 @@ __device__ __forceinline__ int32_t reject_limit(int32_t d, int32_t q) {
 // Next arrival of a pin: skip every pulse narrower than the interconnect delay of
 // its first edge (the fall delay when the pin is at 1, the rise delay when at 0),
 // or than that delay's reject limit when kFull is false; the arrival is the next
-// timestamp plus the delay.  False on a malformed wave.
+// timestamp plus the delay.  On entry s.nx holds w[p + 1] (the word after the
+// previous pulse test), so a step loads one word; a skipped pulse reloads.  False on
+// a malformed wave.
 template <bool kFull>
 __device__ __forceinline__ bool next_arrival(Pin &s, int32_t q) {
     for (;;) {
@@ -102,8 +105,7 @@ __device__ __forceinline__ bool next_arrival(Pin &s, int32_t q) {
             s.a = kEOW;
             return s.p + 2 == s.len;
         }
-        // both words are inside the waveform: load them together
-        const int32_t t1 = __ldg(s.w + s.p + 1);
+        const int32_t t1 = s.nx;
         const int32_t t2 = __ldg(s.w + s.p + 2);
         if (t1 == kEOW) {                // EOW before the last slot: malformed
             s.a = kEOW;
@@ -112,9 +114,11 @@ __device__ __forceinline__ bool next_arrival(Pin &s, int32_t q) {
         const int32_t d = (s.p & 1) ? (int32_t)(s.drf >> 16) : (int32_t)(s.drf & 0xffffu);
         if (t2 - t1 < (kFull ? d : reject_limit(d, q))) {   // the pulse [t1, t2) never reaches the pin
             s.p += 2;
+            s.nx = s.p + 1 < s.len ? __ldg(s.w + s.p + 1) : kEOW;
             continue;
         }
         s.a = t1 + d;
+        s.nx = t2;                       // w[p + 2]: the next transition once this one is taken
         return true;
     }
 }
@@ -126,16 +130,13 @@ struct LaneResult {
     int32_t err;   // 0 or a gatspi_status
 };
 
-// Delay of the arc of switching pin i (its new value is in vbits) to output edge
-// e_out: row = 4*i + 2*e_in + e_out, column = the other pins' values, first pin most
-// significant (vbits holds pin i at bit N-1-i).
+// Delay of the arc of switching pin i to output edge e_out.  The table was laid out
+// at create so that the Fig. 4 entry for row 4*i + 2*e_in + e_out and the column of
+// the other pins' values sits at ((2*i + e_out) << N) | vbits, vbits holding every
+// pin's new value (pin j at bit N-1-j; pin i's bit gives e_in).
 template <int N>
 __device__ __forceinline__ int32_t arc_delay(const int32_t *__restrict__ D, uint32_t vbits, int i, int e_out) {
-    constexpr int kCols = 1 << (N - 1);
-    const int b = N - 1 - i;
-    const int e_in = ((vbits >> b) & 1u) ? 0 : 1;
-    const uint32_t col = ((vbits >> (b + 1)) << b) | (vbits & ((1u << b) - 1u));
-    return __ldg(D + (4 * i + 2 * e_in + e_out) * kCols + col);
+    return __ldg(D + ((((uint32_t)i << 1) | (uint32_t)e_out) << N | vbits));
 }
 
 // Advance pin k, chosen per lane: its state is gathered and written back with
@@ -153,6 +154,7 @@ __device__ __forceinline__ bool advance_pin(Pin (&pin)[N], int k, int32_t q) {
         if (k == i) {
             pin[i].p = s.p;
             pin[i].a = s.a;
+            pin[i].nx = s.nx;
         }
     return ok;
 }
@@ -184,6 +186,7 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
     for (int i = 0; i < N; ++i) {
         pin[i].p = (__ldg(pin[i].w) == -1) ? 1 : 0;
         vbits |= (uint32_t)pin[i].p << (N - 1 - i);
+        pin[i].nx = __ldg(pin[i].w + pin[i].p + 1);   // in range: a wave holds its head and EOW
     }
     const int32_t y0 = (tt >> vbits) & 1;
     int32_t po = y0;        // index of the last output entry

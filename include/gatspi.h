@@ -343,7 +343,11 @@ gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *sim_ms, float *bounds_m
  *   edge_desc   int32 [4 * edges], 16-byte aligned; for edge e:
  *               {driving net, truth-table weight (not read), wire rise | wire fall
  *               << 16, 0}
- *   dly_data    the delay tables of gatspi_netlist
+ *   dly_data    the delay tables of gatspi_netlist laid out for the kernel: the entry
+ *               of row 4*i + 2*e_in + e_out and column c of gate g's table sits at
+ *               dly_data[gate_dly_off[g] + (((2*i + e_out) << n) | v)], v being all n
+ *               pin values after the switch (pin j at bit n-1-j, so pin i's bit gives
+ *               e_in and the others give c); the same size as the Fig. 4 table
  *   window_len  int32 [num_windows]
  *   pool, chunk_base, wend
  *               the waveform store of gatspi_views (pool_words = capacity); the

@@ -19,6 +19,25 @@ import synth
 pytestmark = pytest.mark.gpu
 
 
+def _kernel_tables(net):
+    """The delay tables in the layout gatspi_level_args documents: Fig. 4's row
+    4*i + 2*e_in + e_out, column c at ((2*i + e_out) << n) | v, v = all pin values."""
+    out = np.array(net.dly_data, np.int32)
+    for g in range(net.num_gates):
+        n = int(net.type_num_pins[net.gate_type[g]])
+        cols = 1 << (n - 1)
+        off = int(net.gate_dly_off[g])
+        src = np.asarray(net.dly_data[off:off + 4 * n * cols])
+        for i in range(n):
+            b = n - 1 - i
+            for e_out in (0, 1):
+                for v in range(1 << n):
+                    e_in = 0 if (v >> b) & 1 else 1
+                    col = ((v >> (b + 1)) << b) | (v & ((1 << b) - 1))
+                    out[off + (((2 * i + e_out) << n) | v)] = src[(4 * i + 2 * e_in + e_out) * cols + col]
+    return out
+
+
 def _pack(net):
     """The library's per-gate and per-edge descriptors (layout of gatspi_level_args)."""
     G, E = net.num_gates, net.num_edges
@@ -54,7 +73,7 @@ class Caller:
         gd, ed = _pack(net)
         self.gate_desc = torch.from_numpy(gd).to(dev)
         self.edge_desc = torch.from_numpy(ed).to(dev)
-        self.dly = torch.from_numpy(np.ascontiguousarray(net.dly_data, np.int32)).to(dev)
+        self.dly = torch.from_numpy(_kernel_tables(net)).to(dev)
         self.window_len = torch.from_numpy(np.ascontiguousarray(stim.window_len, np.int32)).to(dev)
         self.pool = torch.zeros(pool_words, dtype=torch.int32, device=dev)
         self.chunk_base = torch.zeros(self.N * self.nch, dtype=torch.int64, device=dev)
