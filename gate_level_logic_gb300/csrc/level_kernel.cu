@@ -97,8 +97,11 @@ __device__ __forceinline__ int32_t reject_limit(int32_t d, int32_t q) {
 // timestamp plus the delay.  On entry s.nx holds w[p + 1] (the word after the
 // previous pulse test), so a step loads one word; a skipped pulse reloads.  False on
 // a malformed wave.
-template <bool kFull>
-__device__ __forceinline__ bool next_arrival(Pin &s, int32_t q) {
+// t2pre: w[p + 2] when the caller has it already (a wave's first words are loaded
+// together), else unused.
+template <bool kFull, bool kPre = false>
+__device__ __forceinline__ bool next_arrival(Pin &s, int32_t q, int32_t t2pre = 0) {
+    bool pre = kPre;
     for (;;) {
         // p + 1 == len - 1 is the EOW slot: no further transition
         if (s.p + 2 >= s.len) {
@@ -106,7 +109,8 @@ __device__ __forceinline__ bool next_arrival(Pin &s, int32_t q) {
             return s.p + 2 == s.len;
         }
         const int32_t t1 = s.nx;
-        const int32_t t2 = __ldg(s.w + s.p + 2);
+        const int32_t t2 = pre ? t2pre : __ldg(s.w + s.p + 2);
+        pre = false;
         if (t1 == kEOW) {                // EOW before the last slot: malformed
             s.a = kEOW;
             return false;
@@ -181,12 +185,26 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
     // initial values: pin index 1 when the waveform starts with -1.  The truth table
     // was re-indexed at create by the pin weights, so its index is the pin values
     // read as a binary number, first pin most significant.
-    uint32_t vbits = 0;
+    // every pin's first four words are loaded at once (the head, the first transition
+    // and the word after it, whichever head the wave has); a wave holds at least its
+    // head and EOW, so words 0 and 1 always exist
+    int32_t x[N][4];
 #pragma unroll
     for (int i = 0; i < N; ++i) {
-        pin[i].p = (__ldg(pin[i].w) == -1) ? 1 : 0;
+        x[i][0] = __ldg(pin[i].w);
+        x[i][1] = __ldg(pin[i].w + 1);
+        x[i][2] = pin[i].len > 2 ? __ldg(pin[i].w + 2) : kEOW;
+        x[i][3] = pin[i].len > 3 ? __ldg(pin[i].w + 3) : kEOW;
+    }
+    uint32_t vbits = 0;
+    int32_t t2first[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const bool one = x[i][0] == -1;
+        pin[i].p = one ? 1 : 0;
         vbits |= (uint32_t)pin[i].p << (N - 1 - i);
-        pin[i].nx = __ldg(pin[i].w + pin[i].p + 1);   // in range: a wave holds its head and EOW
+        pin[i].nx = one ? x[i][2] : x[i][1];          // w[p + 1]
+        t2first[i] = one ? x[i][3] : x[i][2];         // w[p + 2]
     }
     const int32_t y0 = (tt >> vbits) & 1;
     int32_t po = y0;        // index of the last output entry
@@ -198,7 +216,7 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
 
     bool ok = true;
 #pragma unroll
-    for (int i = 0; i < N; ++i) ok &= next_arrival<kFull>(pin[i], q);
+    for (int i = 0; i < N; ++i) ok &= next_arrival<kFull, true>(pin[i], q, t2first[i]);
 
     while (ok) {
         int32_t t = pin[0].a;
