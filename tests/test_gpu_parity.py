@@ -85,9 +85,10 @@ def test_50k_staging_and_launch_variants(gpu, oracle_lib, stage_words, flags):
                 "stage=%d flags=%d" % (stage_words, flags))
 
 
-@pytest.mark.parametrize("W", [1, 2, 3, 7, 16, 31, 32, 33, 63, 64, 65, 100, 257])
+@pytest.mark.parametrize("W", [1, 2, 3, 7, 16, 31, 32, 33, 63, 64, 65, 100, 128, 200, 256, 257, 384])
 def test_window_counts(gpu, oracle_lib, W):
-    """Ragged window chunks, several gates per warp (W < 32), ragged tiles."""
+    """Ragged window chunks, several gates per warp (W < 32), ragged tiles, whole
+    blocks of one gate's chunks (W = 128, 256, 384)."""
     net = synth.generate_netlist(synth.NetlistSpec(num_gates=3001, num_inputs=37, num_levels=9, seed=W,
                                                    cond_fraction=0.3))
     stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=37, cycles=max(W, 300), period=500,
@@ -294,7 +295,7 @@ def test_pulse_percent_50k(gpu, oracle_lib, q, stage_words):
         assert ref.tc.sum() > oracle_lib.simulate(net, stim, threads=THREADS).tc.sum()
 
 
-@pytest.mark.parametrize("W", [5, 32, 70])
+@pytest.mark.parametrize("W", [5, 32, 70, 128])
 def test_pulse_percent_window_counts(gpu, oracle_lib, W):
     net = synth.generate_netlist(synth.NetlistSpec(num_gates=2500, num_inputs=29, num_levels=8, seed=100 + W,
                                                    cond_fraction=0.4))
@@ -304,3 +305,43 @@ def test_pulse_percent_window_counts(gpu, oracle_lib, W):
         ref = oracle_lib.simulate(net, stim, threads=THREADS, pulse_percent=q)
         assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=4, pulse_percent=q), ref,
                     "q=%d W=%d" % (q, W))
+
+
+@pytest.mark.parametrize("stage_words", [0, 3, 24, 64])
+def test_many_windows_staging(gpu, oracle_lib, stage_words):
+    """256 windows (eight chunks per gate) with every staging size."""
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=1200, num_inputs=33, num_levels=6, seed=77,
+                                                   cond_fraction=0.5))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=33, cycles=512, period=400, activity=0.5,
+                                                      windows=256, seed=77, glitch_frac=0.4))
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=stage_words), ref,
+                "stage=%d" % stage_words)
+
+
+def test_empty_level_and_errors_many_windows(gpu, oracle_lib):
+    """An empty level with 128 windows, then a missing delay arc reported with the
+    context still usable."""
+    from gate_level_logic_gb300 import GatspiError
+    tt = synth.truth_table("NAND2")
+    D = uniform_delays(2, 5, 7, tt)
+    net = synth.build_netlist(num_inputs=2, level_gates=[1, 0, 1], type_names=["NAND2"], type_num_pins=[2],
+                              type_tts=[tt], gate_type=[0, 0], fanins=[[0, 1], [2, 1]], wire_rise=np.zeros(4),
+                              wire_fall=np.zeros(4), delay_tables=[D, D])
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=2, cycles=256, period=50, activity=0.5,
+                                                      windows=128, seed=3))
+    ref = oracle_lib.simulate(net, stim)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref, "empty level")
+    bad = np.full_like(D, INF)
+    net2 = synth.build_netlist(num_inputs=2, level_gates=[1, 0, 1], type_names=["NAND2"], type_num_pins=[2],
+                               type_tts=[tt], gate_type=[0, 0], fanins=[[0, 1], [2, 1]], wire_rise=np.zeros(4),
+                               wire_fall=np.zeros(4), delay_tables=[D, bad])
+    with gpu(net2, stim.window_len, pool_words=pool_for(ref, net)) as sim:
+        sim.load(stim.pi_off, stim.pi_words)
+        sim.simulate()
+        with pytest.raises(GatspiError) as e:
+            sim.sync()
+        assert e.value.name == "GATSPI_EBADLUT"
+        sim.simulate()      # the context is still usable
+        with pytest.raises(GatspiError):
+            sim.sync()

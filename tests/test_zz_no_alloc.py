@@ -158,9 +158,14 @@ def built():
     build.build()
 
 
-@pytest.mark.parametrize("name,q", [("tiny", 100), ("50k", 100), ("tiny", 30)])
+@pytest.mark.parametrize("name,q", [("tiny", 100), ("50k", 100), ("tiny", 30), ("w256", 100), ("w256", 60)])
 def test_static_levels_match_regular_path(built, name, q):
-    net, stim = synth.make(name)
+    if name == "w256":     # eight chunks per gate
+        net = synth.generate_netlist(synth.NetlistSpec(num_gates=800, num_inputs=20, num_levels=5, seed=5))
+        stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=20, cycles=512, period=300, activity=0.4,
+                                                          windows=256, seed=5, glitch_frac=0.3))
+    else:
+        net, stim = synth.make(name)
     pool_words = 1 << 26            # room for the bound-sized output regions of every level
     ref = _regular(net, stim, pool_words, pulse_percent=q)
     caller = Caller(net, stim, pool_words, pulse_percent=q)
