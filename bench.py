@@ -101,8 +101,9 @@ def algorithmic_bytes(net, lengths, W):
     P, G, L = net.num_inputs, net.num_gates, net.num_levels
     lens = np.asarray(lengths, np.int64).reshape(P + G, W)
     net_words = lens.sum(axis=1)
-    nchunks = (W + 31) // 32
-    idx_bytes_per_net = 4 * W + 8 * nchunks          # wend + chunk base
+    ngroups = (W + 31) // 32
+    idx_bytes_per_net = 8 * W + 8                     # wstart + wend per window, the net's base
+    plan_bytes_per_gate = 2 * W + 4 * ngroups         # the level's plan: ranks, group offsets (read once)
     per_level = []
     lo = net.level_offsets
     for lvl in range(L):
@@ -111,8 +112,8 @@ def algorithmic_bytes(net, lengths, W):
         read = 4 * int(net_words[srcs].sum()) + idx_bytes_per_net * srcs.size
         write = 4 * int(net_words[P + g0:P + g1].sum()) + idx_bytes_per_net * (g1 - g0)
         desc = 16 * (g1 - g0) + 16 * int(net.fanin_off[g1] - net.fanin_off[g0])
-        stats = 16 * (g1 - g0) * nchunks
-        per_level.append(read + write + desc + stats)
+        stats = 16 * (g1 - g0) * ngroups
+        per_level.append(read + write + desc + stats + plan_bytes_per_gate * (g1 - g0))
     return np.array(per_level, dtype=np.int64)
 
 
@@ -350,6 +351,8 @@ def run_gpu(args):
         over["windows"] = args.windows
     if args.cycles:
         over["cycles"] = args.cycles
+    if args.gates:
+        over["net_num_gates"] = args.gates
     net, stim = synth.make(WORKLOAD, **over)
     W = stim.num_windows
     flags = gatspi.GATSPI_FLAG_LEVEL_TIMING
@@ -470,6 +473,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--windows", type=int, default=0, help="profiling only: number of cycle windows")
     ap.add_argument("--cycles", type=int, default=0, help="profiling only: number of stimulus cycles")
+    ap.add_argument("--gates", type=int, default=0, help="profiling only: number of gates of the netlist")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

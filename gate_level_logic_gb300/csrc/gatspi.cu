@@ -56,7 +56,8 @@ void gatspi_set_last_error(const char *msg) { g_err = msg ? msg : ""; }
 struct gatspi_ctx {
     int device = 0;
     int32_t P = 0, G = 0, L = 0, W = 0;
-    int32_t nchunks = 1, lpg_log2 = 0, slots_per_gate = 1;
+    int32_t ngroups = 1, lpg_log2 = 0, slots_per_gate = 1;
+    long long max_level_gates = 0;
     long long num_nets = 0;
     int32_t *pool = nullptr;
     long long pool_words = 0;
@@ -68,8 +69,12 @@ struct gatspi_ctx {
     int4 *gate_desc = nullptr;
     int4 *edge_desc = nullptr;
     int32_t *dly = nullptr;
-    long long *chunk_base = nullptr;
+    long long *net_base = nullptr;
+    uint32_t *wstart = nullptr;
     uint32_t *wend = nullptr;
+    uint8_t *wlen8 = nullptr;
+    uint16_t *perm = nullptr;
+    uint32_t *goff = nullptr;
     int32_t *window_len = nullptr;
     unsigned long long *tc = nullptr, *t1 = nullptr;
     unsigned long long *tile_status = nullptr;
@@ -112,8 +117,13 @@ struct gatspi_ctx {
         p.dly_data = dly;
         p.pool = pool;
         p.pool_words = pool_words;
-        p.chunk_base = chunk_base;
+        p.net_base = net_base;
+        p.wstart = wstart;
         p.wend = wend;
+        p.wlen8 = wlen8;
+        p.w8stride = (W + 3) & ~3;
+        p.perm = perm;
+        p.goff = goff;
         p.window_len = window_len;
         p.tc = tc;
         p.t1 = t1;
@@ -123,7 +133,7 @@ struct gatspi_ctx {
         p.status = status;
         p.num_inputs = P;
         p.W = W;
-        p.nchunks = nchunks;
+        p.ngroups = ngroups;
         p.lpg_log2 = lpg_log2;
         p.slots_per_gate = slots_per_gate;
         p.stage = stage;
@@ -140,7 +150,8 @@ gatspi_status validate(const gatspi_netlist *nl, const gatspi_config *cfg, long 
     if (P < 0 || G < 0 || L < 0 || T < 0 || P + G > INT32_MAX)
         return fail(GATSPI_EINVAL, "negative or too large netlist sizes");
     if (G > 0 && (L < 1 || T < 1)) return fail(GATSPI_EINVAL, "gates need at least one level and one type");
-    if (cfg->num_windows < 1) return fail(GATSPI_EINVAL, "num_windows must be >= 1");
+    if (cfg->num_windows < 1 || cfg->num_windows > GATSPI_MAX_WINDOWS)
+        return fail(GATSPI_EINVAL, "num_windows must be 1 .. %d", GATSPI_MAX_WINDOWS);
     if (!cfg->window_len) return fail(GATSPI_EINVAL, "window_len is required");
     for (int w = 0; w < cfg->num_windows; ++w)
         if (cfg->window_len[w] < 1 || cfg->window_len[w] > (1ll << 30))
@@ -244,7 +255,8 @@ void free_all(gatspi_ctx *c) {
     if (c->dump_stream) cudaStreamDestroy(c->dump_stream);
     if (c->tc_host) cudaFreeHost(c->tc_host);
     if (c->t1_host) cudaFreeHost(c->t1_host);
-    void *ptrs[] = {c->gate_desc, c->edge_desc, c->dly, c->chunk_base, c->wend, c->window_len, c->tc, c->t1,
+    void *ptrs[] = {c->gate_desc, c->edge_desc, c->dly, c->net_base, c->wstart, c->wend, c->wlen8, c->perm, c->goff,
+                    c->window_len, c->tc, c->t1,
                     c->tile_status, c->tickets, c->level_base, c->status, c->load_off, c->max_time,
                     c->win_start, c->tc_in, c->t1_in};
     for (void *p : ptrs)
@@ -373,14 +385,14 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         c->stage = cfg->stage_words < 0 ? kDefaultStage : cfg->stage_words;
         c->pulse_percent = (cfg->flags & GATSPI_FLAG_PULSE_PERCENT) ? cfg->pulse_percent : 100;
         c->num_nets = (long long)c->P + c->G;
-        c->nchunks = (c->W + 31) / 32;
+        c->ngroups = (c->W + 31) / 32;
         int lpg = 32;
         if (c->W < 32) {
             lpg = 1;
             while (lpg < c->W) lpg <<= 1;
         }
         while ((1 << c->lpg_log2) < lpg) ++c->lpg_log2;
-        c->slots_per_gate = c->nchunks << c->lpg_log2;
+        c->slots_per_gate = c->ngroups << c->lpg_log2;
         c->path_delay_bound = path_bound;
         for (int w = 0; w < c->W; ++w) c->sum_window_len += cfg->window_len[w];
 
@@ -418,13 +430,12 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
             ll.num_gates = c->level_offsets[l + 1] - c->level_offsets[l];
             const long long slots = (long long)ll.num_gates * c->slots_per_gate;
             const long long tiles = std::max<long long>(1, (slots + kTileSlots - 1) / kTileSlots);
-            const long long items = (long long)ll.num_gates * c->nchunks;
-            const long long scan = std::max<long long>(1, (items + kTileSlots - 1) / kTileSlots);
-            if (tiles > INT32_MAX / kTileSlots || items > INT32_MAX)
+            const long long scan = std::max<long long>(1, ll.num_gates);      // one plan warp per gate
+            if (tiles > INT32_MAX / kTileSlots)
                 return fail(GATSPI_EINVAL, "level %d has too many (gate, window) slots", l);
             ll.num_tiles = (int32_t)tiles;
-            ll.num_items = (int32_t)items;
             ll.scan_tiles = (int32_t)scan;
+            c->max_level_gates = std::max<long long>(c->max_level_gates, ll.num_gates);
             ll.tile_base = c->total_tiles;
             c->total_tiles += scan;
             c->launches.push_back(ll);
@@ -434,8 +445,14 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(dev_alloc(&c->gate_desc, gd.size()), "allocating gate descriptors");
         CUDA_TRY(dev_alloc(&c->edge_desc, ed.size()), "allocating edge descriptors");
         CUDA_TRY(dev_alloc(&c->dly, (size_t)dly_len), "allocating delay tables");
-        CUDA_TRY(dev_alloc(&c->chunk_base, (size_t)(c->num_nets * c->nchunks)), "allocating the window index");
+        CUDA_TRY(dev_alloc(&c->net_base, (size_t)std::max<long long>(c->num_nets, 1)), "allocating the window index");
+        CUDA_TRY(dev_alloc(&c->wstart, (size_t)(c->num_nets * c->W)), "allocating the window index");
         CUDA_TRY(dev_alloc(&c->wend, (size_t)(c->num_nets * c->W)), "allocating the window index");
+        CUDA_TRY(dev_alloc(&c->wlen8, (size_t)std::max<long long>(c->num_nets * ((c->W + 3) & ~3), 4)),
+                 "allocating the window index");
+        CUDA_TRY(dev_alloc(&c->perm, (size_t)std::max<long long>(c->max_level_gates * c->W, 1)), "allocating the plan");
+        CUDA_TRY(dev_alloc(&c->goff, (size_t)std::max<long long>(c->max_level_gates * c->ngroups, 1)),
+                 "allocating the plan");
         CUDA_TRY(dev_alloc(&c->window_len, (size_t)c->W), "allocating window lengths");
         CUDA_TRY(dev_alloc(&c->tc, (size_t)c->G), "allocating TC");
         CUDA_TRY(dev_alloc(&c->t1, (size_t)c->G), "allocating T1");
@@ -471,7 +488,7 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(cudaMemset(c->status, 0, sizeof(int32_t) * kStatusWords), "clearing the status");
         CUDA_TRY(cudaMemset(c->tc, 0, sizeof(unsigned long long) * std::max(c->G, 1)), "clearing TC");
         CUDA_TRY(cudaMemset(c->t1, 0, sizeof(unsigned long long) * std::max(c->G, 1)), "clearing T1");
-        CUDA_TRY(set_level_smem_limit(c->stage), "configuring shared memory");
+        CUDA_TRY(set_level_smem_limit(c->stage, c->W), "configuring shared memory");
         if (c->flags & GATSPI_FLAG_LEVEL_TIMING) {
             c->events.resize(2 * c->L + 1, nullptr);
             for (auto &e : c->events) CUDA_TRY(cudaEventCreate(&e), "creating level events");
@@ -700,10 +717,9 @@ gatspi_status gatspi_get_waveform(gatspi_ctx *c, int32_t net, int32_t window, in
     long long base = 0;
     uint32_t end = 0, start = 0;
     const long long k = (long long)net * c->W + window;
-    CUDA_TRY(cudaMemcpy(&base, c->chunk_base + (long long)net * c->nchunks + window / 32, sizeof base,
-                        cudaMemcpyDeviceToHost), "reading the window index");
+    CUDA_TRY(cudaMemcpy(&base, c->net_base + net, sizeof base, cudaMemcpyDeviceToHost), "reading the window index");
+    CUDA_TRY(cudaMemcpy(&start, c->wstart + k, sizeof start, cudaMemcpyDeviceToHost), "reading the window index");
     CUDA_TRY(cudaMemcpy(&end, c->wend + k, sizeof end, cudaMemcpyDeviceToHost), "reading the window index");
-    if (window % 32) CUDA_TRY(cudaMemcpy(&start, c->wend + k - 1, sizeof start, cudaMemcpyDeviceToHost), "reading the window index");
     *len = (size_t)(end - start);
     if (*len > cap || !buf) return fail(GATSPI_EINVAL, "buffer of %zu words too small for %zu", cap, *len);
     CUDA_TRY(cudaMemcpy(buf, c->pool + base + start, *len * sizeof(int32_t), cudaMemcpyDeviceToHost), "reading a waveform");
@@ -717,16 +733,16 @@ gatspi_status gatspi_export_offsets(gatspi_ctx *c, int64_t *start, int32_t *len,
     if (!c->loaded || !c->simulated) return fail(GATSPI_ESTATE, "simulate first");
     gatspi_status st = sync_ctx(c);
     if (st != GATSPI_OK) return st;
-    std::vector<long long> base((size_t)(c->num_nets * c->nchunks));
-    std::vector<uint32_t> wend((size_t)(c->num_nets * c->W));
-    CUDA_TRY(cudaMemcpy(base.data(), c->chunk_base, base.size() * sizeof(long long), cudaMemcpyDeviceToHost), "reading the window index");
-    CUDA_TRY(cudaMemcpy(wend.data(), c->wend, wend.size() * sizeof(uint32_t), cudaMemcpyDeviceToHost), "reading the window index");
+    std::vector<long long> base((size_t)c->num_nets);
+    std::vector<uint32_t> ws((size_t)(c->num_nets * c->W)), we((size_t)(c->num_nets * c->W));
+    CUDA_TRY(cudaMemcpy(base.data(), c->net_base, base.size() * sizeof(long long), cudaMemcpyDeviceToHost), "reading the window index");
+    CUDA_TRY(cudaMemcpy(ws.data(), c->wstart, ws.size() * sizeof(uint32_t), cudaMemcpyDeviceToHost), "reading the window index");
+    CUDA_TRY(cudaMemcpy(we.data(), c->wend, we.size() * sizeof(uint32_t), cudaMemcpyDeviceToHost), "reading the window index");
     for (long long net = 0; net < c->num_nets; ++net)
         for (int w = 0; w < c->W; ++w) {
             const long long k = net * c->W + w;
-            const uint32_t s0 = (w % 32) ? wend[k - 1] : 0u;
-            if (start) start[k] = base[net * c->nchunks + w / 32] + s0;
-            if (len) len[k] = (int32_t)(wend[k] - s0);
+            if (start) start[k] = base[net] + ws[k];
+            if (len) len[k] = (int32_t)(we[k] - ws[k]);
         }
     return GATSPI_OK;
 }
@@ -786,13 +802,13 @@ gatspi_status gatspi_device_views(gatspi_ctx *c, gatspi_views *v) {
                  "reading the pool size");
         v->pool_used = used;
     }
-    v->chunk_base = (const int64_t *)c->chunk_base;
+    v->net_base = (const int64_t *)c->net_base;
+    v->wstart = c->wstart;
     v->wend = c->wend;
     v->tc = c->tc;
     v->t1 = c->t1;
     v->num_nets = (int32_t)c->num_nets;
     v->num_windows = c->W;
-    v->num_chunks = c->nchunks;
     return GATSPI_OK;
 }
 

@@ -20,7 +20,9 @@ constexpr int kWarps = kBlock / 32;
 constexpr int kLevelWarps = GATSPI_LEVEL_WARPS;   // warps per level-kernel block (independent warps)
 constexpr int kLevelBlock = 32 * kLevelWarps;
 constexpr int kLevelMinBlocks = GATSPI_LEVEL_MIN_BLOCKS;  // resident blocks per SM the registers must allow
-constexpr int kTileSlots = 32;            // (gate, window) slots per look-back tile = one warp
+constexpr int kTileSlots = 32;            // (gate, rank) slots per warp of the level kernel
+constexpr int kPlanWarps = 4;             // warps per block of the planning kernel (one gate each)
+constexpr int kSortBuckets = 256;         // counting-sort buckets of the window bounds
 constexpr int kMaxStage = 64;             // upper bound of stage_words
 constexpr int kDefaultStage = 24;
 constexpr int32_t kEOW = GATSPI_EOW;
@@ -42,26 +44,34 @@ struct DevParams {
                                //     truth-table bit k = output for pin values k (first pin most significant)
     const int4 *edge_desc;     // [E] x = source net, y = truth-table weight (unused here), z = wire rise | fall << 16
     const int32_t *dly_data;   // per-instance conditional delay tables
-    // waveform store
+    // waveform store: waveform (net, w) is pool[net_base[net] + wstart[k] .. net_base[net] + wend[k]),
+    // k = net * W + w, EOW included
     int32_t *pool;
     long long pool_words;
-    long long *chunk_base;     // [num_nets * nchunks]
-    uint32_t *wend;            // [num_nets * W]
+    long long *net_base;       // [num_nets] first pool word of the net's region
+    uint32_t *wstart;          // [num_nets * W] relative to net_base
+    uint32_t *wend;            // [num_nets * W] relative to net_base
+    uint8_t *wlen8;            // [num_nets * w8stride] min(window length, 255), for the plan
     const int32_t *window_len; // [W]
+    // the level's plan: per gate, its windows by rank (largest output bound first) and
+    // the offset of every group of 32 ranks inside the gate's region
+    uint16_t *perm;            // [gates of the level * W]
+    uint32_t *goff;            // [gates of the level * ngroups]
     // toggle statistics
     unsigned long long *tc;    // [G]
     unsigned long long *t1;    // [G]
     // scan state
-    unsigned long long *tile_status;  // [total warp tiles], zeroed per simulate
+    unsigned long long *tile_status;  // [total look-back tiles: one per gate], zeroed per simulate
     int32_t *tickets;                 // [L], zeroed per simulate
     long long *level_base;            // [L+1]; [0] = words of the input waveforms
     int32_t *status;                  // [kStatusWords]
     // shape
     int32_t num_inputs;
     int32_t W;
-    int32_t nchunks;          // ceil(W / 32)
-    int32_t lpg_log2;         // log2(lanes per (gate, chunk) segment)
-    int32_t slots_per_gate;   // nchunks << lpg_log2
+    int32_t w8stride;         // W rounded up to a multiple of 4 (rows of wlen8 start 4-byte aligned)
+    int32_t ngroups;          // ceil(W / 32): groups of 32 ranks per gate
+    int32_t lpg_log2;         // log2(lanes per (gate, group) segment)
+    int32_t slots_per_gate;   // ngroups << lpg_log2
     int32_t stage;            // output words staged on chip per lane
     int32_t pulse_percent;    // PATHPULSEPERCENT, 0 .. 100
 };
@@ -71,14 +81,14 @@ struct LevelLaunch {
     int32_t gate_begin;
     int32_t num_gates;
     int32_t num_tiles;      // warps of the level kernel: ceil(gates * slots_per_gate / 32)
-    int32_t num_items;      // (gate, chunk) output regions of the level
-    int32_t scan_tiles;     // warps of the bounds scan: max(1, ceil(num_items / 32))
-    long long tile_base;    // first look-back word of this level's bounds scan
+    int32_t scan_tiles;     // warps of the planning kernel: max(1, gates), one per gate
+    long long tile_base;    // first look-back word of this level's plan
 };
 
 size_t level_smem_bytes(int stage);
-cudaError_t set_level_smem_limit(int stage);   // both variants of the simulation kernel
-cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // output regions
+size_t plan_smem_bytes(int W);
+cudaError_t set_level_smem_limit(int stage, int W);   // the simulation kernels and the planning kernel
+cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // the plan
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s);      // the simulation
 cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s);          // both, in order
 cudaError_t launch_window_lengths(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,

@@ -5,9 +5,9 @@
 // which owns the whole device memory through its own allocator, or code that is
 // not allowed to allocate once it has started.  gatspi_create allocates the
 // context's arrays; this entry point instead takes every input and output buffer
-// from the caller and keeps the only scratch the level's kernels need -- the
-// look-back flags of the output-region scan, its tile ticket and the status word
-// -- in a file-scope device array of fixed size.  Every GPU that loads the library holds
+// from the caller (the level's plan included) and keeps the only scratch the
+// level's kernels need -- the look-back flags of the output-region scan, its tile
+// ticket and the status word -- in a file-scope device array of fixed size.  Every GPU that loads the library holds
 // that array until the process exits.
 #include <cstdio>
 #include <mutex>
@@ -18,7 +18,7 @@ using namespace gatspi;
 
 namespace {
 
-constexpr int kStaticTiles = 1 << 18;                     // scan tiles of one level at most
+constexpr int kStaticTiles = 1 << 18;                     // scan tiles (gates) of one level at most
 constexpr int kTicketWord = kStaticTiles;                 // index of the ticket word
 constexpr int kStatusWord = kStaticTiles + 1;             // index of the status words (2 x 8 bytes)
 constexpr int kScratchWords = kStaticTiles + 4;
@@ -44,13 +44,15 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
         return s;
     };
     if (!a) return err(GATSPI_EINVAL, "args are required");
-    if (!a->gate_desc || !a->edge_desc || !a->dly_data || !a->window_len || !a->pool || !a->chunk_base ||
-        !a->wend || !a->tc || !a->t1 || !a->level_base)
+    if (!a->gate_desc || !a->edge_desc || !a->dly_data || !a->window_len || !a->pool || !a->net_base ||
+        !a->wstart || !a->wend || !a->wlen8 || !a->perm || !a->goff || !a->tc || !a->t1 || !a->level_base)
         return err(GATSPI_EINVAL, "every buffer of gatspi_level_args is required");
     if (((uintptr_t)a->gate_desc & 15) || ((uintptr_t)a->edge_desc & 15))
         return err(GATSPI_EINVAL, "gate_desc and edge_desc must be 16-byte aligned");
+    if ((uintptr_t)a->wlen8 & 3) return err(GATSPI_EINVAL, "wlen8 must be 4-byte aligned");
     if (a->num_inputs < 0 || a->num_windows < 1 || a->gate_begin < 0 || a->num_gates < 0 || a->pool_words < 0)
         return err(GATSPI_EINVAL, "negative sizes");
+    if (a->num_windows > GATSPI_MAX_WINDOWS) return err(GATSPI_EINVAL, "too many windows");
     if (a->stage_words < -1 || a->stage_words > kMaxStage) return err(GATSPI_EINVAL, "stage_words out of range");
     const bool own_percent = (a->flags & GATSPI_FLAG_PULSE_PERCENT) != 0;
     if (own_percent && (a->pulse_percent < 0 || a->pulse_percent > 100))
@@ -58,7 +60,7 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
 
     DevParams p{};
     p.W = a->num_windows;
-    p.nchunks = (p.W + 31) / 32;
+    p.ngroups = (p.W + 31) / 32;
     int lpg = 32;
     if (p.W < 32) {
         lpg = 1;
@@ -66,13 +68,12 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     }
     p.lpg_log2 = 0;
     while ((1 << p.lpg_log2) < lpg) ++p.lpg_log2;
-    p.slots_per_gate = p.nchunks << p.lpg_log2;
+    p.slots_per_gate = p.ngroups << p.lpg_log2;
     const long long slots = (long long)a->num_gates * p.slots_per_gate;
     const long long tiles = slots > 0 ? (slots + kTileSlots - 1) / kTileSlots : 1;
-    const long long items = (long long)a->num_gates * p.nchunks;
-    const long long scan = items > 0 ? (items + kTileSlots - 1) / kTileSlots : 1;
-    if (scan > kStaticTiles)
-        return err(GATSPI_EINVAL, "level too large for the static scratch (at most 262144 x 32 (gate, chunk) regions)");
+    const long long scan = a->num_gates > 0 ? a->num_gates : 1;      // one plan warp per gate
+    if (scan > kStaticTiles) return err(GATSPI_EINVAL, "level too large for the static scratch (at most 262144 gates)");
+    if (tiles > INT32_MAX / kTileSlots) return err(GATSPI_EINVAL, "level has too many (gate, window) slots");
 
     // once per device, with that device current: the device address of the scratch
     int dev = 0;
@@ -99,8 +100,13 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     p.dly_data = a->dly_data;
     p.pool = a->pool;
     p.pool_words = a->pool_words;
-    p.chunk_base = (long long *)a->chunk_base;
+    p.net_base = (long long *)a->net_base;
+    p.wstart = a->wstart;
     p.wend = a->wend;
+    p.wlen8 = a->wlen8;
+    p.w8stride = (a->num_windows + 3) & ~3;
+    p.perm = a->perm;
+    p.goff = a->goff;
     p.window_len = a->window_len;
     p.tc = a->tc;
     p.t1 = a->t1;
@@ -117,13 +123,12 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     l.gate_begin = a->gate_begin;
     l.num_gates = a->num_gates;
     l.num_tiles = (int32_t)tiles;
-    l.num_items = (int32_t)items;
     l.scan_tiles = (int32_t)scan;
     l.tile_base = 0;
 
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_level_smem_limit(p.stage);
+    if (e == cudaSuccess) e = set_level_smem_limit(p.stage, p.W);
     // clear the flags of the tiles this call uses, the ticket and the status
     if (e == cudaSuccess) e = cudaMemsetAsync(words, 0, sizeof(unsigned long long) * (size_t)scan, s);
     if (e == cudaSuccess)

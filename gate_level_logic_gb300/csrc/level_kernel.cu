@@ -2,39 +2,43 @@
 //
 // Two launches per logic level (GATSPI, Section 3, Fig. 5).
 //
-// level_bounds_kernel sizes the output region of every (gate, chunk of 32 windows)
-// of the level before anything is simulated.  An output window can hold at most
-// 3 + sum over pins of (input length - 2) words: every stored toggle needs an
-// iteration of the event loop and every iteration consumes at least one input
-// transition.  Summed over the chunk's windows this is the sum of the pins' source
-// spans (one window-index load per pin) plus (3 - 2n) per window.  The bounds are
-// scanned in (gate, chunk) order -- warp shuffles plus a decoupled look-back over
-// warp tiles; the work per item is a handful of loads, so the waits are short --
-// and give every region its pool offset.  The page sizes its outputs with a full
-// counting pass instead; the bound replaces that pass and leaves a gap after each
-// region (its size is the only cost).
+// level_plan_kernel plans the level before anything is simulated, one warp per
+// gate.  An output window can hold at most 3 + sum over pins of (input length - 2)
+// words: every stored toggle needs an iteration of the event loop and every
+// iteration consumes at least one input transition.  The warp computes this bound
+// for each of the gate's windows from the window index of its sources, ranks the
+// windows by bound, largest first (a stable counting sort: equal bounds keep window
+// order, so the layout depends only on the inputs), and sums the bounds of every
+// group of 32 ranks.  The gate's region is the sum of all its bounds; a decoupled
+// look-back over the gates gives every region its pool offset.  The page sizes its
+// outputs with a full counting pass instead; the bound replaces that pass and leaves
+// a gap after each group (its size is the only cost).  The ranking is for load
+// balance: a warp runs as long as its slowest lane, and the bound follows a window's
+// event count closely, so a warp that gets 32 windows of similar bound keeps its
+// lanes busy.
 //
-// level_kernel simulates.  A warp owns 32 consecutive (gate, window) slots: one gate
-// and 32 consecutive windows (or, for W < 32, several gates with W windows each),
-// the thread mapping the page chooses so that a warp's lanes run the same cell.
-// Each lane runs Algorithm 1 of the page for its (gate, window): merge the fanin
-// waveforms with interconnect inertial filtering, resolve simultaneous switching,
-// look up the truth table by summed pin weights, pick the conditional delay (row =
-// switching pin and edges, column = the other pins' values) and apply the gate's
-// inertial filter.  The kernel comes in two variants: PATHPULSEPERCENT = 100, the
-// page's setting, where the filter cancels exactly the output entries that have
-// not matured and at most one is ever pending; and any other percentage q, where
-// both filters compare against the reject limit floor(d * q / 100), several
-// output entries can be pending and a cancel re-reads the entry before the one it
-// exposes from the lane's own output.  Before simulating, each lane turns its
-// inputs' lengths into its window's own bound and a warp scan gives the window a
-// provisional slot in the region.  The lane keeps the first `stage` output words in
-// shared memory ([word][lane] layout, bank-conflict free) and writes any further
-// word straight to its provisional slot.  A warp scan of the actual lengths then
-// places every window; spilled words are moved down to their final place and the
-// staged words are stored.  Every (gate, window) is simulated once.  TC and T1 are
-// reduced per (gate, chunk) with shuffles and one 64-bit atomic each.  No warp waits
-// for another.
+// level_kernel simulates.  A warp owns 32 slots: one gate and 32 consecutive ranks
+// (or, for W < 32, several gates with all W windows each), so that a warp's lanes
+// run the same cell as in the page's mapping.  Each lane runs Algorithm 1 of the page
+// for its (gate, window): merge the fanin waveforms with interconnect inertial
+// filtering, resolve simultaneous switching, look up the truth table by summed pin
+// weights, pick the conditional delay (row = switching pin and edges, column = the
+// other pins' values) and apply the gate's inertial filter.  The kernel comes in two
+// variants: PATHPULSEPERCENT = 100, the page's setting, where the filter cancels
+// exactly the output entries that have not matured and at most one is ever pending;
+// and any other percentage q, where both filters compare against the reject limit
+// floor(d * q / 100), several output entries can be pending and a cancel re-reads
+// the entry before the one it exposes from the lane's own output.  Before
+// simulating, each lane turns its inputs' lengths into its window's bound and a warp
+// scan gives the window a provisional slot in the group's part of the region.  The
+// lane keeps the first `stage` output words in shared memory ([word][lane] layout,
+// bank-conflict free) and writes any further word straight to its provisional
+// slot.  A warp scan of the actual lengths then places every window in rank order;
+// spilled words are moved down to their final place and the staged words are
+// stored.  Every (gate, window) is simulated once.  The window index records each
+// window's start and end relative to its net's region, since windows are stored in
+// rank order.  TC and T1 are reduced per warp with shuffles and one 64-bit atomic
+// each.  No warp waits for another.
 //
 // No kernel traps: a malformed waveform, a missing delay arc, pool overflow or a
 // stalled look-back sets the device status word and the kernels carry on without
@@ -310,13 +314,22 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane) {
 // predecessors at once, closest first, and stops at the first inclusive prefix.
 // Publishes the tile's aggregate before looking back and its inclusive prefix
 // after.  Waits are bounded: a stalled predecessor raises GATSPI_ETIMEOUT.
-__device__ long long look_back(const DevParams &P, const LevelLaunch &L, int tile, long long total, int lane) {
+// Publish a tile's aggregate (tile 0: its inclusive prefix) ahead of look_back, so
+// that successors need not wait while the tile does other work.
+__device__ __forceinline__ void publish_aggregate(const DevParams &P, const LevelLaunch &L, int tile, long long total,
+                                                  int lane) {
+    if (lane == 0)
+        st_relaxed(P.tile_status + L.tile_base + tile, (tile == 0 ? kFlagIncl : kFlagAgg) | (unsigned long long)total);
+}
+
+__device__ long long look_back(const DevParams &P, const LevelLaunch &L, int tile, long long total, int lane,
+                               bool published = false) {
     unsigned long long *st = P.tile_status + L.tile_base;
     if (tile == 0) {
-        if (lane == 0) st_relaxed(st, kFlagIncl | (unsigned long long)total);
+        if (lane == 0 && !published) st_relaxed(st, kFlagIncl | (unsigned long long)total);
         return 0;
     }
-    if (lane == 0) st_relaxed(st + tile, kFlagAgg | (unsigned long long)total);
+    if (lane == 0 && !published) st_relaxed(st + tile, kFlagAgg | (unsigned long long)total);
     long long excl = 0;
     int k = tile - 1;
     const unsigned long long t0 = global_ns();
@@ -353,47 +366,130 @@ __device__ long long look_back(const DevParams &P, const LevelLaunch &L, int til
     return excl;
 }
 
-// Output region of every (gate, chunk) of the level: bound, scan, chunk_base.
-__global__ void __launch_bounds__(kBlock) level_bounds_kernel(const DevParams P, const LevelLaunch L) {
+// The plan of one gate per warp: window bounds, their ranking (largest first,
+// stable), the offset of every group of 32 ranks, the region's pool offset.
+// Shared memory per warp: the bounds of the gate's windows, the bucket counters of
+// the counting sort, the group sums.
+__global__ void __launch_bounds__(kPlanWarps * 32) level_plan_kernel(const DevParams P, const LevelLaunch L) {
+    extern __shared__ uint32_t psm[];
     const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    uint32_t *bnd = psm + (size_t)warp * (P.W + kSortBuckets + P.ngroups);
+    uint32_t *hist = bnd + P.W;
+    uint32_t *gsum = hist + kSortBuckets;
     int tile = 0;
     if (lane == 0) tile = atomicAdd(P.tickets + L.level, 1);
     tile = __shfl_sync(0xffffffffu, tile, 0);
     if (tile >= L.scan_tiles) return;                      // spare warps of the last block
     const bool skip = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
-    const int item = tile * 32 + lane;
-    const bool valid = !skip && item < L.num_items;
-    int g = 0, c = 0;
-    long long bound = 0;
+    const int gl = tile;                                   // the gate of this warp
+    const bool valid = !skip && gl < L.num_gates;
+    const int g = L.gate_begin + gl;
+    const int W = P.W;
+    long long total = 0;
     if (valid) {
-        const int gl = item / P.nchunks;
-        c = item - gl * P.nchunks;
-        g = L.gate_begin + gl;
+        for (int k = lane; k < kSortBuckets; k += 32) hist[k] = 0;
+        for (int k = lane; k < P.ngroups; k += 32) gsum[k] = 0;
         const int4 gd = __ldg(P.gate_desc + g);
         const int n = gd.y & 7;
-        const int w_last = min(c * 32 + 31, P.W - 1);
-        bound = (long long)(w_last - c * 32 + 1) * (3 - 2 * n);
-        for (int i = 0; i < n; ++i) {
-            const long long src = __ldg(P.edge_desc + gd.x + i).x;
-            bound += __ldg(P.wend + src * P.W + w_last);      // span of the source's chunk
-        }
-    }
-    long long incl = bound;
+        long long src[GATSPI_MAX_PINS];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        for (int i = 0; i < GATSPI_MAX_PINS; ++i) src[i] = i < n ? (long long)__ldg(P.edge_desc + gd.x + i).x : 0;
+        __syncwarp();
+        // bounds from the one-byte window lengths, four consecutive windows per lane
+        // and load; a length of 255 or more is read exactly from the index
+        long long lane_sum = 0;
+        for (int w0 = 4 * lane; w0 < W; w0 += 4 * 32) {
+            uint32_t b[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) b[u] = 3u - 2u * (uint32_t)n;
+#pragma unroll
+            for (int i = 0; i < GATSPI_MAX_PINS; ++i)
+                if (i < n) {
+                    const uint32_t four = __ldg((const uint32_t *)(P.wlen8 + src[i] * P.w8stride + w0));
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int w = w0 + u;
+                        uint32_t len = (four >> (8 * u)) & 0xffu;
+                        if (len == 0xffu && w < W)
+                            len = __ldg(P.wend + src[i] * W + w) - __ldg(P.wstart + src[i] * W + w);
+                        b[u] += len;
+                    }
+                }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int w = w0 + u;
+                if (w < W) {
+                    bnd[w] = b[u];
+                    lane_sum += b[u];
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) lane_sum += __shfl_xor_sync(0xffffffffu, lane_sum, o);
+        total = lane_sum;
+        __syncwarp();
+        // the region's size is known: publish it before ranking, so that later
+        // gates can sum past this one while it ranks its windows
+        publish_aggregate(P, L, tile, total, lane);
+        // bucket counts (bucket 0 = the largest bounds; bounds above 255 share it)
+        for (int w = lane; w < W; w += 32)
+            atomicAdd(&hist[kSortBuckets - 1 - min(bnd[w], (uint32_t)(kSortBuckets - 1))], 1u);
+        __syncwarp();
+        {   // exclusive scan of the bucket counts: the first rank of every bucket
+            constexpr int kPer = kSortBuckets / 32;
+            uint32_t v[kPer], sum = 0;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                v[k] = hist[lane * kPer + k];
+                sum += v[k];
+            }
+            uint32_t run = warp_incl_scan(sum, lane) - sum;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                hist[lane * kPer + k] = run;
+                run += v[k];
+            }
+        }
+        __syncwarp();
+        // ranks, windows in order so that equal bounds keep window order
+        for (int w0 = 0; w0 < W; w0 += 32) {
+            const int w = w0 + lane;
+            const bool act = w < W;
+            const uint32_t b = act ? bnd[w] : 0u;
+            const int key = act ? kSortBuckets - 1 - (int)min(b, (uint32_t)(kSortBuckets - 1)) : kSortBuckets + lane;
+            const unsigned same = __match_any_sync(0xffffffffu, key);
+            const uint32_t first = act ? hist[key] : 0u;
+            __syncwarp();
+            if (act && lane == __ffs(same) - 1) hist[key] = first + (uint32_t)__popc(same);
+            __syncwarp();
+            if (act) {
+                const uint32_t rank = first + (uint32_t)__popc(same & ((1u << lane) - 1u));
+                P.perm[(long long)gl * W + rank] = (uint16_t)w;
+                atomicAdd(&gsum[rank >> 5], b);
+            }
+        }
+        __syncwarp();
+        // group offsets inside the gate's region
+        long long run = 0;
+        for (int j0 = 0; j0 < P.ngroups; j0 += 32) {
+            const int j = j0 + lane;
+            const uint32_t v = j < P.ngroups ? gsum[j] : 0u;
+            const uint32_t incl = warp_incl_scan(v, lane);
+            if (j < P.ngroups) P.goff[(long long)gl * P.ngroups + j] = (uint32_t)(run + incl - v);
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0 && total >= (1ll << 32)) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, g, 1);
     }
-    const long long total = __shfl_sync(0xffffffffu, incl, 31);
-    const long long base = P.level_base[L.level] + look_back(P, L, tile, total, lane);
+    const long long base = P.level_base[L.level] + look_back(P, L, tile, total, lane, valid);
     if (lane == 0 && tile == L.scan_tiles - 1) {
         P.level_base[L.level + 1] = base + total;
         if (base + total > P.pool_words) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, 0, 0);
     }
-    if (valid) P.chunk_base[((long long)P.num_inputs + g) * P.nchunks + c] = base + incl - bound;
+    if (valid && lane == 0) P.net_base[(long long)P.num_inputs + g] = base;
 }
 
-// One warp = 32 consecutive (gate, window) slots of the level.  Warps share nothing
+// One warp = 32 slots of the level: a gate and 32 of its ranks.  Warps share nothing
 // but the shared-memory allocation of their block and never wait for each other.
 // kFull: PATHPULSEPERCENT = 100.
 template <bool kFull>
@@ -405,12 +501,13 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     if (tile >= L.num_tiles) return;                       // spare warps of the last block
     const bool skip = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
 
-    // slot -> (gate, chunk, window): W >= 32 gives one (gate, chunk) per warp,
-    // W < 32 gives 32 >> lpg_log2 gates of lpg lanes each
+    // slot -> (gate, group, rank): W >= 32 gives one (gate, group of 32 ranks) per
+    // warp, W < 32 gives 32 >> lpg_log2 gates of lpg lanes each; the plan maps the
+    // rank to a window
     int gl, c, j;
     if (P.lpg_log2 == 5) {
-        gl = tile / P.nchunks;
-        c = tile - gl * P.nchunks;
+        gl = tile / P.ngroups;
+        c = tile - gl * P.ngroups;
         j = lane;
     } else {
         const int slot = tile * 32 + lane;
@@ -418,23 +515,25 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
         c = 0;
         j = slot & ((1 << P.lpg_log2) - 1);
     }
-    const int w = c * 32 + j;
+    const int rank = c * 32 + j;
     const bool gate_ok = !skip && gl < L.num_gates;
-    const bool valid = gate_ok && w < P.W;
+    const bool valid = gate_ok && rank < P.W;
     const int g = L.gate_begin + gl;
+    const int w = valid ? (int)__ldg(P.perm + (long long)gl * P.W + rank) : 0;
 
     int32_t *stage = smem + warp * (P.stage * 32) + lane;
-    const int seg_lead = lane & ~((1 << P.lpg_log2) - 1);  // first lane of this (gate, chunk) segment
+    const int seg_lead = lane & ~((1 << P.lpg_log2) - 1);  // first lane of this (gate, group) segment
     const long long net = (long long)P.num_inputs + g;
 
-    // Provisional slot of this window inside its (gate, chunk) region: the window's
-    // own bound, 3 + sum over pins of (input length - 2), scanned over the segment.
-    // These bounds add up to the region the bounds kernel reserved.
+    // Provisional slot of this window inside its group's part of the gate's region:
+    // the window's own bound, 3 + sum over pins of (input length - 2), scanned over
+    // the segment in rank order.  These bounds add up to what the plan reserved.
     // Pins of the gate in window w: source waveforms from the window index.
     int4 gd = make_int4(0, 0, 0, 0);
     int32_t Lw = 0;
     uint32_t bound = 0;
-    long long base = 0;
+    uint32_t gofs = 0;      // the group's offset inside the gate's region
+    long long base = 0;     // the group's first pool word
     Pin pins[GATSPI_MAX_PINS];
     if (valid) {
         gd = __ldg(P.gate_desc + g);
@@ -447,14 +546,15 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
                 const int4 e = __ldg(P.edge_desc + gd.x + i);
                 const long long src = e.x;
                 const uint32_t end = __ldg(P.wend + src * P.W + w);
-                const uint32_t start = (w & 31) ? __ldg(P.wend + src * P.W + w - 1) : 0u;
-                pins[i].w = P.pool + __ldg(P.chunk_base + src * P.nchunks + c) + start;
+                const uint32_t start = __ldg(P.wstart + src * P.W + w);
+                pins[i].w = P.pool + __ldg(P.net_base + src) + start;
                 pins[i].len = (int32_t)(end - start);
                 pins[i].drf = (uint32_t)e.z;
                 bound += end - start;
             }
         }
-        base = __ldg(P.chunk_base + net * P.nchunks + c);
+        gofs = __ldg(P.goff + (long long)gl * P.ngroups + c);
+        base = __ldg(P.net_base + net) + gofs;
     }
     const uint32_t bincl = warp_incl_scan(bound, lane);
     const uint32_t bexcl = bincl - bound;
@@ -475,7 +575,7 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     const uint32_t rel = excl - __shfl_sync(0xffffffffu, excl, seg_lead);
     const long long fin = base + rel;
 
-    // TC and T1 per (gate, chunk): reduce over the segment's lanes, one atomic each
+    // TC and T1 per (gate, group): reduce over the segment's lanes, one atomic each
     long long tcs = res.tc, t1s = res.t1;
     for (int o = (1 << P.lpg_log2) >> 1; o >= 1; o >>= 1) {
         tcs += __shfl_xor_sync(0xffffffffu, tcs, o);
@@ -519,7 +619,9 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
         int32_t *dst = P.pool + fin;
         const int kept = min(res.len, P.stage);
         for (int k = 0; k < kept; ++k) dst[k] = stage[k * 32];
-        P.wend[net * P.W + w] = rel + (uint32_t)res.len;
+        P.wstart[net * P.W + w] = gofs + rel;
+        P.wend[net * P.W + w] = gofs + rel + (uint32_t)res.len;
+        P.wlen8[net * P.w8stride + w] = (uint8_t)min(res.len, 255);
     }
 }
 
@@ -535,7 +637,7 @@ __global__ void load_index_kernel(const DevParams P, const long long *__restrict
     const int w = (int)(k % P.W);
     const long long pi = k / P.W;
     const long long s = off[k], e = off[k + 1];
-    const long long c0 = off[k - (w & 31)];            // first window of the chunk
+    const long long c0 = off[k - w];                   // first word of the input's windows
     bool ok = s >= 0 && e <= nwords && e - s >= 2 && e - c0 < (1ll << 32) && c0 <= s && (k > 0 || s == 0);
     int32_t tmax = 0;
     if (ok) {
@@ -560,8 +662,10 @@ __global__ void load_index_kernel(const DevParams P, const long long *__restrict
         return;
     }
     atomicMax(max_time, tmax);
-    if ((w & 31) == 0) P.chunk_base[pi * P.nchunks + (w >> 5)] = c0;
+    if (w == 0) P.net_base[pi] = c0;
+    P.wstart[k] = (uint32_t)(s - c0);
     P.wend[k] = (uint32_t)(e - c0);
+    P.wlen8[pi * P.w8stride + w] = (uint8_t)min(e - s, 255ll);
 }
 
 // Length of waveform (net, sel[s]) for an export of selected windows.
@@ -571,9 +675,7 @@ __global__ void window_lengths_kernel(const DevParams P, long long num_nets, con
     if (k >= num_nets * nsel) return;
     const long long net = k / nsel;
     const int w = sel[k % nsel];
-    const uint32_t end = P.wend[net * P.W + w];
-    const uint32_t start = (w & 31) ? P.wend[net * P.W + w - 1] : 0u;
-    len[k] = (long long)(end - start);
+    len[k] = (long long)(P.wend[net * P.W + w] - P.wstart[net * P.W + w]);
 }
 
 // Copy of waveform (net, sel[s]) to words[off[k] ..], one warp per waveform.
@@ -584,8 +686,7 @@ __global__ void window_gather_kernel(const DevParams P, long long num_nets, cons
     if (k >= num_nets * nsel) return;
     const long long net = k / nsel;
     const int w = sel[k % nsel];
-    const uint32_t start = (w & 31) ? P.wend[net * P.W + w - 1] : 0u;
-    const int32_t *src = P.pool + P.chunk_base[net * P.nchunks + (w >> 5)] + start;
+    const int32_t *src = P.pool + P.net_base[net] + P.wstart[net * P.W + w];
     const long long n = off[k + 1] - off[k];
     for (long long i = lane; i < n; i += 32) words[off[k] + i] = src[i];
 }
@@ -608,9 +709,16 @@ cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const i
 
 size_t level_smem_bytes(int stage) { return (size_t)kLevelWarps * 32 * (size_t)stage * sizeof(int32_t); }
 
+static int plan_warps(int W) { return W > 4096 ? 1 : kPlanWarps; }   // one warp per block for long window lists
+
+size_t plan_smem_bytes(int W) {   // per warp: W bounds, the buckets, the group sums
+    return (size_t)plan_warps(W) * ((size_t)W + kSortBuckets + (size_t)(W + 31) / 32) * sizeof(uint32_t);
+}
+
 cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
-    const unsigned scan_blocks = (unsigned)((l.scan_tiles + kWarps - 1) / kWarps);
-    level_bounds_kernel<<<scan_blocks, kBlock, 0, s>>>(p, l);
+    const int wpb = plan_warps(p.W);
+    const unsigned blocks = (unsigned)((l.scan_tiles + wpb - 1) / wpb);
+    level_plan_kernel<<<blocks, wpb * 32, plan_smem_bytes(p.W), s>>>(p, l);
     return cudaGetLastError();
 }
 
@@ -629,12 +737,16 @@ cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t 
     return e != cudaSuccess ? e : launch_level_sim(p, l, s);
 }
 
-cudaError_t set_level_smem_limit(int stage) {
-    const cudaError_t e = cudaFuncSetAttribute(level_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)level_smem_bytes(stage));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(level_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)level_smem_bytes(stage));
+cudaError_t set_level_smem_limit(int stage, int W) {
+    cudaError_t e = cudaFuncSetAttribute(level_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)level_smem_bytes(stage));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(level_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)level_smem_bytes(stage));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(level_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)plan_smem_bytes(W));
+    return e;
 }
 
 cudaError_t launch_load_index(const DevParams &p, const long long *off, long long nwords, int32_t *max_time,

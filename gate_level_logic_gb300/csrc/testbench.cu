@@ -10,7 +10,7 @@
 // waveform (head [0] or [-1, 0], times strictly increasing from 1, EOW last) and
 // its offsets.
 //
-// tb_cut_kernel: one warp per (input, chunk of 32 windows); lane j takes window
+// tb_cut_kernel: one warp per (input, chunk of 32 consecutive windows); lane j takes window
 // w = 32c + j, which covers [S_w, S_w + L_w).  Two binary searches give the window's
 // transitions (after S_w, before S_w + L_w) and its initial value (the parity of the
 // last entry at or before S_w: a transition exactly at S_w folds into it).  A warp
@@ -99,10 +99,11 @@ __global__ void tb_cut_kernel(const DevParams P, const long long *__restrict__ t
                               const long long *__restrict__ wstart) {
     const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (warp >= (long long)P.num_inputs * P.nchunks) return;
+    const int nch = (P.W + 31) / 32;
+    if (warp >= (long long)P.num_inputs * nch) return;
     if (__shfl_sync(0xffffffffu, lane == 0 ? tb_status(P.status) : 0, 0) != 0) return;   // malformed input
-    const int p = (int)(warp / P.nchunks);
-    const int c = (int)(warp - (long long)p * P.nchunks);
+    const int p = (int)(warp / nch);
+    const int c = (int)(warp - (long long)p * nch);
     const int w = c * 32 + lane;
     const bool valid = w < P.W;
 
@@ -128,21 +129,23 @@ __global__ void tb_cut_kernel(const DevParams P, const long long *__restrict__ t
         if (lane >= o) incl += v;
     }
     const uint32_t excl = incl - wl;
-    long long cb = 0;
-    if (lane == 0) {
-        const long long before = lower_bound(x, h, eow, wstart[c * 32]) - h;   // transitions before S_32c
-        cb = (s - tb_off[0]) + 3ll * P.W * p + before + 96ll * c;
-        P.chunk_base[(long long)p * P.nchunks + c] = cb;
-    }
-    cb = __shfl_sync(0xffffffffu, cb, 0);
+    // the input's region starts at (tb_off[p] - tb_off[0]) + 3 W p; chunk c of it at
+    // (transitions before S_32c) + 96 c further
+    const long long region = (s - tb_off[0]) + 3ll * P.W * p;
+    uint32_t rel = 0;
+    if (lane == 0) rel = (uint32_t)(lower_bound(x, h, eow, wstart[c * 32]) - h + 96ll * c);
+    rel = __shfl_sync(0xffffffffu, rel, 0);
+    if (c == 0 && lane == 0) P.net_base[p] = region;
     if (valid) {
-        int32_t *dst = P.pool + cb + excl;
+        int32_t *dst = P.pool + region + rel + excl;
         int k = 0;
         if (v0) dst[k++] = -1;
         dst[k++] = 0;
         for (long long i = lo; i < hi; ++i) dst[k++] = (int32_t)((long long)x[i] - S);
         dst[k] = kEOW;
-        P.wend[(long long)p * P.W + w] = incl;
+        P.wstart[(long long)p * P.W + w] = rel + excl;
+        P.wend[(long long)p * P.W + w] = rel + incl;
+        P.wlen8[(long long)p * P.w8stride + w] = (uint8_t)min(wl, 255u);
     }
     if (warp == 0 && lane == 0) P.level_base[0] = (tb_off[P.num_inputs] - tb_off[0]) + 3ll * P.W * P.num_inputs;
 }
@@ -157,10 +160,9 @@ __global__ void input_stats_kernel(const DevParams P, unsigned long long *__rest
     const long long p = warp;
     long long toggles = 0, ones = 0;
     for (int w = lane; w < P.W; w += 32) {
-        const long long cb = P.chunk_base[p * P.nchunks + (w >> 5)];
         const uint32_t end = P.wend[p * P.W + w];
-        const uint32_t start = (w & 31) ? P.wend[p * P.W + w - 1] : 0u;
-        const int32_t *x = P.pool + cb + start;
+        const uint32_t start = P.wstart[p * P.W + w];
+        const int32_t *x = P.pool + P.net_base[p] + start;
         const int len = (int)(end - start);
         const long long Lw = P.window_len[w];
         const int h = x[0] == -1 ? 2 : 1;
@@ -204,7 +206,7 @@ cudaError_t launch_testbench_cut(const DevParams &p, const long long *tb_off, co
     tb_check_kernel<<<(unsigned)((check_warps * 32 + threads - 1) / threads), threads, 0, s>>>(p, tb_off, tb, nwords);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const long long cut_warps = (long long)p.num_inputs * p.nchunks;
+    const long long cut_warps = (long long)p.num_inputs * ((p.W + 31) / 32);
     tb_cut_kernel<<<(unsigned)((cut_warps * 32 + threads - 1) / threads), threads, 0, s>>>(p, tb_off, tb, wstart);
     return cudaGetLastError();
 }

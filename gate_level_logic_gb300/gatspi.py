@@ -46,16 +46,18 @@ class gatspi_config(ctypes.Structure):
 
 class gatspi_views(ctypes.Structure):
     _fields_ = [
-        ("pool", _p), ("pool_words", ctypes.c_int64), ("pool_used", ctypes.c_int64), ("chunk_base", _p),
-        ("wend", _p), ("tc", _p), ("t1", _p), ("num_nets", ctypes.c_int32), ("num_windows", ctypes.c_int32),
-        ("num_chunks", ctypes.c_int32),
+        ("pool", _p), ("pool_words", ctypes.c_int64), ("pool_used", ctypes.c_int64), ("net_base", _p),
+        ("wstart", _p), ("wend", _p), ("tc", _p), ("t1", _p), ("num_nets", ctypes.c_int32),
+        ("num_windows", ctypes.c_int32),
     ]
 
 
 class gatspi_level_args(ctypes.Structure):
     _fields_ = [
         ("gate_desc", _p), ("edge_desc", _p), ("dly_data", _p), ("window_len", _p), ("pool", _p),
-        ("pool_words", ctypes.c_int64), ("chunk_base", _p), ("wend", _p), ("tc", _p), ("t1", _p),
+        ("pool_words", ctypes.c_int64), ("net_base", _p), ("wstart", _p), ("wend", _p), ("wlen8", _p), ("perm", _p),
+        ("goff", _p),
+        ("tc", _p), ("t1", _p),
         ("level_base", _p), ("num_inputs", ctypes.c_int32), ("num_windows", ctypes.c_int32),
         ("gate_begin", ctypes.c_int32), ("num_gates", ctypes.c_int32), ("stage_words", ctypes.c_int32),
         ("flags", ctypes.c_uint32), ("pulse_percent", ctypes.c_int32),

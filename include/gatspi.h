@@ -63,6 +63,7 @@ extern "C" {
 #define GATSPI_EOW 2147483647
 #define GATSPI_NO_ARC 2147483647   /* delay-table entry of an arc that cannot occur */
 #define GATSPI_MAX_PINS 4
+#define GATSPI_MAX_WINDOWS 16384   /* cycle windows of one context */
 
 typedef enum {
     GATSPI_OK = 0,
@@ -136,7 +137,7 @@ typedef struct {
 
 /*
  * Run configuration.
- *   num_windows   W >= 1 independent cycle windows
+ *   num_windows   W independent cycle windows, 1 .. GATSPI_MAX_WINDOWS
  *   window_len    host array [W] of window lengths in time units (1 .. 2^30)
  *   flags         GATSPI_FLAG_*
  *   stage_words   output words a thread keeps in shared memory while it simulates
@@ -161,27 +162,25 @@ typedef struct gatspi_ctx gatspi_ctx;
 /*
  * Device views of the simulation state (valid until gatspi_destroy).
  *
- * Windows are grouped in chunks of 32 (one chunk when W <= 32).  The pool holds
- * first the input waveforms as loaded, then the gates' outputs level by level; a
- * level holds one region per (gate, chunk), in (gate, chunk) order, sized by an upper
- * bound of its output (see gatspi_simulate) and filled from its start with the
- * chunk's windows in order, so a gap may follow a region.  Waveform (net, w) starts
- * at pool[chunk_base[net * num_chunks + w / 32] + start] and ends (EOW included) at
- * pool[chunk_base[...] + wend[net * W + w]], where start = 0 for the first window of
- * a chunk and wend[net * W + w - 1] otherwise.  The layout depends only on the
- * inputs: every run gives the same pool.
+ * The pool holds first the input waveforms as loaded, then the gates' outputs level
+ * by level; every net has one region.  A gate's region is sized by upper bounds of
+ * its windows' outputs (see gatspi_simulate); its windows are stored in groups of 32
+ * ranks (windows ordered by bound, largest first), each group packed from the start
+ * of its share, so gaps may follow a group.  Waveform k = (net, w), k = net * W + w,
+ * is pool[net_base[net] + wstart[k] .. net_base[net] + wend[k]) (EOW included).  The
+ * layout depends only on the inputs: every run gives the same pool.
  */
 typedef struct {
     const int32_t *pool;
     int64_t pool_words;            /* capacity                                       */
     int64_t pool_used;             /* words written by the last load + simulate      */
-    const int64_t *chunk_base;     /* [num_nets * num_chunks]                        */
-    const uint32_t *wend;          /* [num_nets * num_windows]                       */
+    const int64_t *net_base;       /* [num_nets] first pool word of the net's region */
+    const uint32_t *wstart;        /* [num_nets * num_windows] relative to net_base  */
+    const uint32_t *wend;          /* [num_nets * num_windows] relative to net_base  */
     const unsigned long long *tc;  /* [num_gates] output toggles summed over windows */
     const unsigned long long *t1;  /* [num_gates] time at 1 summed over windows      */
     int32_t num_nets;
     int32_t num_windows;
-    int32_t num_chunks;
 } gatspi_views;
 
 /*
@@ -241,13 +240,14 @@ gatspi_status gatspi_load_testbench(gatspi_ctx *ctx, const int64_t *off, const i
 /*
  * Re-simulate every level, in order, on `stream` (a cudaStream_t; NULL = legacy
  * default stream).  Asynchronous: returns after enqueueing.  Clears TC/T1 and the
- * device status first.  Per level two kernels run: the first sizes the output
- * region of every (gate, chunk) by an upper bound (an output window holds at most
- * 3 + the sum over its pins of (input length - 2) words, since each stored toggle
- * takes an event-loop iteration and each iteration consumes an input transition)
- * and scans the bounds into pool offsets, in place of the page's counting pass;
- * the second runs Algorithm 1 for every (gate, window) of the level and stores the
- * output waveforms, the window index and TC/T1 per gate.  The level sequence is captured once into a CUDA graph and
+ * device status first.  Per level two kernels run.  The first plans the level: it
+ * bounds every (gate, window) output (an output window holds at most 3 + the sum over
+ * its pins of (input length - 2) words, since each stored toggle takes an event-loop
+ * iteration and each iteration consumes an input transition), ranks each gate's
+ * windows by bound so that a warp gets 32 windows of similar work, and scans the
+ * gates' bound sums into pool offsets, in place of the page's counting pass.  The
+ * second runs Algorithm 1 for every (gate, window) of the level and stores the output
+ * waveforms, the window index and TC/T1 per gate.  The level sequence is captured once into a CUDA graph and
  * replayed by later calls, unless GATSPI_FLAG_NO_GRAPH or GATSPI_FLAG_LEVEL_TIMING
  * is set (then the level kernels are launched directly on `stream`).
  */
@@ -349,9 +349,13 @@ gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *sim_ms, float *bounds_m
  *               pin values after the switch (pin j at bit n-1-j, so pin i's bit gives
  *               e_in and the others give c); the same size as the Fig. 4 table
  *   window_len  int32 [num_windows]
- *   pool, chunk_base, wend
+ *   pool, net_base, wstart, wend, wlen8
  *               the waveform store of gatspi_views (pool_words = capacity); the
- *               sources of this level must already be in it
+ *               sources of this level must already be in it; wlen8 (uint8, 4-byte
+ *               aligned) holds min(length, 255) of waveform (net, w) at
+ *               net * W4 + w, W4 = num_windows rounded up to a multiple of 4
+ *   perm, goff  the level's plan (scratch, written then read by this call):
+ *               uint16 [num_gates * num_windows] and uint32 [num_gates * ceil(W / 32)]
  *   tc, t1      per-gate toggle count and time at 1, accumulated (not cleared)
  *   level_base  int64 [2]: [0] = first pool word of this level's outputs (read),
  *               [1] = one past its last word (written)
@@ -366,8 +370,12 @@ typedef struct {
     const int32_t *window_len;
     int32_t *pool;
     int64_t pool_words;
-    int64_t *chunk_base;
+    int64_t *net_base;
+    uint32_t *wstart;
     uint32_t *wend;
+    uint8_t *wlen8;
+    uint16_t *perm;
+    uint32_t *goff;
     unsigned long long *tc;
     unsigned long long *t1;
     int64_t *level_base;
@@ -392,9 +400,9 @@ typedef struct {
  * process exits.
  *
  *   - No cudaMalloc, cudaFree or allocating library call is made.
- *   - A level may have at most 262144 x 32 = 8388608 (gate, chunk) regions (a
- *     gate has ceil(W / 32) of them); a larger level returns GATSPI_EINVAL before
- *     anything runs.  The caller also makes sure the gates exist.
+ *   - A level may have at most 262144 gates (one look-back flag each); a larger
+ *     level returns GATSPI_EINVAL before anything runs.  The caller also makes sure
+ *     the gates exist.
  *   - The first call on a device looks up the device address of the scratch array
  *     (with that device current); make that first call before any stream capture.
  *   - Every call shares the one array and clears the part it uses before its

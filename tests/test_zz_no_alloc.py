@@ -76,22 +76,32 @@ class Caller:
         self.dly = torch.from_numpy(_kernel_tables(net)).to(dev)
         self.window_len = torch.from_numpy(np.ascontiguousarray(stim.window_len, np.int32)).to(dev)
         self.pool = torch.zeros(pool_words, dtype=torch.int32, device=dev)
-        self.chunk_base = torch.zeros(self.N * self.nch, dtype=torch.int64, device=dev)
+        self.net_base = torch.zeros(self.N, dtype=torch.int64, device=dev)
+        self.wstart = torch.zeros(self.N * W, dtype=torch.int32, device=dev)
         self.wend = torch.zeros(self.N * W, dtype=torch.int32, device=dev)
+        W4 = (W + 3) // 4 * 4
+        self.wlen8 = torch.zeros(self.N * W4, dtype=torch.uint8, device=dev)
+        most = int(np.diff(net.level_offsets).max()) if net.num_levels else 1
+        self.perm = torch.zeros(max(most * W, 1), dtype=torch.int16, device=dev)
+        self.goff = torch.zeros(max(most * self.nch, 1), dtype=torch.int32, device=dev)
         self.tc = torch.zeros(G, dtype=torch.int64, device=dev)
         self.t1 = torch.zeros(G, dtype=torch.int64, device=dev)
         self.level_base = torch.zeros(2, dtype=torch.int64, device=dev)
         self.stage_words = stage_words
         self.pulse_percent = pulse_percent
-        # input waveforms at the front of the pool, with their window index
+        # input waveforms at the front of the pool, with their window index: each
+        # input's windows back to back from its base
         off = stim.pi_off
         nw = int(off[-1])
         self.pool[:nw] = torch.from_numpy(np.ascontiguousarray(stim.pi_words, np.int32)).to(dev)
         k = np.arange(P * W)
-        first = k - (k % W) % 32                      # first window of each (input, chunk)
-        cb = off[first].reshape(P, W)[:, ::32]
-        self.chunk_base[:P * self.nch] = torch.from_numpy(np.ascontiguousarray(cb.ravel(), np.int64)).to(dev)
-        self.wend[:P * W] = torch.from_numpy((off[k + 1] - off[first]).astype(np.int32)).to(dev)
+        first = off[(k // W) * W]
+        self.net_base[:P] = torch.from_numpy(np.ascontiguousarray(off[np.arange(P) * W], np.int64)).to(dev)
+        self.wstart[:P * W] = torch.from_numpy((off[k] - first).astype(np.int32)).to(dev)
+        self.wend[:P * W] = torch.from_numpy((off[k + 1] - first).astype(np.int32)).to(dev)
+        l8 = np.zeros((P, W4), np.uint8)
+        l8[:, :W] = np.minimum(off[k + 1] - off[k], 255).reshape(P, W)
+        self.wlen8[:P * W4] = torch.from_numpy(l8.ravel()).to(dev)
         self.inputs_words = nw
 
     def args(self, gate_begin, num_gates, pool_words=None):
@@ -99,7 +109,9 @@ class Caller:
         return g.gatspi_level_args(
             self.gate_desc.data_ptr(), self.edge_desc.data_ptr(), self.dly.data_ptr(), self.window_len.data_ptr(),
             self.pool.data_ptr(), self.pool.numel() if pool_words is None else pool_words,
-            self.chunk_base.data_ptr(), self.wend.data_ptr(), self.tc.data_ptr(), self.t1.data_ptr(),
+            self.net_base.data_ptr(), self.wstart.data_ptr(), self.wend.data_ptr(), self.wlen8.data_ptr(),
+            self.perm.data_ptr(),
+            self.goff.data_ptr(), self.tc.data_ptr(), self.t1.data_ptr(),
             self.level_base.data_ptr(), self.net.num_inputs, self.W, gate_begin, num_gates, self.stage_words,
             g.GATSPI_FLAG_PULSE_PERCENT, self.pulse_percent)
 
@@ -115,13 +127,12 @@ class Caller:
             self.level_base[0] = base
             g.gatspi_simulate_level_static(self.args(int(lo[lvl]), int(lo[lvl + 1] - lo[lvl])), stream)
             base = int(self.level_base[1].item())
-        cb = self.chunk_base.cpu().numpy()
-        we = self.wend.cpu().numpy().astype(np.int64)
+        nb = self.net_base.cpu().numpy()
+        ws = self.wstart.cpu().numpy().astype(np.uint32).astype(np.int64)
+        we = self.wend.cpu().numpy().astype(np.uint32).astype(np.int64)
         k = np.arange(self.N * self.W)
-        net_id, w = k // self.W, k % self.W
-        first = np.where(w % 32 == 0, 0, we[np.maximum(k - 1, 0)])
-        start = cb[net_id * self.nch + w // 32] + first
-        length = we - first
+        start = nb[k // self.W] + ws
+        length = we - ws
         return (start, length, base), self.pool[:base].cpu().numpy(), self.tc.cpu().numpy(), self.t1.cpu().numpy()
 
 
@@ -190,8 +201,8 @@ def test_static_errors_and_limits(built):
     index, pool, tc, t1 = caller.run()
     assert _same_index(index, ref[0]) and np.array_equal(tc, ref[2])
     assert np.array_equal(_gather(pool, index), _gather(ref[1], ref[0]))
-    # a level beyond the fixed scratch is refused before anything runs: with one
-    # window every gate is one output region, and 2^25 regions > 262144 x 32
+    # a level beyond the fixed scratch is refused before anything runs: one
+    # look-back flag per gate, and 2^25 gates > 262144
     assert stim.num_windows == 1
     big = caller.args(0, 1 << 25)
     with pytest.raises(GatspiError) as e:
