@@ -430,7 +430,7 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
             ll.num_gates = c->level_offsets[l + 1] - c->level_offsets[l];
             const long long slots = (long long)ll.num_gates * c->slots_per_gate;
             const long long tiles = std::max<long long>(1, (slots + kTileSlots - 1) / kTileSlots);
-            const long long scan = std::max<long long>(1, ll.num_gates);      // one plan warp per gate
+            const long long scan = std::max<long long>(1, ((long long)ll.num_gates + 31) / 32);   // placement tiles
             if (tiles > INT32_MAX / kTileSlots)
                 return fail(GATSPI_EINVAL, "level %d has too many (gate, window) slots", l);
             ll.num_tiles = (int32_t)tiles;
@@ -451,7 +451,7 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(dev_alloc(&c->wlen8, (size_t)std::max<long long>(c->num_nets * ((c->W + 3) & ~3), 4)),
                  "allocating the window index");
         CUDA_TRY(dev_alloc(&c->perm, (size_t)std::max<long long>(c->max_level_gates * c->W, 1)), "allocating the plan");
-        CUDA_TRY(dev_alloc(&c->goff, (size_t)std::max<long long>(c->max_level_gates * c->ngroups, 1)),
+        CUDA_TRY(dev_alloc(&c->goff, (size_t)std::max<long long>(c->max_level_gates * (c->ngroups + 1), 1)),
                  "allocating the plan");
         CUDA_TRY(dev_alloc(&c->window_len, (size_t)c->W), "allocating window lengths");
         CUDA_TRY(dev_alloc(&c->tc, (size_t)c->G), "allocating TC");

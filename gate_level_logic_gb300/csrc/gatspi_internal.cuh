@@ -56,12 +56,12 @@ struct DevParams {
     // the level's plan: per gate, its windows by rank (largest output bound first) and
     // the offset of every group of 32 ranks inside the gate's region
     uint16_t *perm;            // [gates of the level * W]
-    uint32_t *goff;            // [gates of the level * ngroups]
+    uint32_t *goff;            // [gates of the level * (ngroups + 1)]: group offsets, then the region's size
     // toggle statistics
     unsigned long long *tc;    // [G]
     unsigned long long *t1;    // [G]
     // scan state
-    unsigned long long *tile_status;  // [total look-back tiles: one per gate], zeroed per simulate
+    unsigned long long *tile_status;  // [total look-back tiles: 32 gates each], zeroed per simulate
     int32_t *tickets;                 // [L], zeroed per simulate
     long long *level_base;            // [L+1]; [0] = words of the input waveforms
     int32_t *status;                  // [kStatusWords]
@@ -81,14 +81,15 @@ struct LevelLaunch {
     int32_t gate_begin;
     int32_t num_gates;
     int32_t num_tiles;      // warps of the level kernel: ceil(gates * slots_per_gate / 32)
-    int32_t scan_tiles;     // warps of the planning kernel: max(1, gates), one per gate
+    int32_t scan_tiles;     // warps of the placement scan: max(1, ceil(gates / 32))
     long long tile_base;    // first look-back word of this level's plan
 };
 
 size_t level_smem_bytes(int stage);
 size_t plan_smem_bytes(int W);
+int plan_gates_per_tile(int W);   // gates (warps) of one planning block
 cudaError_t set_level_smem_limit(int stage, int W);   // the simulation kernels and the planning kernel
-cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // the plan
+cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // plan + placement
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s);      // the simulation
 cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s);          // both, in order
 cudaError_t launch_window_lengths(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,

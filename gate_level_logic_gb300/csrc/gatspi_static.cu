@@ -71,8 +71,9 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     p.slots_per_gate = p.ngroups << p.lpg_log2;
     const long long slots = (long long)a->num_gates * p.slots_per_gate;
     const long long tiles = slots > 0 ? (slots + kTileSlots - 1) / kTileSlots : 1;
-    const long long scan = a->num_gates > 0 ? a->num_gates : 1;      // one plan warp per gate
-    if (scan > kStaticTiles) return err(GATSPI_EINVAL, "level too large for the static scratch (at most 262144 gates)");
+    const long long scan = a->num_gates > 0 ? ((long long)a->num_gates + 31) / 32 : 1;   // placement tiles
+    if (scan > kStaticTiles)
+        return err(GATSPI_EINVAL, "level too large for the static scratch (at most 262144 x 32 gates)");
     if (tiles > INT32_MAX / kTileSlots) return err(GATSPI_EINVAL, "level has too many (gate, window) slots");
 
     // once per device, with that device current: the device address of the scratch

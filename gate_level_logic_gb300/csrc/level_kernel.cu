@@ -314,22 +314,13 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x, int lane) {
 // predecessors at once, closest first, and stops at the first inclusive prefix.
 // Publishes the tile's aggregate before looking back and its inclusive prefix
 // after.  Waits are bounded: a stalled predecessor raises GATSPI_ETIMEOUT.
-// Publish a tile's aggregate (tile 0: its inclusive prefix) ahead of look_back, so
-// that successors need not wait while the tile does other work.
-__device__ __forceinline__ void publish_aggregate(const DevParams &P, const LevelLaunch &L, int tile, long long total,
-                                                  int lane) {
-    if (lane == 0)
-        st_relaxed(P.tile_status + L.tile_base + tile, (tile == 0 ? kFlagIncl : kFlagAgg) | (unsigned long long)total);
-}
-
-__device__ long long look_back(const DevParams &P, const LevelLaunch &L, int tile, long long total, int lane,
-                               bool published = false) {
+__device__ long long look_back(const DevParams &P, const LevelLaunch &L, int tile, long long total, int lane) {
     unsigned long long *st = P.tile_status + L.tile_base;
     if (tile == 0) {
-        if (lane == 0 && !published) st_relaxed(st, kFlagIncl | (unsigned long long)total);
+        if (lane == 0) st_relaxed(st, kFlagIncl | (unsigned long long)total);
         return 0;
     }
-    if (lane == 0 && !published) st_relaxed(st + tile, kFlagAgg | (unsigned long long)total);
+    if (lane == 0) st_relaxed(st + tile, kFlagAgg | (unsigned long long)total);
     long long excl = 0;
     int k = tile - 1;
     const unsigned long long t0 = global_ns();
@@ -367,9 +358,10 @@ __device__ long long look_back(const DevParams &P, const LevelLaunch &L, int til
 }
 
 // The plan of one gate per warp: window bounds, their ranking (largest first,
-// stable), the offset of every group of 32 ranks, the region's pool offset.
-// Shared memory per warp: the bounds of the gate's windows, the bucket counters of
-// the counting sort, the group sums.
+// stable), the offset of every group of 32 ranks and the region's size, stored
+// after the group offsets (goff row of ngroups + 1 entries).  Shared memory per
+// warp: the bounds of the gate's windows, the bucket counters of the counting sort,
+// the group sums.  level_place_kernel then scans the sizes into pool offsets.
 __global__ void __launch_bounds__(kPlanWarps * 32) level_plan_kernel(const DevParams P, const LevelLaunch L) {
     extern __shared__ uint32_t psm[];
     const int lane = threadIdx.x & 31;
@@ -377,17 +369,13 @@ __global__ void __launch_bounds__(kPlanWarps * 32) level_plan_kernel(const DevPa
     uint32_t *bnd = psm + (size_t)warp * (P.W + kSortBuckets + P.ngroups);
     uint32_t *hist = bnd + P.W;
     uint32_t *gsum = hist + kSortBuckets;
-    int tile = 0;
-    if (lane == 0) tile = atomicAdd(P.tickets + L.level, 1);
-    tile = __shfl_sync(0xffffffffu, tile, 0);
-    if (tile >= L.scan_tiles) return;                      // spare warps of the last block
-    const bool skip = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
-    const int gl = tile;                                   // the gate of this warp
-    const bool valid = !skip && gl < L.num_gates;
+    const int gl = blockIdx.x * (blockDim.x >> 5) + warp;   // the gate of this warp
+    if (gl >= L.num_gates) return;
+    if (__shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0) return;
     const int g = L.gate_begin + gl;
     const int W = P.W;
     long long total = 0;
-    if (valid) {
+    {
         for (int k = lane; k < kSortBuckets; k += 32) hist[k] = 0;
         for (int k = lane; k < P.ngroups; k += 32) gsum[k] = 0;
         const int4 gd = __ldg(P.gate_desc + g);
@@ -429,9 +417,8 @@ __global__ void __launch_bounds__(kPlanWarps * 32) level_plan_kernel(const DevPa
         for (int o = 16; o >= 1; o >>= 1) lane_sum += __shfl_xor_sync(0xffffffffu, lane_sum, o);
         total = lane_sum;
         __syncwarp();
-        // the region's size is known: publish it before ranking, so that later
-        // gates can sum past this one while it ranks its windows
-        publish_aggregate(P, L, tile, total, lane);
+    }
+    {
         // bucket counts (bucket 0 = the largest bounds; bounds above 255 share it)
         for (int w = lane; w < W; w += 32)
             atomicAdd(&hist[kSortBuckets - 1 - min(bnd[w], (uint32_t)(kSortBuckets - 1))], 1u);
@@ -476,17 +463,42 @@ __global__ void __launch_bounds__(kPlanWarps * 32) level_plan_kernel(const DevPa
             const int j = j0 + lane;
             const uint32_t v = j < P.ngroups ? gsum[j] : 0u;
             const uint32_t incl = warp_incl_scan(v, lane);
-            if (j < P.ngroups) P.goff[(long long)gl * P.ngroups + j] = (uint32_t)(run + incl - v);
+            if (j < P.ngroups) P.goff[(long long)gl * (P.ngroups + 1) + j] = (uint32_t)(run + incl - v);
             run += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (lane == 0 && total >= (1ll << 32)) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, g, 1);
+        if (lane == 0) {
+            if (total >= (1ll << 32)) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, g, 1);
+            P.goff[(long long)gl * (P.ngroups + 1) + P.ngroups] = (uint32_t)total;   // the region's size
+        }
     }
-    const long long base = P.level_base[L.level] + look_back(P, L, tile, total, lane, valid);
+}
+
+// Pool offsets of the level's gate regions: their sizes (from the plan) scanned in
+// gate order, one thread per gate, warp shuffles plus a decoupled look-back over
+// warp tiles; the values are ready when this kernel starts, so the waits are short.
+__global__ void __launch_bounds__(kBlock) level_place_kernel(const DevParams P, const LevelLaunch L) {
+    const int lane = threadIdx.x & 31;
+    int tile = 0;
+    if (lane == 0) tile = atomicAdd(P.tickets + L.level, 1);
+    tile = __shfl_sync(0xffffffffu, tile, 0);
+    if (tile >= L.scan_tiles) return;                      // spare warps of the last block
+    const bool skip = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
+    const int gl = tile * 32 + lane;
+    const bool valid = !skip && gl < L.num_gates;
+    const long long size = valid ? (long long)__ldg(P.goff + (long long)gl * (P.ngroups + 1) + P.ngroups) : 0;
+    long long incl = size;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const long long total = __shfl_sync(0xffffffffu, incl, 31);
+    const long long base = P.level_base[L.level] + look_back(P, L, tile, total, lane);
     if (lane == 0 && tile == L.scan_tiles - 1) {
         P.level_base[L.level + 1] = base + total;
         if (base + total > P.pool_words) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, 0, 0);
     }
-    if (valid && lane == 0) P.net_base[(long long)P.num_inputs + g] = base;
+    if (valid) P.net_base[(long long)P.num_inputs + L.gate_begin + gl] = base + incl - size;
 }
 
 // One warp = 32 slots of the level: a gate and 32 of its ranks.  Warps share nothing
@@ -553,7 +565,7 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
                 bound += end - start;
             }
         }
-        gofs = __ldg(P.goff + (long long)gl * P.ngroups + c);
+        gofs = __ldg(P.goff + (long long)gl * (P.ngroups + 1) + c);
         base = __ldg(P.net_base + net) + gofs;
     }
     const uint32_t bincl = warp_incl_scan(bound, lane);
@@ -709,16 +721,20 @@ cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const i
 
 size_t level_smem_bytes(int stage) { return (size_t)kLevelWarps * 32 * (size_t)stage * sizeof(int32_t); }
 
-static int plan_warps(int W) { return W > 4096 ? 1 : kPlanWarps; }   // one warp per block for long window lists
+int plan_gates_per_tile(int W) { return W > 4096 ? 1 : kPlanWarps; }   // one warp per block for long window lists
 
 size_t plan_smem_bytes(int W) {   // per warp: W bounds, the buckets, the group sums
-    return (size_t)plan_warps(W) * ((size_t)W + kSortBuckets + (size_t)(W + 31) / 32) * sizeof(uint32_t);
+    return (size_t)plan_gates_per_tile(W) * ((size_t)W + kSortBuckets + (size_t)(W + 31) / 32) * sizeof(uint32_t);
 }
 
 cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
-    const int wpb = plan_warps(p.W);
-    const unsigned blocks = (unsigned)((l.scan_tiles + wpb - 1) / wpb);
-    level_plan_kernel<<<blocks, wpb * 32, plan_smem_bytes(p.W), s>>>(p, l);
+    const int wpb = plan_gates_per_tile(p.W);
+    if (l.num_gates > 0) {
+        level_plan_kernel<<<(unsigned)((l.num_gates + wpb - 1) / wpb), wpb * 32, plan_smem_bytes(p.W), s>>>(p, l);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    level_place_kernel<<<(unsigned)((l.scan_tiles + kWarps - 1) / kWarps), kBlock, 0, s>>>(p, l);
     return cudaGetLastError();
 }
 

@@ -355,7 +355,7 @@ gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *sim_ms, float *bounds_m
  *               aligned) holds min(length, 255) of waveform (net, w) at
  *               net * W4 + w, W4 = num_windows rounded up to a multiple of 4
  *   perm, goff  the level's plan (scratch, written then read by this call):
- *               uint16 [num_gates * num_windows] and uint32 [num_gates * ceil(W / 32)]
+ *               uint16 [num_gates * num_windows] and uint32 [num_gates * (ceil(W / 32) + 1)]
  *   tc, t1      per-gate toggle count and time at 1, accumulated (not cleared)
  *   level_base  int64 [2]: [0] = first pool word of this level's outputs (read),
  *               [1] = one past its last word (written)
@@ -400,9 +400,9 @@ typedef struct {
  * process exits.
  *
  *   - No cudaMalloc, cudaFree or allocating library call is made.
- *   - A level may have at most 262144 gates (one look-back flag each); a larger
- *     level returns GATSPI_EINVAL before anything runs.  The caller also makes sure
- *     the gates exist.
+ *   - A level may have at most 262144 x 32 = 8388608 gates (one look-back flag per
+ *     32); a larger level returns GATSPI_EINVAL before anything runs.  The caller
+ *     also makes sure the gates exist.
  *   - The first call on a device looks up the device address of the scratch array
  *     (with that device current); make that first call before any stream capture.
  *   - Every call shares the one array and clears the part it uses before its

@@ -83,7 +83,7 @@ class Caller:
         self.wlen8 = torch.zeros(self.N * W4, dtype=torch.uint8, device=dev)
         most = int(np.diff(net.level_offsets).max()) if net.num_levels else 1
         self.perm = torch.zeros(max(most * W, 1), dtype=torch.int16, device=dev)
-        self.goff = torch.zeros(max(most * self.nch, 1), dtype=torch.int32, device=dev)
+        self.goff = torch.zeros(max(most * (self.nch + 1), 1), dtype=torch.int32, device=dev)
         self.tc = torch.zeros(G, dtype=torch.int64, device=dev)
         self.t1 = torch.zeros(G, dtype=torch.int64, device=dev)
         self.level_base = torch.zeros(2, dtype=torch.int64, device=dev)
@@ -202,7 +202,7 @@ def test_static_errors_and_limits(built):
     assert _same_index(index, ref[0]) and np.array_equal(tc, ref[2])
     assert np.array_equal(_gather(pool, index), _gather(ref[1], ref[0]))
     # a level beyond the fixed scratch is refused before anything runs: one
-    # look-back flag per gate, and 2^25 gates > 262144
+    # look-back flag per 32 gates, and 2^25 gates > 262144 x 32
     assert stim.num_windows == 1
     big = caller.args(0, 1 << 25)
     with pytest.raises(GatspiError) as e:
