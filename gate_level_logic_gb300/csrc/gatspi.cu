@@ -67,7 +67,6 @@ struct gatspi_ctx {
 
     // device arrays owned by the context
     int4 *gate_desc = nullptr;
-    int4 *edge_desc = nullptr;
     int32_t *dly = nullptr;
     long long *net_base = nullptr;
     uint32_t *wstart = nullptr;
@@ -113,7 +112,6 @@ struct gatspi_ctx {
     DevParams params() const {
         DevParams p{};
         p.gate_desc = gate_desc;
-        p.edge_desc = edge_desc;
         p.dly_data = dly;
         p.pool = pool;
         p.pool_words = pool_words;
@@ -255,7 +253,7 @@ void free_all(gatspi_ctx *c) {
     if (c->dump_stream) cudaStreamDestroy(c->dump_stream);
     if (c->tc_host) cudaFreeHost(c->tc_host);
     if (c->t1_host) cudaFreeHost(c->t1_host);
-    void *ptrs[] = {c->gate_desc, c->edge_desc, c->dly, c->net_base, c->wstart, c->wend, c->wlen8, c->perm, c->goff,
+    void *ptrs[] = {c->gate_desc, c->dly, c->net_base, c->wstart, c->wend, c->wlen8, c->perm, c->goff,
                     c->window_len, c->tc, c->t1,
                     c->tile_status, c->tickets, c->level_base, c->status, c->load_off, c->max_time,
                     c->win_start, c->tc_in, c->t1_in};
@@ -396,10 +394,8 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         c->path_delay_bound = path_bound;
         for (int w = 0; w < c->W; ++w) c->sum_window_len += cfg->window_len[w];
 
-        // gate and edge descriptors
-        const long long E = c->G > 0 ? nl->fanin_off[c->G] : 0;
-        std::vector<int4> gd(std::max(c->G, 1));
-        std::vector<int4> ed(std::max<long long>(E, 1));
+        // gate records: descriptor, source nets, wire delays (unused pins: 0)
+        std::vector<int4> gd(3 * std::max(c->G, 1), make_int4(0, 0, 0, 0));
         for (long long g = 0; g < c->G; ++g) {
             const int t = nl->gate_type[g];
             const int n = nl->type_num_pins[t];
@@ -414,12 +410,15 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
                 mask |= (uint32_t)nl->tt_data[nl->type_tt_off[t] + k] << v;
             }
             const long long d0 = nl->gate_dly_off[g];
-            gd[g] = make_int4(nl->fanin_off[g], (int)(n | (mask << 8)), (int)(uint32_t)(d0 & 0xffffffffll),
-                              (int)(d0 >> 32));
+            int src[4] = {0, 0, 0, 0}, drf[4] = {0, 0, 0, 0};
+            for (int i = 0; i < n; ++i) {
+                src[i] = nl->fanin_net[e0 + i];
+                drf[i] = (int)((uint32_t)nl->wire_rise[e0 + i] | ((uint32_t)nl->wire_fall[e0 + i] << 16));
+            }
+            gd[3 * g] = make_int4(0, (int)(n | (mask << 8)), (int)(uint32_t)(d0 & 0xffffffffll), (int)(d0 >> 32));
+            gd[3 * g + 1] = make_int4(src[0], src[1], src[2], src[3]);
+            gd[3 * g + 2] = make_int4(drf[0], drf[1], drf[2], drf[3]);
         }
-        for (long long e = 0; e < E; ++e)
-            ed[e] = make_int4(nl->fanin_net[e], nl->pin_weight[e],
-                              (int)((uint32_t)nl->wire_rise[e] | ((uint32_t)nl->wire_fall[e] << 16)), 0);
 
         // levels and tiles
         c->level_offsets.assign(nl->level_offsets, nl->level_offsets + c->L + 1);
@@ -443,7 +442,6 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
 
         const long long dly_len = c->G > 0 ? nl->dly_len : 0;
         CUDA_TRY(dev_alloc(&c->gate_desc, gd.size()), "allocating gate descriptors");
-        CUDA_TRY(dev_alloc(&c->edge_desc, ed.size()), "allocating edge descriptors");
         CUDA_TRY(dev_alloc(&c->dly, (size_t)dly_len), "allocating delay tables");
         CUDA_TRY(dev_alloc(&c->net_base, (size_t)std::max<long long>(c->num_nets, 1)), "allocating the window index");
         CUDA_TRY(dev_alloc(&c->wstart, (size_t)(c->num_nets * c->W)), "allocating the window index");
@@ -476,7 +474,6 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(cudaMemcpy(c->win_start, ws.data(), ws.size() * sizeof(long long), cudaMemcpyHostToDevice),
                  "uploading window starts");
         CUDA_TRY(cudaMemcpy(c->gate_desc, gd.data(), gd.size() * sizeof(int4), cudaMemcpyHostToDevice), "uploading gates");
-        CUDA_TRY(cudaMemcpy(c->edge_desc, ed.data(), ed.size() * sizeof(int4), cudaMemcpyHostToDevice), "uploading edges");
         if (dly_len > 0) {
             std::vector<int32_t> packed;
             layout_delay_tables(nl, packed);

@@ -40,9 +40,9 @@ constexpr int kStatusWords = 4;
 // Everything a level kernel reads or writes, by value in the kernel parameters.
 struct DevParams {
     // netlist
-    const int4 *gate_desc;     // [G] x = first edge, y = n | truth table << 8, z/w = delay-table offset lo/hi;
+    const int4 *gate_desc;     // [3G] per gate: {0, n | truth table << 8, delay-table offset lo/hi},
+                               //     {source net of pin 0..3}, {wire rise | fall << 16 of pin 0..3};
                                //     truth-table bit k = output for pin values k (first pin most significant)
-    const int4 *edge_desc;     // [E] x = source net, y = truth-table weight (unused here), z = wire rise | fall << 16
     const int32_t *dly_data;   // per-instance conditional delay tables
     // waveform store: waveform (net, w) is pool[net_base[net] + wstart[k] .. net_base[net] + wend[k]),
     // k = net * W + w, EOW included

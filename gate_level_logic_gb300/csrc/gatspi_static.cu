@@ -44,11 +44,10 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
         return s;
     };
     if (!a) return err(GATSPI_EINVAL, "args are required");
-    if (!a->gate_desc || !a->edge_desc || !a->dly_data || !a->window_len || !a->pool || !a->net_base ||
+    if (!a->gate_desc || !a->dly_data || !a->window_len || !a->pool || !a->net_base ||
         !a->wstart || !a->wend || !a->wlen8 || !a->perm || !a->goff || !a->tc || !a->t1 || !a->level_base)
         return err(GATSPI_EINVAL, "every buffer of gatspi_level_args is required");
-    if (((uintptr_t)a->gate_desc & 15) || ((uintptr_t)a->edge_desc & 15))
-        return err(GATSPI_EINVAL, "gate_desc and edge_desc must be 16-byte aligned");
+    if ((uintptr_t)a->gate_desc & 15) return err(GATSPI_EINVAL, "gate_desc must be 16-byte aligned");
     if ((uintptr_t)a->wlen8 & 3) return err(GATSPI_EINVAL, "wlen8 must be 4-byte aligned");
     if (a->num_inputs < 0 || a->num_windows < 1 || a->gate_begin < 0 || a->num_gates < 0 || a->pool_words < 0)
         return err(GATSPI_EINVAL, "negative sizes");
@@ -97,7 +96,6 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     unsigned long long *words = (unsigned long long *)scratch;
 
     p.gate_desc = (const int4 *)a->gate_desc;
-    p.edge_desc = (const int4 *)a->edge_desc;
     p.dly_data = a->dly_data;
     p.pool = a->pool;
     p.pool_words = a->pool_words;

@@ -378,11 +378,13 @@ __global__ void __launch_bounds__(kPlanWarps * 32) level_plan_kernel(const DevPa
     {
         for (int k = lane; k < kSortBuckets; k += 32) hist[k] = 0;
         for (int k = lane; k < P.ngroups; k += 32) gsum[k] = 0;
-        const int4 gd = __ldg(P.gate_desc + g);
+        const int4 gd = __ldg(P.gate_desc + 3 * (long long)g);
+        const int4 sv = __ldg(P.gate_desc + 3 * (long long)g + 1);
         const int n = gd.y & 7;
+        const int s4[GATSPI_MAX_PINS] = {sv.x, sv.y, sv.z, sv.w};
         long long src[GATSPI_MAX_PINS];
 #pragma unroll
-        for (int i = 0; i < GATSPI_MAX_PINS; ++i) src[i] = i < n ? (long long)__ldg(P.edge_desc + gd.x + i).x : 0;
+        for (int i = 0; i < GATSPI_MAX_PINS; ++i) src[i] = i < n ? (long long)s4[i] : 0;
         __syncwarp();
         // bounds from the one-byte window lengths, four consecutive windows per lane
         // and load; a length of 255 or more is read exactly from the index
@@ -548,20 +550,23 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     long long base = 0;     // the group's first pool word
     Pin pins[GATSPI_MAX_PINS];
     if (valid) {
-        gd = __ldg(P.gate_desc + g);
+        gd = __ldg(P.gate_desc + 3 * (long long)g);
+        const int4 sv = __ldg(P.gate_desc + 3 * (long long)g + 1);
+        const int4 dv = __ldg(P.gate_desc + 3 * (long long)g + 2);
+        const int s4[GATSPI_MAX_PINS] = {sv.x, sv.y, sv.z, sv.w};
+        const int d4[GATSPI_MAX_PINS] = {dv.x, dv.y, dv.z, dv.w};
         Lw = __ldg(P.window_len + w);
         const int n = gd.y & 7;
         bound = 3u - 2u * (uint32_t)n;
 #pragma unroll
         for (int i = 0; i < GATSPI_MAX_PINS; ++i) {
             if (i < n) {
-                const int4 e = __ldg(P.edge_desc + gd.x + i);
-                const long long src = e.x;
+                const long long src = s4[i];
                 const uint32_t end = __ldg(P.wend + src * P.W + w);
                 const uint32_t start = __ldg(P.wstart + src * P.W + w);
                 pins[i].w = P.pool + __ldg(P.net_base + src) + start;
                 pins[i].len = (int32_t)(end - start);
-                pins[i].drf = (uint32_t)e.z;
+                pins[i].drf = (uint32_t)d4[i];
                 bound += end - start;
             }
         }

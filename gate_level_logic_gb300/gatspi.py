@@ -54,7 +54,7 @@ class gatspi_views(ctypes.Structure):
 
 class gatspi_level_args(ctypes.Structure):
     _fields_ = [
-        ("gate_desc", _p), ("edge_desc", _p), ("dly_data", _p), ("window_len", _p), ("pool", _p),
+        ("gate_desc", _p), ("dly_data", _p), ("window_len", _p), ("pool", _p),
         ("pool_words", ctypes.c_int64), ("net_base", _p), ("wstart", _p), ("wend", _p), ("wlen8", _p), ("perm", _p),
         ("goff", _p),
         ("tc", _p), ("t1", _p),

@@ -335,14 +335,14 @@ gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *sim_ms, float *bounds_m
 /*
  * Buffers of one logic level for gatspi_simulate_level_static (all device memory,
  * owned by the caller).  The layouts are the library's own:
- *   gate_desc   int32 [4 * num_gates of the netlist], 16-byte aligned; for gate g:
- *               {first edge of g, n | truth-table bits << 8, low and high 32 bits
- *               of the delay-table offset}; truth-table bit v is the output when the
- *               pin values, read as a binary number with the first pin most
- *               significant, equal v (the page's table re-indexed by pin weight)
- *   edge_desc   int32 [4 * edges], 16-byte aligned; for edge e:
- *               {driving net, truth-table weight (not read), wire rise | wire fall
- *               << 16, 0}
+ *   gate_desc   int32 [12 * num_gates of the netlist], 16-byte aligned; gate g's
+ *               record is the 12 words at 12 * g:
+ *               {0, n | truth-table bits << 8, low and high 32 bits of the
+ *               delay-table offset}, {the net driving pin 0, 1, 2, 3},
+ *               {wire rise | wire fall << 16 of pin 0, 1, 2, 3}, pins past n being 0;
+ *               truth-table bit v is the output when the pin values, read as a
+ *               binary number with the first pin most significant, equal v (the
+ *               page's table re-indexed by pin weight)
  *   dly_data    the delay tables of gatspi_netlist laid out for the kernel: the entry
  *               of row 4*i + 2*e_in + e_out and column c of gate g's table sits at
  *               dly_data[gate_dly_off[g] + (((2*i + e_out) << n) | v)], v being all n
@@ -365,7 +365,6 @@ gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *sim_ms, float *bounds_m
  */
 typedef struct {
     const int32_t *gate_desc;
-    const int32_t *edge_desc;
     const int32_t *dly_data;
     const int32_t *window_len;
     int32_t *pool;

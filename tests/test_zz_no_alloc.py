@@ -39,24 +39,26 @@ def _kernel_tables(net):
 
 
 def _pack(net):
-    """The library's per-gate and per-edge descriptors (layout of gatspi_level_args)."""
-    G, E = net.num_gates, net.num_edges
+    """The library's gate records (layout of gatspi_level_args): per gate the
+    descriptor, the source net of every pin and every pin's wire delays."""
+    G = net.num_gates
     n = net.type_num_pins[net.gate_type].astype(np.int64)
     mask = np.zeros(G, np.int64)
     for t in range(len(net.type_num_pins)):
         nt = int(net.type_num_pins[t])
         bits = sum(int(net.tt_data[net.type_tt_off[t] + k]) << k for k in range(1 << nt))
         mask[net.gate_type == t] = bits
-    gd = np.zeros((G, 4), np.int64)
-    gd[:, 0] = net.fanin_off[:-1]
+    gd = np.zeros((G, 12), np.int64)
     gd[:, 1] = n | (mask << 8)
     gd[:, 2] = net.gate_dly_off & 0xFFFFFFFF
     gd[:, 3] = net.gate_dly_off >> 32
-    ed = np.zeros((E, 4), np.int64)
-    ed[:, 0] = net.fanin_net
-    ed[:, 1] = net.pin_weight
-    ed[:, 2] = net.wire_rise.astype(np.int64) | (net.wire_fall.astype(np.int64) << 16)
-    return gd.astype(np.uint32).view(np.int32).ravel(), ed.astype(np.int32).ravel()
+    wires = net.wire_rise.astype(np.int64) | (net.wire_fall.astype(np.int64) << 16)
+    for i in range(4):
+        has = n > i
+        e = net.fanin_off[:-1][has] + i
+        gd[has, 4 + i] = net.fanin_net[e]
+        gd[has, 8 + i] = wires[e]
+    return gd.astype(np.uint32).view(np.int32).ravel()
 
 
 class Caller:
@@ -70,9 +72,7 @@ class Caller:
         P, G, W = net.num_inputs, net.num_gates, stim.num_windows
         self.N, self.W, self.nch = P + G, W, (W + 31) // 32
         dev = torch.device("cuda", 0)
-        gd, ed = _pack(net)
-        self.gate_desc = torch.from_numpy(gd).to(dev)
-        self.edge_desc = torch.from_numpy(ed).to(dev)
+        self.gate_desc = torch.from_numpy(_pack(net)).to(dev)
         self.dly = torch.from_numpy(_kernel_tables(net)).to(dev)
         self.window_len = torch.from_numpy(np.ascontiguousarray(stim.window_len, np.int32)).to(dev)
         self.pool = torch.zeros(pool_words, dtype=torch.int32, device=dev)
@@ -107,7 +107,7 @@ class Caller:
     def args(self, gate_begin, num_gates, pool_words=None):
         g = self.gatspi
         return g.gatspi_level_args(
-            self.gate_desc.data_ptr(), self.edge_desc.data_ptr(), self.dly.data_ptr(), self.window_len.data_ptr(),
+            self.gate_desc.data_ptr(), self.dly.data_ptr(), self.window_len.data_ptr(),
             self.pool.data_ptr(), self.pool.numel() if pool_words is None else pool_words,
             self.net_base.data_ptr(), self.wstart.data_ptr(), self.wend.data_ptr(), self.wlen8.data_ptr(),
             self.perm.data_ptr(),
