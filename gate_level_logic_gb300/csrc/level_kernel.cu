@@ -99,36 +99,33 @@ __device__ __forceinline__ int32_t reject_limit(int32_t d, int32_t q) {
 // its first edge (the fall delay when the pin is at 1, the rise delay when at 0),
 // or than that delay's reject limit when kFull is false; the arrival is the next
 // timestamp plus the delay.  On entry s.nx holds w[p + 1] (the word after the
-// previous pulse test), so a step loads one word; a skipped pulse reloads.  False on
-// a malformed wave.
+// previous pulse test), so a step loads one word.  The common step is straight-line
+// code, so that lanes advancing different pins stay together; only a swallowed
+// pulse takes the loop.  False on a malformed wave.
 // t2pre: w[p + 2] when the caller has it already (a wave's first words are loaded
 // together), else unused.
 template <bool kFull, bool kPre = false>
 __device__ __forceinline__ bool next_arrival(Pin &s, int32_t q, int32_t t2pre = 0) {
-    bool pre = kPre;
-    for (;;) {
-        // p + 1 == len - 1 is the EOW slot: no further transition
-        if (s.p + 2 >= s.len) {
-            s.a = kEOW;
-            return s.p + 2 == s.len;
+    bool last = s.p + 2 >= s.len;                  // p + 1 is the EOW slot: no further transition
+    int32_t t1 = s.nx;
+    int32_t t2 = kPre ? t2pre : (last ? kEOW : __ldg(s.w + s.p + 2));
+    const int32_t d = (s.p & 1) ? (int32_t)(s.drf >> 16) : (int32_t)(s.drf & 0xffffu);
+    const int32_t lim = kFull ? d : reject_limit(d, q);
+    bool bad = !last && t1 == kEOW;                 // EOW before the last slot: malformed
+    if (!last && !bad && t2 - t1 < lim) {           // the pulse [t1, t2) never reaches the pin
+        for (;;) {
+            s.p += 2;                               // same parity: same delay
+            last = s.p + 2 >= s.len;
+            if (last) break;
+            t1 = __ldg(s.w + s.p + 1);
+            t2 = __ldg(s.w + s.p + 2);
+            bad = t1 == kEOW;
+            if (bad || t2 - t1 >= lim) break;
         }
-        const int32_t t1 = s.nx;
-        const int32_t t2 = pre ? t2pre : __ldg(s.w + s.p + 2);
-        pre = false;
-        if (t1 == kEOW) {                // EOW before the last slot: malformed
-            s.a = kEOW;
-            return false;
-        }
-        const int32_t d = (s.p & 1) ? (int32_t)(s.drf >> 16) : (int32_t)(s.drf & 0xffffu);
-        if (t2 - t1 < (kFull ? d : reject_limit(d, q))) {   // the pulse [t1, t2) never reaches the pin
-            s.p += 2;
-            s.nx = s.p + 1 < s.len ? __ldg(s.w + s.p + 1) : kEOW;
-            continue;
-        }
-        s.a = t1 + d;
-        s.nx = t2;                       // w[p + 2]: the next transition once this one is taken
-        return true;
     }
+    s.a = (last || bad) ? kEOW : t1 + d;
+    s.nx = t2;                                      // w[p + 2]: the next transition once this one is taken
+    return last ? s.p + 2 == s.len : !bad;
 }
 
 struct LaneResult {
@@ -218,7 +215,7 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
     put(0, y0 ? -1 : 0);
     if (y0) put(1, 0);
 
-    bool ok = true;
+    bool ok = true, lutbad = false;
 #pragma unroll
     for (int i = 0; i < N; ++i) ok &= next_arrival<kFull, true>(pin[i], q, t2first[i]);
 
@@ -240,36 +237,44 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
         const int hb = 31 - __clz(swb);
         const int k = N - 1 - hb;                       // first switching pin
         const uint32_t more = swb & ~(1u << hb);        // any others (simultaneous switching)
+        // output update as selects, not branches, so that the lanes stay together:
+        // chg = the truth table changes the output; then the inertial filter either
+        // cancels the last entry or stores a new one
         const int32_t y = (tt >> vbits) & 1;
-        if (y != (po & 1)) {
-            // smallest finite conditional delay among the switching pins
-            const int e_out = y ? 0 : 1;
-            int32_t d = arc_delay<N>(D, vbits, k, e_out);
-            for (uint32_t m = more; m; m &= m - 1u) d = min(d, arc_delay<N>(D, vbits, N - __ffs(m), e_out));
-            if (d == kNoArc) {
-                r.err = GATSPI_EBADLUT;
-                break;
-            }
-            const int32_t to = t + d;
-            // inertial filter: at q = 100, to - top < d exactly when the last entry
-            // has not matured (top > t); otherwise the reject limit decides
-            if (kFull ? top > t : to - top < reject_limit(d, q)) {
-                t1acc -= (po & 1) ? -min(top, Lw) : min(top, Lw);
-                --po;
-                top = second;
-                if (!kFull) second = po > 0 ? get(po - 1) : 0;   // the exposed entry may be pending too
-            } else {
-                ++po;
-                put(po, to);
-                t1acc += (po & 1) ? -min(to, Lw) : min(to, Lw);
-                second = top;
-                top = to;
-            }
+        const int e_out = y ^ 1;
+        // smallest finite conditional delay among the switching pins
+        int32_t d = arc_delay<N>(D, vbits, k, e_out);
+        for (uint32_t m = more; m; m &= m - 1u) d = min(d, arc_delay<N>(D, vbits, N - __ffs(m), e_out));
+        bool chg = y != (po & 1);
+        lutbad |= chg && d == kNoArc;
+        chg = chg && d != kNoArc;
+        const int32_t to = t + (chg ? d : 0);
+        // inertial filter: at q = 100, to - top < d exactly when the last entry
+        // has not matured (top > t); otherwise the reject limit decides
+        const bool cancel = chg && (kFull ? top > t : to - top < reject_limit(d, q));
+        const bool store = chg && !cancel;
+        // time at 1: a cancelled entry gives back what it added, a stored one adds
+        // its clipped time with the sign of its parity; both come to this
+        const int32_t c = min(cancel ? top : to, Lw);
+        t1acc += chg ? ((po & 1) ? c : -c) : 0;
+        po += store ? 1 : (cancel ? -1 : 0);
+        if (store) put(po, to);
+        if (kFull) {
+            const int32_t ntop = cancel ? second : (store ? to : top);
+            second = store ? top : second;
+            top = ntop;
+        } else if (cancel) {
+            top = second;
+            second = po > 0 ? get(po - 1) : 0;           // the exposed entry may be pending too
+        } else if (store) {
+            second = top;
+            top = to;
         }
         ok &= advance_pin<N, kFull>(pin, k, q);
         for (uint32_t m = more; m; m &= m - 1u) ok &= advance_pin<N, kFull>(pin, N - __ffs(m), q);   // lowest bit first
     }
     if (!ok) r.err = GATSPI_EBADWAVE;
+    if (lutbad) r.err = GATSPI_EBADLUT;     // a missing arc is met before any later malformed word
     put(po + 1, kEOW);
     r.len = po + 2;
     r.tc = po - y0;
