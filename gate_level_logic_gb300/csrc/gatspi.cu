@@ -132,6 +132,7 @@ struct gatspi_ctx {
         p.num_inputs = P;
         p.W = W;
         p.ngroups = ngroups;
+        p.ngroups_m = 0xffffffffu / (uint32_t)ngroups;
         p.lpg_log2 = lpg_log2;
         p.slots_per_gate = slots_per_gate;
         p.stage = stage;

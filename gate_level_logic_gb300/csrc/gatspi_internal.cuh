@@ -70,6 +70,7 @@ struct DevParams {
     int32_t W;
     int32_t w8stride;         // W rounded up to a multiple of 4 (rows of wlen8 start 4-byte aligned)
     int32_t ngroups;          // ceil(W / 32): groups of 32 ranks per gate
+    uint32_t ngroups_m;       // floor((2^32 - 1) / ngroups): tile / ngroups by a multiply-high
     int32_t lpg_log2;         // log2(lanes per (gate, group) segment)
     int32_t slots_per_gate;   // ngroups << lpg_log2
     int32_t stage;            // output words staged on chip per lane

@@ -60,6 +60,7 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     DevParams p{};
     p.W = a->num_windows;
     p.ngroups = (p.W + 31) / 32;
+    p.ngroups_m = 0xffffffffu / (uint32_t)p.ngroups;
     int lpg = 32;
     if (p.W < 32) {
         lpg = 1;

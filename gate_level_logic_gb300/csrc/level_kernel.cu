@@ -525,8 +525,11 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     // rank to a window
     int gl, c, j;
     if (P.lpg_log2 == 5) {
-        gl = tile / P.ngroups;
+        // tile / ngroups: the multiply-high estimate is at most two below the quotient
+        gl = (int)__umulhi((uint32_t)tile, P.ngroups_m);
         c = tile - gl * P.ngroups;
+        if (c >= P.ngroups) { ++gl; c -= P.ngroups; }
+        if (c >= P.ngroups) { ++gl; c -= P.ngroups; }
         j = lane;
     } else {
         const int slot = tile * 32 + lane;
@@ -599,9 +602,16 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
 
     // TC and T1 per (gate, group): reduce over the segment's lanes, one atomic each
     long long tcs = res.tc, t1s = res.t1;
-    for (int o = (1 << P.lpg_log2) >> 1; o >= 1; o >>= 1) {
-        tcs += __shfl_xor_sync(0xffffffffu, tcs, o);
-        t1s += __shfl_xor_sync(0xffffffffu, t1s, o);
+    if (P.lpg_log2 == 5) {
+        // one gate per warp: exact 64-bit sums of the 32-bit counts from 16-bit halves
+        const uint32_t tcu = (uint32_t)res.tc, t1u = (uint32_t)res.t1;
+        tcs = ((long long)__reduce_add_sync(0xffffffffu, tcu >> 16) << 16) + __reduce_add_sync(0xffffffffu, tcu & 0xffffu);
+        t1s = ((long long)__reduce_add_sync(0xffffffffu, t1u >> 16) << 16) + __reduce_add_sync(0xffffffffu, t1u & 0xffffu);
+    } else {
+        for (int o = (1 << P.lpg_log2) >> 1; o >= 1; o >>= 1) {
+            tcs += __shfl_xor_sync(0xffffffffu, tcs, o);
+            t1s += __shfl_xor_sync(0xffffffffu, t1s, o);
+        }
     }
     if (gate_ok && j == 0) {
         atomicAdd(P.tc + g, (unsigned long long)tcs);
