@@ -84,13 +84,12 @@ def _sum_over_ranks(dist, x: float) -> float:
     return float(t.item())
 
 
-def workload_config(net, stim, stage_words, pulse_percent=100):
+def workload_config(net, stim, pulse_percent=100):
     return {
         "workload": "1M-gate synthetic netlist, 40 levels, 9-cell mix with SDF-conditional arcs; "
                     "4096 inputs, 10k cycles x period 1000, 5% activity, 10% glitch pairs; 256 cycle windows",
         "gates": int(net.num_gates), "levels": int(net.num_levels), "inputs": int(net.num_inputs),
         "edges": int(net.num_edges), "windows": int(stim.num_windows), "cycles": int(stim.window_cycles.sum()),
-        "stage_words": stage_words,
         "pulse_percent": pulse_percent,
         "l2": "inputs larger than L2 (waveform pool of several GB per step, no flush needed)",
     }
@@ -246,7 +245,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": workload_config(net, stim, None, args.pulse_percent),
+        "config": workload_config(net, stim, args.pulse_percent),
         "gate_cycles_per_s": net.num_gates * cycles * args.steps / total,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, n), "kind": "oracle",
                          "sample": "%d of %d windows per step (all gates)" % (n, W)},
@@ -357,7 +356,7 @@ def run_gpu(args):
     W = stim.num_windows
     flags = gatspi.GATSPI_FLAG_LEVEL_TIMING
     pool_words = int(args.pool_gb * (1 << 30) / 4)
-    sim = Simulator(net, stim.window_len, pool_words=pool_words, stage_words=args.stage_words, flags=flags,
+    sim = Simulator(net, stim.window_len, pool_words=pool_words, flags=flags,
                     pulse_percent=args.pulse_percent)
     stream = torch.cuda.current_stream()
     sim.load(stim.pi_off, stim.pi_words, stream=stream)
@@ -422,7 +421,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": workload_config(net, stim, args.stage_words, args.pulse_percent),
+        "config": workload_config(net, stim, args.pulse_percent),
         "gate_cycles_per_s": gate_cycles_per_s,
         "events_per_step": events_per_step,
         "pool_words_used": pool_used,
@@ -465,7 +464,6 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--stage-words", type=int, default=-1)
     ap.add_argument("--pulse-percent", type=int, default=100,
                     help="PATHPULSEPERCENT of both inertial filters (100 = the page's setting, 0 = transport)")
     ap.add_argument("--pool-gb", type=float, default=48.0)

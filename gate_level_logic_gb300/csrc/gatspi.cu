@@ -61,7 +61,6 @@ struct gatspi_ctx {
     long long num_nets = 0;
     int32_t *pool = nullptr;
     long long pool_words = 0;
-    int stage = kDefaultStage;
     uint32_t flags = 0;
     int32_t pulse_percent = 100;
 
@@ -135,7 +134,6 @@ struct gatspi_ctx {
         p.ngroups_m = 0xffffffffu / (uint32_t)ngroups;
         p.lpg_log2 = lpg_log2;
         p.slots_per_gate = slots_per_gate;
-        p.stage = stage;
         p.pulse_percent = pulse_percent;
         return p;
     }
@@ -155,8 +153,6 @@ gatspi_status validate(const gatspi_netlist *nl, const gatspi_config *cfg, long 
     for (int w = 0; w < cfg->num_windows; ++w)
         if (cfg->window_len[w] < 1 || cfg->window_len[w] > (1ll << 30))
             return fail(GATSPI_EINVAL, "window %d: length must be in 1 .. 2^30", w);
-    if (cfg->stage_words < -1 || cfg->stage_words > kMaxStage)
-        return fail(GATSPI_EINVAL, "stage_words must be -1 or 0 .. %d", kMaxStage);
     if ((cfg->flags & GATSPI_FLAG_PULSE_PERCENT) && (cfg->pulse_percent < 0 || cfg->pulse_percent > 100))
         return fail(GATSPI_EINVAL, "pulse_percent must be 0 .. 100");
     if (G == 0) {
@@ -381,7 +377,6 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         c->pool = d_pool;
         c->pool_words = (long long)pool_words;
         c->flags = cfg->flags;
-        c->stage = cfg->stage_words < 0 ? kDefaultStage : cfg->stage_words;
         c->pulse_percent = (cfg->flags & GATSPI_FLAG_PULSE_PERCENT) ? cfg->pulse_percent : 100;
         c->num_nets = (long long)c->P + c->G;
         c->ngroups = (c->W + 31) / 32;
@@ -486,7 +481,7 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(cudaMemset(c->status, 0, sizeof(int32_t) * kStatusWords), "clearing the status");
         CUDA_TRY(cudaMemset(c->tc, 0, sizeof(unsigned long long) * std::max(c->G, 1)), "clearing TC");
         CUDA_TRY(cudaMemset(c->t1, 0, sizeof(unsigned long long) * std::max(c->G, 1)), "clearing T1");
-        CUDA_TRY(set_level_smem_limit(c->stage, c->W), "configuring shared memory");
+        CUDA_TRY(set_level_smem_limit(c->W), "configuring shared memory");
         if (c->flags & GATSPI_FLAG_LEVEL_TIMING) {
             c->events.resize(2 * c->L + 1, nullptr);
             for (auto &e : c->events) CUDA_TRY(cudaEventCreate(&e), "creating level events");

@@ -23,8 +23,6 @@ constexpr int kLevelMinBlocks = GATSPI_LEVEL_MIN_BLOCKS;  // resident blocks per
 constexpr int kTileSlots = 32;            // (gate, rank) slots per warp of the level kernel
 constexpr int kPlanWarps = 4;             // warps per block of the planning kernel (one gate each)
 constexpr int kSortBuckets = 256;         // counting-sort buckets of the window bounds
-constexpr int kMaxStage = 64;             // upper bound of stage_words
-constexpr int kDefaultStage = 24;
 constexpr int32_t kEOW = GATSPI_EOW;
 constexpr int32_t kNoArc = GATSPI_NO_ARC;
 
@@ -73,7 +71,6 @@ struct DevParams {
     uint32_t ngroups_m;       // floor((2^32 - 1) / ngroups): tile / ngroups by a multiply-high
     int32_t lpg_log2;         // log2(lanes per (gate, group) segment)
     int32_t slots_per_gate;   // ngroups << lpg_log2
-    int32_t stage;            // output words staged on chip per lane
     int32_t pulse_percent;    // PATHPULSEPERCENT, 0 .. 100
 };
 
@@ -86,10 +83,9 @@ struct LevelLaunch {
     long long tile_base;    // first look-back word of this level's plan
 };
 
-size_t level_smem_bytes(int stage);
 size_t plan_smem_bytes(int W);
 int plan_gates_per_tile(int W);   // gates (warps) of one planning block
-cudaError_t set_level_smem_limit(int stage, int W);   // the simulation kernels and the planning kernel
+cudaError_t set_level_smem_limit(int W);   // the planning kernel's shared memory, the simulation kernels' L1
 cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // plan + placement
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s);      // the simulation
 cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s);          // both, in order

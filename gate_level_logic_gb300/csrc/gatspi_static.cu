@@ -52,7 +52,6 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     if (a->num_inputs < 0 || a->num_windows < 1 || a->gate_begin < 0 || a->num_gates < 0 || a->pool_words < 0)
         return err(GATSPI_EINVAL, "negative sizes");
     if (a->num_windows > GATSPI_MAX_WINDOWS) return err(GATSPI_EINVAL, "too many windows");
-    if (a->stage_words < -1 || a->stage_words > kMaxStage) return err(GATSPI_EINVAL, "stage_words out of range");
     const bool own_percent = (a->flags & GATSPI_FLAG_PULSE_PERCENT) != 0;
     if (own_percent && (a->pulse_percent < 0 || a->pulse_percent > 100))
         return err(GATSPI_EINVAL, "pulse_percent must be 0 .. 100");
@@ -115,7 +114,6 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     p.level_base = (long long *)a->level_base;
     p.status = (int32_t *)(words + kStatusWord);
     p.num_inputs = a->num_inputs;
-    p.stage = a->stage_words < 0 ? kDefaultStage : a->stage_words;
     p.pulse_percent = own_percent ? a->pulse_percent : 100;
 
     LevelLaunch l{};
@@ -128,7 +126,7 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
 
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_level_smem_limit(p.stage, p.W);
+    if (e == cudaSuccess) e = set_level_smem_limit(p.W);
     // clear the flags of the tiles this call uses, the ticket and the status
     if (e == cudaSuccess) e = cudaMemsetAsync(words, 0, sizeof(unsigned long long) * (size_t)scan, s);
     if (e == cudaSuccess)

@@ -30,15 +30,14 @@
 // floor(d * q / 100), several output entries can be pending and a cancel re-reads
 // the entry before the one it exposes from the lane's own output.  Before
 // simulating, each lane turns its inputs' lengths into its window's bound and a warp
-// scan gives the window a provisional slot in the group's part of the region.  The
-// lane keeps the first `stage` output words in shared memory ([word][lane] layout,
-// bank-conflict free) and writes any further word straight to its provisional
-// slot.  A warp scan of the actual lengths then places every window in rank order;
-// spilled words are moved down to their final place and the staged words are
-// stored.  Every (gate, window) is simulated once.  The window index records each
-// window's start and end relative to its net's region, since windows are stored in
-// rank order.  TC and T1 are reduced per warp with shuffles and one 64-bit atomic
-// each.  No warp waits for another.
+// scan gives the window its slot, bound-sized, in the group's part of the region;
+// the lane writes its output words straight there, and the gap after them (bound
+// minus length) stays unused.  Every (gate, window) is simulated once and no word is
+// moved afterwards.  The window index records each window's start and end relative
+// to its net's region, since windows are stored in rank order.  TC and T1 are
+// reduced per warp and added with one 64-bit atomic each.  The kernel uses no shared
+// memory, so the SM's whole L1 serves the source waveforms.  No warp waits for
+// another.
 //
 // No kernel traps: a malformed waveform, a missing delay arc, pool overflow or a
 // stalled look-back sets the device status word and the kernels carry on without
@@ -164,24 +163,20 @@ __device__ __forceinline__ bool advance_pin(Pin (&pin)[N], int k, int32_t q) {
     return ok;
 }
 
-// Algorithm 1 for one (gate, window).  The first `stage_words` output words go to
-// shared memory (stride 32), the rest to gout, the window's provisional slot in the
-// pool.
+// Algorithm 1 for one (gate, window).  The output words go to gout, the window's
+// slot in the pool.
 // The loop body is written so that a warp's lanes stay together: the switching
 // pins form a bit mask, the delay lookup and the pin advance serve the first
 // switching pin through a lane-selected pin state, and only simultaneous
 // switching of several pins takes an extra (rare) loop.
 template <int N, bool kFull>
 __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const int32_t *__restrict__ D, int32_t Lw,
-                                               int32_t *stage, int stage_words, int32_t *__restrict__ gout, int32_t q) {
+                                               int32_t *__restrict__ gout, int32_t q) {
     LaneResult r{0, 0, 0, 0};
     auto put = [&](int32_t k, int32_t v) {
-        if (k < stage_words)
-            stage[k * 32] = v;
-        else
-            gout[k] = v;
+        gout[k] = v;
     };
-    auto get = [&](int32_t k) { return k < stage_words ? stage[k * 32] : gout[k]; };   // this lane's own words
+    auto get = [&](int32_t k) { return gout[k]; };   // this lane's own words
 
     // initial values: pin index 1 when the waveform starts with -1.  The truth table
     // was re-indexed at create by the pin weights, so its index is the pin values
@@ -284,23 +279,23 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
 
 template <int N, bool kFull>
 __device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS],
-                                                 int32_t Lw, int32_t *stage, int32_t *gout) {
+                                                 int32_t Lw, int32_t *gout) {
     Pin pin[N];
 #pragma unroll
     for (int i = 0; i < N; ++i) pin[i] = pins[i];
     const uint32_t tt = (uint32_t)gd.y >> 8;
     const long long dly = (long long)(uint32_t)gd.z | ((long long)gd.w << 32);
-    return run_lane<N, kFull>(pin, tt, P.dly_data + dly, Lw, stage, P.stage, gout, P.pulse_percent);
+    return run_lane<N, kFull>(pin, tt, P.dly_data + dly, Lw, gout, P.pulse_percent);
 }
 
 template <bool kFull>
 __device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS], int32_t Lw,
-                                               int32_t *stage, int32_t *gout) {
+                                               int32_t *gout) {
     switch (gd.y & 7) {
-        case 1: return simulate_gate<1, kFull>(P, gd, pins, Lw, stage, gout);
-        case 2: return simulate_gate<2, kFull>(P, gd, pins, Lw, stage, gout);
-        case 3: return simulate_gate<3, kFull>(P, gd, pins, Lw, stage, gout);
-        default: return simulate_gate<4, kFull>(P, gd, pins, Lw, stage, gout);
+        case 1: return simulate_gate<1, kFull>(P, gd, pins, Lw, gout);
+        case 2: return simulate_gate<2, kFull>(P, gd, pins, Lw, gout);
+        case 3: return simulate_gate<3, kFull>(P, gd, pins, Lw, gout);
+        default: return simulate_gate<4, kFull>(P, gd, pins, Lw, gout);
     }
 }
 
@@ -509,11 +504,9 @@ __global__ void __launch_bounds__(kBlock) level_place_kernel(const DevParams P, 
 }
 
 // One warp = 32 slots of the level: a gate and 32 of its ranks.  Warps share nothing
-// but the shared-memory allocation of their block and never wait for each other.
-// kFull: PATHPULSEPERCENT = 100.
+// and never wait for each other.  kFull: PATHPULSEPERCENT = 100.
 template <bool kFull>
 __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(const DevParams P, const LevelLaunch L) {
-    extern __shared__ int32_t smem[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int tile = blockIdx.x * kLevelWarps + warp;
@@ -543,13 +536,12 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     const int g = L.gate_begin + gl;
     const int w = valid ? (int)__ldg(P.perm + (long long)gl * P.W + rank) : 0;
 
-    int32_t *stage = smem + warp * (P.stage * 32) + lane;
     const int seg_lead = lane & ~((1 << P.lpg_log2) - 1);  // first lane of this (gate, group) segment
     const long long net = (long long)P.num_inputs + g;
 
-    // Provisional slot of this window inside its group's part of the gate's region:
-    // the window's own bound, 3 + sum over pins of (input length - 2), scanned over
-    // the segment in rank order.  These bounds add up to what the plan reserved.
+    // Slot of this window inside its group's part of the gate's region: the window's
+    // own bound, 3 + sum over pins of (input length - 2), scanned over the segment in
+    // rank order.  These bounds add up to what the plan reserved.
     // Pins of the gate in window w: source waveforms from the window index.
     int4 gd = make_int4(0, 0, 0, 0);
     int32_t Lw = 0;
@@ -583,22 +575,16 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     }
     const uint32_t bincl = warp_incl_scan(bound, lane);
     const uint32_t bexcl = bincl - bound;
-    const long long prov = base + (bexcl - __shfl_sync(0xffffffffu, bexcl, seg_lead));
+    const uint32_t rel = bexcl - __shfl_sync(0xffffffffu, bexcl, seg_lead);
 
     LaneResult res{0, 0, 0, 0};
     if (valid) {
-        res = dispatch<kFull>(P, gd, pins, Lw, stage, P.pool + prov);
+        res = dispatch<kFull>(P, gd, pins, Lw, P.pool + base + rel);
         if (res.err) {
             raise_error(P.status, res.err, g, w, 0);
             res.len = 0;
         }
     }
-
-    // final place: scan of the actual lengths over the segment
-    const uint32_t incl = warp_incl_scan((uint32_t)res.len, lane);
-    const uint32_t excl = incl - (uint32_t)res.len;
-    const uint32_t rel = excl - __shfl_sync(0xffffffffu, excl, seg_lead);
-    const long long fin = base + rel;
 
     // TC and T1 per (gate, group): reduce over the segment's lanes, one atomic each
     long long tcs = res.tc, t1s = res.t1;
@@ -618,39 +604,7 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
         atomicAdd(P.t1 + g, (unsigned long long)t1s);
     }
 
-    // Words that did not fit on chip sit at their provisional place; move them to the
-    // final one, one window at a time in lane order, the whole warp copying upward in
-    // steps of 32 words.  A final position never exceeds its provisional one, and the
-    // final range of a window ends before the provisional words of any later window
-    // begin, so in sequential order no copy overwrites a word still to be read.  The
-    // lanes of a warp are not ordered in memory without a barrier, though: a later
-    // step's store could land before another lane's earlier-step load of the same
-    // word, hence the __syncwarp between every step's loads and its stores.
-    unsigned spilled = __ballot_sync(0xffffffffu, valid && res.len > P.stage);
-    if (spilled) {
-        __syncwarp();
-        while (spilled) {
-            const int src_lane = __ffs(spilled) - 1;
-            spilled &= spilled - 1u;
-            const long long from = __shfl_sync(0xffffffffu, prov, src_lane) + P.stage;
-            const long long to = __shfl_sync(0xffffffffu, fin, src_lane) + P.stage;
-            const int count = __shfl_sync(0xffffffffu, res.len, src_lane) - P.stage;
-            if (from == to) continue;                       // warp-uniform
-            for (int q0 = 0; q0 < count; q0 += 32) {        // warp-uniform trip count
-                const int q = q0 + lane;
-                int32_t v = 0;
-                if (q < count) v = P.pool[from + q];
-                __syncwarp();
-                if (q < count) P.pool[to + q] = v;
-            }
-            __syncwarp();
-        }
-    }
-
     if (valid) {
-        int32_t *dst = P.pool + fin;
-        const int kept = min(res.len, P.stage);
-        for (int k = 0; k < kept; ++k) dst[k] = stage[k * 32];
         P.wstart[net * P.W + w] = gofs + rel;
         P.wend[net * P.W + w] = gofs + rel + (uint32_t)res.len;
         P.wlen8[net * P.w8stride + w] = (uint8_t)min(res.len, 255);
@@ -739,7 +693,6 @@ cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const i
     return cudaGetLastError();
 }
 
-size_t level_smem_bytes(int stage) { return (size_t)kLevelWarps * 32 * (size_t)stage * sizeof(int32_t); }
 
 int plan_gates_per_tile(int W) { return W > 4096 ? 1 : kPlanWarps; }   // one warp per block for long window lists
 
@@ -759,12 +712,11 @@ cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaSt
 }
 
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
-    const size_t smem = level_smem_bytes(p.stage);
     const unsigned blocks = (unsigned)((l.num_tiles + kLevelWarps - 1) / kLevelWarps);
     if (p.pulse_percent == 100)
-        level_kernel<true><<<blocks, kLevelBlock, smem, s>>>(p, l);
+        level_kernel<true><<<blocks, kLevelBlock, 0, s>>>(p, l);
     else
-        level_kernel<false><<<blocks, kLevelBlock, smem, s>>>(p, l);
+        level_kernel<false><<<blocks, kLevelBlock, 0, s>>>(p, l);
     return cudaGetLastError();
 }
 
@@ -773,12 +725,13 @@ cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t 
     return e != cudaSuccess ? e : launch_level_sim(p, l, s);
 }
 
-cudaError_t set_level_smem_limit(int stage, int W) {
-    cudaError_t e = cudaFuncSetAttribute(level_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)level_smem_bytes(stage));
+cudaError_t set_level_smem_limit(int W) {
+    // the simulation kernel uses no shared memory: all of L1 for the source waveforms
+    cudaError_t e = cudaFuncSetAttribute(level_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxL1);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(level_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)level_smem_bytes(stage));
+        e = cudaFuncSetAttribute(level_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxL1);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(level_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)plan_smem_bytes(W));

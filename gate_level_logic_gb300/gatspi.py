@@ -41,7 +41,7 @@ class gatspi_netlist(ctypes.Structure):
 
 class gatspi_config(ctypes.Structure):
     _fields_ = [("num_windows", ctypes.c_int32), ("window_len", _p), ("flags", ctypes.c_uint32),
-                ("stage_words", ctypes.c_int32), ("pulse_percent", ctypes.c_int32)]
+                ("pulse_percent", ctypes.c_int32)]
 
 
 class gatspi_views(ctypes.Structure):
@@ -59,7 +59,7 @@ class gatspi_level_args(ctypes.Structure):
         ("goff", _p),
         ("tc", _p), ("t1", _p),
         ("level_base", _p), ("num_inputs", ctypes.c_int32), ("num_windows", ctypes.c_int32),
-        ("gate_begin", ctypes.c_int32), ("num_gates", ctypes.c_int32), ("stage_words", ctypes.c_int32),
+        ("gate_begin", ctypes.c_int32), ("num_gates", ctypes.c_int32),
         ("flags", ctypes.c_uint32), ("pulse_percent", ctypes.c_int32),
     ]
 

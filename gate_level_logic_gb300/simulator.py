@@ -35,7 +35,7 @@ class Simulator:
     (100 = the GATSPI page's setting; 0 = transport delay).
     """
 
-    def __init__(self, net, window_len, pool_words: int = None, pool=None, stage_words: int = -1, flags: int = 0,
+    def __init__(self, net, window_len, pool_words: int = None, pool=None, flags: int = 0,
                  device: int = None, pulse_percent: int = 100):
         import torch
         self._torch = torch
@@ -70,8 +70,7 @@ class Simulator:
             keep["dly_data"].size, keep["dly_data"].ctypes.data)
         if int(pulse_percent) != 100:
             flags = int(flags) | _c.GATSPI_FLAG_PULSE_PERCENT
-        cfg = _c.gatspi_config(self.num_windows, keep["window_len"].ctypes.data, int(flags), int(stage_words),
-                               int(pulse_percent))
+        cfg = _c.gatspi_config(self.num_windows, keep["window_len"].ctypes.data, int(flags), int(pulse_percent))
         self.pulse_percent = int(pulse_percent)
         with torch.cuda.device(self.device):
             self.ctx = _c.gatspi_create(nl, cfg, self.pool.data_ptr(), self.pool.numel())

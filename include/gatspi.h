@@ -140,12 +140,6 @@ typedef struct {
  *   num_windows   W independent cycle windows, 1 .. GATSPI_MAX_WINDOWS
  *   window_len    host array [W] of window lengths in time units (1 .. 2^30)
  *   flags         GATSPI_FLAG_*
- *   stage_words   output words a thread keeps in shared memory while it simulates
- *                 (0 .. 64); -1 selects the library default.  Words beyond them are
- *                 written to the window's provisional slot in its output region (a
- *                 slot as long as the window's own bound) and moved to their final
- *                 place once the lengths of the chunk's windows are known; every
- *                 (gate, window) is simulated exactly once whatever the value.
  *   pulse_percent PATHPULSEPERCENT q, 0 .. 100, read only with
  *                 GATSPI_FLAG_PULSE_PERCENT (a zeroed config means 100).
  */
@@ -153,7 +147,6 @@ typedef struct {
     int32_t num_windows;
     const int64_t *window_len;
     uint32_t flags;
-    int32_t stage_words;
     int32_t pulse_percent;
 } gatspi_config;
 
@@ -382,7 +375,6 @@ typedef struct {
     int32_t num_windows;
     int32_t gate_begin;   /* first gate of the level */
     int32_t num_gates;    /* gates in the level */
-    int32_t stage_words;  /* as in gatspi_config */
     uint32_t flags;
     int32_t pulse_percent;
 } gatspi_level_args;

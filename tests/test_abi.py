@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
         assert callable(getattr(lib, n, None)), "no Python wrapper for " + n
 
 
-def _struct(lib, net, W=1, stage=-1):
+def _struct(lib, net, W=1):
     keep = dict(lo=np.ascontiguousarray(net.level_offsets, np.int32), gt=np.ascontiguousarray(net.gate_type, np.int32),
                 tp=np.ascontiguousarray(net.type_num_pins, np.int32), to=np.ascontiguousarray(net.type_tt_off, np.int32),
                 tt=np.ascontiguousarray(net.tt_data, np.uint8), fo=np.ascontiguousarray(net.fanin_off, np.int32),
@@ -51,7 +51,7 @@ def _struct(lib, net, W=1, stage=-1):
                             keep["tt"].ctypes.data, keep["fo"].ctypes.data, keep["fn"].ctypes.data,
                             keep["pw"].ctypes.data, keep["wr"].ctypes.data, keep["wf"].ctypes.data,
                             keep["do"].ctypes.data, keep["dd"].size, keep["dd"].ctypes.data)
-    cfg = lib.gatspi_config(W, keep["wl"].ctypes.data, 0, stage)
+    cfg = lib.gatspi_config(W, keep["wl"].ctypes.data, 0, 0)
     return nl, cfg, keep
 
 
@@ -92,8 +92,6 @@ def test_invalid_netlists_are_rejected_on_the_host(lib, change, needle):
 
 def test_invalid_config_and_pool_are_rejected(lib):
     net, _ = synth.make("tiny")
-    nl, cfg, keep = _struct(lib, net, W=1, stage=65)
-    assert _create_status(lib, nl, cfg)[0] == 1
     nl, cfg, keep = _struct(lib, net, W=1)
     assert _create_status(lib, nl, cfg, pool=0x10004)[0] == 1       # not 16-byte aligned
     assert _create_status(lib, nl, cfg, words=1023)[0] == 1         # not a multiple of 4 words

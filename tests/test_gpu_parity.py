@@ -31,10 +31,9 @@ def gpu():
     return Simulator
 
 
-def run_gpu(Simulator, net, stim, pool_words, stage_words=-1, flags=0, repeat=1, pulse_percent=100):
+def run_gpu(Simulator, net, stim, pool_words, flags=0, repeat=1, pulse_percent=100):
     """Simulate; return every waveform gathered gap-free (CSR, net-major) + statistics."""
-    with Simulator(net, stim.window_len, pool_words=pool_words, stage_words=stage_words, flags=flags,
-                   pulse_percent=pulse_percent) as sim:
+    with Simulator(net, stim.window_len, pool_words=pool_words, flags=flags, pulse_percent=pulse_percent) as sim:
         sim.load(stim.pi_off, stim.pi_words)
         for _ in range(repeat):
             sim.simulate()
@@ -76,13 +75,12 @@ def test_50k_full(gpu, oracle_lib):
     assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref)
 
 
-@pytest.mark.parametrize("stage_words,flags", [(0, 0), (1, 0), (3, 0), (8, 0), (64, 0), (24, 2)])
-def test_50k_staging_and_launch_variants(gpu, oracle_lib, stage_words, flags):
-    """stage 0 sends every output word to the provisional slot; other sizes mix both."""
+@pytest.mark.parametrize("flags", [2])
+def test_50k_launch_variants(gpu, oracle_lib, flags):
+    """The level sequence launched directly instead of replayed from a graph."""
     net, stim = synth.make("50k")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=stage_words, flags=flags), ref,
-                "stage=%d flags=%d" % (stage_words, flags))
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), flags=flags), ref, "flags=%d" % flags)
 
 
 @pytest.mark.parametrize("W", [1, 2, 3, 7, 16, 31, 32, 33, 63, 64, 65, 100, 128, 200, 256, 257, 384])
@@ -94,7 +92,7 @@ def test_window_counts(gpu, oracle_lib, W):
     stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=37, cycles=max(W, 300), period=500,
                                                       activity=0.2, windows=W, seed=W, glitch_frac=0.2))
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=8), ref, "W=%d" % W)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref, "W=%d" % W)
 
 
 def test_random_small_netlists(gpu, oracle_lib):
@@ -104,7 +102,7 @@ def test_random_small_netlists(gpu, oracle_lib):
     for seed in range(120):
         net, stim = pins._random_case(seed)
         ref = oracle_lib.simulate(net, stim)
-        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=(0, 2, 24)[seed % 3]), ref,
+        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref,
                     "seed %d" % seed)
 
 
@@ -133,8 +131,7 @@ def test_simultaneous_switching_of_all_pins(gpu, oracle_lib):
     stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=32, cycles=300, period=200, activity=0.4,
                                                       windows=50, seed=31, glitch_frac=0.3, glitch_span=(1, 5)))
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    for stage in (0, 24):
-        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=stage), ref, "stage %d" % stage)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref)
 
 
 def test_quiet_inputs_and_empty_level(gpu, oracle_lib):
@@ -157,7 +154,7 @@ def test_maximum_activity(gpu, oracle_lib):
     stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=64, cycles=256, period=200, activity=1.0,
                                                       windows=64, seed=5, glitch_frac=0.5, glitch_span=(1, 4)))
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=16), ref)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref)
 
 
 def test_replay_is_deterministic(gpu, oracle_lib):
@@ -275,22 +272,20 @@ def test_1M_sweep_points_sampled(gpu, oracle_lib, activity, W):
 
 @pytest.mark.parametrize("q", [0, 35, 70, 99])
 def test_pulse_percent_random_small(gpu, oracle_lib, q):
-    """The seeded corner-heavy cases at other pulse limits; staging 0 and 2 make the
-    re-read of an exposed entry come from the pool, 24 from shared memory."""
+    """The seeded corner-heavy cases at other pulse limits (a cancel re-reads the
+    exposed entry from the lane's own output)."""
     import test_oracle_pins as pins
     for seed in range(40):
         net, stim = pins._random_case(seed)
         ref = oracle_lib.simulate(net, stim, pulse_percent=q)
-        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=(0, 2, 24)[seed % 3], pulse_percent=q),
-                    ref, "q=%d seed %d" % (q, seed))
+        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), pulse_percent=q), ref, "q=%d seed %d" % (q, seed))
 
 
-@pytest.mark.parametrize("q,stage_words", [(0, -1), (50, -1), (50, 0), (80, 3)])
-def test_pulse_percent_50k(gpu, oracle_lib, q, stage_words):
+@pytest.mark.parametrize("q", [0, 50, 80])
+def test_pulse_percent_50k(gpu, oracle_lib, q):
     net, stim = synth.make("50k")
     ref = oracle_lib.simulate(net, stim, threads=THREADS, pulse_percent=q)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=stage_words, pulse_percent=q), ref,
-                "q=%d stage=%d" % (q, stage_words))
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), pulse_percent=q), ref, "q=%d" % q)
     if q == 0:     # transport delay lets every pulse through: more toggles than the inertial default
         assert ref.tc.sum() > oracle_lib.simulate(net, stim, threads=THREADS).tc.sum()
 
@@ -303,20 +298,19 @@ def test_pulse_percent_window_counts(gpu, oracle_lib, W):
                                                       activity=0.3, windows=W, seed=W, glitch_frac=0.4))
     for q in (10, 60):
         ref = oracle_lib.simulate(net, stim, threads=THREADS, pulse_percent=q)
-        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=4, pulse_percent=q), ref,
+        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), pulse_percent=q), ref,
                     "q=%d W=%d" % (q, W))
 
 
-@pytest.mark.parametrize("stage_words", [0, 3, 24, 64])
-def test_many_windows_staging(gpu, oracle_lib, stage_words):
-    """256 windows (eight chunks per gate) with every staging size."""
-    net = synth.generate_netlist(synth.NetlistSpec(num_gates=1200, num_inputs=33, num_levels=6, seed=77,
+@pytest.mark.parametrize("seed", [77, 78])
+def test_many_windows(gpu, oracle_lib, seed):
+    """256 windows (eight groups of ranks per gate), high activity."""
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=1200, num_inputs=33, num_levels=6, seed=seed,
                                                    cond_fraction=0.5))
     stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=33, cycles=512, period=400, activity=0.5,
-                                                      windows=256, seed=77, glitch_frac=0.4))
+                                                      windows=256, seed=seed, glitch_frac=0.4))
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), stage_words=stage_words), ref,
-                "stage=%d" % stage_words)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref, "seed %d" % seed)
 
 
 def test_empty_level_and_errors_many_windows(gpu, oracle_lib):

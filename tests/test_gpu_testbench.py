@@ -57,7 +57,7 @@ def test_window_counts(gpu, oracle_lib, W):
                                          seed=W, glitch_frac=0.3))
     stim = _oracle_windows(oracle_lib, tb)
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
-    assert_same(_run(gpu, net, tb, _pool(ref, net, tb), stage_words=8), ref, "W=%d" % W)
+    assert_same(_run(gpu, net, tb, _pool(ref, net, tb)), ref, "W=%d" % W)
 
 
 def test_toggles_on_window_boundaries_from_device_memory(gpu, oracle_lib):

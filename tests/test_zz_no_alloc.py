@@ -64,7 +64,7 @@ def _pack(net):
 class Caller:
     """Owns every buffer; runs levels through the allocation-free entry point."""
 
-    def __init__(self, net, stim, pool_words, stage_words=-1, pulse_percent=100):
+    def __init__(self, net, stim, pool_words, pulse_percent=100):
         import torch
         from gate_level_logic_gb300 import gatspi
         self.gatspi, self.torch = gatspi, torch
@@ -87,7 +87,6 @@ class Caller:
         self.tc = torch.zeros(G, dtype=torch.int64, device=dev)
         self.t1 = torch.zeros(G, dtype=torch.int64, device=dev)
         self.level_base = torch.zeros(2, dtype=torch.int64, device=dev)
-        self.stage_words = stage_words
         self.pulse_percent = pulse_percent
         # input waveforms at the front of the pool, with their window index: each
         # input's windows back to back from its base
@@ -112,7 +111,7 @@ class Caller:
             self.net_base.data_ptr(), self.wstart.data_ptr(), self.wend.data_ptr(), self.wlen8.data_ptr(),
             self.perm.data_ptr(),
             self.goff.data_ptr(), self.tc.data_ptr(), self.t1.data_ptr(),
-            self.level_base.data_ptr(), self.net.num_inputs, self.W, gate_begin, num_gates, self.stage_words,
+            self.level_base.data_ptr(), self.net.num_inputs, self.W, gate_begin, num_gates,
             g.GATSPI_FLAG_PULSE_PERCENT, self.pulse_percent)
 
     def run(self):
