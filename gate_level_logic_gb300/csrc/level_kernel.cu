@@ -371,7 +371,6 @@ __global__ void __launch_bounds__(kPlanWarps * 32) level_plan_kernel(const DevPa
     uint32_t *gsum = hist + kSortBuckets;
     const int gl = blockIdx.x * (blockDim.x >> 5) + warp;   // the gate of this warp
     if (gl >= L.num_gates) return;
-    if (__shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0) return;
     const int g = L.gate_begin + gl;
     const int W = P.W;
     long long total = 0;
@@ -484,10 +483,12 @@ __global__ void __launch_bounds__(kBlock) level_place_kernel(const DevParams P, 
     if (lane == 0) tile = atomicAdd(P.tickets + L.level, 1);
     tile = __shfl_sync(0xffffffffu, tile, 0);
     if (tile >= L.scan_tiles) return;                      // spare warps of the last block
-    const bool skip = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
+    const int32_t st = lane == 0 ? ld_status(P.status) : 0;
     const int gl = tile * 32 + lane;
+    const long long raw = gl < L.num_gates ? (long long)__ldg(P.goff + (long long)gl * (P.ngroups + 1) + P.ngroups) : 0;
+    const bool skip = __shfl_sync(0xffffffffu, st, 0) != 0;
     const bool valid = !skip && gl < L.num_gates;
-    const long long size = valid ? (long long)__ldg(P.goff + (long long)gl * (P.ngroups + 1) + P.ngroups) : 0;
+    const long long size = valid ? raw : 0;
     long long incl = size;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -511,7 +512,9 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     const int warp = threadIdx.x >> 5;
     const int tile = blockIdx.x * kLevelWarps + warp;
     if (tile >= L.num_tiles) return;                       // spare warps of the last block
-    const bool skip = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
+    // the status word is read now but waited for only before the first store: after
+    // an error the warp loads in bounds and writes nothing
+    const int32_t st = lane == 0 ? ld_status(P.status) : 0;
 
     // slot -> (gate, group, rank): W >= 32 gives one (gate, group of 32 ranks) per
     // warp, W < 32 gives 32 >> lpg_log2 gates of lpg lanes each; the plan maps the
@@ -531,10 +534,10 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
         j = slot & ((1 << P.lpg_log2) - 1);
     }
     const int rank = c * 32 + j;
-    const bool gate_ok = !skip && gl < L.num_gates;
-    const bool valid = gate_ok && rank < P.W;
+    const bool in_level = gl < L.num_gates;
+    const bool loaded = in_level && rank < P.W;
     const int g = L.gate_begin + gl;
-    const int w = valid ? (int)__ldg(P.perm + (long long)gl * P.W + rank) : 0;
+    const int w = loaded ? (int)__ldg(P.perm + (long long)gl * P.W + rank) : 0;
 
     const int seg_lead = lane & ~((1 << P.lpg_log2) - 1);  // first lane of this (gate, group) segment
     const long long net = (long long)P.num_inputs + g;
@@ -549,7 +552,7 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     uint32_t gofs = 0;      // the group's offset inside the gate's region
     long long base = 0;     // the group's first pool word
     Pin pins[GATSPI_MAX_PINS];
-    if (valid) {
+    if (loaded) {
         gd = __ldg(P.gate_desc + 3 * (long long)g);
         const int4 sv = __ldg(P.gate_desc + 3 * (long long)g + 1);
         const int4 dv = __ldg(P.gate_desc + 3 * (long long)g + 2);
@@ -576,6 +579,9 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     const uint32_t bincl = warp_incl_scan(bound, lane);
     const uint32_t bexcl = bincl - bound;
     const uint32_t rel = bexcl - __shfl_sync(0xffffffffu, bexcl, seg_lead);
+    const bool skip = __shfl_sync(0xffffffffu, st, 0) != 0;
+    const bool gate_ok = in_level && !skip;
+    const bool valid = loaded && !skip;
 
     LaneResult res{0, 0, 0, 0};
     if (valid) {
