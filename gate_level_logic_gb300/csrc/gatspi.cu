@@ -94,6 +94,7 @@ struct gatspi_ctx {
     long long max_window_len = 0;
     bool loaded = false;
     bool simulated = false;
+    bool timed_last = false;   // the last simulate recorded level events
     cudaStream_t last_stream = nullptr;
 
     // TC/T1 copied to pinned host memory level by level while later levels run
@@ -307,7 +308,7 @@ gatspi_status enqueue_levels(gatspi_ctx *c, cudaStream_t s) {
     CUDA_TRY(cudaMemsetAsync(c->status, 0, sizeof(int32_t) * kStatusWords, s), "clearing the status");
     const DevParams p = c->params();
     const bool timing = (c->flags & GATSPI_FLAG_LEVEL_TIMING) != 0;
-    // events: [2l] before the bounds kernel of level l, [2l+1] between it and the
+    // events: [2l] before the bounds kernels of level l, [2l+1] between them and the
     // simulation kernel, [2l+2] after the simulation kernel
     for (int l = 0; l < c->L; ++l) {
         if (timing) CUDA_TRY(cudaEventRecord(c->events[2 * l], s), "recording a level event");
@@ -482,10 +483,8 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(cudaMemset(c->tc, 0, sizeof(unsigned long long) * std::max(c->G, 1)), "clearing TC");
         CUDA_TRY(cudaMemset(c->t1, 0, sizeof(unsigned long long) * std::max(c->G, 1)), "clearing T1");
         CUDA_TRY(set_level_smem_limit(c->W), "configuring shared memory");
-        if (c->flags & GATSPI_FLAG_LEVEL_TIMING) {
-            c->events.resize(2 * c->L + 1, nullptr);
-            for (auto &e : c->events) CUDA_TRY(cudaEventCreate(&e), "creating level events");
-        }
+        c->events.resize(2 * c->L + 1, nullptr);   // level timing can be switched on later
+        for (auto &e : c->events) CUDA_TRY(cudaEventCreate(&e), "creating level events");
         if (c->G > 0) {
             CUDA_TRY(cudaHostAlloc((void **)&c->tc_host, sizeof(unsigned long long) * c->G, cudaHostAllocDefault),
                      "allocating pinned TC");
@@ -603,6 +602,7 @@ gatspi_status gatspi_simulate(gatspi_ctx *c, void *stream) {
     cudaStream_t s = (cudaStream_t)stream;
     c->last_stream = s;
     c->simulated = true;
+    c->timed_last = (c->flags & GATSPI_FLAG_LEVEL_TIMING) != 0;
     // per-level events are recorded on the caller's stream: they cannot be read back
     // from a replayed graph, so timing runs launch the levels directly
     if (c->flags & (GATSPI_FLAG_NO_GRAPH | GATSPI_FLAG_LEVEL_TIMING)) return enqueue_levels(c, s);
@@ -808,9 +808,9 @@ gatspi_status gatspi_device_views(gatspi_ctx *c, gatspi_views *v) {
 gatspi_status gatspi_level_times(gatspi_ctx *c, float *sim_ms, float *bounds_ms, int32_t n) {
     g_err.clear();
     if (!c || (!sim_ms && !bounds_ms)) return fail(GATSPI_EINVAL, "ctx and an output array are required");
-    if (!(c->flags & GATSPI_FLAG_LEVEL_TIMING)) return fail(GATSPI_ESTATE, "created without GATSPI_FLAG_LEVEL_TIMING");
     if (n != c->L) return fail(GATSPI_EINVAL, "ms needs num_levels entries");
     if (!c->simulated) return fail(GATSPI_ESTATE, "simulate first");
+    if (!c->timed_last) return fail(GATSPI_ESTATE, "the last simulate ran without GATSPI_FLAG_LEVEL_TIMING");
     gatspi_status st = sync_ctx(c);
     if (st != GATSPI_OK) return st;
     for (int l = 0; l < c->L; ++l) {
@@ -819,6 +819,16 @@ gatspi_status gatspi_level_times(gatspi_ctx *c, float *sim_ms, float *bounds_ms,
         if (sim_ms)
             CUDA_TRY(cudaEventElapsedTime(&sim_ms[l], c->events[2 * l + 1], c->events[2 * l + 2]), "reading level events");
     }
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_set_level_timing(gatspi_ctx *c, int32_t on) {
+    g_err.clear();
+    if (!c) return fail(GATSPI_EINVAL, "ctx is NULL");
+    if (on)
+        c->flags |= GATSPI_FLAG_LEVEL_TIMING;
+    else
+        c->flags &= ~GATSPI_FLAG_LEVEL_TIMING;
     return GATSPI_OK;
 }
 

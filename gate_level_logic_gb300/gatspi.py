@@ -89,6 +89,7 @@ SIGNATURES = {
     "gatspi_export_windows": (ctypes.c_int, [_p, _p, ctypes.c_int32, _p, _p, ctypes.c_size_t]),
     "gatspi_device_views": (ctypes.c_int, [_p, ctypes.POINTER(gatspi_views)]),
     "gatspi_level_times": (ctypes.c_int, [_p, _p, _p, ctypes.c_int32]),
+    "gatspi_set_level_timing": (ctypes.c_int, [_p, ctypes.c_int32]),
     "gatspi_simulate_level_static": (ctypes.c_int, [ctypes.POINTER(gatspi_level_args), _p]),
     "gatspi_sdf_annotate": (ctypes.c_int, [ctypes.POINTER(gatspi_sdf_design), ctypes.c_char_p, ctypes.c_size_t, _p,
                                            _p, _p]),
@@ -187,6 +188,10 @@ def gatspi_device_views(ctx: int) -> gatspi_views:
 
 def gatspi_level_times(ctx: int, sim_ms: int, bounds_ms: int, n: int):
     _check(library().gatspi_level_times(_p(ctx), _p(sim_ms), _p(bounds_ms), n))
+
+
+def gatspi_set_level_timing(ctx: int, on: bool):
+    _check(library().gatspi_set_level_timing(_p(ctx), 1 if on else 0))
 
 
 def gatspi_simulate_level_static(args: gatspi_level_args, stream: int = 0):

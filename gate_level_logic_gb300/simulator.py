@@ -206,6 +206,11 @@ class Simulator:
         used = self.pool_used()
         return self.pool[:used].cpu().numpy()
 
+    def set_level_timing(self, on: bool):
+        """Record per-level kernel times in the following simulate calls (serialises
+        the kernels), or stop recording them."""
+        _c.gatspi_set_level_timing(self.ctx, on)
+
     def level_times(self):
         """(simulation-kernel ms, bounds-kernel ms) per level of the last simulate."""
         sim = np.zeros(max(self.num_levels, 1), np.float32)

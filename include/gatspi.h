@@ -318,12 +318,21 @@ gatspi_status gatspi_export_windows(gatspi_ctx *ctx, const int32_t *windows, int
 gatspi_status gatspi_device_views(gatspi_ctx *ctx, gatspi_views *out);
 
 /*
- * Per-level kernel times in milliseconds of the last simulate (needs
- * GATSPI_FLAG_LEVEL_TIMING): sim_ms[l] for the simulation kernel of level l,
- * bounds_ms[l] for the kernel that sizes its output regions (either may be NULL;
- * n = num_levels).  Synchronises first.
+ * Per-level kernel times in milliseconds of the last simulate (which must have run
+ * with GATSPI_FLAG_LEVEL_TIMING): sim_ms[l] for the simulation kernel of level l,
+ * bounds_ms[l] for the kernels that plan and place its output regions (either may
+ * be NULL; n = num_levels).  Synchronises first.  GATSPI_ESTATE when the last
+ * simulate was not timed.
  */
 gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *sim_ms, float *bounds_ms, int32_t n);
+
+/*
+ * Switch GATSPI_FLAG_LEVEL_TIMING on (on != 0) or off for the following simulate
+ * calls.  Timed runs launch the levels directly with a CUDA event between every two
+ * kernels; untimed runs replay the captured level graph (unless
+ * GATSPI_FLAG_NO_GRAPH).  GATSPI_EINVAL when ctx is NULL.
+ */
+gatspi_status gatspi_set_level_timing(gatspi_ctx *ctx, int32_t on);
 
 /*
  * Buffers of one logic level for gatspi_simulate_level_static (all device memory,

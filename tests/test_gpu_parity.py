@@ -157,6 +157,28 @@ def test_maximum_activity(gpu, oracle_lib):
     assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref)
 
 
+def test_level_timing_switch(gpu, oracle_lib):
+    """Per-level times exist only after a timed run; switching timing on and off
+    between runs of one context changes nothing in the results."""
+    from gate_level_logic_gb300 import GatspiError
+    net, stim = synth.make("tiny")
+    ref = oracle_lib.simulate(net, stim)
+    with gpu(net, stim.window_len, pool_words=pool_for(ref, net)) as sim:
+        sim.load(stim.pi_off, stim.pi_words)
+        sim.simulate()
+        with pytest.raises(GatspiError) as e:
+            sim.level_times()
+        assert e.value.name == "GATSPI_ESTATE"
+        sim.set_level_timing(True)
+        sim.simulate()
+        lt, bt = sim.level_times()
+        assert lt.shape == (net.num_levels,) and (lt > 0).all() and (bt > 0).all()
+        sim.set_level_timing(False)
+        sim.simulate()
+        tc, t0, t1 = sim.toggle_stats()
+        assert np.array_equal(tc, ref.tc) and np.array_equal(t1, ref.t1)
+
+
 def test_replay_is_deterministic(gpu, oracle_lib):
     net, stim = synth.make("50k")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
