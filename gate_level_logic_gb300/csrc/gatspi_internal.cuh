@@ -22,6 +22,7 @@ constexpr int kLevelBlock = 32 * kLevelWarps;
 constexpr int kLevelMinBlocks = GATSPI_LEVEL_MIN_BLOCKS;  // resident blocks per SM the registers must allow
 constexpr int kTileSlots = 32;            // (gate, rank) slots per warp of the level kernel
 constexpr int kPlanWarps = 4;             // warps per block of the planning kernel (one gate each)
+constexpr int kPlanMinBlocks = 12;        // planning blocks per SM the registers must allow (40 registers)
 constexpr int kSortBuckets = 256;         // counting-sort buckets of the window bounds
 constexpr int32_t kEOW = GATSPI_EOW;
 constexpr int32_t kNoArc = GATSPI_NO_ARC;

@@ -143,15 +143,20 @@ __device__ __forceinline__ int32_t arc_delay(const int32_t *__restrict__ D, uint
     return __ldg(D + ((((uint32_t)i << 1) | (uint32_t)e_out) << N | vbits));
 }
 
-// Advance pin k, chosen per lane: its state is gathered and written back with
-// predicated moves so that the lanes of a warp advance different pins together.
+// Take the transition of pin k (chosen per lane) that has just arrived and find the
+// pin's next arrival: its state is gathered and written back with predicated moves
+// so that the lanes of a warp advance different pins together.
 template <int N, bool kFull>
 __device__ __forceinline__ bool advance_pin(Pin (&pin)[N], int k, int32_t q) {
-    if (N == 1) return next_arrival<kFull>(pin[0], q);
+    if (N == 1) {
+        ++pin[0].p;
+        return next_arrival<kFull>(pin[0], q);
+    }
     Pin s = pin[0];
 #pragma unroll
     for (int i = 1; i < N; ++i)
         if (k == i) s = pin[i];
+    ++s.p;
     const bool ok = next_arrival<kFull>(s, q);
 #pragma unroll
     for (int i = 0; i < N; ++i)
@@ -214,20 +219,17 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
 #pragma unroll
     for (int i = 0; i < N; ++i) ok &= next_arrival<kFull, true>(pin[i], q, t2first[i]);
 
-    while (ok) {
+    for (;;) {
         int32_t t = pin[0].a;
 #pragma unroll
         for (int i = 1; i < N; ++i) t = min(t, pin[i].a);
-        if (t == kEOW) break;
+        if ((t == kEOW) | !ok) break;
 
-        // every pin arriving at t switches together (bit N-1-i = pin i)
+        // every pin arriving at t switches together (bit N-1-i = pin i); each one's
+        // entry index moves on when the pin is advanced below
         uint32_t swb = 0;
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-            const uint32_t hit = pin[i].a == t ? 1u : 0u;
-            swb |= hit << (N - 1 - i);
-            pin[i].p += (int32_t)hit;
-        }
+        for (int i = 0; i < N; ++i) swb |= (pin[i].a == t ? 1u : 0u) << (N - 1 - i);
         vbits ^= swb;
         const int hb = 31 - __clz(swb);
         const int k = N - 1 - hb;                       // first switching pin
@@ -362,7 +364,7 @@ __device__ long long look_back(const DevParams &P, const LevelLaunch &L, int til
 // after the group offsets (goff row of ngroups + 1 entries).  Shared memory per
 // warp: the bounds of the gate's windows, the bucket counters of the counting sort,
 // the group sums.  level_place_kernel then scans the sizes into pool offsets.
-__global__ void __launch_bounds__(kPlanWarps * 32) level_plan_kernel(const DevParams P, const LevelLaunch L) {
+__global__ void __launch_bounds__(kPlanWarps * 32, kPlanMinBlocks) level_plan_kernel(const DevParams P, const LevelLaunch L) {
     extern __shared__ uint32_t psm[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
