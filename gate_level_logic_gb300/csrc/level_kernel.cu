@@ -104,28 +104,38 @@ __device__ __forceinline__ int32_t reject_limit(int32_t d, int32_t q) {
 // t2pre: w[p + 2] when the caller has it already (a wave's first words are loaded
 // together), else unused.
 template <bool kFull, bool kPre = false>
-__device__ __forceinline__ bool next_arrival(Pin &s, int32_t q, int32_t t2pre = 0) {
-    bool last = s.p + 2 >= s.len;                  // p + 1 is the EOW slot: no further transition
-    int32_t t1 = s.nx;
-    int32_t t2 = kPre ? t2pre : (last ? kEOW : __ldg(s.w + s.p + 2));
-    const int32_t d = (s.p & 1) ? (int32_t)(s.drf >> 16) : (int32_t)(s.drf & 0xffffu);
+__device__ __forceinline__ bool next_arrival(int32_t &p, int32_t &a, int32_t &nx, const int32_t *__restrict__ w,
+                                             int32_t len, uint32_t drf, int32_t q, int32_t t2pre = 0) {
+    bool last = p + 2 >= len;                      // p + 1 is the EOW slot: no further transition
+    int32_t t1 = nx;
+    int32_t t2 = kPre ? t2pre : (last ? kEOW : __ldg(w + p + 2));
+    const int32_t d = (p & 1) ? (int32_t)(drf >> 16) : (int32_t)(drf & 0xffffu);
     const int32_t lim = kFull ? d : reject_limit(d, q);
     bool bad = !last && t1 == kEOW;                 // EOW before the last slot: malformed
     if (!last && !bad && t2 - t1 < lim) {           // the pulse [t1, t2) never reaches the pin
         for (;;) {
-            s.p += 2;                               // same parity: same delay
-            last = s.p + 2 >= s.len;
+            p += 2;                                 // same parity: same delay
+            last = p + 2 >= len;
             if (last) break;
-            t1 = __ldg(s.w + s.p + 1);
-            t2 = __ldg(s.w + s.p + 2);
+            t1 = __ldg(w + p + 1);
+            t2 = __ldg(w + p + 2);
             bad = t1 == kEOW;
             if (bad || t2 - t1 >= lim) break;
         }
     }
-    s.a = (last || bad) ? kEOW : t1 + d;
-    s.nx = t2;                                      // w[p + 2]: the next transition once this one is taken
-    return last ? s.p + 2 == s.len : !bad;
+    a = (last || bad) ? kEOW : t1 + d;
+    nx = t2;                                        // w[p + 2]: the next transition once this one is taken
+    return last ? p + 2 == len : !bad;
 }
+
+// The read-only part of a pin for the event loop, kept in shared memory (one column
+// per lane) so that the registers hold only what moves: the entry index, the next
+// arrival and the word after it.
+struct __align__(16) PinConst {
+    const int32_t *w;
+    int32_t len;
+    uint32_t drf;
+};
 
 struct LaneResult {
     int32_t len;   // output words, EOW included
@@ -143,27 +153,39 @@ __device__ __forceinline__ int32_t arc_delay(const int32_t *__restrict__ D, uint
     return __ldg(D + ((((uint32_t)i << 1) | (uint32_t)e_out) << N | vbits));
 }
 
+// The moving state of a lane's pins in the event loop.
+template <int N>
+struct PinMove {
+    int32_t p[N], a[N], nx[N];
+};
+
 // Take the transition of pin k (chosen per lane) that has just arrived and find the
-// pin's next arrival: its state is gathered and written back with predicated moves
-// so that the lanes of a warp advance different pins together.
+// pin's next arrival: the moving state is gathered and written back with predicated
+// moves so that the lanes of a warp advance different pins together; the read-only
+// part comes from the lane's column of the shared table (registers for one pin).
 template <int N, bool kFull>
-__device__ __forceinline__ bool advance_pin(Pin (&pin)[N], int k, int32_t q) {
+__device__ __forceinline__ bool advance_pin(PinMove<N> &m, const Pin &pin0, const PinConst *__restrict__ tab, int k,
+                                            int32_t q) {
     if (N == 1) {
-        ++pin[0].p;
-        return next_arrival<kFull>(pin[0], q);
+        ++m.p[0];
+        return next_arrival<kFull>(m.p[0], m.a[0], m.nx[0], pin0.w, pin0.len, pin0.drf, q);
     }
-    Pin s = pin[0];
+    const PinConst c = tab[k * 32];
+    int32_t p = m.p[0], nx = m.nx[0], a;
 #pragma unroll
     for (int i = 1; i < N; ++i)
-        if (k == i) s = pin[i];
-    ++s.p;
-    const bool ok = next_arrival<kFull>(s, q);
+        if (k == i) {
+            p = m.p[i];
+            nx = m.nx[i];
+        }
+    ++p;
+    const bool ok = next_arrival<kFull>(p, a, nx, c.w, c.len, c.drf, q);
 #pragma unroll
     for (int i = 0; i < N; ++i)
         if (k == i) {
-            pin[i].p = s.p;
-            pin[i].a = s.a;
-            pin[i].nx = s.nx;
+            m.p[i] = p;
+            m.a[i] = a;
+            m.nx[i] = nx;
         }
     return ok;
 }
@@ -175,8 +197,8 @@ __device__ __forceinline__ bool advance_pin(Pin (&pin)[N], int k, int32_t q) {
 // switching pin through a lane-selected pin state, and only simultaneous
 // switching of several pins takes an extra (rare) loop.
 template <int N, bool kFull>
-__device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const int32_t *__restrict__ D, int32_t Lw,
-                                               int32_t *__restrict__ gout, int32_t q) {
+__device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], PinConst *tab, uint32_t tt, const int32_t *__restrict__ D,
+                                               int32_t Lw, int32_t *__restrict__ gout, int32_t q) {
     LaneResult r{0, 0, 0, 0};
     auto put = [&](int32_t k, int32_t v) {
         gout[k] = v;
@@ -216,20 +238,27 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
     if (y0) put(1, 0);
 
     bool ok = true, lutbad = false;
+    PinMove<N> m;
 #pragma unroll
-    for (int i = 0; i < N; ++i) ok &= next_arrival<kFull, true>(pin[i], q, t2first[i]);
+    for (int i = 0; i < N; ++i) {
+        ok &= next_arrival<kFull, true>(pin[i].p, pin[i].a, pin[i].nx, pin[i].w, pin[i].len, pin[i].drf, q, t2first[i]);
+        m.p[i] = pin[i].p;
+        m.a[i] = pin[i].a;
+        m.nx[i] = pin[i].nx;
+        if (N > 1) tab[i * 32] = PinConst{pin[i].w, pin[i].len, pin[i].drf};
+    }
 
     for (;;) {
-        int32_t t = pin[0].a;
+        int32_t t = m.a[0];
 #pragma unroll
-        for (int i = 1; i < N; ++i) t = min(t, pin[i].a);
+        for (int i = 1; i < N; ++i) t = min(t, m.a[i]);
         if ((t == kEOW) | !ok) break;
 
         // every pin arriving at t switches together (bit N-1-i = pin i); each one's
         // entry index moves on when the pin is advanced below
         uint32_t swb = 0;
 #pragma unroll
-        for (int i = 0; i < N; ++i) swb |= (pin[i].a == t ? 1u : 0u) << (N - 1 - i);
+        for (int i = 0; i < N; ++i) swb |= (m.a[i] == t ? 1u : 0u) << (N - 1 - i);
         vbits ^= swb;
         const int hb = 31 - __clz(swb);
         const int k = N - 1 - hb;                       // first switching pin
@@ -267,8 +296,8 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
             second = top;
             top = to;
         }
-        ok &= advance_pin<N, kFull>(pin, k, q);
-        for (uint32_t m = more; m; m &= m - 1u) ok &= advance_pin<N, kFull>(pin, N - __ffs(m), q);   // lowest bit first
+        ok &= advance_pin<N, kFull>(m, pin[0], tab, k, q);
+        for (uint32_t mm = more; mm; mm &= mm - 1u) ok &= advance_pin<N, kFull>(m, pin[0], tab, N - __ffs(mm), q);   // lowest bit first
     }
     if (!ok) r.err = GATSPI_EBADWAVE;
     if (lutbad) r.err = GATSPI_EBADLUT;     // a missing arc is met before any later malformed word
@@ -281,23 +310,23 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], uint32_t tt, const
 
 template <int N, bool kFull>
 __device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS],
-                                                 int32_t Lw, int32_t *gout) {
+                                                 PinConst *tab, int32_t Lw, int32_t *gout) {
     Pin pin[N];
 #pragma unroll
     for (int i = 0; i < N; ++i) pin[i] = pins[i];
     const uint32_t tt = (uint32_t)gd.y >> 8;
     const long long dly = (long long)(uint32_t)gd.z | ((long long)gd.w << 32);
-    return run_lane<N, kFull>(pin, tt, P.dly_data + dly, Lw, gout, P.pulse_percent);
+    return run_lane<N, kFull>(pin, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent);
 }
 
 template <bool kFull>
-__device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS], int32_t Lw,
-                                               int32_t *gout) {
+__device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS],
+                                               PinConst *tab, int32_t Lw, int32_t *gout) {
     switch (gd.y & 7) {
-        case 1: return simulate_gate<1, kFull>(P, gd, pins, Lw, gout);
-        case 2: return simulate_gate<2, kFull>(P, gd, pins, Lw, gout);
-        case 3: return simulate_gate<3, kFull>(P, gd, pins, Lw, gout);
-        default: return simulate_gate<4, kFull>(P, gd, pins, Lw, gout);
+        case 1: return simulate_gate<1, kFull>(P, gd, pins, tab, Lw, gout);
+        case 2: return simulate_gate<2, kFull>(P, gd, pins, tab, Lw, gout);
+        case 3: return simulate_gate<3, kFull>(P, gd, pins, tab, Lw, gout);
+        default: return simulate_gate<4, kFull>(P, gd, pins, tab, Lw, gout);
     }
 }
 
@@ -510,6 +539,7 @@ __global__ void __launch_bounds__(kBlock) level_place_kernel(const DevParams P, 
 // and never wait for each other.  kFull: PATHPULSEPERCENT = 100.
 template <bool kFull>
 __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(const DevParams P, const LevelLaunch L) {
+    __shared__ PinConst pin_tab[kLevelWarps][GATSPI_MAX_PINS * 32];   // [pin][lane] per warp
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int tile = blockIdx.x * kLevelWarps + warp;
@@ -587,7 +617,7 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
 
     LaneResult res{0, 0, 0, 0};
     if (valid) {
-        res = dispatch<kFull>(P, gd, pins, Lw, P.pool + base + rel);
+        res = dispatch<kFull>(P, gd, pins, &pin_tab[warp][lane], Lw, P.pool + base + rel);
         if (res.err) {
             raise_error(P.status, res.err, g, w, 0);
             res.len = 0;
@@ -734,16 +764,7 @@ cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t 
 }
 
 cudaError_t set_level_smem_limit(int W) {
-    // the simulation kernel uses no shared memory: all of L1 for the source waveforms
-    cudaError_t e = cudaFuncSetAttribute(level_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         (int)cudaSharedmemCarveoutMaxL1);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(level_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxL1);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(level_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)plan_smem_bytes(W));
-    return e;
+    return cudaFuncSetAttribute(level_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem_bytes(W));
 }
 
 cudaError_t launch_load_index(const DevParams &p, const long long *off, long long nwords, int32_t *max_time,
