@@ -128,13 +128,24 @@ __device__ __forceinline__ bool next_arrival(int32_t &p, int32_t &a, int32_t &nx
     return last ? p + 2 == len : !bad;
 }
 
-// The read-only part of a pin for the event loop, kept in shared memory (one column
-// per lane) so that the registers hold only what moves: the entry index, the next
-// arrival and the word after it.
-struct __align__(16) PinConst {
+// A pin of a multi-pin cell in the event loop lives in shared memory (one column per
+// lane): its waveform, entry index and the word after the next transition in one
+// 16-byte entry, its length and wire delays in an 8-byte one.  Only the pins' next
+// arrivals stay in registers (the loop takes their minimum every step), so a step
+// reads the chosen pin with two shared loads and writes it back with one store
+// instead of moving every field through per-pin selects.
+struct __align__(16) PinHot {
     const int32_t *w;
+    int32_t p;
+    int32_t nx;
+};
+struct __align__(8) PinCold {
     int32_t len;
     uint32_t drf;
+};
+struct PinTab {
+    PinHot *hot;     // [pin * 32 + lane]: this lane's column
+    PinCold *cold;
 };
 
 struct LaneResult {
@@ -153,41 +164,32 @@ __device__ __forceinline__ int32_t arc_delay(const int32_t *__restrict__ D, uint
     return __ldg(D + ((((uint32_t)i << 1) | (uint32_t)e_out) << N | vbits));
 }
 
-// The moving state of a lane's pins in the event loop.
+// The moving state of a lane's pins in the event loop: every pin's next arrival;
+// the entry index and next word too for a one-pin cell, which keeps its pin in
+// registers.
 template <int N>
 struct PinMove {
     int32_t p[N], a[N], nx[N];
 };
 
 // Take the transition of pin k (chosen per lane) that has just arrived and find the
-// pin's next arrival: the moving state is gathered and written back with predicated
-// moves so that the lanes of a warp advance different pins together; the read-only
-// part comes from the lane's column of the shared table (registers for one pin).
+// pin's next arrival.
 template <int N, bool kFull>
-__device__ __forceinline__ bool advance_pin(PinMove<N> &m, const Pin &pin0, const PinConst *__restrict__ tab, int k,
-                                            int32_t q) {
-    if (N == 1) {
+__device__ __forceinline__ bool advance_pin(PinMove<N> &m, const Pin &pin0, const PinTab &tab, int k, int32_t q) {
+    if constexpr (N == 1) {
         ++m.p[0];
         return next_arrival<kFull>(m.p[0], m.a[0], m.nx[0], pin0.w, pin0.len, pin0.drf, q);
+    } else {
+        const PinHot h = tab.hot[k * 32];
+        const PinCold c = tab.cold[k * 32];
+        int32_t p = h.p + 1, nx = h.nx, a;
+        const bool ok = next_arrival<kFull>(p, a, nx, h.w, c.len, c.drf, q);
+        *reinterpret_cast<int2 *>(&tab.hot[k * 32].p) = make_int2(p, nx);
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (k == i) m.a[i] = a;
+        return ok;
     }
-    const PinConst c = tab[k * 32];
-    int32_t p = m.p[0], nx = m.nx[0], a;
-#pragma unroll
-    for (int i = 1; i < N; ++i)
-        if (k == i) {
-            p = m.p[i];
-            nx = m.nx[i];
-        }
-    ++p;
-    const bool ok = next_arrival<kFull>(p, a, nx, c.w, c.len, c.drf, q);
-#pragma unroll
-    for (int i = 0; i < N; ++i)
-        if (k == i) {
-            m.p[i] = p;
-            m.a[i] = a;
-            m.nx[i] = nx;
-        }
-    return ok;
 }
 
 // Algorithm 1 for one (gate, window).  The output words go to gout, the window's
@@ -197,7 +199,7 @@ __device__ __forceinline__ bool advance_pin(PinMove<N> &m, const Pin &pin0, cons
 // switching pin through a lane-selected pin state, and only simultaneous
 // switching of several pins takes an extra (rare) loop.
 template <int N, bool kFull>
-__device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], PinConst *tab, uint32_t tt, const int32_t *__restrict__ D,
+__device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const PinTab &tab, uint32_t tt, const int32_t *__restrict__ D,
                                                int32_t Lw, int32_t *__restrict__ gout, int32_t q) {
     LaneResult r{0, 0, 0, 0};
     auto put = [&](int32_t k, int32_t v) {
@@ -245,7 +247,10 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], PinConst *tab, uin
         m.p[i] = pin[i].p;
         m.a[i] = pin[i].a;
         m.nx[i] = pin[i].nx;
-        if (N > 1) tab[i * 32] = PinConst{pin[i].w, pin[i].len, pin[i].drf};
+        if (N > 1) {
+            tab.hot[i * 32] = PinHot{pin[i].w, pin[i].p, pin[i].nx};
+            tab.cold[i * 32] = PinCold{pin[i].len, pin[i].drf};
+        }
     }
 
     for (;;) {
@@ -310,7 +315,7 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], PinConst *tab, uin
 
 template <int N, bool kFull>
 __device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS],
-                                                 PinConst *tab, int32_t Lw, int32_t *gout) {
+                                                 const PinTab &tab, int32_t Lw, int32_t *gout) {
     Pin pin[N];
 #pragma unroll
     for (int i = 0; i < N; ++i) pin[i] = pins[i];
@@ -321,7 +326,7 @@ __device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd,
 
 template <bool kFull>
 __device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS],
-                                               PinConst *tab, int32_t Lw, int32_t *gout) {
+                                               const PinTab &tab, int32_t Lw, int32_t *gout) {
     switch (gd.y & 7) {
         case 1: return simulate_gate<1, kFull>(P, gd, pins, tab, Lw, gout);
         case 2: return simulate_gate<2, kFull>(P, gd, pins, tab, Lw, gout);
@@ -539,7 +544,8 @@ __global__ void __launch_bounds__(kBlock) level_place_kernel(const DevParams P, 
 // and never wait for each other.  kFull: PATHPULSEPERCENT = 100.
 template <bool kFull>
 __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(const DevParams P, const LevelLaunch L) {
-    __shared__ PinConst pin_tab[kLevelWarps][GATSPI_MAX_PINS * 32];   // [pin][lane] per warp
+    __shared__ PinHot pin_hot[kLevelWarps][GATSPI_MAX_PINS * 32];     // [pin][lane] per warp
+    __shared__ PinCold pin_cold[kLevelWarps][GATSPI_MAX_PINS * 32];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int tile = blockIdx.x * kLevelWarps + warp;
@@ -617,7 +623,8 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
 
     LaneResult res{0, 0, 0, 0};
     if (valid) {
-        res = dispatch<kFull>(P, gd, pins, &pin_tab[warp][lane], Lw, P.pool + base + rel);
+        const PinTab tab{&pin_hot[warp][lane], &pin_cold[warp][lane]};
+        res = dispatch<kFull>(P, gd, pins, tab, Lw, P.pool + base + rel);
         if (res.err) {
             raise_error(P.status, res.err, g, w, 0);
             res.len = 0;
