@@ -279,7 +279,7 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const PinTab &tab,
         bool chg = y != (po & 1);
         lutbad |= chg && d == kNoArc;
         chg = chg && d != kNoArc;
-        const int32_t to = t + (chg ? d : 0);
+        const int32_t to = (int32_t)((uint32_t)t + (uint32_t)d);   // used only when chg
         // inertial filter: at q = 100, to - top < d exactly when the last entry
         // has not matured (top > t); otherwise the reject limit decides
         const bool cancel = chg && (kFull ? top > t : to - top < reject_limit(d, q));
@@ -287,7 +287,7 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const PinTab &tab,
         // time at 1: a cancelled entry gives back what it added, a stored one adds
         // its clipped time with the sign of its parity; both come to this
         const int32_t c = min(cancel ? top : to, Lw);
-        t1acc += chg ? ((po & 1) ? c : -c) : 0;
+        t1acc += (chg ? 2 * (po & 1) - 1 : 0) * c;
         po += store ? 1 : (cancel ? -1 : 0);
         if (store) put(po, to);
         if (kFull) {
@@ -333,6 +333,28 @@ __device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, Pin 
         case 3: return simulate_gate<3, kFull>(P, gd, pins, tab, Lw, gout);
         default: return simulate_gate<4, kFull>(P, gd, pins, tab, Lw, gout);
     }
+}
+
+// The N pins of a gate in window w from the window index: source waveform, length
+// and wire delays; returns the window's output bound, 3 + sum over pins of
+// (input length - 2).
+template <int N>
+__device__ __forceinline__ uint32_t load_pins(const DevParams &P, int4 sv, int4 dv, int w,
+                                              Pin (&pins)[GATSPI_MAX_PINS]) {
+    const int s4[GATSPI_MAX_PINS] = {sv.x, sv.y, sv.z, sv.w};
+    const int d4[GATSPI_MAX_PINS] = {dv.x, dv.y, dv.z, dv.w};
+    uint32_t bound = 3u - 2u * (uint32_t)N;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const long long src = s4[i];
+        const uint32_t end = __ldg(P.wend + src * P.W + w);
+        const uint32_t start = __ldg(P.wstart + src * P.W + w);
+        pins[i].w = P.pool + __ldg(P.net_base + src) + start;
+        pins[i].len = (int32_t)(end - start);
+        pins[i].drf = (uint32_t)d4[i];
+        bound += end - start;
+    }
+    return bound;
 }
 
 // Inclusive warp scan.
@@ -594,22 +616,12 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
         gd = __ldg(P.gate_desc + 3 * (long long)g);
         const int4 sv = __ldg(P.gate_desc + 3 * (long long)g + 1);
         const int4 dv = __ldg(P.gate_desc + 3 * (long long)g + 2);
-        const int s4[GATSPI_MAX_PINS] = {sv.x, sv.y, sv.z, sv.w};
-        const int d4[GATSPI_MAX_PINS] = {dv.x, dv.y, dv.z, dv.w};
         Lw = __ldg(P.window_len + w);
-        const int n = gd.y & 7;
-        bound = 3u - 2u * (uint32_t)n;
-#pragma unroll
-        for (int i = 0; i < GATSPI_MAX_PINS; ++i) {
-            if (i < n) {
-                const long long src = s4[i];
-                const uint32_t end = __ldg(P.wend + src * P.W + w);
-                const uint32_t start = __ldg(P.wstart + src * P.W + w);
-                pins[i].w = P.pool + __ldg(P.net_base + src) + start;
-                pins[i].len = (int32_t)(end - start);
-                pins[i].drf = (uint32_t)d4[i];
-                bound += end - start;
-            }
+        switch (gd.y & 7) {   // warp-uniform when a warp holds one gate
+            case 1: bound = load_pins<1>(P, sv, dv, w, pins); break;
+            case 2: bound = load_pins<2>(P, sv, dv, w, pins); break;
+            case 3: bound = load_pins<3>(P, sv, dv, w, pins); break;
+            default: bound = load_pins<4>(P, sv, dv, w, pins); break;
         }
         gofs = __ldg(P.goff + (long long)gl * (P.ngroups + 1) + c);
         base = __ldg(P.net_base + net) + gofs;
