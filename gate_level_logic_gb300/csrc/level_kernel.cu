@@ -415,6 +415,48 @@ __device__ long long look_back(const DevParams &P, const LevelLaunch &L, int til
     return excl;
 }
 
+// Output bounds of a gate's W windows into bnd[], from the one-byte window lengths of
+// its N sources: four consecutive windows per lane and load, summed over the pins
+// in 16-bit halves (two windows per register); a length of 255 or more is read
+// exactly from the index and added as a correction.  Returns this lane's sum.
+template <int N>
+__device__ __forceinline__ long long plan_bounds(const DevParams &P, int4 sv, int lane, uint32_t *bnd) {
+    const int W = P.W;
+    const int s4[GATSPI_MAX_PINS] = {sv.x, sv.y, sv.z, sv.w};
+    long long lane_sum = 0;
+    for (int w0 = 4 * lane; w0 < W; w0 += 4 * 32) {
+        uint32_t even = 0, odd = 0;            // windows w0, w0 + 2 and w0 + 1, w0 + 3 in 16-bit halves
+        uint32_t fix[4] = {0, 0, 0, 0};        // lengths beyond 255
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const long long src = s4[i];
+            const uint32_t four = __ldg((const uint32_t *)(P.wlen8 + src * P.w8stride + w0));
+            even += four & 0x00ff00ffu;
+            odd += (four >> 8) & 0x00ff00ffu;
+            if (__vcmpeq4(four, 0xffffffffu)) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int w = w0 + u;
+                    if (((four >> (8 * u)) & 0xffu) == 0xffu && w < W)
+                        fix[u] += __ldg(P.wend + src * W + w) - __ldg(P.wstart + src * W + w) - 255u;
+                }
+            }
+        }
+        const uint32_t base = 3u - 2u * (uint32_t)N;
+        const uint32_t b[4] = {base + (even & 0xffffu) + fix[0], base + (odd & 0xffffu) + fix[1],
+                               base + (even >> 16) + fix[2], base + (odd >> 16) + fix[3]};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int w = w0 + u;
+            if (w < W) {
+                bnd[w] = b[u];
+                lane_sum += b[u];
+            }
+        }
+    }
+    return lane_sum;
+}
+
 // The plan of one gate per warp: window bounds, their ranking (largest first,
 // stable), the offset of every group of 32 ranks and the region's size, stored
 // after the group offsets (goff row of ngroups + 1 entries).  Shared memory per
@@ -437,40 +479,13 @@ __global__ void __launch_bounds__(kPlanWarps * 32, kPlanMinBlocks) level_plan_ke
         for (int k = lane; k < P.ngroups; k += 32) gsum[k] = 0;
         const int4 gd = __ldg(P.gate_desc + 3 * (long long)g);
         const int4 sv = __ldg(P.gate_desc + 3 * (long long)g + 1);
-        const int n = gd.y & 7;
-        const int s4[GATSPI_MAX_PINS] = {sv.x, sv.y, sv.z, sv.w};
-        long long src[GATSPI_MAX_PINS];
-#pragma unroll
-        for (int i = 0; i < GATSPI_MAX_PINS; ++i) src[i] = i < n ? (long long)s4[i] : 0;
         __syncwarp();
-        // bounds from the one-byte window lengths, four consecutive windows per lane
-        // and load; a length of 255 or more is read exactly from the index
         long long lane_sum = 0;
-        for (int w0 = 4 * lane; w0 < W; w0 += 4 * 32) {
-            uint32_t b[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) b[u] = 3u - 2u * (uint32_t)n;
-#pragma unroll
-            for (int i = 0; i < GATSPI_MAX_PINS; ++i)
-                if (i < n) {
-                    const uint32_t four = __ldg((const uint32_t *)(P.wlen8 + src[i] * P.w8stride + w0));
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int w = w0 + u;
-                        uint32_t len = (four >> (8 * u)) & 0xffu;
-                        if (len == 0xffu && w < W)
-                            len = __ldg(P.wend + src[i] * W + w) - __ldg(P.wstart + src[i] * W + w);
-                        b[u] += len;
-                    }
-                }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int w = w0 + u;
-                if (w < W) {
-                    bnd[w] = b[u];
-                    lane_sum += b[u];
-                }
-            }
+        switch (gd.y & 7) {   // warp-uniform: one gate per warp
+            case 1: lane_sum = plan_bounds<1>(P, sv, lane, bnd); break;
+            case 2: lane_sum = plan_bounds<2>(P, sv, lane, bnd); break;
+            case 3: lane_sum = plan_bounds<3>(P, sv, lane, bnd); break;
+            default: lane_sum = plan_bounds<4>(P, sv, lane, bnd); break;
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) lane_sum += __shfl_xor_sync(0xffffffffu, lane_sum, o);

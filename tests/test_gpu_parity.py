@@ -95,6 +95,20 @@ def test_window_counts(gpu, oracle_lib, W):
     assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref, "W=%d" % W)
 
 
+@pytest.mark.parametrize("W", [1, 3, 6])
+def test_long_windows(gpu, oracle_lib, W):
+    """Windows of hundreds to thousands of words: lengths of 255 and more, which the
+    planner reads exactly from the window index instead of the one-byte lengths."""
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=1500, num_inputs=24, num_levels=6, seed=500 + W,
+                                                   cond_fraction=0.3))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=24, cycles=3000, period=300, activity=0.6,
+                                                      windows=W, seed=W, glitch_frac=0.2))
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    lens = np.diff(ref.off)
+    assert lens.max() > 1000 and (lens >= 255).mean() > 0.2
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref, "W=%d" % W)
+
+
 def test_random_small_netlists(gpu, oracle_lib):
     """The seeded corner-heavy cases the oracle was pinned on (zero delays, zero-width
     pulses, 1-4 pin random cells, conditional arcs, multiple windows)."""
