@@ -15,7 +15,7 @@ constexpr int kWarps = kBlock / 32;
 #define GATSPI_LEVEL_WARPS 4
 #endif
 #ifndef GATSPI_LEVEL_MIN_BLOCKS
-#define GATSPI_LEVEL_MIN_BLOCKS (32 / GATSPI_LEVEL_WARPS)
+#define GATSPI_LEVEL_MIN_BLOCKS (36 / GATSPI_LEVEL_WARPS)
 #endif
 constexpr int kLevelWarps = GATSPI_LEVEL_WARPS;   // warps per level-kernel block (independent warps)
 constexpr int kLevelBlock = 32 * kLevelWarps;

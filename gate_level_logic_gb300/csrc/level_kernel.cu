@@ -81,8 +81,8 @@ __device__ void raise_error(int32_t *status, int code, int a, int b, int c) {
 // One fanin pin of a lane.
 struct Pin {
     const int32_t *w;  // the source net's waveform for this window
-    int32_t len;       // its length in words, EOW included
-    int32_t p;         // index of the entry in effect (value = p & 1)
+    uint32_t len;      // its length in words, EOW included
+    uint32_t p;        // index of the entry in effect (value = p & 1)
     int32_t a;         // arrival time of the next transition at the pin, or EOW
     int32_t nx;        // w[p + 1]: the next transition's time, kept from the previous step
     uint32_t drf;      // interconnect delays: rise | fall << 16
@@ -101,15 +101,17 @@ __device__ __forceinline__ int32_t reject_limit(int32_t d, int32_t q) {
 // previous pulse test), so a step loads one word.  The common step is straight-line
 // code, so that lanes advancing different pins stay together; only a swallowed
 // pulse takes the loop.  False on a malformed wave.
-// t2pre: w[p + 2] when the caller has it already (a wave's first words are loaded
-// together), else unused.
+// p and len may be offsets from any base w (the entry is w[p], the window ends at
+// w[len]); par is the pin's value in entry p (p's parity when p counts from the
+// window's start).  t2pre: w[p + 2] when the caller has it already (a wave's first
+// words are loaded together), else unused.
 template <bool kFull, bool kPre = false>
-__device__ __forceinline__ bool next_arrival(int32_t &p, int32_t &a, int32_t &nx, const int32_t *__restrict__ w,
-                                             int32_t len, uint32_t drf, int32_t q, int32_t t2pre = 0) {
+__device__ __forceinline__ bool next_arrival(uint32_t &p, int32_t &a, int32_t &nx, const int32_t *__restrict__ w,
+                                             uint32_t len, uint32_t drf, uint32_t par, int32_t q, int32_t t2pre = 0) {
     bool last = p + 2 >= len;                      // p + 1 is the EOW slot: no further transition
     int32_t t1 = nx;
     int32_t t2 = kPre ? t2pre : (last ? kEOW : __ldg(w + p + 2));
-    const int32_t d = (p & 1) ? (int32_t)(drf >> 16) : (int32_t)(drf & 0xffffu);
+    const int32_t d = par ? (int32_t)(drf >> 16) : (int32_t)(drf & 0xffffu);
     const int32_t lim = kFull ? d : reject_limit(d, q);
     bool bad = !last && t1 == kEOW;                 // EOW before the last slot: malformed
     if (!last && !bad && t2 - t1 < lim) {           // the pulse [t1, t2) never reaches the pin
@@ -129,23 +131,18 @@ __device__ __forceinline__ bool next_arrival(int32_t &p, int32_t &a, int32_t &nx
 }
 
 // A pin of a multi-pin cell in the event loop lives in shared memory (one column per
-// lane): its waveform, entry index and the word after the next transition in one
-// 16-byte entry, its length and wire delays in an 8-byte one.  Only the pins' next
-// arrivals stay in registers (the loop takes their minimum every step), so a step
-// reads the chosen pin with two shared loads and writes it back with one store
-// instead of moving every field through per-pin selects.
-struct __align__(16) PinHot {
-    const int32_t *w;
-    int32_t p;
-    int32_t nx;
-};
-struct __align__(8) PinCold {
-    int32_t len;
-    uint32_t drf;
-};
+// lane, 12 bytes): the offset of its entry in effect and the word after the next
+// transition in one 8-byte entry, the offset one past its window's last word in a
+// 4-byte one, offsets counted in words from the lowest of the lane's waveform
+// pointers.  Only the pins' next arrivals and wire delays stay in registers (the loop
+// takes the arrivals' minimum every step), so a step reads the switching pin with two
+// shared loads and writes it back with one store instead of moving every field
+// through per-pin selects, and the table is small enough to leave most of the SM's
+// L1 to the source waveforms.  A lane whose waveforms lie 2^32 words apart or more
+// cannot use 32-bit offsets; a warp with such a lane keeps its pins in registers.
 struct PinTab {
-    PinHot *hot;     // [pin * 32 + lane]: this lane's column
-    PinCold *cold;
+    int2 *hot;          // [pin * 32 + lane]: {entry offset, next word}
+    uint32_t *end;      // [pin * 32 + lane]
 };
 
 struct LaneResult {
@@ -164,32 +161,60 @@ __device__ __forceinline__ int32_t arc_delay(const int32_t *__restrict__ D, uint
     return __ldg(D + ((((uint32_t)i << 1) | (uint32_t)e_out) << N | vbits));
 }
 
-// The moving state of a lane's pins in the event loop: every pin's next arrival;
-// the entry index and next word too for a one-pin cell, which keeps its pin in
-// registers.
-template <int N>
-struct PinMove {
-    int32_t p[N], a[N], nx[N];
-};
-
 // Take the transition of pin k (chosen per lane) that has just arrived and find the
-// pin's next arrival.
-template <int N, bool kFull>
-__device__ __forceinline__ bool advance_pin(PinMove<N> &m, const Pin &pin0, const PinTab &tab, int k, int32_t q) {
+// pin's next arrival.  vbits holds every pin's value after the step.
+template <int N, bool kFull, bool kTable>
+__device__ __forceinline__ bool advance_pin(Pin (&pin)[N], const int32_t *lb, const PinTab &tab, int k,
+                                            uint32_t vbits, int32_t q) {
     if constexpr (N == 1) {
-        ++m.p[0];
-        return next_arrival<kFull>(m.p[0], m.a[0], m.nx[0], pin0.w, pin0.len, pin0.drf, q);
-    } else {
-        const PinHot h = tab.hot[k * 32];
-        const PinCold c = tab.cold[k * 32];
-        int32_t p = h.p + 1, nx = h.nx, a;
-        const bool ok = next_arrival<kFull>(p, a, nx, h.w, c.len, c.drf, q);
-        *reinterpret_cast<int2 *>(&tab.hot[k * 32].p) = make_int2(p, nx);
+        ++pin[0].p;
+        return next_arrival<kFull>(pin[0].p, pin[0].a, pin[0].nx, pin[0].w, pin[0].len, pin[0].drf, pin[0].p & 1u, q);
+    } else if constexpr (kTable) {
+        const int2 h = tab.hot[k * 32];
+        const uint32_t end = tab.end[k * 32];
+        uint32_t drf = pin[0].drf;
+#pragma unroll
+        for (int i = 1; i < N; ++i)
+            if (k == i) drf = pin[i].drf;
+        uint32_t off = (uint32_t)h.x + 1u;
+        int32_t nx = h.y, a;
+        const bool ok = next_arrival<kFull>(off, a, nx, lb, end, drf, (vbits >> (N - 1 - k)) & 1u, q);
+        tab.hot[k * 32] = make_int2((int32_t)off, nx);
 #pragma unroll
         for (int i = 0; i < N; ++i)
-            if (k == i) m.a[i] = a;
+            if (k == i) pin[i].a = a;
+        return ok;
+    } else {
+        // registers: the pin's state is gathered and written back with predicated
+        // moves so that the lanes of a warp advance different pins together
+        Pin s = pin[0];
+#pragma unroll
+        for (int i = 1; i < N; ++i)
+            if (k == i) s = pin[i];
+        ++s.p;
+        const bool ok = next_arrival<kFull>(s.p, s.a, s.nx, s.w, s.len, s.drf, s.p & 1u, q);
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (k == i) {
+                pin[i].p = s.p;
+                pin[i].a = s.a;
+                pin[i].nx = s.nx;
+            }
         return ok;
     }
+}
+
+// Whether a lane's pins can use 32-bit offsets from the lowest of their waveform
+// pointers (that pointer in lb).
+template <int N>
+__device__ __forceinline__ bool table_fits(const Pin (&pin)[N], const int32_t *&lb) {
+    lb = pin[0].w;
+#pragma unroll
+    for (int i = 1; i < N; ++i) lb = pin[i].w < lb ? pin[i].w : lb;
+    bool fits = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i) fits &= (unsigned long long)(pin[i].w - lb) + pin[i].len < 0xfffffff0ull;
+    return fits;
 }
 
 // Algorithm 1 for one (gate, window).  The output words go to gout, the window's
@@ -198,9 +223,10 @@ __device__ __forceinline__ bool advance_pin(PinMove<N> &m, const Pin &pin0, cons
 // pins form a bit mask, the delay lookup and the pin advance serve the first
 // switching pin through a lane-selected pin state, and only simultaneous
 // switching of several pins takes an extra (rare) loop.
-template <int N, bool kFull>
-__device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const PinTab &tab, uint32_t tt, const int32_t *__restrict__ D,
-                                               int32_t Lw, int32_t *__restrict__ gout, int32_t q) {
+template <int N, bool kFull, bool kTable>
+__device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb, const PinTab &tab, uint32_t tt,
+                                               const int32_t *__restrict__ D, int32_t Lw, int32_t *__restrict__ gout,
+                                               int32_t q) {
     LaneResult r{0, 0, 0, 0};
     auto put = [&](int32_t k, int32_t v) {
         gout[k] = v;
@@ -226,8 +252,8 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const PinTab &tab,
 #pragma unroll
     for (int i = 0; i < N; ++i) {
         const bool one = x[i][0] == -1;
-        pin[i].p = one ? 1 : 0;
-        vbits |= (uint32_t)pin[i].p << (N - 1 - i);
+        pin[i].p = one ? 1u : 0u;
+        vbits |= pin[i].p << (N - 1 - i);
         pin[i].nx = one ? x[i][2] : x[i][1];          // w[p + 1]
         t2first[i] = one ? x[i][3] : x[i][2];         // w[p + 2]
     }
@@ -240,30 +266,28 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const PinTab &tab,
     if (y0) put(1, 0);
 
     bool ok = true, lutbad = false;
-    PinMove<N> m;
 #pragma unroll
     for (int i = 0; i < N; ++i) {
-        ok &= next_arrival<kFull, true>(pin[i].p, pin[i].a, pin[i].nx, pin[i].w, pin[i].len, pin[i].drf, q, t2first[i]);
-        m.p[i] = pin[i].p;
-        m.a[i] = pin[i].a;
-        m.nx[i] = pin[i].nx;
-        if (N > 1) {
-            tab.hot[i * 32] = PinHot{pin[i].w, pin[i].p, pin[i].nx};
-            tab.cold[i * 32] = PinCold{pin[i].len, pin[i].drf};
+        ok &= next_arrival<kFull, true>(pin[i].p, pin[i].a, pin[i].nx, pin[i].w, pin[i].len, pin[i].drf,
+                                        pin[i].p & 1u, q, t2first[i]);
+        if constexpr (N > 1 && kTable) {
+            const uint32_t o = (uint32_t)(pin[i].w - lb);
+            tab.hot[i * 32] = make_int2((int32_t)(o + pin[i].p), pin[i].nx);
+            tab.end[i * 32] = o + pin[i].len;
         }
     }
 
     for (;;) {
-        int32_t t = m.a[0];
+        int32_t t = pin[0].a;
 #pragma unroll
-        for (int i = 1; i < N; ++i) t = min(t, m.a[i]);
+        for (int i = 1; i < N; ++i) t = min(t, pin[i].a);
         if ((t == kEOW) | !ok) break;
 
         // every pin arriving at t switches together (bit N-1-i = pin i); each one's
         // entry index moves on when the pin is advanced below
         uint32_t swb = 0;
 #pragma unroll
-        for (int i = 0; i < N; ++i) swb |= (m.a[i] == t ? 1u : 0u) << (N - 1 - i);
+        for (int i = 0; i < N; ++i) swb |= (pin[i].a == t ? 1u : 0u) << (N - 1 - i);
         vbits ^= swb;
         const int hb = 31 - __clz(swb);
         const int k = N - 1 - hb;                       // first switching pin
@@ -301,8 +325,9 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const PinTab &tab,
             second = top;
             top = to;
         }
-        ok &= advance_pin<N, kFull>(m, pin[0], tab, k, q);
-        for (uint32_t mm = more; mm; mm &= mm - 1u) ok &= advance_pin<N, kFull>(m, pin[0], tab, N - __ffs(mm), q);   // lowest bit first
+        ok &= advance_pin<N, kFull, kTable>(pin, lb, tab, k, vbits, q);
+        for (uint32_t mm = more; mm; mm &= mm - 1u)   // lowest bit first
+            ok &= advance_pin<N, kFull, kTable>(pin, lb, tab, N - __ffs(mm), vbits, q);
     }
     if (!ok) r.err = GATSPI_EBADWAVE;
     if (lutbad) r.err = GATSPI_EBADLUT;     // a missing arc is met before any later malformed word
@@ -321,7 +346,14 @@ __device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd,
     for (int i = 0; i < N; ++i) pin[i] = pins[i];
     const uint32_t tt = (uint32_t)gd.y >> 8;
     const long long dly = (long long)(uint32_t)gd.z | ((long long)gd.w << 32);
-    return run_lane<N, kFull>(pin, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent);
+    if constexpr (N == 1) {
+        return run_lane<N, kFull, false>(pin, pin[0].w, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent);
+    } else {
+        const int32_t *lb;
+        if (table_fits<N>(pin, lb))
+            return run_lane<N, kFull, true>(pin, lb, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent);
+        return run_lane<N, kFull, false>(pin, lb, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent);
+    }
 }
 
 template <bool kFull>
@@ -350,7 +382,7 @@ __device__ __forceinline__ uint32_t load_pins(const DevParams &P, int4 sv, int4 
         const uint32_t end = __ldg(P.wend + src * P.W + w);
         const uint32_t start = __ldg(P.wstart + src * P.W + w);
         pins[i].w = P.pool + __ldg(P.net_base + src) + start;
-        pins[i].len = (int32_t)(end - start);
+        pins[i].len = end - start;
         pins[i].drf = (uint32_t)d4[i];
         bound += end - start;
     }
@@ -581,8 +613,8 @@ __global__ void __launch_bounds__(kBlock) level_place_kernel(const DevParams P, 
 // and never wait for each other.  kFull: PATHPULSEPERCENT = 100.
 template <bool kFull>
 __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(const DevParams P, const LevelLaunch L) {
-    __shared__ PinHot pin_hot[kLevelWarps][GATSPI_MAX_PINS * 32];     // [pin][lane] per warp
-    __shared__ PinCold pin_cold[kLevelWarps][GATSPI_MAX_PINS * 32];
+    __shared__ int2 pin_hot[kLevelWarps][GATSPI_MAX_PINS * 32];       // [pin][lane] per warp
+    __shared__ uint32_t pin_end[kLevelWarps][GATSPI_MAX_PINS * 32];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int tile = blockIdx.x * kLevelWarps + warp;
@@ -650,7 +682,7 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
 
     LaneResult res{0, 0, 0, 0};
     if (valid) {
-        const PinTab tab{&pin_hot[warp][lane], &pin_cold[warp][lane]};
+        const PinTab tab{&pin_hot[warp][lane], &pin_end[warp][lane]};
         res = dispatch<kFull>(P, gd, pins, tab, Lw, P.pool + base + rel);
         if (res.err) {
             raise_error(P.status, res.err, g, w, 0);
@@ -798,7 +830,15 @@ cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t 
 }
 
 cudaError_t set_level_smem_limit(int W) {
-    return cudaFuncSetAttribute(level_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem_bytes(W));
+    // The simulation kernel's pin table takes 6 KB per block (7 KB with the driver's
+    // reserve): 9 blocks fit the 64 KB shared-memory configuration, which leaves the
+    // rest of the SM's 256 KB to L1 for the source waveforms.  The preference is a
+    // percentage of the 228 KB maximum, rounded up by the driver to a configuration.
+    cudaError_t e = cudaFuncSetAttribute(level_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 28);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(level_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 28);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(level_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem_bytes(W));
+    return e;
 }
 
 cudaError_t launch_load_index(const DevParams &p, const long long *off, long long nwords, int32_t *max_time,

@@ -114,8 +114,10 @@ class Caller:
             self.level_base.data_ptr(), self.net.num_inputs, self.W, gate_begin, num_gates,
             g.GATSPI_FLAG_PULSE_PERCENT, self.pulse_percent)
 
-    def run(self):
-        """Every level, in order; returns (offsets, pool, tc, t1) as host arrays."""
+    def run(self, gaps=None, host_pool=True):
+        """Every level, in order; returns (offsets, pool, tc, t1) as host arrays (the pool
+        stays on the device unless host_pool).  gaps: {level: words left unused before
+        the level's outputs}."""
         torch, g = self.torch, self.gatspi
         self.tc.zero_()
         self.t1.zero_()
@@ -123,6 +125,7 @@ class Caller:
         lo = self.net.level_offsets
         stream = torch.cuda.current_stream().cuda_stream
         for lvl in range(self.net.num_levels):
+            base += (gaps or {}).get(lvl, 0)
             self.level_base[0] = base
             g.gatspi_simulate_level_static(self.args(int(lo[lvl]), int(lo[lvl + 1] - lo[lvl])), stream)
             base = int(self.level_base[1].item())
@@ -132,7 +135,8 @@ class Caller:
         k = np.arange(self.N * self.W)
         start = nb[k // self.W] + ws
         length = we - ws
-        return (start, length, base), self.pool[:base].cpu().numpy(), self.tc.cpu().numpy(), self.t1.cpu().numpy()
+        pool = self.pool[:base].cpu().numpy() if host_pool else self.pool
+        return (start, length, base), pool, self.tc.cpu().numpy(), self.t1.cpu().numpy()
 
 
 def _regular(net, stim, pool_words, pulse_percent=100):
@@ -184,6 +188,34 @@ def test_static_levels_match_regular_path(built, name, q):
         assert _same_index(index, ref[0]), "waveform positions differ (run %d)" % attempt
         assert np.array_equal(_gather(pool, index), _gather(ref[1], ref[0])), "waveforms differ (run %d)" % attempt
         assert np.array_equal(tc, ref[2]) and np.array_equal(t1, ref[3]), "statistics differ (run %d)" % attempt
+
+
+def test_sources_far_apart(built):
+    """The inputs at the front of a pool of more than 2^32 words, the first level's
+    outputs beyond word 2^32: gates of the next levels read sources that far apart,
+    which the kernel's 32-bit pin offsets cannot span, so those lanes keep their pins
+    in registers.  Every waveform and statistic still equals the regular path's."""
+    import torch
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=600, num_inputs=16, num_levels=4, seed=9))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=16, cycles=300, period=300, activity=0.4,
+                                                      windows=40, seed=9, glitch_frac=0.3))
+    lo, P, fo = np.asarray(net.level_offsets), net.num_inputs, net.fanin_off
+    mixed = [g for g in range(lo[1], lo[2]) if (net.fanin_net[fo[g]:fo[g + 1]] < P).any()
+             and (net.fanin_net[fo[g]:fo[g + 1]] >= P).any()]
+    assert len(mixed) > 5
+    gap = 1 << 32
+    ref = _regular(net, stim, 1 << 24)
+    caller = Caller(net, stim, gap + (1 << 24))
+    index, pool, tc, t1 = caller.run(gaps={0: gap}, host_pool=False)
+    assert int(index[0][P * stim.num_windows:].max()) > gap           # the outputs do sit beyond 2^32
+    start, length = np.asarray(index[0], np.int64), np.asarray(index[1], np.int64)
+    first = np.concatenate(([0], np.cumsum(length)[:-1]))
+    pos = np.repeat(start - first, length) + np.arange(int(length.sum()))
+    got = pool[torch.from_numpy(pos).to(pool.device)].cpu().numpy()
+    assert np.array_equal(got, _gather(ref[1], ref[0]))
+    assert np.array_equal(tc, ref[2]) and np.array_equal(t1, ref[3])
+    del caller, pool
+    torch.cuda.empty_cache()
 
 
 def test_static_errors_and_limits(built):
