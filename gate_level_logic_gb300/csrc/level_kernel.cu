@@ -833,9 +833,10 @@ cudaError_t set_level_smem_limit(int W) {
     // The simulation kernel's pin table takes 6 KB per block (7 KB with the driver's
     // reserve): 9 blocks fit the 64 KB shared-memory configuration, which leaves the
     // rest of the SM's 256 KB to L1 for the source waveforms.  The preference is a
-    // percentage of the 228 KB maximum, rounded up by the driver to a configuration.
-    cudaError_t e = cudaFuncSetAttribute(level_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 28);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(level_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 28);
+    // percentage that the driver rounds up to a configuration: 20 gives 64 KB on
+    // GB300 (28 already gives 100 KB; 0 gives 8 KB and a single block per SM).
+    cudaError_t e = cudaFuncSetAttribute(level_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 20);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(level_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 20);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(level_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem_bytes(W));
     return e;
