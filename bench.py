@@ -116,11 +116,26 @@ def algorithmic_bytes(net, lengths, W):
     return np.array(per_level, dtype=np.int64)
 
 
-def _kernel_hash():
+def _code_only(text):
+    """Source text without // comments and blank lines: a comment edit leaves the
+    compiled kernel, and so its measured counters, unchanged."""
+    lines = []
+    for line in text.splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code:
+            lines.append(code)
+    return "\n".join(lines)
+
+
+def _kernel_hash(read=None):
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        if read is None:
+            with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update(_code_only(text).encode())
     return h.hexdigest()[:16]
 
 

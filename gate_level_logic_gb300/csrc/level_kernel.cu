@@ -1,6 +1,7 @@
 // Level kernels of the GB300 gate-level re-simulator.
 //
-// Two launches per logic level (GATSPI, Section 3, Fig. 5).
+// Three launches per logic level (GATSPI, Section 3, Fig. 5, whose two passes they
+// replace): planning, placement, simulation.
 //
 // level_plan_kernel plans the level before anything is simulated, one warp per
 // gate.  An output window can hold at most 3 + sum over pins of (input length - 2)
@@ -9,10 +10,11 @@
 // for each of the gate's windows from the window index of its sources, ranks the
 // windows by bound, largest first (a stable counting sort: equal bounds keep window
 // order, so the layout depends only on the inputs), and sums the bounds of every
-// group of 32 ranks.  The gate's region is the sum of all its bounds; a decoupled
-// look-back over the gates gives every region its pool offset.  The page sizes its
-// outputs with a full counting pass instead; the bound replaces that pass and leaves
-// a gap after each group (its size is the only cost).  The ranking is for load
+// group of 32 ranks.  The gate's region is the sum of all its bounds;
+// level_place_kernel scans the region sizes in gate order (a decoupled look-back
+// over tiles of 32 gates) into pool offsets.  The page sizes its outputs with a full
+// counting pass instead; the bound replaces that pass and leaves a gap after each
+// window (its size is the only cost).  The ranking is for load
 // balance: a warp runs as long as its slowest lane, and the bound follows a window's
 // event count closely, so a warp that gets 32 windows of similar bound keeps its
 // lanes busy.
@@ -35,9 +37,10 @@
 // minus length) stays unused.  Every (gate, window) is simulated once and no word is
 // moved afterwards.  The window index records each window's start and end relative
 // to its net's region, since windows are stored in rank order.  TC and T1 are
-// reduced per warp and added with one 64-bit atomic each.  The kernel uses no shared
-// memory, so the SM's whole L1 serves the source waveforms.  No warp waits for
-// another.
+// reduced per warp and added with one 64-bit atomic each.  The pins of a multi-pin
+// cell live in a small shared-memory table per warp (see PinTab), so that the event
+// loop keeps only the pins' next arrivals in registers and most of the SM's L1 is
+// left to the source waveforms.  No warp waits for another.
 //
 // No kernel traps: a malformed waveform, a missing delay arc, pool overflow or a
 // stalled look-back sets the device status word and the kernels carry on without
