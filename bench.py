@@ -285,7 +285,7 @@ def _e2e(args, sim, inputs, net, stream, dist, events_per_step, testbench):
     for _ in range(e2e_steps):
         load(pin_off, pin_words, stream=stream)
         sim.simulate(stream=stream)
-        tc_e, _, t1_e = sim.toggle_stats()
+        tc_e, t1_e, _ = sim.toggle_stats_view()   # the statistics in host memory, no extra copy
     torch.cuda.synchronize()
     e2e_s = _max_over_ranks(dist, time.perf_counter() - t)
     assert int(tc_e.sum()) == events_per_step
@@ -472,9 +472,9 @@ def run_gpu(args):
         "e2e": None if e2e_value is None else {
             "value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "path": "gatspi_load_testbench (whole-testbench waveforms from pinned host memory, cut into windows "
-                    "on the GPU) + gatspi_simulate + gatspi_toggle_stats",
+                    "on the GPU) + gatspi_simulate + gatspi_toggle_stats_host",
             "windowed_inputs": {"value": e2e_win[0], "h2d_bytes_per_step": int(e2e_win[1]),
-                                "path": "gatspi_load_waveforms (host-cut windows) + simulate + toggle_stats"}},
+                                "path": "gatspi_load_waveforms (host-cut windows) + simulate + toggle_stats_host"}},
         "testbench_cut": cut,
         "gpu_launches": int(args.steps * launches_per_step),   # planning (non-empty levels), placement, simulation
         "clocks": clocks.summary(),

@@ -647,6 +647,18 @@ gatspi_status gatspi_toggle_stats(gatspi_ctx *c, int64_t *tc, int64_t *t0, int64
     return GATSPI_OK;
 }
 
+gatspi_status gatspi_toggle_stats_host(gatspi_ctx *c, const uint64_t **tc, const uint64_t **t1, int64_t *window_sum) {
+    g_err.clear();
+    if (!c || !tc || !t1) return fail(GATSPI_EINVAL, "ctx, tc and t1 are required");
+    if (!c->simulated) return fail(GATSPI_ESTATE, "simulate first");
+    gatspi_status st = sync_ctx(c);
+    if (st != GATSPI_OK) return st;
+    *tc = c->G > 0 ? (const uint64_t *)c->tc_host : nullptr;
+    *t1 = c->G > 0 ? (const uint64_t *)c->t1_host : nullptr;
+    if (window_sum) *window_sum = c->sum_window_len;
+    return GATSPI_OK;
+}
+
 gatspi_status gatspi_input_stats(gatspi_ctx *c, int64_t *tc, int64_t *t0, int64_t *t1) {
     g_err.clear();
     if (!c) return fail(GATSPI_EINVAL, "ctx is NULL");

@@ -81,6 +81,7 @@ SIGNATURES = {
     "gatspi_simulate": (ctypes.c_int, [_p, _p]),
     "gatspi_sync": (ctypes.c_int, [_p]),
     "gatspi_toggle_stats": (ctypes.c_int, [_p, _p, _p, _p]),
+    "gatspi_toggle_stats_host": (ctypes.c_int, [_p, ctypes.POINTER(_p), ctypes.POINTER(_p), ctypes.POINTER(ctypes.c_int64)]),
     "gatspi_input_stats": (ctypes.c_int, [_p, _p, _p, _p]),
     "gatspi_write_saif": (ctypes.c_int, [_p, ctypes.c_char_p, ctypes.c_char_p, ctypes.c_char_p, _p]),
     "gatspi_get_waveform": (ctypes.c_int, [_p, ctypes.c_int32, ctypes.c_int32, _p, ctypes.c_size_t,
@@ -153,6 +154,13 @@ def gatspi_sync(ctx: int):
 
 def gatspi_toggle_stats(ctx: int, tc: int, t0: int, t1: int):
     _check(library().gatspi_toggle_stats(_p(ctx), _p(tc), _p(t0), _p(t1)))
+
+
+def gatspi_toggle_stats_host(ctx: int):
+    """(tc pointer, t1 pointer, sum of window lengths)."""
+    tc, t1, ws = _p(), _p(), ctypes.c_int64()
+    _check(library().gatspi_toggle_stats_host(_p(ctx), ctypes.byref(tc), ctypes.byref(t1), ctypes.byref(ws)))
+    return tc.value or 0, t1.value or 0, ws.value
 
 
 def gatspi_input_stats(ctx: int, tc: int, t0: int, t1: int):

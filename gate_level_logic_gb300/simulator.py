@@ -146,6 +146,21 @@ class Simulator:
         n = self.num_gates
         return tc[:n], t0[:n], t1[:n]
 
+    def toggle_stats_view(self):
+        """(tc, t1, sum of window lengths) without a copy: read-only uint64 views of
+        the library's pinned host buffers, valid until the next simulate or close
+        (t0 = sum of window lengths - t1)."""
+        tcp, t1p, ws = _c.gatspi_toggle_stats_host(self.ctx)
+        if self.num_gates == 0 or not tcp:
+            empty = np.zeros(0, np.uint64)
+            return empty, empty, ws
+        u64 = ctypes.POINTER(ctypes.c_uint64)
+        tc = np.ctypeslib.as_array(ctypes.cast(tcp, u64), shape=(self.num_gates,))
+        t1 = np.ctypeslib.as_array(ctypes.cast(t1p, u64), shape=(self.num_gates,))
+        tc.flags.writeable = False
+        t1.flags.writeable = False
+        return tc, t1, ws
+
     def waveform(self, net: int, window: int) -> np.ndarray:
         n = _c.gatspi_get_waveform(self.ctx, net, window, 0, 0)
         buf = np.zeros(max(n, 1), np.int32)

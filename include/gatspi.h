@@ -265,6 +265,16 @@ gatspi_status gatspi_sync(gatspi_ctx *ctx);
 gatspi_status gatspi_toggle_stats(gatspi_ctx *ctx, int64_t *tc, int64_t *t0, int64_t *t1);
 
 /*
+ * The same statistics without a copy: *tc and *t1 point at the library's pinned host
+ * copies (uint64 [num_gates], gate order) that simulate filled level by level, valid
+ * until the next simulate or destroy; t0 = sum of window_len - t1 (*window_sum).
+ * Synchronises first.  GATSPI_ESTATE before the first simulate; NULL pointers for a
+ * netlist without gates.
+ */
+gatspi_status gatspi_toggle_stats_host(gatspi_ctx *ctx, const uint64_t **tc, const uint64_t **t1,
+                                       int64_t *window_sum);
+
+/*
  * The same statistics for the inputs, from the loaded windows (host arrays
  * [num_inputs]; any may be NULL): computed on the device by every load.
  */

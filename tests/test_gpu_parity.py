@@ -193,6 +193,20 @@ def test_level_timing_switch(gpu, oracle_lib):
         assert np.array_equal(tc, ref.tc) and np.array_equal(t1, ref.t1)
 
 
+def test_toggle_stats_view(gpu, oracle_lib):
+    """The zero-copy statistics equal the copied ones and the oracle's."""
+    net, stim = synth.make("50k")
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    with gpu(net, stim.window_len, pool_words=pool_for(ref, net)) as sim:
+        sim.load(stim.pi_off, stim.pi_words)
+        sim.simulate()
+        tc, t1, ws = sim.toggle_stats_view()
+        ctc, ct0, ct1 = sim.toggle_stats()
+        assert not tc.flags.writeable
+        assert np.array_equal(tc.astype(np.int64), ref.tc) and np.array_equal(t1.astype(np.int64), ref.t1)
+        assert np.array_equal(ctc, ref.tc) and np.array_equal(ws - t1.astype(np.int64), ct0)
+
+
 def test_replay_is_deterministic(gpu, oracle_lib):
     net, stim = synth.make("50k")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
