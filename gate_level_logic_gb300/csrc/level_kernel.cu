@@ -305,7 +305,12 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb,
         for (uint32_t m = more; m; m &= m - 1u) d = min(d, arc_delay<N>(D, vbits, N - __ffs(m), e_out));
         bool chg = y != (po & 1);
         lutbad |= chg && d == kNoArc;
-        chg = chg && d != kNoArc;
+        // At q = 100 a missing arc only taints this lane's output, which the error
+        // then discards: its entry (t + the no-arc value wraps below t) is never
+        // cancelled, so the output index stays within the window's slot, and the
+        // filter decision does not have to wait for the delay load.  Below 100 the
+        // reject limit of such a delay is meaningless, so the change is dropped.
+        if (!kFull) chg = chg && d != kNoArc;
         const int32_t to = (int32_t)((uint32_t)t + (uint32_t)d);   // used only when chg
         // inertial filter: at q = 100, to - top < d exactly when the last entry
         // has not matured (top > t); otherwise the reject limit decides
