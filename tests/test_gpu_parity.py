@@ -259,6 +259,32 @@ def test_errors_leave_context_usable(gpu, oracle_lib):
         assert e.value.name == "GATSPI_EBADLUT"
 
 
+@pytest.mark.parametrize("q", [100, 50, 0])
+def test_missing_arc_after_valid_events(gpu, oracle_lib, q):
+    """A buffer whose output-fall arc is missing: the rise at 50 is simulated, the
+    fall at 120 meets the missing arc and the run reports GATSPI_EBADLUT at every
+    PATHPULSEPERCENT; the same context then simulates a stimulus that never needs
+    the arc, and the oracle agrees on it."""
+    from gate_level_logic_gb300 import GatspiError
+    tt = np.array([0, 0, 1, 1], np.uint8)                       # output = first pin
+    D = np.full((8, 2), INF, np.int32)
+    D[0, :] = 5                                                 # first pin rise -> output rise
+    net = single_gate(tt, 2, D)
+    st = synth.from_waveforms([[[0, 50, 120, 300, EOW]], [[0, 70, EOW]]], 400)
+    with gpu(net, st.window_len, pool_words=4096, pulse_percent=q) as sim:
+        sim.load(st.pi_off, st.pi_words)
+        sim.simulate()
+        with pytest.raises(GatspiError) as e:
+            sim.sync()
+        assert e.value.name == "GATSPI_EBADLUT"
+        rise_only = synth.from_waveforms([[[0, 50, EOW]], [[0, 70, EOW]]], 400)
+        ref = oracle_lib.simulate(net, rise_only, pulse_percent=q)
+        sim.load(rise_only.pi_off, rise_only.pi_words)
+        sim.simulate()
+        tc, t0, t1 = sim.toggle_stats()
+        assert np.array_equal(tc, ref.tc) and np.array_equal(t1, ref.t1)
+
+
 def test_single_waveform_and_window_export(gpu, oracle_lib):
     net, stim = synth.make("50k")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
