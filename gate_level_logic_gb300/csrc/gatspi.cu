@@ -120,6 +120,7 @@ struct gatspi_ctx {
         p.wend = wend;
         p.wlen8 = wlen8;
         p.w8stride = (W + 3) & ~3;
+        p.plan_words = plan_words(W);
         p.perm = perm;
         p.goff = goff;
         p.window_len = window_len;

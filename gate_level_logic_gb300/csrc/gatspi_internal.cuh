@@ -68,6 +68,7 @@ struct DevParams {
     int32_t num_inputs;
     int32_t W;
     int32_t w8stride;         // W rounded up to a multiple of 4 (rows of wlen8 start 4-byte aligned)
+    int32_t plan_words;       // shared words per warp of the planning kernel (plan_words(W))
     int32_t ngroups;          // ceil(W / 32): groups of 32 ranks per gate
     uint32_t ngroups_m;       // floor((2^32 - 1) / ngroups): tile / ngroups by a multiply-high
     int32_t lpg_log2;         // log2(lanes per (gate, group) segment)
@@ -84,6 +85,7 @@ struct LevelLaunch {
     long long tile_base;    // first look-back word of this level's plan
 };
 
+int plan_words(int W);
 size_t plan_smem_bytes(int W);
 int plan_gates_per_tile(int W);   // gates (warps) of one planning block
 cudaError_t set_level_smem_limit(int W);   // the planning kernel's shared memory, the simulation kernels' L1

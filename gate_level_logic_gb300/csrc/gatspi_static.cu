@@ -104,6 +104,7 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     p.wend = a->wend;
     p.wlen8 = a->wlen8;
     p.w8stride = (a->num_windows + 3) & ~3;
+    p.plan_words = plan_words(a->num_windows);
     p.perm = a->perm;
     p.goff = a->goff;
     p.window_len = a->window_len;

@@ -485,14 +485,12 @@ __device__ __forceinline__ long long plan_bounds(const DevParams &P, int4 sv, in
         const uint32_t base = 3u - 2u * (uint32_t)N;
         const uint32_t b[4] = {base + (even & 0xffffu) + fix[0], base + (odd & 0xffffu) + fix[1],
                                base + (even >> 16) + fix[2], base + (odd >> 16) + fix[3]};
+        // the four bounds in one 16-byte store (padding words past W included): the
+        // lanes' stores do not share banks
+        *reinterpret_cast<uint4 *>(bnd + w0) = make_uint4(b[0], b[1], b[2], b[3]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int w = w0 + u;
-            if (w < W) {
-                bnd[w] = b[u];
-                lane_sum += b[u];
-            }
-        }
+        for (int u = 0; u < 4; ++u)
+            if (w0 + u < W) lane_sum += b[u];
     }
     return lane_sum;
 }
@@ -503,11 +501,12 @@ __device__ __forceinline__ long long plan_bounds(const DevParams &P, int4 sv, in
 // warp: the bounds of the gate's windows, the bucket counters of the counting sort,
 // the group sums.  level_place_kernel then scans the sizes into pool offsets.
 __global__ void __launch_bounds__(kPlanWarps * 32, kPlanMinBlocks) level_plan_kernel(const DevParams P, const LevelLaunch L) {
-    extern __shared__ uint32_t psm[];
+    extern __shared__ __align__(16) uint32_t psm[];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    uint32_t *bnd = psm + (size_t)warp * (P.W + kSortBuckets + P.ngroups);
-    uint32_t *hist = bnd + P.W;
+    // every array starts 16-byte aligned, so four words move in one access
+    uint32_t *bnd = psm + (size_t)warp * P.plan_words;
+    uint32_t *hist = bnd + P.w8stride;
     uint32_t *gsum = hist + kSortBuckets;
     const int gl = blockIdx.x * (blockDim.x >> 5) + warp;   // the gate of this warp
     if (gl >= L.num_gates) return;
@@ -538,19 +537,23 @@ __global__ void __launch_bounds__(kPlanWarps * 32, kPlanMinBlocks) level_plan_ke
             atomicAdd(&hist[kSortBuckets - 1 - min(bnd[w], (uint32_t)(kSortBuckets - 1))], 1u);
         __syncwarp();
         {   // exclusive scan of the bucket counts: the first rank of every bucket
-            constexpr int kPer = kSortBuckets / 32;
-            uint32_t v[kPer], sum = 0;
-#pragma unroll
-            for (int k = 0; k < kPer; ++k) {
-                v[k] = hist[lane * kPer + k];
-                sum += v[k];
-            }
-            uint32_t run = warp_incl_scan(sum, lane) - sum;
-#pragma unroll
-            for (int k = 0; k < kPer; ++k) {
-                hist[lane * kPer + k] = run;
-                run += v[k];
-            }
+            constexpr int kPer = kSortBuckets / 32;   // 8 buckets per lane, two 16-byte accesses
+            static_assert(kPer == 8, "the scan moves a lane's buckets as two uint4");
+            uint4 *mine = reinterpret_cast<uint4 *>(hist + lane * kPer);
+            uint4 lo = mine[0], hi = mine[1];
+            const uint32_t slo = lo.x + lo.y + lo.z + lo.w;
+            uint32_t run = warp_incl_scan(slo + hi.x + hi.y + hi.z + hi.w, lane) - (slo + hi.x + hi.y + hi.z + hi.w);
+            // exclusive prefix of the lane's eight buckets, in place
+            uint32_t t = lo.x; lo.x = run; run += t;
+            t = lo.y; lo.y = run; run += t;
+            t = lo.z; lo.z = run; run += t;
+            t = lo.w; lo.w = run; run += t;
+            t = hi.x; hi.x = run; run += t;
+            t = hi.y; hi.y = run; run += t;
+            t = hi.z; hi.z = run; run += t;
+            hi.w = run;
+            mine[0] = lo;
+            mine[1] = hi;
         }
         __syncwarp();
         // ranks, windows in order so that equal bounds keep window order
@@ -808,8 +811,12 @@ cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const i
 
 int plan_gates_per_tile(int W) { return W > 4096 ? 1 : kPlanWarps; }   // one warp per block for long window lists
 
-size_t plan_smem_bytes(int W) {   // per warp: W bounds, the buckets, the group sums
-    return (size_t)plan_gates_per_tile(W) * ((size_t)W + kSortBuckets + (size_t)(W + 31) / 32) * sizeof(uint32_t);
+int plan_words(int W) {   // per warp: W bounds, the buckets, the group sums, each padded to 4 words
+    return ((W + 3) & ~3) + kSortBuckets + (((W + 31) / 32 + 3) & ~3);
+}
+
+size_t plan_smem_bytes(int W) {
+    return (size_t)plan_gates_per_tile(W) * (size_t)plan_words(W) * sizeof(uint32_t);
 }
 
 cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
