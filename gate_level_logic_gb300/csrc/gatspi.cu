@@ -427,7 +427,7 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
             ll.num_gates = c->level_offsets[l + 1] - c->level_offsets[l];
             const long long slots = (long long)ll.num_gates * c->slots_per_gate;
             const long long tiles = std::max<long long>(1, (slots + kTileSlots - 1) / kTileSlots);
-            const long long scan = std::max<long long>(1, ((long long)ll.num_gates + 31) / 32);   // placement tiles
+            const long long scan = std::max<long long>(1, ((long long)ll.num_gates + kPlaceTile - 1) / kPlaceTile);
             if (tiles > INT32_MAX / kTileSlots)
                 return fail(GATSPI_EINVAL, "level %d has too many (gate, window) slots", l);
             ll.num_tiles = (int32_t)tiles;

@@ -11,6 +11,7 @@ namespace gatspi {
 
 constexpr int kBlock = 256;               // threads per block of the light kernels
 constexpr int kWarps = kBlock / 32;
+constexpr int kPlaceTile = 1024;          // gates per block (and look-back tile) of the placement scan
 #ifndef GATSPI_LEVEL_WARPS
 #define GATSPI_LEVEL_WARPS 4
 #endif
@@ -60,7 +61,7 @@ struct DevParams {
     unsigned long long *tc;    // [G]
     unsigned long long *t1;    // [G]
     // scan state
-    unsigned long long *tile_status;  // [total look-back tiles: 32 gates each], zeroed per simulate
+    unsigned long long *tile_status;  // [total look-back tiles: kPlaceTile gates each], zeroed per simulate
     int32_t *tickets;                 // [L], zeroed per simulate
     long long *level_base;            // [L+1]; [0] = words of the input waveforms
     int32_t *status;                  // [kStatusWords]
@@ -81,7 +82,7 @@ struct LevelLaunch {
     int32_t gate_begin;
     int32_t num_gates;
     int32_t num_tiles;      // warps of the level kernel: ceil(gates * slots_per_gate / 32)
-    int32_t scan_tiles;     // warps of the placement scan: max(1, ceil(gates / 32))
+    int32_t scan_tiles;     // blocks of the placement scan: max(1, ceil(gates / kPlaceTile))
     long long tile_base;    // first look-back word of this level's plan
 };
 

@@ -18,7 +18,7 @@ using namespace gatspi;
 
 namespace {
 
-constexpr int kStaticTiles = 1 << 18;                     // scan tiles (gates) of one level at most
+constexpr int kStaticTiles = 1 << 13;                     // placement tiles (1024 gates each) of one level at most
 constexpr int kTicketWord = kStaticTiles;                 // index of the ticket word
 constexpr int kStatusWord = kStaticTiles + 1;             // index of the status words (2 x 8 bytes)
 constexpr int kScratchWords = kStaticTiles + 4;
@@ -70,9 +70,9 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     p.slots_per_gate = p.ngroups << p.lpg_log2;
     const long long slots = (long long)a->num_gates * p.slots_per_gate;
     const long long tiles = slots > 0 ? (slots + kTileSlots - 1) / kTileSlots : 1;
-    const long long scan = a->num_gates > 0 ? ((long long)a->num_gates + 31) / 32 : 1;   // placement tiles
+    const long long scan = a->num_gates > 0 ? ((long long)a->num_gates + kPlaceTile - 1) / kPlaceTile : 1;
     if (scan > kStaticTiles)
-        return err(GATSPI_EINVAL, "level too large for the static scratch (at most 262144 x 32 gates)");
+        return err(GATSPI_EINVAL, "level too large for the static scratch (at most 8192 x 1024 gates)");
     if (tiles > INT32_MAX / kTileSlots) return err(GATSPI_EINVAL, "level has too many (gate, window) slots");
 
     // once per device, with that device current: the device address of the scratch

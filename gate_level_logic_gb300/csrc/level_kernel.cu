@@ -591,33 +591,52 @@ __global__ void __launch_bounds__(kPlanWarps * 32, kPlanMinBlocks) level_plan_ke
 }
 
 // Pool offsets of the level's gate regions: their sizes (from the plan) scanned in
-// gate order, one thread per gate, warp shuffles plus a decoupled look-back over
-// warp tiles; the values are ready when this kernel starts, so the waits are short.
-__global__ void __launch_bounds__(kBlock) level_place_kernel(const DevParams P, const LevelLaunch L) {
+// gate order, one thread per gate and one tile of kPlaceTile gates per block (warp
+// shuffles, then the warps' totals), and a decoupled look-back over the tiles; the
+// values are ready when this kernel starts, so the waits are short and few.
+__global__ void __launch_bounds__(kPlaceTile) level_place_kernel(const DevParams P, const LevelLaunch L) {
+    __shared__ long long warp_sum[kPlaceTile / 32];
+    __shared__ long long tile_base;
+    __shared__ int tile_id, stop;
     const int lane = threadIdx.x & 31;
-    int tile = 0;
-    if (lane == 0) tile = atomicAdd(P.tickets + L.level, 1);
-    tile = __shfl_sync(0xffffffffu, tile, 0);
-    if (tile >= L.scan_tiles) return;                      // spare warps of the last block
-    const int32_t st = lane == 0 ? ld_status(P.status) : 0;
-    const int gl = tile * 32 + lane;
-    const long long raw = gl < L.num_gates ? (long long)__ldg(P.goff + (long long)gl * (P.ngroups + 1) + P.ngroups) : 0;
-    const bool skip = __shfl_sync(0xffffffffu, st, 0) != 0;
-    const bool valid = !skip && gl < L.num_gates;
-    const long long size = valid ? raw : 0;
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        tile_id = atomicAdd(P.tickets + L.level, 1);
+        stop = ld_status(P.status) != 0;
+    }
+    __syncthreads();
+    const int tile = tile_id;
+    if (tile >= L.scan_tiles) return;                      // spare blocks
+    const int gl = tile * kPlaceTile + threadIdx.x;
+    const bool valid = !stop && gl < L.num_gates;
+    const long long size = valid ? (long long)__ldg(P.goff + (long long)gl * (P.ngroups + 1) + P.ngroups) : 0;
     long long incl = size;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const long long v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
     }
-    const long long total = __shfl_sync(0xffffffffu, incl, 31);
-    const long long base = P.level_base[L.level] + look_back(P, L, tile, total, lane);
-    if (lane == 0 && tile == L.scan_tiles - 1) {
-        P.level_base[L.level + 1] = base + total;
-        if (base + total > P.pool_words) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, 0, 0);
+    if (lane == 31) warp_sum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        // the warps' totals scanned, then the tile's offset from the look-back
+        const long long t = warp_sum[lane];
+        long long ti = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, ti, o);
+            if (lane >= o) ti += v;
+        }
+        const long long total = __shfl_sync(0xffffffffu, ti, 31);
+        const long long base = P.level_base[L.level] + look_back(P, L, tile, total, lane);
+        warp_sum[lane] = base + ti - t;                    // the first word of each warp's gates
+        if (lane == 0 && tile == L.scan_tiles - 1) {
+            P.level_base[L.level + 1] = base + total;
+            if (base + total > P.pool_words) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, 0, 0);
+        }
     }
-    if (valid) P.net_base[(long long)P.num_inputs + L.gate_begin + gl] = base + incl - size;
+    __syncthreads();
+    if (valid) P.net_base[(long long)P.num_inputs + L.gate_begin + gl] = warp_sum[warp] + incl - size;
 }
 
 // One warp = 32 slots of the level: a gate and 32 of its ranks.  Warps share nothing
@@ -826,7 +845,7 @@ cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaSt
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    level_place_kernel<<<(unsigned)((l.scan_tiles + kWarps - 1) / kWarps), kBlock, 0, s>>>(p, l);
+    level_place_kernel<<<(unsigned)l.scan_tiles, kPlaceTile, 0, s>>>(p, l);
     return cudaGetLastError();
 }
 

@@ -405,13 +405,13 @@ typedef struct {
  * through its own allocator, or code that must not allocate once it has started.
  * The caller passes every input and output buffer (gatspi_level_args); the only
  * scratch, the look-back flags of the output-region scan, its tile ticket and the
- * status word, lives in a file-scope device array of 262144 tile flags plus 32
- * bytes (about 2 MiB) that every GPU which loads the library holds until the
+ * status word, lives in a file-scope device array of 8192 tile flags plus 32
+ * bytes (about 64 KiB) that every GPU which loads the library holds until the
  * process exits.
  *
  *   - No cudaMalloc, cudaFree or allocating library call is made.
- *   - A level may have at most 262144 x 32 = 8388608 gates (one look-back flag per
- *     32); a larger level returns GATSPI_EINVAL before anything runs.  The caller
+ *   - A level may have at most 8192 x 1024 = 8388608 gates (one look-back flag per
+ *     1024); a larger level returns GATSPI_EINVAL before anything runs.  The caller
  *     also makes sure the gates exist.
  *   - The first call on a device looks up the device address of the scratch array
  *     (with that device current); make that first call before any stream capture.

@@ -233,7 +233,7 @@ def test_static_errors_and_limits(built):
     assert _same_index(index, ref[0]) and np.array_equal(tc, ref[2])
     assert np.array_equal(_gather(pool, index), _gather(ref[1], ref[0]))
     # a level beyond the fixed scratch is refused before anything runs: one
-    # look-back flag per 32 gates, and 2^25 gates > 262144 x 32
+    # look-back flag per 1024 gates, and 2^25 gates > 8192 x 1024
     assert stim.num_windows == 1
     big = caller.args(0, 1 << 25)
     with pytest.raises(GatspiError) as e:
