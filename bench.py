@@ -84,14 +84,20 @@ def _sum_over_ranks(dist, x: float) -> float:
     return float(t.item())
 
 
-def workload_config(net, stim, pulse_percent=100):
+def workload_config(net, stim, pulse_percent=100, overrides=None):
+    name = ("1M-gate synthetic netlist, 40 levels, 9-cell mix with SDF-conditional arcs; "
+            "4096 inputs, 10k cycles x period 1000, 5% activity, 10% glitch pairs; 256 cycle windows")
+    extra = {}
+    if overrides:
+        name = "not the default workload: " + name + ", with the overrides listed"
+        extra["overrides"] = overrides
     return {
-        "workload": "1M-gate synthetic netlist, 40 levels, 9-cell mix with SDF-conditional arcs; "
-                    "4096 inputs, 10k cycles x period 1000, 5% activity, 10% glitch pairs; 256 cycle windows",
+        "workload": name,
         "gates": int(net.num_gates), "levels": int(net.num_levels), "inputs": int(net.num_inputs),
         "edges": int(net.num_edges), "windows": int(stim.num_windows), "cycles": int(stim.window_cycles.sum()),
         "pulse_percent": pulse_percent,
         "l2": "inputs larger than L2 (waveform pool of several GB per step, no flush needed)",
+        **extra,
     }
 
 
@@ -367,7 +373,13 @@ def run_gpu(args):
         over["cycles"] = args.cycles
     if args.gates:
         over["net_num_gates"] = args.gates
-    net, stim = synth.make(WORKLOAD, **over)
+    if args.sweep:
+        activity, windows = args.sweep.split(":")
+        net, stim = synth.sweep(float(activity), int(windows))
+        over = {"sweep_point": {"activity": float(activity), "windows": int(windows), "stimulus_seed": 4,
+                                "glitch_pairs": 0.0}}
+    else:
+        net, stim = synth.make(WORKLOAD, **over)
     W = stim.num_windows
     flags = 0
     pool_words = int(args.pool_gb * (1 << 30) / 4)
@@ -442,7 +454,7 @@ def run_gpu(args):
     traffic = _traffic(net.num_levels)
 
     # ---- end to end through the C ABI: host buffers, copies inside the region ---
-    if args.no_e2e:
+    if args.no_e2e or args.sweep:      # the end-to-end legs run on the default workload only
         e2e_value, h2d, d2h, e2e_win, cut = None, 0, 0, None, None
     else:
         tb = synth.testbench(WORKLOAD, **over)
@@ -454,7 +466,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": workload_config(net, stim, args.pulse_percent),
+        "config": workload_config(net, stim, args.pulse_percent, over),
         "gate_cycles_per_s": gate_cycles_per_s,
         "events_per_step": events_per_step,
         "pool_words_used": pool_used,
@@ -506,6 +518,8 @@ def main():
     ap.add_argument("--windows", type=int, default=0, help="profiling only: number of cycle windows")
     ap.add_argument("--cycles", type=int, default=0, help="profiling only: number of stimulus cycles")
     ap.add_argument("--gates", type=int, default=0, help="profiling only: number of gates of the netlist")
+    ap.add_argument("--sweep", default="", metavar="ACTIVITY:WINDOWS",
+                    help="one point of the activity x windows sweep on the same netlist instead of the default")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
