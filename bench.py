@@ -451,7 +451,7 @@ def run_gpu(args):
         peak_src = "measured"
     else:
         peak, peak_src = 6800.0, "fallback"
-    traffic = _traffic(net.num_levels)
+    traffic = None if over else _traffic(net.num_levels)   # the record is of the default workload
 
     # ---- end to end through the C ABI: host buffers, copies inside the region ---
     if args.no_e2e or args.sweep:      # the end-to-end legs run on the default workload only
