@@ -11,8 +11,9 @@ Prints one JSON line (rank 0):
              GPU, simulate, D2H of the toggle statistics (and, for comparison, the same
              with windows cut on the host beforehand)
   roofline   the level kernel against the measured HBM copy bandwidth, on
-             algorithmic bytes (each consumed waveform read once, each output
-             written once, window index read and written once, descriptors once)
+             algorithmic bytes (each consumed waveform read once per run, each
+             output written once, 8 B of window index per consumed (net, window)
+             and per (gate, window), descriptors once)
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
 
 ``--impl reference`` times the CPU oracle instead (a plain event-driven simulator,
@@ -102,24 +103,40 @@ def workload_config(net, stim, pulse_percent=100, overrides=None):
 
 
 def algorithmic_bytes(net, lengths, W):
-    """Per-level algorithmic bytes from the run's own waveform lengths."""
-    P, G, L = net.num_inputs, net.num_gates, net.num_levels
+    """Algorithmic bytes of one run (every level): each consumed (net, window) waveform
+    read once, each output written once, 8 B of window index per consumed (net,
+    window) and per (gate, window), and the gate descriptors once (16 B per gate and
+    per fanin edge).  Returns (total, parts)."""
+    P, G = net.num_inputs, net.num_gates
     lens = np.asarray(lengths, np.int64).reshape(P + G, W)
     net_words = lens.sum(axis=1)
-    ngroups = (W + 31) // 32
-    idx_bytes_per_net = 8 * W + 8                     # wstart + wend per window, the net's base
-    plan_bytes_per_gate = 2 * W + 4 * ngroups         # the level's plan: ranks, group offsets (read once)
-    per_level = []
+    consumed = np.unique(net.fanin_net)
+    parts = {
+        "read_waveforms": 4 * int(net_words[consumed].sum()),
+        "write_waveforms": 4 * int(net_words[P:].sum()),
+        "window_index": 8 * W * (int(consumed.size) + G),
+        "descriptors": 16 * G + 16 * int(net.num_edges),
+    }
+    return sum(parts.values()), parts
+
+
+def demand_bytes(net, lengths, W):
+    """Per level: the waveforms of every distinct source net of the level read (a net
+    consumed by several levels counts in each), the level's outputs written, their
+    window index read and written, and the level's gate descriptors."""
+    P = net.num_inputs
+    lens = np.asarray(lengths, np.int64).reshape(-1, W)
+    net_words = lens.sum(axis=1)
     lo = net.level_offsets
-    for lvl in range(L):
+    out = []
+    for lvl in range(net.num_levels):
         g0, g1 = int(lo[lvl]), int(lo[lvl + 1])
         srcs = np.unique(net.fanin_net[net.fanin_off[g0]:net.fanin_off[g1]])
-        read = 4 * int(net_words[srcs].sum()) + idx_bytes_per_net * srcs.size
-        write = 4 * int(net_words[P + g0:P + g1].sum()) + idx_bytes_per_net * (g1 - g0)
+        read = 4 * int(net_words[srcs].sum()) + 8 * W * srcs.size
+        write = 4 * int(net_words[P + g0:P + g1].sum()) + 8 * W * (g1 - g0)
         desc = 16 * (g1 - g0) + 16 * int(net.fanin_off[g1] - net.fanin_off[g0])
-        stats = 16 * (g1 - g0) * ngroups
-        per_level.append(read + write + desc + stats + plan_bytes_per_gate * (g1 - g0))
-    return np.array(per_level, dtype=np.int64)
+        out.append(read + write + desc)
+    return np.array(out, dtype=np.int64)
 
 
 def _code_only(text):
@@ -145,18 +162,21 @@ def _kernel_hash(read=None):
     return h.hexdigest()[:16]
 
 
-def _traffic(launches):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this
-    exact kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "level_kernel_1M_traffic.json")
+def _traffic(demand_per_launch):
+    """DRAM bytes per level_kernel launch: the ratio of DRAM traffic to demand bytes
+    that ncu measured on the committed small case (the same kernel source, two
+    launches), applied to this workload's mean demand bytes per launch; None when the
+    record is missing or was taken on other kernel code."""
+    path = os.path.join(ROOT, "profiles", "level_kernel_small_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
-        return None
+        return None, None
     if rec.get("kernel_sha") != _kernel_hash():
-        return None
-    return rec.get("dram_bytes_per_launch")
+        return None, None
+    ratio = float(rec["dram_bytes"]) / float(rec["demand_bytes"])
+    return ratio * float(demand_per_launch), ratio
 
 
 class ClockSampler:
@@ -393,8 +413,13 @@ def run_gpu(args):
     tc, t0, t1 = sim.toggle_stats()
     events_per_step = int(tc.sum())
     _, lengths = sim.export_offsets()
-    lvl_bytes = algorithmic_bytes(net, lengths, W)
+    run_bytes, run_parts = algorithmic_bytes(net, lengths, W)
+    lvl_demand = demand_bytes(net, lengths, W)
     waveform_words = int(lengths.sum())
+    if args.dump_levels and rank == 0:
+        with open(args.dump_levels, "w") as f:
+            json.dump({"demand_bytes": lvl_demand.tolist(), "algorithmic_bytes_per_run": run_bytes,
+                       "algorithmic_parts": run_parts}, f)
     pool_used = sim.pool_used()
     del lengths
 
@@ -441,9 +466,10 @@ def run_gpu(args):
     launches_per_step = int(2 * net.num_levels + np.count_nonzero(np.diff(lo)))
     gate_cycles_per_s = _sum_over_ranks(dist, gate_cycles * args.steps) / total_s
 
-    # roofline of the level kernel: algorithmic bytes / its own event time
+    # roofline of the level kernel: the run's algorithmic bytes per launch (one launch
+    # per level) over its mean launch time, i.e. all of them over its total time
     kern_s = level_ms.sum() / 1e3
-    achieved = float(lvl_bytes.sum() * args.steps / kern_s / 1e9)
+    achieved = float(run_bytes * args.steps / kern_s / 1e9)
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(peaks_path):
         with open(peaks_path) as f:
@@ -451,7 +477,7 @@ def run_gpu(args):
         peak_src = "measured"
     else:
         peak, peak_src = 6800.0, "fallback"
-    traffic = None if over else _traffic(net.num_levels)   # the record is of the default workload
+    traffic, traffic_ratio = _traffic(float(lvl_demand.mean()))
 
     # ---- end to end through the C ABI: host buffers, copies inside the region ---
     if args.no_e2e or args.sweep:      # the end-to-end legs run on the default workload only
@@ -475,7 +501,14 @@ def run_gpu(args):
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": traffic, "peak_source": peak_src,
             "kernel": "level_kernel (one launch per logic level)",
-            "algorithmic_bytes_per_launch": float(lvl_bytes.mean()),
+            "algorithmic_bytes_per_launch": float(run_bytes) / net.num_levels,
+            "algorithmic_bytes_per_step": run_parts,
+            "demand_bytes_per_launch": float(lvl_demand.mean()),
+            "traffic_note": None if traffic is None else
+            "ncu DRAM bytes / demand bytes = %.3f on the committed small case "
+            "(profiles/level_kernel_small_traffic.json), times this workload's demand bytes per launch"
+            % traffic_ratio,
+            "step_achieved_gbs": float(run_bytes * args.steps / total_s / 1e9),
             "avg_launch_ms": float(level_ms.sum() / (args.steps * net.num_levels)),
             "share_of_step": float(level_ms.sum() / sum(serial_ms)),
             "serialised_step_ms": float(np.mean(serial_ms)),
@@ -518,6 +551,8 @@ def main():
     ap.add_argument("--windows", type=int, default=0, help="profiling only: number of cycle windows")
     ap.add_argument("--cycles", type=int, default=0, help="profiling only: number of stimulus cycles")
     ap.add_argument("--gates", type=int, default=0, help="profiling only: number of gates of the netlist")
+    ap.add_argument("--dump-levels", default="", metavar="PATH",
+                    help="profiling only: write the run's per-level demand bytes to PATH (JSON)")
     ap.add_argument("--sweep", default="", metavar="ACTIVITY:WINDOWS",
                     help="one point of the activity x windows sweep on the same netlist instead of the default")
     args = ap.parse_args()

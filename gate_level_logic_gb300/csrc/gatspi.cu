@@ -95,6 +95,8 @@ struct gatspi_ctx {
     bool loaded = false;
     bool simulated = false;
     bool timed_last = false;   // the last simulate recorded level events
+    int32_t stall_level = -1;          // gatspi_inject_scan_stall: the level whose scan stalls in the next simulate
+    long long stall_wait_ns = 0;       // and the wait limit of that simulate
     cudaStream_t last_stream = nullptr;
 
     // TC/T1 copied to pinned host memory level by level while later levels run
@@ -137,6 +139,7 @@ struct gatspi_ctx {
         p.lpg_log2 = lpg_log2;
         p.slots_per_gate = slots_per_gate;
         p.pulse_percent = pulse_percent;
+        p.spin_limit_ns = stall_level >= 0 ? (unsigned long long)stall_wait_ns : kSpinLimitNs;
         return p;
     }
 };
@@ -306,6 +309,10 @@ gatspi_status enqueue_levels(gatspi_ctx *c, cudaStream_t s) {
     CUDA_TRY(cudaMemsetAsync(c->tile_status, 0, sizeof(unsigned long long) * std::max<long long>(c->total_tiles, 1), s),
              "clearing the scan state");
     CUDA_TRY(cudaMemsetAsync(c->tickets, 0, sizeof(int32_t) * std::max(c->L, 1), s), "clearing the tile tickets");
+    // an injected stall: the level's first ticket becomes 1 (its low byte set), so no
+    // block ever takes tile 0 and the tiles after it wait for a flag nobody sets
+    if (c->stall_level >= 0)
+        CUDA_TRY(cudaMemsetAsync(c->tickets + c->stall_level, 1, 1, s), "injecting a scan stall");
     CUDA_TRY(cudaMemsetAsync(c->status, 0, sizeof(int32_t) * kStatusWords, s), "clearing the status");
     const DevParams p = c->params();
     const bool timing = (c->flags & GATSPI_FLAG_LEVEL_TIMING) != 0;
@@ -483,7 +490,7 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(cudaMemset(c->status, 0, sizeof(int32_t) * kStatusWords), "clearing the status");
         CUDA_TRY(cudaMemset(c->tc, 0, sizeof(unsigned long long) * std::max(c->G, 1)), "clearing TC");
         CUDA_TRY(cudaMemset(c->t1, 0, sizeof(unsigned long long) * std::max(c->G, 1)), "clearing T1");
-        CUDA_TRY(set_level_smem_limit(c->W), "configuring shared memory");
+        CUDA_TRY(set_level_smem_limit(), "configuring shared memory");
         c->events.resize(2 * c->L + 1, nullptr);   // level timing can be switched on later
         for (auto &e : c->events) CUDA_TRY(cudaEventCreate(&e), "creating level events");
         if (c->G > 0) {
@@ -606,6 +613,11 @@ gatspi_status gatspi_simulate(gatspi_ctx *c, void *stream) {
     c->timed_last = (c->flags & GATSPI_FLAG_LEVEL_TIMING) != 0;
     // per-level events are recorded on the caller's stream: they cannot be read back
     // from a replayed graph, so timing runs launch the levels directly
+    if (c->stall_level >= 0) {   // an injected stall runs once, launched directly
+        const gatspi_status st = enqueue_levels(c, s);
+        c->stall_level = -1;
+        return st;
+    }
     if (c->flags & (GATSPI_FLAG_NO_GRAPH | GATSPI_FLAG_LEVEL_TIMING)) return enqueue_levels(c, s);
     if (!c->graph_exec) {
         CUDA_TRY(cudaStreamCreateWithFlags(&c->capture_stream, cudaStreamNonBlocking), "creating the capture stream");
@@ -794,6 +806,27 @@ gatspi_status gatspi_export_windows(gatspi_ctx *c, const int32_t *windows, int32
     return st;
 }
 
+gatspi_status gatspi_net_digests(gatspi_ctx *c, int64_t net_begin, int64_t num_nets, uint64_t *digest) {
+    g_err.clear();
+    if (!c || (!digest && num_nets)) return fail(GATSPI_EINVAL, "ctx and digest are required");
+    if (net_begin < 0 || num_nets < 0 || net_begin + num_nets > c->num_nets)
+        return fail(GATSPI_EINVAL, "nets [%lld, %lld) outside 0 .. %lld", (long long)net_begin,
+                    (long long)(net_begin + num_nets), c->num_nets);
+    if (!c->loaded) return fail(GATSPI_ESTATE, "load the inputs first");
+    if (net_begin + num_nets > c->P && !c->simulated) return fail(GATSPI_ESTATE, "simulate before digesting gates");
+    gatspi_status st = sync_ctx(c);
+    if (st != GATSPI_OK || num_nets == 0) return st;
+    unsigned long long *d_out = nullptr;
+    st = [&]() -> gatspi_status {
+        CUDA_TRY(dev_alloc(&d_out, (size_t)num_nets), "allocating digest scratch");
+        CUDA_TRY(launch_net_digests(c->params(), net_begin, num_nets, d_out, nullptr), "digesting waveforms");
+        CUDA_TRY(cudaMemcpy(digest, d_out, sizeof(uint64_t) * num_nets, cudaMemcpyDeviceToHost), "reading digests");
+        return GATSPI_OK;
+    }();
+    if (d_out) cudaFree(d_out);
+    return st;
+}
+
 gatspi_status gatspi_device_views(gatspi_ctx *c, gatspi_views *v) {
     g_err.clear();
     if (!c || !v) return fail(GATSPI_EINVAL, "ctx and out are required");
@@ -842,6 +875,19 @@ gatspi_status gatspi_set_level_timing(gatspi_ctx *c, int32_t on) {
         c->flags |= GATSPI_FLAG_LEVEL_TIMING;
     else
         c->flags &= ~GATSPI_FLAG_LEVEL_TIMING;
+    return GATSPI_OK;
+}
+
+gatspi_status gatspi_inject_scan_stall(gatspi_ctx *c, int32_t level, int64_t wait_ns) {
+    g_err.clear();
+    if (!c) return fail(GATSPI_EINVAL, "ctx is NULL");
+    if (level < 0 || level >= c->L) return fail(GATSPI_EINVAL, "level %d out of range", level);
+    if (c->launches[level].scan_tiles < 2)
+        return fail(GATSPI_EINVAL, "level %d has %d gates: a stall needs more than %d", level,
+                    c->launches[level].num_gates, kPlaceTile);
+    if (wait_ns < 1000 || wait_ns > 10000000000ll) return fail(GATSPI_EINVAL, "wait_ns must be 1 us .. 10 s");
+    c->stall_level = level;
+    c->stall_wait_ns = wait_ns;
     return GATSPI_OK;
 }
 

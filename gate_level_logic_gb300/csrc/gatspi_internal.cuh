@@ -32,7 +32,7 @@ constexpr int32_t kNoArc = GATSPI_NO_ARC;
 constexpr unsigned long long kFlagAgg = 1ull << 62;
 constexpr unsigned long long kFlagIncl = 2ull << 62;
 constexpr unsigned long long kValueMask = (1ull << 62) - 1;
-constexpr unsigned long long kSpinLimitNs = 2000000000ull;   // 2 s without progress -> ETIMEOUT
+constexpr unsigned long long kSpinLimitNs = 2000000000ull;   // default: 2 s without progress -> ETIMEOUT
 
 // Device status word: [0] first error code, [1..3] details (gate / net, window, extra).
 constexpr int kStatusWords = 4;
@@ -75,6 +75,7 @@ struct DevParams {
     int32_t lpg_log2;         // log2(lanes per (gate, group) segment)
     int32_t slots_per_gate;   // ngroups << lpg_log2
     int32_t pulse_percent;    // PATHPULSEPERCENT, 0 .. 100
+    unsigned long long spin_limit_ns;   // how long a look-back wait may see no progress before ETIMEOUT
 };
 
 struct LevelLaunch {
@@ -89,7 +90,7 @@ struct LevelLaunch {
 int plan_words(int W);
 size_t plan_smem_bytes(int W);
 int plan_gates_per_tile(int W);   // gates (warps) of one planning block
-cudaError_t set_level_smem_limit(int W);   // the planning kernel's shared memory, the simulation kernels' L1
+cudaError_t set_level_smem_limit();   // the planning kernel's shared memory (largest W), the simulation kernels' L1
 cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // plan + placement
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s);      // the simulation
 cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s);          // both, in order
@@ -97,6 +98,8 @@ cudaError_t launch_window_lengths(const DevParams &p, long long num_nets, const 
                                   long long *len, cudaStream_t s);
 cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,
                                  const long long *off, int32_t *words, cudaStream_t s);
+cudaError_t launch_net_digests(const DevParams &p, long long net0, long long n, unsigned long long *out,
+                               cudaStream_t s);
 cudaError_t launch_load_index(const DevParams &p, const long long *off, long long nwords, int32_t *max_time,
                               cudaStream_t s);
 

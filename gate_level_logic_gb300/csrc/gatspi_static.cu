@@ -116,6 +116,7 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     p.status = (int32_t *)(words + kStatusWord);
     p.num_inputs = a->num_inputs;
     p.pulse_percent = own_percent ? a->pulse_percent : 100;
+    p.spin_limit_ns = kSpinLimitNs;
 
     LevelLaunch l{};
     l.level = 0;
@@ -127,7 +128,7 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
 
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_level_smem_limit(p.W);
+    if (e == cudaSuccess) e = set_level_smem_limit();
     // clear the flags of the tiles this call uses, the ticket and the status
     if (e == cudaSuccess) e = cudaMemsetAsync(words, 0, sizeof(unsigned long long) * (size_t)scan, s);
     if (e == cudaSuccess)

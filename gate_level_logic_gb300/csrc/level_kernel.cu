@@ -434,7 +434,7 @@ __device__ long long look_back(const DevParams &P, const LevelLaunch &L, int til
             if (lane == 0) {
                 if (ld_status(P.status) != 0) {
                     stop = true;                                       // another warp failed: stop waiting
-                } else if (global_ns() - t0 > kSpinLimitNs) {
+                } else if (global_ns() - t0 > P.spin_limit_ns) {
                     raise_error(P.status, GATSPI_ETIMEOUT, L.level, tile, k);
                     stop = true;
                 }
@@ -811,6 +811,26 @@ __global__ void window_gather_kernel(const DevParams P, long long num_nets, cons
     for (long long i = lane; i < n; i += 32) words[off[k] + i] = src[i];
 }
 
+// Digest of every net of [net0, net0 + n): 64-bit FNV-1a, a byte at a time, over the
+// little-endian bytes of the net's waveforms in window order (each with its head and
+// EOW), one thread per net.  For comparing runs without moving their waveforms.
+__global__ void net_digest_kernel(const DevParams P, long long net0, long long n, unsigned long long *__restrict__ out) {
+    const long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= n) return;
+    const long long net = net0 + k;
+    const int32_t *base = P.pool + P.net_base[net];
+    unsigned long long h = 14695981039346656037ull;
+    for (int w = 0; w < P.W; ++w) {
+        const uint32_t s = P.wstart[net * P.W + w], e = P.wend[net * P.W + w];
+        for (uint32_t i = s; i < e; ++i) {
+            const uint32_t u = (uint32_t)base[i];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) h = (h ^ ((u >> (8 * b)) & 0xffu)) * 1099511628211ull;
+        }
+    }
+    out[k] = h;
+}
+
 }  // namespace
 
 cudaError_t launch_window_lengths(const DevParams &p, long long num_nets, const int32_t *sel, int nsel, long long *len,
@@ -827,6 +847,12 @@ cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const i
     return cudaGetLastError();
 }
 
+
+cudaError_t launch_net_digests(const DevParams &p, long long net0, long long n, unsigned long long *out,
+                               cudaStream_t s) {
+    if (n > 0) net_digest_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p, net0, n, out);
+    return cudaGetLastError();
+}
 
 int plan_gates_per_tile(int W) { return W > 4096 ? 1 : kPlanWarps; }   // one warp per block for long window lists
 
@@ -863,7 +889,7 @@ cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t 
     return e != cudaSuccess ? e : launch_level_sim(p, l, s);
 }
 
-cudaError_t set_level_smem_limit(int W) {
+cudaError_t set_level_smem_limit() {
     // The simulation kernel's pin table takes 6 KB per block (7 KB with the driver's
     // reserve): 9 blocks fit the 64 KB shared-memory configuration, which leaves the
     // rest of the SM's 256 KB to L1 for the source waveforms.  The preference is a
@@ -871,8 +897,13 @@ cudaError_t set_level_smem_limit(int W) {
     // GB300 (28 already gives 100 KB; 0 gives 8 KB and a single block per SM).
     cudaError_t e = cudaFuncSetAttribute(level_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 20);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(level_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 20);
+    // The planning kernel's dynamic shared memory limit is an attribute of the kernel,
+    // shared by every context of the process: it is always set to what the largest
+    // window count needs, so that no context lowers it below another's launches.
+    size_t most = 0;
+    for (int w = 1; w <= GATSPI_MAX_WINDOWS; ++w) most = plan_smem_bytes(w) > most ? plan_smem_bytes(w) : most;
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(level_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem_bytes(W));
+        e = cudaFuncSetAttribute(level_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
     return e;
 }
 

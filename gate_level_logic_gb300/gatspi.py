@@ -88,12 +88,14 @@ SIGNATURES = {
                                            ctypes.POINTER(ctypes.c_size_t)]),
     "gatspi_export_offsets": (ctypes.c_int, [_p, _p, _p, ctypes.c_size_t]),
     "gatspi_export_windows": (ctypes.c_int, [_p, _p, ctypes.c_int32, _p, _p, ctypes.c_size_t]),
+    "gatspi_net_digests": (ctypes.c_int, [_p, ctypes.c_int64, ctypes.c_int64, _p]),
     "gatspi_device_views": (ctypes.c_int, [_p, ctypes.POINTER(gatspi_views)]),
     "gatspi_level_times": (ctypes.c_int, [_p, _p, _p, ctypes.c_int32]),
     "gatspi_set_level_timing": (ctypes.c_int, [_p, ctypes.c_int32]),
     "gatspi_simulate_level_static": (ctypes.c_int, [ctypes.POINTER(gatspi_level_args), _p]),
     "gatspi_sdf_annotate": (ctypes.c_int, [ctypes.POINTER(gatspi_sdf_design), ctypes.c_char_p, ctypes.c_size_t, _p,
                                            _p, _p]),
+    "gatspi_inject_scan_stall": (ctypes.c_int, [_p, ctypes.c_int32, ctypes.c_int64]),
     "gatspi_destroy": (None, [_p]),
     "gatspi_last_error": (ctypes.c_char_p, []),
     "gatspi_status_name": (ctypes.c_char_p, [ctypes.c_int]),
@@ -188,6 +190,10 @@ def gatspi_export_windows(ctx: int, windows: int, nsel: int, off: int, words: in
     _check(library().gatspi_export_windows(_p(ctx), _p(windows), nsel, _p(off), _p(words), cap))
 
 
+def gatspi_net_digests(ctx: int, net_begin: int, num_nets: int, digest: int):
+    _check(library().gatspi_net_digests(_p(ctx), net_begin, num_nets, _p(digest)))
+
+
 def gatspi_device_views(ctx: int) -> gatspi_views:
     v = gatspi_views()
     _check(library().gatspi_device_views(_p(ctx), ctypes.byref(v)))
@@ -210,6 +216,10 @@ def gatspi_sdf_annotate(design: gatspi_sdf_design, text: bytes, dly_data: int, w
                         wire_fall: int = 0):
     _check(library().gatspi_sdf_annotate(ctypes.byref(design), text, len(text), _p(dly_data), _p(wire_rise),
                                          _p(wire_fall)))
+
+
+def gatspi_inject_scan_stall(ctx: int, level: int, wait_ns: int):
+    _check(library().gatspi_inject_scan_stall(_p(ctx), level, wait_ns))
 
 
 def gatspi_destroy(ctx: int):

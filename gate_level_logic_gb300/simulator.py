@@ -210,6 +210,15 @@ class Simulator:
         _c.gatspi_export_windows(self.ctx, sel.ctypes.data, sel.size, off.ctypes.data, words.ctypes.data, words.size)
         return off, words[:int(off[-1])]
 
+    def net_digests(self, net_begin: int = 0, num_nets: int = None) -> np.ndarray:
+        """uint64 [num_nets]: the 64-bit FNV-1a digest of each net's waveforms in
+        window order (gatspi_net_digests)."""
+        if num_nets is None:
+            num_nets = self.num_nets - net_begin
+        out = np.zeros(max(int(num_nets), 1), np.uint64)
+        _c.gatspi_net_digests(self.ctx, int(net_begin), int(num_nets), out.ctypes.data)
+        return out[:int(num_nets)]
+
     def views(self) -> _c.gatspi_views:
         return _c.gatspi_device_views(self.ctx)
 

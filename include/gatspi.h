@@ -324,6 +324,19 @@ gatspi_status gatspi_export_offsets(gatspi_ctx *ctx, int64_t *start, int32_t *le
 gatspi_status gatspi_export_windows(gatspi_ctx *ctx, const int32_t *windows, int32_t nsel, int64_t *off,
                                     int32_t *words, size_t cap);
 
+/*
+ * Digest of every net's waveforms, for checking a run against a reference without
+ * moving its waveforms (the page checks its results by comparing the SAIF files and
+ * spot-checking waveforms, Section 4).  digest[k] (host uint64 [num_nets]) is the
+ * 64-bit FNV-1a hash (offset basis 14695981039346656037, prime 1099511628211, one
+ * byte at a time) of the little-endian bytes of net (net_begin + k)'s waveforms
+ * concatenated in window order, each window's Fig. 3 array with its head and its
+ * GATSPI_EOW.  Inputs need a load, gates a simulate (GATSPI_ESTATE otherwise).
+ * Allocates and frees device scratch; synchronises first.  EINVAL when the range
+ * leaves 0 .. num_inputs + num_gates.
+ */
+gatspi_status gatspi_net_digests(gatspi_ctx *ctx, int64_t net_begin, int64_t num_nets, uint64_t *digest);
+
 /* Device views of the pool, window index and statistics (see gatspi_views). */
 gatspi_status gatspi_device_views(gatspi_ctx *ctx, gatspi_views *out);
 
@@ -473,6 +486,20 @@ typedef struct {
 
 gatspi_status gatspi_sdf_annotate(const gatspi_sdf_design *design, const char *text, size_t len, int32_t *dly_data,
                                   int32_t *wire_rise, int32_t *wire_fall);
+
+/*
+ * Failure injection for the bounded device waits (the page has no counterpart).  The
+ * only place a kernel waits for another block is the decoupled look-back of the
+ * output-region scan (see gatspi_simulate); every such wait gives up after a time
+ * limit with GATSPI_ETIMEOUT instead of hanging.  This call arms the next
+ * gatspi_simulate (launched directly, not from the graph) to stall the scan of
+ * `level`: its first tile is never taken, so the tiles after it wait for a flag that
+ * nothing sets, give up after wait_ns (1 us .. 10 s) and latch GATSPI_ETIMEOUT; the
+ * following kernels see the status and write nothing, and the context stays usable
+ * (the simulate after it runs normally).  The level must have more than 1024 gates
+ * (two tiles); EINVAL otherwise.
+ */
+gatspi_status gatspi_inject_scan_stall(gatspi_ctx *ctx, int32_t level, int64_t wait_ns);
 
 /* Release the context's device arrays (not the borrowed pool).  NULL is allowed. */
 void gatspi_destroy(gatspi_ctx *ctx);

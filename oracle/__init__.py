@@ -10,7 +10,11 @@ Two independent CPU simulators, both plain C compiled with gcc:
   the GATSPI page (Section 3) gate by gate in level order and window by window
   (optionally with windows spread over threads; windows are independent);
 * ``bruteforce`` -- a unit-time-step simulator of inertial wire and gate
-  elements, used to pin ``simulate`` on tiny netlists.
+  elements, used to pin ``simulate`` on tiny netlists;
+* ``digest`` -- the same Algorithm 1 run (a level-parallel driver around the same
+  per-task routine) that keeps no merged pool and returns a 64-bit FNV-1a digest of
+  every net's waveforms instead, continued over consecutive batches of windows, for
+  runs too large to compare word by word.
 
 And the testbench restructuring: ``restructure`` cuts whole-testbench input
 waveforms into the cycle windows (GATSPI page, Sections 1, 4 and 5).
@@ -84,6 +88,11 @@ def _load(path=None):
                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p),
                                            ctypes.POINTER(ctypes.c_int64), ctypes.c_char_p, ctypes.c_int]
         lib.oracle_restructure.restype = ctypes.c_int
+        lib.oracle_digest.argtypes = sig + [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_char_p, ctypes.c_int]
+        lib.oracle_digest.restype = ctypes.c_int
+        lib.oracle_fnv1a64.argtypes = [ctypes.c_uint64, ctypes.c_void_p, ctypes.c_int64]
+        lib.oracle_fnv1a64.restype = ctypes.c_uint64
         lib.oracle_free.argtypes = [ctypes.c_void_p]
         lib.oracle_free.restype = None
         _libs[path] = lib
@@ -207,3 +216,53 @@ def restructure(tb_off, tb_words, window_len, lib_path: str = None):
     finally:
         lib.oracle_free(ptr)
     return off, words
+
+
+FNV_OFFSET = 14695981039346656037
+
+
+@dataclass
+class Digest:
+    """Running digests of a run done in consecutive batches of windows."""
+    net_hash: np.ndarray    # uint64 [P+G]: FNV-1a of each net's waveforms so far, window order
+    net_words: np.ndarray   # int64 [P+G]: words hashed so far
+    tc: np.ndarray          # int64 [G]
+    t1: np.ndarray          # int64 [G]
+    window_time: int        # sum of the window lengths so far (T0 = window_time - T1)
+
+    @classmethod
+    def start(cls, num_inputs: int, num_gates: int) -> "Digest":
+        n = num_inputs + num_gates
+        return cls(net_hash=np.full(n, FNV_OFFSET, np.uint64), net_words=np.zeros(n, np.int64),
+                   tc=np.zeros(num_gates, np.int64), t1=np.zeros(num_gates, np.int64), window_time=0)
+
+
+def digest(net, stim, state: Digest = None, threads: int = 1, lib_path: str = None,
+           pulse_percent: int = 100) -> Digest:
+    """Algorithm 1 over every gate and window of ``stim`` (levels in order, a level's
+    (gate, window) tasks spread over ``threads``); continues ``state`` (a new one if
+    None) with this batch of windows, which must follow the windows already in it."""
+    lib = _load(lib_path)
+    s, keep = _marshal(net, stim)
+    if state is None:
+        state = Digest.start(net.num_inputs, net.num_gates)
+    G = net.num_gates
+    tc = np.zeros(max(G, 1), np.int64)
+    t1 = np.zeros(max(G, 1), np.int64)
+    h = np.ascontiguousarray(state.net_hash, np.uint64).copy()
+    nw = np.ascontiguousarray(state.net_words, np.int64).copy()
+    err = ctypes.create_string_buffer(512)
+    rc = lib.oracle_digest(ctypes.byref(s), int(stim.num_windows), keep["window_len"].ctypes.data,
+                           keep["pi_off"].ctypes.data, keep["pi_words"].ctypes.data, int(pulse_percent), int(threads),
+                           h.ctypes.data, nw.ctypes.data, tc.ctypes.data, t1.ctypes.data, err, 512)
+    if rc != 0:
+        raise OracleError(rc, err.value.decode(errors="replace"))
+    return Digest(net_hash=h, net_words=nw, tc=state.tc + tc[:G], t1=state.t1 + t1[:G],
+                  window_time=state.window_time + int(np.asarray(stim.window_len, np.int64).sum()))
+
+
+def fnv1a64(data: bytes, h: int = FNV_OFFSET, lib_path: str = None) -> int:
+    """The oracle's 64-bit FNV-1a over raw bytes (for pinning it on published vectors)."""
+    lib = _load(lib_path)
+    buf = ctypes.create_string_buffer(bytes(data), max(len(data), 1))
+    return int(lib.oracle_fnv1a64(ctypes.c_uint64(h), buf, len(data)))

@@ -420,3 +420,244 @@ int oracle_simulate(const oracle_netlist *nl, int32_t W, const int64_t *window_l
 }
 
 void oracle_free(void *p) { free(p); }
+
+/* ---- digests of every net's waveforms (level-parallel driver) -------------- */
+/*
+ * For checking runs too large to keep or compare word by word.  A net's digest is
+ * the 64-bit FNV-1a hash (offset basis 14695981039346656037, prime 1099511628211,
+ * one byte at a time) of the little-endian bytes of its waveforms concatenated in
+ * window order, each window's array with its head and its EOW.  The caller passes
+ * every net's running hash in and gets it back continued, so windows can be
+ * simulated in consecutive batches (windows are independent) with the digest of the
+ * whole run at the end.
+ *
+ * The driver processes the levels in order; inside a level every (gate, window) is
+ * independent, so the level's tasks, gate-major, are split into one contiguous
+ * range per thread.  Each task is simulate_task() above, unchanged.
+ */
+static uint64_t fnv1a_words(uint64_t h, const int32_t *w, int64_t n) {
+    for (int64_t k = 0; k < n; ++k) {
+        const uint32_t u = (uint32_t)w[k];
+        for (int b = 0; b < 4; ++b) {
+            h ^= (u >> (8 * b)) & 0xffu;
+            h *= 1099511628211ULL;
+        }
+    }
+    return h;
+}
+
+uint64_t oracle_fnv1a64(uint64_t h, const uint8_t *bytes, int64_t n) {
+    for (int64_t k = 0; k < n; ++k) {
+        h ^= bytes[k];
+        h *= 1099511628211ULL;
+    }
+    return h;
+}
+
+typedef struct {
+    const oracle_netlist *nl;
+    int32_t W;
+    const int64_t *window_len;
+    const int64_t *pi_off;
+    const int32_t *pi_words;
+    int32_t pulse_percent;
+    int32_t g0;               /* first gate of the level */
+    int64_t k0, k1;           /* task range [k0, k1): task k = (g0 + k / W, k % W) */
+    const int32_t **wave;     /* [G * W] output of (gate, window), once its level is done */
+    int32_t *wlen;            /* [G * W] */
+    wbuf out;                 /* this thread's outputs of this level, task order */
+    int64_t *start;           /* [k1 - k0] start of each task's output in out */
+    int64_t *tc, *t1;         /* [gates of the level] partial sums */
+    int status;
+    char msg[256];
+} lvl_worker;
+
+static void *lvl_worker_run(void *arg) {
+    lvl_worker *wk = (lvl_worker *)arg;
+    const oracle_netlist *nl = wk->nl;
+    const int32_t P = nl->num_inputs, W = wk->W;
+    wbuf O = {0, 0, 0};
+    const int32_t *Win[MAXP];
+    int32_t wr[MAXP], wf[MAXP], wt[MAXP];
+    for (int64_t k = wk->k0; k < wk->k1; ++k) {
+        const int32_t g = wk->g0 + (int32_t)(k / W), w = (int32_t)(k % W);
+        const int32_t ty = nl->gate_type[g];
+        const int n = nl->type_num_pins[ty];
+        const int32_t e0 = nl->fanin_off[g];
+        for (int i = 0; i < n; ++i) {
+            const int32_t s = nl->fanin_net[e0 + i];
+            wr[i] = nl->wire_rise[e0 + i];
+            wf[i] = nl->wire_fall[e0 + i];
+            wt[i] = nl->pin_weight[e0 + i];
+            Win[i] = s < P ? wk->pi_words + wk->pi_off[(int64_t)s * W + w] : wk->wave[(int64_t)(s - P) * W + w];
+        }
+        int64_t tc = 0, t1 = 0;
+        const int st = simulate_task(n, Win, wr, wf, wt, nl->tt_data + nl->type_tt_off[ty],
+                                     nl->dly_data + nl->gate_dly_off[g], wk->window_len[w], wk->pulse_percent, &O,
+                                     &tc, &t1);
+        if (st != ORACLE_OK) {
+            wk->status = st;
+            snprintf(wk->msg, sizeof wk->msg, "gate %d window %d: %s", g, w,
+                     st == ORACLE_EBADLUT ? "every switching arc has no delay"
+                     : st == ORACLE_EINVAL ? "timestamp reaches EOW" : "out of memory");
+            break;
+        }
+        const int64_t at = wk->out.len;
+        if (wbuf_reserve(&wk->out, at + O.len)) {
+            wk->status = ORACLE_ENOMEM;
+            snprintf(wk->msg, sizeof wk->msg, "out of memory");
+            break;
+        }
+        memcpy(wk->out.w + at, O.w, (size_t)O.len * sizeof(int32_t));
+        wk->out.len = at + O.len;
+        wk->start[k - wk->k0] = at;
+        wk->wlen[(int64_t)g * W + w] = (int32_t)O.len;
+        wk->tc[g - wk->g0] += tc;
+        wk->t1[g - wk->g0] += t1;
+    }
+    free(O.w);
+    return NULL;
+}
+
+typedef struct {
+    const int32_t *const *wave;   /* per (net, window) first word */
+    const int64_t *len;           /* per (net, window) words */
+    int32_t W;
+    int64_t n0, n1;               /* net range */
+    uint64_t *hash;               /* [nets], continued */
+    int64_t *words;               /* [nets], accumulated */
+} hash_worker;
+
+static void *hash_worker_run(void *arg) {
+    hash_worker *hw = (hash_worker *)arg;
+    for (int64_t net = hw->n0; net < hw->n1; ++net)
+        for (int32_t w = 0; w < hw->W; ++w) {
+            const int64_t k = net * hw->W + w;
+            hw->hash[net] = fnv1a_words(hw->hash[net], hw->wave[k], hw->len[k]);
+            hw->words[net] += hw->len[k];
+        }
+    return NULL;
+}
+
+/* Simulate every gate in every window and continue each net's digest (net_hash,
+ * [P + G], in/out) and word count (net_words, in/out) over this run's windows in
+ * window order; TC and T1 of every gate are added to tc[G] and t1[G]. */
+int oracle_digest(const oracle_netlist *nl, int32_t W, const int64_t *window_len, const int64_t *pi_off,
+                  const int32_t *pi_words, int32_t pulse_percent, int nthreads, uint64_t *net_hash,
+                  int64_t *net_words, int64_t *tc, int64_t *t1, char *err, int errlen) {
+    if (pulse_percent < 0 || pulse_percent > 100) {
+        snprintf(err, errlen, "PATHPULSEPERCENT must be 0 .. 100");
+        return ORACLE_EINVAL;
+    }
+    int st = validate(nl, W, pi_off, pi_words, err, errlen);
+    if (st) return st;
+    const int32_t P = nl->num_inputs, G = nl->num_gates, L = nl->num_levels;
+    if (nthreads < 1) nthreads = 1;
+    const int64_t NW = (int64_t)(P + G) * W;
+    const int32_t **wave = (const int32_t **)calloc((size_t)(NW + 1), sizeof(int32_t *));
+    int64_t *len = (int64_t *)calloc((size_t)(NW + 1), sizeof(int64_t));
+    int32_t *glen = (int32_t *)calloc((size_t)((int64_t)G * W + 1), sizeof(int32_t));
+    wbuf *bufs = (wbuf *)calloc((size_t)L * nthreads + 1, sizeof(wbuf));   /* [level][thread] */
+    lvl_worker *wk = (lvl_worker *)calloc((size_t)nthreads, sizeof(lvl_worker));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!wave || !len || !glen || !bufs || !wk || !th) {
+        st = ORACLE_ENOMEM;
+        snprintf(err, errlen, "out of memory");
+    }
+    for (int64_t k = 0; st == ORACLE_OK && k < (int64_t)P * W; ++k) {
+        wave[k] = pi_words + pi_off[k];
+        len[k] = pi_off[k + 1] - pi_off[k];
+    }
+    /* gate outputs, level by level; wave[] of a level's gates is set once it is done */
+    const int32_t **gwave = wave + (int64_t)P * W;
+    for (int32_t l = 0; st == ORACLE_OK && l < L; ++l) {
+        const int32_t g0 = nl->level_offsets[l], ng = nl->level_offsets[l + 1] - g0;
+        const int64_t ntask = (int64_t)ng * W;
+        for (int k = 0; k < nthreads; ++k) {
+            lvl_worker *x = &wk[k];
+            memset(x, 0, sizeof *x);
+            x->nl = nl;
+            x->W = W;
+            x->window_len = window_len;
+            x->pi_off = pi_off;
+            x->pi_words = pi_words;
+            x->pulse_percent = pulse_percent;
+            x->g0 = g0;
+            x->k0 = ntask * k / nthreads;
+            x->k1 = ntask * (k + 1) / nthreads;
+            x->wave = gwave;
+            x->wlen = glen;
+            x->start = (int64_t *)calloc((size_t)(x->k1 - x->k0 + 1), sizeof(int64_t));
+            x->tc = (int64_t *)calloc((size_t)ng + 1, sizeof(int64_t));
+            x->t1 = (int64_t *)calloc((size_t)ng + 1, sizeof(int64_t));
+            if (!x->start || !x->tc || !x->t1) st = ORACLE_ENOMEM;
+        }
+        if (st == ORACLE_OK) {
+            if (nthreads == 1) {
+                lvl_worker_run(&wk[0]);
+            } else {
+                for (int k = 0; k < nthreads; ++k) pthread_create(&th[k], NULL, lvl_worker_run, &wk[k]);
+                for (int k = 0; k < nthreads; ++k) pthread_join(th[k], NULL);
+            }
+            for (int k = 0; k < nthreads && st == ORACLE_OK; ++k)
+                if (wk[k].status) {
+                    st = wk[k].status;
+                    snprintf(err, errlen, "%s", wk[k].msg);
+                }
+        } else {
+            snprintf(err, errlen, "out of memory");
+        }
+        for (int k = 0; k < nthreads; ++k) {
+            lvl_worker *x = &wk[k];
+            if (st == ORACLE_OK) {
+                for (int64_t t = x->k0; t < x->k1; ++t) {
+                    const int64_t gk = (int64_t)g0 * W + t;      /* (gate, window) index */
+                    gwave[gk] = x->out.w + x->start[t - x->k0];
+                    len[(int64_t)P * W + gk] = glen[gk];
+                }
+                for (int32_t j = 0; j < ng; ++j) {
+                    tc[g0 + j] += x->tc[j];
+                    t1[g0 + j] += x->t1[j];
+                }
+            }
+            bufs[(int64_t)l * nthreads + k] = x->out;      /* kept: later levels read it */
+            free(x->start);
+            free(x->tc);
+            free(x->t1);
+        }
+    }
+    if (st == ORACLE_OK) {
+        const int64_t nets = (int64_t)P + G;
+        hash_worker *hw = (hash_worker *)calloc((size_t)nthreads, sizeof(hash_worker));
+        if (!hw) {
+            st = ORACLE_ENOMEM;
+            snprintf(err, errlen, "out of memory");
+        } else {
+            for (int k = 0; k < nthreads; ++k) {
+                hw[k].wave = wave;
+                hw[k].len = len;
+                hw[k].W = W;
+                hw[k].n0 = nets * k / nthreads;
+                hw[k].n1 = nets * (k + 1) / nthreads;
+                hw[k].hash = net_hash;
+                hw[k].words = net_words;
+            }
+            if (nthreads == 1) {
+                hash_worker_run(&hw[0]);
+            } else {
+                for (int k = 0; k < nthreads; ++k) pthread_create(&th[k], NULL, hash_worker_run, &hw[k]);
+                for (int k = 0; k < nthreads; ++k) pthread_join(th[k], NULL);
+            }
+            free(hw);
+        }
+    }
+    if (bufs)
+        for (int64_t k = 0; k < (int64_t)L * nthreads; ++k) free(bufs[k].w);
+    free(bufs);
+    free(wave);
+    free(len);
+    free(glen);
+    free(wk);
+    free(th);
+    return st;
+}

@@ -7,5 +7,5 @@ from .cells import CELL_MIX, SCAN_MIX, truth_table  # noqa: F401
 from .netlist import INF, Netlist, NetlistSpec, build_netlist, generate_netlist, possible_rows  # noqa: F401
 from .stimulus import (EOW, Stimulus, StimulusSpec, Testbench, from_waveforms, generate_stimulus,  # noqa: F401
                        generate_testbench, select_windows)
-from .workloads import WORKLOADS, make, sweep, testbench  # noqa: F401
+from .workloads import SWEEP_ACTIVITY, SWEEP_WINDOWS, WORKLOADS, make, sweep, testbench  # noqa: F401
 from .sdf import SdfText, write_sdf  # noqa: F401

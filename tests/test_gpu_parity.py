@@ -2,10 +2,9 @@
 
 Waveforms, window offsets and toggle statistics are integers: the bar is bit-exact
 equality.  Small and medium cases compare the whole pool; the 1M-gate workload (the
-configuration bench.py times) compares the whole pool too; the 5M-gate, scan-style
-and sweep workloads compare every net's waveform in sampled windows (windows are
-independent re-simulations, so the oracle can recompute any subset of them) plus
-invariants that hold at any size.
+configuration bench.py times) compares the whole pool too.  The 5M-gate, scan-style
+and sweep workloads are compared in full against stored oracle digests
+(test_gpu_digests.py).
 """
 import os
 
@@ -305,43 +304,6 @@ def test_1M_full(gpu, oracle_lib):
     net, stim = synth.make("1M")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
     assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref, "1M")
-
-
-def _sampled(gpu, oracle_lib, net, stim, windows, pool_words):
-    with gpu(net, stim.window_len, pool_words=pool_words) as sim:
-        sim.load(stim.pi_off, stim.pi_words)
-        sim.simulate()
-        tc, t0, t1 = sim.toggle_stats()
-        off, words = sim.export_windows(windows)
-        used = sim.pool_used()
-    sub = oracle_lib.simulate(net, synth.select_windows(stim, windows), threads=min(THREADS, len(windows)))
-    assert np.array_equal(off, sub.off), "offsets of the sampled windows differ"
-    assert np.array_equal(words, sub.pool), "waveforms of the sampled windows differ"
-    # properties at any size: T0 + T1 covers every window; TC at least the sampled windows' toggles
-    assert np.array_equal(t0 + t1, np.full(net.num_gates, int(stim.window_len.sum())))
-    assert (tc >= sub.tc).all() and (t1 >= sub.t1).all()
-    assert used <= pool_words
-    return tc
-
-
-@pytest.mark.slow
-def test_5M_sampled(gpu, oracle_lib):
-    net, stim = synth.make("5M")
-    _sampled(gpu, oracle_lib, net, stim, [0, 77, 127], pool_words=36 << 30)
-
-
-@pytest.mark.slow
-def test_scan500k_sampled(gpu, oracle_lib):
-    net, stim = synth.make("scan500k")
-    _sampled(gpu, oracle_lib, net, stim, [0, 131, 255], pool_words=24 << 30)
-
-
-@pytest.mark.slow
-@pytest.mark.parametrize("activity,W", [(0.01, 1), (0.20, 16), (0.50, 256), (0.05, 4096)])
-def test_1M_sweep_points_sampled(gpu, oracle_lib, activity, W):
-    net, stim = synth.sweep(activity, W)
-    windows = [0] if W == 1 else [0, W // 2 + 1, W - 1]
-    _sampled(gpu, oracle_lib, net, stim, windows, pool_words=40 << 30)
 
 
 # ---- PATHPULSEPERCENT below 100 (several pending output events; transport at 0) ----

@@ -6,8 +6,9 @@ allocate after start-up): they hand over every buffer, and the level kernel's on
 scratch sits in a fixed device array inside the library.  This test plays such a
 caller: it allocates every buffer itself (torch tensors), lays out the input
 waveforms and their window index itself, runs every logic level through the new
-entry point, and checks the result against the regular path (gatspi_simulate)
-bit for bit -- twice in a row, since every call reuses the one scratch array.
+entry point, and checks the result against the regular path (gatspi_simulate) and
+against the CPU oracle bit for bit -- twice in a row, since every call reuses the
+one scratch array.
 """
 import ctypes
 
@@ -173,7 +174,7 @@ def built():
 
 
 @pytest.mark.parametrize("name,q", [("tiny", 100), ("50k", 100), ("tiny", 30), ("w256", 100), ("w256", 60)])
-def test_static_levels_match_regular_path(built, name, q):
+def test_static_levels_match_regular_path(built, oracle_lib, name, q):
     if name == "w256":     # eight chunks per gate
         net = synth.generate_netlist(synth.NetlistSpec(num_gates=800, num_inputs=20, num_levels=5, seed=5))
         stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=20, cycles=512, period=300, activity=0.4,
@@ -182,12 +183,18 @@ def test_static_levels_match_regular_path(built, name, q):
         net, stim = synth.make(name)
     pool_words = 1 << 26            # room for the bound-sized output regions of every level
     ref = _regular(net, stim, pool_words, pulse_percent=q)
+    # the CPU oracle directly as well: every waveform in (net, window) order and the
+    # statistics, so a fault shared by both GPU paths cannot pass unseen
+    orc = oracle_lib.simulate(net, stim, threads=8, pulse_percent=q)
     caller = Caller(net, stim, pool_words, pulse_percent=q)
     for attempt in range(2):                        # two runs in a row share the scratch
         index, pool, tc, t1 = caller.run()
         assert _same_index(index, ref[0]), "waveform positions differ (run %d)" % attempt
         assert np.array_equal(_gather(pool, index), _gather(ref[1], ref[0])), "waveforms differ (run %d)" % attempt
         assert np.array_equal(tc, ref[2]) and np.array_equal(t1, ref[3]), "statistics differ (run %d)" % attempt
+        assert np.array_equal(_gather(pool, index), orc.pool), "waveforms differ from the oracle (run %d)" % attempt
+        assert np.array_equal(np.asarray(index[1], np.int64), np.diff(orc.off)), "lengths differ from the oracle"
+        assert np.array_equal(tc, orc.tc) and np.array_equal(t1, orc.t1), "statistics differ from the oracle"
 
 
 def test_sources_far_apart(built):
