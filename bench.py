@@ -18,8 +18,10 @@ Prints one JSON line (rank 0):
 
 ``--impl reference`` times the CPU oracle instead (a plain event-driven simulator,
 windows spread over the host cores), on a bounded sample per step.
-Under torchrun every rank runs its own replica of the workload (replicas only:
-the method needs no exchange between GPUs); rank 0 prints the aggregate.
+Under torchrun (N ranks, one GPU each) the windows are split over the GPUs: the
+testbench is N times longer, rank r simulates the r-th contiguous range of its
+windows (as many as one GPU does alone: weak scaling), and the per-gate TC/T1 are
+summed over the ranks once; rank 0 prints the aggregate.
 """
 from __future__ import annotations
 
@@ -85,9 +87,21 @@ def _sum_over_ranks(dist, x: float) -> float:
     return float(t.item())
 
 
-def workload_config(net, stim, pulse_percent=100, overrides=None):
-    name = ("1M-gate synthetic netlist, 40 levels, 9-cell mix with SDF-conditional arcs; "
-            "4096 inputs, 10k cycles x period 1000, 5% activity, 10% glitch pairs; 256 cycle windows")
+WORKLOAD_NAMES = {
+    "1M": ("1M-gate synthetic netlist, 40 levels, 9-cell mix with SDF-conditional arcs; "
+           "4096 inputs, 10k cycles x period 1000, 5% activity, 10% glitch pairs; 256 cycle windows"),
+    "5M": ("5M-gate synthetic netlist, 60 levels, 9-cell mix, 30% of multi-input cells with SDF-conditional "
+           "arcs; 16384 inputs, 2000 cycles x period 1000, 20% activity; 128 cycle windows"),
+    "scan500k": ("500k-gate scan-style netlist of NAND2/NOR2/XOR2, 30 levels; 4096 inputs, 100k cycles x "
+                 "period 1000, 2% activity; 256 cycle windows"),
+}
+
+
+def workload_config(net, stim, pulse_percent=100, overrides=None, workload=WORKLOAD, world=1):
+    name = WORKLOAD_NAMES[workload]
+    if world > 1:
+        name += ("; the testbench %dx longer, its windows split into %d contiguous ranges, one per GPU"
+                 % (world, world))
     extra = {}
     if overrides:
         name = "not the default workload: " + name + ", with the overrides listed"
@@ -97,19 +111,21 @@ def workload_config(net, stim, pulse_percent=100, overrides=None):
         "gates": int(net.num_gates), "levels": int(net.num_levels), "inputs": int(net.num_inputs),
         "edges": int(net.num_edges), "windows": int(stim.num_windows), "cycles": int(stim.window_cycles.sum()),
         "pulse_percent": pulse_percent,
+        "parallelism": ("windows split over %d GPUs (one contiguous range each, one int64 sum of TC/T1 "
+                        "at the end)" % world) if world > 1 else "one GPU",
         "l2": "inputs larger than L2 (waveform pool of several GB per step, no flush needed)",
         **extra,
     }
 
 
-def algorithmic_bytes(net, lengths, W):
+def algorithmic_bytes(net, net_words, W):
     """Algorithmic bytes of one run (every level): each consumed (net, window) waveform
     read once, each output written once, 8 B of window index per consumed (net,
     window) and per (gate, window), and the gate descriptors once (16 B per gate and
-    per fanin edge).  Returns (total, parts)."""
+    per fanin edge).  ``net_words``: words of every net over all its windows.
+    Returns (total, parts)."""
     P, G = net.num_inputs, net.num_gates
-    lens = np.asarray(lengths, np.int64).reshape(P + G, W)
-    net_words = lens.sum(axis=1)
+    net_words = np.asarray(net_words, np.int64)
     consumed = np.unique(net.fanin_net)
     parts = {
         "read_waveforms": 4 * int(net_words[consumed].sum()),
@@ -120,13 +136,12 @@ def algorithmic_bytes(net, lengths, W):
     return sum(parts.values()), parts
 
 
-def demand_bytes(net, lengths, W):
+def demand_bytes(net, net_words, W):
     """Per level: the waveforms of every distinct source net of the level read (a net
     consumed by several levels counts in each), the level's outputs written, their
     window index read and written, and the level's gate descriptors."""
     P = net.num_inputs
-    lens = np.asarray(lengths, np.int64).reshape(-1, W)
-    net_words = lens.sum(axis=1)
+    net_words = np.asarray(net_words, np.int64)
     lo = net.level_offsets
     out = []
     for lvl in range(net.num_levels):
@@ -265,7 +280,8 @@ def run_reference(args):
     import synth
     import oracle
     oracle.build()
-    net, stim = synth.make(WORKLOAD)
+    workload = getattr(args, "workload", WORKLOAD)
+    net, stim = synth.make(workload)
     cores = os.cpu_count() or 1
     W = stim.num_windows
     n = min(W, 2 * cores)
@@ -286,7 +302,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": workload_config(net, stim, args.pulse_percent),
+        "config": workload_config(net, stim, args.pulse_percent, workload=workload),
         "gate_cycles_per_s": net.num_gates * cycles * args.steps / total,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, n), "kind": "oracle",
                          "sample": "%d of %d windows per step (all gates)" % (n, W)},
@@ -299,8 +315,10 @@ def run_reference(args):
 def _e2e(args, sim, inputs, net, stream, dist, events_per_step, testbench):
     """Same metric through the public API with host buffers: every step copies the
     inputs in (and, with ``testbench``, cuts the whole-testbench waveforms into windows
-    on the GPU), simulates and reads the statistics back."""
+    on the GPU), simulates and reads the statistics back; with several ranks, each
+    rank's statistics are then summed over the ranks (the run's one collective)."""
     import torch
+    from gate_level_logic_gb300 import shard
     pin_off = torch.from_numpy(np.ascontiguousarray(inputs[0], np.int64)).pin_memory()
     pin_words = torch.from_numpy(np.ascontiguousarray(inputs[1], np.int32)).pin_memory()
     load = sim.load_testbench if testbench else sim.load
@@ -312,9 +330,12 @@ def _e2e(args, sim, inputs, net, stream, dist, events_per_step, testbench):
         load(pin_off, pin_words, stream=stream)
         sim.simulate(stream=stream)
         tc_e, t1_e, _ = sim.toggle_stats_view()   # the statistics in host memory, no extra copy
+        if dist is not None:
+            local = int(tc_e.sum())
+            tc_e, t1_e = shard.sum_stats(dist, tc_e.astype(np.int64), t1_e.astype(np.int64))
     torch.cuda.synchronize()
     e2e_s = _max_over_ranks(dist, time.perf_counter() - t)
-    assert int(tc_e.sum()) == events_per_step
+    assert (local if dist is not None else int(tc_e.sum())) == events_per_step
     e2e_value = _sum_over_ranks(dist, events_per_step * e2e_steps) / e2e_s
     h2d = pin_off.numel() * 8 + pin_words.numel() * 4
     d2h = 2 * 8 * net.num_gates + 16       # TC and T1 per gate, status word
@@ -380,7 +401,7 @@ def run_gpu(args):
     import torch
 
     import synth
-    from gate_level_logic_gb300 import Simulator, build, gatspi
+    from gate_level_logic_gb300 import build, shard
 
     rank, world, local = _dist()
     dist = _init_pg(world)
@@ -393,35 +414,46 @@ def run_gpu(args):
         over["cycles"] = args.cycles
     if args.gates:
         over["net_num_gates"] = args.gates
+    workload = args.workload
     if args.sweep:
         activity, windows = args.sweep.split(":")
         net, stim = synth.sweep(float(activity), int(windows))
         over = {"sweep_point": {"activity": float(activity), "windows": int(windows), "stimulus_seed": 4,
                                 "glitch_pairs": 0.0}}
     else:
-        net, stim = synth.make(WORKLOAD, **over)
-    W = stim.num_windows
+        kw = dict(over)
+        if world > 1:
+            # weak scaling: every rank simulates as many windows as one GPU does alone,
+            # its own contiguous range of one testbench that many times longer
+            _, stim_kw = synth.WORKLOADS[workload]
+            kw["cycles"] = world * int(kw.get("cycles", stim_kw["cycles"]))
+            kw["windows"] = world * int(kw.get("windows", stim_kw["windows"]))
+        net, stim = synth.make(workload, **kw)
     flags = 0
-    pool_words = int(args.pool_gb * (1 << 30) / 4)
-    sim = Simulator(net, stim.window_len, pool_words=pool_words, flags=flags,
-                    pulse_percent=args.pulse_percent)
+    pool_gb = args.pool_gb if args.pool_gb > 0 else {"1M": 48.0, "5M": 170.0, "scan500k": 64.0}[workload]
+    pool_words = int(pool_gb * (1 << 30) / 4)
+    part = shard.WindowShard(net, stim.window_len, world, rank, pool_words=pool_words, flags=flags,
+                             pulse_percent=args.pulse_percent)
+    sim = part.sim
     stream = torch.cuda.current_stream()
-    sim.load(stim.pi_off, stim.pi_words, stream=stream)
+    part.load(stim.pi_off, stim.pi_words, stream=stream)
+    rank_off, rank_words = shard.slice_windows(stim.pi_off, stim.pi_words, net.num_inputs, stim.num_windows,
+                                               part.w0, part.w1)
+    W = part.w1 - part.w0                           # this rank's windows
 
     for _ in range(max(args.warmup, 1)):
         sim.simulate(stream=stream)
     tc, t0, t1 = sim.toggle_stats()
-    events_per_step = int(tc.sum())
-    _, lengths = sim.export_offsets()
-    run_bytes, run_parts = algorithmic_bytes(net, lengths, W)
-    lvl_demand = demand_bytes(net, lengths, W)
-    waveform_words = int(lengths.sum())
+    events_per_step = int(tc.sum())                 # this rank's
+    _, net_words = sim.net_digests(with_words=True)
+    run_bytes, run_parts = algorithmic_bytes(net, net_words, W)
+    lvl_demand = demand_bytes(net, net_words, W)
+    waveform_words = int(net_words.sum())
     if args.dump_levels and rank == 0:
         with open(args.dump_levels, "w") as f:
             json.dump({"demand_bytes": lvl_demand.tolist(), "algorithmic_bytes_per_run": run_bytes,
                        "algorithmic_parts": run_parts}, f)
     pool_used = sim.pool_used()
-    del lengths
 
     # ---- timed region: device time, inputs resident ----------------------------
     # The step as a user runs it: the captured level graph, each kernel starting in
@@ -480,10 +512,13 @@ def run_gpu(args):
     traffic, traffic_ratio = _traffic(float(lvl_demand.mean()))
 
     # ---- end to end through the C ABI: host buffers, copies inside the region ---
-    if args.no_e2e or args.sweep:      # the end-to-end legs run on the default workload only
+    if args.no_e2e or args.sweep:      # no end-to-end legs on sweep points
         e2e_value, h2d, d2h, e2e_win, cut = None, 0, 0, None, None
+    elif world > 1:                    # each rank copies its own windows in
+        e2e_win = _e2e(args, sim, (rank_off, rank_words), net, stream, dist, events_per_step, False)
+        e2e_value, h2d, d2h, cut = e2e_win[0], e2e_win[1], e2e_win[2], None
     else:
-        tb = synth.testbench(WORKLOAD, **over)
+        tb = synth.testbench(workload, **over)
         e2e_value, h2d, d2h = _e2e(args, sim, (tb.off, tb.words), net, stream, dist, events_per_step, True)
         e2e_win = _e2e(args, sim, (stim.pi_off, stim.pi_words), net, stream, dist, events_per_step, False)
         cut = _testbench_cut(args, sim, tb, stream, rank == 0 and not args.no_cpu_baseline)
@@ -492,7 +527,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": workload_config(net, stim, args.pulse_percent, over),
+        "config": workload_config(net, stim, args.pulse_percent, over, workload, world),
         "gate_cycles_per_s": gate_cycles_per_s,
         "events_per_step": events_per_step,
         "pool_words_used": pool_used,
@@ -514,20 +549,26 @@ def run_gpu(args):
             "serialised_step_ms": float(np.mean(serial_ms)),
             "bounds_kernel_avg_ms": float(bounds_ms.sum() / (args.steps * net.num_levels)),
         },
-        "e2e": None if e2e_value is None else {
+        "e2e": None if e2e_value is None else ({
+            "value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "path": "gatspi_load_waveforms (each rank's windows from pinned host memory) + gatspi_simulate + "
+                    "gatspi_toggle_stats_host + one int64 all-reduce of TC/T1 over the ranks"} if world > 1 else {
             "value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "path": "gatspi_load_testbench (whole-testbench waveforms from pinned host memory, cut into windows "
                     "on the GPU) + gatspi_simulate + gatspi_toggle_stats_host",
             "windowed_inputs": {"value": e2e_win[0], "h2d_bytes_per_step": int(e2e_win[1]),
-                                "path": "gatspi_load_waveforms (host-cut windows) + simulate + toggle_stats_host"}},
+                                "path": "gatspi_load_waveforms (host-cut windows) + simulate + toggle_stats_host"}}),
         "testbench_cut": cut,
         "gpu_launches": int(args.steps * launches_per_step),   # planning (non-empty levels), placement, simulation
         "clocks": clocks.summary(),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if world > 1:                      # the run's result: the statistics summed over the ranks
+        tc_all, _ = shard.sum_stats(dist, tc, t1)
+        line["events_all_ranks_per_step"] = int(tc_all.sum())
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sim.close()
         line["cpu_baseline"] = cpu_baseline(net, stim, pulse_percent=args.pulse_percent)
-    if rank == 0 and not args.no_e2e:
+    if rank == 0 and world == 1 and not args.no_e2e:
         line["sdf_translate"] = _sdf_translate(not args.no_cpu_baseline)
     if rank == 0:
         print(json.dumps(line))
@@ -545,7 +586,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--pulse-percent", type=int, default=100,
                     help="PATHPULSEPERCENT of both inertial filters (100 = the page's setting, 0 = transport)")
-    ap.add_argument("--pool-gb", type=float, default=48.0)
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOAD_NAMES),
+                    help="the workload timed (the 1M-gate configuration by default)")
+    ap.add_argument("--pool-gb", type=float, default=0.0, help="waveform pool (0: sized for the workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--windows", type=int, default=0, help="profiling only: number of cycle windows")

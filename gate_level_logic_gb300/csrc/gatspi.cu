@@ -67,6 +67,7 @@ struct gatspi_ctx {
     // device arrays owned by the context
     int4 *gate_desc = nullptr;
     int32_t *dly = nullptr;
+    int32_t *gate_order = nullptr;   // W < 32: every level's gates by pin count
     long long *net_base = nullptr;
     uint32_t *wstart = nullptr;
     uint32_t *wend = nullptr;
@@ -115,6 +116,7 @@ struct gatspi_ctx {
         DevParams p{};
         p.gate_desc = gate_desc;
         p.dly_data = dly;
+        p.gate_order = gate_order;
         p.pool = pool;
         p.pool_words = pool_words;
         p.net_base = net_base;
@@ -255,7 +257,7 @@ void free_all(gatspi_ctx *c) {
     if (c->dump_stream) cudaStreamDestroy(c->dump_stream);
     if (c->tc_host) cudaFreeHost(c->tc_host);
     if (c->t1_host) cudaFreeHost(c->t1_host);
-    void *ptrs[] = {c->gate_desc, c->dly, c->net_base, c->wstart, c->wend, c->wlen8, c->perm, c->goff,
+    void *ptrs[] = {c->gate_desc, c->dly, c->gate_order, c->net_base, c->wstart, c->wend, c->wlen8, c->perm, c->goff,
                     c->window_len, c->tc, c->t1,
                     c->tile_status, c->tickets, c->level_base, c->status, c->load_off, c->max_time,
                     c->win_start, c->tc_in, c->t1_in};
@@ -447,6 +449,19 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
 
         const long long dly_len = c->G > 0 ? nl->dly_len : 0;
         CUDA_TRY(dev_alloc(&c->gate_desc, gd.size()), "allocating gate descriptors");
+        if (c->lpg_log2 < 5 && c->G > 0) {
+            // several gates share a warp: take every level's gates by pin count (stable)
+            std::vector<int32_t> order((size_t)c->G);
+            for (int l = 0; l < c->L; ++l) {
+                size_t k = (size_t)c->level_offsets[l];
+                for (int n = 1; n <= GATSPI_MAX_PINS; ++n)
+                    for (int32_t g = c->level_offsets[l]; g < c->level_offsets[l + 1]; ++g)
+                        if (nl->type_num_pins[nl->gate_type[g]] == n) order[k++] = g;
+            }
+            CUDA_TRY(dev_alloc(&c->gate_order, order.size()), "allocating the gate order");
+            CUDA_TRY(cudaMemcpy(c->gate_order, order.data(), order.size() * sizeof(int32_t), cudaMemcpyHostToDevice),
+                     "uploading the gate order");
+        }
         CUDA_TRY(dev_alloc(&c->dly, (size_t)dly_len), "allocating delay tables");
         CUDA_TRY(dev_alloc(&c->net_base, (size_t)std::max<long long>(c->num_nets, 1)), "allocating the window index");
         CUDA_TRY(dev_alloc(&c->wstart, (size_t)(c->num_nets * c->W)), "allocating the window index");
@@ -806,7 +821,8 @@ gatspi_status gatspi_export_windows(gatspi_ctx *c, const int32_t *windows, int32
     return st;
 }
 
-gatspi_status gatspi_net_digests(gatspi_ctx *c, int64_t net_begin, int64_t num_nets, uint64_t *digest) {
+gatspi_status gatspi_net_digests(gatspi_ctx *c, int64_t net_begin, int64_t num_nets, uint64_t *digest,
+                                 int64_t *words) {
     g_err.clear();
     if (!c || (!digest && num_nets)) return fail(GATSPI_EINVAL, "ctx and digest are required");
     if (net_begin < 0 || num_nets < 0 || net_begin + num_nets > c->num_nets)
@@ -817,13 +833,18 @@ gatspi_status gatspi_net_digests(gatspi_ctx *c, int64_t net_begin, int64_t num_n
     gatspi_status st = sync_ctx(c);
     if (st != GATSPI_OK || num_nets == 0) return st;
     unsigned long long *d_out = nullptr;
+    long long *d_words = nullptr;
     st = [&]() -> gatspi_status {
         CUDA_TRY(dev_alloc(&d_out, (size_t)num_nets), "allocating digest scratch");
-        CUDA_TRY(launch_net_digests(c->params(), net_begin, num_nets, d_out, nullptr), "digesting waveforms");
+        CUDA_TRY(dev_alloc(&d_words, (size_t)num_nets), "allocating digest scratch");
+        CUDA_TRY(launch_net_digests(c->params(), net_begin, num_nets, d_out, d_words, nullptr), "digesting waveforms");
         CUDA_TRY(cudaMemcpy(digest, d_out, sizeof(uint64_t) * num_nets, cudaMemcpyDeviceToHost), "reading digests");
+        if (words)
+            CUDA_TRY(cudaMemcpy(words, d_words, sizeof(int64_t) * num_nets, cudaMemcpyDeviceToHost), "reading counts");
         return GATSPI_OK;
     }();
     if (d_out) cudaFree(d_out);
+    if (d_words) cudaFree(d_words);
     return st;
 }
 

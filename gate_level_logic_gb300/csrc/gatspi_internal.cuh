@@ -44,6 +44,8 @@ struct DevParams {
                                //     {source net of pin 0..3}, {wire rise | fall << 16 of pin 0..3};
                                //     truth-table bit k = output for pin values k (first pin most significant)
     const int32_t *dly_data;   // per-instance conditional delay tables
+    const int32_t *gate_order; // [G] or null: with W < 32 (several gates per warp) the gates of every
+                               //     level in the order the simulation kernel takes them, by pin count
     // waveform store: waveform (net, w) is pool[net_base[net] + wstart[k] .. net_base[net] + wend[k]),
     // k = net * W + w, EOW included
     int32_t *pool;
@@ -99,7 +101,7 @@ cudaError_t launch_window_lengths(const DevParams &p, long long num_nets, const 
 cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,
                                  const long long *off, int32_t *words, cudaStream_t s);
 cudaError_t launch_net_digests(const DevParams &p, long long net0, long long n, unsigned long long *out,
-                               cudaStream_t s);
+                               long long *words, cudaStream_t s);
 cudaError_t launch_load_index(const DevParams &p, const long long *off, long long nwords, int32_t *max_time,
                               cudaStream_t s);
 

@@ -596,7 +596,6 @@ __global__ void __launch_bounds__(kPlanWarps * 32, kPlanMinBlocks) level_plan_ke
 // values are ready when this kernel starts, so the waits are short and few.
 __global__ void __launch_bounds__(kPlaceTile) level_place_kernel(const DevParams P, const LevelLaunch L) {
     __shared__ long long warp_sum[kPlaceTile / 32];
-    __shared__ long long tile_base;
     __shared__ int tile_id, stop;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -665,8 +664,11 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
         if (c >= P.ngroups) { ++gl; c -= P.ngroups; }
         j = lane;
     } else {
+        // several gates per warp: the level's gates are taken by pin count, so that the
+        // gates sharing a warp run the same code
         const int slot = tile * 32 + lane;
         gl = slot >> P.lpg_log2;
+        if (P.gate_order && gl < L.num_gates) gl = __ldg(P.gate_order + L.gate_begin + gl) - L.gate_begin;
         c = 0;
         j = slot & ((1 << P.lpg_log2) - 1);
     }
@@ -814,14 +816,17 @@ __global__ void window_gather_kernel(const DevParams P, long long num_nets, cons
 // Digest of every net of [net0, net0 + n): 64-bit FNV-1a, a byte at a time, over the
 // little-endian bytes of the net's waveforms in window order (each with its head and
 // EOW), one thread per net.  For comparing runs without moving their waveforms.
-__global__ void net_digest_kernel(const DevParams P, long long net0, long long n, unsigned long long *__restrict__ out) {
+__global__ void net_digest_kernel(const DevParams P, long long net0, long long n, unsigned long long *__restrict__ out,
+                                  long long *__restrict__ words) {
     const long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (k >= n) return;
     const long long net = net0 + k;
     const int32_t *base = P.pool + P.net_base[net];
     unsigned long long h = 14695981039346656037ull;
+    long long count = 0;
     for (int w = 0; w < P.W; ++w) {
         const uint32_t s = P.wstart[net * P.W + w], e = P.wend[net * P.W + w];
+        count += e - s;
         for (uint32_t i = s; i < e; ++i) {
             const uint32_t u = (uint32_t)base[i];
 #pragma unroll
@@ -829,6 +834,7 @@ __global__ void net_digest_kernel(const DevParams P, long long net0, long long n
         }
     }
     out[k] = h;
+    words[k] = count;
 }
 
 }  // namespace
@@ -849,8 +855,8 @@ cudaError_t launch_window_gather(const DevParams &p, long long num_nets, const i
 
 
 cudaError_t launch_net_digests(const DevParams &p, long long net0, long long n, unsigned long long *out,
-                               cudaStream_t s) {
-    if (n > 0) net_digest_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p, net0, n, out);
+                               long long *words, cudaStream_t s) {
+    if (n > 0) net_digest_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p, net0, n, out, words);
     return cudaGetLastError();
 }
 

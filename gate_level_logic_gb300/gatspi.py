@@ -88,7 +88,7 @@ SIGNATURES = {
                                            ctypes.POINTER(ctypes.c_size_t)]),
     "gatspi_export_offsets": (ctypes.c_int, [_p, _p, _p, ctypes.c_size_t]),
     "gatspi_export_windows": (ctypes.c_int, [_p, _p, ctypes.c_int32, _p, _p, ctypes.c_size_t]),
-    "gatspi_net_digests": (ctypes.c_int, [_p, ctypes.c_int64, ctypes.c_int64, _p]),
+    "gatspi_net_digests": (ctypes.c_int, [_p, ctypes.c_int64, ctypes.c_int64, _p, _p]),
     "gatspi_device_views": (ctypes.c_int, [_p, ctypes.POINTER(gatspi_views)]),
     "gatspi_level_times": (ctypes.c_int, [_p, _p, _p, ctypes.c_int32]),
     "gatspi_set_level_timing": (ctypes.c_int, [_p, ctypes.c_int32]),
@@ -190,8 +190,8 @@ def gatspi_export_windows(ctx: int, windows: int, nsel: int, off: int, words: in
     _check(library().gatspi_export_windows(_p(ctx), _p(windows), nsel, _p(off), _p(words), cap))
 
 
-def gatspi_net_digests(ctx: int, net_begin: int, num_nets: int, digest: int):
-    _check(library().gatspi_net_digests(_p(ctx), net_begin, num_nets, _p(digest)))
+def gatspi_net_digests(ctx: int, net_begin: int, num_nets: int, digest: int, words: int = 0):
+    _check(library().gatspi_net_digests(_p(ctx), net_begin, num_nets, _p(digest), _p(words)))
 
 
 def gatspi_device_views(ctx: int) -> gatspi_views:

@@ -210,14 +210,17 @@ class Simulator:
         _c.gatspi_export_windows(self.ctx, sel.ctypes.data, sel.size, off.ctypes.data, words.ctypes.data, words.size)
         return off, words[:int(off[-1])]
 
-    def net_digests(self, net_begin: int = 0, num_nets: int = None) -> np.ndarray:
+    def net_digests(self, net_begin: int = 0, num_nets: int = None, with_words: bool = False):
         """uint64 [num_nets]: the 64-bit FNV-1a digest of each net's waveforms in
-        window order (gatspi_net_digests)."""
+        window order (gatspi_net_digests); with ``with_words`` also the int64 number
+        of words of each net."""
         if num_nets is None:
             num_nets = self.num_nets - net_begin
-        out = np.zeros(max(int(num_nets), 1), np.uint64)
-        _c.gatspi_net_digests(self.ctx, int(net_begin), int(num_nets), out.ctypes.data)
-        return out[:int(num_nets)]
+        n = int(num_nets)
+        out = np.zeros(max(n, 1), np.uint64)
+        words = np.zeros(max(n, 1), np.int64)
+        _c.gatspi_net_digests(self.ctx, int(net_begin), n, out.ctypes.data, words.ctypes.data)
+        return (out[:n], words[:n]) if with_words else out[:n]
 
     def views(self) -> _c.gatspi_views:
         return _c.gatspi_device_views(self.ctx)

@@ -157,9 +157,9 @@ typedef struct gatspi_ctx gatspi_ctx;
  *
  * The pool holds first the input waveforms as loaded, then the gates' outputs level
  * by level; every net has one region.  A gate's region is sized by upper bounds of
- * its windows' outputs (see gatspi_simulate); its windows are stored in groups of 32
- * ranks (windows ordered by bound, largest first), each group packed from the start
- * of its share, so gaps may follow a group.  Waveform k = (net, w), k = net * W + w,
+ * its windows' outputs (see gatspi_simulate); its windows are stored in rank order
+ * (windows ordered by bound, largest first), each in a slot as long as its bound, so
+ * a gap may follow every window.  Waveform k = (net, w), k = net * W + w,
  * is pool[net_base[net] + wstart[k] .. net_base[net] + wend[k]) (EOW included).  The
  * layout depends only on the inputs: every run gives the same pool.
  */
@@ -254,7 +254,11 @@ gatspi_status gatspi_simulate(gatspi_ctx *ctx, void *stream);
  * the stream has finished and gatspi_toggle_stats reads no device memory.
  */
 
-/* Wait for the last simulate / load and report a latched device error. */
+/*
+ * Wait for the last simulate / load and report a latched device error.  The page's
+ * host waits for the level loop before dumping the statistics (Section 3, Fig. 5);
+ * this is that wait, plus the report of the device status word.
+ */
 gatspi_status gatspi_sync(gatspi_ctx *ctx);
 
 /*
@@ -296,7 +300,8 @@ gatspi_status gatspi_write_saif(gatspi_ctx *ctx, const char *path, const char *d
                                 const char *const *net_names);
 
 /*
- * Copy one (net, window) waveform to host memory.  *len receives its length in
+ * Copy one (net, window) waveform to host memory (the page spot-checks waveforms
+ * against a reference simulator's, Section 4).  *len receives its length in
  * words (EOW included) even when it exceeds cap, in which case nothing is copied
  * and EINVAL is returned.  Synchronises first.
  */
@@ -305,7 +310,8 @@ gatspi_status gatspi_get_waveform(gatspi_ctx *ctx, int32_t net, int32_t window, 
 
 /*
  * Write the pool position and length (EOW included) of every (net, window)
- * waveform, net-major and window-minor, to host memory: waveform k = net * W + w
+ * waveform, net-major and window-minor, to host memory (the offsets into the Fig. 5
+ * waveform pool that the page's scan produces): waveform k = net * W + w
  * occupies pool[start[k] .. start[k] + len[k]) (n = num_nets * W entries; either
  * array may be NULL).  Synchronises first.
  */
@@ -317,8 +323,9 @@ gatspi_status gatspi_export_offsets(gatspi_ctx *ctx, int64_t *start, int32_t *le
  *   off      host int64 [num_nets * nsel + 1]: waveform (net, windows[s]) occupies
  *            words[off[net * nsel + s] .. off[net * nsel + s + 1])
  *   words    host int32 [cap], or NULL to query the size (off is still filled)
- * Windows are independent re-simulations, so this is the natural unit to check or
- * dump a slice of a large run.  Allocates and frees device scratch; synchronises.
+ * Windows are independent re-simulations (cycle parallelism, Sections 1 and 4), so
+ * this is the natural unit to check or dump a slice of a large run.  Allocates and
+ * frees device scratch; synchronises.
  * EINVAL if cap < off[num_nets * nsel] (off is filled either way).
  */
 gatspi_status gatspi_export_windows(gatspi_ctx *ctx, const int32_t *windows, int32_t nsel, int64_t *off,
@@ -331,13 +338,16 @@ gatspi_status gatspi_export_windows(gatspi_ctx *ctx, const int32_t *windows, int
  * 64-bit FNV-1a hash (offset basis 14695981039346656037, prime 1099511628211, one
  * byte at a time) of the little-endian bytes of net (net_begin + k)'s waveforms
  * concatenated in window order, each window's Fig. 3 array with its head and its
- * GATSPI_EOW.  Inputs need a load, gates a simulate (GATSPI_ESTATE otherwise).
- * Allocates and frees device scratch; synchronises first.  EINVAL when the range
- * leaves 0 .. num_inputs + num_gates.
+ * GATSPI_EOW; words[k] (host int64 [num_nets], or NULL) the number of words hashed.
+ * Inputs need a load, gates a simulate (GATSPI_ESTATE otherwise).  Allocates and
+ * frees device scratch; synchronises first.  EINVAL when the range leaves
+ * 0 .. num_inputs + num_gates.
  */
-gatspi_status gatspi_net_digests(gatspi_ctx *ctx, int64_t net_begin, int64_t num_nets, uint64_t *digest);
+gatspi_status gatspi_net_digests(gatspi_ctx *ctx, int64_t net_begin, int64_t num_nets, uint64_t *digest,
+                                 int64_t *words);
 
-/* Device views of the pool, window index and statistics (see gatspi_views). */
+/* Device views of the pool, window index and statistics (see gatspi_views): the
+ * Fig. 5 pool and offsets for callers that keep working on the device. */
 gatspi_status gatspi_device_views(gatspi_ctx *ctx, gatspi_views *out);
 
 /*
@@ -501,13 +511,15 @@ gatspi_status gatspi_sdf_annotate(const gatspi_sdf_design *design, const char *t
  */
 gatspi_status gatspi_inject_scan_stall(gatspi_ctx *ctx, int32_t level, int64_t wait_ns);
 
-/* Release the context's device arrays (not the borrowed pool).  NULL is allowed. */
+/* Release the context's device arrays (not the borrowed pool).  NULL is allowed.
+ * The page has no counterpart (a library lifetime call). */
 void gatspi_destroy(gatspi_ctx *ctx);
 
-/* Message about the calling thread's last failed call ("" if none). */
+/* Message about the calling thread's last failed call ("" if none).  The page has
+ * no counterpart (error reporting of this ABI). */
 const char *gatspi_last_error(void);
 
-/* Name of a status code. */
+/* Name of a status code.  The page has no counterpart. */
 const char *gatspi_status_name(gatspi_status s);
 
 #ifdef __cplusplus

@@ -42,7 +42,11 @@ def gpu():
 
 def _pool_for_device(net, W):
     """Pool words: the free device memory less the context's own arrays and a margin."""
+    import gc
+
     import torch
+    gc.collect()
+    torch.cuda.empty_cache()          # the previous workload's pool back to the driver
     free, _ = torch.cuda.mem_get_info()
     nets = net.num_inputs + net.num_gates
     widest = int(np.diff(net.level_offsets).max())
@@ -65,12 +69,13 @@ def test_net_digests_match_exports_and_oracle(gpu, oracle_lib):
             sim.load(stim.pi_off, stim.pi_words)
             inputs_only = sim.net_digests(0, net.num_inputs)
             sim.simulate()
-            got = sim.net_digests()
+            got, counts = sim.net_digests(with_words=True)
             off, words = sim.export_all()
             part = sim.net_digests(net.num_inputs + 7, 5)
         expect = digests.net_digests(ref.off, ref.pool, net.num_nets, W)
         assert np.array_equal(digests.net_digests(off, words, net.num_nets, W), expect)
         assert np.array_equal(got, expect)
+        assert np.array_equal(counts, np.diff(ref.off).reshape(net.num_nets, W).sum(axis=1))
         assert np.array_equal(inputs_only, expect[:net.num_inputs])
         assert np.array_equal(part, expect[net.num_inputs + 7:net.num_inputs + 12])
         d = oracle_lib.digest(net, stim, threads=THREADS)
@@ -114,10 +119,7 @@ def test_full_size_against_oracle_digests(gpu, name):
         sim.load(stim.pi_off, stim.pi_words)
         sim.simulate()
         tc, t0, t1 = sim.toggle_stats()
-        h = sim.net_digests()
-        _, lens = sim.export_offsets()
-    words = lens.reshape(net.num_nets, W).sum(axis=1, dtype=np.int64)
-    del lens
+        h, words = sim.net_digests(with_words=True)
     assert np.array_equal(t0 + t1, np.full(net.num_gates, rec["window_time"]))
     assert digests.input_record(net.num_inputs, h, words) == rec["inputs"]
     got = digests.level_records(net.level_offsets, net.num_inputs, h, words, tc, t1)
@@ -131,12 +133,17 @@ def test_stalled_scan_times_out_and_context_recovers(gpu, oracle_lib):
     for a flag nothing sets) gives up after the limit with GATSPI_ETIMEOUT instead of
     hanging; the next simulate of the same context is exact."""
     from gate_level_logic_gb300 import GatspiError, gatspi
+    tiny, tstim = synth.make("tiny")      # 50 gates per level: a single scan tile, nothing to stall
+    with gpu(tiny, tstim.window_len, pool_words=1 << 16) as sim:
+        with pytest.raises(GatspiError) as e:
+            gatspi.gatspi_inject_scan_stall(sim.ctx, 1, 10_000)
+        assert e.value.name == "GATSPI_EINVAL"
     net, stim = synth.make("50k")         # 2500 gates per level: three scan tiles
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
     with gpu(net, stim.window_len, pool_words=4 * ref.pool.size + 4096) as sim:
         sim.load(stim.pi_off, stim.pi_words)
         with pytest.raises(GatspiError) as e:
-            gatspi.gatspi_inject_scan_stall(sim.ctx, 0, 10_000)   # 500 gates: a single tile
+            gatspi.gatspi_inject_scan_stall(sim.ctx, net.num_levels, 10_000)
         assert e.value.name == "GATSPI_EINVAL"
         for level in (3, 0):
             gatspi.gatspi_inject_scan_stall(sim.ctx, level, 20_000_000)   # 20 ms
