@@ -273,7 +273,7 @@ gatspi_status read_status(gatspi_ctx *c) {
         case GATSPI_EPOOL_OVERFLOW:
             return fail(GATSPI_EPOOL_OVERFLOW, "waveform pool too small (%lld words) at level %d", c->pool_words, st[1]);
         case GATSPI_EBADWAVE:
-            return fail(GATSPI_EBADWAVE, "malformed waveform while simulating %d, window %d", st[1], st[2]);
+            return fail(GATSPI_EBADWAVE, "malformed waveform (net %d, window %d)", st[1], st[2]);
         case GATSPI_EBADLUT:
             return fail(GATSPI_EBADLUT, "gate %d window %d: every switching arc of an output change has no delay", st[1], st[2]);
         case GATSPI_ETIMEOUT:

@@ -42,9 +42,10 @@
 // loop keeps only the pins' next arrivals in registers and most of the SM's L1 is
 // left to the source waveforms.  No warp waits for another.
 //
-// No kernel traps: a malformed waveform, a missing delay arc, pool overflow or a
-// stalled look-back sets the device status word and the kernels carry on without
-// writing out of bounds.
+// No kernel traps: a missing delay arc, pool overflow or a stalled look-back sets the
+// device status word and the kernels carry on without writing out of bounds.  Input
+// waveforms are checked when they are loaded (load_index_kernel, the testbench cut);
+// every later waveform is this kernel's own output.
 #include "gatspi_internal.cuh"
 
 namespace gatspi {
@@ -103,34 +104,33 @@ __device__ __forceinline__ int32_t reject_limit(int32_t d, int32_t q) {
 // timestamp plus the delay.  On entry s.nx holds w[p + 1] (the word after the
 // previous pulse test), so a step loads one word.  The common step is straight-line
 // code, so that lanes advancing different pins stay together; only a swallowed
-// pulse takes the loop.  False on a malformed wave.
+// pulse takes the loop.  The waves are well formed: inputs are checked when they are
+// loaded and every output is written by this kernel; whatever a wave holds, the
+// reads stay inside it (len bounds them) and the loop ends.
 // p and len may be offsets from any base w (the entry is w[p], the window ends at
 // w[len]); par is the pin's value in entry p (p's parity when p counts from the
 // window's start).  t2pre: w[p + 2] when the caller has it already (a wave's first
 // words are loaded together), else unused.
 template <bool kFull, bool kPre = false>
-__device__ __forceinline__ bool next_arrival(uint32_t &p, int32_t &a, int32_t &nx, const int32_t *__restrict__ w,
+__device__ __forceinline__ void next_arrival(uint32_t &p, int32_t &a, int32_t &nx, const int32_t *__restrict__ w,
                                              uint32_t len, uint32_t drf, uint32_t par, int32_t q, int32_t t2pre = 0) {
     bool last = p + 2 >= len;                      // p + 1 is the EOW slot: no further transition
     int32_t t1 = nx;
     int32_t t2 = kPre ? t2pre : (last ? kEOW : __ldg(w + p + 2));
     const int32_t d = par ? (int32_t)(drf >> 16) : (int32_t)(drf & 0xffffu);
     const int32_t lim = kFull ? d : reject_limit(d, q);
-    bool bad = !last && t1 == kEOW;                 // EOW before the last slot: malformed
-    if (!last && !bad && t2 - t1 < lim) {           // the pulse [t1, t2) never reaches the pin
+    if (!last && t2 - t1 < lim) {                   // the pulse [t1, t2) never reaches the pin
         for (;;) {
             p += 2;                                 // same parity: same delay
             last = p + 2 >= len;
             if (last) break;
             t1 = __ldg(w + p + 1);
             t2 = __ldg(w + p + 2);
-            bad = t1 == kEOW;
-            if (bad || t2 - t1 >= lim) break;
+            if (t2 - t1 >= lim) break;
         }
     }
-    a = (last || bad) ? kEOW : t1 + d;
+    a = last ? kEOW : t1 + d;
     nx = t2;                                        // w[p + 2]: the next transition once this one is taken
-    return last ? p + 2 == len : !bad;
 }
 
 // A pin of a multi-pin cell in the event loop lives in shared memory (one column per
@@ -167,11 +167,11 @@ __device__ __forceinline__ int32_t arc_delay(const int32_t *__restrict__ D, uint
 // Take the transition of pin k (chosen per lane) that has just arrived and find the
 // pin's next arrival.  vbits holds every pin's value after the step.
 template <int N, bool kFull, bool kTable>
-__device__ __forceinline__ bool advance_pin(Pin (&pin)[N], const int32_t *lb, const PinTab &tab, int k,
+__device__ __forceinline__ void advance_pin(Pin (&pin)[N], const int32_t *lb, const PinTab &tab, int k,
                                             uint32_t vbits, int32_t q) {
     if constexpr (N == 1) {
         ++pin[0].p;
-        return next_arrival<kFull>(pin[0].p, pin[0].a, pin[0].nx, pin[0].w, pin[0].len, pin[0].drf, pin[0].p & 1u, q);
+        next_arrival<kFull>(pin[0].p, pin[0].a, pin[0].nx, pin[0].w, pin[0].len, pin[0].drf, pin[0].p & 1u, q);
     } else if constexpr (kTable) {
         const int2 h = tab.hot[k * 32];
         const uint32_t end = tab.end[k * 32];
@@ -181,12 +181,11 @@ __device__ __forceinline__ bool advance_pin(Pin (&pin)[N], const int32_t *lb, co
             if (k == i) drf = pin[i].drf;
         uint32_t off = (uint32_t)h.x + 1u;
         int32_t nx = h.y, a;
-        const bool ok = next_arrival<kFull>(off, a, nx, lb, end, drf, (vbits >> (N - 1 - k)) & 1u, q);
+        next_arrival<kFull>(off, a, nx, lb, end, drf, (vbits >> (N - 1 - k)) & 1u, q);
         tab.hot[k * 32] = make_int2((int32_t)off, nx);
 #pragma unroll
         for (int i = 0; i < N; ++i)
             if (k == i) pin[i].a = a;
-        return ok;
     } else {
         // registers: the pin's state is gathered and written back with predicated
         // moves so that the lanes of a warp advance different pins together
@@ -195,7 +194,7 @@ __device__ __forceinline__ bool advance_pin(Pin (&pin)[N], const int32_t *lb, co
         for (int i = 1; i < N; ++i)
             if (k == i) s = pin[i];
         ++s.p;
-        const bool ok = next_arrival<kFull>(s.p, s.a, s.nx, s.w, s.len, s.drf, s.p & 1u, q);
+        next_arrival<kFull>(s.p, s.a, s.nx, s.w, s.len, s.drf, s.p & 1u, q);
 #pragma unroll
         for (int i = 0; i < N; ++i)
             if (k == i) {
@@ -203,7 +202,6 @@ __device__ __forceinline__ bool advance_pin(Pin (&pin)[N], const int32_t *lb, co
                 pin[i].a = s.a;
                 pin[i].nx = s.nx;
             }
-        return ok;
     }
 }
 
@@ -268,10 +266,10 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb,
     put(0, y0 ? -1 : 0);
     if (y0) put(1, 0);
 
-    bool ok = true, lutbad = false;
+    bool lutbad = false;
 #pragma unroll
     for (int i = 0; i < N; ++i) {
-        ok &= next_arrival<kFull, true>(pin[i].p, pin[i].a, pin[i].nx, pin[i].w, pin[i].len, pin[i].drf,
+        next_arrival<kFull, true>(pin[i].p, pin[i].a, pin[i].nx, pin[i].w, pin[i].len, pin[i].drf,
                                         pin[i].p & 1u, q, t2first[i]);
         if constexpr (N > 1 && kTable) {
             const uint32_t o = (uint32_t)(pin[i].w - lb);
@@ -284,7 +282,7 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb,
         int32_t t = pin[0].a;
 #pragma unroll
         for (int i = 1; i < N; ++i) t = min(t, pin[i].a);
-        if ((t == kEOW) | !ok) break;
+        if (t == kEOW) break;
 
         // every pin arriving at t switches together (bit N-1-i = pin i); each one's
         // entry index moves on when the pin is advanced below
@@ -333,12 +331,11 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb,
             second = top;
             top = to;
         }
-        ok &= advance_pin<N, kFull, kTable>(pin, lb, tab, k, vbits, q);
+        advance_pin<N, kFull, kTable>(pin, lb, tab, k, vbits, q);
         for (uint32_t mm = more; mm; mm &= mm - 1u)   // lowest bit first
-            ok &= advance_pin<N, kFull, kTable>(pin, lb, tab, N - __ffs(mm), vbits, q);
+            advance_pin<N, kFull, kTable>(pin, lb, tab, N - __ffs(mm), vbits, q);
     }
-    if (!ok) r.err = GATSPI_EBADWAVE;
-    if (lutbad) r.err = GATSPI_EBADLUT;     // a missing arc is met before any later malformed word
+    if (lutbad) r.err = GATSPI_EBADLUT;
     put(po + 1, kEOW);
     r.len = po + 2;
     r.tc = po - y0;

@@ -46,6 +46,7 @@ class Simulator:
         self.num_gates = int(net.num_gates)
         self.num_levels = int(net.num_levels)
         self.num_nets = self.num_inputs + self.num_gates
+        self._owns_pool = pool is None
         if pool is None:
             if pool_words is None:
                 raise ValueError("give pool_words or pool")
@@ -78,9 +79,12 @@ class Simulator:
 
     # -- lifecycle ---------------------------------------------------------------
     def close(self):
+        """Release the context; a pool this object allocated is dropped with it."""
         if getattr(self, "ctx", None):
             _c.gatspi_destroy(self.ctx)
             self.ctx = None
+            if getattr(self, "_owns_pool", False):
+                self.pool = None
 
     def __del__(self):
         try:

@@ -33,8 +33,8 @@
  *   - host arrays passed in are copied during the call; the caller keeps ownership;
  *   - the waveform pool is borrowed: a device buffer the caller allocates (for
  *     example a torch int32 tensor) and keeps alive until gatspi_destroy;
- *   - asynchronous failures (pool overflow, malformed waveform, missing delay arc,
- *     a stalled scan) are latched in a device status word and reported by the next
+ *   - asynchronous failures (pool overflow, missing delay arc, a stalled scan) are
+ *     latched in a device status word and reported by the next
  *     synchronising call (gatspi_sync, gatspi_toggle_stats, gatspi_get_waveform,
  *     gatspi_export_offsets);
  *   - a context is used by one host thread at a time.
@@ -386,7 +386,10 @@ gatspi_status gatspi_set_level_timing(gatspi_ctx *ctx, int32_t on);
  *   window_len  int32 [num_windows]
  *   pool, net_base, wstart, wend, wlen8
  *               the waveform store of gatspi_views (pool_words = capacity); the
- *               sources of this level must already be in it; wlen8 (uint8, 4-byte
+ *               sources of this level must already be in it, well formed (the regular
+ *               path checks every input when it loads it; from a malformed source this
+ *               call writes unspecified words, but reads and writes stay inside the
+ *               source's window and the output's slot); wlen8 (uint8, 4-byte
  *               aligned) holds min(length, 255) of waveform (net, w) at
  *               net * W4 + w, W4 = num_windows rounded up to a multiple of 4
  *   perm, goff  the level's plan (scratch, written then read by this call):
@@ -442,7 +445,7 @@ typedef struct {
  *     kernel runs; calls that overlap on the GPU (other streams, other threads)
  *     race on it and must be serialised by the caller.
  *   - Synchronous: enqueues on `stream`, waits for it, and returns the kernel's
- *     status (GATSPI_EPOOL_OVERFLOW, GATSPI_EBADWAVE, GATSPI_EBADLUT, ...).
+ *     status (GATSPI_EPOOL_OVERFLOW, GATSPI_EBADLUT, ...).
  * Results are identical to the level kernels gatspi_simulate runs.
  */
 gatspi_status gatspi_simulate_level_static(const gatspi_level_args *args, void *stream);

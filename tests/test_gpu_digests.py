@@ -40,13 +40,18 @@ def gpu():
     return Simulator
 
 
-def _pool_for_device(net, W):
-    """Pool words: the free device memory less the context's own arrays and a margin."""
+def _release_device_memory():
     import gc
 
     import torch
     gc.collect()
-    torch.cuda.empty_cache()          # the previous workload's pool back to the driver
+    torch.cuda.empty_cache()
+
+
+def _pool_for_device(net, W):
+    """Pool words: the free device memory less the context's own arrays and a margin."""
+    import torch
+    _release_device_memory()          # the previous workload's pool back to the driver
     free, _ = torch.cuda.mem_get_info()
     nets = net.num_inputs + net.num_gates
     widest = int(np.diff(net.level_offsets).max())
@@ -115,11 +120,14 @@ def test_full_size_against_oracle_digests(gpu, name):
     assert digests.inputs_sha256(net, stim) == rec["inputs_sha256"], \
         "the generator drew other inputs than the stored oracle run"
     W = stim.num_windows
-    with gpu(net, stim.window_len, pool_words=_pool_for_device(net, W)) as sim:
-        sim.load(stim.pi_off, stim.pi_words)
-        sim.simulate()
-        tc, t0, t1 = sim.toggle_stats()
-        h, words = sim.net_digests(with_words=True)
+    try:
+        with gpu(net, stim.window_len, pool_words=_pool_for_device(net, W)) as sim:
+            sim.load(stim.pi_off, stim.pi_words)
+            sim.simulate()
+            tc, t0, t1 = sim.toggle_stats()
+            h, words = sim.net_digests(with_words=True)
+    finally:
+        _release_device_memory()      # the pool took most of the device: give it back for later tests
     assert np.array_equal(t0 + t1, np.full(net.num_gates, rec["window_time"]))
     assert digests.input_record(net.num_inputs, h, words) == rec["inputs"]
     got = digests.level_records(net.level_offsets, net.num_inputs, h, words, tc, t1)
