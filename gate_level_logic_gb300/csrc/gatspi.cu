@@ -141,6 +141,7 @@ struct gatspi_ctx {
         p.lpg_log2 = lpg_log2;
         p.slots_per_gate = slots_per_gate;
         p.pulse_percent = pulse_percent;
+        p.ranked = windows_ranked(W) ? 1 : 0;
         p.spin_limit_ns = stall_level >= 0 ? (unsigned long long)stall_wait_ns : kSpinLimitNs;
         return p;
     }
@@ -468,7 +469,8 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(dev_alloc(&c->wend, (size_t)(c->num_nets * c->W)), "allocating the window index");
         CUDA_TRY(dev_alloc(&c->wlen8, (size_t)std::max<long long>(c->num_nets * ((c->W + 3) & ~3), 4)),
                  "allocating the window index");
-        CUDA_TRY(dev_alloc(&c->perm, (size_t)std::max<long long>(c->max_level_gates * c->W, 1)), "allocating the plan");
+        CUDA_TRY(dev_alloc(&c->perm, (size_t)(windows_ranked(c->W) ? std::max<long long>(c->max_level_gates * c->W, 1) : 1)),
+                 "allocating the plan");
         CUDA_TRY(dev_alloc(&c->goff, (size_t)std::max<long long>(c->max_level_gates * (c->ngroups + 1), 1)),
                  "allocating the plan");
         CUDA_TRY(dev_alloc(&c->window_len, (size_t)c->W), "allocating window lengths");

@@ -25,6 +25,11 @@ constexpr int kTileSlots = 32;            // (gate, rank) slots per warp of the 
 constexpr int kPlanWarps = 4;             // warps per block of the planning kernel (one gate each)
 constexpr int kPlanMinBlocks = 12;        // planning blocks per SM the registers must allow (40 registers)
 constexpr int kSortBuckets = 256;         // counting-sort buckets of the window bounds
+// Up to this many windows a gate's windows are ranked by bound for the simulation
+// warps (load balance); beyond it the windows are short (few cycles each), set-up
+// dominates and they are taken in window order, with no plan of ranks.
+constexpr int kRankMaxWindows = 1024;
+inline bool windows_ranked(int W) { return W <= kRankMaxWindows; }
 constexpr int32_t kEOW = GATSPI_EOW;
 constexpr int32_t kNoArc = GATSPI_NO_ARC;
 
@@ -57,7 +62,7 @@ struct DevParams {
     const int32_t *window_len; // [W]
     // the level's plan: per gate, its windows by rank (largest output bound first) and
     // the offset of every group of 32 ranks inside the gate's region
-    uint16_t *perm;            // [gates of the level * W]
+    uint16_t *perm;            // [gates of the level * W] (ranked windows only)
     uint32_t *goff;            // [gates of the level * (ngroups + 1)]: group offsets, then the region's size
     // toggle statistics
     unsigned long long *tc;    // [G]
@@ -77,6 +82,7 @@ struct DevParams {
     int32_t lpg_log2;         // log2(lanes per (gate, group) segment)
     int32_t slots_per_gate;   // ngroups << lpg_log2
     int32_t pulse_percent;    // PATHPULSEPERCENT, 0 .. 100
+    int32_t ranked;           // windows_ranked(W): perm holds the ranks; else rank = window
     unsigned long long spin_limit_ns;   // how long a look-back wait may see no progress before ETIMEOUT
 };
 

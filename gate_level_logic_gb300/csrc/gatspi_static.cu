@@ -116,6 +116,7 @@ extern "C" gatspi_status gatspi_simulate_level_static(const gatspi_level_args *a
     p.status = (int32_t *)(words + kStatusWord);
     p.num_inputs = a->num_inputs;
     p.pulse_percent = own_percent ? a->pulse_percent : 100;
+    p.ranked = windows_ranked(a->num_windows) ? 1 : 0;
     p.spin_limit_ns = kSpinLimitNs;
 
     LevelLaunch l{};

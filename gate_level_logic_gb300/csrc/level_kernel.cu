@@ -587,6 +587,80 @@ __global__ void __launch_bounds__(kPlanWarps * 32, kPlanMinBlocks) level_plan_ke
     }
 }
 
+// The plan of one gate per warp when the windows are not ranked (many short
+// windows): the windows' output bounds, 128 consecutive windows per step (four per
+// lane from one 4-byte load of the byte lengths per pin, the bounds summed in 16-bit
+// halves as in plan_bounds), each group of 32 windows (eight lanes) summed by a
+// segmented warp reduction into the group offsets and the region's size.  No shared
+// memory, no ranks.
+template <int N>
+__device__ __forceinline__ void plan_window_order(const DevParams &P, const LevelLaunch &L, int gl, int4 sv, int lane) {
+    const int W = P.W;
+    const int s4[GATSPI_MAX_PINS] = {sv.x, sv.y, sv.z, sv.w};
+    uint32_t *goff = P.goff + (long long)gl * (P.ngroups + 1);
+    long long run = 0;
+    for (int w0 = 4 * lane; w0 - 4 * lane < W; w0 += 4 * 32) {
+        long long part = 0;   // this lane's four windows
+        if (w0 < W) {
+            uint32_t even = 0, odd = 0;        // windows w0, w0 + 2 and w0 + 1, w0 + 3 in 16-bit halves
+            uint32_t fix[4] = {0, 0, 0, 0};    // lengths beyond 255
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const long long src = s4[i];
+                const uint32_t four = __ldg((const uint32_t *)(P.wlen8 + src * P.w8stride + w0));
+                even += four & 0x00ff00ffu;
+                odd += (four >> 8) & 0x00ff00ffu;
+                if (__vcmpeq4(four, 0xffffffffu)) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int w = w0 + u;
+                        if (((four >> (8 * u)) & 0xffu) == 0xffu && w < W)
+                            fix[u] += __ldg(P.wend + src * W + w) - __ldg(P.wstart + src * W + w) - 255u;
+                    }
+                }
+            }
+            const uint32_t base = 3u - 2u * (uint32_t)N;
+            const uint32_t b[4] = {base + (even & 0xffffu) + fix[0], base + (odd & 0xffffu) + fix[1],
+                                   base + (even >> 16) + fix[2], base + (odd >> 16) + fix[3]};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (w0 + u < W) part += b[u];
+        }
+        // the group of 32 windows of this step that holds lane's windows: lanes 8k .. 8k+7
+        long long gsum = part;
+#pragma unroll
+        for (int o = 4; o >= 1; o >>= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
+        // the four groups' sums (lanes 0, 8, 16, 24) and their running offsets
+        const long long g0 = __shfl_sync(0xffffffffu, gsum, 0), g1 = __shfl_sync(0xffffffffu, gsum, 8);
+        const long long g2 = __shfl_sync(0xffffffffu, gsum, 16), g3 = __shfl_sync(0xffffffffu, gsum, 24);
+        const int grp = (w0 - 4 * lane) >> 5;            // first group of this step
+        if (lane < 4 && grp + lane < P.ngroups) {
+            const long long before = lane == 0 ? 0 : lane == 1 ? g0 : lane == 2 ? g0 + g1 : g0 + g1 + g2;
+            goff[grp + lane] = (uint32_t)(run + before);
+        }
+        run += g0 + g1 + g2 + g3;
+    }
+    if (lane == 0) {
+        if (run >= (1ll << 32)) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, L.gate_begin + gl, 1);
+        goff[P.ngroups] = (uint32_t)run;   // the region's size
+    }
+}
+
+__global__ void __launch_bounds__(kPlanWarps * 32) level_plan_window_order_kernel(const DevParams P, const LevelLaunch L) {
+    const int lane = threadIdx.x & 31;
+    const int gl = blockIdx.x * kPlanWarps + (threadIdx.x >> 5);
+    if (gl >= L.num_gates) return;
+    const int g = L.gate_begin + gl;
+    const int4 gd = __ldg(P.gate_desc + 3 * (long long)g);
+    const int4 sv = __ldg(P.gate_desc + 3 * (long long)g + 1);
+    switch (gd.y & 7) {   // warp-uniform: one gate per warp
+        case 1: plan_window_order<1>(P, L, gl, sv, lane); break;
+        case 2: plan_window_order<2>(P, L, gl, sv, lane); break;
+        case 3: plan_window_order<3>(P, L, gl, sv, lane); break;
+        default: plan_window_order<4>(P, L, gl, sv, lane); break;
+    }
+}
+
 // Pool offsets of the level's gate regions: their sizes (from the plan) scanned in
 // gate order, one thread per gate and one tile of kPlaceTile gates per block (warp
 // shuffles, then the warps' totals), and a decoupled look-back over the tiles; the
@@ -673,7 +747,7 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     const bool in_level = gl < L.num_gates;
     const bool loaded = in_level && rank < P.W;
     const int g = L.gate_begin + gl;
-    const int w = loaded ? (int)__ldg(P.perm + (long long)gl * P.W + rank) : 0;
+    const int w = loaded ? (P.ranked ? (int)__ldg(P.perm + (long long)gl * P.W + rank) : rank) : 0;
 
     const int seg_lead = lane & ~((1 << P.lpg_log2) - 1);  // first lane of this (gate, group) segment
     const long long net = (long long)P.num_inputs + g;
@@ -857,10 +931,10 @@ cudaError_t launch_net_digests(const DevParams &p, long long net0, long long n, 
     return cudaGetLastError();
 }
 
-int plan_gates_per_tile(int W) { return W > 4096 ? 1 : kPlanWarps; }   // one warp per block for long window lists
+int plan_gates_per_tile(int) { return kPlanWarps; }
 
 int plan_words(int W) {   // per warp: W bounds, the buckets, the group sums, each padded to 4 words
-    return ((W + 3) & ~3) + kSortBuckets + (((W + 31) / 32 + 3) & ~3);
+    return windows_ranked(W) ? ((W + 3) & ~3) + kSortBuckets + (((W + 31) / 32 + 3) & ~3) : 0;
 }
 
 size_t plan_smem_bytes(int W) {
@@ -870,7 +944,11 @@ size_t plan_smem_bytes(int W) {
 cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
     const int wpb = plan_gates_per_tile(p.W);
     if (l.num_gates > 0) {
-        level_plan_kernel<<<(unsigned)((l.num_gates + wpb - 1) / wpb), wpb * 32, plan_smem_bytes(p.W), s>>>(p, l);
+        const unsigned blocks = (unsigned)((l.num_gates + wpb - 1) / wpb);
+        if (p.ranked)
+            level_plan_kernel<<<blocks, wpb * 32, plan_smem_bytes(p.W), s>>>(p, l);
+        else
+            level_plan_window_order_kernel<<<blocks, kPlanWarps * 32, 0, s>>>(p, l);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

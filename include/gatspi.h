@@ -158,7 +158,8 @@ typedef struct gatspi_ctx gatspi_ctx;
  * The pool holds first the input waveforms as loaded, then the gates' outputs level
  * by level; every net has one region.  A gate's region is sized by upper bounds of
  * its windows' outputs (see gatspi_simulate); its windows are stored in rank order
- * (windows ordered by bound, largest first), each in a slot as long as its bound, so
+ * (windows ordered by bound, largest first; window order beyond 1024 windows), each
+ * in a slot as long as its bound, so
  * a gap may follow every window.  Waveform k = (net, w), k = net * W + w,
  * is pool[net_base[net] + wstart[k] .. net_base[net] + wend[k]) (EOW included).  The
  * layout depends only on the inputs: every run gives the same pool.
@@ -237,8 +238,9 @@ gatspi_status gatspi_load_testbench(gatspi_ctx *ctx, const int64_t *off, const i
  * bounds every (gate, window) output (an output window holds at most 3 + the sum over
  * its pins of (input length - 2) words, since each stored toggle takes an event-loop
  * iteration and each iteration consumes an input transition), ranks each gate's
- * windows by bound so that a warp gets 32 windows of similar work, and scans the
- * gates' bound sums into pool offsets, in place of the page's counting pass.  The
+ * windows by bound so that a warp gets 32 windows of similar work (up to 1024
+ * windows; beyond, the windows are short and are taken in window order), and scans
+ * the gates' bound sums into pool offsets, in place of the page's counting pass.  The
  * second runs Algorithm 1 for every (gate, window) of the level and stores the output
  * waveforms, the window index and TC/T1 per gate.  The level sequence is captured once into a CUDA graph and
  * replayed by later calls, unless GATSPI_FLAG_NO_GRAPH or GATSPI_FLAG_LEVEL_TIMING
@@ -393,7 +395,8 @@ gatspi_status gatspi_set_level_timing(gatspi_ctx *ctx, int32_t on);
  *               aligned) holds min(length, 255) of waveform (net, w) at
  *               net * W4 + w, W4 = num_windows rounded up to a multiple of 4
  *   perm, goff  the level's plan (scratch, written then read by this call):
- *               uint16 [num_gates * num_windows] and uint32 [num_gates * (ceil(W / 32) + 1)]
+ *               uint16 [num_gates * num_windows] (unused beyond 1024 windows, which
+ *               are taken in window order) and uint32 [num_gates * (ceil(W / 32) + 1)]
  *   tc, t1      per-gate toggle count and time at 1, accumulated (not cleared)
  *   level_base  int64 [2]: [0] = first pool word of this level's outputs (read),
  *               [1] = one past its last word (written)

@@ -82,10 +82,12 @@ def test_50k_launch_variants(gpu, oracle_lib, flags):
     assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), flags=flags), ref, "flags=%d" % flags)
 
 
-@pytest.mark.parametrize("W", [1, 2, 3, 7, 16, 31, 32, 33, 63, 64, 65, 100, 128, 200, 256, 257, 384])
+@pytest.mark.parametrize("W", [1, 2, 3, 7, 16, 31, 32, 33, 63, 64, 65, 100, 128, 200, 256, 257, 384, 1024, 1025,
+                               1500])
 def test_window_counts(gpu, oracle_lib, W):
     """Ragged window chunks, several gates per warp (W < 32), ragged tiles, whole
-    blocks of one gate's chunks (W = 128, 256, 384)."""
+    blocks of one gate's chunks (W = 128, 256, 384), the most windows that are ranked
+    (1024) and windows taken in window order beyond it (1025, 1500)."""
     net = synth.generate_netlist(synth.NetlistSpec(num_gates=3001, num_inputs=37, num_levels=9, seed=W,
                                                    cond_fraction=0.3))
     stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=37, cycles=max(W, 300), period=500,
@@ -105,6 +107,20 @@ def test_long_windows(gpu, oracle_lib, W):
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
     lens = np.diff(ref.off)
     assert lens.max() > 700 and (lens >= 255).mean() > 0.2
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref, "W=%d" % W)
+
+
+def test_long_windows_in_window_order(gpu, oracle_lib):
+    """More than 1024 windows (taken in window order) of 255 words and more: the
+    planner reads those lengths exactly from the window index."""
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=300, num_inputs=24, num_levels=4, seed=611,
+                                                   cond_fraction=0.3))
+    W = 1025
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=24, cycles=W * 260, period=300, activity=1.0,
+                                                      windows=W, seed=11))
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    lens = np.diff(ref.off)
+    assert (lens >= 255).mean() > 0.5
     assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref, "W=%d" % W)
 
 
