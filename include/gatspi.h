@@ -266,12 +266,14 @@ gatspi_status gatspi_sync(gatspi_ctx *ctx);
 /*
  * SAIF-style toggle statistics per gate, summed over windows (host arrays [G]; any
  * may be NULL): tc = output toggles, t1 = time at 1, t0 = time at 0, with
- * t0 + t1 = sum of window_len.  Synchronises first.
+ * t0 + t1 = sum of window_len -- the per-net activity the page's re-simulation
+ * produces for power analysis (Section 3, Fig. 2).  Synchronises first.
  */
 gatspi_status gatspi_toggle_stats(gatspi_ctx *ctx, int64_t *tc, int64_t *t0, int64_t *t1);
 
 /*
- * The same statistics without a copy: *tc and *t1 point at the library's pinned host
+ * The same statistics without a copy (the page dumps its statistics while the GPU
+ * works, Section 3): *tc and *t1 point at the library's pinned host
  * copies (uint64 [num_gates], gate order) that simulate filled level by level, valid
  * until the next simulate or destroy; t0 = sum of window_len - t1 (*window_sum).
  * Synchronises first.  GATSPI_ESTATE before the first simulate; NULL pointers for a
@@ -282,7 +284,8 @@ gatspi_status gatspi_toggle_stats_host(gatspi_ctx *ctx, const uint64_t **tc, con
 
 /*
  * The same statistics for the inputs, from the loaded windows (host arrays
- * [num_inputs]; any may be NULL): computed on the device by every load.
+ * [num_inputs]; any may be NULL): computed on the device by every load.  A SAIF
+ * file covers every net, inputs included (Section 3, Fig. 2).
  */
 gatspi_status gatspi_input_stats(gatspi_ctx *ctx, int64_t *tc, int64_t *t0, int64_t *t1);
 
@@ -353,8 +356,9 @@ gatspi_status gatspi_net_digests(gatspi_ctx *ctx, int64_t net_begin, int64_t num
 gatspi_status gatspi_device_views(gatspi_ctx *ctx, gatspi_views *out);
 
 /*
- * Per-level kernel times in milliseconds of the last simulate (which must have run
- * with GATSPI_FLAG_LEVEL_TIMING): sim_ms[l] for the simulation kernel of level l,
+ * Per-level kernel times in milliseconds of the last simulate (the page profiles the
+ * kernel level by level, Section 5, Table 6), which must have run
+ * with GATSPI_FLAG_LEVEL_TIMING: sim_ms[l] for the simulation kernel of level l,
  * bounds_ms[l] for the kernels that plan and place its output regions (either may
  * be NULL; n = num_levels).  Synchronises first.  GATSPI_ESTATE when the last
  * simulate was not timed.
@@ -362,8 +366,8 @@ gatspi_status gatspi_device_views(gatspi_ctx *ctx, gatspi_views *out);
 gatspi_status gatspi_level_times(gatspi_ctx *ctx, float *sim_ms, float *bounds_ms, int32_t n);
 
 /*
- * Switch GATSPI_FLAG_LEVEL_TIMING on (on != 0) or off for the following simulate
- * calls.  Timed runs launch the levels directly with a CUDA event between every two
+ * Switch GATSPI_FLAG_LEVEL_TIMING (per-level times, Section 5, Table 6) on (on != 0)
+ * or off for the following simulate calls.  Timed runs launch the levels directly with a CUDA event between every two
  * kernels; untimed runs replay the captured level graph (unless
  * GATSPI_FLAG_NO_GRAPH).  GATSPI_EINVAL when ctx is NULL.
  */
