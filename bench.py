@@ -97,7 +97,7 @@ WORKLOAD_NAMES = {
 }
 
 
-def workload_config(net, stim, pulse_percent=100, overrides=None, workload=WORKLOAD, world=1):
+def workload_config(net, stim, pulse_percent=100, overrides=None, workload=WORKLOAD, world=1, compact=False):
     name = WORKLOAD_NAMES[workload]
     if world > 1:
         name += ("; the testbench %dx longer, its windows split into %d contiguous ranges, one per GPU"
@@ -111,6 +111,7 @@ def workload_config(net, stim, pulse_percent=100, overrides=None, workload=WORKL
         "gates": int(net.num_gates), "levels": int(net.num_levels), "inputs": int(net.num_inputs),
         "edges": int(net.num_edges), "windows": int(stim.num_windows), "cycles": int(stim.window_cycles.sum()),
         "pulse_percent": pulse_percent,
+        "packed_levels": bool(compact),
         "parallelism": ("windows split over %d GPUs (one contiguous range each, one int64 sum of TC/T1 "
                         "at the end)" % world) if world > 1 else "one GPU",
         "l2": "inputs larger than L2 (waveform pool of several GB per step, no flush needed)",
@@ -429,7 +430,7 @@ def run_gpu(args):
             kw["cycles"] = world * int(kw.get("cycles", stim_kw["cycles"]))
             kw["windows"] = world * int(kw.get("windows", stim_kw["windows"]))
         net, stim = synth.make(workload, **kw)
-    flags = 0
+    flags = 0x8 if args.compact else 0       # GATSPI_FLAG_COMPACT
     pool_gb = args.pool_gb if args.pool_gb > 0 else {"1M": 48.0, "5M": 170.0, "scan500k": 64.0}[workload]
     pool_words = int(pool_gb * (1 << 30) / 4)
     part = shard.WindowShard(net, stim.window_len, world, rank, pool_words=pool_words, flags=flags,
@@ -527,7 +528,7 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": workload_config(net, stim, args.pulse_percent, over, workload, world),
+        "config": workload_config(net, stim, args.pulse_percent, over, workload, world, args.compact),
         "gate_cycles_per_s": gate_cycles_per_s,
         "events_per_step": events_per_step,
         "pool_words_used": pool_used,
@@ -589,6 +590,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOAD_NAMES),
                     help="the workload timed (the 1M-gate configuration by default)")
     ap.add_argument("--pool-gb", type=float, default=0.0, help="waveform pool (0: sized for the workload)")
+    ap.add_argument("--compact", action="store_true",
+                    help="pack every level to its exact size after simulating it (GATSPI_FLAG_COMPACT)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--windows", type=int, default=0, help="profiling only: number of cycle windows")

@@ -68,6 +68,10 @@ struct gatspi_ctx {
     int4 *gate_desc = nullptr;
     int32_t *dly = nullptr;
     int32_t *gate_order = nullptr;   // W < 32: every level's gates by pin count
+    bool compact = false;            // GATSPI_FLAG_COMPACT
+    uint32_t *gexact = nullptr;      // compaction: exact words per (gate, group) of a level
+    long long *old_base = nullptr;   // compaction: a level's bound-sized regions
+    long long *level_bound = nullptr, *level_need = nullptr;   // compaction: [L]
     long long *net_base = nullptr;
     uint32_t *wstart = nullptr;
     uint32_t *wend = nullptr;
@@ -89,6 +93,7 @@ struct gatspi_ctx {
     // host copies
     std::vector<int32_t> level_offsets;
     std::vector<LevelLaunch> launches;
+    std::vector<LevelLaunch> exact_launches;   // compaction: the scans of the exact sizes
     long long total_tiles = 0;
     long long sum_window_len = 0;
     long long path_delay_bound = 0;   // levels * (max wire delay + max gate delay)
@@ -142,6 +147,11 @@ struct gatspi_ctx {
         p.slots_per_gate = slots_per_gate;
         p.pulse_percent = pulse_percent;
         p.ranked = windows_ranked(W) ? 1 : 0;
+        p.compact = compact ? 1 : 0;
+        p.gexact = gexact;
+        p.old_base = old_base;
+        p.level_bound = level_bound;
+        p.level_need = level_need;
         p.spin_limit_ns = stall_level >= 0 ? (unsigned long long)stall_wait_ns : kSpinLimitNs;
         return p;
     }
@@ -258,7 +268,7 @@ void free_all(gatspi_ctx *c) {
     if (c->dump_stream) cudaStreamDestroy(c->dump_stream);
     if (c->tc_host) cudaFreeHost(c->tc_host);
     if (c->t1_host) cudaFreeHost(c->t1_host);
-    void *ptrs[] = {c->gate_desc, c->dly, c->gate_order, c->net_base, c->wstart, c->wend, c->wlen8, c->perm, c->goff,
+    void *ptrs[] = {c->gexact, c->old_base, c->level_bound, c->level_need, c->gate_desc, c->dly, c->gate_order, c->net_base, c->wstart, c->wend, c->wlen8, c->perm, c->goff,
                     c->window_len, c->tc, c->t1,
                     c->tile_status, c->tickets, c->level_base, c->status, c->load_off, c->max_time,
                     c->win_start, c->tc_in, c->t1_in};
@@ -309,9 +319,10 @@ gatspi_status input_stats(gatspi_ctx *c, cudaStream_t s) {
 gatspi_status enqueue_levels(gatspi_ctx *c, cudaStream_t s) {
     CUDA_TRY(cudaMemsetAsync(c->tc, 0, sizeof(unsigned long long) * std::max(c->G, 1), s), "clearing TC");
     CUDA_TRY(cudaMemsetAsync(c->t1, 0, sizeof(unsigned long long) * std::max(c->G, 1), s), "clearing T1");
-    CUDA_TRY(cudaMemsetAsync(c->tile_status, 0, sizeof(unsigned long long) * std::max<long long>(c->total_tiles, 1), s),
-             "clearing the scan state");
-    CUDA_TRY(cudaMemsetAsync(c->tickets, 0, sizeof(int32_t) * std::max(c->L, 1), s), "clearing the tile tickets");
+    const int scans = c->compact ? 2 : 1;   // compaction scans every level twice
+    CUDA_TRY(cudaMemsetAsync(c->tile_status, 0, sizeof(unsigned long long) * std::max<long long>(scans * c->total_tiles, 1),
+                             s), "clearing the scan state");
+    CUDA_TRY(cudaMemsetAsync(c->tickets, 0, sizeof(int32_t) * std::max(scans * c->L, 1), s), "clearing the tile tickets");
     // an injected stall: the level's first ticket becomes 1 (its low byte set), so no
     // block ever takes tile 0 and the tiles after it wait for a flag nobody sets
     if (c->stall_level >= 0)
@@ -323,6 +334,10 @@ gatspi_status enqueue_levels(gatspi_ctx *c, cudaStream_t s) {
     // simulation kernel, [2l+2] after the simulation kernel
     for (int l = 0; l < c->L; ++l) {
         if (timing) CUDA_TRY(cudaEventRecord(c->events[2 * l], s), "recording a level event");
+        // compaction: the previous level is packed before this one is planned (its
+        // time counts with this level's bounds kernels)
+        if (c->compact && l > 0)
+            CUDA_TRY(launch_level_compact(p, c->launches[l - 1], c->exact_launches[l - 1], s), "packing a level");
         CUDA_TRY(launch_level_bounds(p, c->launches[l], s), "launching a bounds kernel");
         if (timing) CUDA_TRY(cudaEventRecord(c->events[2 * l + 1], s), "recording a level event");
         CUDA_TRY(launch_level_sim(p, c->launches[l], s), "launching a level kernel");
@@ -339,6 +354,8 @@ gatspi_status enqueue_levels(gatspi_ctx *c, cudaStream_t s) {
         }
     }
     if (timing && c->L > 0) CUDA_TRY(cudaEventRecord(c->events[2 * c->L], s), "recording a level event");
+    if (c->compact && c->L > 0)
+        CUDA_TRY(launch_level_compact(p, c->launches[c->L - 1], c->exact_launches[c->L - 1], s), "packing a level");
     if (c->G > 0) {   // the stream's later work waits for the dump
         CUDA_TRY(cudaEventRecord(c->dump_done, c->dump_stream), "recording the dump's end");
         CUDA_TRY(cudaStreamWaitEvent(s, c->dump_done, 0), "joining the dump");
@@ -444,9 +461,18 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
             ll.scan_tiles = (int32_t)scan;
             c->max_level_gates = std::max<long long>(c->max_level_gates, ll.num_gates);
             ll.tile_base = c->total_tiles;
+            ll.ticket = l;
             c->total_tiles += scan;
             c->launches.push_back(ll);
         }
+        c->compact = (cfg->flags & GATSPI_FLAG_COMPACT) != 0;
+        if (c->compact)
+            for (int l = 0; l < c->L; ++l) {   // the exact scans: their own tickets and look-back words
+                LevelLaunch ex = c->launches[l];
+                ex.tile_base += c->total_tiles;
+                ex.ticket = c->L + l;
+                c->exact_launches.push_back(ex);
+            }
 
         const long long dly_len = c->G > 0 ? nl->dly_len : 0;
         CUDA_TRY(dev_alloc(&c->gate_desc, gd.size()), "allocating gate descriptors");
@@ -476,8 +502,17 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
         CUDA_TRY(dev_alloc(&c->window_len, (size_t)c->W), "allocating window lengths");
         CUDA_TRY(dev_alloc(&c->tc, (size_t)c->G), "allocating TC");
         CUDA_TRY(dev_alloc(&c->t1, (size_t)c->G), "allocating T1");
-        CUDA_TRY(dev_alloc(&c->tile_status, (size_t)c->total_tiles), "allocating the scan state");
-        CUDA_TRY(dev_alloc(&c->tickets, (size_t)c->L), "allocating tile tickets");
+        const int scans = c->compact ? 2 : 1;
+        CUDA_TRY(dev_alloc(&c->tile_status, (size_t)(scans * c->total_tiles)), "allocating the scan state");
+        CUDA_TRY(dev_alloc(&c->tickets, (size_t)(scans * c->L)), "allocating tile tickets");
+        if (c->compact) {
+            CUDA_TRY(dev_alloc(&c->gexact, (size_t)std::max<long long>(c->max_level_gates * c->ngroups, 1)),
+                     "allocating the compaction state");
+            CUDA_TRY(dev_alloc(&c->old_base, (size_t)std::max<long long>(c->max_level_gates, 1)),
+                     "allocating the compaction state");
+            CUDA_TRY(dev_alloc(&c->level_bound, (size_t)std::max(c->L, 1)), "allocating the compaction state");
+            CUDA_TRY(dev_alloc(&c->level_need, (size_t)std::max(c->L, 1)), "allocating the compaction state");
+        }
         CUDA_TRY(dev_alloc(&c->level_base, (size_t)c->L + 1), "allocating level bases");
         CUDA_TRY(dev_alloc(&c->status, (size_t)kStatusWords), "allocating the status word");
         CUDA_TRY(dev_alloc(&c->load_off, (size_t)((long long)c->P * c->W + 1)), "allocating load offsets");
@@ -862,6 +897,12 @@ gatspi_status gatspi_device_views(gatspi_ctx *c, gatspi_views *v) {
         long long used = 0;
         CUDA_TRY(cudaMemcpy(&used, c->level_base + (c->simulated ? c->L : 0), sizeof used, cudaMemcpyDeviceToHost),
                  "reading the pool size");
+        if (c->compact && c->simulated && c->L > 0) {   // the most any level needed with its scratch
+            std::vector<long long> need((size_t)c->L);
+            CUDA_TRY(cudaMemcpy(need.data(), c->level_need, sizeof(long long) * c->L, cudaMemcpyDeviceToHost),
+                     "reading the pool size");
+            for (long long n : need) used = std::max(used, n);
+        }
         v->pool_used = used;
     }
     v->net_base = (const int64_t *)c->net_base;

@@ -83,6 +83,13 @@ struct DevParams {
     int32_t slots_per_gate;   // ngroups << lpg_log2
     int32_t pulse_percent;    // PATHPULSEPERCENT, 0 .. 100
     int32_t ranked;           // windows_ranked(W): perm holds the ranks; else rank = window
+    // compaction (GATSPI_FLAG_COMPACT): every level is simulated into bound-sized regions
+    // placed down from the top of the pool, then packed to exact size at the front
+    int32_t compact;
+    uint32_t *gexact;         // [gates of the level * ngroups] output words of every (gate, group)
+    long long *old_base;      // [gates of the level] the gate's bound-sized region before packing
+    long long *level_bound;   // [L] words of the level's bound-sized regions
+    long long *level_need;    // [L] pool words the level needed: packed front + its bound-sized regions
     unsigned long long spin_limit_ns;   // how long a look-back wait may see no progress before ETIMEOUT
 };
 
@@ -92,7 +99,8 @@ struct LevelLaunch {
     int32_t num_gates;
     int32_t num_tiles;      // warps of the level kernel: ceil(gates * slots_per_gate / 32)
     int32_t scan_tiles;     // blocks of the placement scan: max(1, ceil(gates / kPlaceTile))
-    long long tile_base;    // first look-back word of this level's plan
+    long long tile_base;    // first look-back word of this level's scan
+    int32_t ticket;         // this scan's tile ticket (level, or L + level for the exact scan)
 };
 
 int plan_words(int W);
@@ -101,6 +109,8 @@ int plan_gates_per_tile(int W);   // gates (warps) of one planning block
 cudaError_t set_level_smem_limit();   // the planning kernel's shared memory (largest W), the simulation kernels' L1
 cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // plan + placement
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s);      // the simulation
+cudaError_t launch_level_compact(const DevParams &p, const LevelLaunch &l, const LevelLaunch &exact,
+                                 cudaStream_t s);  // compaction: exact scan + packing copy
 cudaError_t launch_level(const DevParams &p, const LevelLaunch &l, cudaStream_t s);          // both, in order
 cudaError_t launch_window_lengths(const DevParams &p, long long num_nets, const int32_t *sel, int nsel,
                                   long long *len, cudaStream_t s);

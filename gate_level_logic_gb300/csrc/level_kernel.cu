@@ -665,13 +665,20 @@ __global__ void __launch_bounds__(kPlanWarps * 32) level_plan_window_order_kerne
 // gate order, one thread per gate and one tile of kPlaceTile gates per block (warp
 // shuffles, then the warps' totals), and a decoupled look-back over the tiles; the
 // values are ready when this kernel starts, so the waits are short and few.
+// kMode: kPlaceFront -- the regions of the bounds from the front of the free pool;
+// kPlaceTop -- the same regions placed down from the top of the pool (compaction:
+// the level's scratch); kPlaceExact -- regions of the exact output sizes from the
+// front (compaction: where the packing copy puts the level).
+enum { kPlaceFront = 0, kPlaceTop = 1, kPlaceExact = 2 };
+
+template <int kMode>
 __global__ void __launch_bounds__(kPlaceTile) level_place_kernel(const DevParams P, const LevelLaunch L) {
     __shared__ long long warp_sum[kPlaceTile / 32];
     __shared__ int tile_id, stop;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        tile_id = atomicAdd(P.tickets + L.level, 1);
+        tile_id = atomicAdd(P.tickets + L.ticket, 1);
         stop = ld_status(P.status) != 0;
     }
     __syncthreads();
@@ -679,7 +686,15 @@ __global__ void __launch_bounds__(kPlaceTile) level_place_kernel(const DevParams
     if (tile >= L.scan_tiles) return;                      // spare blocks
     const int gl = tile * kPlaceTile + threadIdx.x;
     const bool valid = !stop && gl < L.num_gates;
-    const long long size = valid ? (long long)__ldg(P.goff + (long long)gl * (P.ngroups + 1) + P.ngroups) : 0;
+    long long size = 0;
+    if (valid) {
+        if (kMode == kPlaceExact) {
+            const uint32_t *ge = P.gexact + (long long)gl * P.ngroups;
+            for (int c = 0; c < P.ngroups; ++c) size += __ldg(ge + c);
+        } else {
+            size = (long long)__ldg(P.goff + (long long)gl * (P.ngroups + 1) + P.ngroups);
+        }
+    }
     long long incl = size;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -698,15 +713,38 @@ __global__ void __launch_bounds__(kPlaceTile) level_place_kernel(const DevParams
             if (lane >= o) ti += v;
         }
         const long long total = __shfl_sync(0xffffffffu, ti, 31);
-        const long long base = P.level_base[L.level] + look_back(P, L, tile, total, lane);
+        const long long front = kMode == kPlaceTop ? 0 : P.level_base[L.level];
+        const long long base = front + look_back(P, L, tile, total, lane);
         warp_sum[lane] = base + ti - t;                    // the first word of each warp's gates
         if (lane == 0 && tile == L.scan_tiles - 1) {
-            P.level_base[L.level + 1] = base + total;
-            if (base + total > P.pool_words) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, 0, 0);
+            if (kMode == kPlaceFront) {
+                P.level_base[L.level + 1] = base + total;
+                if (base + total > P.pool_words) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, 0, 0);
+            } else if (kMode == kPlaceTop) {
+                // the level's scratch [pool top - total, pool top) must stay above the packed front
+                P.level_bound[L.level] = base + total;
+                if (P.level_base[L.level] + base + total > P.pool_words)
+                    raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, 0, 0);
+            } else {
+                // the packed level must end below the scratch it is copied from
+                const long long bound = P.level_bound[L.level];
+                P.level_base[L.level + 1] = base + total;
+                P.level_need[L.level] = base + total + bound;
+                if (base + total + bound > P.pool_words) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, 0, 0);
+            }
         }
     }
     __syncthreads();
-    if (valid) P.net_base[(long long)P.num_inputs + L.gate_begin + gl] = warp_sum[warp] + incl - size;
+    if (valid) {
+        const long long net = (long long)P.num_inputs + L.gate_begin + gl;
+        if (kMode == kPlaceTop) {
+            const long long b = P.pool_words - (warp_sum[warp] + incl);   // down from the top
+            P.net_base[net] = b;
+            P.old_base[gl] = b;
+        } else {
+            P.net_base[net] = warp_sum[warp] + incl - size;
+        }
+    }
 }
 
 // One warp = 32 slots of the level: a gate and 32 of its ranks.  Warps share nothing
@@ -810,12 +848,94 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
         atomicAdd(P.tc + g, (unsigned long long)tcs);
         atomicAdd(P.t1 + g, (unsigned long long)t1s);
     }
+    if (P.compact) {   // the (gate, group)'s output words, for the packing
+        uint32_t lsum = (uint32_t)res.len;
+        if (P.lpg_log2 == 5) {
+            lsum = __reduce_add_sync(0xffffffffu, lsum);
+        } else {
+            for (int o = (1 << P.lpg_log2) >> 1; o >= 1; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+        }
+        if (gate_ok && j == 0) P.gexact[(long long)gl * P.ngroups + c] = lsum;
+    }
 
     if (valid) {
         P.wstart[net * P.W + w] = gofs + rel;
         P.wend[net * P.W + w] = gofs + rel + (uint32_t)res.len;
         P.wlen8[net * P.w8stride + w] = (uint8_t)min(res.len, 255);
     }
+}
+
+// Packing of a level's outputs (compaction): every window moves from its bound-sized
+// slot in the level's scratch to its place in the gate's exact region, windows in
+// rank order and back to back; the window index is rewritten relative to the packed
+// region.  Same tiling as level_kernel (one (gate, group of 32 ranks) per warp, or
+// several gates per warp below 32 windows); a group's first word is the sum of the
+// gate's earlier groups' exact sizes.  The warp copies every segment's run of words
+// across its lanes: stores contiguous, each word's window found by a search of fixed
+// steps over the lanes' run offsets, so that every lane takes part in every shuffle.
+__global__ void __launch_bounds__(kLevelBlock) level_pack_kernel(const DevParams P, const LevelLaunch L) {
+    const int lane = threadIdx.x & 31;
+    const int tile = blockIdx.x * kLevelWarps + (threadIdx.x >> 5);
+    if (tile >= L.num_tiles) return;
+    const bool stop = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
+    int gl, c, j;
+    if (P.lpg_log2 == 5) {
+        gl = (int)__umulhi((uint32_t)tile, P.ngroups_m);
+        c = tile - gl * P.ngroups;
+        if (c >= P.ngroups) { ++gl; c -= P.ngroups; }
+        if (c >= P.ngroups) { ++gl; c -= P.ngroups; }
+        j = lane;
+    } else {
+        const int slot = tile * 32 + lane;
+        gl = slot >> P.lpg_log2;
+        if (P.gate_order && gl < L.num_gates) gl = __ldg(P.gate_order + L.gate_begin + gl) - L.gate_begin;
+        c = 0;
+        j = slot & ((1 << P.lpg_log2) - 1);
+    }
+    const int rank = c * 32 + j;
+    const bool in_level = gl < L.num_gates;
+    const bool loaded = !stop && in_level && rank < P.W;
+    const long long net = (long long)P.num_inputs + L.gate_begin + gl;
+    const int w = loaded ? (P.ranked ? (int)__ldg(P.perm + (long long)gl * P.W + rank) : rank) : 0;
+    const long long k = net * P.W + w;
+    uint32_t ws = 0, len = 0;
+    if (loaded) {
+        ws = P.wstart[k];
+        len = P.wend[k] - ws;
+    }
+    // the gate's earlier groups
+    long long before = 0;
+    if (P.lpg_log2 == 5 && in_level) {
+        const uint32_t *ge = P.gexact + (long long)gl * P.ngroups;
+        for (int cc = lane; cc < c; cc += 32) before += ge[cc];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+    }
+    // this window's place in its segment (rank order)
+    const int seg_lead = lane & ~((1 << P.lpg_log2) - 1);
+    const uint32_t incl = warp_incl_scan(len, lane);
+    const uint32_t excl = incl - len - (__shfl_sync(0xffffffffu, incl, seg_lead) - __shfl_sync(0xffffffffu, len, seg_lead));
+    const uint32_t rel = (uint32_t)before + excl;
+    const long long src0 = loaded ? P.old_base[gl] + ws : 0;      // this window's first word (scratch)
+    const long long dst0 = loaded ? P.net_base[net] + rel : 0;    // and its packed place
+    const int seg_n = 1 << P.lpg_log2;
+    for (int s0 = 0; s0 < 32; s0 += seg_n) {
+        const uint32_t run = __shfl_sync(0xffffffffu, excl + len, s0 + seg_n - 1);   // the segment's words
+        const long long dbase = __shfl_sync(0xffffffffu, dst0, s0);
+        for (uint32_t x = lane; x - lane < run; x += 32) {
+            int lo = s0;   // last lane of the segment whose window starts at or before word x
+            for (int step = seg_n >> 1; step >= 1; step >>= 1) {
+                const uint32_t e = __shfl_sync(0xffffffffu, excl, lo + step);
+                if (e <= x) lo += step;
+            }
+            const uint32_t e = __shfl_sync(0xffffffffu, excl, lo);
+            const long long sb = __shfl_sync(0xffffffffu, src0, lo);
+            if (x < run) P.pool[dbase + x] = __ldcg(P.pool + sb + (x - e));
+        }
+    }
+    if (!loaded) return;
+    P.wstart[k] = rel;
+    P.wend[k] = rel + len;
 }
 
 // Window index of the loaded input waveforms and a format check of every one of
@@ -952,7 +1072,19 @@ cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaSt
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    level_place_kernel<<<(unsigned)l.scan_tiles, kPlaceTile, 0, s>>>(p, l);
+    if (p.compact)
+        level_place_kernel<kPlaceTop><<<(unsigned)l.scan_tiles, kPlaceTile, 0, s>>>(p, l);
+    else
+        level_place_kernel<kPlaceFront><<<(unsigned)l.scan_tiles, kPlaceTile, 0, s>>>(p, l);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_level_compact(const DevParams &p, const LevelLaunch &l, const LevelLaunch &exact, cudaStream_t s) {
+    level_place_kernel<kPlaceExact><<<(unsigned)exact.scan_tiles, kPlaceTile, 0, s>>>(p, exact);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const unsigned blocks = (unsigned)((l.num_tiles + kLevelWarps - 1) / kLevelWarps);
+    level_pack_kernel<<<blocks, kLevelBlock, 0, s>>>(p, l);
     return cudaGetLastError();
 }
 

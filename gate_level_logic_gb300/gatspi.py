@@ -19,6 +19,7 @@ GATSPI_HOST, GATSPI_DEVICE = 0, 1
 GATSPI_FLAG_LEVEL_TIMING = 0x1
 GATSPI_FLAG_NO_GRAPH = 0x2
 GATSPI_FLAG_PULSE_PERCENT = 0x4
+GATSPI_FLAG_COMPACT = 0x8
 
 STATUS = {
     0: "GATSPI_OK", 1: "GATSPI_EINVAL", 2: "GATSPI_ENOMEM", 3: "GATSPI_EPOOL_OVERFLOW", 4: "GATSPI_EBADWAVE",

@@ -84,6 +84,7 @@ enum { GATSPI_HOST = 0, GATSPI_DEVICE = 1 };
 #define GATSPI_FLAG_LEVEL_TIMING 0x1u  /* record CUDA events around every level kernel (no graph) */
 #define GATSPI_FLAG_NO_GRAPH 0x2u      /* launch level kernels directly, no CUDA graph  */
 #define GATSPI_FLAG_PULSE_PERCENT 0x4u /* apply pulse_percent (else PATHPULSEPERCENT = 100) */
+#define GATSPI_FLAG_COMPACT 0x8u       /* pack every level to its exact size (see gatspi_simulate) */
 
 /*
  * Levelised netlist (all host arrays, copied by gatspi_create).
@@ -249,7 +250,16 @@ gatspi_status gatspi_load_testbench(gatspi_ctx *ctx, const int64_t *off, const i
 gatspi_status gatspi_simulate(gatspi_ctx *ctx, void *stream);
 
 /*
- * (continuation of gatspi_simulate) After each level's simulation kernel, that
+ * (continuation of gatspi_simulate) With GATSPI_FLAG_COMPACT every level is simulated
+ * into bound-sized regions placed down from the top of the pool, then a scan of the
+ * exact sizes and a copy pack it to exact size at the front, windows back to back,
+ * before the next level is planned: the pool then holds the waveforms themselves
+ * (exact sizes, as the page's counting pass gives, Section 3, Fig. 5) plus room for
+ * one level's bound-sized regions, at the cost of copying every level once.
+ * gatspi_views.pool_used then reports the most words any level needed (the packed
+ * front plus its bound-sized regions); EPOOL_OVERFLOW when that exceeds the pool.
+ *
+ * After each level's simulation kernel, that
  * level's TC and T1 are copied to pinned host memory on a side stream while the
  * later levels run (the page dumps its statistics asynchronously as well, Section 3);
  * `stream` waits for the copies at the end, so the statistics are on the host once

@@ -38,7 +38,7 @@ def run_gpu(Simulator, net, stim, pool_words, flags=0, repeat=1, pulse_percent=1
             sim.simulate()
         tc, t0, t1 = sim.toggle_stats()
         off, words = sim.export_all()
-        return dict(off=off, pool=words, tc=tc, t0=t0, t1=t1)
+        return dict(off=off, pool=words, tc=tc, t0=t0, t1=t1, pool_used=sim.pool_used())
 
 
 def assert_same(got, ref, what=""):
@@ -316,10 +316,59 @@ def test_single_waveform_and_window_export(gpu, oracle_lib):
 
 @pytest.mark.slow
 def test_1M_full(gpu, oracle_lib):
-    """The configuration bench.py times: 1M gates, 40 levels, 256 windows; whole pool."""
+    """The configuration bench.py times: 1M gates, 40 levels, 256 windows; whole pool,
+    also with every level packed to its exact size (GATSPI_FLAG_COMPACT)."""
+    from gate_level_logic_gb300 import gatspi
     net, stim = synth.make("1M")
     ref = oracle_lib.simulate(net, stim, threads=THREADS)
     assert_same(run_gpu(gpu, net, stim, pool_for(ref, net)), ref, "1M")
+    got = run_gpu(gpu, net, stim, pool_for(ref, net), flags=gatspi.GATSPI_FLAG_COMPACT, repeat=2)
+    assert_same(got, ref, "1M packed")
+    assert got["pool_used"] <= 1.3 * ref.pool.size
+
+
+@pytest.mark.parametrize("W", [1, 3, 16, 33, 256, 1025])
+@pytest.mark.parametrize("q", [100, 40])
+def test_compact_levels(gpu, oracle_lib, W, q):
+    """Every level packed to its exact size after it is simulated: the same waveforms
+    and statistics, the pool holding the waveforms plus one level's bound-sized
+    regions; two runs in a row (the packing rewrites the window index)."""
+    from gate_level_logic_gb300 import gatspi
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=2600, num_inputs=31, num_levels=7, seed=700 + W,
+                                                   cond_fraction=0.3))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=31, cycles=max(W, 300), period=400,
+                                                      activity=0.3, windows=W, seed=W, glitch_frac=0.3))
+    ref = oracle_lib.simulate(net, stim, threads=THREADS, pulse_percent=q)
+    got = run_gpu(gpu, net, stim, pool_for(ref, net), flags=gatspi.GATSPI_FLAG_COMPACT, repeat=2, pulse_percent=q)
+    assert_same(got, ref, "packed W=%d q=%d" % (W, q))
+    # the packed waveforms plus at most one level's bound-sized regions
+    P, G = net.num_inputs, net.num_gates
+    words = np.diff(ref.off).reshape(P + G, W).sum(axis=1)
+    lo = np.asarray(net.level_offsets)
+    level_bound = max(int(words[net.fanin_net[net.fanin_off[a]:net.fanin_off[b]]].sum()) + 3 * (b - a) * W
+                      for a, b in zip(lo[:-1], lo[1:]))
+    assert ref.pool.size <= got["pool_used"] <= ref.pool.size + level_bound
+
+
+def test_compact_pool_too_small(gpu, oracle_lib):
+    """A pool with room for the waveforms but not for a level's bound-sized regions
+    on top of the packed front: GATSPI_EPOOL_OVERFLOW, and the context still works
+    with a quiet stimulus."""
+    from gate_level_logic_gb300 import GatspiError, gatspi
+    net, stim = synth.make("tiny")
+    ref = oracle_lib.simulate(net, stim)
+    with gpu(net, stim.window_len, pool_words=int(ref.pool.size * 1.02) // 4 * 4 + 4,
+             flags=gatspi.GATSPI_FLAG_COMPACT) as sim:
+        sim.load(stim.pi_off, stim.pi_words)
+        sim.simulate()
+        with pytest.raises(GatspiError) as e:
+            sim.sync()
+        assert e.value.name == "GATSPI_EPOOL_OVERFLOW"
+        quiet = synth.from_waveforms([[[0, EOW]] for _ in range(net.num_inputs)], stim.window_len)
+        sim.load(quiet.pi_off, quiet.pi_words)
+        sim.simulate()
+        tc, _, _ = sim.toggle_stats()
+        assert (tc == 0).all()
 
 
 # ---- PATHPULSEPERCENT below 100 (several pending output events; transport at 0) ----
