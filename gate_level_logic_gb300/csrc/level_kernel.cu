@@ -117,6 +117,10 @@ __device__ __forceinline__ void next_arrival(uint32_t &p, int32_t &a, int32_t &n
     bool last = p + 2 >= len;                      // p + 1 is the EOW slot: no further transition
     int32_t t1 = nx;
     int32_t t2 = kPre ? t2pre : (last ? kEOW : __ldg(w + p + 2));
+    // a long window: on entering a new 32-byte sector, ask L1 for the next one, so that
+    // a lane running through hundreds of words does not wait for every sector in turn
+    if (!kPre && (((uintptr_t)(w + p + 2) & 31u) == 0) && p + 10 < len)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(w + p + 10));
     const int32_t d = par ? (int32_t)(drf >> 16) : (int32_t)(drf & 0xffffu);
     const int32_t lim = kFull ? d : reject_limit(d, q);
     if (!last && t2 - t1 < lim) {                   // the pulse [t1, t2) never reaches the pin
@@ -922,15 +926,26 @@ __global__ void __launch_bounds__(kLevelBlock) level_pack_kernel(const DevParams
     for (int s0 = 0; s0 < 32; s0 += seg_n) {
         const uint32_t run = __shfl_sync(0xffffffffu, excl + len, s0 + seg_n - 1);   // the segment's words
         const long long dbase = __shfl_sync(0xffffffffu, dst0, s0);
-        for (uint32_t x = lane; x - lane < run; x += 32) {
-            int lo = s0;   // last lane of the segment whose window starts at or before word x
-            for (int step = seg_n >> 1; step >= 1; step >>= 1) {
-                const uint32_t e = __shfl_sync(0xffffffffu, excl, lo + step);
-                if (e <= x) lo += step;
+        // four words per lane per round, their loads issued before their stores
+        for (uint32_t x0 = 0; x0 < run; x0 += 128) {
+            int32_t v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t x = x0 + 32u * u + lane;
+                int lo = s0;   // last lane of the segment whose window starts at or before word x
+                for (int step = seg_n >> 1; step >= 1; step >>= 1) {
+                    const uint32_t e = __shfl_sync(0xffffffffu, excl, lo + step);
+                    if (e <= x) lo += step;
+                }
+                const uint32_t e = __shfl_sync(0xffffffffu, excl, lo);
+                const long long sb = __shfl_sync(0xffffffffu, src0, lo);
+                v[u] = x < run ? __ldcg(P.pool + sb + (x - e)) : 0;
             }
-            const uint32_t e = __shfl_sync(0xffffffffu, excl, lo);
-            const long long sb = __shfl_sync(0xffffffffu, src0, lo);
-            if (x < run) P.pool[dbase + x] = __ldcg(P.pool + sb + (x - e));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t x = x0 + 32u * u + lane;
+                if (x < run) P.pool[dbase + x] = v[u];
+            }
         }
     }
     if (!loaded) return;
