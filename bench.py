@@ -494,7 +494,7 @@ def run_gpu(args):
     total_s = _max_over_ranks(dist, sum(step_ms) / 1e3)
     all_events = _sum_over_ranks(dist, events_per_step * args.steps)
     value = all_events / total_s
-    gate_cycles = net.num_gates * int(stim.window_cycles.sum())
+    gate_cycles = net.num_gates * int(stim.window_cycles[part.w0:part.w1].sum())   # this rank's windows
     lo = np.asarray(net.level_offsets)
     launches_per_step = int(2 * net.num_levels + np.count_nonzero(np.diff(lo)))
     gate_cycles_per_s = _sum_over_ranks(dist, gate_cycles * args.steps) / total_s
