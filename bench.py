@@ -430,7 +430,7 @@ def run_gpu(args):
             kw["cycles"] = world * int(kw.get("cycles", stim_kw["cycles"]))
             kw["windows"] = world * int(kw.get("windows", stim_kw["windows"]))
         net, stim = synth.make(workload, **kw)
-    flags = 0x8 if args.compact else 0       # GATSPI_FLAG_COMPACT
+    flags = (0x8 if args.compact else 0) | (0x10 if args.whole_windows else 0)   # COMPACT, WHOLE_WINDOWS
     pool_gb = args.pool_gb if args.pool_gb > 0 else {"1M": 48.0, "5M": 170.0, "scan500k": 64.0}[workload]
     pool_words = int(pool_gb * (1 << 30) / 4)
     part = shard.WindowShard(net, stim.window_len, world, rank, pool_words=pool_words, flags=flags,
@@ -438,6 +438,7 @@ def run_gpu(args):
     sim = part.sim
     stream = torch.cuda.current_stream()
     part.load(stim.pi_off, stim.pi_words, stream=stream)
+    lanes_per_window = sim.lanes_per_window()   # > 1: windows cut into time chunks
     rank_off, rank_words = shard.slice_windows(stim.pi_off, stim.pi_words, net.num_inputs, stim.num_windows,
                                                part.w0, part.w1)
     W = part.w1 - part.w0                           # this rank's windows
@@ -529,6 +530,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
         "config": workload_config(net, stim, args.pulse_percent, over, workload, world, args.compact),
+        "lanes_per_window": lanes_per_window,
         "gate_cycles_per_s": gate_cycles_per_s,
         "events_per_step": events_per_step,
         "pool_words_used": pool_used,
@@ -592,6 +594,9 @@ def main():
     ap.add_argument("--pool-gb", type=float, default=0.0, help="waveform pool (0: sized for the workload)")
     ap.add_argument("--compact", action="store_true",
                     help="pack every level to its exact size after simulating it (GATSPI_FLAG_COMPACT)")
+    ap.add_argument("--whole-windows", action="store_true",
+                    help="never cut a window into time chunks (GATSPI_FLAG_WHOLE_WINDOWS; matters at 16 windows "
+                         "or fewer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--windows", type=int, default=0, help="profiling only: number of cycle windows")

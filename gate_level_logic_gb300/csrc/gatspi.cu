@@ -69,6 +69,7 @@ struct gatspi_ctx {
     int32_t *dly = nullptr;
     int32_t *gate_order = nullptr;   // W < 32: every level's gates by pin count
     bool compact = false;            // GATSPI_FLAG_COMPACT
+    bool long_windows = false;       // the loaded inputs average kLongWindowWords words or more per window
     uint32_t *gexact = nullptr;      // compaction: exact words per (gate, group) of a level
     long long *old_base = nullptr;   // compaction: a level's bound-sized regions
     long long *level_bound = nullptr, *level_need = nullptr;   // compaction: [L]
@@ -147,6 +148,7 @@ struct gatspi_ctx {
         p.slots_per_gate = slots_per_gate;
         p.pulse_percent = pulse_percent;
         p.ranked = windows_ranked(W) ? 1 : 0;
+        p.chunks = chunks_per_window(W, pulse_percent, flags, long_windows);
         p.compact = compact ? 1 : 0;
         p.gexact = gexact;
         p.old_base = old_base;
@@ -173,6 +175,8 @@ gatspi_status validate(const gatspi_netlist *nl, const gatspi_config *cfg, long 
             return fail(GATSPI_EINVAL, "window %d: length must be in 1 .. 2^30", w);
     if ((cfg->flags & GATSPI_FLAG_PULSE_PERCENT) && (cfg->pulse_percent < 0 || cfg->pulse_percent > 100))
         return fail(GATSPI_EINVAL, "pulse_percent must be 0 .. 100");
+    if ((cfg->flags & GATSPI_FLAG_WHOLE_WINDOWS) && (cfg->flags & GATSPI_FLAG_CUT_WINDOWS))
+        return fail(GATSPI_EINVAL, "GATSPI_FLAG_WHOLE_WINDOWS and GATSPI_FLAG_CUT_WINDOWS exclude each other");
     if (G == 0) {
         *path_bound = 0;
         return GATSPI_OK;
@@ -258,6 +262,19 @@ void layout_delay_tables(const gatspi_netlist *nl, std::vector<int32_t> &out) {
     }
 }
 
+// After a load: whether its windows are long (level_chunk_kernel's rule); a change of
+// the kernel that simulates them makes the captured level graph stale.
+void set_long_windows(gatspi_ctx *c, long long window_words) {
+    const long long n = (long long)c->P * c->W;
+    const bool lw = n > 0 && window_words >= kLongWindowWords * n;
+    if (lw == c->long_windows) return;
+    c->long_windows = lw;
+    if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
+    if (c->graph) cudaGraphDestroy(c->graph);
+    c->graph_exec = nullptr;
+    c->graph = nullptr;
+}
+
 void free_all(gatspi_ctx *c) {
     if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
     if (c->graph) cudaGraphDestroy(c->graph);
@@ -289,6 +306,9 @@ gatspi_status read_status(gatspi_ctx *c) {
             return fail(GATSPI_EBADLUT, "gate %d window %d: every switching arc of an output change has no delay", st[1], st[2]);
         case GATSPI_ETIMEOUT:
             return fail(GATSPI_ETIMEOUT, "scan look-back stalled at level %d tile %d (waiting on tile %d)", st[1], st[2], st[3]);
+        case GATSPI_EINTERNAL:
+            return fail(GATSPI_EINTERNAL, "library fault: a chunk of gate %d window %d (lane %d) outgrew its bound",
+                        st[1], st[2], st[3]);
         default: return fail((gatspi_status)st[0], "device error %d", st[0]);
     }
 }
@@ -369,6 +389,12 @@ extern "C" {
 
 const char *gatspi_last_error(void) { return g_err.c_str(); }
 
+int32_t gatspi_lanes_per_window(const gatspi_ctx *c) {
+    if (!c) return 0;
+    const int k = chunks_per_window(c->W, c->pulse_percent, c->flags, c->long_windows);
+    return k > 1 ? k : 1;
+}
+
 const char *gatspi_status_name(gatspi_status s) {
     switch (s) {
         case GATSPI_OK: return "GATSPI_OK";
@@ -380,6 +406,7 @@ const char *gatspi_status_name(gatspi_status s) {
         case GATSPI_ESTATE: return "GATSPI_ESTATE";
         case GATSPI_EBADLUT: return "GATSPI_EBADLUT";
         case GATSPI_ETIMEOUT: return "GATSPI_ETIMEOUT";
+        case GATSPI_EINTERNAL: return "GATSPI_EINTERNAL";
     }
     return "GATSPI_UNKNOWN";
 }
@@ -600,6 +627,7 @@ gatspi_status gatspi_load_waveforms(gatspi_ctx *c, const int64_t *off, const int
                     c->path_delay_bound);
     gatspi_status ist = input_stats(c, s);
     if (ist != GATSPI_OK) return ist;
+    set_long_windows(c, (long long)nwords);
     c->loaded = true;
     return GATSPI_OK;
 }
@@ -650,6 +678,7 @@ gatspi_status gatspi_load_testbench(gatspi_ctx *c, const int64_t *off, const int
     if (st[0] != 0) return read_status(c);
     gatspi_status ist = input_stats(c, s);
     if (ist != GATSPI_OK) return ist;
+    set_long_windows(c, (long long)nwords + 2 * W * P);   // transitions, plus a head and an EOW per window
     c->loaded = true;
     return GATSPI_OK;
 }
@@ -672,7 +701,8 @@ gatspi_status gatspi_simulate(gatspi_ctx *c, void *stream) {
     }
     if (c->flags & (GATSPI_FLAG_NO_GRAPH | GATSPI_FLAG_LEVEL_TIMING)) return enqueue_levels(c, s);
     if (!c->graph_exec) {
-        CUDA_TRY(cudaStreamCreateWithFlags(&c->capture_stream, cudaStreamNonBlocking), "creating the capture stream");
+        if (!c->capture_stream)
+            CUDA_TRY(cudaStreamCreateWithFlags(&c->capture_stream, cudaStreamNonBlocking), "creating the capture stream");
         CUDA_TRY(cudaStreamBeginCapture(c->capture_stream, cudaStreamCaptureModeThreadLocal), "beginning capture");
         gatspi_status st = enqueue_levels(c, c->capture_stream);
         cudaGraph_t g = nullptr;

@@ -228,47 +228,78 @@ __device__ __forceinline__ bool table_fits(const Pin (&pin)[N], const int32_t *&
 // pins form a bit mask, the delay lookup and the pin advance serve the first
 // switching pin through a lane-selected pin state, and only simultaneous
 // switching of several pins takes an extra (rare) loop.
-template <int N, bool kFull, bool kTable>
+// kChunk: one time chunk of the window (level_chunk_kernel).  A chunk that does not
+// start the window starts from each pin's entry in effect at its cut (pin[i].p, set
+// by the caller), with no output entry pending, and writes no head: its entries go to
+// gout[1], gout[2], ... (gout is moved down by the output value at the cut, so that
+// the parity of an entry's index stays its value).  Every chunk stops before the
+// first arrival at or after tend, writes no EOW, and returns in len the index of its
+// last entry, in tc its entries (stores less cancels) and in t1 its signed sum of
+// clipped entries, without the final adjustment.
+template <int N, bool kFull, bool kTable, bool kChunk = false>
 __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb, const PinTab &tab, uint32_t tt,
                                                const int32_t *__restrict__ D, int32_t Lw, int32_t *__restrict__ gout,
-                                               int32_t q) {
+                                               int32_t q, bool from_start = true, int32_t tend = kEOW,
+                                               int32_t cap = 0) {
     LaneResult r{0, 0, 0, 0};
+    // a chunk holds at most cap entries (its pins' transitions): a write past them
+    // would be a fault of the library's bound, so it is recorded instead of made
+    int32_t wcap = 0;
+    bool over = false;
     auto put = [&](int32_t k, int32_t v) {
-        gout[k] = v;
+        if (!kChunk || k <= wcap) gout[k] = v;
+        else over = true;
     };
     auto get = [&](int32_t k) { return gout[k]; };   // this lane's own words
 
-    // initial values: pin index 1 when the waveform starts with -1.  The truth table
-    // was re-indexed at create by the pin weights, so its index is the pin values
-    // read as a binary number, first pin most significant.
-    // every pin's first four words are loaded at once (the head, the first transition
-    // and the word after it, whichever head the wave has); a wave holds at least its
-    // head and EOW, so words 0 and 1 always exist
-    int32_t x[N][4];
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        x[i][0] = __ldg(pin[i].w);
-        x[i][1] = __ldg(pin[i].w + 1);
-        x[i][2] = pin[i].len > 2 ? __ldg(pin[i].w + 2) : kEOW;
-        x[i][3] = pin[i].len > 3 ? __ldg(pin[i].w + 3) : kEOW;
-    }
     uint32_t vbits = 0;
     int32_t t2first[N];
+    if (!kChunk || from_start) {
+        // initial values: pin index 1 when the waveform starts with -1.  The truth
+        // table was re-indexed at create by the pin weights, so its index is the pin
+        // values read as a binary number, first pin most significant.
+        // every pin's first four words are loaded at once (the head, the first
+        // transition and the word after it, whichever head the wave has); a wave
+        // holds at least its head and EOW, so words 0 and 1 always exist
+        int32_t x[N][4];
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const bool one = x[i][0] == -1;
-        pin[i].p = one ? 1u : 0u;
-        vbits |= pin[i].p << (N - 1 - i);
-        pin[i].nx = one ? x[i][2] : x[i][1];          // w[p + 1]
-        t2first[i] = one ? x[i][3] : x[i][2];         // w[p + 2]
+        for (int i = 0; i < N; ++i) {
+            x[i][0] = __ldg(pin[i].w);
+            x[i][1] = __ldg(pin[i].w + 1);
+            x[i][2] = pin[i].len > 2 ? __ldg(pin[i].w + 2) : kEOW;
+            x[i][3] = pin[i].len > 3 ? __ldg(pin[i].w + 3) : kEOW;
+        }
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const bool one = x[i][0] == -1;
+            pin[i].p = one ? 1u : 0u;
+            vbits |= pin[i].p << (N - 1 - i);
+            pin[i].nx = one ? x[i][2] : x[i][1];          // w[p + 1]
+            t2first[i] = one ? x[i][3] : x[i][2];         // w[p + 2]
+        }
+    } else {
+        // a cut: every pin's entry in effect is given, and entry p + 1 exists (at
+        // worst the EOW)
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const uint32_t p = pin[i].p;
+            vbits |= (p & 1u) << (N - 1 - i);
+            pin[i].nx = __ldg(pin[i].w + p + 1);
+            t2first[i] = p + 2 < pin[i].len ? __ldg(pin[i].w + p + 2) : kEOW;
+        }
     }
     const int32_t y0 = (tt >> vbits) & 1;
     int32_t po = y0;        // index of the last output entry
     int32_t top = 0;        // O[po]
     int32_t second = 0;     // O[po - 1] (read only after a store, or after a cancel when kFull is false)
     int32_t t1acc = 0;      // signed sum of clipped entries: time at 1 before the final adjustment
-    put(0, y0 ? -1 : 0);
-    if (y0) put(1, 0);
+    wcap = y0 + cap;
+    if (!kChunk || from_start) {
+        put(0, y0 ? -1 : 0);
+        if (y0) put(1, 0);
+    } else {
+        gout -= y0;
+    }
 
     bool lutbad = false;
 #pragma unroll
@@ -286,7 +317,7 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb,
         int32_t t = pin[0].a;
 #pragma unroll
         for (int i = 1; i < N; ++i) t = min(t, pin[i].a);
-        if (t == kEOW) break;
+        if (kChunk ? t >= tend : t == kEOW) break;
 
         // every pin arriving at t switches together (bit N-1-i = pin i); each one's
         // entry index moves on when the pin is advanced below
@@ -340,39 +371,51 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb,
             advance_pin<N, kFull, kTable>(pin, lb, tab, N - __ffs(mm), vbits, q);
     }
     if (lutbad) r.err = GATSPI_EBADLUT;
-    put(po + 1, kEOW);
-    r.len = po + 2;
-    r.tc = po - y0;
-    r.t1 = t1acc + ((po & 1) ? Lw : 0);
+    if (kChunk && over) r.err = GATSPI_EINTERNAL;
+    if constexpr (kChunk) {
+        r.len = po;
+        r.tc = po - y0;
+        r.t1 = t1acc;
+    } else {
+        put(po + 1, kEOW);
+        r.len = po + 2;
+        r.tc = po - y0;
+        r.t1 = t1acc + ((po & 1) ? Lw : 0);
+    }
     return r;
 }
 
-template <int N, bool kFull>
+template <int N, bool kFull, bool kChunk = false>
 __device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS],
-                                                 const PinTab &tab, int32_t Lw, int32_t *gout) {
+                                                 const PinTab &tab, int32_t Lw, int32_t *gout, bool from_start = true,
+                                                 int32_t tend = kEOW, int32_t cap = 0) {
     Pin pin[N];
 #pragma unroll
     for (int i = 0; i < N; ++i) pin[i] = pins[i];
     const uint32_t tt = (uint32_t)gd.y >> 8;
     const long long dly = (long long)(uint32_t)gd.z | ((long long)gd.w << 32);
     if constexpr (N == 1) {
-        return run_lane<N, kFull, false>(pin, pin[0].w, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent);
+        return run_lane<N, kFull, false, kChunk>(pin, pin[0].w, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent,
+                                                 from_start, tend, cap);
     } else {
         const int32_t *lb;
         if (table_fits<N>(pin, lb))
-            return run_lane<N, kFull, true>(pin, lb, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent);
-        return run_lane<N, kFull, false>(pin, lb, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent);
+            return run_lane<N, kFull, true, kChunk>(pin, lb, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent,
+                                                    from_start, tend, cap);
+        return run_lane<N, kFull, false, kChunk>(pin, lb, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent,
+                                                 from_start, tend, cap);
     }
 }
 
-template <bool kFull>
+template <bool kFull, bool kChunk = false>
 __device__ __forceinline__ LaneResult dispatch(const DevParams &P, int4 gd, Pin (&pins)[GATSPI_MAX_PINS],
-                                               const PinTab &tab, int32_t Lw, int32_t *gout) {
+                                               const PinTab &tab, int32_t Lw, int32_t *gout, bool from_start = true,
+                                               int32_t tend = kEOW, int32_t cap = 0) {
     switch (gd.y & 7) {
-        case 1: return simulate_gate<1, kFull>(P, gd, pins, tab, Lw, gout);
-        case 2: return simulate_gate<2, kFull>(P, gd, pins, tab, Lw, gout);
-        case 3: return simulate_gate<3, kFull>(P, gd, pins, tab, Lw, gout);
-        default: return simulate_gate<4, kFull>(P, gd, pins, tab, Lw, gout);
+        case 1: return simulate_gate<1, kFull, kChunk>(P, gd, pins, tab, Lw, gout, from_start, tend, cap);
+        case 2: return simulate_gate<2, kFull, kChunk>(P, gd, pins, tab, Lw, gout, from_start, tend, cap);
+        case 3: return simulate_gate<3, kFull, kChunk>(P, gd, pins, tab, Lw, gout, from_start, tend, cap);
+        default: return simulate_gate<4, kFull, kChunk>(P, gd, pins, tab, Lw, gout, from_start, tend, cap);
     }
 }
 
@@ -869,6 +912,266 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     }
 }
 
+// Windows cut into time chunks (fewer than 32 windows, PATHPULSEPERCENT = 100): with
+// few windows a lane runs its gate through a long stretch of the testbench and a level
+// lasts as long as its busiest gate's serial chain.  Here a warp takes one gate and
+// gives each of its windows K = 32 / W lanes; lane k of a window simulates the window
+// from its k-th cut to the next.  A cut T is a time at which the gate is quiet: no
+// pin has a transition in [T - M1, T + M2), M1 = the largest wire delay of its pins +
+// its largest gate delay, M2 = that wire delay + 1.  Then, whatever happened before,
+// every pin's entry in effect at T is its last transition before T (a pulse around T
+// is wider than any reject limit, so none is swallowed across it), every arrival
+// before T comes from a transition before T - M1 and every arrival at or after T from
+// one at or after T + M2, and every output entry made before T lies before T, so no
+// later event can cancel it (at q = 100 an entry is cancelled only by an event
+// earlier than the entry).  The simulation from T on therefore needs only the pins'
+// entries in effect and the output value at T (the truth table of the pins' values),
+// and yields exactly the entries, toggles and time at 1 of the whole window's run.
+// Lane k looks for its cut from k * Lw / K on (the first quiet time, within a few
+// dozen transitions and before the next lane's start); a lane that finds none leaves
+// its stretch to the lane before.  Each chunk writes its entries into its own part of
+// the window's slot (as many words as its pins have transitions in the chunk); after
+// the event loops the warp moves the entries of every chunk after the first down
+// behind the previous one's, in ascending order (each word moves to a lower or equal
+// address, so no word is overwritten before it is read), and closes the window with
+// its EOW.
+constexpr int kCutSteps = 64;   // transitions a cut search may pass before it gives up
+
+// First index in [lo, hi] whose word is >= v; w[hi] >= v must hold (the EOW does).
+__device__ __forceinline__ uint32_t lower_bound_words(const int32_t *w, uint32_t lo, uint32_t hi, long long v) {
+    while (lo < hi) {
+        const uint32_t mid = lo + ((hi - lo) >> 1);
+        if ((long long)__ldg(w + mid) < v) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// The first quiet time at or after T0 (see above) and every pin's entry in effect
+// there, or false when none is found before Tnext or within kCutSteps transitions.
+template <int N>
+__device__ __forceinline__ bool find_cut(Pin (&pins)[GATSPI_MAX_PINS], long long T0, long long Tnext, int32_t M1,
+                                         int32_t M2, int32_t &T, uint32_t (&pos)[GATSPI_MAX_PINS]) {
+    long long cur = T0 - M1 > 1 ? T0 - M1 : 1;   // where the quiet stretch would start
+    if (cur + M1 >= Tnext) return false;
+    uint32_t q[N];
+    long long v[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        q[i] = lower_bound_words(pins[i].w, 1u, pins[i].len - 1u, cur);   // transitions are >= 1
+        v[i] = __ldg(pins[i].w + q[i]);
+    }
+    for (int step = 0; step < kCutSteps; ++step) {
+        long long m = v[0];
+#pragma unroll
+        for (int i = 1; i < N; ++i) m = m < v[i] ? m : v[i];
+        if (m >= cur + M1 + M2) {                    // [cur, cur + M1 + M2) holds no transition
+            T = (int32_t)(cur + M1);
+#pragma unroll
+            for (int i = 0; i < N; ++i) pos[i] = q[i] - 1u;
+            return true;
+        }
+        cur = m + 1;
+        if (cur + M1 >= Tnext) return false;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (v[i] == m) {                         // m < EOW here, so q[i] + 1 is in the window
+                ++q[i];
+                v[i] = __ldg(pins[i].w + q[i]);
+            }
+    }
+    return false;
+}
+
+// 8 blocks per SM: 64 registers, which the cut search and the moves use (9 blocks at
+// 56 registers spill and run 2-8 % slower)
+constexpr int kChunkMinBlocks = 8;
+__global__ void __launch_bounds__(kLevelBlock, kChunkMinBlocks) level_chunk_kernel(const DevParams P,
+                                                                                  const LevelLaunch L) {
+    __shared__ int2 pin_hot[kLevelWarps][GATSPI_MAX_PINS * 32];
+    __shared__ uint32_t pin_end[kLevelWarps][GATSPI_MAX_PINS * 32];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int gl = blockIdx.x * kLevelWarps + warp;        // one gate per warp
+    if (gl >= L.num_gates) return;
+    // after an error (read now) the warp reads no waveform and writes nothing: the
+    // window index of this level's sources may then never have been written
+    const bool skip = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
+    const int K = P.chunks;
+    const int W = P.W;
+    const int rank = lane / K;
+    const int k = lane - rank * K;
+    const int lead = rank * K < 32 ? rank * K : 31;         // the window's first lane
+    const bool loaded = rank < W;
+    const int g = L.gate_begin + gl;
+    const long long net = (long long)P.num_inputs + g;
+    const int w = loaded ? (P.ranked ? (int)__ldg(P.perm + (long long)gl * W + rank) : rank) : 0;
+
+    const int4 gd = __ldg(P.gate_desc + 3 * (long long)g);
+    const int4 sv = __ldg(P.gate_desc + 3 * (long long)g + 1);
+    const int4 dv = __ldg(P.gate_desc + 3 * (long long)g + 2);
+    const int n = gd.y & 7;
+    const int32_t Lw = loaded ? __ldg(P.window_len + w) : 0;
+    Pin pins[GATSPI_MAX_PINS];
+    uint32_t bound = 0;
+    if (loaded) {
+        switch (n) {
+            case 1: bound = load_pins<1>(P, sv, dv, w, pins); break;
+            case 2: bound = load_pins<2>(P, sv, dv, w, pins); break;
+            case 3: bound = load_pins<3>(P, sv, dv, w, pins); break;
+            default: bound = load_pins<4>(P, sv, dv, w, pins); break;
+        }
+    }
+    const uint32_t gofs = __ldg(P.goff + (long long)gl * (P.ngroups + 1));
+    const long long base = __ldg(P.net_base + net) + gofs;
+
+    // the window's slot: a scan of the windows' bounds in rank order
+    const uint32_t bw = loaded && k == 0 ? bound : 0u;
+    const uint32_t bexcl = warp_incl_scan(bw, lane) - bw;
+    const uint32_t slotrel = __shfl_sync(0xffffffffu, bexcl, lead);
+    int32_t *slot = P.pool + base + slotrel;
+
+    // the margins of a quiet time: the largest wire delay of the pins and the largest
+    // finite delay of the gate's table (read by the whole warp)
+    int32_t wdmax = 0;
+    {
+        const int d4[GATSPI_MAX_PINS] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+        for (int i = 0; i < GATSPI_MAX_PINS; ++i)
+            if (i < n) wdmax = max(wdmax, max(d4[i] & 0xffff, (int)((uint32_t)d4[i] >> 16)));
+    }
+    uint32_t dgmax = 0;
+    {
+        const long long dly = (long long)(uint32_t)gd.z | ((long long)gd.w << 32);
+        const int entries = (2 * n) << n;
+        for (int e = lane; e < entries; e += 32) {
+            const int32_t d = __ldg(P.dly_data + dly + e);
+            if (d != kNoArc) dgmax = max(dgmax, (uint32_t)d);
+        }
+        dgmax = __reduce_max_sync(0xffffffffu, dgmax);
+    }
+    const int32_t M1 = wdmax + (int32_t)dgmax, M2 = wdmax + 1;
+
+    // this lane's cut and every pin's entry in effect there (lane 0 of a window: its
+    // start)
+    bool valid = false;
+    int32_t T = 0;
+    uint32_t pos[GATSPI_MAX_PINS] = {0, 0, 0, 0};
+    if (loaded && !skip) {
+        if (k == 0) {
+            valid = true;
+#pragma unroll
+            for (int i = 0; i < GATSPI_MAX_PINS; ++i)
+                if (i < n) pos[i] = __ldg(pins[i].w) == -1 ? 1u : 0u;
+        } else {
+            const long long T0 = (long long)k * Lw / K;
+            const long long Tn = k + 1 < K ? (long long)(k + 1) * Lw / K : (long long)Lw;
+            switch (n) {
+                case 1: valid = find_cut<1>(pins, T0, Tn, M1, M2, T, pos); break;
+                case 2: valid = find_cut<2>(pins, T0, Tn, M1, M2, T, pos); break;
+                case 3: valid = find_cut<3>(pins, T0, Tn, M1, M2, T, pos); break;
+                default: valid = find_cut<4>(pins, T0, Tn, M1, M2, T, pos); break;
+            }
+        }
+    }
+    // the chunk runs to the next valid cut of the window (or to the window's end)
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+    const unsigned seg = (K == 32 ? 0xffffffffu : ((1u << K) - 1u)) << (lead & 31);
+    const unsigned above = lane == 31 ? 0u : ~((2u << lane) - 1u);
+    const unsigned later = vmask & seg & above;
+    const int nxt = later ? __ffs(later) - 1 : lane;
+    const int32_t tend_n = __shfl_sync(0xffffffffu, T, nxt);
+    const int32_t tend = later ? tend_n : kEOW;
+    uint32_t cb = 0;   // transitions of the chunk over its pins: a bound on its entries
+#pragma unroll
+    for (int i = 0; i < GATSPI_MAX_PINS; ++i) {
+        const uint32_t pe_n = __shfl_sync(0xffffffffu, pos[i], nxt);
+        if (valid && i < n) cb += (later ? pe_n : pins[i].len - 2u) - pos[i];
+    }
+    // chunk regions inside the slot: chunk 0 from word 0 (head and entries), chunk k
+    // from word 2 + the bounds of the chunks before it
+    const uint32_t cbx = valid ? cb : 0u;
+    const uint32_t cexcl = warp_incl_scan(cbx, lane) - cbx;
+    const uint32_t off = 2u + cexcl - __shfl_sync(0xffffffffu, cexcl, lead);
+
+    LaneResult res{0, 0, 0, 0};
+    if (valid) {
+        const PinTab tab{&pin_hot[warp][lane], &pin_end[warp][lane]};
+#pragma unroll
+        for (int i = 0; i < GATSPI_MAX_PINS; ++i) pins[i].p = pos[i];
+        res = dispatch<true, true>(P, gd, pins, tab, Lw, k == 0 ? slot : slot + off - 1, k == 0, tend, (int32_t)cb);
+        if (res.err) raise_error(P.status, res.err, g, w, k);
+    }
+    // exact places: chunk k's entries follow the head and the entries of the chunks
+    // before it (never more than the chunk's bound, even after a recorded fault)
+    const int32_t cnt = valid ? min(res.tc, (int32_t)cb) : 0;
+    const int32_t y0w = __shfl_sync(0xffffffffu, res.len - res.tc, lead);   // the window's initial value
+    const uint32_t incl = warp_incl_scan((uint32_t)cnt, lane);
+    const uint32_t E = (uint32_t)y0w + 1u + (incl - (uint32_t)cnt) - (__shfl_sync(0xffffffffu, incl, lead) -
+                                                                      (uint32_t)__shfl_sync(0xffffffffu, cnt, lead));
+    const uint32_t Eend = __shfl_sync(0xffffffffu, E + (uint32_t)cnt, (lead + K - 1) & 31);
+
+    // The moves of every window of the warp as one list: word i belongs to the chunk
+    // (a lane with k >= 1) whose run of the list starts last at or before i; within
+    // a window the list ascends by destination.  kMoveWords words per lane and round:
+    // all loads of a round before its stores.
+    constexpr int kMoveWords = 4;
+    const uint32_t m = loaded && k > 0 ? (uint32_t)cnt : 0u;
+    const uint32_t mincl = warp_incl_scan(m, lane);
+    const uint32_t M = mincl - m;
+    const uint32_t total = __shfl_sync(0xffffffffu, mincl, 31);
+    const uint32_t shift = (k == 0 ? E : off) - E;          // source - destination of this chunk's words
+    int32_t *wslot = P.pool + base;
+    __syncwarp();
+    if (!skip) {
+        for (uint32_t i0 = 0; i0 < total; i0 += 32u * kMoveWords) {
+            int32_t v[kMoveWords];
+            uint32_t dst[kMoveWords];
+#pragma unroll
+            for (int u = 0; u < kMoveWords; ++u) {
+                const uint32_t i = i0 + 32u * u + (uint32_t)lane;
+                int c = 0;
+#pragma unroll
+                for (int stp = 16; stp >= 1; stp >>= 1)
+                    if (__shfl_sync(0xffffffffu, M, c + stp) <= i) c += stp;
+                const uint32_t d = __shfl_sync(0xffffffffu, slotrel + E, c) + (i - __shfl_sync(0xffffffffu, M, c));
+                const uint32_t sh = __shfl_sync(0xffffffffu, shift, c);
+                dst[u] = d;
+                v[u] = i < total ? __ldcg(wslot + d + sh) : 0;
+            }
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < kMoveWords; ++u)
+                if (i0 + 32u * u + (uint32_t)lane < total) wslot[dst[u]] = v[u];
+            __syncwarp();
+        }
+    }
+    const bool head = loaded && k == 0 && !skip;
+    if (head) {
+        slot[Eend] = kEOW;
+        const uint32_t len = Eend + 1u;
+        P.wstart[net * W + w] = gofs + slotrel;
+        P.wend[net * W + w] = gofs + slotrel + len;
+        P.wlen8[net * P.w8stride + w] = (uint8_t)min(len, 255u);
+    }
+    // TC and T1 of the gate: every chunk's entries and signed sums, and each window's
+    // final value over its length
+    long long tcs = cnt;
+    long long t1s = (valid ? (long long)res.t1 : 0) + (head && ((Eend - 1u) & 1u) ? (long long)Lw : 0);
+    long long ws_len = head ? (long long)Eend + 1 : 0;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        tcs += __shfl_xor_sync(0xffffffffu, tcs, o);
+        t1s += __shfl_xor_sync(0xffffffffu, t1s, o);
+        ws_len += __shfl_xor_sync(0xffffffffu, ws_len, o);
+    }
+    if (lane == 0 && !skip) {
+        atomicAdd(P.tc + g, (unsigned long long)tcs);
+        atomicAdd(P.t1 + g, (unsigned long long)t1s);
+        if (P.compact) P.gexact[(long long)gl * P.ngroups] = (uint32_t)ws_len;
+    }
+}
+
 // Packing of a level's outputs (compaction): every window moves from its bound-sized
 // slot in the level's scratch to its place in the gate's exact region, windows in
 // rank order and back to back; the window index is rewritten relative to the packed
@@ -1104,6 +1407,11 @@ cudaError_t launch_level_compact(const DevParams &p, const LevelLaunch &l, const
 }
 
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
+    if (p.chunks > 1 && p.pulse_percent == 100) {   // one warp per gate
+        if (l.num_gates > 0)
+            level_chunk_kernel<<<(unsigned)((l.num_gates + kLevelWarps - 1) / kLevelWarps), kLevelBlock, 0, s>>>(p, l);
+        return cudaGetLastError();
+    }
     const unsigned blocks = (unsigned)((l.num_tiles + kLevelWarps - 1) / kLevelWarps);
     if (p.pulse_percent == 100)
         level_kernel<true><<<blocks, kLevelBlock, 0, s>>>(p, l);
@@ -1125,6 +1433,7 @@ cudaError_t set_level_smem_limit() {
     // GB300 (28 already gives 100 KB; 0 gives 8 KB and a single block per SM).
     cudaError_t e = cudaFuncSetAttribute(level_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 20);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(level_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 20);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(level_chunk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 20);
     // The planning kernel's dynamic shared memory limit is an attribute of the kernel,
     // shared by every context of the process: it is always set to what the largest
     // window count needs, so that no context lowers it below another's launches.

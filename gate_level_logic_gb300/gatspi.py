@@ -20,10 +20,12 @@ GATSPI_FLAG_LEVEL_TIMING = 0x1
 GATSPI_FLAG_NO_GRAPH = 0x2
 GATSPI_FLAG_PULSE_PERCENT = 0x4
 GATSPI_FLAG_COMPACT = 0x8
+GATSPI_FLAG_WHOLE_WINDOWS = 0x10
+GATSPI_FLAG_CUT_WINDOWS = 0x20
 
 STATUS = {
     0: "GATSPI_OK", 1: "GATSPI_EINVAL", 2: "GATSPI_ENOMEM", 3: "GATSPI_EPOOL_OVERFLOW", 4: "GATSPI_EBADWAVE",
-    5: "GATSPI_ECUDA", 6: "GATSPI_ESTATE", 7: "GATSPI_EBADLUT", 8: "GATSPI_ETIMEOUT",
+    5: "GATSPI_ECUDA", 6: "GATSPI_ESTATE", 7: "GATSPI_EBADLUT", 8: "GATSPI_ETIMEOUT", 9: "GATSPI_EINTERNAL",
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
@@ -81,6 +83,7 @@ SIGNATURES = {
     "gatspi_load_testbench": (ctypes.c_int, [_p, _p, _p, ctypes.c_size_t, ctypes.c_int, _p]),
     "gatspi_simulate": (ctypes.c_int, [_p, _p]),
     "gatspi_sync": (ctypes.c_int, [_p]),
+    "gatspi_lanes_per_window": (ctypes.c_int32, [_p]),
     "gatspi_toggle_stats": (ctypes.c_int, [_p, _p, _p, _p]),
     "gatspi_toggle_stats_host": (ctypes.c_int, [_p, ctypes.POINTER(_p), ctypes.POINTER(_p), ctypes.POINTER(ctypes.c_int64)]),
     "gatspi_input_stats": (ctypes.c_int, [_p, _p, _p, _p]),
@@ -153,6 +156,12 @@ def gatspi_simulate(ctx: int, stream: int = 0):
 
 def gatspi_sync(ctx: int):
     _check(library().gatspi_sync(_p(ctx)))
+
+
+def gatspi_lanes_per_window(ctx: int) -> int:
+    """Lanes the next simulate gives each window: 32 // W when it cuts windows into
+    time chunks, else 1."""
+    return int(library().gatspi_lanes_per_window(_p(ctx)))
 
 
 def gatspi_toggle_stats(ctx: int, tc: int, t0: int, t1: int):

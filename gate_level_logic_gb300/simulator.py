@@ -214,6 +214,11 @@ class Simulator:
         _c.gatspi_export_windows(self.ctx, sel.ctypes.data, sel.size, off.ctypes.data, words.ctypes.data, words.size)
         return off, words[:int(off[-1])]
 
+    def lanes_per_window(self) -> int:
+        """Lanes the next simulate gives each window (32 // W when windows are cut into
+        time chunks, else 1)."""
+        return _c.gatspi_lanes_per_window(self.ctx)
+
     def net_digests(self, net_begin: int = 0, num_nets: int = None, with_words: bool = False):
         """uint64 [num_nets]: the 64-bit FNV-1a digest of each net's waveforms in
         window order (gatspi_net_digests); with ``with_words`` also the int64 number

@@ -74,7 +74,9 @@ typedef enum {
     GATSPI_ECUDA = 5,           /* a CUDA runtime call failed                        */
     GATSPI_ESTATE = 6,          /* call out of order (e.g. simulate before load)     */
     GATSPI_EBADLUT = 7,         /* every switching arc of an output change is NO_ARC */
-    GATSPI_ETIMEOUT = 8         /* a device-side wait gave up (scan look-back)       */
+    GATSPI_ETIMEOUT = 8,        /* a device-side wait gave up (scan look-back)       */
+    GATSPI_EINTERNAL = 9        /* a kernel found one of the library's own bounds
+                                   broken (a library fault); the access was not made  */
 } gatspi_status;
 
 /* Where a buffer passed to gatspi_load_waveforms lives. */
@@ -85,6 +87,8 @@ enum { GATSPI_HOST = 0, GATSPI_DEVICE = 1 };
 #define GATSPI_FLAG_NO_GRAPH 0x2u      /* launch level kernels directly, no CUDA graph  */
 #define GATSPI_FLAG_PULSE_PERCENT 0x4u /* apply pulse_percent (else PATHPULSEPERCENT = 100) */
 #define GATSPI_FLAG_COMPACT 0x8u       /* pack every level to its exact size (see gatspi_simulate) */
+#define GATSPI_FLAG_WHOLE_WINDOWS 0x10u /* never cut a window into time chunks (see gatspi_simulate) */
+#define GATSPI_FLAG_CUT_WINDOWS 0x20u   /* cut windows into time chunks whatever their length */
 
 /*
  * Levelised netlist (all host arrays, copied by gatspi_create).
@@ -264,6 +268,23 @@ gatspi_status gatspi_simulate(gatspi_ctx *ctx, void *stream);
  * later levels run (the page dumps its statistics asynchronously as well, Section 3);
  * `stream` waits for the copies at the end, so the statistics are on the host once
  * the stream has finished and gatspi_toggle_stats reads no device memory.
+ *
+ * With 16 windows or fewer at PATHPULSEPERCENT = 100, when the windows are long (the
+ * last load averaged 32 words or more per (input, window); always with
+ * GATSPI_FLAG_CUT_WINDOWS, never with GATSPI_FLAG_WHOLE_WINDOWS; the two flags
+ * exclude each other: EINVAL at create), a lane would run its gate through a long
+ * window alone, so each gate takes one warp and each of its windows 32 / W lanes,
+ * every lane simulating the window between two cuts: times at which none of the
+ * gate's pins has a transition within its largest wire delay after, nor within that
+ * wire delay plus its largest gate delay before.  At such a time every pin's entry in
+ * effect is its last transition, no pulse spans it, and no output entry made before
+ * it can be cancelled by an event after it, so the stretches simulate independently
+ * and give exactly the whole window's waveform, toggles and time at 1 (the page runs
+ * windows, not stretches of one, in parallel: Section 4, cycle parallelism).  A lane
+ * that finds no cut near its share leaves its stretch to the lane before.  The warp
+ * then moves the stretches' entries together inside the window's slot.  A load that
+ * changes whether the windows are long makes the next simulate capture its graph
+ * again.
  */
 
 /*
@@ -272,6 +293,13 @@ gatspi_status gatspi_simulate(gatspi_ctx *ctx, void *stream);
  * this is that wait, plus the report of the device status word.
  */
 gatspi_status gatspi_sync(gatspi_ctx *ctx);
+
+/*
+ * Lanes the next gatspi_simulate gives each window: 32 / num_windows when it cuts the
+ * windows into time chunks (see gatspi_simulate), else 1; 0 for a NULL ctx.  Decided
+ * by the flags, the window count, PATHPULSEPERCENT and the last load.
+ */
+int32_t gatspi_lanes_per_window(const gatspi_ctx *ctx);
 
 /*
  * SAIF-style toggle statistics per gate, summed over windows (host arrays [G]; any
