@@ -1114,8 +1114,8 @@ __global__ void __launch_bounds__(kLevelBlock, kChunkMinBlocks) level_chunk_kern
     // The moves of every window of the warp as one list: word i belongs to the chunk
     // (a lane with k >= 1) whose run of the list starts last at or before i; within
     // a window the list ascends by destination.  kMoveWords words per lane and round:
-    // all loads of a round before its stores.
-    constexpr int kMoveWords = 4;
+    // all loads of a round before its stores (8: 0-3 % faster than 4, 2 % faster than 2).
+    constexpr int kMoveWords = 8;
     const uint32_t m = loaded && k > 0 ? (uint32_t)cnt : 0u;
     const uint32_t mincl = warp_incl_scan(m, lane);
     const uint32_t M = mincl - m;
