@@ -68,6 +68,7 @@ struct gatspi_ctx {
     int4 *gate_desc = nullptr;
     int32_t *dly = nullptr;
     int32_t *gate_order = nullptr;   // W < 32: every level's gates by pin count
+    int32_t *heavy_order = nullptr;  // W <= 16: a level's gates, heaviest first (level_chunk_kernel)
     bool compact = false;            // GATSPI_FLAG_COMPACT
     bool long_windows = false;       // the loaded inputs average kLongWindowWords words or more per window
     uint32_t *gexact = nullptr;      // compaction: exact words per (gate, group) of a level
@@ -123,6 +124,7 @@ struct gatspi_ctx {
         p.gate_desc = gate_desc;
         p.dly_data = dly;
         p.gate_order = gate_order;
+        p.heavy_order = heavy_order;
         p.pool = pool;
         p.pool_words = pool_words;
         p.net_base = net_base;
@@ -285,7 +287,7 @@ void free_all(gatspi_ctx *c) {
     if (c->dump_stream) cudaStreamDestroy(c->dump_stream);
     if (c->tc_host) cudaFreeHost(c->tc_host);
     if (c->t1_host) cudaFreeHost(c->t1_host);
-    void *ptrs[] = {c->gexact, c->old_base, c->level_bound, c->level_need, c->gate_desc, c->dly, c->gate_order, c->net_base, c->wstart, c->wend, c->wlen8, c->perm, c->goff,
+    void *ptrs[] = {c->gexact, c->old_base, c->level_bound, c->level_need, c->gate_desc, c->dly, c->gate_order, c->heavy_order, c->net_base, c->wstart, c->wend, c->wlen8, c->perm, c->goff,
                     c->window_len, c->tc, c->t1,
                     c->tile_status, c->tickets, c->level_base, c->status, c->load_off, c->max_time,
                     c->win_start, c->tc_in, c->t1_in};
@@ -513,6 +515,9 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
                         if (nl->type_num_pins[nl->gate_type[g]] == n) order[k++] = g;
             }
             CUDA_TRY(dev_alloc(&c->gate_order, order.size()), "allocating the gate order");
+            if (c->W <= 16)
+                CUDA_TRY(dev_alloc(&c->heavy_order, (size_t)std::max<long long>(c->max_level_gates, 1)),
+                         "allocating the gate order");
             CUDA_TRY(cudaMemcpy(c->gate_order, order.data(), order.size() * sizeof(int32_t), cudaMemcpyHostToDevice),
                      "uploading the gate order");
         }

@@ -49,6 +49,7 @@ struct DevParams {
                                //     {source net of pin 0..3}, {wire rise | fall << 16 of pin 0..3};
                                //     truth-table bit k = output for pin values k (first pin most significant)
     const int32_t *dly_data;   // per-instance conditional delay tables
+    int32_t *heavy_order;      // [gates of the level]: level_chunk_kernel's gate order, heaviest first
     const int32_t *gate_order; // [G] or null: with W < 32 (several gates per warp) the gates of every
                                //     level in the order the simulation kernel takes them, by pin count
     // waveform store: waveform (net, w) is pool[net_base[net] + wstart[k] .. net_base[net] + wend[k]),

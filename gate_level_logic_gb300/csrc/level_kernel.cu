@@ -986,14 +986,45 @@ __device__ __forceinline__ bool find_cut(Pin (&pins)[GATSPI_MAX_PINS], long long
 // 8 blocks per SM: 64 registers, which the cut search and the moves use (9 blocks at
 // 56 registers spill and run 2-8 % slower)
 constexpr int kChunkMinBlocks = 8;
+// The order in which level_chunk_kernel takes a level's gates: heaviest first (by the
+// size of the gate's output region, the sum of its windows' bounds, in power-of-two
+// classes), so that the longest warps start in the first wave and the light ones fill
+// in around them instead of a heavy gate starting last and holding the level up.  One
+// block; the order within a class is whatever the atomics give (it changes nothing in
+// the results, only which warp runs when).
+constexpr int kOrderThreads = 1024;
+__global__ void __launch_bounds__(kOrderThreads) level_order_kernel(const DevParams P, const LevelLaunch L) {
+    __shared__ uint32_t cursor[33];
+    const int n = L.num_gates;
+    if (threadIdx.x < 33) cursor[threadIdx.x] = 0;
+    __syncthreads();
+    auto cls = [&](int gl) {   // 0 for the largest regions
+        const uint32_t size = __ldg(P.goff + (long long)gl * (P.ngroups + 1) + P.ngroups);
+        return size ? __clz(size) : 32;
+    };
+    for (int gl = threadIdx.x; gl < n; gl += kOrderThreads) atomicAdd(&cursor[cls(gl)], 1u);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t run = 0;
+        for (int c = 0; c < 33; ++c) {
+            const uint32_t v = cursor[c];
+            cursor[c] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int gl = threadIdx.x; gl < n; gl += kOrderThreads) P.heavy_order[atomicAdd(&cursor[cls(gl)], 1u)] = gl;
+}
+
 __global__ void __launch_bounds__(kLevelBlock, kChunkMinBlocks) level_chunk_kernel(const DevParams P,
                                                                                   const LevelLaunch L) {
     __shared__ int2 pin_hot[kLevelWarps][GATSPI_MAX_PINS * 32];
     __shared__ uint32_t pin_end[kLevelWarps][GATSPI_MAX_PINS * 32];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int gl = blockIdx.x * kLevelWarps + warp;        // one gate per warp
-    if (gl >= L.num_gates) return;
+    const int tile = blockIdx.x * kLevelWarps + warp;      // one gate per warp, heaviest first
+    if (tile >= L.num_gates) return;
+    const int gl = __ldg(P.heavy_order + tile);
     // after an error (read now) the warp reads no waveform and writes nothing: the
     // window index of this level's sources may then never have been written
     const bool skip = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
@@ -1407,9 +1438,11 @@ cudaError_t launch_level_compact(const DevParams &p, const LevelLaunch &l, const
 }
 
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
-    if (p.chunks > 1 && p.pulse_percent == 100) {   // one warp per gate
-        if (l.num_gates > 0)
+    if (p.chunks > 1 && p.pulse_percent == 100) {   // one warp per gate, heaviest first
+        if (l.num_gates > 0) {
+            level_order_kernel<<<1, kOrderThreads, 0, s>>>(p, l);
             level_chunk_kernel<<<(unsigned)((l.num_gates + kLevelWarps - 1) / kLevelWarps), kLevelBlock, 0, s>>>(p, l);
+        }
         return cudaGetLastError();
     }
     const unsigned blocks = (unsigned)((l.num_tiles + kLevelWarps - 1) / kLevelWarps);
