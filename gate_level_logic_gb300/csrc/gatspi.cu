@@ -69,8 +69,13 @@ struct gatspi_ctx {
     int32_t *dly = nullptr;
     int32_t *gate_order = nullptr;   // W < 32: every level's gates by pin count
     int32_t *heavy_order = nullptr;  // W <= 16: a level's gates, heaviest first (level_chunk_kernel)
+    uint32_t *seg_items = nullptr, *seg_count = nullptr, *seg_cnt = nullptr;   // W = 1: segments of heavy gates
+    int32_t *seg_counter = nullptr;
+    int32_t resident_warps = 0;
     bool compact = false;            // GATSPI_FLAG_COMPACT
     bool long_windows = false;       // the loaded inputs average kLongWindowWords words or more per window
+    bool split_windows = false;      // one window of kSplitWindowWords words or more per input: segments
+    bool dense_windows = false;      // kDenseWindowWords words or more per input window
     uint32_t *gexact = nullptr;      // compaction: exact words per (gate, group) of a level
     long long *old_base = nullptr;   // compaction: a level's bound-sized regions
     long long *level_bound = nullptr, *level_need = nullptr;   // compaction: [L]
@@ -125,6 +130,15 @@ struct gatspi_ctx {
         p.dly_data = dly;
         p.gate_order = gate_order;
         p.heavy_order = heavy_order;
+        // segments of one window: when its windows are cut and very long, or cut by force
+        const bool seg = chunks_per_window(W, pulse_percent, flags, long_windows) > 1 &&
+                         (split_windows || (flags & GATSPI_FLAG_CUT_WINDOWS));
+        p.seg_items = seg ? seg_items : nullptr;
+        p.seg_kernel = seg || (W >= 2 && dense_windows) ? 1 : 0;
+        p.seg_count = seg_count;
+        p.seg_cnt = seg_cnt;
+        p.seg_counter = seg_counter;
+        p.resident_warps = resident_warps;
         p.pool = pool;
         p.pool_words = pool_words;
         p.net_base = net_base;
@@ -264,13 +278,18 @@ void layout_delay_tables(const gatspi_netlist *nl, std::vector<int32_t> &out) {
     }
 }
 
-// After a load: whether its windows are long (level_chunk_kernel's rule); a change of
-// the kernel that simulates them makes the captured level graph stale.
+// After a load: whether its windows are long (level_chunk_kernel's rule) and, with one
+// window, long enough for segments; a change of the kernel that simulates them makes
+// the captured level graph stale.
 void set_long_windows(gatspi_ctx *c, long long window_words) {
     const long long n = (long long)c->P * c->W;
     const bool lw = n > 0 && window_words >= kLongWindowWords * n;
-    if (lw == c->long_windows) return;
+    const bool sw = n > 0 && c->W == 1 && window_words >= kSplitWindowWords * n;
+    const bool dw = n > 0 && window_words >= kDenseWindowWords * n;
+    if (lw == c->long_windows && sw == c->split_windows && dw == c->dense_windows) return;
     c->long_windows = lw;
+    c->split_windows = sw;
+    c->dense_windows = dw;
     if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
     if (c->graph) cudaGraphDestroy(c->graph);
     c->graph_exec = nullptr;
@@ -287,7 +306,7 @@ void free_all(gatspi_ctx *c) {
     if (c->dump_stream) cudaStreamDestroy(c->dump_stream);
     if (c->tc_host) cudaFreeHost(c->tc_host);
     if (c->t1_host) cudaFreeHost(c->t1_host);
-    void *ptrs[] = {c->gexact, c->old_base, c->level_bound, c->level_need, c->gate_desc, c->dly, c->gate_order, c->heavy_order, c->net_base, c->wstart, c->wend, c->wlen8, c->perm, c->goff,
+    void *ptrs[] = {c->gexact, c->old_base, c->level_bound, c->level_need, c->gate_desc, c->dly, c->gate_order, c->heavy_order, c->seg_items, c->seg_count, c->seg_cnt, c->seg_counter, c->net_base, c->wstart, c->wend, c->wlen8, c->perm, c->goff,
                     c->window_len, c->tc, c->t1,
                     c->tile_status, c->tickets, c->level_base, c->status, c->load_off, c->max_time,
                     c->win_start, c->tc_in, c->t1_in};
@@ -342,6 +361,9 @@ gatspi_status enqueue_levels(gatspi_ctx *c, cudaStream_t s) {
     CUDA_TRY(cudaMemsetAsync(c->tc, 0, sizeof(unsigned long long) * std::max(c->G, 1), s), "clearing TC");
     CUDA_TRY(cudaMemsetAsync(c->t1, 0, sizeof(unsigned long long) * std::max(c->G, 1), s), "clearing T1");
     const int scans = c->compact ? 2 : 1;   // compaction scans every level twice
+    if (c->seg_counter)   // a run that stopped on an error may have left segments uncounted
+        CUDA_TRY(cudaMemsetAsync(c->seg_counter, 0, sizeof(int32_t) * (size_t)std::max<long long>(c->max_level_gates, 1), s),
+                 "clearing the segment counters");
     CUDA_TRY(cudaMemsetAsync(c->tile_status, 0, sizeof(unsigned long long) * std::max<long long>(scans * c->total_tiles, 1),
                              s), "clearing the scan state");
     CUDA_TRY(cudaMemsetAsync(c->tickets, 0, sizeof(int32_t) * std::max(scans * c->L, 1), s), "clearing the tile tickets");
@@ -518,6 +540,18 @@ gatspi_status gatspi_create(const gatspi_netlist *nl, const gatspi_config *cfg, 
             if (c->W <= 16)
                 CUDA_TRY(dev_alloc(&c->heavy_order, (size_t)std::max<long long>(c->max_level_gates, 1)),
                          "allocating the gate order");
+            if (c->W == 1) {
+                const size_t mg = (size_t)std::max<long long>(c->max_level_gates, 1);
+                CUDA_TRY(dev_alloc(&c->seg_items, mg + kExtraSegments), "allocating the segment list");
+                CUDA_TRY(dev_alloc(&c->seg_count, (size_t)1), "allocating the segment list");
+                CUDA_TRY(dev_alloc(&c->seg_cnt, mg * kMaxSegments), "allocating the segment list");
+                CUDA_TRY(dev_alloc(&c->seg_counter, mg), "allocating the segment list");
+                CUDA_TRY(cudaMemset(c->seg_counter, 0, mg * sizeof(int32_t)), "clearing the segment counters");
+                // 8 blocks of 4 warps per SM (level_chunk_kernel's occupancy)
+                int sms = 0;
+                CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device), "reading the SM count");
+                c->resident_warps = std::max(sms, 1) * 32;
+            }
             CUDA_TRY(cudaMemcpy(c->gate_order, order.data(), order.size() * sizeof(int32_t), cudaMemcpyHostToDevice),
                      "uploading the gate order");
         }

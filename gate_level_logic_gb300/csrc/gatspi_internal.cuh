@@ -50,6 +50,14 @@ struct DevParams {
                                //     truth-table bit k = output for pin values k (first pin most significant)
     const int32_t *dly_data;   // per-instance conditional delay tables
     int32_t *heavy_order;      // [gates of the level]: level_chunk_kernel's gate order, heaviest first
+    // one window cut into time chunks: a heavy gate's window split into segments, one
+    // warp each (null unless W = 1)
+    uint32_t *seg_items;       // [gates of the level + kExtraSegments]: gate | segment << 24 | (segments - 1) << 28
+    uint32_t *seg_count;       // [1]: items of the level
+    uint32_t *seg_cnt;         // [gates of the level * kMaxSegments]: entries of every segment (bit 31: y0)
+    int32_t *seg_counter;      // [gates of the level]: segments finished (reset by the last)
+    int32_t resident_warps;    // warps the GPU holds at once in level_chunk_kernel
+    int32_t seg_kernel;        // level_chunk_kernel<true> (segments possible) instead of <false>
     const int32_t *gate_order; // [G] or null: with W < 32 (several gates per warp) the gates of every
                                //     level in the order the simulation kernel takes them, by pin count
     // waveform store: waveform (net, w) is pool[net_base[net] + wstart[k] .. net_base[net] + wend[k]),
@@ -113,6 +121,16 @@ int plan_words(int W);
 // GATSPI_FLAG_CUT_WINDOWS; never with GATSPI_FLAG_WHOLE_WINDOWS.  0: every window in
 // one lane.
 constexpr long long kLongWindowWords = 32;
+constexpr int kMaxSegments = 8;        // warps one gate's window may take (one window)
+constexpr int kExtraSegments = 4096;   // segments beyond one per gate, per level
+constexpr unsigned long long kSegmentMinWords = 16384;  // bound words a segment needs at least
+// One window is split into segments (several warps per heavy gate) when the loaded
+// inputs average this many words or more per input, or whenever windows are cut by
+// GATSPI_FLAG_CUT_WINDOWS; shorter windows gain less than the segment code costs.
+constexpr long long kSplitWindowWords = 4096;
+// From this many words per input window on, cut windows of 2 .. 16 run faster in the
+// segment-capable instantiation of level_chunk_kernel (measured; nothing is split).
+constexpr long long kDenseWindowWords = 100;
 inline int chunks_per_window(int W, int pulse_percent, uint32_t flags, bool long_windows) {
     const bool cut = (flags & GATSPI_FLAG_CUT_WINDOWS) || (long_windows && !(flags & GATSPI_FLAG_WHOLE_WINDOWS));
     return W >= 1 && W <= 16 && pulse_percent == 100 && cut ? 32 / W : 0;

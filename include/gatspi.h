@@ -88,7 +88,8 @@ enum { GATSPI_HOST = 0, GATSPI_DEVICE = 1 };
 #define GATSPI_FLAG_PULSE_PERCENT 0x4u /* apply pulse_percent (else PATHPULSEPERCENT = 100) */
 #define GATSPI_FLAG_COMPACT 0x8u       /* pack every level to its exact size (see gatspi_simulate) */
 #define GATSPI_FLAG_WHOLE_WINDOWS 0x10u /* never cut a window into time chunks (see gatspi_simulate) */
-#define GATSPI_FLAG_CUT_WINDOWS 0x20u   /* cut windows into time chunks whatever their length */
+#define GATSPI_FLAG_CUT_WINDOWS 0x20u   /* cut windows into time chunks whatever their length (one
+                                           window: heavy gates also split into segments) */
 
 /*
  * Levelised netlist (all host arrays, copied by gatspi_create).
@@ -282,7 +283,11 @@ gatspi_status gatspi_simulate(gatspi_ctx *ctx, void *stream);
  * and give exactly the whole window's waveform, toggles and time at 1 (the page runs
  * windows, not stretches of one, in parallel: Section 4, cycle parallelism).  A lane
  * that finds no cut near its share leaves its stretch to the lane before.  The warp
- * then moves the stretches' entries together inside the window's slot.  A load that
+ * then moves the stretches' entries together inside the window's slot.  Each level's
+ * gates are taken heaviest first.  With one window of 4096 words or more per input
+ * (or with GATSPI_FLAG_CUT_WINDOWS), a gate whose work exceeds its level's share per
+ * warp the GPU holds takes up to 8 warps, each a segment of the window between two
+ * such times, and the last warp to finish moves the segments together.  A load that
  * changes whether the windows are long makes the next simulate capture its graph
  * again.
  */

@@ -190,3 +190,51 @@ def test_cut_window_flags_exclude_each_other(gpu):
     with pytest.raises(GatspiError) as e:
         gpu(net, stim.window_len, pool_words=1 << 16, flags=cut | whole)
     assert e.value.name == "GATSPI_EINVAL"
+
+
+def test_one_window_segments(gpu, oracle_lib):
+    """One window: a gate whose work exceeds its level's share per resident warp takes
+    up to 8 warps, one per segment of the window between two quiet times, and the last
+    warp to finish moves the segments together.  A lone gate per level always takes all
+    8; a few heavy gates among many light ones take several; replays and a second
+    context must find every per-gate counter reset."""
+    cut, _ = flags()
+    tt = np.array([0, 1, 1, 0], np.uint8)                       # XOR2
+    D = np.full((8, 2), 7, np.int32)
+    one = single_gate(tt, 2, D, wire_rise=[1, 2], wire_fall=[2, 1])
+    stim1 = synth.generate_stimulus(synth.StimulusSpec(num_inputs=2, cycles=3000, period=200, activity=0.7,
+                                                       windows=1, seed=81, glitch_frac=0.3))
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=4000, num_inputs=16, num_levels=8, seed=82,
+                                                   cond_fraction=0.3, fanout_mean=6.0))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=16, cycles=4000, period=300, activity=0.6,
+                                                      windows=1, seed=82, glitch_frac=0.2))
+    for nt, st in ((one, stim1), (net, stim)):
+        ref = oracle_lib.simulate(nt, st, threads=THREADS)
+        for fl in (cut, 0):
+            assert_same(run_gpu(gpu, nt, st, pool_for(ref, nt), flags=fl, repeat=3), ref, "flags %d" % fl)
+
+
+def test_one_window_segments_after_a_stalled_scan(gpu, oracle_lib):
+    """A stalled scan stops a one-window run in the middle of a level whose heavy gates
+    are split into segments; the next simulates of the same context (direct and from
+    the graph) must be exact, so no segment counter may carry over."""
+    from gate_level_logic_gb300 import GatspiError, gatspi
+    cut, _ = flags()
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=9000, num_inputs=40, num_levels=6, seed=83,
+                                                   fanout_mean=5.0))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=40, cycles=2000, period=300, activity=0.5,
+                                                      windows=1, seed=83, glitch_frac=0.2))
+    ref = oracle_lib.simulate(net, stim, threads=THREADS)
+    with gpu(net, stim.window_len, pool_words=pool_for(ref, net), flags=cut) as sim:
+        sim.load(stim.pi_off, stim.pi_words)
+        assert sim.lanes_per_window() == 32
+        gatspi.gatspi_inject_scan_stall(sim.ctx, 3, 20_000_000)   # 1500 gates: two scan tiles
+        sim.simulate()
+        with pytest.raises(GatspiError) as e:
+            sim.sync()
+        assert e.value.name == "GATSPI_ETIMEOUT", str(e.value)
+        for _ in range(2):
+            sim.simulate()
+            tc, t0, t1 = sim.toggle_stats()
+            off, pool = sim.export_all()
+            assert_same(dict(off=off, pool=pool, tc=tc, t0=t0, t1=t1), ref, "after the stall")
