@@ -42,6 +42,12 @@
 // loop keeps only the pins' next arrivals in registers and most of the SM's L1 is
 // left to the source waveforms.  No warp waits for another.
 //
+// With 16 windows or fewer and long windows, level_chunk_kernel replaces level_kernel:
+// one warp per gate, each window cut at quiet times of the gate into stretches that
+// the lanes simulate in parallel (see there); level_order_kernel orders the gates
+// heaviest first and, with one window, splits the heaviest into segments of several
+// warps.
+//
 // No kernel traps: a missing delay arc, pool overflow or a stalled look-back sets the
 // device status word and the kernels carry on without writing out of bounds.  Input
 // waveforms are checked when they are loaded (load_index_kernel, the testbench cut);
@@ -912,7 +918,7 @@ __global__ void __launch_bounds__(kLevelBlock, kLevelMinBlocks) level_kernel(con
     }
 }
 
-// Windows cut into time chunks (fewer than 32 windows, PATHPULSEPERCENT = 100): with
+// Windows cut into time chunks (16 windows or fewer, PATHPULSEPERCENT = 100): with
 // few windows a lane runs its gate through a long stretch of the testbench and a level
 // lasts as long as its busiest gate's serial chain.  Here a warp takes one gate and
 // gives each of its windows K = 32 / W lanes; lane k of a window simulates the window
