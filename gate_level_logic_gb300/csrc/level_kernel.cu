@@ -152,7 +152,8 @@ __device__ __forceinline__ void next_arrival(uint32_t &p, int32_t &a, int32_t &n
 // shared loads and writes it back with one store instead of moving every field
 // through per-pin selects, and the table is small enough to leave most of the SM's
 // L1 to the source waveforms.  A lane whose waveforms lie 2^32 words apart or more
-// cannot use 32-bit offsets; a warp with such a lane keeps its pins in registers.
+// (pools beyond 16 GiB) counts each pin's offsets from its own window instead, and the
+// step selects the switching pin's window pointer (kPinsFar).
 struct PinTab {
     int2 *hot;          // [pin * 32 + lane]: {entry offset, next word}
     uint32_t *end;      // [pin * 32 + lane]
@@ -174,49 +175,44 @@ __device__ __forceinline__ int32_t arc_delay(const int32_t *__restrict__ D, uint
     return __ldg(D + ((((uint32_t)i << 1) | (uint32_t)e_out) << N | vbits));
 }
 
+// Where a multi-pin lane's pin table counts its offsets from (kPins): kPinsNear, from
+// the lowest of the lane's waveform pointers, one pointer for every pin (the lane's
+// waveforms lie within 2^32 words); kPinsFar, from each pin's own window, whose
+// pointer the step selects among the pins' (a few more instructions, no limit on how
+// far apart the sources lie).  A one-pin cell keeps its pin in registers (kPinsOne).
+enum { kPinsOne = 0, kPinsNear = 1, kPinsFar = 2 };
+
 // Take the transition of pin k (chosen per lane) that has just arrived and find the
 // pin's next arrival.  vbits holds every pin's value after the step.
-template <int N, bool kFull, bool kTable>
+template <int N, bool kFull, int kPins>
 __device__ __forceinline__ void advance_pin(Pin (&pin)[N], const int32_t *lb, const PinTab &tab, int k,
                                             uint32_t vbits, int32_t q) {
     if constexpr (N == 1) {
         ++pin[0].p;
         next_arrival<kFull>(pin[0].p, pin[0].a, pin[0].nx, pin[0].w, pin[0].len, pin[0].drf, pin[0].p & 1u, q);
-    } else if constexpr (kTable) {
+    } else {
         const int2 h = tab.hot[k * 32];
         const uint32_t end = tab.end[k * 32];
         uint32_t drf = pin[0].drf;
+        const int32_t *base = kPins == kPinsNear ? lb : pin[0].w;
 #pragma unroll
         for (int i = 1; i < N; ++i)
-            if (k == i) drf = pin[i].drf;
+            if (k == i) {
+                drf = pin[i].drf;
+                if constexpr (kPins == kPinsFar) base = pin[i].w;
+            }
         uint32_t off = (uint32_t)h.x + 1u;
         int32_t nx = h.y, a;
-        next_arrival<kFull>(off, a, nx, lb, end, drf, (vbits >> (N - 1 - k)) & 1u, q);
+        next_arrival<kFull>(off, a, nx, base, end, drf, (vbits >> (N - 1 - k)) & 1u, q);
         tab.hot[k * 32] = make_int2((int32_t)off, nx);
 #pragma unroll
         for (int i = 0; i < N; ++i)
             if (k == i) pin[i].a = a;
-    } else {
-        // registers: the pin's state is gathered and written back with predicated
-        // moves so that the lanes of a warp advance different pins together
-        Pin s = pin[0];
-#pragma unroll
-        for (int i = 1; i < N; ++i)
-            if (k == i) s = pin[i];
-        ++s.p;
-        next_arrival<kFull>(s.p, s.a, s.nx, s.w, s.len, s.drf, s.p & 1u, q);
-#pragma unroll
-        for (int i = 0; i < N; ++i)
-            if (k == i) {
-                pin[i].p = s.p;
-                pin[i].a = s.a;
-                pin[i].nx = s.nx;
-            }
     }
 }
 
 // Whether a lane's pins can use 32-bit offsets from the lowest of their waveform
-// pointers (that pointer in lb).
+// pointers (that pointer in lb): kPinsNear, else kPinsFar.
 template <int N>
 __device__ __forceinline__ bool table_fits(const Pin (&pin)[N], const int32_t *&lb) {
     lb = pin[0].w;
@@ -242,7 +238,7 @@ __device__ __forceinline__ bool table_fits(const Pin (&pin)[N], const int32_t *&
 // first arrival at or after tend, writes no EOW, and returns in len the index of its
 // last entry, in tc its entries (stores less cancels) and in t1 its signed sum of
 // clipped entries, without the final adjustment.
-template <int N, bool kFull, bool kTable, bool kChunk = false>
+template <int N, bool kFull, int kPins, bool kChunk = false>
 __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb, const PinTab &tab, uint32_t tt,
                                                const int32_t *__restrict__ D, int32_t Lw, int32_t *__restrict__ gout,
                                                int32_t q, bool from_start = true, int32_t tend = kEOW,
@@ -312,8 +308,8 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb,
     for (int i = 0; i < N; ++i) {
         next_arrival<kFull, true>(pin[i].p, pin[i].a, pin[i].nx, pin[i].w, pin[i].len, pin[i].drf,
                                         pin[i].p & 1u, q, t2first[i]);
-        if constexpr (N > 1 && kTable) {
-            const uint32_t o = (uint32_t)(pin[i].w - lb);
+        if constexpr (N > 1) {
+            const uint32_t o = kPins == kPinsNear ? (uint32_t)(pin[i].w - lb) : 0u;
             tab.hot[i * 32] = make_int2((int32_t)(o + pin[i].p), pin[i].nx);
             tab.end[i * 32] = o + pin[i].len;
         }
@@ -372,9 +368,9 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb,
             second = top;
             top = to;
         }
-        advance_pin<N, kFull, kTable>(pin, lb, tab, k, vbits, q);
+        advance_pin<N, kFull, kPins>(pin, lb, tab, k, vbits, q);
         for (uint32_t mm = more; mm; mm &= mm - 1u)   // lowest bit first
-            advance_pin<N, kFull, kTable>(pin, lb, tab, N - __ffs(mm), vbits, q);
+            advance_pin<N, kFull, kPins>(pin, lb, tab, N - __ffs(mm), vbits, q);
     }
     if (lutbad) r.err = GATSPI_EBADLUT;
     if (kChunk && over) r.err = GATSPI_EINTERNAL;
@@ -401,15 +397,15 @@ __device__ __forceinline__ LaneResult simulate_gate(const DevParams &P, int4 gd,
     const uint32_t tt = (uint32_t)gd.y >> 8;
     const long long dly = (long long)(uint32_t)gd.z | ((long long)gd.w << 32);
     if constexpr (N == 1) {
-        return run_lane<N, kFull, false, kChunk>(pin, pin[0].w, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent,
-                                                 from_start, tend, cap);
+        return run_lane<N, kFull, kPinsOne, kChunk>(pin, pin[0].w, tab, tt, P.dly_data + dly, Lw, gout,
+                                                    P.pulse_percent, from_start, tend, cap);
     } else {
         const int32_t *lb;
         if (table_fits<N>(pin, lb))
-            return run_lane<N, kFull, true, kChunk>(pin, lb, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent,
+            return run_lane<N, kFull, kPinsNear, kChunk>(pin, lb, tab, tt, P.dly_data + dly, Lw, gout,
+                                                         P.pulse_percent, from_start, tend, cap);
+        return run_lane<N, kFull, kPinsFar, kChunk>(pin, lb, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent,
                                                     from_start, tend, cap);
-        return run_lane<N, kFull, false, kChunk>(pin, lb, tab, tt, P.dly_data + dly, Lw, gout, P.pulse_percent,
-                                                 from_start, tend, cap);
     }
 }
 
@@ -1383,44 +1379,45 @@ __global__ void __launch_bounds__(kLevelBlock, kChunkMinBlocks) level_chunk_kern
 
     // a segment of a split window (one window): its statistics, its entry count, then
     // the join by the last of the gate's warps to finish
-    if constexpr (!kSeg) return;
+    if constexpr (kSeg) {
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        tcs += __shfl_xor_sync(0xffffffffu, tcs, o);
-        t1s += __shfl_xor_sync(0xffffffffu, t1s, o);
-    }
-    if (lane == 0) {
-        if (!skip) {
-            atomicAdd(P.tc + g, (unsigned long long)tcs);
-            atomicAdd(P.t1 + g, (unsigned long long)t1s);
+        for (int o = 16; o >= 1; o >>= 1) {
+            tcs += __shfl_xor_sync(0xffffffffu, tcs, o);
+            t1s += __shfl_xor_sync(0xffffffffu, t1s, o);
         }
-        P.seg_cnt[(long long)gl * kMaxSegments + q] = (Eend - first) | (q == 0 && y0w ? 0x80000000u : 0u);
-    }
-    __threadfence();   // this warp's words and count before its arrival
-    __syncwarp();
-    int arrived = 0;
-    if (lane == 0) arrived = atomicAdd(P.seg_counter + gl, 1);
-    const bool last = __shfl_sync(0xffffffffu, arrived, 0) == Q - 1;
-    if (!last) return;
-    __threadfence();
-    const bool bad = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
-    if (lane == 0) P.seg_counter[gl] = 0;   // ready for the next level
-    if (bad) return;
-    const uint32_t cj = lane < Q ? __ldcg(P.seg_cnt + (long long)gl * kMaxSegments + lane) : 0u;
-    const uint32_t y0 = __shfl_sync(0xffffffffu, cj, 0) >> 31;
-    const uint32_t nj = cj & 0x7fffffffu;
-    const uint32_t jincl = warp_incl_scan(nj, lane);
-    const uint32_t Ej = y0 + 1u + jincl - nj;               // segment j's exact first word
-    const uint32_t Sj = lane == 0 ? Ej : Rj;                // where its entries are now
-    move_runs(P.pool + base, slotrel + Ej, Sj - Ej, lane >= 1 && lane < Q ? nj : 0u, lane);
-    const uint32_t Ew = y0 + 1u + __shfl_sync(0xffffffffu, jincl, 31);   // the window's EOW word
-    if (lane == 0) {
-        slot[Ew] = kEOW;
-        P.wstart[net * W + w] = gofs + slotrel;
-        P.wend[net * W + w] = gofs + slotrel + Ew + 1u;
-        P.wlen8[net * P.w8stride + w] = (uint8_t)min(Ew + 1u, 255u);
-        if ((Ew - 1u) & 1u) atomicAdd(P.t1 + g, (unsigned long long)Lw);
-        if (P.compact) P.gexact[(long long)gl * P.ngroups] = Ew + 1u;
+        if (lane == 0) {
+            if (!skip) {
+                atomicAdd(P.tc + g, (unsigned long long)tcs);
+                atomicAdd(P.t1 + g, (unsigned long long)t1s);
+            }
+            P.seg_cnt[(long long)gl * kMaxSegments + q] = (Eend - first) | (q == 0 && y0w ? 0x80000000u : 0u);
+        }
+        __threadfence();   // this warp's words and count before its arrival
+        __syncwarp();
+        int arrived = 0;
+        if (lane == 0) arrived = atomicAdd(P.seg_counter + gl, 1);
+        const bool last = __shfl_sync(0xffffffffu, arrived, 0) == Q - 1;
+        if (!last) return;
+        __threadfence();
+        const bool bad = __shfl_sync(0xffffffffu, lane == 0 ? ld_status(P.status) : 0, 0) != 0;
+        if (lane == 0) P.seg_counter[gl] = 0;   // ready for the next level
+        if (bad) return;
+        const uint32_t cj = lane < Q ? __ldcg(P.seg_cnt + (long long)gl * kMaxSegments + lane) : 0u;
+        const uint32_t y0 = __shfl_sync(0xffffffffu, cj, 0) >> 31;
+        const uint32_t nj = cj & 0x7fffffffu;
+        const uint32_t jincl = warp_incl_scan(nj, lane);
+        const uint32_t Ej = y0 + 1u + jincl - nj;               // segment j's exact first word
+        const uint32_t Sj = lane == 0 ? Ej : Rj;                // where its entries are now
+        move_runs(P.pool + base, slotrel + Ej, Sj - Ej, lane >= 1 && lane < Q ? nj : 0u, lane);
+        const uint32_t Ew = y0 + 1u + __shfl_sync(0xffffffffu, jincl, 31);   // the window's EOW word
+        if (lane == 0) {
+            slot[Ew] = kEOW;
+            P.wstart[net * W + w] = gofs + slotrel;
+            P.wend[net * W + w] = gofs + slotrel + Ew + 1u;
+            P.wlen8[net * P.w8stride + w] = (uint8_t)min(Ew + 1u, 255u);
+            if ((Ew - 1u) & 1u) atomicAdd(P.t1 + g, (unsigned long long)Lw);
+            if (P.compact) P.gexact[(long long)gl * P.ngroups] = Ew + 1u;
+        }
     }
 }
 
