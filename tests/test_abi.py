@@ -109,3 +109,18 @@ def test_invalid_config_and_pool_are_rejected(lib):
 def test_status_names(lib):
     for code, name in lib.STATUS.items():
         assert lib.gatspi_status_name(code) == name
+
+
+def test_window_cutting_flags_on_the_host(lib):
+    """The two window-cutting flags exclude each other (rejected before any device
+    call), the binding's flag values are the header's, and the lanes query answers 0
+    for no context."""
+    net, _ = synth.make("tiny")
+    nl, cfg, keep = _struct(lib, net, W=1)
+    cfg.flags = lib.GATSPI_FLAG_WHOLE_WINDOWS | lib.GATSPI_FLAG_CUT_WINDOWS
+    rc, msg = _create_status(lib, nl, cfg)
+    assert rc == 1 and "exclude" in msg, (rc, msg)
+    text = open(os.path.join(ROOT, "include", "gatspi.h")).read()
+    for name, value in re.findall(r"#define (GATSPI_FLAG_[A-Z_]+) (0x[0-9a-f]+)u", text):
+        assert getattr(lib, name) == int(value, 16), name
+    assert lib.gatspi_lanes_per_window(0) == 0
