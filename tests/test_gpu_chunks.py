@@ -238,3 +238,27 @@ def test_one_window_segments_after_a_stalled_scan(gpu, oracle_lib):
             tc, t0, t1 = sim.toggle_stats()
             off, pool = sim.export_all()
             assert_same(dict(off=off, pool=pool, tc=tc, t0=t0, t1=t1), ref, "after the stall")
+
+
+@pytest.mark.parametrize("W", [2, 3, 4, 16])
+def test_long_windows_of_heavy_gates(gpu, oracle_lib, W):
+    """Two to sixteen long windows (thousands of words per input window) cut into
+    stretches: a lone gate, a netlist of many gates with heavy ones, with and without
+    packing, against the oracle."""
+    from gate_level_logic_gb300 import gatspi
+    cut, _ = flags()
+    tt = np.array([0, 1, 1, 0], np.uint8)                       # XOR2
+    D = np.full((8, 2), 9, np.int32)
+    one = single_gate(tt, 2, D, wire_rise=[2, 0], wire_fall=[1, 3])
+    stim1 = synth.generate_stimulus(synth.StimulusSpec(num_inputs=2, cycles=4000 * W, period=200, activity=0.7,
+                                                       windows=W, seed=90 + W, glitch_frac=0.3))
+    ref1 = oracle_lib.simulate(one, stim1)
+    assert_same(run_gpu(gpu, one, stim1, pool_for(ref1, one), flags=cut, repeat=2), ref1, "lone gate")
+    if W == 4:
+        net = synth.generate_netlist(synth.NetlistSpec(num_gates=4000, num_inputs=16, num_levels=8, seed=95,
+                                                       cond_fraction=0.3, fanout_mean=6.0))
+        stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=16, cycles=8000, period=300, activity=0.6,
+                                                          windows=W, seed=95, glitch_frac=0.2))
+        ref = oracle_lib.simulate(net, stim, threads=THREADS)
+        for fl in (cut, 0, cut | gatspi.GATSPI_FLAG_COMPACT):
+            assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), flags=fl, repeat=2), ref, "flags %#x" % fl)
