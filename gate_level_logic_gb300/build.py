@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgatspi.so")
-SOURCES = ("gatspi.cu", "level_kernel.cu", "gatspi_static.cu", "testbench.cu", "sdf.cpp")
+SOURCES = ("gatspi.cu", "level_kernel.cu", "chunk_kernel.cu", "gatspi_static.cu", "testbench.cu", "sdf.cpp")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

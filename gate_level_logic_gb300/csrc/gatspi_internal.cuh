@@ -137,7 +137,11 @@ inline int chunks_per_window(int W, int pulse_percent, uint32_t flags, bool long
 }
 size_t plan_smem_bytes(int W);
 int plan_gates_per_tile(int W);   // gates (warps) of one planning block
-cudaError_t set_level_smem_limit();   // the planning kernel's shared memory (largest W), the simulation kernels' L1
+cudaError_t set_level_smem_limit();
+// chunk_kernel.cu: the level's simulation with windows cut into time chunks
+// (DevParams::chunks > 1), and its kernels' shared-memory configuration.
+cudaError_t launch_level_chunks(const DevParams &p, const LevelLaunch &l, cudaStream_t s);
+cudaError_t set_chunk_smem_limit();   // the planning kernel's shared memory (largest W), the simulation kernels' L1
 cudaError_t launch_level_bounds(const DevParams &p, const LevelLaunch &l, cudaStream_t s);   // plan + placement
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s);      // the simulation
 cudaError_t launch_level_compact(const DevParams &p, const LevelLaunch &l, const LevelLaunch &exact,
