@@ -45,7 +45,8 @@ METRIC = "output toggle events/sec and gate-cycles/sec at 1 GB300; % of HBM roof
 UNIT = "output toggle events/s"
 WORKLOAD = "1M"
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SOURCES = ("gate_level_logic_gb300/csrc/level_kernel.cu", "gate_level_logic_gb300/csrc/gatspi_internal.cuh")
+KERNEL_SOURCES = ("gate_level_logic_gb300/csrc/lane.cuh", "gate_level_logic_gb300/csrc/level_kernel.cu",
+                  "gate_level_logic_gb300/csrc/gatspi_internal.cuh")
 
 
 def _dist():
