@@ -200,8 +200,9 @@ def test_static_levels_match_regular_path(built, oracle_lib, name, q):
 def test_sources_far_apart(built):
     """The inputs at the front of a pool of more than 2^32 words, the first level's
     outputs beyond word 2^32: gates of the next levels read sources that far apart,
-    which the kernel's 32-bit pin offsets cannot span, so those lanes keep their pins
-    in registers.  Every waveform and statistic still equals the regular path's."""
+    which offsets from one pointer cannot span in 32 bits, so those lanes count each
+    pin's offsets from its own window.  Every waveform and statistic still equals the
+    regular path's."""
     import torch
     net = synth.generate_netlist(synth.NetlistSpec(num_gates=600, num_inputs=16, num_levels=4, seed=9))
     stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=16, cycles=300, period=300, activity=0.4,
