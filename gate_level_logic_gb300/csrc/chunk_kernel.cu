@@ -245,9 +245,10 @@ __device__ __forceinline__ void move_runs(int32_t *p, uint32_t dst, uint32_t shi
 // time at 1.  No warp waits for another.  A segment whose quiet time is not found is
 // empty, and the segment before it runs on to the next found one.
 // kSeg: the instantiation that can split a gate's one window into segments.  Its
-// code generation also happens to run windows that are not split 2-9 % faster at 2-16
-// windows of 100 words or more per input, and 4-6 % slower on shorter ones, so the
-// host picks the instantiation by the loaded inputs (DevParams::seg_kernel).
+// code generation also happens to run windows that are not split a little faster at
+// high activity (1-2 % at 20 and 50 %, 2-16 windows) and a little slower at low (about
+// 3 % at 5 %), so the host picks the instantiation by the loaded inputs' words per
+// window (DevParams::seg_kernel).
 template <bool kSeg>
 __global__ void __launch_bounds__(kLevelBlock, kChunkMinBlocks) level_chunk_kernel(const DevParams P,
                                                                                   const LevelLaunch L) {
