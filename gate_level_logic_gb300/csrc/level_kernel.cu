@@ -254,46 +254,63 @@ __device__ __forceinline__ void plan_window_order(const DevParams &P, const Leve
     const int s4[GATSPI_MAX_PINS] = {sv.x, sv.y, sv.z, sv.w};
     uint32_t *goff = P.goff + (long long)gl * (P.ngroups + 1);
     long long run = 0;
-    for (int w0 = 4 * lane; w0 - 4 * lane < W; w0 += 4 * 32) {
-        long long part = 0;   // this lane's four windows
-        if (w0 < W) {
-            uint32_t even = 0, odd = 0;        // windows w0, w0 + 2 and w0 + 1, w0 + 3 in 16-bit halves
-            uint32_t fix[4] = {0, 0, 0, 0};    // lengths beyond 255
+    // kAhead steps' length words are loaded before any of them is summed, so that a
+    // lane has that many loads per pin in flight instead of one
+    constexpr int kAhead = 4;
+    const int steps = (W + 127) / 128;
+    for (int s0 = 0; s0 < steps; s0 += kAhead) {
+        uint32_t fours[kAhead][N];
 #pragma unroll
-            for (int i = 0; i < N; ++i) {
-                const long long src = s4[i];
-                const uint32_t four = __ldg((const uint32_t *)(P.wlen8 + src * P.w8stride + w0));
-                even += four & 0x00ff00ffu;
-                odd += (four >> 8) & 0x00ff00ffu;
-                if (__vcmpeq4(four, 0xffffffffu)) {
+        for (int u = 0; u < kAhead; ++u) {
+            const int w0 = (s0 + u) * 128 + 4 * lane;
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int w = w0 + u;
-                        if (((four >> (8 * u)) & 0xffu) == 0xffu && w < W)
-                            fix[u] += __ldg(P.wend + src * W + w) - __ldg(P.wstart + src * W + w) - 255u;
+            for (int i = 0; i < N; ++i)
+                fours[u][i] = w0 < W ? __ldg((const uint32_t *)(P.wlen8 + (long long)s4[i] * P.w8stride + w0)) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            if (s0 + u >= steps) break;                  // warp-uniform
+            const int w0 = (s0 + u) * 128 + 4 * lane;
+            long long part = 0;   // this lane's four windows
+            if (w0 < W) {
+                uint32_t even = 0, odd = 0;        // windows w0, w0 + 2 and w0 + 1, w0 + 3 in 16-bit halves
+                uint32_t fix[4] = {0, 0, 0, 0};    // lengths beyond 255
+#pragma unroll
+                for (int i = 0; i < N; ++i) {
+                    const long long src = s4[i];
+                    const uint32_t four = fours[u][i];
+                    even += four & 0x00ff00ffu;
+                    odd += (four >> 8) & 0x00ff00ffu;
+                    if (__vcmpeq4(four, 0xffffffffu)) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int w = w0 + v;
+                            if (((four >> (8 * v)) & 0xffu) == 0xffu && w < W)
+                                fix[v] += __ldg(P.wend + src * W + w) - __ldg(P.wstart + src * W + w) - 255u;
+                        }
                     }
                 }
+                const uint32_t base = 3u - 2u * (uint32_t)N;
+                const uint32_t b[4] = {base + (even & 0xffffu) + fix[0], base + (odd & 0xffffu) + fix[1],
+                                       base + (even >> 16) + fix[2], base + (odd >> 16) + fix[3]};
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (w0 + v < W) part += b[v];
             }
-            const uint32_t base = 3u - 2u * (uint32_t)N;
-            const uint32_t b[4] = {base + (even & 0xffffu) + fix[0], base + (odd & 0xffffu) + fix[1],
-                                   base + (even >> 16) + fix[2], base + (odd >> 16) + fix[3]};
+            // the group of 32 windows of this step that holds lane's windows: lanes 8k .. 8k+7
+            long long gsum = part;
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                if (w0 + u < W) part += b[u];
+            for (int o = 4; o >= 1; o >>= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
+            // the four groups' sums (lanes 0, 8, 16, 24) and their running offsets
+            const long long g0 = __shfl_sync(0xffffffffu, gsum, 0), g1 = __shfl_sync(0xffffffffu, gsum, 8);
+            const long long g2 = __shfl_sync(0xffffffffu, gsum, 16), g3 = __shfl_sync(0xffffffffu, gsum, 24);
+            const int grp = (s0 + u) * 4;                    // first group of this step
+            if (lane < 4 && grp + lane < P.ngroups) {
+                const long long before = lane == 0 ? 0 : lane == 1 ? g0 : lane == 2 ? g0 + g1 : g0 + g1 + g2;
+                goff[grp + lane] = (uint32_t)(run + before);
+            }
+            run += g0 + g1 + g2 + g3;
         }
-        // the group of 32 windows of this step that holds lane's windows: lanes 8k .. 8k+7
-        long long gsum = part;
-#pragma unroll
-        for (int o = 4; o >= 1; o >>= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
-        // the four groups' sums (lanes 0, 8, 16, 24) and their running offsets
-        const long long g0 = __shfl_sync(0xffffffffu, gsum, 0), g1 = __shfl_sync(0xffffffffu, gsum, 8);
-        const long long g2 = __shfl_sync(0xffffffffu, gsum, 16), g3 = __shfl_sync(0xffffffffu, gsum, 24);
-        const int grp = (w0 - 4 * lane) >> 5;            // first group of this step
-        if (lane < 4 && grp + lane < P.ngroups) {
-            const long long before = lane == 0 ? 0 : lane == 1 ? g0 : lane == 2 ? g0 + g1 : g0 + g1 + g2;
-            goff[grp + lane] = (uint32_t)(run + before);
-        }
-        run += g0 + g1 + g2 + g3;
     }
     if (lane == 0) {
         if (run >= (1ll << 32)) raise_error(P.status, GATSPI_EPOOL_OVERFLOW, L.level, L.gate_begin + gl, 1);
