@@ -240,17 +240,19 @@ gatspi_status gatspi_load_testbench(gatspi_ctx *ctx, const int64_t *off, const i
 /*
  * Re-simulate every level, in order, on `stream` (a cudaStream_t; NULL = legacy
  * default stream).  Asynchronous: returns after enqueueing.  Clears TC/T1 and the
- * device status first.  Per level two kernels run.  The first plans the level: it
- * bounds every (gate, window) output (an output window holds at most 3 + the sum over
- * its pins of (input length - 2) words, since each stored toggle takes an event-loop
- * iteration and each iteration consumes an input transition), ranks each gate's
- * windows by bound so that a warp gets 32 windows of similar work (up to 1024
- * windows; beyond, the windows are short and are taken in window order), and scans
- * the gates' bound sums into pool offsets, in place of the page's counting pass.  The
- * second runs Algorithm 1 for every (gate, window) of the level and stores the output
- * waveforms, the window index and TC/T1 per gate.  The level sequence is captured once into a CUDA graph and
- * replayed by later calls, unless GATSPI_FLAG_NO_GRAPH or GATSPI_FLAG_LEVEL_TIMING
- * is set (then the level kernels are launched directly on `stream`).
+ * device status first.  Per level three kernels run, in place of the page's
+ * counting and writing passes.  The first plans the level: it bounds every (gate,
+ * window) output (an output window holds at most 3 + the sum over its pins of (input
+ * length - 2) words, since each stored toggle takes an event-loop iteration and each
+ * iteration consumes an input transition) and ranks each gate's windows by bound so
+ * that a warp gets 32 windows of similar work (up to 1024 windows; beyond, the windows
+ * are short and are taken in window order).  The second scans the gates' bound sums
+ * into pool offsets.  The third runs Algorithm 1 for every (gate, window) of the level
+ * and stores the output waveforms, the window index and TC/T1 per gate.  Windows cut
+ * into time chunks (below) add a kernel that orders the gates, packing two more.  The
+ * level sequence is captured once into a CUDA graph and replayed by later calls,
+ * unless GATSPI_FLAG_NO_GRAPH or GATSPI_FLAG_LEVEL_TIMING is set (then the level
+ * kernels are launched directly on `stream`).
  */
 gatspi_status gatspi_simulate(gatspi_ctx *ctx, void *stream);
 
