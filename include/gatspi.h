@@ -48,7 +48,9 @@
  * W independent windows; every window starts from the zero-delay steady state of
  * its input values and is simulated to completion (events scheduled past the
  * window's end are kept in the waveform and counted in TC; T1/T0 count only
- * [0, window_len)).
+ * [0, window_len)).  With few, long windows the library also splits each window at
+ * times when the gate is quiet and simulates the stretches in parallel, which gives
+ * exactly the window's result (see gatspi_simulate).
  */
 #ifndef GATSPI_H
 #define GATSPI_H
