@@ -500,6 +500,9 @@ typedef struct {
  *     race on it and must be serialised by the caller.
  *   - Synchronous: enqueues on `stream`, waits for it, and returns the kernel's
  *     status (GATSPI_EPOOL_OVERFLOW, GATSPI_EBADLUT, ...).
+ *   - Every window runs whole, one lane each: the time-chunk form of few long
+ *     windows (GATSPI_FLAG_CUT_WINDOWS) needs per-level scratch that this call
+ *     does not have.  That form gives the same words, so only the speed differs.
  * Results are identical to the level kernels gatspi_simulate runs.
  */
 gatspi_status gatspi_simulate_level_static(const gatspi_level_args *args, void *stream);
