@@ -346,3 +346,31 @@ def test_pin_weights_are_data(oracle_lib):
     a = oracle_lib.simulate(net, stim)
     b = oracle_lib.simulate(perm, stim)
     assert np.array_equal(a.pool, b.pool) and np.array_equal(a.tc, b.tc) and np.array_equal(a.t1, b.t1)
+
+
+def _bound_slack(net, stim, r):
+    """Per (gate, window): 3 + sum over pins of (source length - 2), minus the output's
+    length (words, EOW included).  Each arrival step stores at most one entry, so a
+    window's entries are at most its pins' transitions, at most (length - 2) each; the
+    head takes one or two words and the EOW one."""
+    P, G, W = net.num_inputs, net.num_gates, stim.num_windows
+    lens = np.diff(r.off).reshape(P + G, W)
+    pins = np.diff(net.fanin_off).astype(np.int64)
+    gate_of_edge = np.repeat(np.arange(G), pins)
+    src = lens[np.asarray(net.fanin_net, np.int64)] - 2                  # [E, W]
+    per_gate = np.zeros((G, W), np.int64)
+    np.add.at(per_gate, gate_of_edge, src)
+    return 3 + per_gate - lens[P:]
+
+
+def test_output_length_bound(oracle_lib):
+    """Every output fits the bound its inputs' lengths give (the size of its slot before
+    anything is simulated), and the bound is reached: a constant one word smaller
+    would be exceeded, and one word larger would never be used."""
+    cases = [_random_case(seed) for seed in range(600)] + [synth.make("tiny"), synth.make("50k")]
+    tight = 0
+    for net, stim in cases:
+        slack = _bound_slack(net, stim, oracle_lib.simulate(net, stim, threads=4))
+        assert slack.min() >= 0
+        tight += int(np.sum(slack == 0))
+    assert tight > 0
