@@ -126,3 +126,57 @@ def test_quiet_cut_equals_whole_window(oracle_lib):
     assert checked > 3000, checked
     for name in ("M1 without the gate delay", "M1 without the wire delay", "M2 = 0"):
         assert wrong[name] > 0, (name, wrong)
+
+
+def _split_many_matches(oracle_lib, net, inits, edges, whole, cuts):
+    """Whether the window simulated as len(cuts) + 1 windows, split at every cut (each
+    part starting from the pins' values at its cut), equals the whole run."""
+    bounds = [0] + list(cuts) + [LENGTH]
+    waves = []
+    for v0, e in zip(inits, edges):
+        parts = []
+        for a, b in zip(bounds[:-1], bounds[1:]):
+            v_a = (v0 + sum(1 for t in e if t <= a)) % 2 if a else v0
+            parts.append(_wave(v_a, [t - a for t in e if a < t < b]))
+        waves.append(parts)
+    many = oracle_lib.simulate(net, synth.from_waveforms(waves, np.diff(bounds)))
+    out = whole.gate_wave(0, 0)
+    joined = []
+    for k, a in enumerate(bounds[:-1]):
+        part = many.gate_wave(0, k)
+        if value_at(part, 0) != value_at(out, a):
+            return False
+        joined += [t + a for t in changes(part)]
+    return (joined == changes(out) and int(many.tc[0]) == int(whole.tc[0])
+            and int(many.t1[0]) == int(whole.t1[0]))
+
+
+def test_many_quiet_cuts_equal_whole_window(oracle_lib):
+    """A window cut at up to 31 quiet times at once, the way 32 lanes cut it: lane k
+    takes the first quiet time at or after k * L / 32 that lies before the next
+    lane's start, and a lane that finds none leaves its stretch to the lane before."""
+    rng = np.random.default_rng(77)
+    windows = 0
+    cuts_total = 0
+    for case in range(300):
+        net, n, D, rise, fall = _random_gate(rng)
+        inits = [int(rng.integers(0, 2)) for _ in range(n)]
+        edges = [_random_edges(rng) for _ in range(n)]
+        whole = oracle_lib.simulate(net, synth.from_waveforms([[_wave(v, e)] for v, e in zip(inits, edges)],
+                                                               LENGTH))
+        wd = int(max(rise.max(), fall.max()))
+        finite = D[D != INF]
+        dg = int(finite.max()) if finite.size else 0
+        m1, m2 = wd + dg, wd + 1
+        s = np.asarray(sorted(t for e in edges for t in e), np.int64)
+        cuts = []
+        for k in range(1, 32):
+            lo, hi = k * LENGTH // 32, (k + 1) * LENGTH // 32
+            for T in range(max(lo, m1 + 1), hi):
+                if np.searchsorted(s, T + m2, side="left") == np.searchsorted(s, T - m1, side="left"):
+                    cuts.append(T)
+                    break
+        assert _split_many_matches(oracle_lib, net, inits, edges, whole, cuts), (case, cuts)
+        windows += 1
+        cuts_total += len(cuts)
+    assert cuts_total > 20 * windows, (cuts_total, windows)
