@@ -179,21 +179,49 @@ def _kernel_hash(read=None):
     return h.hexdigest()[:16]
 
 
-def _traffic(demand_per_launch):
-    """DRAM bytes per level_kernel launch: the ratio of DRAM traffic to demand bytes
-    that ncu measured on the committed small case (the same kernel source, two
-    launches), applied to this workload's mean demand bytes per launch; None when the
+# The plan ranks a gate's windows by bound up to this many windows per context and
+# takes more in window order (the window index's perm is unused beyond it).
+RANKED_WINDOWS = 1024
+
+# How a run's levels are simulated, which decides the kernel its roofline describes
+# and the ncu record its DRAM traffic is scaled from (None: no record).
+SIM_REGIMES = {
+    "ranked": ("level_kernel (one launch per logic level; windows ranked by bound)",
+               "level_kernel_small_traffic.json"),
+    "window_order": ("level_kernel (one launch per logic level; windows in window order)",
+                     "level_kernel_4096windows_traffic.json"),
+    "cut": ("level_order_kernel + level_chunk_kernel (one pair per logic level; windows cut into time chunks)",
+            None),
+}
+
+
+def sim_regime(lanes_per_window, windows):
+    """The regime of a context with `windows` windows whose windows get
+    `lanes_per_window` lanes each (more than one: cut into time chunks)."""
+    if lanes_per_window > 1:
+        return "cut"
+    return "ranked" if windows <= RANKED_WINDOWS else "window_order"
+
+
+def _traffic(demand_per_launch, regime, pulse_percent=100):
+    """DRAM bytes per simulation launch: the ratio of DRAM traffic to demand bytes that
+    ncu measured on the committed small case of the same regime (the same kernel
+    source, PATHPULSEPERCENT = 100, two launches), applied to this workload's mean
+    demand bytes per launch.  (None, None, None) when the regime has no record, the
+    run uses another PATHPULSEPERCENT (another instantiation of the kernel), or the
     record is missing or was taken on other kernel code."""
-    path = os.path.join(ROOT, "profiles", "level_kernel_small_traffic.json")
+    name = SIM_REGIMES[regime][1]
+    if name is None or pulse_percent != 100:
+        return None, None, None
     try:
-        with open(path) as f:
+        with open(os.path.join(ROOT, "profiles", name)) as f:
             rec = json.load(f)
     except (OSError, ValueError):
-        return None, None
+        return None, None, None
     if rec.get("kernel_sha") != _kernel_hash():
-        return None, None
+        return None, None, None
     ratio = float(rec["dram_bytes"]) / float(rec["demand_bytes"])
-    return ratio * float(demand_per_launch), ratio
+    return ratio * float(demand_per_launch), ratio, name
 
 
 class ClockSampler:
@@ -512,7 +540,8 @@ def run_gpu(args):
         peak_src = "measured"
     else:
         peak, peak_src = 6800.0, "fallback"
-    traffic, traffic_ratio = _traffic(float(lvl_demand.mean()))
+    regime = sim_regime(lanes_per_window, W)
+    traffic, traffic_ratio, traffic_rec = _traffic(float(lvl_demand.mean()), regime, args.pulse_percent)
 
     # ---- end to end through the C ABI: host buffers, copies inside the region ---
     if args.no_e2e or args.sweep:      # no end-to-end legs on sweep points
@@ -539,14 +568,13 @@ def run_gpu(args):
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": traffic, "peak_source": peak_src,
-            "kernel": "level_kernel (one launch per logic level)",
+            "kernel": SIM_REGIMES[regime][0],
             "algorithmic_bytes_per_launch": float(run_bytes) / net.num_levels,
             "algorithmic_bytes_per_step": run_parts,
             "demand_bytes_per_launch": float(lvl_demand.mean()),
             "traffic_note": None if traffic is None else
             "ncu DRAM bytes / demand bytes = %.3f on the committed small case "
-            "(profiles/level_kernel_small_traffic.json), times this workload's demand bytes per launch"
-            % traffic_ratio,
+            "(profiles/%s), times this workload's demand bytes per launch" % (traffic_ratio, traffic_rec),
             "step_achieved_gbs": float(run_bytes * args.steps / total_s / 1e9),
             "avg_launch_ms": float(level_ms.sum() / (args.steps * net.num_levels)),
             "share_of_step": float(level_ms.sum() / sum(serial_ms)),

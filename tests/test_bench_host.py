@@ -3,7 +3,11 @@ numerator: each consumed waveform read once per run, each output written once, 8
 of window index per consumed (net, window) and per (gate, window), 16 bytes per gate
 and per fanin edge) and the per-level demand bytes, on a netlist small enough to count
 by hand."""
+import json
+import os
+
 import numpy as np
+import pytest
 
 import bench
 import synth
@@ -45,3 +49,34 @@ def test_demand_bytes_by_hand():
     assert per_level.tolist() == [level0, level1, level2]
     total, parts = bench.algorithmic_bytes(net, words, W)
     assert per_level.sum() > total     # demand counts A twice and every level's index again
+
+
+def test_regime_picks_kernel_and_traffic_record(monkeypatch):
+    """The roofline names the kernels that simulated the levels and scales its DRAM
+    traffic from the ncu record of the same regime: windows ranked by bound (up to
+    1024 windows), in window order (beyond), or cut into time chunks (no record);
+    another PATHPULSEPERCENT or a record taken on other kernel code gives none."""
+    assert bench.sim_regime(1, 1) == "ranked"
+    assert bench.sim_regime(1, 256) == "ranked"
+    assert bench.sim_regime(1, 1024) == "ranked"
+    assert bench.sim_regime(1, 1025) == "window_order"
+    assert bench.sim_regime(1, 4096) == "window_order"
+    assert bench.sim_regime(32, 1) == "cut"
+    assert bench.sim_regime(2, 16) == "cut"
+    assert "level_chunk_kernel" in bench.SIM_REGIMES["cut"][0]
+    ratios = {}
+    for regime in ("ranked", "window_order"):
+        traffic, ratio, name = bench._traffic(1e8, regime)
+        with open(os.path.join(bench.ROOT, "profiles", name)) as f:
+            rec = json.load(f)
+        assert rec["kernel_sha"] == bench._kernel_hash()          # taken on the committed kernel code
+        assert sum(x["dram_read"] + x["dram_write"] for x in rec["launches"]) == rec["dram_bytes"]
+        assert sum(x["demand_bytes"] for x in rec["launches"]) == rec["demand_bytes"]
+        assert ratio == pytest.approx(rec["dram_bytes"] / rec["demand_bytes"])
+        assert traffic == pytest.approx(1e8 * ratio)
+        ratios[regime] = ratio
+    assert ratios["ranked"] != ratios["window_order"]
+    assert bench._traffic(1e8, "cut") == (None, None, None)
+    assert bench._traffic(1e8, "ranked", pulse_percent=60) == (None, None, None)
+    monkeypatch.setattr(bench, "_kernel_hash", lambda: "0" * 16)
+    assert bench._traffic(1e8, "window_order") == (None, None, None)
