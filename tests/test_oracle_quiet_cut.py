@@ -81,7 +81,7 @@ def _quiet_times(edges_all, m1, m2, rng):
     return sorted(set(first.tolist()) | set(last.tolist()) | set(mid))
 
 
-def _split_matches(oracle_lib, net, inits, edges, whole, T):
+def _split_matches(oracle_lib, net, inits, edges, whole, T, pulse_percent=100):
     """Whether the window simulated as [0, T) and [T, LENGTH) equals the whole run."""
     waves = []
     for v0, e in zip(inits, edges):
@@ -89,7 +89,7 @@ def _split_matches(oracle_lib, net, inits, edges, whole, T):
         after = [t - T for t in e if t > T]
         v_T = (v0 + sum(1 for t in e if t <= T)) % 2
         waves.append([_wave(v0, before), _wave(v_T, after)])
-    two = oracle_lib.simulate(net, synth.from_waveforms(waves, [T, LENGTH - T]))
+    two = oracle_lib.simulate(net, synth.from_waveforms(waves, [T, LENGTH - T]), pulse_percent=pulse_percent)
     out = whole.gate_wave(0, 0)
     a, b = two.gate_wave(0, 0), two.gate_wave(0, 1)
     return (value_at(a, 0) == value_at(out, 0) and value_at(b, 0) == value_at(out, T)
@@ -180,3 +180,26 @@ def test_many_quiet_cuts_equal_whole_window(oracle_lib):
         windows += 1
         cuts_total += len(cuts)
     assert cuts_total > 20 * windows, (cuts_total, windows)
+
+
+def test_quiet_cut_holds_below_pulse_percent_100(oracle_lib):
+    """The same cut rule at PATHPULSEPERCENT 75, 50 and 0 (transport): the split window
+    still equals the whole run.  A pulse around T is wider than any reject limit, and an
+    event after T makes an entry at least M2 + 1 + its delay after the last entry before
+    T, more than that delay's reject limit, so no entry before T is ever cancelled."""
+    for q in (75, 50, 0):
+        rng = np.random.default_rng(500 + q)
+        checked = 0
+        for case in range(150):
+            net, n, D, rise, fall = _random_gate(rng)
+            inits = [int(rng.integers(0, 2)) for _ in range(n)]
+            edges = [_random_edges(rng) for _ in range(n)]
+            stim = synth.from_waveforms([[_wave(v, e)] for v, e in zip(inits, edges)], LENGTH)
+            whole = oracle_lib.simulate(net, stim, pulse_percent=q)
+            wd = int(max(rise.max(), fall.max()))
+            finite = D[D != INF]
+            dg = int(finite.max()) if finite.size else 0
+            for T in _quiet_times([t for e in edges for t in e], wd + dg, wd + 1, rng):
+                assert _split_matches(oracle_lib, net, inits, edges, whole, T, pulse_percent=q), (q, case, T)
+                checked += 1
+        assert checked > 1000, (q, checked)
