@@ -1,5 +1,5 @@
 // Level kernels for windows cut into time chunks (16 windows or fewer, long windows,
-// PATHPULSEPERCENT = 100): the cut search, the heaviest-first gate order (with the
+// any PATHPULSEPERCENT): the cut search, the heaviest-first gate order (with the
 // segments of one window's heavy gates), the moves that join the stretches, and
 // level_chunk_kernel itself.  The per-lane simulation is lane.cuh's run_lane.
 #include "gatspi_internal.cuh"
@@ -9,7 +9,7 @@ namespace gatspi {
 
 namespace {
 
-// Windows cut into time chunks (16 windows or fewer, PATHPULSEPERCENT = 100): with
+// Windows cut into time chunks (16 windows or fewer, any PATHPULSEPERCENT): with
 // few windows a lane runs its gate through a long stretch of the testbench and a level
 // lasts as long as its busiest gate's serial chain.  Here a warp takes one gate and
 // gives each of its windows K = 32 / W lanes; lane k of a window simulates the window
@@ -21,7 +21,9 @@ namespace {
 // before T comes from a transition before T - M1 and every arrival at or after T from
 // one at or after T + M2, and every output entry made before T lies before T, so no
 // later event can cancel it (at q = 100 an entry is cancelled only by an event
-// earlier than the entry).  The simulation from T on therefore needs only the pins'
+// earlier than the entry; at any q an event after T makes an entry at least
+// M2 + 1 + its delay d after every entry before T, more than the reject limit of d,
+// so none of those is cancelled either).  The simulation from T on therefore needs only the pins'
 // entries in effect and the output value at T (the truth table of the pins' values),
 // and yields exactly the entries, toggles and time at 1 of the whole window's run.
 // Lane k looks for its cut from k * Lw / K on (the first quiet time, within a few
@@ -244,12 +246,13 @@ __device__ __forceinline__ void move_runs(int32_t *p, uint32_t dst, uint32_t shi
 // Q-1 down behind each other, writes the EOW and the window index, and adds the final
 // time at 1.  No warp waits for another.  A segment whose quiet time is not found is
 // empty, and the segment before it runs on to the next found one.
+// kFull: PATHPULSEPERCENT = 100 (else the reject-limit filter, see run_lane).
 // kSeg: the instantiation that can split a gate's one window into segments.  Its
 // code generation also happens to run windows that are not split a little faster at
 // high activity (1-2 % at 20 and 50 %, 2-16 windows) and a little slower at low (about
 // 3 % at 5 %), so the host picks the instantiation by the loaded inputs' words per
 // window (DevParams::seg_kernel).
-template <bool kSeg>
+template <bool kSeg, bool kFull>
 __global__ void __launch_bounds__(kLevelBlock, kChunkMinBlocks) level_chunk_kernel(const DevParams P,
                                                                                   const LevelLaunch L) {
     __shared__ int2 pin_hot[kLevelWarps][GATSPI_MAX_PINS * 32];
@@ -425,7 +428,7 @@ __global__ void __launch_bounds__(kLevelBlock, kChunkMinBlocks) level_chunk_kern
         const PinTab tab{&pin_hot[warp][lane], &pin_end[warp][lane]};
 #pragma unroll
         for (int i = 0; i < GATSPI_MAX_PINS; ++i) pins[i].p = pos[i];
-        res = dispatch<true, true>(P, gd, pins, tab, Lw, from_start ? slot : slot + off - 1, from_start, tend,
+        res = dispatch<kFull, true>(P, gd, pins, tab, Lw, from_start ? slot : slot + off - 1, from_start, tend,
                                    (int32_t)cb);
         if (res.err) raise_error(P.status, res.err, g, w, k);
     }
@@ -525,18 +528,26 @@ cudaError_t launch_level_chunks(const DevParams &p, const LevelLaunch &l, cudaSt
         const long long warps = (long long)l.num_gates + (p.seg_items ? kExtraSegments : 0);
         const unsigned blocks = (unsigned)((warps + kLevelWarps - 1) / kLevelWarps);
         level_order_kernel<<<1, kOrderThreads, 0, s>>>(p, l);
-        if (p.seg_kernel)
-            level_chunk_kernel<true><<<blocks, kLevelBlock, 0, s>>>(p, l);
+        const bool full = p.pulse_percent == 100;
+        if (p.seg_kernel && full)
+            level_chunk_kernel<true, true><<<blocks, kLevelBlock, 0, s>>>(p, l);
+        else if (p.seg_kernel)
+            level_chunk_kernel<true, false><<<blocks, kLevelBlock, 0, s>>>(p, l);
+        else if (full)
+            level_chunk_kernel<false, true><<<blocks, kLevelBlock, 0, s>>>(p, l);
         else
-            level_chunk_kernel<false><<<blocks, kLevelBlock, 0, s>>>(p, l);
+            level_chunk_kernel<false, false><<<blocks, kLevelBlock, 0, s>>>(p, l);
     }
     return cudaGetLastError();
 }
 
 cudaError_t set_chunk_smem_limit() {
     // the same pin table and shared-memory configuration as level_kernel
-    cudaError_t e = cudaFuncSetAttribute(level_chunk_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 20);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(level_chunk_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 20);
+    const cudaFuncAttribute a = cudaFuncAttributePreferredSharedMemoryCarveout;
+    cudaError_t e = cudaFuncSetAttribute(level_chunk_kernel<false, true>, a, 20);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(level_chunk_kernel<true, true>, a, 20);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(level_chunk_kernel<false, false>, a, 20);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(level_chunk_kernel<true, false>, a, 20);
     return e;
 }
 

@@ -131,7 +131,7 @@ struct gatspi_ctx {
         p.gate_order = gate_order;
         p.heavy_order = heavy_order;
         // segments of one window: when its windows are cut and very long, or cut by force
-        const bool seg = chunks_per_window(W, pulse_percent, flags, long_windows) > 1 &&
+        const bool seg = chunks_per_window(W, flags, long_windows) > 1 &&
                          (split_windows || (flags & GATSPI_FLAG_CUT_WINDOWS));
         p.seg_items = seg ? seg_items : nullptr;
         p.seg_kernel = seg || (W >= 2 && dense_windows) ? 1 : 0;
@@ -164,7 +164,7 @@ struct gatspi_ctx {
         p.slots_per_gate = slots_per_gate;
         p.pulse_percent = pulse_percent;
         p.ranked = windows_ranked(W) ? 1 : 0;
-        p.chunks = chunks_per_window(W, pulse_percent, flags, long_windows);
+        p.chunks = chunks_per_window(W, flags, long_windows);
         p.compact = compact ? 1 : 0;
         p.gexact = gexact;
         p.old_base = old_base;
@@ -415,7 +415,7 @@ const char *gatspi_last_error(void) { return g_err.c_str(); }
 
 int32_t gatspi_lanes_per_window(const gatspi_ctx *c) {
     if (!c) return 0;
-    const int k = chunks_per_window(c->W, c->pulse_percent, c->flags, c->long_windows);
+    const int k = chunks_per_window(c->W, c->flags, c->long_windows);
     return k > 1 ? k : 1;
 }
 

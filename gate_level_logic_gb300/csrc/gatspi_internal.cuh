@@ -92,7 +92,7 @@ struct DevParams {
     int32_t slots_per_gate;   // ngroups << lpg_log2
     int32_t pulse_percent;    // PATHPULSEPERCENT, 0 .. 100
     int32_t ranked;           // windows_ranked(W): perm holds the ranks; else rank = window
-    int32_t chunks;           // > 1: lanes per window of level_chunk_kernel (W <= 16, q = 100); else 0
+    int32_t chunks;           // > 1: lanes per window of level_chunk_kernel (W <= 16); else 0
     // compaction (GATSPI_FLAG_COMPACT): every level is simulated into bound-sized regions
     // placed down from the top of the pool, then packed to exact size at the front
     int32_t compact;
@@ -114,8 +114,8 @@ struct LevelLaunch {
 };
 
 int plan_words(int W);
-// Lanes per window of level_chunk_kernel: 32 / W with 16 windows or fewer at
-// PATHPULSEPERCENT = 100 when the windows are long (the loaded inputs average
+// Lanes per window of level_chunk_kernel: 32 / W with 16 windows or fewer, at any
+// PATHPULSEPERCENT, when the windows are long (the loaded inputs average
 // kLongWindowWords words or more per (input, window): shorter windows lose more to
 // finding cuts and moving the chunks together than they gain), or always with
 // GATSPI_FLAG_CUT_WINDOWS; never with GATSPI_FLAG_WHOLE_WINDOWS.  0: every window in
@@ -131,9 +131,9 @@ constexpr long long kSplitWindowWords = 4096;
 // From this many words per input window on, cut windows of 2 .. 16 run faster in the
 // segment-capable instantiation of level_chunk_kernel (measured; nothing is split).
 constexpr long long kDenseWindowWords = 100;
-inline int chunks_per_window(int W, int pulse_percent, uint32_t flags, bool long_windows) {
+inline int chunks_per_window(int W, uint32_t flags, bool long_windows) {
     const bool cut = (flags & GATSPI_FLAG_CUT_WINDOWS) || (long_windows && !(flags & GATSPI_FLAG_WHOLE_WINDOWS));
-    return W >= 1 && W <= 16 && pulse_percent == 100 && cut ? 32 / W : 0;
+    return W >= 1 && W <= 16 && cut ? 32 / W : 0;
 }
 size_t plan_smem_bytes(int W);
 int plan_gates_per_tile(int W);   // gates (warps) of one planning block

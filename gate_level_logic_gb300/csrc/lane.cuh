@@ -192,7 +192,11 @@ __device__ __forceinline__ bool table_fits(const Pin (&pin)[N], const int32_t *&
 // the parity of an entry's index stays its value).  Every chunk stops before the
 // first arrival at or after tend, writes no EOW, and returns in len the index of its
 // last entry, in tc its entries (stores less cancels) and in t1 its signed sum of
-// clipped entries, without the final adjustment.
+// clipped entries, without the final adjustment.  The entry in effect at the cut
+// (index y0) lies before the cut and is never cancelled: any event after the cut
+// makes an entry more than its delay's reject limit after it.  The chunk does not
+// hold that entry and stands in time 0 for it, which gives the same filter decisions
+// (it too lies at least that far before every later entry).
 template <int N, bool kFull, int kPins, bool kChunk = false>
 __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb, const PinTab &tab, uint32_t tt,
                                                const int32_t *__restrict__ D, int32_t Lw, int32_t *__restrict__ gout,
@@ -318,7 +322,9 @@ __device__ __forceinline__ LaneResult run_lane(Pin (&pin)[N], const int32_t *lb,
             top = ntop;
         } else if (cancel) {
             top = second;
-            second = po > 0 ? get(po - 1) : 0;           // the exposed entry may be pending too
+            // the exposed entry may be pending too; below a chunk's first entry lies
+            // the entry in effect at its cut, which another lane wrote (stand-in 0)
+            second = po > (kChunk && !from_start ? y0 + 1 : 0) ? get(po - 1) : 0;
         } else if (store) {
             second = top;
             top = to;

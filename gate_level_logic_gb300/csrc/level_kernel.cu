@@ -772,7 +772,7 @@ cudaError_t launch_level_compact(const DevParams &p, const LevelLaunch &l, const
 }
 
 cudaError_t launch_level_sim(const DevParams &p, const LevelLaunch &l, cudaStream_t s) {
-    if (p.chunks > 1 && p.pulse_percent == 100) return launch_level_chunks(p, l, s);   // chunk_kernel.cu
+    if (p.chunks > 1) return launch_level_chunks(p, l, s);   // chunk_kernel.cu
     const unsigned blocks = (unsigned)((l.num_tiles + kLevelWarps - 1) / kLevelWarps);
     if (p.pulse_percent == 100)
         level_kernel<true><<<blocks, kLevelBlock, 0, s>>>(p, l);

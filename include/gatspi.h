@@ -274,24 +274,26 @@ gatspi_status gatspi_simulate(gatspi_ctx *ctx, void *stream);
  * `stream` waits for the copies at the end, so the statistics are on the host once
  * the stream has finished and gatspi_toggle_stats reads no device memory.
  *
- * With 16 windows or fewer at PATHPULSEPERCENT = 100, when the windows are long (the
+ * With 16 windows or fewer, at any PATHPULSEPERCENT, when the windows are long (the
  * last load averaged 32 words or more per (input, window); always with
  * GATSPI_FLAG_CUT_WINDOWS, never with GATSPI_FLAG_WHOLE_WINDOWS; the two flags
  * exclude each other: EINVAL at create), a lane would run its gate through a long
  * window alone, so each gate takes one warp and each of its windows 32 / W lanes,
  * every lane simulating the window between two cuts: times at which none of the
  * gate's pins has a transition within its largest wire delay after, nor within that
- * wire delay plus its largest gate delay before.  At such a time every pin's entry in
- * effect is its last transition, no pulse spans it, and no output entry made before
- * it can be cancelled by an event after it, so the stretches simulate independently
- * and give exactly the whole window's waveform, toggles and time at 1 (the page runs
- * windows, not stretches of one, in parallel: Section 4, cycle parallelism).  A lane
- * that finds no cut near its share leaves its stretch to the lane before.  The warp
- * then moves the stretches' entries together inside the window's slot.  Each level's
- * gates are taken heaviest first.  With one window of 4096 words or more per input
- * (or with GATSPI_FLAG_CUT_WINDOWS), a gate whose work exceeds its level's share per
- * warp the GPU holds takes up to 8 warps, each a segment of the window between two
- * such times, and the last warp to finish moves the segments together.  A load that
+ * wire delay plus its largest gate delay before.  At such a time every pin's entry
+ * in effect is its last transition, no pulse spans it, and no output entry made
+ * before it can be cancelled by an event after it (below 100 %, every entry an
+ * event after it makes lies more than that delay's reject limit later), so the
+ * stretches simulate independently and give exactly the whole window's waveform,
+ * toggles and time at 1 (the page runs windows, not stretches of one, in parallel:
+ * Section 4, cycle parallelism).  A lane that finds no cut near its share leaves
+ * its stretch to the lane before.  The warp then moves the stretches' entries
+ * together inside the window's slot.  Each level's gates are taken heaviest first.
+ * With one window of 4096 words or more per input (or with
+ * GATSPI_FLAG_CUT_WINDOWS), a gate whose work exceeds its level's share per warp
+ * the GPU holds takes up to 8 warps, each a segment of the window between two such
+ * times, and the last warp to finish moves the segments together.  A load that
  * changes whether the windows are long makes the next simulate capture its graph
  * again.
  */
@@ -306,7 +308,7 @@ gatspi_status gatspi_sync(gatspi_ctx *ctx);
 /*
  * Lanes the next gatspi_simulate gives each window: 32 / num_windows when it cuts the
  * windows into time chunks (see gatspi_simulate), else 1; 0 for a NULL ctx.  Decided
- * by the flags, the window count, PATHPULSEPERCENT and the last load.
+ * by the flags, the window count and the last load.
  */
 int32_t gatspi_lanes_per_window(const gatspi_ctx *ctx);
 

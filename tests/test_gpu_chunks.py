@@ -1,11 +1,11 @@
-"""Windows cut into time chunks (16 windows or fewer, PATHPULSEPERCENT = 100): every
+"""Windows cut into time chunks (16 windows or fewer, any PATHPULSEPERCENT): every
 lane of a gate's warp simulates its window between two quiet times of the gate, and the
 warp moves the chunks' entries together.  The waveforms, window offsets and TC/T0/T1
 must equal the oracle's whole-window run bit for bit, whichever cuts are found, on the
 corner cases the oracle was pinned on (zero delays, zero-width pulses, 1-4 pin random
 cells, conditional arcs), on stretches too busy to hold a cut, on every launch path, with
-packing, after a stalled scan, and when a load switches a context between cut and whole
-windows."""
+packing, after a stalled scan, when a load switches a context between cut and whole
+windows, and below PATHPULSEPERCENT 100."""
 import os
 
 import numpy as np
@@ -262,3 +262,57 @@ def test_long_windows_of_heavy_gates(gpu, oracle_lib, W):
         ref = oracle_lib.simulate(net, stim, threads=THREADS)
         for fl in (cut, 0, cut | gatspi.GATSPI_FLAG_COMPACT):
             assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), flags=fl, repeat=2), ref, "flags %#x" % fl)
+
+
+@pytest.mark.parametrize("q", [60, 0])
+@pytest.mark.parametrize("W", [1, 3, 16])
+def test_cut_windows_below_pulse_percent_100(gpu, oracle_lib, W, q):
+    """PATHPULSEPERCENT below 100 (0: transport delay), cut and whole: several output
+    entries can be pending, and a cancel in a stretch can expose the entry in effect at
+    its cut, which the lane before wrote; against the oracle at the same percentage."""
+    cut, whole = flags()
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=3001, num_inputs=37, num_levels=9, seed=700 + W,
+                                                   cond_fraction=0.3))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=37, cycles=2000, period=300, activity=0.3,
+                                                      windows=W, seed=W + 40, glitch_frac=0.3))
+    ref = oracle_lib.simulate(net, stim, threads=THREADS, pulse_percent=q)
+    pw = pool_for(ref, net)
+    with gpu(net, stim.window_len, pool_words=pw, flags=cut, pulse_percent=q) as sim:
+        sim.load(stim.pi_off, stim.pi_words)
+        assert sim.lanes_per_window() == 32 // W
+    assert_same(run_gpu(gpu, net, stim, pw, flags=cut, pulse_percent=q), ref, "cut W=%d q=%d" % (W, q))
+    assert_same(run_gpu(gpu, net, stim, pw, flags=whole, pulse_percent=q), ref, "whole W=%d q=%d" % (W, q))
+
+
+def test_cut_windows_random_small_netlists_below_100(gpu, oracle_lib):
+    """The 120 corner-heavy cases cut at PATHPULSEPERCENT = 50."""
+    import test_oracle_pins as pins
+    cut, _ = flags()
+    for seed in range(120):
+        net, stim = pins._random_case(seed)
+        ref = oracle_lib.simulate(net, stim, pulse_percent=50)
+        assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), flags=cut, pulse_percent=50), ref,
+                    "seed %d" % seed)
+
+
+def test_cut_windows_below_100_segments_and_launch_paths(gpu, oracle_lib):
+    """One window split into segments at PATHPULSEPERCENT = 40 (replayed), and three
+    windows at 30 on every launch path, packing included."""
+    from gate_level_logic_gb300 import gatspi
+    cut, _ = flags()
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=4000, num_inputs=16, num_levels=8, seed=82,
+                                                   cond_fraction=0.3, fanout_mean=6.0))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=16, cycles=4000, period=300, activity=0.6,
+                                                      windows=1, seed=82, glitch_frac=0.2))
+    ref = oracle_lib.simulate(net, stim, threads=THREADS, pulse_percent=40)
+    assert_same(run_gpu(gpu, net, stim, pool_for(ref, net), flags=cut, repeat=3, pulse_percent=40), ref,
+                "segments q=40")
+    net = synth.generate_netlist(synth.NetlistSpec(num_gates=2500, num_inputs=32, num_levels=10, seed=74,
+                                                   cond_fraction=0.3))
+    stim = synth.generate_stimulus(synth.StimulusSpec(num_inputs=32, cycles=1500, period=400, activity=0.4,
+                                                      windows=3, seed=74, glitch_frac=0.2))
+    ref = oracle_lib.simulate(net, stim, threads=THREADS, pulse_percent=30)
+    pw = pool_for(ref, net)
+    for extra in (0, gatspi.GATSPI_FLAG_NO_GRAPH, gatspi.GATSPI_FLAG_LEVEL_TIMING, gatspi.GATSPI_FLAG_COMPACT):
+        assert_same(run_gpu(gpu, net, stim, pw, flags=cut | extra, repeat=2, pulse_percent=30), ref,
+                    "q=30 flags %#x" % extra)

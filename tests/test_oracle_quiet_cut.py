@@ -5,8 +5,8 @@ The kernels for few long windows also start a gate's simulation in the middle of
 window, at a quiet time T: no input pin of the gate has a transition in
 [T - M1, T + M2), where M1 = the largest wire delay of its pins (rise or fall) + the
 largest finite delay of its table and M2 = that wire delay + 1.  The claim is that,
-at PATHPULSEPERCENT = 100, the gate's run from T on then depends only on every pin's
-value at T.  In the oracle's own terms: the window simulated as two windows, [0, T)
+at any PATHPULSEPERCENT, the gate's run from T on then depends only on every pin's
+value at T (the first two tests take 100, the third 75, 50 and 0).  In the oracle's own terms: the window simulated as two windows, [0, T)
 and [T, L), the second starting from the pins' values at T, gives exactly the
 single window's output, with the same value at T, the same entries on either side
 (shifted by T), the same toggle count and the same time at 1.
