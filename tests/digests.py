@@ -145,4 +145,16 @@ def large_workloads() -> dict:
             out["sweep-%g-%d" % (a, w)] = (
                 "1M-gate netlist, stimulus seed 4, %g%% activity, no glitch pairs, %d windows" % (100 * a, w),
                 (lambda a=a, w=w: _sweep_point(a, w)))
+    # below PATHPULSEPERCENT 100, where few long windows are cut into time chunks: one
+    # window (at 50 % its heavy gates are split into segments) and sixteen at 0
+    # (transport delay)
+    for a, w, q in ((0.05, 1, 50), (0.5, 1, 50), (0.2, 16, 0)):
+        out["sweep-%g-%d-q%d" % (a, w, q)] = (
+            "1M-gate netlist, stimulus seed 4, %g%% activity, no glitch pairs, %d windows, PATHPULSEPERCENT %d"
+            % (100 * a, w, q), (lambda a=a, w=w: _sweep_point(a, w)))
     return out
+
+
+def pulse_percent(name: str) -> int:
+    """PATHPULSEPERCENT of a stored workload: its name's '-qN' suffix, else 100."""
+    return int(name.rsplit("-q", 1)[1]) if "-q" in name else 100

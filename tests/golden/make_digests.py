@@ -1,8 +1,9 @@
 """Write the oracle's digests of the large workloads to ``tests/golden/digests/``.
 
 These are the expected values of the full-size parity tests (``tests/test_gpu_digests.py``):
-the 5M-gate workload, the scan-style 500k-gate run and all sixteen points of the
-activity x windows sweep on the 1M-gate netlist.  Each is simulated completely by
+the 5M-gate workload, the scan-style 500k-gate run, all sixteen points of the
+activity x windows sweep on the 1M-gate netlist, and three of them again below
+PATHPULSEPERCENT 100 (names ending in -qN).  Each is simulated completely by
 the CPU oracle (Algorithm 1 of the GATSPI page, Section 3), every gate in every
 window, and stored as per-level records (exact word, TC and T1 sums plus
 position-keyed mixes of every gate's waveform digest, TC and T1; see
@@ -50,7 +51,7 @@ def compute(name, desc, make, threads):
     for w0 in range(0, W, per):
         sel = np.arange(w0, min(W, w0 + per))
         sub = stim if sel.size == W else synth.select_windows(stim, sel)
-        state = oracle.digest(net, sub, state=state, threads=threads)
+        state = oracle.digest(net, sub, state=state, threads=threads, pulse_percent=digests.pulse_percent(name))
         batches += 1
     t_sim = time.time() - t1
     rec = {
@@ -59,6 +60,7 @@ def compute(name, desc, make, threads):
         "inputs_sha256": digests.inputs_sha256(net, stim),
         "num_inputs": int(net.num_inputs), "num_gates": int(net.num_gates), "num_levels": int(net.num_levels),
         "num_windows": int(W), "window_time": int(state.window_time),
+        "pulse_percent": digests.pulse_percent(name),
         "events": int(state.tc.sum()), "words": int(state.net_words.sum()),
         "inputs": digests.input_record(net.num_inputs, state.net_hash, state.net_words),
         "levels": digests.level_records(net.level_offsets, net.num_inputs, state.net_hash, state.net_words,

@@ -116,12 +116,14 @@ def _golden(name):
 def test_full_size_against_oracle_digests(gpu, name):
     rec = _golden(name)
     _, make = digests.large_workloads()[name]
+    q = digests.pulse_percent(name)
+    assert rec.get("pulse_percent", 100) == q
     net, stim = make()
     assert digests.inputs_sha256(net, stim) == rec["inputs_sha256"], \
         "the generator drew other inputs than the stored oracle run"
     W = stim.num_windows
     try:
-        with gpu(net, stim.window_len, pool_words=_pool_for_device(net, W)) as sim:
+        with gpu(net, stim.window_len, pool_words=_pool_for_device(net, W), pulse_percent=q) as sim:
             sim.load(stim.pi_off, stim.pi_words)
             sim.simulate()
             tc, t0, t1 = sim.toggle_stats()
