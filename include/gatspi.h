@@ -308,7 +308,9 @@ gatspi_status gatspi_sync(gatspi_ctx *ctx);
 /*
  * Lanes the next gatspi_simulate gives each window: 32 / num_windows when it cuts the
  * windows into time chunks (see gatspi_simulate), else 1; 0 for a NULL ctx.  Decided
- * by the flags, the window count and the last load.
+ * by the flags, the window count and the last load.  The page has no counterpart: it
+ * runs windows, not stretches of one window, in parallel (Section 4, cycle
+ * parallelism).
  */
 int32_t gatspi_lanes_per_window(const gatspi_ctx *ctx);
 
