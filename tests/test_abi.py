@@ -124,3 +124,23 @@ def test_window_cutting_flags_on_the_host(lib):
     for name, value in re.findall(r"#define (GATSPI_FLAG_[A-Z_]+) (0x[0-9a-f]+)u", text):
         assert getattr(lib, name) == int(value, 16), name
     assert lib.gatspi_lanes_per_window(0) == 0
+
+
+def test_every_entry_point_cites_its_passage():
+    """Each function of the C ABI is documented by the comment block above it (a struct
+    of its arguments may stand in between), and that comment names the passage of the
+    GATSPI page it implements or says that the page has no counterpart."""
+    text = open(os.path.join(ROOT, "include", "gatspi.h")).read()
+    passage = re.compile(r"Sections? \d|Fig\. \d|Algorithm 1|the page|no counterpart")
+    names = declared_functions()
+    assert len(names) >= 20
+    for name in names:
+        m = re.search(r"\n[a-z_0-9 ]+[ *]" + name + r"\s*\(", text)
+        assert m, name
+        before = text[:m.start()]
+        start = before.rfind("/*")
+        assert start >= 0 and before.rfind("*/") > start, name
+        gap = before[before.rfind("*/") + 2:]
+        assert gap.strip() == "" or gap.lstrip().startswith("typedef struct"), (name, gap[:80])
+        comment = re.sub(r"\s*\n\s*\*?\s*", " ", before[start:])   # one line, margins dropped
+        assert passage.search(comment), name
