@@ -144,3 +144,29 @@ def test_every_entry_point_cites_its_passage():
         assert gap.strip() == "" or gap.lstrip().startswith("typedef struct"), (name, gap[:80])
         comment = re.sub(r"\s*\n\s*\*?\s*", " ", before[start:])   # one line, margins dropped
         assert passage.search(comment), name
+
+
+def test_product_path_does_not_use_the_oracle(lib):
+    """The library and its binding neither import nor include anything under oracle/,
+    and using them loads no oracle module: only the tests, smoke() and bench.py's
+    CPU-baseline and reference legs run the oracle."""
+    import subprocess
+    import sys
+    pkg = os.path.join(ROOT, "gate_level_logic_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h", ".c")):
+                with open(os.path.join(dirpath, f)) as fh:
+                    text = fh.read()
+                assert not re.search(r"^\s*(import oracle|from oracle)\b|#include\s*[\"<][^\">]*oracle", text, re.M), f
+    code = ("import sys, numpy as np, synth\n"
+            "from gate_level_logic_gb300 import gatspi, sdf_annotate\n"
+            "net = synth.generate_netlist(synth.NetlistSpec(num_gates=200, num_inputs=8, num_levels=4, seed=1,\n"
+            "                                              cond_cells=('AOI21',), cond_fraction=0.5))\n"
+            "s = synth.write_sdf(net, seed=1)\n"
+            "sdf_annotate(s.text, net.type_names, s.pin_names, net.gate_type, s.instance_names, net.fanin_off,\n"
+            "             net.gate_dly_off, net.dly_data.size, 1000)\n"
+            "gatspi.gatspi_status_name(0)\n"
+            "bad = [m for m in sys.modules if m == 'oracle' or m.startswith('oracle.')]\n"
+            "assert not bad, bad\n")
+    subprocess.run([sys.executable, "-c", code], check=True, cwd=ROOT)
