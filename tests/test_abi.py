@@ -170,3 +170,16 @@ def test_product_path_does_not_use_the_oracle(lib):
             "bad = [m for m in sys.modules if m == 'oracle' or m.startswith('oracle.')]\n"
             "assert not bad, bad\n")
     subprocess.run([sys.executable, "-c", code], check=True, cwd=ROOT)
+
+
+def test_missing_library_fails_loudly(lib, monkeypatch, tmp_path):
+    """Without libgatspi.so every call of the binding raises: there is no CPU fallback
+    to run instead."""
+    monkeypatch.setattr(lib, "LIB_PATH", str(tmp_path / "libgatspi.so"))
+    monkeypatch.setattr(lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        lib.library()
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        lib.gatspi_status_name(0)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        lib.gatspi_lanes_per_window(None)
