@@ -61,3 +61,29 @@ def test_kernel_hash_ignores_comments():
     b = "int x = 1;\nint y = 2;   // two\n"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only("int x = 1;\n") != bench._code_only("int x = 2;\n")
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    """Rank 0 of the reference arm prints one JSON line on the bench's metric, unit and
+    workload: the oracle timed as it stands on host cores, with its cpu_baseline block
+    and an end-to-end block that copies nothing, both equal to the line's value."""
+    import argparse
+    import json
+    import bench
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    args = argparse.Namespace(steps=1, warmup=0, pulse_percent=100)
+    assert bench.run_reference(args) == 0
+    lines = [x for x in capsys.readouterr().out.splitlines() if x.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["n_gpus"] == 1
+    assert (d["steps"], d["warmup"]) == (1, 0) and d["ms_per_step"] > 0
+    assert d["config"]["workload"] == bench.WORKLOAD_NAMES[bench.WORKLOAD]
+    assert d["config"]["gates"] == 1_000_000 and d["config"]["windows"] == 256
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and "windows" in cb["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
