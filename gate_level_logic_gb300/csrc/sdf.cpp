@@ -111,14 +111,28 @@ Tree parse_tree(std::string_view s) {
 enum Op : int { kVar = 0, kConst, kNot, kAnd, kOr, kBitAnd, kBitOr, kXor, kEq, kNe };
 
 struct Cond {
+    static constexpr int kStack = 256;   // operands eval can hold at once
     std::vector<int> code;   // pairs (op, arg)
     bool names(int pin) const {
         for (size_t k = 0; k < code.size(); k += 2)
             if (code[k] == kVar && code[k + 1] == pin) return true;
         return false;
     }
+    // Most operands pending at once while evaluating: the parser refuses a condition
+    // that needs more than kStack (nesting is bounded, but each level can leave one
+    // operand pending per binary precedence level).
+    int stack_depth() const {
+        int sp = 0, most = 0;
+        for (size_t k = 0; k < code.size(); k += 2) {
+            const int op = code[k];
+            sp += (op == kVar || op == kConst) ? 1 : (op == kNot ? 0 : -1);
+            most = sp > most ? sp : most;
+        }
+        return most;
+    }
     int eval(const int *val) const {
-        int st[256];
+        int st[kStack];
+        st[0] = 0;
         int sp = 0;
         for (size_t k = 0; k < code.size(); k += 2) {
             const int op = code[k];
@@ -508,6 +522,7 @@ struct Annotator {
                     cp.lex(text.substr(text.find('|') + 1));
                     cp.binary(0);
                     if (cp.k != cp.tok.size()) sdf_fail("bad condition: " + text);
+                    if (cp.out.stack_depth() > Cond::kStack) sdf_fail("condition too long: " + text);
                     hit = cond_cache.emplace(std::move(text), std::move(cp.out)).first;
                 }
                 iopath(t, body, g, &hit->second, dly);

@@ -104,3 +104,24 @@ def test_simulation_from_translated_tables(lib, oracle_lib):
     theirs.dly_data, theirs.wire_rise, theirs.wire_fall = osdf.annotate(*args)
     ref = oracle_lib.simulate(theirs, stim, threads=8)
     assert_same(run_gpu(Simulator, mine, stim, pool_for(ref, mine)), ref, "from SDF")
+
+
+def _nested_condition(levels):
+    """B || B && B | B ^ B & B == (...): each level leaves six operands pending, one per
+    binary precedence level, and nests one parenthesis deeper."""
+    s = "B"
+    for _ in range(levels):
+        s = "B || B && B | B ^ B & B == (%s)" % s
+    return s
+
+
+def test_condition_operand_bound(lib):
+    """A condition whose evaluation would hold more operands at once than the
+    translator's evaluation stack (256) is refused, though its nesting is within the
+    limit; one within the bound translates as the oracle translates it."""
+    text = ts._wrap(ts._cell("(COND %s (IOPATH (posedge A) Y (1)))" % _nested_condition(45)))
+    with pytest.raises(lib.SdfError, match="too long"):
+        ts.translate(lib, text, ts.NAND2)
+    text = ts._wrap(ts._cell("(COND %s (IOPATH (posedge A) Y (3)))" % _nested_condition(20)))
+    for a, b in zip(ts.translate(lib, text, ts.NAND2), ts.translate(osdf, text, ts.NAND2)):
+        assert np.array_equal(a, b)
