@@ -58,6 +58,8 @@ struct Tree {
     }
 };
 
+constexpr size_t kMaxListDepth = 1000;
+
 Tree parse_tree(std::string_view s) {
     Tree t;
     t.nodes.reserve(s.size() / 4 + 16);
@@ -72,6 +74,9 @@ Tree parse_tree(std::string_view s) {
         if (std::isspace((unsigned char)c)) {
             ++i;
         } else if (c == '(') {
+            // lists are walked recursively later (flatten): bound their depth, far
+            // beyond any SDF statement (a few levels; conditions stop at 48 anyway)
+            if (marks.size() > kMaxListDepth) sdf_fail("lists nested too deeply at byte " + std::to_string(i));
             marks.push_back(pending.size());
             ++i;
         } else if (c == ')') {

@@ -125,3 +125,12 @@ def test_condition_operand_bound(lib):
     text = ts._wrap(ts._cell("(COND %s (IOPATH (posedge A) Y (3)))" % _nested_condition(20)))
     for a, b in zip(ts.translate(lib, text, ts.NAND2), ts.translate(osdf, text, ts.NAND2)):
         assert np.array_equal(a, b)
+
+
+def test_deeply_nested_lists_are_refused(lib):
+    """SDF lists nested 100000 deep (inside a COND) are refused with EINVAL when the
+    text is parsed, before anything walks them recursively."""
+    deep = "(" * 100000 + "B" + ")" * 100000
+    text = ts._wrap(ts._cell("(COND %s (IOPATH (posedge A) Y (1)))" % deep))
+    with pytest.raises(lib.SdfError, match="nested too deeply"):
+        ts.translate(lib, text, ts.NAND2)
