@@ -310,10 +310,15 @@ int32_t convert(std::string_view v, long long file_fs, long long unit_fs) {
             dot = true;
         } else if (std::isdigit((unsigned char)c)) {
             any = true;
-            if (digits < 30) {
+            // at most 20 significant digits, so that mant * file_fs (< 10^20 * 10^17)
+            // fits the 128-bit arithmetic; zeros beyond them are exact (a power of ten),
+            // any other digit is refused rather than dropped
+            if (digits < 20) {
                 mant = mant * 10 + (c - '0');
                 if (mant != 0) ++digits;
                 if (dot) --exp10;
+            } else if (c != '0') {
+                sdf_fail("more than 20 significant digits: " + std::string(v));
             } else if (!dot) {
                 ++exp10;
             }

@@ -134,3 +134,28 @@ def test_deeply_nested_lists_are_refused(lib):
     text = ts._wrap(ts._cell("(COND %s (IOPATH (posedge A) Y (1)))" % deep))
     with pytest.raises(lib.SdfError, match="nested too deeply"):
         ts.translate(lib, text, ts.NAND2)
+
+
+def test_number_precision_bound(lib):
+    """Delay values keep 20 significant digits exactly, and zeros after them, whatever
+    the TIMESCALE (up to 100 s, where 20 digits times the file unit still fit the
+    translator's 128-bit arithmetic); a value with more significant digits is refused,
+    never rounded off and never overflowed."""
+    cases = (("1.00000000000000000000000000", "1ns"),       # zeros beyond 20 digits: exact
+             ("0.12345678901234567890", "1ns"),             # 20 digits: 123 ps
+             ("3.1400000000000000000000000000", "1ps"),     # 3 ps
+             ("99999999999999999999", "100s"))              # the largest mantissa and file unit: too large
+    for value, unit in cases:
+        text = ts._wrap(ts._cell("(IOPATH A Y (%s))" % value), timescale="(TIMESCALE %s)" % unit)
+        try:
+            want = ts.translate(osdf, text, ts.NAND2)
+        except osdf.SdfError:
+            with pytest.raises(lib.SdfError, match="too large"):
+                ts.translate(lib, text, ts.NAND2)
+            continue
+        for a, b in zip(ts.translate(lib, text, ts.NAND2), want):
+            assert np.array_equal(a, b), value
+    for value in ("1.000000000000000000001", "123456789012345678901", "9" * 29):
+        text = ts._wrap(ts._cell("(IOPATH A Y (%s))" % value), timescale="(TIMESCALE 100s)")
+        with pytest.raises(lib.SdfError, match="significant digits"):
+            ts.translate(lib, text, ts.NAND2)
