@@ -257,10 +257,14 @@ struct CondParser {
             ++k;
         } else {
             ++k;
-            if (t->find('\'') != std::string::npos) {
-                const char last = t->back();
-                if (last != '0' && last != '1') sdf_fail("bad literal " + *t);
-                emit(kConst, last - '0');
+            const size_t quote = t->find('\'');
+            if (quote != std::string::npos) {
+                // a one-bit binary literal, sized or not: digits, 'b or 'B, then 0 or 1
+                bool lit = t->size() == quote + 3 && ((*t)[quote + 1] == 'b' || (*t)[quote + 1] == 'B') &&
+                           (t->back() == '0' || t->back() == '1');
+                for (size_t u = 0; u < quote; ++u) lit = lit && std::isdigit((unsigned char)(*t)[u]);
+                if (!lit) sdf_fail("bad literal " + *t);
+                emit(kConst, t->back() - '0');
             } else if (*t == "0" || *t == "1") {
                 emit(kConst, (*t)[0] - '0');
             } else {

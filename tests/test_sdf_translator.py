@@ -159,3 +159,22 @@ def test_number_precision_bound(lib):
         text = ts._wrap(ts._cell("(IOPATH A Y (%s))" % value), timescale="(TIMESCALE 100s)")
         with pytest.raises(lib.SdfError, match="significant digits"):
             ts.translate(lib, text, ts.NAND2)
+
+
+@pytest.mark.parametrize("lit", ["1'1", "1'bc0", "1'b10", "'1", "1'x1", "a'b1"])
+def test_malformed_literals_are_refused_by_both(lib, lit):
+    """Only one-bit binary literals are conditions' constants (0, 1, 1'b0, 1'b1, 'b0,
+    'b1, any size digits): anything else with a quote is refused, by the library as by
+    the oracle."""
+    text = ts._wrap(ts._cell("(COND B == %s (IOPATH (posedge A) Y (1)))" % lit))
+    with pytest.raises(osdf.SdfError):
+        ts.translate(osdf, text, ts.NAND2)
+    with pytest.raises(lib.SdfError):
+        ts.translate(lib, text, ts.NAND2)
+
+
+@pytest.mark.parametrize("lit", ["1'b1", "1'B0", "'b1", "4'b0", "0", "1"])
+def test_literals_translate_like_the_oracle(lib, lit):
+    text = ts._wrap(ts._cell("(COND B == %s (IOPATH (posedge A) Y (2)))" % lit))
+    for a, b in zip(ts.translate(lib, text, ts.NAND2), ts.translate(osdf, text, ts.NAND2)):
+        assert np.array_equal(a, b)
