@@ -345,18 +345,22 @@ int32_t convert(std::string_view v, long long file_fs, long long unit_fs) {
     }
     if (!any || i != v.size()) sdf_fail("bad number " + std::string(v));
     if (neg && mant != 0) sdf_fail("negative delay " + std::string(v));
-    // value = mant * 10^exp10 * file_fs / unit_fs
-    __int128 num = mant * (__int128)file_fs, den = unit_fs;
+    // value = mant * 10^exp10 * file_fs / unit_fs = num / den, exactly, in unsigned
+    // 128-bit arithmetic: num < 10^20 * 10^17 < 2^123 to start with
+    using u128 = unsigned __int128;
+    u128 num = (u128)mant * (u128)file_fs, den = (u128)unit_fs;
     for (; exp10 > 0; --exp10) {
         num *= 10;
-        if (num > ((__int128)1 << 100)) sdf_fail("delay too large: " + std::string(v));
+        if (num > ((u128)1 << 100)) sdf_fail("delay too large: " + std::string(v));
     }
     for (; exp10 < 0; ++exp10) {
-        den *= 10;
-        if (den > ((__int128)1 << 100)) sdf_fail("delay too precise: " + std::string(v));
+        if (den > 2 * num) return 0;   // below one half, and every further 10 makes it smaller
+        den *= 10;                     // den <= 2 num < 2^124 before, so < 2^128 after
     }
-    const __int128 r = (2 * num + den) / (2 * den);
-    if (r >= GATSPI_NO_ARC) sdf_fail("delay too large: " + std::string(v));
+    // nearest integer, halves up: the quotient, plus one when 2 * rem >= den
+    const u128 q = num / den, rem = num - q * den;
+    const u128 r = q + (rem >= den - rem ? 1 : 0);
+    if (r >= (u128)GATSPI_NO_ARC) sdf_fail("delay too large: " + std::string(v));
     return (int32_t)r;
 }
 

@@ -139,12 +139,16 @@ def test_deeply_nested_lists_are_refused(lib):
 def test_number_precision_bound(lib):
     """Delay values keep 20 significant digits exactly, and zeros after them, whatever
     the TIMESCALE (up to 100 s, where 20 digits times the file unit still fit the
-    translator's 128-bit arithmetic); a value with more significant digits is refused,
-    never rounded off and never overflowed."""
+    translator's 128-bit arithmetic) and however small (a value below half a unit is
+    0, exactly half rounds up); a value with more significant digits is refused, never
+    rounded off and never overflowed."""
     cases = (("1.00000000000000000000000000", "1ns"),       # zeros beyond 20 digits: exact
              ("0.12345678901234567890", "1ns"),             # 20 digits: 123 ps
              ("3.1400000000000000000000000000", "1ps"),     # 3 ps
-             ("99999999999999999999", "100s"))              # the largest mantissa and file unit: too large
+             ("99999999999999999999", "100s"),              # the largest mantissa and file unit: too large
+             (".721812064E-24", "100ns"),                   # far below one unit: 0, exactly
+             ("5e-4", "1ns"),                                # exactly one half a unit: rounds up to 1
+             ("4.9999999999999999999e-4", "1ns"))           # just below one half: 0
     for value, unit in cases:
         text = ts._wrap(ts._cell("(IOPATH A Y (%s))" % value), timescale="(TIMESCALE %s)" % unit)
         try:
