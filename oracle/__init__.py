@@ -94,6 +94,8 @@ def _load(path=None):
         lib.oracle_fnv1a64.argtypes = [ctypes.c_uint64, ctypes.c_void_p, ctypes.c_int64]
         lib.oracle_fnv1a64.restype = ctypes.c_uint64
         lib.oracle_free.argtypes = [ctypes.c_void_p]
+        lib.oracle_set_literal_skip.argtypes = [ctypes.c_int]
+        lib.oracle_set_literal_skip.restype = None
         lib.oracle_free.restype = None
         _libs[path] = lib
     return _libs[path]
@@ -159,11 +161,21 @@ def _finish(lib, rc, err, pool_ptr, pool_words, off, tc, t1, net, stim):
                   num_windows=stim.num_windows)
 
 
-def simulate(net, stim, threads: int = 1, lib_path: str = None, pulse_percent: int = 100) -> Result:
+def simulate(net, stim, threads: int = 1, lib_path: str = None, pulse_percent: int = 100,
+             literal_skip: bool = False) -> Result:
     """Event-driven oracle (Algorithm 1) over all gates and windows.  ``pulse_percent``
     is PATHPULSEPERCENT: the inertial reject limit of both filters as a percentage of
-    the delay (100 = the page's setting, 0 = transport delay)."""
+    the delay (100 = the page's setting, 0 = transport delay).  ``literal_skip`` runs
+    the study variant of the interconnect pulse test: one test per pin and iteration
+    of the event loop, as Algorithm 1 writes it, instead of skipping every narrow pulse
+    in a row (the reading the rest of the project computes)."""
     lib = _load(lib_path)
+    if literal_skip:
+        lib.oracle_set_literal_skip(1)
+        try:
+            return simulate(net, stim, threads, lib_path, pulse_percent)
+        finally:
+            lib.oracle_set_literal_skip(0)
     s, keep = _marshal(net, stim)
     W = int(stim.num_windows)
     off = np.zeros((net.num_inputs + net.num_gates) * W + 1, dtype=np.int64)

@@ -50,6 +50,13 @@
  * exposes the entry before it, which a later event may cancel in turn.  q = 0 is
  * transport delay: no pulse is filtered, and only an output event scheduled before
  * the last scheduled one replaces it.
+ *
+ * Study variant (off unless oracle_set_literal_skip(1) is called): the interconnect
+ * pulse test written in Algorithm 1 as a single test, taken literally -- each pin
+ * skips at most one narrow pulse per iteration of the event loop, so the first edge
+ * of a second narrow pulse right behind it can be taken in that iteration.  The
+ * reading above (skip until the next pulse is wide enough) is what every other
+ * part of this project computes.
  */
 #include <pthread.h>
 #include <stdio.h>
@@ -63,6 +70,10 @@
 #define MAXP 8
 #define RISE 0
 #define FALL 1
+
+/* study variant of the interconnect pulse test (see the header); set before a run */
+static int g_literal_skip = 0;
+void oracle_set_literal_skip(int on) { g_literal_skip = on != 0; }
 
 /* reject limit of a delay d at PATHPULSEPERCENT q */
 static int64_t reject_limit(int64_t d, int32_t q) { return d * q / 100; }
@@ -119,15 +130,18 @@ static int simulate_task(int n, const int32_t *const *Win, const int32_t *wire_r
         int64_t t = EOW;
         for (int i = 0; i < n; ++i) {
             int64_t d;
-            for (;;) {
+            for (int skipped = 0;; ) {
                 d = (p[i] % 2) ? wire_fall[i] : wire_rise[i]; /* edge leaving the current value */
                 if (Win[i][p[i] + 1] == EOW) break;
+                if (g_literal_skip && skipped) break;          /* study variant: one test only */
                 /* interconnect inertial filter: a pulse narrower than the reject limit
                  * of d never reaches the pin (the limit is d itself at q = 100) */
-                if ((int64_t)Win[i][p[i] + 2] - reject_limit(d, q) - (int64_t)Win[i][p[i] + 1] < 0)
+                if ((int64_t)Win[i][p[i] + 2] - reject_limit(d, q) - (int64_t)Win[i][p[i] + 1] < 0) {
                     p[i] += 2;
-                else
+                    skipped = 1;
+                } else {
                     break;
+                }
             }
             a[i] = (Win[i][p[i] + 1] == EOW) ? EOW : (int64_t)Win[i][p[i] + 1] + d;
             if (a[i] < t) t = a[i];

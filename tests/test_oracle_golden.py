@@ -192,3 +192,27 @@ def test_pulse_percent_skewed_delays(oracle_lib, q):
     buf = single_gate(tt, 1, uniform_delays(1, 10, 2, tt))
     r = oracle_lib.simulate(buf, synth.from_waveforms([[SKEW_WAVE]], 100), pulse_percent=q)
     assert r.gate_wave(0, 0).tolist() == SKEW_EXPECT[q]
+
+
+def test_literal_single_pulse_test_study_variant(oracle_lib):
+    """The interconnect pulse test read literally (one test per pin and event-loop
+    iteration, the study variant) against the reading every other part takes (skip
+    until the next pulse is wide enough).  A buffer (gate delay 1) behind a wire of
+    delay 5; its input, at 0, toggles at 10, 12, 13, 15 and 100: two pulses of width 2
+    back to back, then an edge, in a window of 200.
+      reading taken: both pulses are skipped; 100 arrives at 105 and the output rises
+        at 106: [0, 106, EOW], TC 1, T1 = 200 - 106 = 94;
+      literal: the first iteration skips [10, 12) only and takes 13 (arriving at 18),
+        so the output rises at 19; [15, 100) is wide, 15 arrives at 20 and the output
+        falls at 21 (21 - 19 = 2 is not below the gate delay 1, so it is kept); 100
+        gives 106: [0, 19, 21, 106, EOW], TC 3, T1 = 2 + 94 = 96."""
+    buf = single_gate(np.array([0, 1], np.uint8), 1, uniform_delays(1, 1, 1), wire_rise=[5], wire_fall=[5])
+    stim = synth.from_waveforms([[[0, 10, 12, 13, 15, 100, EOW]]], 200)
+    taken = oracle_lib.simulate(buf, stim)
+    literal = oracle_lib.simulate(buf, stim, literal_skip=True)
+    assert taken.gate_wave(0, 0).tolist() == [0, 106, EOW]
+    assert (int(taken.tc[0]), int(taken.t1[0])) == (1, 94)
+    assert literal.gate_wave(0, 0).tolist() == [0, 19, 21, 106, EOW]
+    assert (int(literal.tc[0]), int(literal.t1[0])) == (3, 96)
+    # the switch is cleared after the call: the next run takes the reading again
+    assert oracle_lib.simulate(buf, stim).gate_wave(0, 0).tolist() == [0, 106, EOW]

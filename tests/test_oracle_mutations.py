@@ -19,8 +19,7 @@ SRC = os.path.join(os.path.dirname(oracle.__file__))
 
 MUTANTS = {
     "wire filter tested once, not repeated": (
-        "                    p[i] += 2;\n                else\n                    break;",
-        "                    p[i] += 2;\n                break;"),
+        "if (g_literal_skip && skipped) break;", "if (skipped) break;"),
     "wire filter not strict": (
         "(int64_t)Win[i][p[i] + 1] < 0)", "(int64_t)Win[i][p[i] + 1] <= 0)"),
     "wire rise/fall swapped": (
