@@ -56,6 +56,10 @@ def test_regime_picks_kernel_and_traffic_record(monkeypatch):
     traffic from the ncu record of the same regime: windows ranked by bound (up to
     1024 windows), in window order (beyond), or cut into time chunks (no record);
     another PATHPULSEPERCENT or a record taken on other kernel code gives none."""
+    import re
+    with open(os.path.join(bench.ROOT, "gate_level_logic_gb300", "csrc", "gatspi_internal.cuh")) as f:
+        lib_limit = int(re.search(r"kRankMaxWindows\s*=\s*(\d+)", f.read()).group(1))
+    assert bench.RANKED_WINDOWS == lib_limit      # the same threshold as the library's planner
     assert bench.sim_regime(1, 1) == "ranked"
     assert bench.sim_regime(1, 256) == "ranked"
     assert bench.sim_regime(1, 1024) == "ranked"
