@@ -123,6 +123,11 @@ def test_window_cutting_flags_on_the_host(lib):
     text = open(os.path.join(ROOT, "include", "gatspi.h")).read()
     for name, value in re.findall(r"#define (GATSPI_FLAG_[A-Z_]+) (0x[0-9a-f]+)u", text):
         assert getattr(lib, name) == int(value, 16), name
+    for name in ("GATSPI_EOW", "GATSPI_NO_ARC", "GATSPI_MAX_PINS"):
+        value = re.search(r"#define %s (\d+)" % name, text).group(1)
+        assert getattr(lib, name) == int(value), name
+    where = re.search(r"enum \{ GATSPI_HOST = (\d+), GATSPI_DEVICE = (\d+) \}", text)
+    assert (lib.GATSPI_HOST, lib.GATSPI_DEVICE) == (int(where.group(1)), int(where.group(2)))
     assert lib.gatspi_lanes_per_window(0) == 0
 
 
