@@ -90,12 +90,13 @@ Tree parse_tree(std::string_view s) {
             pending.push_back((int)t.nodes.size() - 1);
             ++i;
         } else {
-            size_t j = i;
-            if (c == '"') {
-                j = s.find('"', i + 1);
-                if (j == std::string_view::npos) sdf_fail("unterminated string");
+            // a quoted string runs to the next quote, wherever it is; a quote with none
+            // after it starts an ordinary atom, which runs to a space or a parenthesis
+            size_t j = c == '"' ? s.find('"', i + 1) : std::string_view::npos;
+            if (j != std::string_view::npos) {
                 ++j;
             } else {
+                j = i;
                 while (j < n && !std::isspace((unsigned char)s[j]) && s[j] != '(' && s[j] != ')') ++j;
             }
             t.nodes.push_back(Node{false, s.substr(i, j - i)});
@@ -471,8 +472,10 @@ struct Annotator {
                 const Node &part = t.kid(cell, q);
                 if (t.is(part, "CELLTYPE")) {
                     if (part.count < 2 || t.kid(part, 1).list) sdf_fail("bad CELLTYPE");
+                    // the name without the quotes around it (every leading and trailing one)
                     celltype = t.kid(part, 1).atom;
-                    if (celltype.size() >= 2 && celltype.front() == '"') celltype = celltype.substr(1, celltype.size() - 2);
+                    const size_t a = celltype.find_first_not_of('"'), b = celltype.find_last_not_of('"');
+                    celltype = a == std::string_view::npos ? std::string_view() : celltype.substr(a, b - a + 1);
                 } else if (t.is(part, "INSTANCE")) {
                     if (part.count > 1) {
                         iname = t.kid(part, 1).atom;

@@ -182,3 +182,20 @@ def test_literals_translate_like_the_oracle(lib, lit):
     text = ts._wrap(ts._cell("(COND B == %s (IOPATH (posedge A) Y (2)))" % lit))
     for a, b in zip(ts.translate(lib, text, ts.NAND2), ts.translate(osdf, text, ts.NAND2)):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("spelling", ['NAND2"', '"NAND2""'])
+def test_celltype_quotes_as_the_oracle_reads_them(lib, spelling):
+    """A CELLTYPE with a stray quote (found by a differential fuzz): the library reads
+    the name as the oracle does, without every quote around it, and both then agree
+    (or both refuse)."""
+    text = ts._wrap(ts._cell("(IOPATH A Y (1))")).replace('(CELLTYPE "NAND2")', "(CELLTYPE %s)" % spelling)
+    assert spelling in text
+    try:
+        want = ts.translate(osdf, text, ts.NAND2)
+    except osdf.SdfError:
+        with pytest.raises(lib.SdfError):
+            ts.translate(lib, text, ts.NAND2)
+        return
+    for a, b in zip(ts.translate(lib, text, ts.NAND2), want):
+        assert np.array_equal(a, b)
